@@ -1,0 +1,370 @@
+"""Forward-pass throughput of the nanochat-style GPT on B300 through the nc C ABI.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload d12] [--impl ours|reference]
+
+One step = one nc_forward over a [B, T] batch of synthetic tokens (every kernel of the hot
+path).  `value` = tokens/s over all ranks with inputs already in HBM; `e2e` = the same metric
+through nc_forward_host (pinned host tokens in, host logits out, copies inside the timed
+region).  The dominant kernel's roofline numbers come from CUDA events recorded around every
+launch on the launching stream during the timed region.  `--impl reference` times the fp64
+CPU oracle (the only reference this path has) on a bounded sample of the same workload.
+Under torchrun each rank runs an independent replica (the forward needs no collective).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "forward tokens/sec at d12 T=2048 on 1 B300; % of BF16 tensor-core peak"
+UNIT = "tokens/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def window_pairs(T: int, W: int) -> int:
+    """Visible (query, key) pairs of one head over one row: sum_i min(i+1, W+1) (W < 0: full)."""
+    if W < 0 or W >= T:
+        return T * (T + 1) // 2
+    return (W + 1) * (W + 2) // 2 + (T - W - 1) * (W + 1)
+
+
+def kernel_work(cfg, B: int, T: int):
+    """Algorithmic work per launch of each kernel class (FLOPs for contractions, bytes otherwise)."""
+    M = B * T
+    C, H, Hkv, D, F, V, L = (cfg.n_embd, cfg.n_head, cfg.n_kv_head, cfg.head_dim, cfg.mlp_hidden,
+                             cfg.vocab_size, cfg.n_layer)
+    attn_flops = sum(4 * D * H * B * window_pairs(T, cfg.window_left[i]) for i in range(L)) / L
+    return {
+        "qkv_rope_qknorm_ve": ("tensor", 2.0 * M * C * (H + 2 * Hkv) * D),
+        "attention": ("tensor", attn_flops),
+        "oproj_residual": ("tensor", 2.0 * M * H * D * C),
+        "fc_relu2": ("tensor", 2.0 * M * C * F),
+        "proj_residual": ("tensor", 2.0 * M * F * C),
+        "lmhead_softcap": ("tensor", 2.0 * M * C * V),
+        # average over the 2L+1 launches: block start reads x, x0 and writes x, xn (14 B/elt);
+        # pre-MLP reads x, writes xn (6 B/elt); final reads x, x_mid, writes xn (10 B/elt)
+        "rownorm": ("hbm", M * C * (14.0 * L + 6.0 * L + 10.0) / (2 * L + 1)),
+        "embed_smear": ("hbm", M * C * (2 + 4) + M * 4),
+    }
+
+
+def model_flops(cfg, B, T):
+    w = kernel_work(cfg, B, T)
+    L = cfg.n_layer
+    per_layer = sum(w[k][1] for k in ("qkv_rope_qknorm_ve", "attention", "oproj_residual", "fc_relu2",
+                                      "proj_residual"))
+    return L * per_layer + w["lmhead_softcap"][1]
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu = gpu_index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, pw, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+                pw.append(float(parts[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "power_w_max": max(pw),
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def oracle_sample(wl, wts, tok, n_tokens: int):
+    """Run the fp64 oracle on the first n_tokens positions of batch row 0; returns seconds."""
+    import numpy as np
+    import oracle as O
+    W = O.OracleWeights.from_synth(wl.model, wts)
+    t0 = time.perf_counter()
+    O.forward_row(wl.model, W, tok[0, :n_tokens].numpy())
+    return time.perf_counter() - t0
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        info = threadpool_info()
+        n = [i.get("num_threads") for i in info if i.get("internal_api") in ("openblas", "mkl", "blis")]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return len(os.sched_getaffinity(0))
+
+
+def run_reference(args, rank, world):
+    """The CPU oracle timed on the host cores, rank 0 only."""
+    if rank != 0:
+        return
+    from synth import get_workload, make_tokens, make_weights
+    wl = get_workload(args.workload)
+    wts = make_weights(wl.model, seed=wl.seed, init=wl.init)
+    tok = make_tokens(wl)
+    n = min(args.ref_tokens, wl.T)
+    for _ in range(args.warmup):
+        oracle_sample(wl, wts, tok, n)
+    secs = [oracle_sample(wl, wts, tok, n) for _ in range(args.steps)]
+    total = sum(secs)
+    value = n * args.steps / total
+    sample = f"positions 0..{n - 1} of batch row 0 of the {wl.name} workload (causal prefix, exact logits)"
+    cores = blas_threads()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "B": wl.B, "T": wl.T, "sample_tokens_per_step": n},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+    from synth import get_workload, make_tokens, make_weights
+    from decoder_only_forward_02_b300 import build
+    build.build()
+    from decoder_only_forward_02_b300 import binding as NB
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    wl = get_workload(args.workload)
+    cfg = wl.model
+    wts_cpu = make_weights(cfg, seed=wl.seed, init=wl.init)
+    wts = {k: (v.to(dev) if torch.is_tensor(v) else v) for k, v in wts_cpu.items()}
+    tok_cpu = make_tokens(wl)
+    tok = tok_cpu.to(dev)
+    model = NB.Model(cfg, wts, device=dev)
+    B, T, V = wl.B, wl.T, cfg.vocab_size
+    logits = torch.empty((B, T, V), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    for _ in range(max(args.warmup, 3)):
+        model.forward(tok, out=logits)
+    torch.cuda.synchronize()
+    st = model.status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} after warm-up")
+
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    model.timing(True)
+    barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        model.forward(tok, out=logits)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    ms = e0.elapsed_time(e1)
+    model.timing(False)
+    clk = clocks.stop()
+    ktimes = model.timing_read()
+    if model.status() != 0:
+        raise RuntimeError("device status set during the timed region")
+
+    t_max = torch.tensor([ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t_max, op=dist.ReduceOp.MAX)
+    ms_max = float(t_max.item())
+    ms_step = ms_max / args.steps
+    value = world * B * T * args.steps / (ms_max / 1000.0)
+
+    # end to end through host buffers
+    e2e = None
+    if not args.no_e2e:
+        tok_h = tok_cpu.pin_memory()
+        out_h = torch.empty((B, T, V), dtype=torch.float32).pin_memory()
+        for _ in range(2):
+            model.forward_host(tok_h, out_h)
+        e2e_steps = max(1, min(args.steps, args.e2e_steps))
+        barrier()
+        torch.cuda.synchronize()
+        h0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            model.forward_host(tok_h, out_h)
+        torch.cuda.synchronize()
+        h_ms = 1000 * (time.perf_counter() - h0)
+        tm = torch.tensor([h_ms], dtype=torch.float64, device=dev)
+        if world > 1:
+            dist.all_reduce(tm, op=dist.ReduceOp.MAX)
+        e2e = {"value": world * B * T * e2e_steps / (float(tm.item()) / 1000.0), "unit": UNIT,
+               "h2d_bytes_per_step": int(tok_h.numel() * 4), "d2h_bytes_per_step": int(out_h.numel() * 4),
+               "steps": e2e_steps}
+        del out_h
+
+    if rank != 0:
+        return
+    peaks, peak_src = load_peaks()
+    work = kernel_work(cfg, B, T)
+    kern = {}
+    for name, (tot, n) in ktimes.items():
+        if n:
+            kern[name] = {"ms_total": tot, "launches": n, "ms_per_launch": tot / n,
+                          "share": tot / max(1e-9, sum(t for t, _ in ktimes.values()))}
+    dom = max(kern, key=lambda k: kern[k]["ms_total"])
+    bound, per_launch = work[dom]
+    avg_s = kern[dom]["ms_per_launch"] / 1000.0
+    if bound == "tensor":
+        achieved = per_launch / avg_s / 1e12
+        peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+        unit = "TFLOP/s"
+    else:
+        achieved = per_launch / avg_s / 1e9
+        peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+        unit = "GB/s"
+    for name in kern:
+        b, wk = work[name]
+        s = kern[name]["ms_per_launch"] / 1000.0
+        kern[name]["achieved"] = wk / s / (1e12 if b == "tensor" else 1e9)
+        kern[name]["unit"] = "TFLOP/s" if b == "tensor" else "GB/s"
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tpath):
+        t = json.load(open(tpath))
+        if t.get("kernel") == dom and t.get("workload") == wl.name and t.get("source_hash") == _src_hash():
+            traffic = t.get("bytes_per_launch")
+    flops = model_flops(cfg, B, T)
+    tflops = flops / (ms_step / 1000.0) / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,0.02) bf16 weights, uniform tokens)",
+        "config": {"workload": wl.name, "B": B, "T": T, "n_layer": cfg.n_layer, "n_embd": cfg.n_embd,
+                   "n_head": cfg.n_head, "n_kv_head": cfg.n_kv_head, "vocab": V,
+                   "windows": "SSSL short=%d" % max(cfg.window_left), "logits": "fp32",
+                   "l2": "no flush: each step writes %.2f GB of logits and reads %.2f GB of weights, "
+                         "far above the 126 MB L2" % (B * T * V * 4 / 1e9, _weight_bytes(wts_cpu) / 1e9),
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "model_tflops": tflops,
+        "pct_bf16_peak": 100.0 * tflops / float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])),
+        "pct_bf16_peak_sustained": 100.0 * tflops / float(
+            peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])),
+        "roofline": {"kernel": dom, "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": f"{peak_src} ({'bf16_tflops_sustained' if bound == 'tensor' else 'hbm_gbs'})"},
+        "kernels": kern,
+        "gpu_launches": model.launch_count() * args.steps,
+        "clocks": clk,
+        "e2e": e2e,
+    }
+    if not args.no_cpu_baseline and world >= 1:
+        n = min(args.cpu_tokens, T)
+        secs = oracle_sample(wl, wts_cpu, tok_cpu, n)
+        line["cpu_baseline"] = {"value": n / secs, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+                                "sample": f"fp64 oracle on positions 0..{n - 1} of batch row 0 "
+                                          f"({secs:.1f} s, causal prefix: exact logits for those positions)"}
+    print(json.dumps(line), flush=True)
+
+
+_HASH = None
+
+
+def _src_hash():
+    global _HASH
+    if _HASH is None:
+        import hashlib
+        h = hashlib.sha1()
+        d = os.path.join(ROOT, "decoder_only_forward_02_b300", "csrc")
+        for f in sorted(os.listdir(d)):
+            h.update(open(os.path.join(d, f), "rb").read())
+        _HASH = h.hexdigest()[:12]
+    return _HASH
+
+
+def _weight_bytes(w):
+    import torch
+    return sum(v.numel() * v.element_size() for v in w.values() if torch.is_tensor(v))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="d12")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--cpu-tokens", type=int, default=2048)
+    ap.add_argument("--ref-tokens", type=int, default=512)
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    run_ours(args, rank, world, local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

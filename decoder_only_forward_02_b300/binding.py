@@ -1,0 +1,328 @@
+"""ctypes binding of the C ABI in ``include/nc.h``.
+
+Argument marshalling only: every step of the forward pass runs in the CUDA kernels of
+``libnc.so``.  PyTorch supplies device memory and streams.  There is no fallback: if the
+library is missing, loading it raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Dict, Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libnc.so")
+
+NC_OK = 0
+STATUS_NAMES = {0: "NC_OK", 1: "NC_ERR_INVALID_ARG", 2: "NC_ERR_UNSUPPORTED", 3: "NC_ERR_WORKSPACE",
+                4: "NC_ERR_CUDA", 5: "NC_ERR_DEVICE_TIMEOUT", 6: "NC_ERR_TOKEN_RANGE"}
+KERNEL_CLASSES = ["embed_smear", "rownorm", "qkv_rope_qknorm_ve", "attention", "oproj_residual",
+                  "fc_relu2", "proj_residual", "lmhead_softcap"]
+
+c_int_p = ctypes.POINTER(ctypes.c_int)
+c_void_pp = ctypes.POINTER(ctypes.c_void_p)
+
+
+class NcConfig(ctypes.Structure):
+    _fields_ = [
+        ("n_layer", ctypes.c_int), ("n_embd", ctypes.c_int), ("n_head", ctypes.c_int),
+        ("n_kv_head", ctypes.c_int), ("head_dim", ctypes.c_int), ("mlp_hidden", ctypes.c_int),
+        ("vocab_size", ctypes.c_int), ("seq_len_ctx", ctypes.c_int),
+        ("window_left", c_int_p), ("has_ve", ctypes.POINTER(ctypes.c_ubyte)),
+        ("use_smear", ctypes.c_int), ("use_backout", ctypes.c_int), ("embed_norm", ctypes.c_int),
+        ("smear_gate_channels", ctypes.c_int), ("ve_gate_channels", ctypes.c_int),
+        ("ve_gate_scale", ctypes.c_float), ("rms_eps", ctypes.c_float), ("rope_base", ctypes.c_float),
+        ("softcap", ctypes.c_float),
+    ]
+
+
+class NcWeights(ctypes.Structure):
+    _fields_ = [
+        ("wte", ctypes.c_void_p), ("wq", c_void_pp), ("wk", c_void_pp), ("wv", c_void_pp),
+        ("wo", c_void_pp), ("wfc", c_void_pp), ("wproj", c_void_pp), ("ve_table", c_void_pp),
+        ("ve_gate", c_void_pp), ("smear_gate", ctypes.c_void_p), ("lm_head", ctypes.c_void_p),
+        ("resid_lambdas", ctypes.POINTER(ctypes.c_float)), ("x0_lambdas", ctypes.POINTER(ctypes.c_float)),
+        ("backout_lambda", ctypes.c_float),
+    ]
+
+
+_SIGS = {
+    "nc_model_packed_bytes": (ctypes.c_int, [ctypes.POINTER(NcConfig), ctypes.POINTER(ctypes.c_size_t)]),
+    "nc_model_create": (ctypes.c_int, [ctypes.POINTER(NcConfig), ctypes.POINTER(NcWeights), ctypes.c_void_p,
+                                       ctypes.c_size_t, ctypes.c_void_p, ctypes.POINTER(ctypes.c_void_p)]),
+    "nc_workspace_bytes": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+                                          ctypes.POINTER(ctypes.c_size_t)]),
+    "nc_workspace_bytes_host": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+                                               ctypes.POINTER(ctypes.c_size_t)]),
+    "nc_forward": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                                  ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "nc_forward_host": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+                                       ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "nc_get_status": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
+    "nc_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "nc_model_destroy": (None, [ctypes.c_void_p]),
+    "nc_timing_enable": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int]),
+    "nc_timing_read": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.POINTER(ctypes.c_double),
+                                      ctypes.POINTER(ctypes.c_int)]),
+    "nc_kernel_class_name": (ctypes.c_char_p, [ctypes.c_int]),
+    "nc_forward_launch_count": (ctypes.c_int, [ctypes.c_void_p]),
+    # per-kernel entry points (include/nc_ops.h)
+    "nc_op_gemm": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                  ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_float,
+                                  ctypes.c_void_p, ctypes.c_void_p]),
+    "nc_op_qkv": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p] + [ctypes.c_int] * 6 +
+                  [ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                   ctypes.c_int] + [ctypes.c_void_p] * 5),
+    "nc_op_rope_table": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_float,
+                                        ctypes.c_void_p]),
+    "nc_op_attention": (ctypes.c_int, [ctypes.c_void_p] * 3 + [ctypes.c_int] * 6 +
+                        [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
+    "nc_op_rownorm": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_float, ctypes.c_float,
+                                     ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_float,
+                                     ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_float, ctypes.c_void_p,
+                                     ctypes.c_void_p]),
+    "nc_op_embed_smear": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                                         ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+                                         ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
+}
+
+EPI = {"bf16": 0, "resid_f32": 1, "relu2_bf16": 2, "softcap_f32": 3}
+
+
+class ops:
+    """Per-kernel entry points; tensors are CUDA tensors, launches go on the current stream."""
+
+    @staticmethod
+    def gemm(A, B, epi="bf16", out=None, resid=None, cap=15.0, status=None):
+        M, K = A.shape
+        N = B.shape[0]
+        if out is None:
+            dt = torch.bfloat16 if epi in ("bf16", "relu2_bf16") else torch.float32
+            out = torch.empty((M, N), dtype=dt, device=A.device)
+        check(lib().nc_op_gemm(A.data_ptr(), B.data_ptr(), M, N, K, EPI[epi], out.data_ptr(), out.shape[1],
+                               _ptr(resid), cap, _ptr(status), _stream_handle(None)), "nc_op_gemm")
+        return out
+
+    @staticmethod
+    def rope_table(T, D, base, device):
+        t = torch.empty((T, D // 2, 2), dtype=torch.float32, device=device)
+        check(lib().nc_op_rope_table(t.data_ptr(), T, D, base, _stream_handle(None)), "nc_op_rope_table")
+        return t
+
+    @staticmethod
+    def qkv(xn, wqkv, T, H, Hkv, D, rope, eps, gate=None, ve=None, tokens=None, V=0, status=None):
+        M, C = xn.shape
+        dev = xn.device
+        q = torch.empty((M, H * D), dtype=torch.bfloat16, device=dev)
+        k = torch.empty((M, Hkv * D), dtype=torch.bfloat16, device=dev)
+        v = torch.empty((M, Hkv * D), dtype=torch.bfloat16, device=dev)
+        check(lib().nc_op_qkv(xn.data_ptr(), wqkv.data_ptr(), M, T, C, H, Hkv, D, rope.data_ptr(), eps, _ptr(gate),
+                              _ptr(ve), _ptr(tokens), V, q.data_ptr(), k.data_ptr(), v.data_ptr(), _ptr(status),
+                              _stream_handle(None)), "nc_op_qkv")
+        return q, k, v
+
+    @staticmethod
+    def attention(q, k, v, B, T, H, Hkv, D, window, status=None):
+        y = torch.empty_like(q)
+        check(lib().nc_op_attention(q.data_ptr(), k.data_ptr(), v.data_ptr(), B, T, H, Hkv, D, window, y.data_ptr(),
+                                    _ptr(status), _stream_handle(None)), "nc_op_attention")
+        return y
+
+    @staticmethod
+    def rownorm(x, y=None, a=1.0, b=0.0, x_out=None, eps=1e-6, wg=None, c_g=0, gate_scale=1.0, want_gate=False):
+        M, C = x.shape
+        xn = torch.empty((M, C), dtype=torch.bfloat16, device=x.device)
+        gate = None
+        Hkv = 0
+        if want_gate:
+            Hkv = wg.shape[0]
+            gate = torch.empty((M, Hkv), dtype=torch.float32, device=x.device)
+        check(lib().nc_op_rownorm(x.data_ptr(), _ptr(y), a, b, _ptr(x_out), xn.data_ptr(), M, C, eps, _ptr(wg), Hkv,
+                                  c_g, gate_scale, _ptr(gate), _stream_handle(None)), "nc_op_rownorm")
+        return xn, gate
+
+    @staticmethod
+    def embed_smear(tokens, wte, smear_gate=None, c_s=0, embed_norm=False, eps=1e-6, status=None):
+        B, T = tokens.shape
+        V, C = wte.shape
+        x0 = torch.empty((B * T, C), dtype=torch.float32, device=wte.device)
+        check(lib().nc_op_embed_smear(tokens.data_ptr(), B, T, wte.data_ptr(), V, C, _ptr(smear_gate),
+                                      c_s or C, int(embed_norm), eps, x0.data_ptr(), _ptr(status),
+                                      _stream_handle(None)), "nc_op_embed_smear")
+        return x0
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load ``libnc.so`` (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with decoder_only_forward_02_b300.build")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+class NcError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {STATUS_NAMES.get(code, code)} ({lib().nc_status_string(code).decode()})")
+
+
+def check(code: int, what: str) -> None:
+    if code != NC_OK:
+        raise NcError(code, what)
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream_handle(stream: Optional[torch.cuda.Stream]) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def make_config(cfg) -> tuple:
+    """Build an NcConfig from any object with the model's attribute names.
+
+    Returns (struct, keepalive) - the per-layer arrays must stay alive while the struct is used.
+    """
+    L = cfg.n_layer
+    win = (ctypes.c_int * L)(*cfg.window_left)
+    ve = (ctypes.c_ubyte * L)(*[1 if v else 0 for v in cfg.has_ve])
+    c = NcConfig(
+        n_layer=L, n_embd=cfg.n_embd, n_head=cfg.n_head, n_kv_head=cfg.n_kv_head, head_dim=cfg.head_dim,
+        mlp_hidden=cfg.mlp_hidden, vocab_size=cfg.vocab_size, seq_len_ctx=cfg.seq_len_ctx,
+        window_left=ctypes.cast(win, c_int_p), has_ve=ctypes.cast(ve, ctypes.POINTER(ctypes.c_ubyte)),
+        use_smear=int(bool(cfg.use_smear)), use_backout=int(bool(cfg.use_backout)),
+        embed_norm=int(bool(getattr(cfg, "embed_norm", False))),
+        smear_gate_channels=int(getattr(cfg, "smear_gate_channels", 0)),
+        ve_gate_channels=int(getattr(cfg, "ve_gate_channels", 0)),
+        ve_gate_scale=float(getattr(cfg, "ve_gate_scale", 1.0)), rms_eps=float(getattr(cfg, "rms_eps", 1e-6)),
+        rope_base=float(getattr(cfg, "rope_base", 10000.0)), softcap=float(getattr(cfg, "softcap", 15.0)))
+    return c, (win, ve)
+
+
+def packed_bytes(cfg) -> int:
+    c, keep = make_config(cfg)
+    n = ctypes.c_size_t()
+    check(lib().nc_model_packed_bytes(ctypes.byref(c), ctypes.byref(n)), "nc_model_packed_bytes")
+    return n.value
+
+
+class Model:
+    """A created nc_model.  ``weights``: dict of device bf16 tensors (names as in the weights
+    layout: wte, wq.i, wk.i, wv.i, wo.i, wfc.i, wproj.i, ve.i, veg.i, smear, lm_head) plus the
+    float lists resid_lambdas, x0_lambdas and the float backout_lambda."""
+
+    def __init__(self, cfg, weights: Dict[str, object], device: Optional[torch.device] = None,
+                 stream: Optional[torch.cuda.Stream] = None):
+        self.cfg = cfg
+        self.device = torch.device(device) if device is not None else weights["wte"].device
+        self._cstruct, self._keep = make_config(cfg)
+        L = cfg.n_layer
+
+        def arr(name, optional=False):
+            vals = []
+            for i in range(L):
+                t = weights.get(f"{name}.{i}")
+                if t is None and not optional:
+                    raise KeyError(f"{name}.{i}")
+                vals.append(_ptr(t))
+            return (ctypes.c_void_p * L)(*vals)
+
+        self._arrays = {n: arr(n, optional=n in ("ve", "veg")) for n in
+                        ("wq", "wk", "wv", "wo", "wfc", "wproj", "ve", "veg")}
+        lr = (ctypes.c_float * L)(*weights["resid_lambdas"])
+        l0 = (ctypes.c_float * L)(*weights["x0_lambdas"])
+        self._lams = (lr, l0)
+        self._weights = weights  # keep the device tensors alive
+        w = NcWeights(
+            wte=_ptr(weights["wte"]), lm_head=_ptr(weights["lm_head"]),
+            smear_gate=_ptr(weights.get("smear")) if cfg.use_smear else None,
+            resid_lambdas=ctypes.cast(lr, ctypes.POINTER(ctypes.c_float)),
+            x0_lambdas=ctypes.cast(l0, ctypes.POINTER(ctypes.c_float)),
+            backout_lambda=float(weights["backout_lambda"]),
+            **{("ve_table" if k == "ve" else "ve_gate" if k == "veg" else k): ctypes.cast(v, c_void_pp)
+               for k, v in self._arrays.items()})
+        self._wstruct = w
+        n = ctypes.c_size_t()
+        check(lib().nc_model_packed_bytes(ctypes.byref(self._cstruct), ctypes.byref(n)), "nc_model_packed_bytes")
+        self.packed = torch.empty(n.value, dtype=torch.uint8, device=self.device)
+        h = ctypes.c_void_p()
+        check(lib().nc_model_create(ctypes.byref(self._cstruct), ctypes.byref(w), self.packed.data_ptr(), n.value,
+                                    _stream_handle(stream), ctypes.byref(h)), "nc_model_create")
+        self.handle = h
+        self._ws: Dict[tuple, torch.Tensor] = {}
+
+    def __del__(self):
+        h = getattr(self, "handle", None)
+        if h is not None and h.value:
+            try:
+                lib().nc_model_destroy(h)
+            except Exception:
+                pass
+            self.handle = None
+
+    def workspace_bytes(self, B: int, T: int, host: bool = False) -> int:
+        n = ctypes.c_size_t()
+        fn = lib().nc_workspace_bytes_host if host else lib().nc_workspace_bytes
+        check(fn(self.handle, B, T, ctypes.byref(n)), "nc_workspace_bytes")
+        return n.value
+
+    def workspace(self, B: int, T: int, host: bool = False) -> torch.Tensor:
+        key = (B, T, host)
+        if key not in self._ws:
+            self._ws[key] = torch.empty(self.workspace_bytes(B, T, host), dtype=torch.uint8, device=self.device)
+        return self._ws[key]
+
+    def forward(self, tokens: torch.Tensor, out: Optional[torch.Tensor] = None,
+                stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+        """tokens: device int32 [B, T] -> fp32 logits [B, T, V] (asynchronous)."""
+        if tokens.dtype != torch.int32 or not tokens.is_cuda or not tokens.is_contiguous():
+            raise ValueError("tokens must be a contiguous int32 CUDA tensor")
+        B, T = tokens.shape
+        V = self.cfg.vocab_size
+        if out is None:
+            out = torch.empty((B, T, V), dtype=torch.float32, device=self.device)
+        ws = self.workspace(B, T)
+        check(lib().nc_forward(self.handle, tokens.data_ptr(), B, T, out.data_ptr(), ws.data_ptr(), ws.numel(),
+                               _stream_handle(stream)), "nc_forward")
+        return out
+
+    def forward_host(self, tokens: torch.Tensor, out: torch.Tensor,
+                     stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+        """tokens: host int32 [B, T] (pinned for full speed) -> out: host fp32 [B, T, V]; synchronous."""
+        B, T = tokens.shape
+        ws = self.workspace(B, T, host=True)
+        check(lib().nc_forward_host(self.handle, tokens.data_ptr(), B, T, out.data_ptr(), ws.data_ptr(),
+                                    ws.numel(), _stream_handle(stream)), "nc_forward_host")
+        return out
+
+    def status(self, stream: Optional[torch.cuda.Stream] = None) -> int:
+        """Synchronise and return (and clear) the device status code."""
+        return lib().nc_get_status(self.handle, _stream_handle(stream))
+
+    def timing(self, enable: bool) -> None:
+        check(lib().nc_timing_enable(self.handle, int(enable)), "nc_timing_enable")
+
+    def timing_read(self) -> Dict[str, tuple]:
+        out = {}
+        for k, name in enumerate(KERNEL_CLASSES):
+            ms = ctypes.c_double()
+            n = ctypes.c_int()
+            check(lib().nc_timing_read(self.handle, k, ctypes.byref(ms), ctypes.byref(n)), "nc_timing_read")
+            out[name] = (ms.value, n.value)
+        return out
+
+    def launch_count(self) -> int:
+        return lib().nc_forward_launch_count(self.handle)

@@ -1,0 +1,500 @@
+// model.cu -- the C ABI declared in include/nc.h: validation, weight packing, workspace
+// layout and the per-layer launch sequence of the forward pass.
+//
+// Launch sequence for one forward ("Nanochat在nanoGPT之上的新增功能", section 1 table and
+// notes; order of the block as described there: pre-norm attention, then pre-norm MLP):
+//   embed+smear -> x0
+//   per layer i:  rownorm (x <- lr_i*x + l0_i*x0, xn = norm(x), VE gate)  -> QKV GEMM (RoPE,
+//                 QK-norm, v += gate*ve) -> attention -> out-proj GEMM (+residual) ->
+//                 rownorm -> fc GEMM (ReLU^2) -> proj GEMM (+residual; after layer L/2-1 the
+//                 result is written to a separate buffer, which becomes the backout cache)
+//   rownorm (x - lb*x_mid, norm) -> lm_head GEMM (soft-cap)
+#include "internal.h"
+
+#include <cudaTypedefs.h>
+
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <vector>
+
+namespace nc {
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+}  // namespace
+
+bool make_tmap_bf16_2d(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer,
+                       uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer) {
+  auto fn = get_encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_stride_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace nc
+
+using nc::bf16;
+
+namespace {
+
+constexpr size_t ALIGN = 256;
+inline size_t align_up(size_t x) { return (x + ALIGN - 1) / ALIGN * ALIGN; }
+inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+struct TimedLaunch {
+  int cls;
+  cudaEvent_t a, b;
+};
+
+struct Layout {
+  size_t x0, xa, xm, xn, q, k, v, gate, y, h, end;
+};
+
+}  // namespace
+
+struct nc_model {
+  nc_config cfg{};
+  std::vector<int> window;
+  std::vector<unsigned char> has_ve;
+  std::vector<float> lr, l0;
+  float lb = 0.f;
+  const bf16* wte = nullptr;
+  const bf16* smear = nullptr;
+  const bf16* lm = nullptr;
+  std::vector<const bf16*> wo, wfc, wproj, ve, veg;
+  bf16* wqkv = nullptr;     // packed [L][(H+2Hkv)*D][C]
+  float2* rope = nullptr;   // [seq_len_ctx][D/2]
+  int* status = nullptr;    // device status word
+  int num_sms = 148;
+  bool timing = false;
+  std::vector<TimedLaunch> pending;
+  std::vector<cudaEvent_t> free_events;
+  double acc_ms[NC_K_COUNT] = {};
+  int acc_n[NC_K_COUNT] = {};
+
+  int C() const { return cfg.n_embd; }
+  int Nqkv() const { return (cfg.n_head + 2 * cfg.n_kv_head) * cfg.head_dim; }
+  size_t qkv_layer_elems() const { return static_cast<size_t>(Nqkv()) * C(); }
+};
+
+namespace {
+
+nc_status validate_config(const nc_config* c) {
+  if (c == nullptr) return NC_ERR_INVALID_ARG;
+  if (c->n_layer < 1 || c->n_embd < 1 || c->n_head < 1 || c->n_kv_head < 1 || c->head_dim < 1 ||
+      c->mlp_hidden < 1 || c->vocab_size < 1 || c->seq_len_ctx < 1)
+    return NC_ERR_INVALID_ARG;
+  if (c->window_left == nullptr || c->has_ve == nullptr) return NC_ERR_INVALID_ARG;
+  if (c->n_embd != c->n_head * c->head_dim) return NC_ERR_INVALID_ARG;
+  if (c->n_head % c->n_kv_head != 0) return NC_ERR_INVALID_ARG;
+  if (c->smear_gate_channels < 0 || c->smear_gate_channels > c->n_embd) return NC_ERR_INVALID_ARG;
+  if (c->ve_gate_channels < 0 || c->ve_gate_channels > c->n_embd) return NC_ERR_INVALID_ARG;
+  if (!(c->rms_eps >= 0.f) || !(c->softcap > 0.f) || !(c->rope_base > 0.f)) return NC_ERR_INVALID_ARG;
+  if (c->head_dim != 64 && c->head_dim != 128) return NC_ERR_UNSUPPORTED;
+  if (c->n_embd % 128 != 0 || c->n_embd > 2048) return NC_ERR_UNSUPPORTED;
+  if (c->mlp_hidden % 64 != 0 || c->vocab_size % 64 != 0) return NC_ERR_UNSUPPORTED;
+  if (c->smear_gate_channels % 4 != 0 || c->ve_gate_channels % 4 != 0) return NC_ERR_UNSUPPORTED;
+  return NC_OK;
+}
+
+size_t packed_bytes_for(const nc_config* c) {
+  const size_t status = ALIGN;
+  const size_t rope = align_up(static_cast<size_t>(c->seq_len_ctx) * (c->head_dim / 2) * sizeof(float2));
+  const size_t qkv = static_cast<size_t>(c->n_layer) * (c->n_head + 2 * c->n_kv_head) * c->head_dim *
+                     c->n_embd * sizeof(bf16);
+  return status + rope + align_up(qkv);
+}
+
+Layout layout_for(const nc_model* m, int B, int T) {
+  const nc_config& c = m->cfg;
+  const size_t M = static_cast<size_t>(B) * T;
+  Layout L{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off += align_up(bytes);
+    return o;
+  };
+  L.x0 = take(M * c.n_embd * 4);
+  L.xa = take(M * c.n_embd * 4);
+  L.xm = take(c.use_backout ? M * c.n_embd * 4 : 0);
+  L.xn = take(M * c.n_embd * 2);
+  L.q = take(M * c.n_head * c.head_dim * 2);
+  L.k = take(M * c.n_kv_head * c.head_dim * 2);
+  L.v = take(M * c.n_kv_head * c.head_dim * 2);
+  L.gate = take(M * c.n_kv_head * 4);
+  L.y = take(M * c.n_head * c.head_dim * 2);
+  L.h = take(M * c.mlp_hidden * 2);
+  L.end = off;
+  return L;
+}
+
+cudaEvent_t take_event(nc_model* m) {
+  if (!m->free_events.empty()) {
+    cudaEvent_t e = m->free_events.back();
+    m->free_events.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+
+// Runs `launch` and, with timing on, brackets it with an event pair on `stream`.
+template <typename F>
+cudaError_t timed(nc_model* m, int cls, cudaStream_t stream, F&& launch) {
+  if (!m->timing) return launch();
+  TimedLaunch t{cls, take_event(m), take_event(m)};
+  cudaEventRecord(t.a, stream);
+  cudaError_t e = launch();
+  cudaEventRecord(t.b, stream);
+  m->pending.push_back(t);
+  return e;
+}
+
+void flush_timing(nc_model* m) {
+  for (auto& t : m->pending) {
+    float ms = 0.f;
+    cudaEventSynchronize(t.b);
+    if (cudaEventElapsedTime(&ms, t.a, t.b) == cudaSuccess) {
+      m->acc_ms[t.cls] += ms;
+      m->acc_n[t.cls] += 1;
+    }
+    m->free_events.push_back(t.a);
+    m->free_events.push_back(t.b);
+  }
+  m->pending.clear();
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* nc_status_string(nc_status s) {
+  switch (s) {
+    case NC_OK: return "ok";
+    case NC_ERR_INVALID_ARG: return "invalid argument";
+    case NC_ERR_UNSUPPORTED: return "unsupported configuration";
+    case NC_ERR_WORKSPACE: return "buffer smaller than required";
+    case NC_ERR_CUDA: return "CUDA runtime error";
+    case NC_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+    case NC_ERR_TOKEN_RANGE: return "token id out of range";
+    default: return "unknown status";
+  }
+}
+
+const char* nc_kernel_class_name(nc_kernel_class k) {
+  static const char* names[NC_K_COUNT] = {"embed_smear", "rownorm",  "qkv_rope_qknorm_ve",
+                                          "attention",   "oproj_residual", "fc_relu2",
+                                          "proj_residual", "lmhead_softcap"};
+  return (k >= 0 && k < NC_K_COUNT) ? names[k] : "unknown";
+}
+
+nc_status nc_model_packed_bytes(const nc_config* cfg, size_t* bytes) {
+  if (bytes == nullptr) return NC_ERR_INVALID_ARG;
+  nc_status s = validate_config(cfg);
+  if (s != NC_OK) return s;
+  *bytes = packed_bytes_for(cfg);
+  return NC_OK;
+}
+
+nc_status nc_model_create(const nc_config* cfg, const nc_weights* w, void* packed_buf,
+                          size_t packed_bytes, void* stream_, nc_model** out) {
+  if (out == nullptr) return NC_ERR_INVALID_ARG;
+  *out = nullptr;
+  nc_status s = validate_config(cfg);
+  if (s != NC_OK) return s;
+  if (w == nullptr || packed_buf == nullptr) return NC_ERR_INVALID_ARG;
+  if (!aligned(packed_buf, ALIGN)) return NC_ERR_INVALID_ARG;
+  if (packed_bytes < packed_bytes_for(cfg)) return NC_ERR_WORKSPACE;
+  const int L = cfg->n_layer;
+  if (w->wte == nullptr || w->lm_head == nullptr || w->wq == nullptr || w->wk == nullptr ||
+      w->wv == nullptr || w->wo == nullptr || w->wfc == nullptr || w->wproj == nullptr ||
+      w->resid_lambdas == nullptr || w->x0_lambdas == nullptr)
+    return NC_ERR_INVALID_ARG;
+  if (cfg->use_smear && w->smear_gate == nullptr) return NC_ERR_INVALID_ARG;
+  for (int i = 0; i < L; ++i) {
+    const void* ptrs[] = {w->wq[i], w->wk[i], w->wv[i], w->wo[i], w->wfc[i], w->wproj[i]};
+    for (const void* p : ptrs)
+      if (p == nullptr || !aligned(p, 16)) return NC_ERR_INVALID_ARG;
+    if (cfg->has_ve[i]) {
+      if (w->ve_table == nullptr || w->ve_gate == nullptr || w->ve_table[i] == nullptr ||
+          w->ve_gate[i] == nullptr || !aligned(w->ve_table[i], 16) || !aligned(w->ve_gate[i], 8))
+        return NC_ERR_INVALID_ARG;
+    }
+  }
+  if (!aligned(w->wte, 16) || !aligned(w->lm_head, 16)) return NC_ERR_INVALID_ARG;
+  if (cfg->use_smear && !aligned(w->smear_gate, 8)) return NC_ERR_INVALID_ARG;
+
+  nc_model* m = new (std::nothrow) nc_model();
+  if (m == nullptr) return NC_ERR_INVALID_ARG;
+  m->cfg = *cfg;
+  m->window.assign(cfg->window_left, cfg->window_left + L);
+  m->has_ve.assign(cfg->has_ve, cfg->has_ve + L);
+  m->cfg.window_left = m->window.data();
+  m->cfg.has_ve = m->has_ve.data();
+  m->lr.assign(w->resid_lambdas, w->resid_lambdas + L);
+  m->l0.assign(w->x0_lambdas, w->x0_lambdas + L);
+  m->lb = w->backout_lambda;
+  m->wte = static_cast<const bf16*>(w->wte);
+  m->lm = static_cast<const bf16*>(w->lm_head);
+  m->smear = cfg->use_smear ? static_cast<const bf16*>(w->smear_gate) : nullptr;
+  for (int i = 0; i < L; ++i) {
+    m->wo.push_back(static_cast<const bf16*>(w->wo[i]));
+    m->wfc.push_back(static_cast<const bf16*>(w->wfc[i]));
+    m->wproj.push_back(static_cast<const bf16*>(w->wproj[i]));
+    m->ve.push_back(cfg->has_ve[i] ? static_cast<const bf16*>(w->ve_table[i]) : nullptr);
+    m->veg.push_back(cfg->has_ve[i] ? static_cast<const bf16*>(w->ve_gate[i]) : nullptr);
+  }
+  uint8_t* base = static_cast<uint8_t*>(packed_buf);
+  m->status = reinterpret_cast<int*>(base);
+  m->rope = reinterpret_cast<float2*>(base + ALIGN);
+  m->wqkv = reinterpret_cast<bf16*>(
+      base + ALIGN + align_up(static_cast<size_t>(cfg->seq_len_ctx) * (cfg->head_dim / 2) * sizeof(float2)));
+
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&m->num_sms, cudaDevAttrMultiProcessorCount, dev);
+  const size_t C = cfg->n_embd, qd = static_cast<size_t>(cfg->n_head) * cfg->head_dim,
+               kd = static_cast<size_t>(cfg->n_kv_head) * cfg->head_dim;
+  for (int i = 0; i < L && e == cudaSuccess; ++i) {
+    bf16* dst = m->wqkv + static_cast<size_t>(i) * m->qkv_layer_elems();
+    e = cudaMemcpyAsync(dst, w->wq[i], qd * C * 2, cudaMemcpyDeviceToDevice, stream);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(dst + qd * C, w->wk[i], kd * C * 2, cudaMemcpyDeviceToDevice, stream);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(dst + (qd + kd) * C, w->wv[i], kd * C * 2, cudaMemcpyDeviceToDevice, stream);
+  }
+  if (e == cudaSuccess) e = cudaMemsetAsync(m->status, 0, sizeof(int), stream);
+  if (e == cudaSuccess)
+    e = nc::launch_rope_table(m->rope, cfg->seq_len_ctx, cfg->head_dim, cfg->rope_base, stream);
+  if (e != cudaSuccess) {
+    delete m;
+    return NC_ERR_CUDA;
+  }
+  *out = m;
+  return NC_OK;
+}
+
+nc_status nc_workspace_bytes(const nc_model* m, int B, int T, size_t* bytes) {
+  if (m == nullptr || bytes == nullptr || B < 1 || T < 1) return NC_ERR_INVALID_ARG;
+  if (T > m->cfg.seq_len_ctx) return NC_ERR_UNSUPPORTED;
+  *bytes = layout_for(m, B, T).end;
+  return NC_OK;
+}
+
+nc_status nc_workspace_bytes_host(const nc_model* m, int B, int T, size_t* bytes) {
+  size_t base = 0;
+  nc_status s = nc_workspace_bytes(m, B, T, &base);
+  if (s != NC_OK) return s;
+  const size_t M = static_cast<size_t>(B) * T;
+  *bytes = base + align_up(M * 4) + align_up(M * m->cfg.vocab_size * 4);
+  return NC_OK;
+}
+
+nc_status nc_forward(nc_model* m, const int32_t* tokens, int B, int T, float* logits,
+                     void* workspace, size_t ws_bytes, void* stream_) {
+  if (m == nullptr || tokens == nullptr || logits == nullptr || workspace == nullptr)
+    return NC_ERR_INVALID_ARG;
+  if (B < 1 || T < 1) return NC_ERR_INVALID_ARG;
+  if (T > m->cfg.seq_len_ctx) return NC_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * T > (1LL << 30)) return NC_ERR_UNSUPPORTED;
+  if (!aligned(workspace, ALIGN) || !aligned(logits, 16) || !aligned(tokens, 4)) return NC_ERR_INVALID_ARG;
+  const Layout Lo = layout_for(m, B, T);
+  if (ws_bytes < Lo.end) return NC_ERR_WORKSPACE;
+
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  const nc_config& c = m->cfg;
+  const int M = B * T, C = c.n_embd, H = c.n_head, Hkv = c.n_kv_head, D = c.head_dim;
+  const int F = c.mlp_hidden, V = c.vocab_size, L = c.n_layer;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  float* x0 = reinterpret_cast<float*>(ws + Lo.x0);
+  float* xa = reinterpret_cast<float*>(ws + Lo.xa);
+  float* xm = reinterpret_cast<float*>(ws + Lo.xm);
+  bf16* xn = reinterpret_cast<bf16*>(ws + Lo.xn);
+  bf16* q = reinterpret_cast<bf16*>(ws + Lo.q);
+  bf16* k = reinterpret_cast<bf16*>(ws + Lo.k);
+  bf16* v = reinterpret_cast<bf16*>(ws + Lo.v);
+  float* gate = reinterpret_cast<float*>(ws + Lo.gate);
+  bf16* y = reinterpret_cast<bf16*>(ws + Lo.y);
+  bf16* h = reinterpret_cast<bf16*>(ws + Lo.h);
+  const int c_s = c.smear_gate_channels ? c.smear_gate_channels : C;
+  const int c_g = c.ve_gate_channels ? c.ve_gate_channels : C;
+  const int mid = L / 2 - 1;
+
+  cudaError_t e = timed(m, NC_K_EMBED, stream, [&] {
+    return nc::launch_embed_smear(tokens, B, T, m->wte, V, C, m->smear, c_s, c.embed_norm, c.rms_eps, x0,
+                                  m->status, stream);
+  });
+  const float* cur = x0;
+  for (int i = 0; i < L && e == cudaSuccess; ++i) {
+    const bool ve = m->has_ve[i] != 0;
+    e = timed(m, NC_K_NORM, stream, [&] {
+      return nc::launch_rownorm(cur, x0, m->lr[i], m->l0[i], xa, xn, M, C, c.rms_eps, m->veg[i], Hkv, c_g,
+                                c.ve_gate_scale, ve ? gate : nullptr, stream);
+    });
+    cur = xa;
+    if (e != cudaSuccess) break;
+    nc::GemmEpi qe;
+    qe.kind = nc::EPI_QKV;
+    qe.q = q;
+    qe.k = k;
+    qe.v = v;
+    qe.H = H;
+    qe.Hkv = Hkv;
+    qe.D = D;
+    qe.T = T;
+    qe.rope = m->rope;
+    qe.eps = c.rms_eps;
+    qe.gate = ve ? gate : nullptr;
+    qe.ve = m->ve[i];
+    qe.tokens = tokens;
+    qe.V = V;
+    qe.status = m->status;
+    e = timed(m, NC_K_QKV, stream, [&] {
+      return nc::launch_gemm(xn, m->wqkv + static_cast<size_t>(i) * m->qkv_layer_elems(), M, m->Nqkv(), C,
+                             qe, m->num_sms, stream);
+    });
+    if (e != cudaSuccess) break;
+    e = timed(m, NC_K_ATTN, stream, [&] {
+      return nc::launch_attention(q, k, v, B, T, H, Hkv, D, m->window[i], y, m->status, stream);
+    });
+    if (e != cudaSuccess) break;
+    nc::GemmEpi re;
+    re.kind = nc::EPI_RESID_F32;
+    re.out = xa;
+    re.ldo = C;
+    re.resid = xa;
+    re.ldr = C;
+    re.status = m->status;
+    e = timed(m, NC_K_OPROJ, stream, [&] {
+      return nc::launch_gemm(y, m->wo[i], M, C, H * D, re, m->num_sms, stream);
+    });
+    if (e != cudaSuccess) break;
+    e = timed(m, NC_K_NORM, stream, [&] {
+      return nc::launch_rownorm(xa, nullptr, 1.f, 0.f, nullptr, xn, M, C, c.rms_eps, nullptr, 0, c_g, 1.f,
+                                nullptr, stream);
+    });
+    if (e != cudaSuccess) break;
+    nc::GemmEpi fe;
+    fe.kind = nc::EPI_RELU2_BF16;
+    fe.out = h;
+    fe.ldo = F;
+    fe.status = m->status;
+    e = timed(m, NC_K_FC, stream, [&] { return nc::launch_gemm(xn, m->wfc[i], M, F, C, fe, m->num_sms, stream); });
+    if (e != cudaSuccess) break;
+    nc::GemmEpi pe = re;
+    float* dst = (c.use_backout && i == mid) ? xm : xa;
+    pe.out = dst;
+    pe.resid = xa;
+    e = timed(m, NC_K_PROJ, stream, [&] { return nc::launch_gemm(h, m->wproj[i], M, C, F, pe, m->num_sms, stream); });
+    cur = dst;
+  }
+  if (e == cudaSuccess) {
+    const float* xmid = c.use_backout ? (mid < 0 ? x0 : xm) : nullptr;
+    e = timed(m, NC_K_NORM, stream, [&] {
+      return nc::launch_rownorm(cur, xmid, 1.f, xmid ? -m->lb : 0.f, nullptr, xn, M, C, c.rms_eps, nullptr, 0,
+                                c_g, 1.f, nullptr, stream);
+    });
+  }
+  if (e == cudaSuccess) {
+    nc::GemmEpi le;
+    le.kind = nc::EPI_SOFTCAP_F32;
+    le.out = logits;
+    le.ldo = V;
+    le.cap = c.softcap;
+    le.status = m->status;
+    e = timed(m, NC_K_LMHEAD, stream, [&] { return nc::launch_gemm(xn, m->lm, M, V, C, le, m->num_sms, stream); });
+  }
+  return e == cudaSuccess ? NC_OK : NC_ERR_CUDA;
+}
+
+nc_status nc_forward_host(nc_model* m, const int32_t* tokens_host, int B, int T, float* logits_host,
+                          void* workspace, size_t ws_bytes, void* stream_) {
+  if (m == nullptr || tokens_host == nullptr || logits_host == nullptr || workspace == nullptr)
+    return NC_ERR_INVALID_ARG;
+  size_t need = 0;
+  nc_status s = nc_workspace_bytes_host(m, B, T, &need);
+  if (s != NC_OK) return s;
+  if (ws_bytes < need) return NC_ERR_WORKSPACE;
+  if (!aligned(workspace, ALIGN)) return NC_ERR_INVALID_ARG;
+  size_t base = 0;
+  nc_workspace_bytes(m, B, T, &base);
+  const size_t M = static_cast<size_t>(B) * T;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int32_t* tok_dev = reinterpret_cast<int32_t*>(ws + base);
+  float* logits_dev = reinterpret_cast<float*>(ws + base + align_up(M * 4));
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  if (cudaMemcpyAsync(tok_dev, tokens_host, M * 4, cudaMemcpyHostToDevice, stream) != cudaSuccess)
+    return NC_ERR_CUDA;
+  s = nc_forward(m, tok_dev, B, T, logits_dev, workspace, base, stream_);
+  if (s != NC_OK) return s;
+  if (cudaMemcpyAsync(logits_host, logits_dev, M * m->cfg.vocab_size * 4, cudaMemcpyDeviceToHost, stream) !=
+      cudaSuccess)
+    return NC_ERR_CUDA;
+  return cudaStreamSynchronize(stream) == cudaSuccess ? NC_OK : NC_ERR_CUDA;
+}
+
+nc_status nc_get_status(nc_model* m, void* stream_) {
+  if (m == nullptr) return NC_ERR_INVALID_ARG;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  int h = 0;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return NC_ERR_CUDA;
+  if (cudaMemcpy(&h, m->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return NC_ERR_CUDA;
+  if (cudaMemset(m->status, 0, sizeof(int)) != cudaSuccess) return NC_ERR_CUDA;
+  return static_cast<nc_status>(h);
+}
+
+void nc_model_destroy(nc_model* m) {
+  if (m == nullptr) return;
+  flush_timing(m);
+  for (cudaEvent_t e : m->free_events) cudaEventDestroy(e);
+  delete m;
+}
+
+nc_status nc_timing_enable(nc_model* m, int enable) {
+  if (m == nullptr) return NC_ERR_INVALID_ARG;
+  m->timing = enable != 0;
+  return NC_OK;
+}
+
+nc_status nc_timing_read(nc_model* m, nc_kernel_class k, double* total_ms, int* launches) {
+  if (m == nullptr || total_ms == nullptr || launches == nullptr || k < 0 || k >= NC_K_COUNT)
+    return NC_ERR_INVALID_ARG;
+  flush_timing(m);
+  *total_ms = m->acc_ms[k];
+  *launches = m->acc_n[k];
+  m->acc_ms[k] = 0.0;
+  m->acc_n[k] = 0;
+  return NC_OK;
+}
+
+int nc_forward_launch_count(const nc_model* m) {
+  if (m == nullptr) return 0;
+  return 1 + 7 * m->cfg.n_layer + 2;
+}
+
+}  // extern "C"

@@ -1,0 +1,221 @@
+// rowops.cu -- memory-bound per-row kernels: embedding + smear, residual mix + RMSNorm
+// (+ value-embedding gate), and the rotary-angle table.
+//
+// One warp per row, 8 rows per 256-thread block; each lane owns C/128 groups of 4
+// consecutive channels (offset 128*i + 4*lane), so every load and store is a coalesced
+// 128-bit (fp32) or 64-bit (bf16 x4) access; reductions are warp shuffles.
+//
+// Definitions ("Nanochat在nanoGPT之上的新增功能", section 1 table and notes):
+//   RMSNorm has no learned weight; smear adds sigmoid(gate(x)) times the previous token's
+//   embedding; blocks rescale the residual stream by resid_lambdas and add x0_lambdas * x0;
+//   backout subtracts lambda times the residual cached at mid depth before the final norm.
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace nc {
+namespace {
+
+constexpr int ROWS_PER_BLOCK = 8;
+
+__device__ __forceinline__ float4 ld_bf16x4(const bf16* p) {
+  const uint2 u = *reinterpret_cast<const uint2*>(p);
+  const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+  const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+  return make_float4(a.x, a.y, b.x, b.y);
+}
+
+__device__ __forceinline__ void st_bf16x4(bf16* p, float4 v) {
+  uint2 u;
+  u.x = pack_bf16(v.x, v.y);
+  u.y = pack_bf16(v.z, v.w);
+  *reinterpret_cast<uint2*>(p) = u;
+}
+
+__device__ __forceinline__ float sigmoidf_(float z) { return 1.0f / (1.0f + expf(-z)); }
+
+template <int NV4>
+__device__ __forceinline__ void load_embedding(const bf16* wte, int tok, int V, int lane, bool norm,
+                                               float eps, float4 (&e)[NV4]) {
+  constexpr int C = NV4 * 128;
+  const bool ok = tok >= 0 && tok < V;
+#pragma unroll
+  for (int i = 0; i < NV4; ++i)
+    e[i] = ok ? ld_bf16x4(wte + static_cast<size_t>(tok) * C + i * 128 + lane * 4)
+              : make_float4(0.f, 0.f, 0.f, 0.f);
+  if (norm) {
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < NV4; ++i) ss += e[i].x * e[i].x + e[i].y * e[i].y + e[i].z * e[i].z + e[i].w * e[i].w;
+    const float r = rsqrtf(warp_sum(ss) * (1.0f / C) + eps);
+#pragma unroll
+    for (int i = 0; i < NV4; ++i) {
+      e[i].x *= r; e[i].y *= r; e[i].z *= r; e[i].w *= r;
+    }
+  }
+}
+
+template <int NV4>
+__global__ void __launch_bounds__(32 * ROWS_PER_BLOCK)
+    embed_smear_kernel(const int32_t* __restrict__ tokens, int M, int T, const bf16* __restrict__ wte,
+                       int V, const bf16* __restrict__ smear_gate, int c_s, int embed_norm, float eps,
+                       float* __restrict__ x0, int* status) {
+  constexpr int C = NV4 * 128;
+  const int lane = threadIdx.x & 31;
+  const int row = blockIdx.x * ROWS_PER_BLOCK + (threadIdx.x >> 5);
+  if (row >= M) return;
+  const int t = row % T;
+  const int tok = tokens[row];
+  if ((tok < 0 || tok >= V) && lane == 0) record_error(status, NC_ERR_TOKEN_RANGE);
+  float4 e[NV4];
+  load_embedding<NV4>(wte, tok, V, lane, embed_norm != 0, eps, e);
+  if (smear_gate != nullptr && t > 0) {
+    float dot = 0.f;
+#pragma unroll
+    for (int i = 0; i < NV4; ++i) {
+      const int c = i * 128 + lane * 4;
+      if (c < c_s) {
+        const float4 g = ld_bf16x4(smear_gate + c);
+        dot += e[i].x * g.x + e[i].y * g.y + e[i].z * g.z + e[i].w * g.w;
+      }
+    }
+    const float gate = sigmoidf_(warp_sum(dot));
+    float4 p[NV4];
+    load_embedding<NV4>(wte, tokens[row - 1], V, lane, embed_norm != 0, eps, p);
+#pragma unroll
+    for (int i = 0; i < NV4; ++i) {
+      e[i].x = fmaf(gate, p[i].x, e[i].x);
+      e[i].y = fmaf(gate, p[i].y, e[i].y);
+      e[i].z = fmaf(gate, p[i].z, e[i].z);
+      e[i].w = fmaf(gate, p[i].w, e[i].w);
+    }
+  }
+  float* dst = x0 + static_cast<size_t>(row) * C;
+#pragma unroll
+  for (int i = 0; i < NV4; ++i) *reinterpret_cast<float4*>(dst + i * 128 + lane * 4) = e[i];
+}
+
+template <int NV4>
+__global__ void __launch_bounds__(32 * ROWS_PER_BLOCK)
+    rownorm_kernel(const float* x, const float* y, float a, float b,
+                   float* x_out, bf16* __restrict__ xn, int M, float eps, const bf16* __restrict__ wg,
+                   int Hkv, int c_g, float gate_scale, float* __restrict__ gate) {
+  constexpr int C = NV4 * 128;
+  const int lane = threadIdx.x & 31;
+  const int row = blockIdx.x * ROWS_PER_BLOCK + (threadIdx.x >> 5);
+  if (row >= M) return;
+  const size_t base = static_cast<size_t>(row) * C;
+  float4 v[NV4];
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < NV4; ++i) {
+    const int c = i * 128 + lane * 4;
+    float4 u = *reinterpret_cast<const float4*>(x + base + c);
+    if (y != nullptr) {
+      const float4 w = *reinterpret_cast<const float4*>(y + base + c);
+      u.x = a * u.x + b * w.x;
+      u.y = a * u.y + b * w.y;
+      u.z = a * u.z + b * w.z;
+      u.w = a * u.w + b * w.w;
+    } else if (a != 1.0f) {
+      u.x *= a; u.y *= a; u.z *= a; u.w *= a;
+    }
+    v[i] = u;
+    ss += u.x * u.x + u.y * u.y + u.z * u.z + u.w * u.w;
+  }
+  if (x_out != nullptr) {
+#pragma unroll
+    for (int i = 0; i < NV4; ++i) *reinterpret_cast<float4*>(x_out + base + i * 128 + lane * 4) = v[i];
+  }
+  const float r = rsqrtf(warp_sum(ss) * (1.0f / C) + eps);
+#pragma unroll
+  for (int i = 0; i < NV4; ++i) {
+    v[i].x *= r; v[i].y *= r; v[i].z *= r; v[i].w *= r;
+    st_bf16x4(xn + base + i * 128 + lane * 4, v[i]);
+  }
+  if (gate != nullptr) {
+    for (int h = 0; h < Hkv; ++h) {
+      float dot = 0.f;
+#pragma unroll
+      for (int i = 0; i < NV4; ++i) {
+        const int c = i * 128 + lane * 4;
+        if (c < c_g) {
+          const float4 g = ld_bf16x4(wg + static_cast<size_t>(h) * c_g + c);
+          dot += v[i].x * g.x + v[i].y * g.y + v[i].z * g.z + v[i].w * g.w;
+        }
+      }
+      dot = warp_sum(dot);
+      if (lane == 0) gate[static_cast<size_t>(row) * Hkv + h] = gate_scale * sigmoidf_(dot);
+    }
+  }
+}
+
+__global__ void rope_table_kernel(float2* table, int T, int half, double base) {
+  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= T * half) return;
+  const int t = idx / half, i = idx % half;
+  const double inv = pow(base, -2.0 * i / (2.0 * half));
+  double s, c;
+  sincos(static_cast<double>(t) * inv, &s, &c);
+  table[idx] = make_float2(static_cast<float>(c), static_cast<float>(s));
+}
+
+template <template <int> class Fn, typename... Args>
+cudaError_t dispatch_nv4(int C, Args&&... args) {
+  switch (C / 128) {
+#define NC_CASE(n) case n: return Fn<n>::run(args...);
+    NC_CASE(1) NC_CASE(2) NC_CASE(3) NC_CASE(4) NC_CASE(5) NC_CASE(6) NC_CASE(7) NC_CASE(8)
+    NC_CASE(9) NC_CASE(10) NC_CASE(11) NC_CASE(12) NC_CASE(13) NC_CASE(14) NC_CASE(15) NC_CASE(16)
+#undef NC_CASE
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <int NV4>
+struct EmbedLaunch {
+  static cudaError_t run(const int32_t* tokens, int M, int T, const bf16* wte, int V,
+                         const bf16* smear_gate, int c_s, int embed_norm, float eps, float* x0,
+                         int* status, cudaStream_t stream) {
+    const int grid = (M + ROWS_PER_BLOCK - 1) / ROWS_PER_BLOCK;
+    embed_smear_kernel<NV4><<<grid, 32 * ROWS_PER_BLOCK, 0, stream>>>(
+        tokens, M, T, wte, V, smear_gate, c_s, embed_norm, eps, x0, status);
+    return cudaGetLastError();
+  }
+};
+
+template <int NV4>
+struct NormLaunch {
+  static cudaError_t run(const float* x, const float* y, float a, float b, float* x_out, bf16* xn,
+                         int M, float eps, const bf16* wg, int Hkv, int c_g, float gate_scale,
+                         float* gate, cudaStream_t stream) {
+    const int grid = (M + ROWS_PER_BLOCK - 1) / ROWS_PER_BLOCK;
+    rownorm_kernel<NV4><<<grid, 32 * ROWS_PER_BLOCK, 0, stream>>>(x, y, a, b, x_out, xn, M, eps, wg,
+                                                                  Hkv, c_g, gate_scale, gate);
+    return cudaGetLastError();
+  }
+};
+
+}  // namespace
+
+cudaError_t launch_embed_smear(const int32_t* tokens, int B, int T, const bf16* wte, int V, int C,
+                               const bf16* smear_gate, int c_s, int embed_norm, float eps,
+                               float* x0, int* status, cudaStream_t stream) {
+  if (C % 128 != 0 || c_s % 4 != 0) return cudaErrorInvalidValue;
+  return dispatch_nv4<EmbedLaunch>(C, tokens, B * T, T, wte, V, smear_gate, c_s, embed_norm, eps,
+                                   x0, status, stream);
+}
+
+cudaError_t launch_rownorm(const float* x, const float* y, float a, float b, float* x_out, bf16* xn,
+                           int M, int C, float eps, const bf16* wg, int Hkv, int c_g,
+                           float gate_scale, float* gate, cudaStream_t stream) {
+  if (C % 128 != 0 || (gate != nullptr && c_g % 4 != 0)) return cudaErrorInvalidValue;
+  return dispatch_nv4<NormLaunch>(C, x, y, a, b, x_out, xn, M, eps, wg, Hkv, c_g, gate_scale, gate,
+                                  stream);
+}
+
+cudaError_t launch_rope_table(float2* table, int T, int D, float base, cudaStream_t stream) {
+  const int n = T * (D / 2);
+  rope_table_kernel<<<(n + 255) / 256, 256, 0, stream>>>(table, T, D / 2, static_cast<double>(base));
+  return cudaGetLastError();
+}
+
+}  // namespace nc

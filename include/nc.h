@@ -1,0 +1,190 @@
+/*
+ * nc.h -- C ABI of the B300 (sm_103a) forward pass of a nanochat-style
+ * decoder-only GPT.
+ *
+ * What the forward computes (web pages cited by title and section):
+ *
+ *  - "Nanochat在nanoGPT之上的新增功能" (what nanochat adds over nanoGPT),
+ *    section 1 feature table and the notes under it: rotary position
+ *    embedding and no position table; RMSNorm without learned parameters;
+ *    squared-ReLU MLP; separate q, k, v and output projections, no biases;
+ *    grouped-query attention; q and k RMS-normalised after RoPE; logits
+ *    soft-capped by tanh to (-15, 15); per-layer sliding windows, three
+ *    short (a quarter of the context) then one full, the last layer always
+ *    full; value embeddings added to v through a gate on alternating layers
+ *    including the last; smear (the previous token's embedding mixed in
+ *    through a sigmoid gate); backout (a lambda times the residual stream
+ *    cached at mid depth is subtracted before the final norm); per-layer
+ *    resid_lambdas / x0_lambdas; untied embedding and lm_head.
+ *  - "NanoChat基础训练报告" (NanoChat base-training report), section
+ *    "模型架构": the d12 shape (12 layers, 768 wide, 6 heads of 128, 6 kv
+ *    heads, 32,768 vocabulary, value embeddings with a learned gate on the
+ *    odd layers).
+ *  - "nanochat — 架构与原理" (nanochat architecture and principles), section
+ *    2 component table: GPT.forward(idx) maps token ids to logits; the
+ *    attention backend and the FP8 path it lists are prior art here.
+ *
+ * Readings of what the pages leave open (all fixed by nc_config fields):
+ *  - RMSNorm is x / sqrt(mean(x^2) + rms_eps).
+ *  - RoPE pairs channel d with d + head_dim/2, angle pos * rope_base^(-2d/D),
+ *    y1 = x1 cos + x2 sin, y2 = -x1 sin + x2 cos; positions restart at 0 in
+ *    every batch row (no document mask).
+ *  - Window W (window_left[i] >= 0): query i sees keys max(0, i-W) .. i.
+ *    window_left[i] < 0: plain causal.
+ *  - GQA: query head h reads kv head h / (n_head / n_kv_head).
+ *  - Smear gate: sigmoid(e_t[:c_s] . smear_gate), one scalar per token,
+ *    times the previous token's (pre-smear) embedding; the first token of a
+ *    row is unchanged.  The smeared embedding is x0.
+ *  - Value-embedding gate: ve_gate_scale * sigmoid(a_t[:c_g] . ve_gate[g])
+ *    per token and kv head g, a_t the block's normalised input;
+ *    v <- v + gate * ve_table[token].
+ *  - x <- resid_lambdas[i] * x + x0_lambdas[i] * x0 at the start of block i.
+ *  - Backout caches x after block n_layer/2 - 1 (x0 when n_layer == 1).
+ *
+ * Numerics: bf16 weights and activations into the tensor cores, fp32
+ * accumulation, fp32 residual stream, fp32 softmax statistics.
+ *
+ * Threading: a model is not re-entrant; calls on one model must not overlap.
+ */
+#ifndef NC_H
+#define NC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define NC_API __attribute__((visibility("default")))
+#else
+#define NC_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  NC_OK = 0,
+  NC_ERR_INVALID_ARG = 1,     /* null pointer, non-positive size, inconsistent shape */
+  NC_ERR_UNSUPPORTED = 2,     /* valid but not implemented (e.g. head_dim not 64/128) */
+  NC_ERR_WORKSPACE = 3,       /* caller buffer smaller than the size query returned */
+  NC_ERR_CUDA = 4,            /* a CUDA runtime call failed */
+  NC_ERR_DEVICE_TIMEOUT = 5,  /* a bounded device-side wait ran out (kernel returned early) */
+  NC_ERR_TOKEN_RANGE = 6      /* a token id outside [0, vocab_size); that row used zeros */
+} nc_status;
+
+/* Model hyper-parameters.  Host memory; copied by nc_model_create. */
+typedef struct {
+  int n_layer;
+  int n_embd;                 /* C; must equal n_head * head_dim; multiple of 128 */
+  int n_head;                 /* H */
+  int n_kv_head;              /* Hkv; divides n_head */
+  int head_dim;               /* D: 64 or 128 */
+  int mlp_hidden;             /* F; multiple of 64 */
+  int vocab_size;             /* V; multiple of 64 */
+  int seq_len_ctx;            /* largest T accepted by nc_forward */
+  const int *window_left;     /* [n_layer]; < 0 = full causal */
+  const unsigned char *has_ve;/* [n_layer]; nonzero = value-embedding layer */
+  int use_smear;
+  int use_backout;
+  int embed_norm;             /* RMSNorm the token embedding before smear (default 0) */
+  int smear_gate_channels;    /* c_s, 0 = n_embd */
+  int ve_gate_channels;       /* c_g, 0 = n_embd */
+  float ve_gate_scale;        /* default 1 */
+  float rms_eps;              /* default 1e-6 */
+  float rope_base;            /* default 10000 */
+  float softcap;              /* default 15 */
+} nc_config;
+
+/* Weights.  Matrices are bf16, row-major in the nn.Linear layout [out, in],
+ * in device memory.  BORROWED: they must outlive the model.  Per-layer
+ * arrays are host arrays of n_layer device pointers; entries of ve_table and
+ * ve_gate are ignored (may be NULL) on layers without value embeddings. */
+typedef struct {
+  const void *wte;                    /* [V, C] */
+  const void *const *wq;              /* [H*D, C] per layer */
+  const void *const *wk;              /* [Hkv*D, C] */
+  const void *const *wv;              /* [Hkv*D, C] */
+  const void *const *wo;              /* [C, H*D] */
+  const void *const *wfc;             /* [F, C] */
+  const void *const *wproj;           /* [C, F] */
+  const void *const *ve_table;        /* [V, Hkv*D] */
+  const void *const *ve_gate;         /* [Hkv, c_g] */
+  const void *smear_gate;             /* [c_s]; unused if !use_smear */
+  const void *lm_head;                /* [V, C] */
+  const float *resid_lambdas;         /* host [n_layer], copied */
+  const float *x0_lambdas;            /* host [n_layer], copied */
+  float backout_lambda;
+} nc_weights;
+
+typedef struct nc_model nc_model;
+
+/* Size in bytes of the device buffer nc_model_create fills with the packed
+ * q|k|v weights, the rotary table for seq_len_ctx positions and the device
+ * status word.  Host-only; validates the config. */
+NC_API nc_status nc_model_packed_bytes(const nc_config *cfg, size_t *bytes);
+
+/* Validate cfg, copy it, pack W_q|W_k|W_v of each layer into packed_buf
+ * (device, >= nc_model_packed_bytes, 256-byte aligned, caller-owned, must
+ * outlive the model) and fill the rotary table, on `stream`
+ * (cudaStream_t; NULL = legacy default stream).  The model itself owns only
+ * host state.  On error *out is NULL. */
+NC_API nc_status nc_model_create(const nc_config *cfg, const nc_weights *w, void *packed_buf,
+                          size_t packed_bytes, void *stream, nc_model **out);
+
+/* Device workspace needed by nc_forward for a [B, T] batch.  Host-only. */
+NC_API nc_status nc_workspace_bytes(const nc_model *m, int B, int T, size_t *bytes);
+
+/* Forward pass: tokens (device int32 [B, T]) -> logits (device fp32
+ * [B, T, V], row-major), soft-capped.  Asynchronous on `stream`; argument
+ * errors are returned synchronously before any device work; device-side
+ * errors (token range, wait timeout) are recorded in the status word and
+ * returned by nc_get_status.  workspace: device, >= nc_workspace_bytes,
+ * 256-byte aligned, caller-owned; T <= seq_len_ctx. */
+NC_API nc_status nc_forward(nc_model *m, const int32_t *tokens, int B, int T, float *logits,
+                     void *workspace, size_t ws_bytes, void *stream);
+
+/* Same forward with HOST buffers: copies tokens (host int32 [B, T]) in,
+ * runs nc_forward, copies logits (host fp32 [B, T, V]) out and synchronises
+ * `stream`.  Staging areas live in `workspace`, sized by
+ * nc_workspace_bytes_host.  Pinned host memory gives full copy bandwidth. */
+NC_API nc_status nc_workspace_bytes_host(const nc_model *m, int B, int T, size_t *bytes);
+NC_API nc_status nc_forward_host(nc_model *m, const int32_t *tokens_host, int B, int T,
+                          float *logits_host, void *workspace, size_t ws_bytes, void *stream);
+
+/* Synchronise `stream`, read and clear the device status word. */
+NC_API nc_status nc_get_status(nc_model *m, void *stream);
+
+NC_API const char *nc_status_string(nc_status s);
+
+/* Frees host state only (the caller owns every device buffer). */
+NC_API void nc_model_destroy(nc_model *m);
+
+/* ---- per-kernel timing (CUDA events recorded on the launch stream) ---- */
+
+/* Kernel classes timed when timing is enabled. */
+typedef enum {
+  NC_K_EMBED = 0,     /* embedding gather + smear */
+  NC_K_NORM = 1,      /* residual/x0 mix, backout, RMSNorm -> bf16 (+ VE gate) */
+  NC_K_QKV = 2,       /* q|k|v GEMM with RoPE, QK-norm and value-embedding epilogue */
+  NC_K_ATTN = 3,      /* windowed causal GQA attention */
+  NC_K_OPROJ = 4,     /* attention output projection + residual add */
+  NC_K_FC = 5,        /* MLP up projection + squared ReLU */
+  NC_K_PROJ = 6,      /* MLP down projection + residual add */
+  NC_K_LMHEAD = 7,    /* lm_head GEMM + tanh soft-cap */
+  NC_K_COUNT = 8
+} nc_kernel_class;
+
+/* enable != 0: every following nc_forward records an event pair around each
+ * launch; nc_timing_read sums them (syncs the events) and resets. */
+NC_API nc_status nc_timing_enable(nc_model *m, int enable);
+NC_API nc_status nc_timing_read(nc_model *m, nc_kernel_class k, double *total_ms, int *launches);
+NC_API const char *nc_kernel_class_name(nc_kernel_class k);
+
+/* Number of kernels one nc_forward launches for this model. */
+NC_API int nc_forward_launch_count(const nc_model *m);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NC_H */

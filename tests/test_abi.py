@@ -1,0 +1,95 @@
+"""C-ABI checks that need no GPU: the library loads, exports every declared symbol, and the
+host-side validation returns the documented status codes before touching the device."""
+import ctypes
+import os
+import re
+from dataclasses import replace
+
+import pytest
+
+from decoder_only_forward_02_b300 import binding as B
+from synth import get_workload
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    names = []
+    for h in ("nc.h", "nc_ops.h"):
+        src = open(os.path.join(ROOT, "include", h)).read()
+        names += re.findall(r"^NC_API\s+[\w\s\*]+?\b(nc_\w+)\s*\(", src, flags=re.M)
+    return names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = B.lib()
+    names = _declared()
+    assert len(names) >= 19
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) >= set(B._SIGS)
+
+
+def test_status_strings():
+    lib = B.lib()
+    for code in range(7):
+        assert lib.nc_status_string(code)
+    assert lib.nc_status_string(99) == b"unknown status"
+
+
+def _packed(cfg):
+    c, keep = B.make_config(cfg)
+    n = ctypes.c_size_t()
+    return B.lib().nc_model_packed_bytes(ctypes.byref(c), ctypes.byref(n)), n.value
+
+
+def test_packed_bytes_formula():
+    cfg = get_workload("d12").model
+    code, n = _packed(cfg)
+    assert code == 0
+    qkv = 12 * (6 + 12) * 128 * 768 * 2
+    rope = 2048 * 64 * 8
+    assert n == 256 + rope + qkv
+
+
+@pytest.mark.parametrize("change,code", [
+    (dict(n_embd=640), 1),           # C != H*D
+    (dict(n_kv_head=4), 1),          # H % Hkv != 0
+    (dict(head_dim=96, n_embd=576), 2),
+    (dict(mlp_hidden=3000), 2),
+    (dict(vocab_size=32769), 2),
+    (dict(smear_gate_channels=6), 2),
+    (dict(ve_gate_channels=1000), 1),
+    (dict(n_layer=0, window_left=(), has_ve=()), 1),
+])
+def test_config_validation(change, code):
+    cfg = replace(get_workload("d12").model, **change)
+    assert _packed(cfg)[0] == code
+
+
+def test_null_arguments_rejected_without_device_work():
+    lib = B.lib()
+    c, keep = B.make_config(get_workload("tiny").model)
+    n = ctypes.c_size_t()
+    assert lib.nc_model_packed_bytes(None, ctypes.byref(n)) == 1
+    assert lib.nc_model_packed_bytes(ctypes.byref(c), None) == 1
+    h = ctypes.c_void_p(1)
+    assert lib.nc_model_create(ctypes.byref(c), None, None, 0, None, ctypes.byref(h)) == 1
+    assert h.value is None
+    assert lib.nc_forward(None, None, 1, 1, None, None, 0, None) == 1
+    assert lib.nc_forward_host(None, None, 1, 1, None, None, 0, None) == 1
+    assert lib.nc_workspace_bytes(None, 1, 1, ctypes.byref(n)) == 1
+    assert lib.nc_get_status(None, None) == 1
+    assert lib.nc_timing_enable(None, 1) == 1
+    assert lib.nc_forward_launch_count(None) == 0
+    lib.nc_model_destroy(None)
+    # per-kernel entry points validate before launching
+    assert lib.nc_op_gemm(None, None, 1, 32, 64, 0, None, 32, None, 15.0, None, None) == 1
+    assert lib.nc_op_attention(None, None, None, 1, 1, 1, 1, 128, -1, None, None, None) == 1
+    assert lib.nc_op_rownorm(None, None, 1.0, 0.0, None, None, 1, 128, 1e-6, None, 0, 0, 1.0, None, None) == 1
+    assert lib.nc_op_rope_table(None, 4, 8, 1e4, None) == 1
+
+
+def test_kernel_class_names():
+    lib = B.lib()
+    assert [lib.nc_kernel_class_name(i).decode() for i in range(8)] == B.KERNEL_CLASSES
