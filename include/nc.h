@@ -151,6 +151,29 @@ NC_API nc_status nc_workspace_bytes_host(const nc_model *m, int B, int T, size_t
 NC_API nc_status nc_forward_host(nc_model *m, const int32_t *tokens_host, int B, int T,
                           float *logits_host, void *workspace, size_t ws_bytes, void *stream);
 
+/* Forward pass for callers that cannot allocate device memory when they run the model
+ * (for example code hosted by a framework that owns all device memory through its own pool
+ * and forbids raw cudaMalloc, or a latency-bound serving loop where cudaMalloc/cudaFree
+ * would synchronise the device).  The source pages have no counterpart to this call; it
+ * only changes where the forward's scratch lives.
+ *
+ * Identical to nc_forward, except that the activation scratch is a fixed array of
+ * NC_STATIC_SCRATCH_BYTES built into the library (every GPU that loads the library keeps
+ * it reserved until the process exits) instead of a caller workspace.  The caller passes
+ * only the model, tokens (device int32 [B, T]) and logits (device fp32 [B, T, V]).
+ *  - Limit: returns NC_ERR_WORKSPACE, before any device work, when nc_workspace_bytes(B, T)
+ *    exceeds NC_STATIC_SCRATCH_BYTES (at d12 width that is roughly 1,400 tokens per call).
+ *  - Allocates nothing: no cudaMalloc, cudaFree or allocating library routine.  Keep
+ *    per-kernel timing (nc_timing_enable) off, since it creates CUDA events.
+ *  - The first call on each device looks up the array's device address with that device
+ *    current; make that first call before any stream capture.
+ *  - All calls share the one array, which keeps the previous call's contents (nothing in it
+ *    needs to start at zero).  Calls that overlap on the GPU (other streams, other models,
+ *    other threads) race on it: serialise them. */
+#define NC_STATIC_SCRATCH_BYTES (32u * 1024u * 1024u)
+NC_API nc_status nc_forward_static_scratch(nc_model *m, const int32_t *tokens, int B, int T,
+                                           float *logits, void *stream);
+
 /* Synchronise `stream`, read and clear the device status word. */
 NC_API nc_status nc_get_status(nc_model *m, void *stream);
 
