@@ -41,9 +41,16 @@ struct GemmEpi {
   int* status = nullptr;
 };
 
-// Encodes TMA descriptors through the driver entry point (no link-time libcuda).
-bool make_tmap_bf16_2d(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer,
-                       uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer);
+// Encodes a 2-D TMA descriptor with 128-byte swizzling through the driver entry point
+// (no link-time libcuda).  inner/outer are extents in elements, row stride in bytes.
+bool make_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* ptr, uint64_t inner,
+                  uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer);
+
+inline bool make_tmap_bf16_2d(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer,
+                              uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer) {
+  return make_tmap_2d(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ptr, inner, outer, row_stride_bytes,
+                      box_inner, box_outer);
+}
 
 // C[M, N] = epi(A[M, K] . B[N, K]^T); A, B bf16 row-major (K contiguous).
 // Requires K % 64 == 0, N % 32 == 0, 16-byte aligned rows.
