@@ -315,6 +315,64 @@ def run_ours(args, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
+def run_single_kernel(args):
+    """Launch one kernel class `--launches` times at the workload's shapes through the per-kernel
+    entry points (small device footprint; used for profiler captures of one kernel)."""
+    import torch
+    from synth import get_workload
+    from decoder_only_forward_02_b300 import build
+    build.build()
+    from decoder_only_forward_02_b300 import binding as NB
+    ops = NB.ops
+    wl = get_workload(args.workload)
+    c = wl.model
+    M, C, H, Hkv, D, F, V = wl.M, c.n_embd, c.n_head, c.n_kv_head, c.head_dim, c.mlp_hidden, c.vocab_size
+    dev = torch.device("cuda", 0)
+    g = torch.Generator(device=dev).manual_seed(0)
+
+    def rnd(shape, scale=1.0, dtype=torch.bfloat16):
+        return (torch.randn(shape, generator=g, device=dev) * scale).to(dtype)
+
+    def unit(t):
+        return (t.float() / t.float().pow(2).mean(-1, keepdim=True).sqrt()).to(torch.bfloat16)
+
+    k = args.only_kernel
+    window = max(c.window_left) if args.window is None else args.window
+    if k == "qkv":
+        xn, w = rnd((M, C)), rnd(((H + 2 * Hkv) * D, C), 0.02)
+        rope = ops.rope_table(wl.T, D, c.rope_base, dev)
+        gate = torch.rand((M, Hkv), generator=g, device=dev)
+        ve, tok = rnd((V, Hkv * D), 0.02), torch.randint(0, V, (M,), generator=g, device=dev, dtype=torch.int32)
+        fn = lambda: ops.qkv(xn, w, wl.T, H, Hkv, D, rope, c.rms_eps, gate, ve, tok, V)
+    elif k == "attention":
+        q, kk, v = unit(rnd((M, H, D))).reshape(M, -1), unit(rnd((M, Hkv, D))).reshape(M, -1), rnd((M, Hkv * D))
+        fn = lambda: ops.attention(q, kk, v, wl.B, wl.T, H, Hkv, D, window)
+    elif k in ("oproj", "proj"):
+        K = H * D if k == "oproj" else F
+        a, w, x = rnd((M, K)), rnd((C, K), 0.02), rnd((M, C), 1.0, torch.float32)
+        fn = lambda: ops.gemm(a, w, "resid_f32", out=x, resid=x)
+    elif k == "fc":
+        a, w = rnd((M, C)), rnd((F, C), 0.02)
+        fn = lambda: ops.gemm(a, w, "relu2_bf16")
+    elif k == "lmhead":
+        a, w = rnd((M, C)), rnd((V, C), 0.02)
+        out = torch.empty((M, V), dtype=torch.float32, device=dev)
+        fn = lambda: ops.gemm(a, w, "softcap_f32", out=out, cap=c.softcap)
+    elif k == "rownorm":
+        x, x0, wg = rnd((M, C), 1.0, torch.float32), rnd((M, C), 1.0, torch.float32), rnd((Hkv, C), 0.02)
+        fn = lambda: ops.rownorm(x, x0, 1.0, 0.1, x, c.rms_eps, wg, C, 1.0, True)
+    elif k == "embed":
+        tok = torch.randint(0, V, (wl.B, wl.T), generator=g, device=dev, dtype=torch.int32)
+        wte, sg = rnd((V, C), 0.02), rnd((C,), 0.02)
+        fn = lambda: ops.embed_smear(tok, wte, sg, C)
+    else:
+        raise SystemExit(f"unknown kernel {k}")
+    for _ in range(args.launches):
+        fn()
+    torch.cuda.synchronize()
+    print(json.dumps({"kernel": k, "workload": wl.name, "launches": args.launches, "ok": True}))
+
+
 _HASH = None
 
 
@@ -347,7 +405,15 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-tokens", type=int, default=2048)
     ap.add_argument("--ref-tokens", type=int, default=512)
+    ap.add_argument("--only-kernel", default=None,
+                    help="launch one kernel class (qkv, attention, oproj, fc, proj, lmhead, rownorm, embed) "
+                         "at the workload's shapes, for profiler captures")
+    ap.add_argument("--launches", type=int, default=3)
+    ap.add_argument("--window", type=int, default=None)
     args = ap.parse_args()
+    if args.only_kernel:
+        run_single_kernel(args)
+        return
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
