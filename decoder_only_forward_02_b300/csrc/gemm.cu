@@ -3,13 +3,20 @@
 //   C[M, N] = epilogue(A[M, K] . B[N, K]^T),  A and B bf16, K contiguous (nn.Linear layout),
 //   fp32 accumulation in tensor memory.
 //
-// Roles (320 threads, one CTA per SM, grid = min(tiles, SMs), static round-robin tiles,
-// row-block index fastest so that concurrent CTAs share the same weight tile in L2):
-//   warp 0       TMA producer: 128x64 A box + 256x64 B box per stage, 128-byte swizzle,
-//                4-stage shared-memory ring guarded by full/empty mbarriers.
-//   warp 1       allocates 512 TMEM columns (two 128x256 fp32 accumulators) and issues
-//                tcgen05.mma 128x256x16 from one lane; tcgen05.commit frees each stage and
-//                publishes each finished accumulator.
+// CTA pairs (clusters of 2 on neighbouring SMs, one CTA per SM) compute 256x256 tiles with
+// the pair form of tcgen05.mma: each CTA holds 128 rows of A and 128 of the 256 rows of B
+// in its own shared memory and receives its 128 rows of the fp32 accumulator in its own
+// TMEM, so each SM stages 32 KB instead of 48 KB per 64-deep k-block and the tensor cores read
+// half of B from the peer.  Persistent grid: min(pair tiles, co-resident pairs); pair tiles
+// are taken round-robin with the row-block index fastest (concurrent pairs share a weight tile).
+// Roles (320 threads per CTA):
+//   warp 0       TMA producer (both CTAs): its A box (128x64) and B half (128x64) per stage,
+//                128-byte swizzle, 6-stage ring; both CTAs' copies complete on the leader
+//                CTA's full barrier, which the leader arms with the pair's byte count.
+//   warp 1       allocates 512 TMEM columns in both CTAs (two 128x256 fp32 accumulators);
+//                in the leader one lane issues tcgen05.mma (M=256, N=256, K=16) for the pair;
+//                pair commits free each stage in both CTAs and publish each finished
+//                accumulator to both CTAs' epilogues.
 //   warps 2..9   epilogue: two warpgroups, each owns 128 accumulator columns; every thread
 //                owns one output row (TMEM lane).  A warp reads its 32 rows x 128 columns with
 //                tcgen05.ld, releases the accumulator, applies the fused epilogue, writes
@@ -34,9 +41,13 @@
 namespace nc {
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int BM = 128;            // rows of A (and of D) held by each CTA of a pair
+constexpr int PAIR_M = 2 * BM;     // rows of one pair tile
+constexpr int BN = 256;            // columns of one pair tile
+constexpr int B_ROWS = BN / 2;     // rows of B (columns of D) loaded by each CTA
+constexpr int BK = 64, STAGES = 6;
 constexpr int A_BYTES = BM * BK * 2;
-constexpr int B_BYTES = BN * BK * 2;
+constexpr int B_BYTES = B_ROWS * BK * 2;
 constexpr int NUM_EPI_WARPS = 8;
 constexpr int THREADS = 64 + 32 * NUM_EPI_WARPS;
 constexpr uint32_t TMEM_COLS = 2 * BN;
@@ -118,11 +129,12 @@ struct OutMaps {
   CUtensorMap o0, o1, o2;   // output (EPI_*), or q / k / v (EPI_QKV)
 };
 
-// Release an accumulator buffer to the MMA warp (after this warp's last tcgen05.ld of it).
+// Release an accumulator buffer to the pair's MMA thread (after this warp's last tcgen05.ld
+// of it); `bar` is the leader CTA's barrier as a shared::cluster address.
 __device__ __forceinline__ void release_acc(int lane, uint32_t bar) {
   tc_fence_before();
   __syncwarp();
-  if (lane == 0) mbar_arrive(bar);
+  if (lane == 0) mbar_arrive_cluster(bar);
 }
 
 // Epilogue of one warp: rows [m0w, m0w + 32) (this thread: row m0w + lane), accumulator
@@ -302,7 +314,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   Ctrl* ctl = reinterpret_cast<Ctrl*>(smem + OFF_CTRL);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int num_m = (M + BM - 1) / BM, num_n = (N + BN - 1) / BN;
+  const uint32_t rank = cluster_ctarank();            // 0: pair leader (issues the MMAs)
+  const int pair = static_cast<int>(blockIdx.x) >> 1, npairs = static_cast<int>(gridDim.x) >> 1;
+  const int num_m = (M + PAIR_M - 1) / PAIR_M, num_n = (N + BN - 1) / BN;
   const int num_tiles = num_m * num_n, kblocks = K / BK;
   int* status = ep.status;
 
@@ -313,7 +327,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(smem_u32(&ctl->tfull[a]), 1);
-      mbar_init(smem_u32(&ctl->tempty[a]), NUM_EPI_WARPS);
+      mbar_init(smem_u32(&ctl->tempty[a]), 2 * NUM_EPI_WARPS);
     }
     mbar_init(smem_u32(&ctl->drain), 1);
     ctl->abort = 0;
@@ -324,11 +338,11 @@ __global__ void __launch_bounds__(THREADS, 1)
     tma_prefetch_desc(&tmB);
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(&ctl->tmem_base), TMEM_COLS);
-    tmem_relinquish();
+    tmem_alloc_pair(smem_u32(&ctl->tmem_base), TMEM_COLS);
+    tmem_relinquish_pair();
   }
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();   // barriers of both CTAs initialised, TMEM allocated
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
   volatile int* abort = &ctl->abort;
@@ -337,55 +351,58 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (lane == 0) {
       uint32_t it = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+      for (int tile = pair; tile < num_tiles && ok; tile += npairs) {
         const int mb = tile % num_m, nb = tile / num_m;
         for (int kb = 0; kb < kblocks; ++kb) {
           const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
-          if (!mbar_wait(smem_u32(&ctl->empty[s]), ph ^ 1, abort, status)) {
+          if (!mbar_wait_cluster(smem_u32(&ctl->empty[s]), ph ^ 1, abort, status)) {
             ok = false;
             break;
           }
-          const uint32_t fb = smem_u32(&ctl->full[s]);
-          mbar_arrive_expect_tx(fb, A_BYTES + B_BYTES);
-          tma_load_2d(sA + s * A_BYTES, &tmA, fb, kb * BK, mb * BM);
-          tma_load_2d(sB + s * B_BYTES, &tmB, fb, kb * BK, nb * BN);
+          const uint32_t fb = mapa_shared(smem_u32(&ctl->full[s]), 0);   // the leader's barrier
+          if (rank == 0) mbar_arrive_expect_tx(smem_u32(&ctl->full[s]), 2 * (A_BYTES + B_BYTES));
+          tma_load_2d_pair(sA + s * A_BYTES, &tmA, fb, kb * BK, mb * PAIR_M + static_cast<int>(rank) * BM);
+          tma_load_2d_pair(sB + s * B_BYTES, &tmB, fb, kb * BK, nb * BN + static_cast<int>(rank) * B_ROWS);
           ++it;
         }
       }
-      // Every issued load must land before the CTA may exit.
-      for (uint32_t j = (it > STAGES ? it - STAGES : 0); j < it; ++j)
-        mbar_wait(smem_u32(&ctl->full[j % STAGES]), (j / STAGES) & 1, nullptr, status);
+      // The leader's full barriers count both CTAs' copies: once its last phases completed,
+      // every copy issued by the pair has landed (the peer exits only after the final sync).
+      if (rank == 0) {
+        for (uint32_t j = (it > STAGES ? it - STAGES : 0); j < it; ++j)
+          mbar_wait_cluster(smem_u32(&ctl->full[j % STAGES]), (j / STAGES) & 1, nullptr, status);
+      }
     }
     __syncwarp();
   } else if (warp == 1) {
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
+    if (lane == 0 && rank == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(PAIR_M, BN);
       uint32_t it = 0, tc = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++tc) {
+      for (int tile = pair; tile < num_tiles && ok; tile += npairs, ++tc) {
         const uint32_t a = tc & 1, aph = (tc >> 1) & 1;
-        if (!mbar_wait(smem_u32(&ctl->tempty[a]), aph ^ 1, abort, status)) break;
+        if (!mbar_wait_cluster(smem_u32(&ctl->tempty[a]), aph ^ 1, abort, status)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem + a * BN;
         for (int kb = 0; kb < kblocks; ++kb) {
           const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
-          if (!mbar_wait(smem_u32(&ctl->full[s]), ph, abort, status)) {
+          if (!mbar_wait_cluster(smem_u32(&ctl->full[s]), ph, abort, status)) {
             ok = false;
             break;
           }
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
-            umma_bf16(d_tmem, sdesc_kmajor_sw128(sA + s * A_BYTES + kk * 32),
-                      sdesc_kmajor_sw128(sB + s * B_BYTES + kk * 32), idesc, (kb | kk) != 0 ? 1u : 0u);
+            umma_bf16_pair(d_tmem, sdesc_kmajor_sw128(sA + s * A_BYTES + kk * 32),
+                           sdesc_kmajor_sw128(sB + s * B_BYTES + kk * 32), idesc, (kb | kk) != 0 ? 1u : 0u);
           }
-          umma_commit(smem_u32(&ctl->empty[s]));
+          umma_commit_pair(smem_u32(&ctl->empty[s]), 0x3);
           ++it;
         }
         if (!ok) break;
-        umma_commit(smem_u32(&ctl->tfull[a]));
+        umma_commit_pair(smem_u32(&ctl->tfull[a]), 0x3);
       }
-      umma_commit(smem_u32(&ctl->drain));
+      umma_commit_pair(smem_u32(&ctl->drain), 0x1);
       mbar_wait(smem_u32(&ctl->drain), 0, nullptr, status);
     }
     __syncwarp();
@@ -396,25 +413,26 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint8_t* slab = smem + OFF_SLAB + ew * SLAB_BYTES;
     const uint32_t slab_s = smem_u32(slab);
     uint32_t tc = 0;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++tc) {
+    for (int tile = pair; tile < num_tiles; tile += npairs, ++tc) {
       const uint32_t a = tc & 1, aph = (tc >> 1) & 1;
-      const bool ok = mbar_wait(smem_u32(&ctl->tfull[a]), aph, abort, status);
+      const bool ok = mbar_wait_cluster(smem_u32(&ctl->tfull[a]), aph, abort, status);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
       const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + a * BN + group * 128;
       const int mb = tile % num_m, nb = tile / num_m;
-      epilogue_warp<KIND, D>(taddr, smem_u32(&ctl->tempty[a]), lane, mb * BM + quarter * 32, nb * BN + group * 128,
-                             M, N, ep, om, slab, slab_s);
+      epilogue_warp<KIND, D>(taddr, mapa_shared(smem_u32(&ctl->tempty[a]), 0), lane,
+                             mb * PAIR_M + static_cast<int>(rank) * BM + quarter * 32, nb * BN + group * 128, M, N,
+                             ep, om, slab, slab_s);
     }
     if (lane == 0) bulk_wait<0>();   // stores complete before the CTA exits
     __syncwarp();
   }
 
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();   // all MMAs done and all TMEM reads of both CTAs finished
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, TMEM_COLS);
+    tmem_dealloc_pair(tmem, TMEM_COLS);
   }
 }
 
@@ -423,14 +441,31 @@ cudaError_t launch_kind(const CUtensorMap& ta, const CUtensorMap& tb, const OutM
                         const GemmEpi& epi, int num_sms, cudaStream_t stream) {
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [] {
+  static int max_pairs = 0;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  std::call_once(once, [&] {
     attr_err = cudaFuncSetAttribute(gemm_tc_kernel<KIND, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (attr_err != cudaSuccess) return;
+    cudaLaunchConfig_t q = cfg;
+    q.gridDim = dim3(2 * (num_sms / 2));
+    if (cudaOccupancyMaxActiveClusters(&max_pairs, gemm_tc_kernel<KIND, D>, &q) != cudaSuccess || max_pairs < 1)
+      max_pairs = num_sms / 2;
   });
   if (attr_err != cudaSuccess) return attr_err;
-  const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
-  const int grid = tiles < num_sms ? tiles : num_sms;
-  gemm_tc_kernel<KIND, D><<<grid, THREADS, SMEM_BYTES, stream>>>(ta, tb, om, M, N, K, epi);
-  return cudaGetLastError();
+  const int tiles = ((M + PAIR_M - 1) / PAIR_M) * ((N + BN - 1) / BN);
+  const int pairs = tiles < max_pairs ? tiles : max_pairs;
+  cfg.gridDim = dim3(2 * pairs);
+  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<KIND, D>, ta, tb, om, M, N, K, epi);
 }
 
 }  // namespace
@@ -440,7 +475,7 @@ cudaError_t launch_gemm(const bf16* A, const bf16* B, int M, int N, int K, const
   if (M <= 0 || N <= 0 || K <= 0 || K % BK != 0 || N % 32 != 0) return cudaErrorInvalidValue;
   CUtensorMap ta, tb;
   if (!make_tmap_bf16_2d(&ta, A, K, M, static_cast<uint64_t>(K) * 2, BK, BM)) return cudaErrorInvalidValue;
-  if (!make_tmap_bf16_2d(&tb, B, K, N, static_cast<uint64_t>(K) * 2, BK, BN)) return cudaErrorInvalidValue;
+  if (!make_tmap_bf16_2d(&tb, B, K, N, static_cast<uint64_t>(K) * 2, BK, B_ROWS)) return cudaErrorInvalidValue;
   OutMaps om;
   const uint64_t Mu = static_cast<uint64_t>(M);
   bool ok = true;
