@@ -57,10 +57,8 @@ def kernel_work(cfg, B: int, T: int):
         "fc_relu2": ("tensor", 2.0 * M * C * F),
         "proj_residual": ("tensor", 2.0 * M * F * C),
         "lmhead_softcap": ("tensor", 2.0 * M * C * V),
-        # average over the 2L+1 launches: block start reads x, x0 and writes x, xn (14 B/elt);
-        # pre-MLP reads x, writes xn (6 B/elt); final reads x, x_mid, writes xn (10 B/elt)
-        "rownorm": ("hbm", M * C * (14.0 * L + 6.0 * L + 10.0) / (2 * L + 1)),
-        "embed_smear": ("hbm", M * C * (2 + 4) + M * 4),
+        # wte row gather (bf16), x0 and x written (fp32), bf16 copy, token ids
+        "embed_smear": ("hbm", M * C * (2 + 4 + 4 + 2) + M * 4),
     }
 
 
@@ -85,7 +83,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
 
@@ -203,7 +201,7 @@ def run_ours(args, rank, world, local_rank):
 
     clocks = ClockSampler(local_rank)
     clocks.start()
-    model.timing(True)
+    time.sleep(0.3)   # let the sampler start before the timed region
     barrier()
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
@@ -215,11 +213,17 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     barrier()
     ms = e0.elapsed_time(e1)
-    model.timing(False)
     clk = clocks.stop()
-    ktimes = model.timing_read()
     if model.status() != 0:
         raise RuntimeError("device status set during the timed region")
+    # Per-kernel times: the same steps again, with a CUDA-event pair recorded around every
+    # launch on the launching stream (kept out of the region that gives `value`).
+    model.timing(True)
+    for _ in range(args.steps):
+        model.forward(tok, out=logits)
+    torch.cuda.synchronize()
+    model.timing(False)
+    ktimes = model.timing_read()
 
     t_max = torch.tensor([ms], dtype=torch.float64, device=dev)
     if world > 1:
@@ -339,28 +343,32 @@ def run_single_kernel(args):
     k = args.only_kernel
     window = max(c.window_left) if args.window is None else args.window
     if k == "qkv":
-        xn, w = rnd((M, C)), rnd(((H + 2 * Hkv) * D, C), 0.02)
+        xb, w = rnd((M, C)), rnd(((H + 2 * Hkv) * D, C), 0.02)
+        ssp = torch.rand((M, C // 128), generator=g, device=dev) * 100
+        gp = torch.randn((M, Hkv, C // 128), generator=g, device=dev)
         rope = ops.rope_table(wl.T, D, c.rope_base, dev)
-        gate = torch.rand((M, Hkv), generator=g, device=dev)
         ve, tok = rnd((V, Hkv * D), 0.02), torch.randint(0, V, (M,), generator=g, device=dev, dtype=torch.int32)
-        fn = lambda: ops.qkv(xn, w, wl.T, H, Hkv, D, rope, c.rms_eps, gate, ve, tok, V)
+        fn = lambda: ops.qkv(xb, w, wl.T, H, Hkv, D, rope, c.rms_eps, ssp, gp, 1.0, ve, tok, V)
     elif k == "attention":
         q, kk, v = unit(rnd((M, H, D))).reshape(M, -1), unit(rnd((M, Hkv, D))).reshape(M, -1), rnd((M, Hkv * D))
         fn = lambda: ops.attention(q, kk, v, wl.B, wl.T, H, Hkv, D, window)
     elif k in ("oproj", "proj"):
         K = H * D if k == "oproj" else F
-        a, w, x = rnd((M, K)), rnd((C, K), 0.02), rnd((M, C), 1.0, torch.float32)
-        fn = lambda: ops.gemm(a, w, "resid_f32", out=x, resid=x)
+        a, w, x, x0 = rnd((M, K)), rnd((C, K), 0.02), rnd((M, C), 1.0, torch.float32), rnd((M, C), 1.0, torch.float32)
+        wg = rnd((Hkv, C), 0.02)
+        if k == "oproj":
+            fn = lambda: ops.gemm_residual(a, w, x, x_out=x)
+        else:   # the MLP down projection with the next block's mix and value-embedding gate partials
+            fn = lambda: ops.gemm_residual(a, w, x, 0.9, 0.1, x0, x, None, wg, C)
     elif k == "fc":
         a, w = rnd((M, C)), rnd((F, C), 0.02)
-        fn = lambda: ops.gemm(a, w, "relu2_bf16")
+        ssp = torch.rand((M, C // 128), generator=g, device=dev) * 100
+        fn = lambda: ops.gemm(a, w, "relu2_bf16", ssp=ssp, C=C)
     elif k == "lmhead":
         a, w = rnd((M, C)), rnd((V, C), 0.02)
+        ssp = torch.rand((M, C // 128), generator=g, device=dev) * 100
         out = torch.empty((M, V), dtype=torch.float32, device=dev)
-        fn = lambda: ops.gemm(a, w, "softcap_f32", out=out, cap=c.softcap)
-    elif k == "rownorm":
-        x, x0, wg = rnd((M, C), 1.0, torch.float32), rnd((M, C), 1.0, torch.float32), rnd((Hkv, C), 0.02)
-        fn = lambda: ops.rownorm(x, x0, 1.0, 0.1, x, c.rms_eps, wg, C, 1.0, True)
+        fn = lambda: ops.gemm(a, w, "softcap_f32", out=out, ssp=ssp, C=C, cap=c.softcap)
     elif k == "embed":
         tok = torch.randint(0, V, (wl.B, wl.T), generator=g, device=dev, dtype=torch.int32)
         wte, sg = rnd((V, C), 0.02), rnd((C,), 0.02)
@@ -396,8 +404,8 @@ def _weight_bytes(w):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default="d12")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -406,7 +414,7 @@ def main():
     ap.add_argument("--cpu-tokens", type=int, default=2048)
     ap.add_argument("--ref-tokens", type=int, default=512)
     ap.add_argument("--only-kernel", default=None,
-                    help="launch one kernel class (qkv, attention, oproj, fc, proj, lmhead, rownorm, embed) "
+                    help="launch one kernel class (qkv, attention, oproj, fc, proj, lmhead, embed) "
                          "at the workload's shapes, for profiler captures")
     ap.add_argument("--launches", type=int, default=3)
     ap.add_argument("--window", type=int, default=None)

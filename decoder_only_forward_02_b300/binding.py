@@ -18,8 +18,9 @@ LIB_PATH = os.path.join(_PKG, "libnc.so")
 NC_OK = 0
 STATUS_NAMES = {0: "NC_OK", 1: "NC_ERR_INVALID_ARG", 2: "NC_ERR_UNSUPPORTED", 3: "NC_ERR_WORKSPACE",
                 4: "NC_ERR_CUDA", 5: "NC_ERR_DEVICE_TIMEOUT", 6: "NC_ERR_TOKEN_RANGE"}
-KERNEL_CLASSES = ["embed_smear", "rownorm", "qkv_rope_qknorm_ve", "attention", "oproj_residual",
-                  "fc_relu2", "proj_residual", "lmhead_softcap"]
+KERNEL_CLASSES = ["embed_smear", "qkv_rope_qknorm_ve", "attention", "oproj_residual", "fc_relu2",
+                  "proj_residual", "lmhead_softcap"]
+SS_GROUP = 128   # columns per partial sum of squares
 
 c_int_p = ctypes.POINTER(ctypes.c_int)
 c_void_pp = ctypes.POINTER(ctypes.c_void_p)
@@ -62,6 +63,7 @@ _SIGS = {
                                        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "nc_get_status": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
     "nc_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "nc_last_cuda_error": (ctypes.c_char_p, []),
     "nc_model_destroy": (None, [ctypes.c_void_p]),
     "nc_timing_enable": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int]),
     "nc_timing_read": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.POINTER(ctypes.c_double),
@@ -70,57 +72,74 @@ _SIGS = {
     "nc_forward_launch_count": (ctypes.c_int, [ctypes.c_void_p]),
     # per-kernel entry points (include/nc_ops.h)
     "nc_op_gemm": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-                                  ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_float,
-                                  ctypes.c_void_p, ctypes.c_void_p]),
+                                  ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int,
+                                  ctypes.c_float, ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p]),
+    "nc_op_gemm_residual": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+                                           ctypes.c_int, ctypes.c_void_p, ctypes.c_float, ctypes.c_float]
+                            + [ctypes.c_void_p] * 6 + [ctypes.c_int, ctypes.c_int] + [ctypes.c_void_p] * 3),
     "nc_op_qkv": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p] + [ctypes.c_int] * 6 +
-                  [ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
-                   ctypes.c_int] + [ctypes.c_void_p] * 5),
+                  [ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_float,
+                   ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int] + [ctypes.c_void_p] * 5),
     "nc_op_rope_table": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_float,
                                         ctypes.c_void_p]),
     "nc_op_attention": (ctypes.c_int, [ctypes.c_void_p] * 3 + [ctypes.c_int] * 6 +
                         [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
-    "nc_op_rownorm": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_float, ctypes.c_float,
-                                     ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_float,
-                                     ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_float, ctypes.c_void_p,
-                                     ctypes.c_void_p]),
     "nc_op_embed_smear": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
                                          ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
-                                         ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
+                                         ctypes.c_float, ctypes.c_float] + [ctypes.c_void_p] * 5 +
+                          [ctypes.c_int, ctypes.c_int] + [ctypes.c_void_p] * 3),
 }
 
-EPI = {"bf16": 0, "resid_f32": 1, "relu2_bf16": 2, "softcap_f32": 3}
+EPI = {"bf16": 0, "relu2_bf16": 2, "softcap_f32": 3}
 
 
 class ops:
     """Per-kernel entry points; tensors are CUDA tensors, launches go on the current stream."""
 
     @staticmethod
-    def gemm(A, B, epi="bf16", out=None, resid=None, cap=15.0, status=None):
+    def gemm(A, B, epi="bf16", out=None, ssp=None, C=0, eps=1e-6, cap=15.0, status=None):
         M, K = A.shape
         N = B.shape[0]
         if out is None:
             dt = torch.bfloat16 if epi in ("bf16", "relu2_bf16") else torch.float32
             out = torch.empty((M, N), dtype=dt, device=A.device)
         check(lib().nc_op_gemm(A.data_ptr(), B.data_ptr(), M, N, K, EPI[epi], out.data_ptr(), out.shape[1],
-                               _ptr(resid), cap, _ptr(status), _stream_handle(None)), "nc_op_gemm")
+                               _ptr(ssp), C, eps, cap, _ptr(status), _stream_handle(None)), "nc_op_gemm")
         return out
 
     @staticmethod
+    def gemm_residual(A, B, resid, a=1.0, b=0.0, Y=None, x_out=None, xm_out=None, wg=None, c_g=0, status=None):
+        """Returns (xb, ssp, gp); x_out / xm_out are written in place when given."""
+        M, K = A.shape
+        N = B.shape[0]
+        dev = A.device
+        xb = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        ssp = torch.empty((M, N // SS_GROUP), dtype=torch.float32, device=dev)
+        Hkv = 0 if wg is None else wg.shape[0]
+        gp = None if wg is None else torch.empty((M, Hkv, N // SS_GROUP), dtype=torch.float32, device=dev)
+        check(lib().nc_op_gemm_residual(A.data_ptr(), B.data_ptr(), M, N, K, resid.data_ptr(), a, b, _ptr(Y),
+                                        _ptr(x_out), _ptr(xm_out), xb.data_ptr(), ssp.data_ptr(), _ptr(wg), Hkv,
+                                        c_g, _ptr(gp), _ptr(status), _stream_handle(None)), "nc_op_gemm_residual")
+        return xb, ssp, gp
+
+    @staticmethod
     def rope_table(T, D, base, device):
-        t = torch.empty((T, D // 2, 2), dtype=torch.float32, device=device)
+        """[D/2, T, 2] fp32 (cos, sin), position fastest."""
+        t = torch.empty((D // 2, T, 2), dtype=torch.float32, device=device)
         check(lib().nc_op_rope_table(t.data_ptr(), T, D, base, _stream_handle(None)), "nc_op_rope_table")
         return t
 
     @staticmethod
-    def qkv(xn, wqkv, T, H, Hkv, D, rope, eps, gate=None, ve=None, tokens=None, V=0, status=None):
-        M, C = xn.shape
-        dev = xn.device
+    def qkv(xb, wqkv, T, H, Hkv, D, rope, eps, ssp, gp=None, gate_scale=1.0, ve=None, tokens=None, V=0,
+            status=None):
+        M, C = xb.shape
+        dev = xb.device
         q = torch.empty((M, H * D), dtype=torch.bfloat16, device=dev)
         k = torch.empty((M, Hkv * D), dtype=torch.bfloat16, device=dev)
         v = torch.empty((M, Hkv * D), dtype=torch.bfloat16, device=dev)
-        check(lib().nc_op_qkv(xn.data_ptr(), wqkv.data_ptr(), M, T, C, H, Hkv, D, rope.data_ptr(), eps, _ptr(gate),
-                              _ptr(ve), _ptr(tokens), V, q.data_ptr(), k.data_ptr(), v.data_ptr(), _ptr(status),
-                              _stream_handle(None)), "nc_op_qkv")
+        check(lib().nc_op_qkv(xb.data_ptr(), wqkv.data_ptr(), M, T, C, H, Hkv, D, rope.data_ptr(), rope.shape[1],
+                              eps, ssp.data_ptr(), _ptr(gp), gate_scale, _ptr(ve), _ptr(tokens), V, q.data_ptr(),
+                              k.data_ptr(), v.data_ptr(), _ptr(status), _stream_handle(None)), "nc_op_qkv")
         return q, k, v
 
     @staticmethod
@@ -131,27 +150,25 @@ class ops:
         return y
 
     @staticmethod
-    def rownorm(x, y=None, a=1.0, b=0.0, x_out=None, eps=1e-6, wg=None, c_g=0, gate_scale=1.0, want_gate=False):
-        M, C = x.shape
-        xn = torch.empty((M, C), dtype=torch.bfloat16, device=x.device)
-        gate = None
-        Hkv = 0
-        if want_gate:
-            Hkv = wg.shape[0]
-            gate = torch.empty((M, Hkv), dtype=torch.float32, device=x.device)
-        check(lib().nc_op_rownorm(x.data_ptr(), _ptr(y), a, b, _ptr(x_out), xn.data_ptr(), M, C, eps, _ptr(wg), Hkv,
-                                  c_g, gate_scale, _ptr(gate), _stream_handle(None)), "nc_op_rownorm")
-        return xn, gate
-
-    @staticmethod
-    def embed_smear(tokens, wte, smear_gate=None, c_s=0, embed_norm=False, eps=1e-6, status=None):
+    def embed_smear(tokens, wte, smear_gate=None, c_s=0, embed_norm=False, eps=1e-6, a=1.0, wg=None, c_g=0,
+                    status=None):
+        """Returns (x0, x, xb, ssp, gp)."""
         B, T = tokens.shape
         V, C = wte.shape
-        x0 = torch.empty((B * T, C), dtype=torch.float32, device=wte.device)
-        check(lib().nc_op_embed_smear(tokens.data_ptr(), B, T, wte.data_ptr(), V, C, _ptr(smear_gate),
-                                      c_s or C, int(embed_norm), eps, x0.data_ptr(), _ptr(status),
+        dev = wte.device
+        M = B * T
+        x0 = torch.empty((M, C), dtype=torch.float32, device=dev)
+        x = torch.empty((M, C), dtype=torch.float32, device=dev)
+        xb = torch.empty((M, C), dtype=torch.bfloat16, device=dev)
+        ssp = torch.empty((M, C // SS_GROUP), dtype=torch.float32, device=dev)
+        Hkv = 0 if wg is None else wg.shape[0]
+        gp = None if wg is None else torch.empty((M, Hkv, C // SS_GROUP), dtype=torch.float32, device=dev)
+        check(lib().nc_op_embed_smear(tokens.data_ptr(), B, T, wte.data_ptr(), V, C, _ptr(smear_gate), c_s or C,
+                                      int(embed_norm), eps, a, x0.data_ptr(), x.data_ptr(), xb.data_ptr(),
+                                      ssp.data_ptr(), _ptr(wg), Hkv, c_g or C, _ptr(gp), _ptr(status),
                                       _stream_handle(None)), "nc_op_embed_smear")
-        return x0
+        return x0, x, xb, ssp, gp
+
 
 _lib: Optional[ctypes.CDLL] = None
 
@@ -174,7 +191,10 @@ def lib() -> ctypes.CDLL:
 class NcError(RuntimeError):
     def __init__(self, code: int, what: str):
         self.code = code
-        super().__init__(f"{what}: {STATUS_NAMES.get(code, code)} ({lib().nc_status_string(code).decode()})")
+        msg = f"{what}: {STATUS_NAMES.get(code, code)} ({lib().nc_status_string(code).decode()})"
+        if code == 4:
+            msg += f" [{lib().nc_last_cuda_error().decode()}]"
+        super().__init__(msg)
 
 
 def check(code: int, what: str) -> None:

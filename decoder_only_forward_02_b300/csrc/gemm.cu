@@ -8,30 +8,37 @@
 // in its own shared memory and receives its 128 rows of the fp32 accumulator in its own
 // TMEM, so each SM stages 32 KB instead of 48 KB per 64-deep k-block and the tensor cores read
 // half of B from the peer.  Persistent grid: min(pair tiles, co-resident pairs); pair tiles
-// are taken round-robin with the row-block index fastest (concurrent pairs share a weight tile).
+// are taken round-robin with the column-block index fastest, so the pairs running at the same
+// time share one row block of A (read from DRAM once) and the weights stay in L2.
 // Roles (320 threads per CTA):
 //   warp 0       TMA producer (both CTAs): its A box (128x64) and B half (128x64) per stage,
-//                128-byte swizzle, 6-stage ring; both CTAs' copies complete on the leader
+//                128-byte swizzle, 5-stage ring; both CTAs' copies complete on the leader
 //                CTA's full barrier, which the leader arms with the pair's byte count.
 //   warp 1       allocates 512 TMEM columns in both CTAs (two 128x256 fp32 accumulators);
 //                in the leader one lane issues tcgen05.mma (M=256, N=256, K=16) for the pair;
 //                pair commits free each stage in both CTAs and publish each finished
 //                accumulator to both CTAs' epilogues.
 //   warps 2..9   epilogue: two warpgroups, each owns 128 accumulator columns; every thread
-//                owns one output row (TMEM lane).  A warp reads its 32 rows x 128 columns with
-//                tcgen05.ld, releases the accumulator, applies the fused epilogue, writes
-//                32-row x 128-byte chunks into its own 128-byte-swizzled shared slab and
-//                stores each chunk with one TMA bulk-tensor store.
+//                owns one output row (TMEM lane).  A warp reads its 32 rows with tcgen05.ld,
+//                applies the fused epilogue, writes 32-row x 128-byte boxes into one of its two
+//                128-byte-swizzled shared buffers and stores each box with one TMA store.
 // The double-buffered accumulator lets the epilogue of tile i overlap the MMAs of tile i+1.
 //
-// Fused epilogues (what each computes is defined on "Nanochat在nanoGPT之上的新增功能",
-// section 1 feature table and notes):
-//   EPI_RESID_F32    residual add of an output projection (attention c_proj, MLP c_proj);
-//                    the residual chunk is read with row-coalesced loads through the slab
-//   EPI_RELU2_BF16   squared ReLU of the MLP up projection
-//   EPI_SOFTCAP_F32  tanh soft-cap (+-cap) of the untied lm_head logits (hardware tanh)
-//   EPI_QKV          split of the packed q|k|v projection; RoPE then per-head RMSNorm of q
-//                    and k; on value-embedding layers v += gate * ve[token]
+// Fused epilogues (the operations are those of "Nanochat在nanoGPT之上的新增功能", section 1
+// feature table and notes; RMSNorm has no weight, so norm(x) W^T = diag(1/rms(x)) (x W^T) and
+// the normalisation of a GEMM's input becomes a per-row scale of its accumulator):
+//   EPI_RESID        residual update of an output projection (attention c_proj, MLP c_proj):
+//                    x += acc, then optionally the backout cache, the next block's
+//                    resid_lambdas/x0_lambdas mix or the final backout subtraction; writes the
+//                    stream (fp32), its bf16 copy (the next GEMM's A operand), per-row partial
+//                    sums of squares over 128-column groups (the next RMSNorm) and, before a
+//                    value-embedding layer, partial dot products with its gate weights
+//   EPI_RELU2_BF16   squared ReLU of the MLP up projection, input RMSNorm as a row scale
+//   EPI_SOFTCAP_F32  tanh soft-cap (+-cap) of the untied lm_head logits, final RMSNorm as a row
+//                    scale (hardware tanh)
+//   EPI_QKV          split of the packed q|k|v projection, input RMSNorm as a row scale; RoPE
+//                    then per-head RMSNorm of q and k; on value-embedding layers
+//                    v += gate * ve[token] with gate = scale * sigmoid(rs * (x . w_gate))
 //   EPI_BF16         plain store (used by tests of the mainloop)
 #include "internal.h"
 #include "ptx.cuh"
@@ -45,13 +52,14 @@ constexpr int BM = 128;            // rows of A (and of D) held by each CTA of a
 constexpr int PAIR_M = 2 * BM;     // rows of one pair tile
 constexpr int BN = 256;            // columns of one pair tile
 constexpr int B_ROWS = BN / 2;     // rows of B (columns of D) loaded by each CTA
-constexpr int BK = 64, STAGES = 6;
+constexpr int BK = 64, STAGES = 5;
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = B_ROWS * BK * 2;
 constexpr int NUM_EPI_WARPS = 8;
 constexpr int THREADS = 64 + 32 * NUM_EPI_WARPS;
 constexpr uint32_t TMEM_COLS = 2 * BN;
-constexpr int SLAB_BYTES = 32 * 128;   // per epilogue warp: 32 rows x 128 B
+constexpr int SLAB_BUF = 32 * 128;       // one staging buffer: 32 rows x 128 B
+constexpr int SLAB_BYTES = 2 * SLAB_BUF; // two per epilogue warp, used alternately
 
 struct __align__(8) Ctrl {
   uint64_t full[STAGES];
@@ -67,66 +75,104 @@ constexpr int OFF_SLAB = STAGES * (A_BYTES + B_BYTES);
 constexpr int OFF_CTRL = OFF_SLAB + NUM_EPI_WARPS * SLAB_BYTES;
 constexpr int SMEM_BYTES = 1024 + OFF_CTRL + static_cast<int>(sizeof(Ctrl));
 
-// ---------------------------------------------------------------- slab helpers
-// A slab holds a [32 rows][128 B] box in the TMA 128-byte swizzle: 16-byte chunk c of row r
-// sits at chunk position c ^ (r % 8).
+// ---------------------------------------------------------------- staging slabs
+// A buffer holds a [32 rows][128 B] box in the TMA 128-byte swizzle: 16-byte chunk c of row r
+// sits at chunk position c ^ (r % 8).  Each epilogue warp owns two buffers and alternates
+// between them, one per TMA store, so a store can be in flight while the next is staged.
 
-__device__ __forceinline__ uint4* slab_chunk(uint8_t* slab, int r, int c) {
-  return reinterpret_cast<uint4*>(slab + r * 128 + ((c ^ (r & 7)) << 4));
+__device__ __forceinline__ uint4* slab_chunk(uint8_t* buf, int r, int c) {
+  return reinterpret_cast<uint4*>(buf + r * 128 + ((c ^ (r & 7)) << 4));
 }
 
-// Before overwriting the slab: the previous TMA store must have finished reading it.
-__device__ __forceinline__ void slab_acquire(int lane) {
-  if (lane == 0) bulk_wait_read<0>();
-  __syncwarp();
-}
+struct Slab {
+  uint8_t* base;
+  uint32_t base_s;
+  uint32_t n;   // stores issued so far (warp-uniform)
 
-// Publish the slab to the async proxy and store it as box (x, y) of `map`.
-__device__ __forceinline__ void slab_store(uint32_t slab, const CUtensorMap* map, int x, int y, int lane) {
-  fence_proxy_async_smem();
-  __syncwarp();
-  if (lane == 0) {
-    tma_store_2d(map, slab, x, y);
-    bulk_commit();
+  __device__ __forceinline__ uint8_t* buf() const { return base + (n & 1u) * SLAB_BUF; }
+  // Before writing the current buffer: the store issued from it two stores ago must have
+  // finished reading it (the most recent store, from the other buffer, may still run).
+  __device__ __forceinline__ void acquire(int lane) const {
+    if (lane == 0) bulk_wait_read<1>();
+    __syncwarp();
   }
-}
-
-// Row `lane` of the slab <- 8 x 16 B.
-__device__ __forceinline__ void slab_put_row(uint8_t* slab, int lane, const uint4 (&x)[8]) {
+  // Publish the current buffer to the async proxy and store it as box (x, y) of `map`.
+  __device__ __forceinline__ void store(const CUtensorMap* map, int x, int y, int lane) {
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(map, base_s + (n & 1u) * SLAB_BUF, x, y);
+      bulk_commit();
+    }
+    ++n;
+  }
+  __device__ __forceinline__ void store_hint(const CUtensorMap* map, int x, int y, int lane, uint64_t policy) {
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d_hint(map, base_s + (n & 1u) * SLAB_BUF, x, y, policy);
+      bulk_commit();
+    }
+    ++n;
+  }
+  // Row `lane` of the current buffer <- 8 x 16 B.
+  __device__ __forceinline__ void put_row(int lane, const uint4 (&x)[8]) const {
 #pragma unroll
-  for (int c = 0; c < 8; ++c) *slab_chunk(slab, lane, c) = x[c];
+    for (int c = 0; c < 8; ++c) *slab_chunk(buf(), lane, c) = x[c];
+  }
+  __device__ __forceinline__ void put_row_f32(int lane, const float (&x)[32]) const {
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+      *reinterpret_cast<float4*>(slab_chunk(buf(), lane, c)) = make_float4(x[4 * c], x[4 * c + 1], x[4 * c + 2], x[4 * c + 3]);
+  }
+  // Transpose a [32 rows][32 fp32] chunk loaded row-coalesced (load k of lane l holds row
+  // 4k + l/8, columns 4(l%8)..+3) into row `lane` of this thread.
+  __device__ __forceinline__ void transpose_f32(int lane, const float4 (&v)[8], float (&row)[32]) const {
+    __syncwarp();
+#pragma unroll
+    for (int k = 0; k < 8; ++k) *reinterpret_cast<float4*>(slab_chunk(buf(), k * 4 + (lane >> 3), lane & 7)) = v[k];
+    __syncwarp();
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const float4 t = *reinterpret_cast<const float4*>(slab_chunk(buf(), lane, c));
+      row[4 * c] = t.x;
+      row[4 * c + 1] = t.y;
+      row[4 * c + 2] = t.z;
+      row[4 * c + 3] = t.w;
+    }
+    __syncwarp();
+  }
+};
+
+// Row-coalesced load of the [32 rows][32 fp32] chunk at (m0w, c0) of a row-major matrix.
+__device__ __forceinline__ void load_chunk_f32(const float* p, int ld, int m0w, int c0, int M, int lane,
+                                               float4 (&v)[8]) {
+  const int rsub = lane >> 3, csub = (lane & 7) * 4;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const int gm = m0w + k * 4 + rsub;
+    v[k] = gm < M ? *reinterpret_cast<const float4*>(p + static_cast<size_t>(gm) * ld + c0 + csub)
+                  : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
 }
 
 __device__ __forceinline__ uint4 pack8_bf16(const float* a) {
   return make_uint4(pack_bf16(a[0], a[1]), pack_bf16(a[2], a[3]), pack_bf16(a[4], a[5]), pack_bf16(a[6], a[7]));
 }
 
-// Rotate pairs (d, d + D/2) by the position's angles, then RMS-normalise over the head.
-template <int D>
-__device__ __forceinline__ void rope_rmsnorm(float* x, const float2* rope_row, float eps) {
-  const float4* rp = reinterpret_cast<const float4*>(rope_row);
-#pragma unroll
-  for (int d2 = 0; d2 < D / 4; ++d2) {
-    const float4 cs = __ldg(rp + d2);
-    const int d = 2 * d2;
-    float x1 = x[d], x2 = x[d + D / 2];
-    x[d] = x1 * cs.x + x2 * cs.y;
-    x[d + D / 2] = -x1 * cs.y + x2 * cs.x;
-    x1 = x[d + 1];
-    x2 = x[d + 1 + D / 2];
-    x[d + 1] = x1 * cs.z + x2 * cs.w;
-    x[d + 1 + D / 2] = -x1 * cs.w + x2 * cs.z;
-  }
+// 1 / rms of row m from its partial sums of squares (1 when no partials are given).
+__device__ __forceinline__ float row_scale(const GemmEpi& ep, int m, int M) {
+  if (ep.ssp_in == nullptr || m >= M) return 1.f;
+  const float* p = ep.ssp_in + static_cast<size_t>(m) * ep.ncg;
   float ss = 0.f;
-#pragma unroll
-  for (int d = 0; d < D; ++d) ss = fmaf(x[d], x[d], ss);
-  const float r = rsqrtf(ss * (1.0f / D) + eps);
-#pragma unroll
-  for (int d = 0; d < D; ++d) x[d] *= r;
+  for (int g = 0; g < ep.ncg; ++g) ss += p[g];
+  return rsqrtf(ss * ep.inv_ncols + ep.eps);
 }
 
+__device__ __forceinline__ float sigmoid_fast(float z) { return 1.0f / (1.0f + __expf(-z)); }
+
 struct OutMaps {
-  CUtensorMap o0, o1, o2;   // output (EPI_*), or q / k / v (EPI_QKV)
+  CUtensorMap o0, o1, o2;   // EPI_RESID: x_out, xm_out, xb;  EPI_QKV: q, k, v;  else: out
 };
 
 // Release an accumulator buffer to the pair's MMA thread (after this warp's last tcgen05.ld
@@ -137,175 +183,339 @@ __device__ __forceinline__ void release_acc(int lane, uint32_t bar) {
   if (lane == 0) mbar_arrive_cluster(bar);
 }
 
-// Epilogue of one warp: rows [m0w, m0w + 32) (this thread: row m0w + lane), accumulator
-// columns [n0, n0 + 128) at TMEM address taddr (lane quarter already applied).
+// ---------------------------------------------------------------- per-tile prologue
+// Row data an epilogue needs that does not depend on the accumulator: loaded (and the
+// epilogue's global inputs prefetched into L2) before the warp waits for the tile's MMAs, so
+// those latencies overlap the mainloop instead of the epilogue.
+struct EpiPre {
+  float rs = 1.f;     // input RMSNorm row scale
+  float g[2] = {0.f, 0.f};   // value-embedding gate per head of the column group (EPI_QKV)
+  int tok = -1;       // token id of the row when a gate applies, else -1
+};
+
 template <int KIND, int D>
-__device__ __forceinline__ void epilogue_warp(uint32_t taddr, uint32_t tempty, int lane, int m0w, int n0, int M,
-                                              int N, const GemmEpi& ep, const OutMaps& om, uint8_t* slab,
-                                              uint32_t slab_s) {
+__device__ __forceinline__ EpiPre epi_pre(int lane, int m0w, int n0, int M, int N, const GemmEpi& ep) {
+  EpiPre p;
   const int m = m0w + lane;
-  if constexpr (KIND == EPI_RESID_F32 || KIND == EPI_SOFTCAP_F32) {
-#pragma unroll 1
-    for (int ch = 0; ch < 4; ++ch) {
-      const int c0 = n0 + ch * 32;
-      const bool live = c0 < N;   // warp-uniform (N % 32 == 0)
-      uint32_t r[32];
-      tmem_ld32(taddr + ch * 32, r);
-      float4 rv[8];
-      const int rsub = lane >> 3, csub = (lane & 7) * 4;
-      if constexpr (KIND == EPI_RESID_F32) {
-        // residual chunk [32 rows][32 cols]: each load instruction covers 4 whole rows
+  if (n0 >= N || m >= M) return p;
+  if constexpr (KIND == EPI_RESID) {
+    const size_t off = static_cast<size_t>(m) * N + n0;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const int gm = m0w + k * 4 + rsub;
-          rv[k] = (live && gm < M)
-                      ? *reinterpret_cast<const float4*>(ep.resid + static_cast<size_t>(gm) * ep.ldr + c0 + csub)
-                      : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-      }
-      tmem_ld_wait(r);
-      if (ch == 3) release_acc(lane, tempty);
-      if (!live) continue;
-      slab_acquire(lane);
-      if constexpr (KIND == EPI_RESID_F32) {
-#pragma unroll
-        for (int k = 0; k < 8; ++k) *reinterpret_cast<float4*>(slab_chunk(slab, k * 4 + rsub, lane & 7)) = rv[k];
-        __syncwarp();
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          float4* p = reinterpret_cast<float4*>(slab_chunk(slab, lane, c));
-          float4 x = *p;
-          x.x += __uint_as_float(r[c * 4 + 0]);
-          x.y += __uint_as_float(r[c * 4 + 1]);
-          x.z += __uint_as_float(r[c * 4 + 2]);
-          x.w += __uint_as_float(r[c * 4 + 3]);
-          *p = x;
-        }
-      } else {
-        const float cap = ep.cap, inv = 1.0f / ep.cap;
-        uint4 o[8];
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          o[c] = make_uint4(__float_as_uint(cap * tanh_approx(__uint_as_float(r[c * 4 + 0]) * inv)),
-                            __float_as_uint(cap * tanh_approx(__uint_as_float(r[c * 4 + 1]) * inv)),
-                            __float_as_uint(cap * tanh_approx(__uint_as_float(r[c * 4 + 2]) * inv)),
-                            __float_as_uint(cap * tanh_approx(__uint_as_float(r[c * 4 + 3]) * inv)));
-        }
-        slab_put_row(slab, lane, o);
-      }
-      slab_store(slab_s, &om.o0, c0, m0w, lane);
+    for (int l = 0; l < 4; ++l) {
+      prefetch_l2(ep.resid + off + l * 32);
+      if (ep.Y != nullptr) prefetch_l2(ep.Y + off + l * 32);
     }
-  } else if constexpr (KIND == EPI_BF16 || KIND == EPI_RELU2_BF16) {
-#pragma unroll 1
-    for (int ch = 0; ch < 2; ++ch) {
-      const int c0 = n0 + ch * 64;
-      uint32_t r[32], r2[32];
-      tmem_ld32(taddr + ch * 64, r);
-      tmem_ld32(taddr + ch * 64 + 32, r2);
-      tmem_ld_wait(r);
-      tmem_ld_wait(r2);
-      if (ch == 1) release_acc(lane, tempty);
-      if (c0 >= N) continue;
-      uint4 o[8];
+  } else if constexpr (KIND == EPI_RELU2_BF16 || KIND == EPI_SOFTCAP_F32 || KIND == EPI_QKV) {
+    p.rs = row_scale(ep, m, M);
+    if constexpr (KIND == EPI_QKV) {
+      const int vcol0 = (ep.H + ep.Hkv) * D, kcols = ep.Hkv * D;
+      if (ep.gp_in != nullptr && n0 + 128 > vcol0) {
+        const int tok = ep.tokens[m];
+        p.tok = (tok >= 0 && tok < ep.V) ? tok : -1;
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        float a[8];
+        for (int s = 0; s < 128 / D; ++s) {
+          const int c = n0 + s * D;
+          if (c < vcol0 || c >= N) continue;
+          const int hv = (c - vcol0) / D;
+          const float* gp = ep.gp_in + (static_cast<size_t>(m) * ep.Hkv + hv) * ep.ncg;
+          float z = 0.f;
+          for (int i = 0; i < ep.ncg; ++i) z += gp[i];
+          p.g[s] = ep.gate_scale * sigmoid_fast(p.rs * z);
+          if (p.tok >= 0) {
+            const bf16* row = ep.ve + static_cast<size_t>(p.tok) * kcols + static_cast<size_t>(hv) * D;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int e = c * 8 + j;
-          float t = __uint_as_float(e < 32 ? r[e] : r2[e - 32]);
-          if constexpr (KIND == EPI_RELU2_BF16) {
-            t = fmaxf(t, 0.f);
-            t = t * t;
+            for (int l = 0; l < D * 2 / 128; ++l) prefetch_l2(row + l * 64);
           }
-          a[j] = t;
         }
-        o[c] = pack8_bf16(a);
-      }
-      slab_acquire(lane);
-      slab_put_row(slab, lane, o);
-      slab_store(slab_s, &om.o0, c0, m0w, lane);
-    }
-  } else if constexpr (KIND == EPI_QKV) {
-    float v[128];
-    {
-      uint32_t r0[32], r1[32], r2[32], r3[32];
-      tmem_ld32(taddr + 0, r0);
-      tmem_ld32(taddr + 32, r1);
-      tmem_ld32(taddr + 64, r2);
-      tmem_ld32(taddr + 96, r3);
-      tmem_ld_wait(r0);
-      tmem_ld_wait(r1);
-      tmem_ld_wait(r2);
-      tmem_ld_wait(r3);
-      release_acc(lane, tempty);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        v[i] = __uint_as_float(r0[i]);
-        v[32 + i] = __uint_as_float(r1[i]);
-        v[64 + i] = __uint_as_float(r2[i]);
-        v[96 + i] = __uint_as_float(r3[i]);
       }
     }
-    const int qcols = ep.H * D, kcols = ep.Hkv * D;
-    const int pos = m % ep.T;
+  }
+  return p;
+}
+
+// ---------------------------------------------------------------- epilogues
+// One warp: rows [m0w, m0w + 32) (this thread: row m0w + lane), accumulator columns
+// [n0, n0 + 128) at TMEM address taddr (lane quarter applied).  Each releases the accumulator
+// after its last tcgen05.ld.
+
+// Plain bf16 store, or relu(rs * acc)^2 (MLP up projection, squared ReLU).
+template <bool RELU2>
+__device__ __forceinline__ void epi_bf16(uint32_t taddr, uint32_t tempty, int lane, int m0w, int n0, int M, int N,
+                                         const GemmEpi& ep, const OutMaps& om, Slab& sl, const EpiPre& pre) {
+  const float rs = pre.rs;
+#pragma unroll 1
+  for (int ch = 0; ch < 2; ++ch) {
+    const int c0 = n0 + ch * 64;
+    if (c0 >= N) break;
+    uint32_t r[32], r2[32];
+    tmem_ld32(taddr + ch * 64, r);
+    tmem_ld32(taddr + ch * 64 + 32, r2);
+    tmem_ld_wait(r);
+    tmem_ld_wait(r2);
+    uint4 o[8];
 #pragma unroll
-    for (int s = 0; s < 128 / D; ++s) {
-      const int c = n0 + s * D;
-      if (c >= N) break;
-      float* x = &v[s * D];
-      const CUtensorMap* map;
-      int xcol;
-      if (c < qcols + kcols) {
-        rope_rmsnorm<D>(x, ep.rope + static_cast<size_t>(pos) * (D / 2), ep.eps);
-        if (c < qcols) {
-          map = &om.o0;
-          xcol = c;
-        } else {
-          map = &om.o1;
-          xcol = c - qcols;
+    for (int c = 0; c < 8; ++c) {
+      float a[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int e = c * 8 + j;
+        float t = __uint_as_float(e < 32 ? r[e] : r2[e - 32]);
+        if constexpr (RELU2) {
+          t = fmaxf(t * rs, 0.f);
+          t = t * t;
         }
-      } else {
-        xcol = c - qcols - kcols;
-        map = &om.o2;
-        const int hv = xcol / D;
-        if (ep.gate != nullptr && m < M) {
-          const float g = ep.gate[static_cast<size_t>(m) * ep.Hkv + hv];
-          const int tok = ep.tokens[m];
-          if (tok >= 0 && tok < ep.V) {
-            const uint4* vr = reinterpret_cast<const uint4*>(ep.ve + static_cast<size_t>(tok) * kcols +
-                                                             static_cast<size_t>(hv) * D);
+        a[j] = t;
+      }
+      o[c] = pack8_bf16(a);
+    }
+    sl.acquire(lane);
+    sl.put_row(lane, o);
+    sl.store(&om.o0, c0, m0w, lane);
+  }
+  release_acc(lane, tempty);
+}
+
+// cap * tanh(rs * acc / cap), fp32 (logit soft-cap of the lm_head).
+__device__ __forceinline__ void epi_softcap(uint32_t taddr, uint32_t tempty, int lane, int m0w, int n0, int M,
+                                            int N, const GemmEpi& ep, const OutMaps& om, Slab& sl, const EpiPre& pre,
+                                            uint64_t store_policy) {
+  const float cap = ep.cap;
+  const float sc = pre.rs / cap;
+#pragma unroll 1
+  for (int ch = 0; ch < 4; ++ch) {
+    const int c0 = n0 + ch * 32;
+    if (c0 >= N) break;
+    uint32_t r[32];
+    tmem_ld32(taddr + ch * 32, r);
+    tmem_ld_wait(r);
+    uint4 o[8];
 #pragma unroll
-            for (int c8 = 0; c8 < D / 8; ++c8) {
-              const uint4 u = __ldg(vr + c8);
-              const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&u);
+    for (int c = 0; c < 8; ++c) {
+      o[c] = make_uint4(__float_as_uint(cap * tanh_approx(__uint_as_float(r[c * 4 + 0]) * sc)),
+                        __float_as_uint(cap * tanh_approx(__uint_as_float(r[c * 4 + 1]) * sc)),
+                        __float_as_uint(cap * tanh_approx(__uint_as_float(r[c * 4 + 2]) * sc)),
+                        __float_as_uint(cap * tanh_approx(__uint_as_float(r[c * 4 + 3]) * sc)));
+    }
+    sl.acquire(lane);
+    sl.put_row(lane, o);
+    sl.store_hint(&om.o0, c0, m0w, lane, store_policy);
+  }
+  release_acc(lane, tempty);
+}
+
+// Residual stream update (attention and MLP output projections), with the next consumer's
+// inputs: the bf16 copy of the new stream and its partial sums of squares (the consumer's
+// RMSNorm row scale), and on request the next block's residual mix, the backout cache, the
+// final backout, and the value-embedding gate partial dot products.
+__device__ __forceinline__ void epi_resid(uint32_t taddr, uint32_t tempty, int lane, int m0w, int n0, int M, int N,
+                                          const GemmEpi& ep, const OutMaps& om, Slab& sl, const EpiPre&) {
+  if (n0 >= N) {
+    release_acc(lane, tempty);
+    return;
+  }
+  const int m = m0w + lane;
+  const bool has_gate = ep.wg != nullptr;
+  float ss = 0.f;
+  float gacc[MAX_GATE_HEADS];
 #pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                const float2 f = __bfloat1622float2(h2[j]);
-                x[c8 * 8 + 2 * j] = fmaf(g, f.x, x[c8 * 8 + 2 * j]);
-                x[c8 * 8 + 2 * j + 1] = fmaf(g, f.y, x[c8 * 8 + 2 * j + 1]);
+  for (int h = 0; h < MAX_GATE_HEADS; ++h) gacc[h] = 0.f;
+  uint32_t xbp[32];
+#pragma unroll 1
+  for (int cp = 0; cp < 2; ++cp) {
+#pragma unroll
+  for (int hf = 0; hf < 2; ++hf) {
+    const int ch = cp * 2 + hf;
+    const int c0 = n0 + ch * 32;
+    uint32_t r[32];
+    tmem_ld32(taddr + ch * 32, r);
+    float4 rv[8], yv[8];
+    load_chunk_f32(ep.resid, N, m0w, c0, M, lane, rv);
+    if (ep.Y != nullptr) load_chunk_f32(ep.Y, N, m0w, c0, M, lane, yv);
+    tmem_ld_wait(r);
+    if (ch == 3) release_acc(lane, tempty);
+    float x[32];
+    sl.acquire(lane);
+    sl.transpose_f32(lane, rv, x);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) x[j] += __uint_as_float(r[j]);
+    if (ep.xm_out != nullptr) {   // backout cache: the stream after this block, before mixing
+      sl.put_row_f32(lane, x);
+      sl.store(&om.o1, c0, m0w, lane);
+      sl.acquire(lane);
+    }
+    if (ep.Y != nullptr) {
+      float y[32];
+      sl.transpose_f32(lane, yv, y);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) x[j] = fmaf(ep.a, x[j], ep.b * y[j]);
+    } else if (ep.a != 1.f) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) x[j] *= ep.a;
+    }
+#pragma unroll
+    for (int j = 0; j < 32; ++j) ss = fmaf(x[j], x[j], ss);
+    if (has_gate) {
+#pragma unroll
+      for (int h = 0; h < MAX_GATE_HEADS; ++h) {
+        if (h < ep.Hkv) {
+          const bf16* w = ep.wg + static_cast<size_t>(h) * ep.c_g + c0;
+          float acc = gacc[h];
+#pragma unroll
+          for (int q8 = 0; q8 < 4; ++q8) {
+            if (c0 + q8 * 8 < ep.c_g) {
+              const uint4 u = __ldg(reinterpret_cast<const uint4*>(w + q8 * 8));
+              const __nv_bfloat162* w2 = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+              for (int t = 0; t < 4; ++t) {
+                const float2 f = __bfloat1622float2(w2[t]);
+                acc = fmaf(x[q8 * 8 + 2 * t], f.x, acc);
+                acc = fmaf(x[q8 * 8 + 2 * t + 1], f.y, acc);
               }
             }
           }
+          gacc[h] = acc;
         }
       }
+    }
+    if (ep.x_out != nullptr) {
+      sl.put_row_f32(lane, x);
+      sl.store(&om.o0, c0, m0w, lane);
+    }
 #pragma unroll
-      for (int cc = 0; cc < D / 64; ++cc) {
-        uint4 o[8];
+    for (int j = 0; j < 16; ++j) xbp[hf * 16 + j] = pack_bf16(x[2 * j], x[2 * j + 1]);
+    if (hf == 1) {
+      uint4 o[8];
 #pragma unroll
-        for (int c8 = 0; c8 < 8; ++c8) o[c8] = pack8_bf16(x + cc * 64 + c8 * 8);
-        slab_acquire(lane);
-        slab_put_row(slab, lane, o);
-        slab_store(slab_s, map, xcol + cc * 64, m0w, lane);
-      }
+      for (int c = 0; c < 8; ++c) o[c] = make_uint4(xbp[4 * c], xbp[4 * c + 1], xbp[4 * c + 2], xbp[4 * c + 3]);
+      sl.acquire(lane);
+      sl.put_row(lane, o);
+      sl.store(&om.o2, c0 - 32, m0w, lane);
+    }
+  }
+  }
+  if (m < M) {
+    const int g = n0 / SS_GROUP;
+    ep.ssp_out[static_cast<size_t>(m) * ep.ncg + g] = ss;
+    if (has_gate) {
+#pragma unroll
+      for (int h = 0; h < MAX_GATE_HEADS; ++h)
+        if (h < ep.Hkv) ep.gp_out[(static_cast<size_t>(m) * ep.Hkv + h) * ep.ncg + g] = gacc[h];
     }
   }
 }
 
+// Packed q|k|v projection: q and k heads are rotated (RoPE) and RMS-normalised per head, v
+// heads get the value-embedding gate term.  rs (the block's input RMSNorm) scales every
+// column; for q and k the head norm is taken from the unrotated accumulator, since the
+// rotation keeps each head's norm.
+template <int D>
+__device__ __forceinline__ void epi_qkv(uint32_t taddr, uint32_t tempty, int lane, int m0w, int n0, int M, int N,
+                                        const GemmEpi& ep, const OutMaps& om, Slab& sl, const EpiPre& pre) {
+  const int m = m0w + lane;
+  const float rs = pre.rs;
+  const int qcols = ep.H * D, kcols = ep.Hkv * D;
+  const int pos = m < M ? m % ep.T : 0;
+#pragma unroll
+  for (int s = 0; s < 128 / D; ++s) {
+    const int c = n0 + s * D;
+    if (c >= N) break;
+    const uint32_t tb = taddr + s * D;
+    uint32_t outp[D / 2];   // the head as packed bf16 pairs
+    const CUtensorMap* map;
+    int xcol;
+    if (c < qcols + kcols) {
+      if (c < qcols) {
+        map = &om.o0;
+        xcol = c;
+      } else {
+        map = &om.o1;
+        xcol = c - qcols;
+      }
+      float ss = 0.f;
+#pragma unroll
+      for (int ch = 0; ch < D / 32; ++ch) {
+        uint32_t r[32];
+        tmem_ld32(tb + ch * 32, r);
+        tmem_ld_wait(r);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) ss = fmaf(__uint_as_float(r[j]), __uint_as_float(r[j]), ss);
+      }
+      const float sc = rs * rsqrtf(rs * rs * ss * (1.0f / D) + ep.eps);
+      const float2* rope = ep.rope + pos;
+#pragma unroll
+      for (int hc = 0; hc < D / 64; ++hc) {
+        uint32_t lo[32], hi[32];
+        tmem_ld32(tb + hc * 32, lo);
+        tmem_ld32(tb + D / 2 + hc * 32, hi);
+        float2 cs[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) cs[j] = __ldg(rope + static_cast<size_t>(hc * 32 + j) * ep.rope_ld);
+        tmem_ld_wait(lo);
+        tmem_ld_wait(hi);
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+          const float a0 = __uint_as_float(lo[j]), b0 = __uint_as_float(hi[j]);
+          const float a1 = __uint_as_float(lo[j + 1]), b1 = __uint_as_float(hi[j + 1]);
+          const float y0 = (a0 * cs[j].x + b0 * cs[j].y) * sc, z0 = (b0 * cs[j].x - a0 * cs[j].y) * sc;
+          const float y1 = (a1 * cs[j + 1].x + b1 * cs[j + 1].y) * sc, z1 = (b1 * cs[j + 1].x - a1 * cs[j + 1].y) * sc;
+          outp[(hc * 32 + j) / 2] = pack_bf16(y0, y1);
+          outp[(D / 2 + hc * 32 + j) / 2] = pack_bf16(z0, z1);
+        }
+      }
+    } else {
+      xcol = c - qcols - kcols;
+      map = &om.o2;
+      const int hv = xcol / D;
+      const float g = pre.g[s];
+      const uint4* vr = pre.tok >= 0 ? reinterpret_cast<const uint4*>(ep.ve + static_cast<size_t>(pre.tok) * kcols +
+                                                                      static_cast<size_t>(hv) * D)
+                                     : nullptr;
+#pragma unroll
+      for (int cc = 0; cc < D / 64; ++cc) {
+        uint32_t r0[32], r1[32];
+        tmem_ld32(tb + cc * 64, r0);
+        tmem_ld32(tb + cc * 64 + 32, r1);
+        uint4 e[8];
+#pragma unroll
+        for (int c8 = 0; c8 < 8; ++c8) e[c8] = vr ? __ldg(vr + cc * 8 + c8) : make_uint4(0u, 0u, 0u, 0u);
+        tmem_ld_wait(r0);
+        tmem_ld_wait(r1);
+#pragma unroll
+        for (int c8 = 0; c8 < 8; ++c8) {
+          const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&e[c8]);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int idx = c8 * 8 + 2 * j;
+            const float2 f = __bfloat1622float2(h2[j]);
+            const float v0 = __uint_as_float(idx < 32 ? r0[idx] : r1[idx - 32]);
+            const float v1 = __uint_as_float(idx + 1 < 32 ? r0[idx + 1] : r1[idx + 1 - 32]);
+            outp[(cc * 64 + idx) / 2] = pack_bf16(fmaf(g, f.x, v0 * rs), fmaf(g, f.y, v1 * rs));
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int cc = 0; cc < D / 64; ++cc) {
+      uint4 o[8];
+#pragma unroll
+      for (int c8 = 0; c8 < 8; ++c8)
+        o[c8] = make_uint4(outp[cc * 32 + 4 * c8], outp[cc * 32 + 4 * c8 + 1], outp[cc * 32 + 4 * c8 + 2],
+                           outp[cc * 32 + 4 * c8 + 3]);
+      sl.acquire(lane);
+      sl.put_row(lane, o);
+      sl.store(map, xcol + cc * 64, m0w, lane);
+    }
+  }
+  release_acc(lane, tempty);
+}
+
 template <int KIND, int D>
+// 10 warps spread 3/3/2/2 over the four 16K-register SM sub-partitions: at most 168
+// registers per thread.
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ OutMaps om, int M, int N, int K, const __grid_constant__ GemmEpi ep) {
+                   const __grid_constant__ OutMaps om, int M, int N, int K, int n_fast,
+                   const __grid_constant__ GemmEpi ep) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -349,10 +559,14 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   if (warp == 0) {
     if (lane == 0) {
+      // The operand shared by the pairs running at the same time is read once per wave; the
+      // other one is re-read for every tile of the walk and should stay in L2.
+      const uint64_t pol_a = n_fast ? policy_evict_first() : policy_evict_last();
+      const uint64_t pol_b = n_fast ? policy_evict_last() : policy_evict_first();
       uint32_t it = 0;
       bool ok = true;
       for (int tile = pair; tile < num_tiles && ok; tile += npairs) {
-        const int mb = tile % num_m, nb = tile / num_m;
+        const int mb = n_fast ? tile / num_n : tile % num_m, nb = n_fast ? tile % num_n : tile / num_m;
         for (int kb = 0; kb < kblocks; ++kb) {
           const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
           if (!mbar_wait_cluster(smem_u32(&ctl->empty[s]), ph ^ 1, abort, status)) {
@@ -361,8 +575,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           const uint32_t fb = mapa_shared(smem_u32(&ctl->full[s]), 0);   // the leader's barrier
           if (rank == 0) mbar_arrive_expect_tx(smem_u32(&ctl->full[s]), 2 * (A_BYTES + B_BYTES));
-          tma_load_2d_pair(sA + s * A_BYTES, &tmA, fb, kb * BK, mb * PAIR_M + static_cast<int>(rank) * BM);
-          tma_load_2d_pair(sB + s * B_BYTES, &tmB, fb, kb * BK, nb * BN + static_cast<int>(rank) * B_ROWS);
+          tma_load_2d_pair_hint(sA + s * A_BYTES, &tmA, fb, kb * BK, mb * PAIR_M + static_cast<int>(rank) * BM, pol_a);
+          tma_load_2d_pair_hint(sB + s * B_BYTES, &tmB, fb, kb * BK, nb * BN + static_cast<int>(rank) * B_ROWS, pol_b);
           ++it;
         }
       }
@@ -410,19 +624,24 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int ew = warp - 2;
     const int quarter = warp & 3;
     const int group = ew >> 2;
-    uint8_t* slab = smem + OFF_SLAB + ew * SLAB_BYTES;
-    const uint32_t slab_s = smem_u32(slab);
+    Slab sl{smem + OFF_SLAB + ew * SLAB_BYTES, smem_u32(smem + OFF_SLAB + ew * SLAB_BYTES), 0u};
+    const uint64_t store_policy = policy_evict_first();   // logits are written once, never re-read
     uint32_t tc = 0;
     for (int tile = pair; tile < num_tiles; tile += npairs, ++tc) {
       const uint32_t a = tc & 1, aph = (tc >> 1) & 1;
+      const int mb = n_fast ? tile / num_n : tile % num_m, nb = n_fast ? tile % num_n : tile / num_m;
+      const int m0w = mb * PAIR_M + static_cast<int>(rank) * BM + quarter * 32, n0 = nb * BN + group * 128;
+      const EpiPre pre = epi_pre<KIND, D>(lane, m0w, n0, M, N, ep);
       const bool ok = mbar_wait_cluster(smem_u32(&ctl->tfull[a]), aph, abort, status);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
       const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + a * BN + group * 128;
-      const int mb = tile % num_m, nb = tile / num_m;
-      epilogue_warp<KIND, D>(taddr, mapa_shared(smem_u32(&ctl->tempty[a]), 0), lane,
-                             mb * PAIR_M + static_cast<int>(rank) * BM + quarter * 32, nb * BN + group * 128, M, N,
-                             ep, om, slab, slab_s);
+      const uint32_t tempty = mapa_shared(smem_u32(&ctl->tempty[a]), 0);
+      if constexpr (KIND == EPI_RESID) epi_resid(taddr, tempty, lane, m0w, n0, M, N, ep, om, sl, pre);
+      else if constexpr (KIND == EPI_SOFTCAP_F32)
+        epi_softcap(taddr, tempty, lane, m0w, n0, M, N, ep, om, sl, pre, store_policy);
+      else if constexpr (KIND == EPI_QKV) epi_qkv<D>(taddr, tempty, lane, m0w, n0, M, N, ep, om, sl, pre);
+      else epi_bf16<KIND == EPI_RELU2_BF16>(taddr, tempty, lane, m0w, n0, M, N, ep, om, sl, pre);
     }
     if (lane == 0) bulk_wait<0>();   // stores complete before the CTA exits
     __syncwarp();
@@ -465,7 +684,12 @@ cudaError_t launch_kind(const CUtensorMap& ta, const CUtensorMap& tb, const OutM
   const int tiles = ((M + PAIR_M - 1) / PAIR_M) * ((N + BN - 1) / BN);
   const int pairs = tiles < max_pairs ? tiles : max_pairs;
   cfg.gridDim = dim3(2 * pairs);
-  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<KIND, D>, ta, tb, om, M, N, K, epi);
+  // Walk the column blocks fastest when A is the larger operand (the pairs of a wave then
+  // share one row block of A), the row blocks fastest otherwise (they share a block of B).
+  const int n_fast = M >= N ? 1 : 0;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<KIND, D>, ta, tb, om, M, N, K, n_fast, epi);
+  if (e != cudaSuccess) cudaGetLastError();   // a failed launch must not resurface in a later call
+  return e;
 }
 
 }  // namespace
@@ -480,7 +704,17 @@ cudaError_t launch_gemm(const bf16* A, const bf16* B, int M, int N, int K, const
   const uint64_t Mu = static_cast<uint64_t>(M);
   bool ok = true;
   switch (epi.kind) {
-    case EPI_RESID_F32:
+    case EPI_RESID: {
+      if (N % SS_GROUP != 0 || epi.resid == nullptr || epi.xb == nullptr || epi.ssp_out == nullptr ||
+          epi.ncg != N / SS_GROUP || (epi.wg != nullptr && (epi.gp_out == nullptr || epi.Hkv < 1 ||
+                                                           epi.Hkv > MAX_GATE_HEADS || epi.c_g % 8 != 0)))
+        return cudaErrorInvalidValue;
+      const uint64_t ld4 = static_cast<uint64_t>(N) * 4;
+      if (epi.x_out) ok = make_tmap_2d(&om.o0, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, epi.x_out, N, Mu, ld4, 32, 32);
+      if (ok && epi.xm_out) ok = make_tmap_2d(&om.o1, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, epi.xm_out, N, Mu, ld4, 32, 32);
+      if (ok) ok = make_tmap_bf16_2d(&om.o2, epi.xb, N, Mu, static_cast<uint64_t>(N) * 2, 64, 32);
+      break;
+    }
     case EPI_SOFTCAP_F32:
       ok = make_tmap_2d(&om.o0, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, epi.out, N, Mu, static_cast<uint64_t>(epi.ldo) * 4, 32, 32);
       break;
@@ -490,6 +724,8 @@ cudaError_t launch_gemm(const bf16* A, const bf16* B, int M, int N, int K, const
       break;
     case EPI_QKV: {
       const uint64_t qc = static_cast<uint64_t>(epi.H) * epi.D, kc = static_cast<uint64_t>(epi.Hkv) * epi.D;
+      if (epi.rope == nullptr || epi.rope_ld < 1 || (epi.gp_in != nullptr && (epi.ve == nullptr || epi.tokens == nullptr)))
+        return cudaErrorInvalidValue;
       ok = make_tmap_bf16_2d(&om.o0, epi.q, qc, Mu, qc * 2, 64, 32) &&
            make_tmap_bf16_2d(&om.o1, epi.k, kc, Mu, kc * 2, 64, 32) &&
            make_tmap_bf16_2d(&om.o2, epi.v, kc, Mu, kc * 2, 64, 32);
@@ -500,7 +736,7 @@ cudaError_t launch_gemm(const bf16* A, const bf16* B, int M, int N, int K, const
   if (!ok) return cudaErrorInvalidValue;
   switch (epi.kind) {
     case EPI_BF16: return launch_kind<EPI_BF16, 0>(ta, tb, om, M, N, K, epi, num_sms, stream);
-    case EPI_RESID_F32: return launch_kind<EPI_RESID_F32, 0>(ta, tb, om, M, N, K, epi, num_sms, stream);
+    case EPI_RESID: return launch_kind<EPI_RESID, 0>(ta, tb, om, M, N, K, epi, num_sms, stream);
     case EPI_RELU2_BF16: return launch_kind<EPI_RELU2_BF16, 0>(ta, tb, om, M, N, K, epi, num_sms, stream);
     case EPI_SOFTCAP_F32: return launch_kind<EPI_SOFTCAP_F32, 0>(ta, tb, om, M, N, K, epi, num_sms, stream);
     case EPI_QKV:

@@ -14,32 +14,68 @@ using bf16 = __nv_bfloat16;
 
 enum EpiKind : int {
   EPI_BF16 = 0,         // out(bf16) = acc
-  EPI_RESID_F32 = 1,    // out(f32) = resid + acc   (resid may alias out)
-  EPI_RELU2_BF16 = 2,   // out(bf16) = relu(acc)^2
-  EPI_SOFTCAP_F32 = 3,  // out(f32) = cap * tanh(acc / cap)
+  EPI_RESID = 1,        // residual stream update (see GemmEpi, "residual" fields)
+  EPI_RELU2_BF16 = 2,   // out(bf16) = relu(rs * acc)^2
+  EPI_SOFTCAP_F32 = 3,  // out(f32) = cap * tanh(rs * acc / cap)
   EPI_QKV = 4,          // q|k|v split, RoPE + RMSNorm on q and k, value-embedding gate on v
 };
 
+// Columns covered by one partial sum of squares (one epilogue thread's share of a row).
+constexpr int SS_GROUP = 128;
+
 struct GemmEpi {
   int kind = EPI_BF16;
+  int* status = nullptr;
+
+  // Row scale of the consuming epilogues (RELU2, SOFTCAP, QKV): rs[m] = 1 / sqrt(sum_g
+  // ssp[m, g] / ncols + eps), ssp fp32 [M, ncg] partial sums of squares; ssp == null -> rs = 1.
+  const float* ssp_in = nullptr;
+  int ncg = 0;            // partial sums per row (ncols / SS_GROUP)
+  float inv_ncols = 0.f;  // 1 / ncols
+  float eps = 1e-6f;
+
+  // EPI_BF16 / EPI_RELU2_BF16 / EPI_SOFTCAP_F32
   void* out = nullptr;
   int ldo = 0;
-  const float* resid = nullptr;
-  int ldr = 0;
   float cap = 15.f;
+
+  // EPI_RESID (N = ncols of the stream, N % 128 == 0):
+  //   xr = resid + acc;  xm_out <- xr (if set);  x' = a * xr + b * Y (Y may be null);
+  //   x_out <- x' (if set, may alias resid);  xb <- bf16(x');
+  //   ssp_out[m, g] = sum of x'^2 over columns [128 g, 128 g + 128);
+  //   if wg: gp_out[m, h, g] = sum over those columns c < c_g of x'[c] * wg[h, c], h < Hkv.
+  const float* resid = nullptr;
+  float a = 1.f, b = 0.f;
+  const float* Y = nullptr;
+  float* x_out = nullptr;
+  float* xm_out = nullptr;
+  bf16* xb = nullptr;
+  float* ssp_out = nullptr;
+  const bf16* wg = nullptr;
+  int c_g = 0;
+  float* gp_out = nullptr;
+
   // EPI_QKV
   bf16* q = nullptr;
   bf16* k = nullptr;
   bf16* v = nullptr;
   int H = 0, Hkv = 0, D = 0, T = 1;
-  const float2* rope = nullptr;   // [T_ctx][D/2] (cos, sin)
-  float eps = 1e-6f;
-  const float* gate = nullptr;    // [M, Hkv] or null (no value embedding on this layer)
+  int rope_ld = 0;                // row length (positions) of the rotary table
+  const float2* rope = nullptr;   // [D/2][rope_ld] (cos, sin), position fastest
+  const float* gp_in = nullptr;   // [M, Hkv, ncg] gate pre-activation partials, or null (no VE)
+  float gate_scale = 1.f;
   const bf16* ve = nullptr;       // [V, Hkv*D]
   const int32_t* tokens = nullptr;
   int V = 0;
-  int* status = nullptr;
 };
+
+// Largest number of kv heads whose value-embedding gate partials one epilogue thread keeps.
+constexpr int MAX_GATE_HEADS = 16;
+
+// Records `e` as the calling thread's last CUDA error (read by nc_last_cuda_error) and maps it
+// to a status: NC_OK for cudaSuccess, NC_ERR_CUDA otherwise.
+nc_status cuda_status(cudaError_t e);
+const char* last_cuda_error_name();
 
 // Encodes a 2-D TMA descriptor with 128-byte swizzling through the driver entry point
 // (no link-time libcuda).  inner/outer are extents in elements, row stride in bytes.
@@ -57,16 +93,14 @@ inline bool make_tmap_bf16_2d(CUtensorMap* map, const void* ptr, uint64_t inner,
 cudaError_t launch_gemm(const bf16* A, const bf16* B, int M, int N, int K, const GemmEpi& epi,
                         int num_sms, cudaStream_t stream);
 
+// x0 = smear(wte[tokens]); x = a * x0; xb = bf16(x); ssp[m, g] = sum of x^2 over column group g;
+// if wg: gp[m, h, g] = sum over group g columns c < c_g of x[c] * wg[h, c].
 cudaError_t launch_embed_smear(const int32_t* tokens, int B, int T, const bf16* wte, int V, int C,
-                               const bf16* smear_gate, int c_s, int embed_norm, float eps,
-                               float* x0, int* status, cudaStream_t stream);
+                               const bf16* smear_gate, int c_s, int embed_norm, float eps, float a,
+                               float* x0, float* x, bf16* xb, float* ssp, const bf16* wg, int Hkv,
+                               int c_g, float* gp, int* status, cudaStream_t stream);
 
-// x_new = a*x + b*y (y may be null when b == 0); optionally stored to x_out;
-// xn = bf16(x_new / rms(x_new)); optionally gate[m, g] = scale*sigmoid(xn32[:c_g] . wg[g]).
-cudaError_t launch_rownorm(const float* x, const float* y, float a, float b, float* x_out, bf16* xn,
-                           int M, int C, float eps, const bf16* wg, int Hkv, int c_g,
-                           float gate_scale, float* gate, cudaStream_t stream);
-
+// table[i][t] = (cos, sin)(t * base^(-2i/D)), i < D/2, t < T (position fastest).
 cudaError_t launch_rope_table(float2* table, int T, int D, float base, cudaStream_t stream);
 
 // y[M, H*D] = windowed causal GQA attention of q [M, H*D], k/v [M, Hkv*D].

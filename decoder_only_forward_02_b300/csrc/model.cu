@@ -2,13 +2,20 @@
 // layout and the per-layer launch sequence of the forward pass.
 //
 // Launch sequence for one forward ("Nanochat在nanoGPT之上的新增功能", section 1 table and
-// notes; order of the block as described there: pre-norm attention, then pre-norm MLP):
-//   embed+smear -> x0
-//   per layer i:  rownorm (x <- lr_i*x + l0_i*x0, xn = norm(x), VE gate)  -> QKV GEMM (RoPE,
-//                 QK-norm, v += gate*ve) -> attention -> out-proj GEMM (+residual) ->
-//                 rownorm -> fc GEMM (ReLU^2) -> proj GEMM (+residual; after layer L/2-1 the
-//                 result is written to a separate buffer, which becomes the backout cache)
-//   rownorm (x - lb*x_mid, norm) -> lm_head GEMM (soft-cap)
+// notes; each block is pre-norm attention, then pre-norm MLP).  RMSNorm has no weight, so each
+// norm is split: the kernel that writes the residual stream also writes its bf16 copy and
+// per-row partial sums of squares, and the GEMM that consumes it scales its accumulator rows
+// by 1 / rms.
+//   embed: x0 = smear(wte[tok]); x = (lr_0 + l0_0) x0 (+ bf16 copy, partial sums, VE gate partials)
+//   per layer i:
+//     QKV GEMM  (row scale, RoPE, QK-norm, v += gate * ve)
+//     attention
+//     out-proj GEMM: x += y Wo^T (+ bf16 copy, partial sums)
+//     fc GEMM   (row scale, ReLU^2)
+//     proj GEMM: x += h Wproj^T; after layer L/2-1 that result is also the backout cache;
+//                then x = lr_{i+1} x + l0_{i+1} x0 for the next block (+ its VE gate partials),
+//                or after the last layer x - lb * x_mid (final norm's input)
+//   lm_head GEMM (row scale, soft-cap)
 #include "internal.h"
 
 #include <cudaTypedefs.h>
@@ -38,6 +45,18 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
 }
 
 }  // namespace
+
+namespace {
+thread_local cudaError_t g_last_cuda_error = cudaSuccess;
+}  // namespace
+
+nc_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return NC_OK;
+  g_last_cuda_error = e;
+  return NC_ERR_CUDA;
+}
+
+const char* last_cuda_error_name() { return cudaGetErrorName(g_last_cuda_error); }
 
 bool make_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* ptr, uint64_t inner,
                   uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer) {
@@ -69,7 +88,7 @@ struct TimedLaunch {
 };
 
 struct Layout {
-  size_t x0, xa, xm, xn, q, k, v, gate, y, h, end;
+  size_t x0, x, xm, xb, q, k, v, y, h, ssp, gp, end;
 };
 
 }  // namespace
@@ -115,7 +134,9 @@ nc_status validate_config(const nc_config* c) {
   if (c->head_dim != 64 && c->head_dim != 128) return NC_ERR_UNSUPPORTED;
   if (c->n_embd % 128 != 0 || c->n_embd > 2048) return NC_ERR_UNSUPPORTED;
   if (c->mlp_hidden % 64 != 0 || c->vocab_size % 64 != 0) return NC_ERR_UNSUPPORTED;
-  if (c->smear_gate_channels % 4 != 0 || c->ve_gate_channels % 4 != 0) return NC_ERR_UNSUPPORTED;
+  if (c->smear_gate_channels % 4 != 0 || c->ve_gate_channels % 8 != 0) return NC_ERR_UNSUPPORTED;
+  for (int i = 0; i < c->n_layer; ++i)
+    if (c->has_ve[i] && c->n_kv_head > nc::MAX_GATE_HEADS) return NC_ERR_UNSUPPORTED;
   return NC_OK;
 }
 
@@ -138,15 +159,16 @@ Layout layout_for(const nc_model* m, int B, int T) {
     return o;
   };
   L.x0 = take(M * c.n_embd * 4);
-  L.xa = take(M * c.n_embd * 4);
+  L.x = take(M * c.n_embd * 4);
   L.xm = take(c.use_backout ? M * c.n_embd * 4 : 0);
-  L.xn = take(M * c.n_embd * 2);
+  L.xb = take(M * c.n_embd * 2);
   L.q = take(M * c.n_head * c.head_dim * 2);
   L.k = take(M * c.n_kv_head * c.head_dim * 2);
   L.v = take(M * c.n_kv_head * c.head_dim * 2);
-  L.gate = take(M * c.n_kv_head * 4);
   L.y = take(M * c.n_head * c.head_dim * 2);
   L.h = take(M * c.mlp_hidden * 2);
+  L.ssp = take(M * (c.n_embd / nc::SS_GROUP) * 4);
+  L.gp = take(M * c.n_kv_head * (c.n_embd / nc::SS_GROUP) * 4);
   L.end = off;
   return L;
 }
@@ -205,10 +227,11 @@ const char* nc_status_string(nc_status s) {
   }
 }
 
+const char* nc_last_cuda_error(void) { return nc::last_cuda_error_name(); }
+
 const char* nc_kernel_class_name(nc_kernel_class k) {
-  static const char* names[NC_K_COUNT] = {"embed_smear", "rownorm",  "qkv_rope_qknorm_ve",
-                                          "attention",   "oproj_residual", "fc_relu2",
-                                          "proj_residual", "lmhead_softcap"};
+  static const char* names[NC_K_COUNT] = {"embed_smear", "qkv_rope_qknorm_ve", "attention", "oproj_residual",
+                                          "fc_relu2",    "proj_residual",      "lmhead_softcap"};
   return (k >= 0 && k < NC_K_COUNT) ? names[k] : "unknown";
 }
 
@@ -241,7 +264,7 @@ nc_status nc_model_create(const nc_config* cfg, const nc_weights* w, void* packe
       if (p == nullptr || !aligned(p, 16)) return NC_ERR_INVALID_ARG;
     if (cfg->has_ve[i]) {
       if (w->ve_table == nullptr || w->ve_gate == nullptr || w->ve_table[i] == nullptr ||
-          w->ve_gate[i] == nullptr || !aligned(w->ve_table[i], 16) || !aligned(w->ve_gate[i], 8))
+          w->ve_gate[i] == nullptr || !aligned(w->ve_table[i], 16) || !aligned(w->ve_gate[i], 16))
         return NC_ERR_INVALID_ARG;
     }
   }
@@ -293,7 +316,7 @@ nc_status nc_model_create(const nc_config* cfg, const nc_weights* w, void* packe
     e = nc::launch_rope_table(m->rope, cfg->seq_len_ctx, cfg->head_dim, cfg->rope_base, stream);
   if (e != cudaSuccess) {
     delete m;
-    return NC_ERR_CUDA;
+    return nc::cuda_status(e);
   }
   *out = m;
   return NC_OK;
@@ -330,35 +353,52 @@ nc_status nc_forward(nc_model* m, const int32_t* tokens, int B, int T, float* lo
   const nc_config& c = m->cfg;
   const int M = B * T, C = c.n_embd, H = c.n_head, Hkv = c.n_kv_head, D = c.head_dim;
   const int F = c.mlp_hidden, V = c.vocab_size, L = c.n_layer;
+  const int ncg = C / nc::SS_GROUP;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   float* x0 = reinterpret_cast<float*>(ws + Lo.x0);
-  float* xa = reinterpret_cast<float*>(ws + Lo.xa);
+  float* x = reinterpret_cast<float*>(ws + Lo.x);
   float* xm = reinterpret_cast<float*>(ws + Lo.xm);
-  bf16* xn = reinterpret_cast<bf16*>(ws + Lo.xn);
+  bf16* xb = reinterpret_cast<bf16*>(ws + Lo.xb);
   bf16* q = reinterpret_cast<bf16*>(ws + Lo.q);
   bf16* k = reinterpret_cast<bf16*>(ws + Lo.k);
   bf16* v = reinterpret_cast<bf16*>(ws + Lo.v);
-  float* gate = reinterpret_cast<float*>(ws + Lo.gate);
   bf16* y = reinterpret_cast<bf16*>(ws + Lo.y);
   bf16* h = reinterpret_cast<bf16*>(ws + Lo.h);
+  float* ssp = reinterpret_cast<float*>(ws + Lo.ssp);
+  float* gp = reinterpret_cast<float*>(ws + Lo.gp);
   const int c_s = c.smear_gate_channels ? c.smear_gate_channels : C;
   const int c_g = c.ve_gate_channels ? c.ve_gate_channels : C;
   const int mid = L / 2 - 1;
 
+  // Row-scale inputs shared by the consuming epilogues.
+  auto consumer = [&](nc::GemmEpi& e) {
+    e.ssp_in = ssp;
+    e.ncg = ncg;
+    e.inv_ncols = 1.0f / static_cast<float>(C);
+    e.eps = c.rms_eps;
+    e.status = m->status;
+  };
+  // Residual-stream update of an output projection: x += acc, bf16 copy and partial sums.
+  auto resid = [&](nc::GemmEpi& e) {
+    e.kind = nc::EPI_RESID;
+    e.resid = x;
+    e.x_out = x;
+    e.xb = xb;
+    e.ssp_out = ssp;
+    e.ncg = ncg;
+    e.status = m->status;
+  };
+
   cudaError_t e = timed(m, NC_K_EMBED, stream, [&] {
-    return nc::launch_embed_smear(tokens, B, T, m->wte, V, C, m->smear, c_s, c.embed_norm, c.rms_eps, x0,
-                                  m->status, stream);
+    const bool ve0 = m->has_ve[0] != 0;
+    return nc::launch_embed_smear(tokens, B, T, m->wte, V, C, m->smear, c_s, c.embed_norm, c.rms_eps,
+                                  m->lr[0] + m->l0[0], x0, x, xb, ssp, ve0 ? m->veg[0] : nullptr, Hkv, c_g,
+                                  ve0 ? gp : nullptr, m->status, stream);
   });
-  const float* cur = x0;
   for (int i = 0; i < L && e == cudaSuccess; ++i) {
     const bool ve = m->has_ve[i] != 0;
-    e = timed(m, NC_K_NORM, stream, [&] {
-      return nc::launch_rownorm(cur, x0, m->lr[i], m->l0[i], xa, xn, M, C, c.rms_eps, m->veg[i], Hkv, c_g,
-                                c.ve_gate_scale, ve ? gate : nullptr, stream);
-    });
-    cur = xa;
-    if (e != cudaSuccess) break;
     nc::GemmEpi qe;
+    consumer(qe);
     qe.kind = nc::EPI_QKV;
     qe.q = q;
     qe.k = k;
@@ -368,14 +408,14 @@ nc_status nc_forward(nc_model* m, const int32_t* tokens, int B, int T, float* lo
     qe.D = D;
     qe.T = T;
     qe.rope = m->rope;
-    qe.eps = c.rms_eps;
-    qe.gate = ve ? gate : nullptr;
+    qe.rope_ld = c.seq_len_ctx;
+    qe.gp_in = ve ? gp : nullptr;
+    qe.gate_scale = c.ve_gate_scale;
     qe.ve = m->ve[i];
     qe.tokens = tokens;
     qe.V = V;
-    qe.status = m->status;
     e = timed(m, NC_K_QKV, stream, [&] {
-      return nc::launch_gemm(xn, m->wqkv + static_cast<size_t>(i) * m->qkv_layer_elems(), M, m->Nqkv(), C,
+      return nc::launch_gemm(xb, m->wqkv + static_cast<size_t>(i) * m->qkv_layer_elems(), M, m->Nqkv(), C,
                              qe, m->num_sms, stream);
     });
     if (e != cudaSuccess) break;
@@ -383,53 +423,50 @@ nc_status nc_forward(nc_model* m, const int32_t* tokens, int B, int T, float* lo
       return nc::launch_attention(q, k, v, B, T, H, Hkv, D, m->window[i], y, m->status, stream);
     });
     if (e != cudaSuccess) break;
-    nc::GemmEpi re;
-    re.kind = nc::EPI_RESID_F32;
-    re.out = xa;
-    re.ldo = C;
-    re.resid = xa;
-    re.ldr = C;
-    re.status = m->status;
-    e = timed(m, NC_K_OPROJ, stream, [&] {
-      return nc::launch_gemm(y, m->wo[i], M, C, H * D, re, m->num_sms, stream);
-    });
-    if (e != cudaSuccess) break;
-    e = timed(m, NC_K_NORM, stream, [&] {
-      return nc::launch_rownorm(xa, nullptr, 1.f, 0.f, nullptr, xn, M, C, c.rms_eps, nullptr, 0, c_g, 1.f,
-                                nullptr, stream);
-    });
+    nc::GemmEpi oe;
+    resid(oe);
+    e = timed(m, NC_K_OPROJ, stream, [&] { return nc::launch_gemm(y, m->wo[i], M, C, H * D, oe, m->num_sms, stream); });
     if (e != cudaSuccess) break;
     nc::GemmEpi fe;
+    consumer(fe);
     fe.kind = nc::EPI_RELU2_BF16;
     fe.out = h;
     fe.ldo = F;
-    fe.status = m->status;
-    e = timed(m, NC_K_FC, stream, [&] { return nc::launch_gemm(xn, m->wfc[i], M, F, C, fe, m->num_sms, stream); });
+    e = timed(m, NC_K_FC, stream, [&] { return nc::launch_gemm(xb, m->wfc[i], M, F, C, fe, m->num_sms, stream); });
     if (e != cudaSuccess) break;
-    nc::GemmEpi pe = re;
-    float* dst = (c.use_backout && i == mid) ? xm : xa;
-    pe.out = dst;
-    pe.resid = xa;
+    nc::GemmEpi pe;
+    resid(pe);
+    if (c.use_backout && i == mid) pe.xm_out = xm;
+    if (i + 1 < L) {   // the next block's residual mix and, on a VE layer, its gate partials
+      pe.a = m->lr[i + 1];
+      pe.b = m->l0[i + 1];
+      pe.Y = x0;
+      if (m->has_ve[i + 1]) {
+        pe.wg = m->veg[i + 1];
+        pe.Hkv = Hkv;
+        pe.c_g = c_g;
+        pe.gp_out = gp;
+      }
+    } else {           // final: backout, then only the lm_head's inputs are needed
+      pe.x_out = nullptr;
+      if (c.use_backout) {
+        pe.a = 1.f;
+        pe.b = -m->lb;
+        pe.Y = mid < 0 ? x0 : xm;
+      }
+    }
     e = timed(m, NC_K_PROJ, stream, [&] { return nc::launch_gemm(h, m->wproj[i], M, C, F, pe, m->num_sms, stream); });
-    cur = dst;
-  }
-  if (e == cudaSuccess) {
-    const float* xmid = c.use_backout ? (mid < 0 ? x0 : xm) : nullptr;
-    e = timed(m, NC_K_NORM, stream, [&] {
-      return nc::launch_rownorm(cur, xmid, 1.f, xmid ? -m->lb : 0.f, nullptr, xn, M, C, c.rms_eps, nullptr, 0,
-                                c_g, 1.f, nullptr, stream);
-    });
   }
   if (e == cudaSuccess) {
     nc::GemmEpi le;
+    consumer(le);
     le.kind = nc::EPI_SOFTCAP_F32;
     le.out = logits;
     le.ldo = V;
     le.cap = c.softcap;
-    le.status = m->status;
-    e = timed(m, NC_K_LMHEAD, stream, [&] { return nc::launch_gemm(xn, m->lm, M, V, C, le, m->num_sms, stream); });
+    e = timed(m, NC_K_LMHEAD, stream, [&] { return nc::launch_gemm(xb, m->lm, M, V, C, le, m->num_sms, stream); });
   }
-  return e == cudaSuccess ? NC_OK : NC_ERR_CUDA;
+  return nc::cuda_status(e);
 }
 
 nc_status nc_forward_host(nc_model* m, const int32_t* tokens_host, int B, int T, float* logits_host,
@@ -448,23 +485,24 @@ nc_status nc_forward_host(nc_model* m, const int32_t* tokens_host, int B, int T,
   int32_t* tok_dev = reinterpret_cast<int32_t*>(ws + base);
   float* logits_dev = reinterpret_cast<float*>(ws + base + align_up(M * 4));
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
-  if (cudaMemcpyAsync(tok_dev, tokens_host, M * 4, cudaMemcpyHostToDevice, stream) != cudaSuccess)
-    return NC_ERR_CUDA;
+  s = nc::cuda_status(cudaMemcpyAsync(tok_dev, tokens_host, M * 4, cudaMemcpyHostToDevice, stream));
+  if (s != NC_OK) return s;
   s = nc_forward(m, tok_dev, B, T, logits_dev, workspace, base, stream_);
   if (s != NC_OK) return s;
-  if (cudaMemcpyAsync(logits_host, logits_dev, M * m->cfg.vocab_size * 4, cudaMemcpyDeviceToHost, stream) !=
-      cudaSuccess)
-    return NC_ERR_CUDA;
-  return cudaStreamSynchronize(stream) == cudaSuccess ? NC_OK : NC_ERR_CUDA;
+  s = nc::cuda_status(
+      cudaMemcpyAsync(logits_host, logits_dev, M * m->cfg.vocab_size * 4, cudaMemcpyDeviceToHost, stream));
+  if (s != NC_OK) return s;
+  return nc::cuda_status(cudaStreamSynchronize(stream));
 }
 
 nc_status nc_get_status(nc_model* m, void* stream_) {
   if (m == nullptr) return NC_ERR_INVALID_ARG;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   int h = 0;
-  if (cudaStreamSynchronize(stream) != cudaSuccess) return NC_ERR_CUDA;
-  if (cudaMemcpy(&h, m->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return NC_ERR_CUDA;
-  if (cudaMemset(m->status, 0, sizeof(int)) != cudaSuccess) return NC_ERR_CUDA;
+  nc_status s = nc::cuda_status(cudaStreamSynchronize(stream));
+  if (s == NC_OK) s = nc::cuda_status(cudaMemcpy(&h, m->status, sizeof(int), cudaMemcpyDeviceToHost));
+  if (s == NC_OK) s = nc::cuda_status(cudaMemset(m->status, 0, sizeof(int)));
+  if (s != NC_OK) return s;
   return static_cast<nc_status>(h);
 }
 
@@ -494,7 +532,7 @@ nc_status nc_timing_read(nc_model* m, nc_kernel_class k, double* total_ms, int* 
 
 int nc_forward_launch_count(const nc_model* m) {
   if (m == nullptr) return 0;
-  return 1 + 7 * m->cfg.n_layer + 2;
+  return 2 + 5 * m->cfg.n_layer;
 }
 
 }  // extern "C"

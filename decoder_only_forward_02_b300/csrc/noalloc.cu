@@ -28,11 +28,15 @@ void* g_scratch_ptr[kMaxDevices] = {};
 // Device address of the scratch array on the current device (looked up once per device).
 nc_status scratch_for_current_device(void** out) {
   int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return NC_ERR_CUDA;
+  const nc_status s = nc::cuda_status(cudaGetDevice(&dev));
+  if (s != NC_OK) return s;
+  if (dev < 0 || dev >= kMaxDevices) return NC_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lock(g_mutex);
   if (g_scratch_ptr[dev] == nullptr) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || p == nullptr) return NC_ERR_CUDA;
+    const nc_status e = nc::cuda_status(cudaGetSymbolAddress(&p, g_static_scratch));
+    if (e != NC_OK) return e;
+    if (p == nullptr) return NC_ERR_CUDA;
     g_scratch_ptr[dev] = p;
   }
   *out = g_scratch_ptr[dev];

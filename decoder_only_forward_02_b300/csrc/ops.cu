@@ -11,47 +11,88 @@ int device_sms() {
 }
 
 inline bool al(const void* p, size_t a) { return p != nullptr && reinterpret_cast<uintptr_t>(p) % a == 0; }
-inline nc_status cuda_status(cudaError_t e) { return e == cudaSuccess ? NC_OK : NC_ERR_CUDA; }
+inline bool al_or_null(const void* p, size_t a) { return p == nullptr || reinterpret_cast<uintptr_t>(p) % a == 0; }
+using nc::cuda_status;
 
 }  // namespace
 
 extern "C" {
 
 nc_status nc_op_gemm(const void* A, const void* B, int M, int N, int K, nc_epilogue epi, void* out, int ldo,
-                     const float* resid, float cap, int* status, void* stream) {
+                     const float* ssp, int C, float eps, float cap, int* status, void* stream) {
   if (!al(A, 16) || !al(B, 16) || !al(out, 16) || M < 1 || N < 1 || K < 1 || ldo < N || ldo % 8 != 0)
     return NC_ERR_INVALID_ARG;
+  if (!al_or_null(ssp, 4) || (ssp != nullptr && (C < nc::SS_GROUP || C % nc::SS_GROUP != 0)))
+    return NC_ERR_INVALID_ARG;
   if (K % 64 != 0 || N % 32 != 0) return NC_ERR_UNSUPPORTED;
-  if (epi == NC_EPI_RESID_F32 && !al(resid, 16)) return NC_ERR_INVALID_ARG;
   if (epi == NC_EPI_SOFTCAP_F32 && !(cap > 0.f)) return NC_ERR_INVALID_ARG;
   nc::GemmEpi e;
   switch (epi) {
     case NC_EPI_BF16: e.kind = nc::EPI_BF16; break;
-    case NC_EPI_RESID_F32: e.kind = nc::EPI_RESID_F32; break;
     case NC_EPI_RELU2_BF16: e.kind = nc::EPI_RELU2_BF16; break;
     case NC_EPI_SOFTCAP_F32: e.kind = nc::EPI_SOFTCAP_F32; break;
     default: return NC_ERR_INVALID_ARG;
   }
   e.out = out;
   e.ldo = ldo;
-  e.resid = resid;
-  e.ldr = ldo;
   e.cap = cap;
   e.status = status;
+  if (ssp != nullptr && epi != NC_EPI_BF16) {
+    e.ssp_in = ssp;
+    e.ncg = C / nc::SS_GROUP;
+    e.inv_ncols = 1.0f / static_cast<float>(C);
+    e.eps = eps;
+  }
   return cuda_status(nc::launch_gemm(static_cast<const nc::bf16*>(A), static_cast<const nc::bf16*>(B), M, N, K,
                                      e, device_sms(), static_cast<cudaStream_t>(stream)));
 }
 
-nc_status nc_op_qkv(const void* xn, const void* wqkv, int M, int T, int C, int H, int Hkv, int D,
-                    const float* rope, float eps, const float* gate, const void* ve, const int32_t* tokens, int V,
-                    void* q, void* k, void* v, int* status, void* stream) {
-  if (!al(xn, 16) || !al(wqkv, 16) || !al(rope, 16) || !al(q, 16) || !al(k, 16) || !al(v, 16) || M < 1 ||
-      T < 1 || C < 1 || H < 1 || Hkv < 1 || H % Hkv != 0)
+nc_status nc_op_gemm_residual(const void* A, const void* B, int M, int N, int K, const float* resid, float a,
+                              float b, const float* Y, float* x_out, float* xm_out, void* xb, float* ssp,
+                              const void* wg, int Hkv, int c_g, float* gp, int* status, void* stream) {
+  if (!al(A, 16) || !al(B, 16) || !al(resid, 16) || !al(xb, 16) || !al(ssp, 4) || M < 1 || N < 1 || K < 1)
     return NC_ERR_INVALID_ARG;
-  if (gate != nullptr && (!al(ve, 16) || tokens == nullptr || V < 1)) return NC_ERR_INVALID_ARG;
-  if ((D != 64 && D != 128) || C % 64 != 0) return NC_ERR_UNSUPPORTED;
+  if (!al_or_null(Y, 16) || !al_or_null(x_out, 16) || !al_or_null(xm_out, 16)) return NC_ERR_INVALID_ARG;
+  if (wg != nullptr && (!al(wg, 16) || !al(gp, 4) || Hkv < 1 || c_g < 8 || c_g > N)) return NC_ERR_INVALID_ARG;
+  if (K % 64 != 0 || N % nc::SS_GROUP != 0) return NC_ERR_UNSUPPORTED;
+  if (wg != nullptr && (Hkv > nc::MAX_GATE_HEADS || c_g % 8 != 0)) return NC_ERR_UNSUPPORTED;
+  nc::GemmEpi e;
+  e.kind = nc::EPI_RESID;
+  e.status = status;
+  e.resid = resid;
+  e.a = a;
+  e.b = b;
+  e.Y = Y;
+  e.x_out = x_out;
+  e.xm_out = xm_out;
+  e.xb = static_cast<nc::bf16*>(xb);
+  e.ssp_out = ssp;
+  e.ncg = N / nc::SS_GROUP;
+  if (wg != nullptr) {
+    e.wg = static_cast<const nc::bf16*>(wg);
+    e.Hkv = Hkv;
+    e.c_g = c_g;
+    e.gp_out = gp;
+  }
+  return cuda_status(nc::launch_gemm(static_cast<const nc::bf16*>(A), static_cast<const nc::bf16*>(B), M, N, K,
+                                     e, device_sms(), static_cast<cudaStream_t>(stream)));
+}
+
+nc_status nc_op_qkv(const void* xb, const void* wqkv, int M, int T, int C, int H, int Hkv, int D, const float* rope,
+                    int rope_ld, float eps, const float* ssp, const float* gp, float gate_scale, const void* ve,
+                    const int32_t* tokens, int V, void* q, void* k, void* v, int* status, void* stream) {
+  if (!al(xb, 16) || !al(wqkv, 16) || !al(rope, 16) || !al(q, 16) || !al(k, 16) || !al(v, 16) || !al(ssp, 4) ||
+      M < 1 || T < 1 || C < 1 || H < 1 || Hkv < 1 || H % Hkv != 0 || rope_ld < T)
+    return NC_ERR_INVALID_ARG;
+  if (gp != nullptr && (!al(gp, 4) || !al(ve, 16) || tokens == nullptr || V < 1)) return NC_ERR_INVALID_ARG;
+  if ((D != 64 && D != 128) || C % nc::SS_GROUP != 0) return NC_ERR_UNSUPPORTED;
   nc::GemmEpi e;
   e.kind = nc::EPI_QKV;
+  e.status = status;
+  e.ssp_in = ssp;
+  e.ncg = C / nc::SS_GROUP;
+  e.inv_ncols = 1.0f / static_cast<float>(C);
+  e.eps = eps;
   e.q = static_cast<nc::bf16*>(q);
   e.k = static_cast<nc::bf16*>(k);
   e.v = static_cast<nc::bf16*>(v);
@@ -60,13 +101,13 @@ nc_status nc_op_qkv(const void* xn, const void* wqkv, int M, int T, int C, int H
   e.D = D;
   e.T = T;
   e.rope = reinterpret_cast<const float2*>(rope);
-  e.eps = eps;
-  e.gate = gate;
+  e.rope_ld = rope_ld;
+  e.gp_in = gp;
+  e.gate_scale = gate_scale;
   e.ve = static_cast<const nc::bf16*>(ve);
   e.tokens = tokens;
   e.V = V;
-  e.status = status;
-  return cuda_status(nc::launch_gemm(static_cast<const nc::bf16*>(xn), static_cast<const nc::bf16*>(wqkv), M,
+  return cuda_status(nc::launch_gemm(static_cast<const nc::bf16*>(xb), static_cast<const nc::bf16*>(wqkv), M,
                                      (H + 2 * Hkv) * D, C, e, device_sms(), static_cast<cudaStream_t>(stream)));
 }
 
@@ -87,27 +128,21 @@ nc_status nc_op_attention(const void* q, const void* k, const void* v, int B, in
                                           static_cast<nc::bf16*>(y), status, static_cast<cudaStream_t>(stream)));
 }
 
-nc_status nc_op_rownorm(const float* x, const float* y, float a, float b, float* x_out, void* xn, int M, int C,
-                        float eps, const void* wg, int Hkv, int c_g, float gate_scale, float* gate, void* stream) {
-  if (!al(x, 16) || !al(xn, 16) || M < 1 || C < 1) return NC_ERR_INVALID_ARG;
-  if ((y != nullptr && !al(y, 16)) || (x_out != nullptr && !al(x_out, 16))) return NC_ERR_INVALID_ARG;
-  if (gate != nullptr && (!al(wg, 8) || Hkv < 1 || c_g < 4 || c_g > C)) return NC_ERR_INVALID_ARG;
-  if (C % 128 != 0 || C > 2048 || (gate != nullptr && c_g % 4 != 0)) return NC_ERR_UNSUPPORTED;
-  return cuda_status(nc::launch_rownorm(x, y, a, b, x_out, static_cast<nc::bf16*>(xn), M, C, eps,
-                                        static_cast<const nc::bf16*>(wg), Hkv, c_g, gate_scale, gate,
-                                        static_cast<cudaStream_t>(stream)));
-}
-
 nc_status nc_op_embed_smear(const int32_t* tokens, int B, int T, const void* wte, int V, int C,
-                            const void* smear_gate, int c_s, int embed_norm, float eps, float* x0, int* status,
+                            const void* smear_gate, int c_s, int embed_norm, float eps, float a, float* x0, float* x,
+                            void* xb, float* ssp, const void* wg, int Hkv, int c_g, float* gp, int* status,
                             void* stream) {
-  if (tokens == nullptr || !al(wte, 16) || !al(x0, 16) || B < 1 || T < 1 || V < 1 || C < 1)
+  if (tokens == nullptr || !al(wte, 16) || !al(x0, 16) || !al(x, 16) || !al(xb, 16) || !al(ssp, 4) || B < 1 ||
+      T < 1 || V < 1 || C < 1)
     return NC_ERR_INVALID_ARG;
   if (smear_gate != nullptr && (!al(smear_gate, 8) || c_s < 4 || c_s > C)) return NC_ERR_INVALID_ARG;
-  if (C % 128 != 0 || C > 2048 || (smear_gate != nullptr && c_s % 4 != 0)) return NC_ERR_UNSUPPORTED;
+  if (wg != nullptr && (!al(wg, 8) || !al(gp, 4) || Hkv < 1 || c_g < 4 || c_g > C)) return NC_ERR_INVALID_ARG;
+  if (C % 128 != 0 || C > 2048 || (smear_gate != nullptr && c_s % 4 != 0) || (wg != nullptr && c_g % 4 != 0))
+    return NC_ERR_UNSUPPORTED;
   return cuda_status(nc::launch_embed_smear(tokens, B, T, static_cast<const nc::bf16*>(wte), V, C,
-                                            static_cast<const nc::bf16*>(smear_gate), c_s, embed_norm, eps, x0,
-                                            status, static_cast<cudaStream_t>(stream)));
+                                            static_cast<const nc::bf16*>(smear_gate), c_s, embed_norm, eps, a, x0,
+                                            x, static_cast<nc::bf16*>(xb), ssp, static_cast<const nc::bf16*>(wg),
+                                            Hkv, c_g, gp, status, static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

@@ -1,14 +1,16 @@
-// rowops.cu -- memory-bound per-row kernels: embedding + smear, residual mix + RMSNorm
-// (+ value-embedding gate), and the rotary-angle table.
+// rowops.cu -- memory-bound per-row kernels: the token embedding with smear and the first
+// block's residual mix, and the rotary-angle table.
 //
 // One warp per row, 8 rows per 256-thread block; each lane owns C/128 groups of 4
 // consecutive channels (offset 128*i + 4*lane), so every load and store is a coalesced
-// 128-bit (fp32) or 64-bit (bf16 x4) access; reductions are warp shuffles.
+// 128-bit (fp32) or 64-bit (bf16 x4) access; reductions are warp shuffles.  Group i of a lane
+// is column group i of the row (128 channels), the unit of the partial sums the GEMM
+// epilogues consume.
 //
-// Definitions ("Nanochat在nanoGPT之上的新增功能", section 1 table and notes):
-//   RMSNorm has no learned weight; smear adds sigmoid(gate(x)) times the previous token's
-//   embedding; blocks rescale the residual stream by resid_lambdas and add x0_lambdas * x0;
-//   backout subtracts lambda times the residual cached at mid depth before the final norm.
+// Definitions ("Nanochat在nanoGPT之上的新增功能", section 1 table and notes): smear adds
+// sigmoid(gate(x)) times the previous token's embedding; blocks rescale the residual stream by
+// resid_lambdas and add x0_lambdas * x0 (for the first block x = x0, so x = (l_r + l_0) x0);
+// RMSNorm has no learned weight, and the value-embedding gate reads the normalised block input.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -33,6 +35,8 @@ __device__ __forceinline__ void st_bf16x4(bf16* p, float4 v) {
 
 __device__ __forceinline__ float sigmoidf_(float z) { return 1.0f / (1.0f + expf(-z)); }
 
+__device__ __forceinline__ float dot4(float4 a, float4 b) { return a.x * b.x + a.y * b.y + a.z * b.z + a.w * b.w; }
+
 template <int NV4>
 __device__ __forceinline__ void load_embedding(const bf16* wte, int tok, int V, int lane, bool norm,
                                                float eps, float4 (&e)[NV4]) {
@@ -45,7 +49,7 @@ __device__ __forceinline__ void load_embedding(const bf16* wte, int tok, int V, 
   if (norm) {
     float ss = 0.f;
 #pragma unroll
-    for (int i = 0; i < NV4; ++i) ss += e[i].x * e[i].x + e[i].y * e[i].y + e[i].z * e[i].z + e[i].w * e[i].w;
+    for (int i = 0; i < NV4; ++i) ss += dot4(e[i], e[i]);
     const float r = rsqrtf(warp_sum(ss) * (1.0f / C) + eps);
 #pragma unroll
     for (int i = 0; i < NV4; ++i) {
@@ -58,7 +62,9 @@ template <int NV4>
 __global__ void __launch_bounds__(32 * ROWS_PER_BLOCK)
     embed_smear_kernel(const int32_t* __restrict__ tokens, int M, int T, const bf16* __restrict__ wte,
                        int V, const bf16* __restrict__ smear_gate, int c_s, int embed_norm, float eps,
-                       float* __restrict__ x0, int* status) {
+                       float a, float* __restrict__ x0, float* __restrict__ x, bf16* __restrict__ xb,
+                       float* __restrict__ ssp, const bf16* __restrict__ wg, int Hkv, int c_g,
+                       float* __restrict__ gp, int* status) {
   constexpr int C = NV4 * 128;
   const int lane = threadIdx.x & 31;
   const int row = blockIdx.x * ROWS_PER_BLOCK + (threadIdx.x >> 5);
@@ -73,10 +79,7 @@ __global__ void __launch_bounds__(32 * ROWS_PER_BLOCK)
 #pragma unroll
     for (int i = 0; i < NV4; ++i) {
       const int c = i * 128 + lane * 4;
-      if (c < c_s) {
-        const float4 g = ld_bf16x4(smear_gate + c);
-        dot += e[i].x * g.x + e[i].y * g.y + e[i].z * g.z + e[i].w * g.w;
-      }
+      if (c < c_s) dot += dot4(e[i], ld_bf16x4(smear_gate + c));
     }
     const float gate = sigmoidf_(warp_sum(dot));
     float4 p[NV4];
@@ -89,70 +92,31 @@ __global__ void __launch_bounds__(32 * ROWS_PER_BLOCK)
       e[i].w = fmaf(gate, p[i].w, e[i].w);
     }
   }
-  float* dst = x0 + static_cast<size_t>(row) * C;
-#pragma unroll
-  for (int i = 0; i < NV4; ++i) *reinterpret_cast<float4*>(dst + i * 128 + lane * 4) = e[i];
-}
-
-template <int NV4>
-__global__ void __launch_bounds__(32 * ROWS_PER_BLOCK)
-    rownorm_kernel(const float* x, const float* y, float a, float b,
-                   float* x_out, bf16* __restrict__ xn, int M, float eps, const bf16* __restrict__ wg,
-                   int Hkv, int c_g, float gate_scale, float* __restrict__ gate) {
-  constexpr int C = NV4 * 128;
-  const int lane = threadIdx.x & 31;
-  const int row = blockIdx.x * ROWS_PER_BLOCK + (threadIdx.x >> 5);
-  if (row >= M) return;
   const size_t base = static_cast<size_t>(row) * C;
-  float4 v[NV4];
-  float ss = 0.f;
 #pragma unroll
   for (int i = 0; i < NV4; ++i) {
-    const int c = i * 128 + lane * 4;
-    float4 u = *reinterpret_cast<const float4*>(x + base + c);
-    if (y != nullptr) {
-      const float4 w = *reinterpret_cast<const float4*>(y + base + c);
-      u.x = a * u.x + b * w.x;
-      u.y = a * u.y + b * w.y;
-      u.z = a * u.z + b * w.z;
-      u.w = a * u.w + b * w.w;
-    } else if (a != 1.0f) {
-      u.x *= a; u.y *= a; u.z *= a; u.w *= a;
-    }
-    v[i] = u;
-    ss += u.x * u.x + u.y * u.y + u.z * u.z + u.w * u.w;
-  }
-  if (x_out != nullptr) {
-#pragma unroll
-    for (int i = 0; i < NV4; ++i) *reinterpret_cast<float4*>(x_out + base + i * 128 + lane * 4) = v[i];
-  }
-  const float r = rsqrtf(warp_sum(ss) * (1.0f / C) + eps);
-#pragma unroll
-  for (int i = 0; i < NV4; ++i) {
-    v[i].x *= r; v[i].y *= r; v[i].z *= r; v[i].w *= r;
-    st_bf16x4(xn + base + i * 128 + lane * 4, v[i]);
-  }
-  if (gate != nullptr) {
-    for (int h = 0; h < Hkv; ++h) {
-      float dot = 0.f;
-#pragma unroll
-      for (int i = 0; i < NV4; ++i) {
-        const int c = i * 128 + lane * 4;
-        if (c < c_g) {
-          const float4 g = ld_bf16x4(wg + static_cast<size_t>(h) * c_g + c);
-          dot += v[i].x * g.x + v[i].y * g.y + v[i].z * g.z + v[i].w * g.w;
-        }
+    *reinterpret_cast<float4*>(x0 + base + i * 128 + lane * 4) = e[i];
+    const float4 v = make_float4(a * e[i].x, a * e[i].y, a * e[i].z, a * e[i].w);
+    *reinterpret_cast<float4*>(x + base + i * 128 + lane * 4) = v;
+    st_bf16x4(xb + base + i * 128 + lane * 4, v);
+    const float s = warp_sum(dot4(v, v));
+    if (lane == 0) ssp[static_cast<size_t>(row) * NV4 + i] = s;
+    if (wg != nullptr) {
+      const int c = i * 128 + lane * 4;
+      for (int h = 0; h < Hkv; ++h) {
+        const float d = warp_sum(c < c_g ? dot4(v, ld_bf16x4(wg + static_cast<size_t>(h) * c_g + c)) : 0.f);
+        if (lane == 0) gp[(static_cast<size_t>(row) * Hkv + h) * NV4 + i] = d;
       }
-      dot = warp_sum(dot);
-      if (lane == 0) gate[static_cast<size_t>(row) * Hkv + h] = gate_scale * sigmoidf_(dot);
     }
   }
 }
 
+// table[i * T + t] = (cos, sin)(t * base^(-2i/D)): position fastest, so the threads of a warp
+// (consecutive rows, i.e. consecutive positions) read one contiguous run per pair index i.
 __global__ void rope_table_kernel(float2* table, int T, int half, double base) {
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= T * half) return;
-  const int t = idx / half, i = idx % half;
+  const int i = idx / T, t = idx % T;
   const double inv = pow(base, -2.0 * i / (2.0 * half));
   double s, c;
   sincos(static_cast<double>(t) * inv, &s, &c);
@@ -173,23 +137,12 @@ cudaError_t dispatch_nv4(int C, Args&&... args) {
 template <int NV4>
 struct EmbedLaunch {
   static cudaError_t run(const int32_t* tokens, int M, int T, const bf16* wte, int V,
-                         const bf16* smear_gate, int c_s, int embed_norm, float eps, float* x0,
+                         const bf16* smear_gate, int c_s, int embed_norm, float eps, float a, float* x0,
+                         float* x, bf16* xb, float* ssp, const bf16* wg, int Hkv, int c_g, float* gp,
                          int* status, cudaStream_t stream) {
     const int grid = (M + ROWS_PER_BLOCK - 1) / ROWS_PER_BLOCK;
     embed_smear_kernel<NV4><<<grid, 32 * ROWS_PER_BLOCK, 0, stream>>>(
-        tokens, M, T, wte, V, smear_gate, c_s, embed_norm, eps, x0, status);
-    return cudaGetLastError();
-  }
-};
-
-template <int NV4>
-struct NormLaunch {
-  static cudaError_t run(const float* x, const float* y, float a, float b, float* x_out, bf16* xn,
-                         int M, float eps, const bf16* wg, int Hkv, int c_g, float gate_scale,
-                         float* gate, cudaStream_t stream) {
-    const int grid = (M + ROWS_PER_BLOCK - 1) / ROWS_PER_BLOCK;
-    rownorm_kernel<NV4><<<grid, 32 * ROWS_PER_BLOCK, 0, stream>>>(x, y, a, b, x_out, xn, M, eps, wg,
-                                                                  Hkv, c_g, gate_scale, gate);
+        tokens, M, T, wte, V, smear_gate, c_s, embed_norm, eps, a, x0, x, xb, ssp, wg, Hkv, c_g, gp, status);
     return cudaGetLastError();
   }
 };
@@ -197,19 +150,13 @@ struct NormLaunch {
 }  // namespace
 
 cudaError_t launch_embed_smear(const int32_t* tokens, int B, int T, const bf16* wte, int V, int C,
-                               const bf16* smear_gate, int c_s, int embed_norm, float eps,
-                               float* x0, int* status, cudaStream_t stream) {
-  if (C % 128 != 0 || c_s % 4 != 0) return cudaErrorInvalidValue;
-  return dispatch_nv4<EmbedLaunch>(C, tokens, B * T, T, wte, V, smear_gate, c_s, embed_norm, eps,
-                                   x0, status, stream);
-}
-
-cudaError_t launch_rownorm(const float* x, const float* y, float a, float b, float* x_out, bf16* xn,
-                           int M, int C, float eps, const bf16* wg, int Hkv, int c_g,
-                           float gate_scale, float* gate, cudaStream_t stream) {
-  if (C % 128 != 0 || (gate != nullptr && c_g % 4 != 0)) return cudaErrorInvalidValue;
-  return dispatch_nv4<NormLaunch>(C, x, y, a, b, x_out, xn, M, eps, wg, Hkv, c_g, gate_scale, gate,
-                                  stream);
+                               const bf16* smear_gate, int c_s, int embed_norm, float eps, float a,
+                               float* x0, float* x, bf16* xb, float* ssp, const bf16* wg, int Hkv,
+                               int c_g, float* gp, int* status, cudaStream_t stream) {
+  if (C % 128 != 0 || c_s % 4 != 0 || (wg != nullptr && (c_g % 4 != 0 || gp == nullptr)))
+    return cudaErrorInvalidValue;
+  return dispatch_nv4<EmbedLaunch>(C, tokens, B * T, T, wte, V, smear_gate, c_s, embed_norm, eps, a, x0,
+                                   x, xb, ssp, wg, Hkv, c_g, gp, status, stream);
 }
 
 cudaError_t launch_rope_table(float2* table, int T, int D, float base, cudaStream_t stream) {

@@ -88,7 +88,7 @@ typedef struct {
   int use_backout;
   int embed_norm;             /* RMSNorm the token embedding before smear (default 0) */
   int smear_gate_channels;    /* c_s, 0 = n_embd */
-  int ve_gate_channels;       /* c_g, 0 = n_embd */
+  int ve_gate_channels;       /* c_g, 0 = n_embd; multiple of 8 */
   float ve_gate_scale;        /* default 1 */
   float rms_eps;              /* default 1e-6 */
   float rope_base;            /* default 10000 */
@@ -108,7 +108,7 @@ typedef struct {
   const void *const *wfc;             /* [F, C] */
   const void *const *wproj;           /* [C, F] */
   const void *const *ve_table;        /* [V, Hkv*D] */
-  const void *const *ve_gate;         /* [Hkv, c_g] */
+  const void *const *ve_gate;         /* [Hkv, c_g], 16-byte aligned */
   const void *smear_gate;             /* [c_s]; unused if !use_smear */
   const void *lm_head;                /* [V, C] */
   const float *resid_lambdas;         /* host [n_layer], copied */
@@ -179,6 +179,10 @@ NC_API nc_status nc_get_status(nc_model *m, void *stream);
 
 NC_API const char *nc_status_string(nc_status s);
 
+/* Name of the CUDA runtime error behind the most recent NC_ERR_CUDA returned to the calling
+ * thread by any nc_* call ("cudaSuccess" if there was none).  Host-only. */
+NC_API const char *nc_last_cuda_error(void);
+
 /* Frees host state only (the caller owns every device buffer). */
 NC_API void nc_model_destroy(nc_model *m);
 
@@ -186,15 +190,14 @@ NC_API void nc_model_destroy(nc_model *m);
 
 /* Kernel classes timed when timing is enabled. */
 typedef enum {
-  NC_K_EMBED = 0,     /* embedding gather + smear */
-  NC_K_NORM = 1,      /* residual/x0 mix, backout, RMSNorm -> bf16 (+ VE gate) */
-  NC_K_QKV = 2,       /* q|k|v GEMM with RoPE, QK-norm and value-embedding epilogue */
-  NC_K_ATTN = 3,      /* windowed causal GQA attention */
-  NC_K_OPROJ = 4,     /* attention output projection + residual add */
-  NC_K_FC = 5,        /* MLP up projection + squared ReLU */
-  NC_K_PROJ = 6,      /* MLP down projection + residual add */
-  NC_K_LMHEAD = 7,    /* lm_head GEMM + tanh soft-cap */
-  NC_K_COUNT = 8
+  NC_K_EMBED = 0,     /* embedding gather + smear + first block's residual mix */
+  NC_K_QKV = 1,       /* q|k|v GEMM: input RMSNorm, RoPE, QK-norm, value-embedding gate */
+  NC_K_ATTN = 2,      /* windowed causal GQA attention */
+  NC_K_OPROJ = 3,     /* attention output projection + residual add (+ next norm's inputs) */
+  NC_K_FC = 4,        /* MLP up projection: input RMSNorm + squared ReLU */
+  NC_K_PROJ = 5,      /* MLP down projection + residual add, next block's mix / backout */
+  NC_K_LMHEAD = 6,    /* lm_head GEMM: final RMSNorm + tanh soft-cap */
+  NC_K_COUNT = 7
 } nc_kernel_class;
 
 /* enable != 0: every following nc_forward records an event pair around each

@@ -22,28 +22,47 @@ extern "C" {
 
 typedef enum {
   NC_EPI_BF16 = 0,        /* out bf16 [M, ldo] = acc */
-  NC_EPI_RESID_F32 = 1,   /* out fp32 [M, ldo] = resid + acc; resid may equal out */
-  NC_EPI_RELU2_BF16 = 2,  /* out bf16 = relu(acc)^2     (squared-ReLU row of the feature table) */
-  NC_EPI_SOFTCAP_F32 = 3  /* out fp32 = cap*tanh(acc/cap) (logit soft-cap row of the feature table) */
+  NC_EPI_RELU2_BF16 = 2,  /* out bf16 = relu(rs * acc)^2     (squared-ReLU row of the feature table) */
+  NC_EPI_SOFTCAP_F32 = 3  /* out fp32 = cap*tanh(rs * acc/cap) (logit soft-cap row of the feature table) */
 } nc_epilogue;
 
-/* acc[M, N] = A[M, K] . B[N, K]^T (tcgen05, fp32 accumulation), then the epilogue.
- * K % 64 == 0, N % 32 == 0, ldo >= N, rows 16-byte aligned. */
+/* Partial sums of squares ("ssp"): fp32 [M, C/128]; ssp[m, g] = sum of x[m, c]^2 over the 128
+ * columns c of group g.  A consumer turns them into the RMSNorm row scale
+ * rs[m] = 1 / sqrt(sum_g ssp[m, g] / C + eps), so that norm(x) W^T = rs * (x W^T). */
+
+/* acc[M, N] = A[M, K] . B[N, K]^T (tcgen05, fp32 accumulation), then the epilogue; rs from
+ * `ssp` over C columns (ssp == NULL: rs = 1).  K % 64 == 0, N % 32 == 0, ldo >= N, rows 16-byte
+ * aligned. */
 NC_API nc_status nc_op_gemm(const void *A, const void *B, int M, int N, int K, nc_epilogue epi,
-                            void *out, int ldo, const float *resid, float cap, int *status,
-                            void *stream);
+                            void *out, int ldo, const float *ssp, int C, float eps, float cap,
+                            int *status, void *stream);
 
-/* Packed q|k|v projection of a block: acc = xn[M, C] . wqkv[(H+2Hkv)*D, C]^T, split into
- * q [M, H*D], k [M, Hkv*D], v [M, Hkv*D] (bf16).  q and k: RoPE at position (row % T) from
- * `rope` (fp32 pairs (cos, sin), [>= T][D/2], see nc_op_rope_table), then RMSNorm over each
- * head (eps).  v: if gate != NULL, v += gate[m, g] * ve[tokens[m], g*D:(g+1)*D] (gate fp32
- * [M, Hkv], ve [V, Hkv*D]); out-of-range tokens add nothing. */
-NC_API nc_status nc_op_qkv(const void *xn, const void *wqkv, int M, int T, int C, int H, int Hkv,
-                           int D, const float *rope, float eps, const float *gate, const void *ve,
-                           const int32_t *tokens, int V, void *q, void *k, void *v, int *status,
-                           void *stream);
+/* Residual-stream update of an output projection, N = C columns (C % 128 == 0):
+ *   xr = resid + A . B^T;  xm_out <- xr (if non-NULL);  x' = a * xr + b * Y (Y may be NULL);
+ *   x_out <- x' (if non-NULL; may equal resid);  xb <- bf16(x');  ssp <- partial sums of x'^2;
+ *   if wg != NULL: gp[m, h, g] = sum over group-g columns c < c_g of x'[c] * wg[h, c], h < Hkv
+ *   (gp fp32 [M, Hkv, C/128], wg bf16 [Hkv, c_g] 16-byte aligned, Hkv <= 16, c_g % 8 == 0).
+ * resid, Y, x_out, xm_out fp32 [M, C]; xb bf16 [M, C]. */
+NC_API nc_status nc_op_gemm_residual(const void *A, const void *B, int M, int N, int K,
+                                     const float *resid, float a, float b, const float *Y,
+                                     float *x_out, float *xm_out, void *xb, float *ssp,
+                                     const void *wg, int Hkv, int c_g, float *gp, int *status,
+                                     void *stream);
 
-/* rope[t][i] = (cos, sin)(t * base^(-2i/D)), t < T, i < D/2, fp32 (angles in fp64). */
+/* Packed q|k|v projection of a block: acc = xb[M, C] . wqkv[(H+2Hkv)*D, C]^T scaled by the input
+ * RMSNorm row scale rs (from ssp), split into q [M, H*D], k [M, Hkv*D], v [M, Hkv*D] (bf16).
+ * q and k: RoPE at position (row % T) from `rope` (see nc_op_rope_table; rope_ld = its
+ * position count, >= T), then RMSNorm over each head (eps).  v: if gp != NULL (fp32
+ * [M, Hkv, C/128], see nc_op_gemm_residual), v += gate_scale * sigmoid(rs * sum_g gp[m, g', g])
+ * * ve[tokens[m], g'*D:(g'+1)*D] for kv head g' (ve bf16 [V, Hkv*D]); out-of-range tokens add
+ * nothing. */
+NC_API nc_status nc_op_qkv(const void *xb, const void *wqkv, int M, int T, int C, int H, int Hkv,
+                           int D, const float *rope, int rope_ld, float eps, const float *ssp,
+                           const float *gp, float gate_scale, const void *ve, const int32_t *tokens,
+                           int V, void *q, void *k, void *v, int *status, void *stream);
+
+/* rope[i][t] = (cos, sin)(t * base^(-2i/D)), i < D/2, t < T, fp32 pairs, position fastest
+ * (angles in fp64). */
 NC_API nc_status nc_op_rope_table(float *rope, int T, int D, float base, void *stream);
 
 /* Windowed causal GQA attention: q [B*T, H*D], k, v [B*T, Hkv*D] -> y [B*T, H*D] (bf16);
@@ -51,20 +70,15 @@ NC_API nc_status nc_op_rope_table(float *rope, int T, int D, float base, void *s
 NC_API nc_status nc_op_attention(const void *q, const void *k, const void *v, int B, int T, int H,
                                  int Hkv, int D, int window, void *y, int *status, void *stream);
 
-/* Row kernel: x' = a*x + b*y (y may be NULL: x' = a*x), stored to x_out if non-NULL (may equal
- * x); xn = bf16(x' / sqrt(mean(x'^2) + eps)); if gate != NULL also
- * gate[m, g] = gate_scale * sigmoid(xn32[m, :c_g] . wg[g, :c_g]) (xn32 = unrounded).
- * x, y, x_out fp32 [M, C]; C % 128 == 0; c_g % 4 == 0. */
-NC_API nc_status nc_op_rownorm(const float *x, const float *y, float a, float b, float *x_out,
-                               void *xn, int M, int C, float eps, const void *wg, int Hkv, int c_g,
-                               float gate_scale, float *gate, void *stream);
-
 /* x0[b*T+t] = e_t + sigmoid(e_t[:c_s] . smear_gate) * e_{t-1} (t >= 1, same row b), e = wte[token]
- * (RMS-normalised first if embed_norm); smear_gate NULL = no smear.  Out-of-range tokens give a
- * zero embedding and NC_ERR_TOKEN_RANGE in *status.  x0 fp32 [B*T, C]. */
+ * (RMS-normalised first if embed_norm); smear_gate NULL = no smear.  Then x = a * x0, xb = bf16(x),
+ * ssp = partial sums of x^2 and, if wg != NULL, gp as in nc_op_gemm_residual.  Out-of-range tokens
+ * give a zero embedding and NC_ERR_TOKEN_RANGE in *status.  x0, x fp32 [B*T, C]. */
 NC_API nc_status nc_op_embed_smear(const int32_t *tokens, int B, int T, const void *wte, int V,
                                    int C, const void *smear_gate, int c_s, int embed_norm,
-                                   float eps, float *x0, int *status, void *stream);
+                                   float eps, float a, float *x0, float *x, void *xb, float *ssp,
+                                   const void *wg, int Hkv, int c_g, float *gp, int *status,
+                                   void *stream);
 
 #ifdef __cplusplus
 }

@@ -60,6 +60,7 @@ def test_packed_bytes_formula():
     (dict(vocab_size=32769), 2),
     (dict(smear_gate_channels=6), 2),
     (dict(ve_gate_channels=1000), 1),
+    (dict(ve_gate_channels=12), 2),  # gate rows are read 8 channels at a time
     (dict(n_layer=0, window_left=(), has_ve=()), 1),
 ])
 def test_config_validation(change, code):
@@ -84,12 +85,16 @@ def test_null_arguments_rejected_without_device_work():
     assert lib.nc_forward_launch_count(None) == 0
     lib.nc_model_destroy(None)
     # per-kernel entry points validate before launching
-    assert lib.nc_op_gemm(None, None, 1, 32, 64, 0, None, 32, None, 15.0, None, None) == 1
+    assert lib.nc_op_gemm(None, None, 1, 32, 64, 0, None, 32, None, 0, 1e-6, 15.0, None, None) == 1
+    assert lib.nc_op_gemm_residual(None, None, 1, 128, 64, None, 1.0, 0.0, None, None, None, None, None, None, 0,
+                                   0, None, None, None) == 1
     assert lib.nc_op_attention(None, None, None, 1, 1, 1, 1, 128, -1, None, None, None) == 1
-    assert lib.nc_op_rownorm(None, None, 1.0, 0.0, None, None, 1, 128, 1e-6, None, 0, 0, 1.0, None, None) == 1
     assert lib.nc_op_rope_table(None, 4, 8, 1e4, None) == 1
+    assert lib.nc_op_embed_smear(None, 1, 1, None, 1, 128, None, 0, 0, 1e-6, 1.0, None, None, None, None, None, 0,
+                                 0, None, None, None) == 1
 
 
 def test_kernel_class_names():
     lib = B.lib()
-    assert [lib.nc_kernel_class_name(i).decode() for i in range(8)] == B.KERNEL_CLASSES
+    assert [lib.nc_kernel_class_name(i).decode() for i in range(7)] == B.KERNEL_CLASSES
+    assert lib.nc_kernel_class_name(7) == b"unknown"

@@ -70,6 +70,7 @@ def test_timing_counts_launches(tiny):
     t = m.timing_read()
     L = wl.model.n_layer
     assert t["embed_smear"][1] == 2 and t["lmhead_softcap"][1] == 2
-    assert t["rownorm"][1] == 2 * (2 * L + 1)
+    assert t["qkv_rope_qknorm_ve"][1] == 2 * L and t["proj_residual"][1] == 2 * L
+    assert m.launch_count() == 2 + 5 * L
     assert sum(n for _, n in t.values()) == 2 * m.launch_count()
     assert all(ms >= 0 for ms, _ in t.values())
