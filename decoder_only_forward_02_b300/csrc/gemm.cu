@@ -52,28 +52,43 @@ constexpr int BM = 128;            // rows of A (and of D) held by each CTA of a
 constexpr int PAIR_M = 2 * BM;     // rows of one pair tile
 constexpr int BN = 256;            // columns of one pair tile
 constexpr int B_ROWS = BN / 2;     // rows of B (columns of D) loaded by each CTA
-constexpr int BK = 64, STAGES = 5;
+constexpr int BK = 64;
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = B_ROWS * BK * 2;
 constexpr int NUM_EPI_WARPS = 8;
-constexpr int THREADS = 64 + 32 * NUM_EPI_WARPS;
+constexpr int EPI_WARP0 = 4;                    // epilogue warps 4..11 (warpgroups 1 and 2)
+constexpr int THREADS = 32 * (EPI_WARP0 + NUM_EPI_WARPS);
+// Register split (launch: 384 threads x 168): warpgroup 0 (TMA producer, MMA issuer, two idle
+// warps) drops to 56, the two epilogue warpgroups rise to 224: 128*56 + 256*224 = 384*168.
+constexpr int REGS_CTRL = 56, REGS_EPI = 224;
+static_assert(128 * REGS_CTRL + 256 * REGS_EPI <= THREADS * 168, "register split exceeds the launch allocation");
+constexpr int MAX_NCG = 16;                     // column groups of a row (n_embd <= 2048)
 constexpr uint32_t TMEM_COLS = 2 * BN;
 constexpr int SLAB_BUF = 32 * 128;       // one staging buffer: 32 rows x 128 B
 constexpr int SLAB_BYTES = 2 * SLAB_BUF; // two per epilogue warp, used alternately
+constexpr int GATE_BYTES = MAX_GATE_HEADS * 128 * 2;   // gate weights of one 128-column group (per warp)
 
-struct __align__(8) Ctrl {
-  uint64_t full[STAGES];
-  uint64_t empty[STAGES];
-  uint64_t tfull[2];
-  uint64_t tempty[2];
-  uint64_t drain;
-  uint32_t tmem_base;
-  int abort;
+// The residual-update epilogue (whose K is the long one of the MLP down projection) takes a
+// 4-stage operand ring, and each of its warps keeps its own copy of the gate weights of its
+// column group in shared memory; the other kinds use 5 stages.
+template <int KIND>
+struct Cfg {
+  static constexpr int STAGES = KIND == EPI_RESID ? 4 : 5;
+  static constexpr int OFF_SLAB = STAGES * (A_BYTES + B_BYTES);
+  static constexpr int OFF_GATE = OFF_SLAB + NUM_EPI_WARPS * SLAB_BYTES;
+  static constexpr int OFF_CTRL = OFF_GATE + (KIND == EPI_RESID ? NUM_EPI_WARPS * GATE_BYTES : 0);
+  struct __align__(8) Ctrl {
+    uint64_t full[STAGES];
+    uint64_t empty[STAGES];
+    uint64_t tfull[2];
+    uint64_t tempty[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort;
+  };
+  static constexpr int SMEM_BYTES = 1024 + OFF_CTRL + static_cast<int>(sizeof(Ctrl));
+  static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
-
-constexpr int OFF_SLAB = STAGES * (A_BYTES + B_BYTES);
-constexpr int OFF_CTRL = OFF_SLAB + NUM_EPI_WARPS * SLAB_BYTES;
-constexpr int SMEM_BYTES = 1024 + OFF_CTRL + static_cast<int>(sizeof(Ctrl));
 
 // ---------------------------------------------------------------- staging slabs
 // A buffer holds a [32 rows][128 B] box in the TMA 128-byte swizzle: 16-byte chunk c of row r
@@ -90,6 +105,13 @@ struct Slab {
   uint32_t n;   // stores issued so far (warp-uniform)
 
   __device__ __forceinline__ uint8_t* buf() const { return base + (n & 1u) * SLAB_BUF; }
+  // The buffer the k-th store from now (k = 0 or 1) will be issued from.
+  __device__ __forceinline__ uint8_t* buf_ahead(int k) const { return base + ((n + k) & 1u) * SLAB_BUF; }
+  // Before writing both buffers: every earlier store has finished reading its buffer.
+  __device__ __forceinline__ void acquire_both(int lane) const {
+    if (lane == 0) bulk_wait_read<0>();
+    __syncwarp();
+  }
   // Before writing the current buffer: the store issued from it two stores ago must have
   // finished reading it (the most recent store, from the other buffer, may still run).
   __device__ __forceinline__ void acquire(int lane) const {
@@ -102,15 +124,6 @@ struct Slab {
     __syncwarp();
     if (lane == 0) {
       tma_store_2d(map, base_s + (n & 1u) * SLAB_BUF, x, y);
-      bulk_commit();
-    }
-    ++n;
-  }
-  __device__ __forceinline__ void store_hint(const CUtensorMap* map, int x, int y, int lane, uint64_t policy) {
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) {
-      tma_store_2d_hint(map, base_s + (n & 1u) * SLAB_BUF, x, y, policy);
       bulk_commit();
     }
     ++n;
@@ -160,15 +173,6 @@ __device__ __forceinline__ uint4 pack8_bf16(const float* a) {
   return make_uint4(pack_bf16(a[0], a[1]), pack_bf16(a[2], a[3]), pack_bf16(a[4], a[5]), pack_bf16(a[6], a[7]));
 }
 
-// 1 / rms of row m from its partial sums of squares (1 when no partials are given).
-__device__ __forceinline__ float row_scale(const GemmEpi& ep, int m, int M) {
-  if (ep.ssp_in == nullptr || m >= M) return 1.f;
-  const float* p = ep.ssp_in + static_cast<size_t>(m) * ep.ncg;
-  float ss = 0.f;
-  for (int g = 0; g < ep.ncg; ++g) ss += p[g];
-  return rsqrtf(ss * ep.inv_ncols + ep.eps);
-}
-
 __device__ __forceinline__ float sigmoid_fast(float z) { return 1.0f / (1.0f + __expf(-z)); }
 
 struct OutMaps {
@@ -184,20 +188,29 @@ __device__ __forceinline__ void release_acc(int lane, uint32_t bar) {
 }
 
 // ---------------------------------------------------------------- per-tile prologue
-// Row data an epilogue needs that does not depend on the accumulator: loaded (and the
-// epilogue's global inputs prefetched into L2) before the warp waits for the tile's MMAs, so
-// those latencies overlap the mainloop instead of the epilogue.
+// Row data an epilogue needs that does not depend on the accumulator (the RMSNorm partial sums,
+// the value-embedding gate partials, the token id).  Its loads are issued one tile ahead, while
+// the epilogue of the previous tile runs, and reduced just before the tile's epilogue, so their
+// latency is off the epilogue's critical path.  Residual-update tiles instead prefetch their
+// residual rows into L2 one tile ahead.
+template <int D>
+struct PreRaw {
+  float ss[MAX_NCG];
+  float gp[128 / (D > 0 ? D : 128)][MAX_NCG];
+  int tok;
+};
+
 struct EpiPre {
-  float rs = 1.f;     // input RMSNorm row scale
-  float g[2] = {0.f, 0.f};   // value-embedding gate per head of the column group (EPI_QKV)
-  int tok = -1;       // token id of the row when a gate applies, else -1
+  float rs = 1.f;              // input RMSNorm row scale
+  float g[2] = {0.f, 0.f};     // value-embedding gate per head of the column group (EPI_QKV)
+  int tok = -1;                // token id of the row when a gate applies, else -1
 };
 
 template <int KIND, int D>
-__device__ __forceinline__ EpiPre epi_pre(int lane, int m0w, int n0, int M, int N, const GemmEpi& ep) {
-  EpiPre p;
+__device__ __forceinline__ void pre_issue(PreRaw<D>& raw, int lane, int m0w, int n0, int M, int N,
+                                          const GemmEpi& ep) {
   const int m = m0w + lane;
-  if (n0 >= N || m >= M) return p;
+  if (n0 >= N || m >= M) return;
   if constexpr (KIND == EPI_RESID) {
     const size_t off = static_cast<size_t>(m) * N + n0;
 #pragma unroll
@@ -206,23 +219,59 @@ __device__ __forceinline__ EpiPre epi_pre(int lane, int m0w, int n0, int M, int 
       if (ep.Y != nullptr) prefetch_l2(ep.Y + off + l * 32);
     }
   } else if constexpr (KIND == EPI_RELU2_BF16 || KIND == EPI_SOFTCAP_F32 || KIND == EPI_QKV) {
-    p.rs = row_scale(ep, m, M);
+    if (ep.ssp_in != nullptr) {
+      const float* p = ep.ssp_in + static_cast<size_t>(m) * ep.ncg;
+#pragma unroll
+      for (int g = 0; g < MAX_NCG; ++g)
+        if (g < ep.ncg) raw.ss[g] = p[g];
+    }
     if constexpr (KIND == EPI_QKV) {
-      const int vcol0 = (ep.H + ep.Hkv) * D, kcols = ep.Hkv * D;
+      const int vcol0 = (ep.H + ep.Hkv) * D;
       if (ep.gp_in != nullptr && n0 + 128 > vcol0) {
-        const int tok = ep.tokens[m];
-        p.tok = (tok >= 0 && tok < ep.V) ? tok : -1;
+        raw.tok = ep.tokens[m];
 #pragma unroll
         for (int s = 0; s < 128 / D; ++s) {
           const int c = n0 + s * D;
           if (c < vcol0 || c >= N) continue;
-          const int hv = (c - vcol0) / D;
-          const float* gp = ep.gp_in + (static_cast<size_t>(m) * ep.Hkv + hv) * ep.ncg;
+          const float* gp = ep.gp_in + (static_cast<size_t>(m) * ep.Hkv + (c - vcol0) / D) * ep.ncg;
+#pragma unroll
+          for (int g = 0; g < MAX_NCG; ++g)
+            if (g < ep.ncg) raw.gp[s][g] = gp[g];
+        }
+      }
+    }
+  }
+}
+
+template <int KIND, int D>
+__device__ __forceinline__ EpiPre pre_finish(const PreRaw<D>& raw, int lane, int m0w, int n0, int M, int N,
+                                             const GemmEpi& ep) {
+  EpiPre p;
+  const int m = m0w + lane;
+  if (n0 >= N || m >= M) return p;
+  if constexpr (KIND == EPI_RELU2_BF16 || KIND == EPI_SOFTCAP_F32 || KIND == EPI_QKV) {
+    if (ep.ssp_in != nullptr) {
+      float ss = 0.f;
+#pragma unroll
+      for (int g = 0; g < MAX_NCG; ++g)
+        if (g < ep.ncg) ss += raw.ss[g];
+      p.rs = rsqrtf(ss * ep.inv_ncols + ep.eps);
+    }
+    if constexpr (KIND == EPI_QKV) {
+      const int vcol0 = (ep.H + ep.Hkv) * D, kcols = ep.Hkv * D;
+      if (ep.gp_in != nullptr && n0 + 128 > vcol0) {
+        p.tok = (raw.tok >= 0 && raw.tok < ep.V) ? raw.tok : -1;
+#pragma unroll
+        for (int s = 0; s < 128 / D; ++s) {
+          const int c = n0 + s * D;
+          if (c < vcol0 || c >= N) continue;
           float z = 0.f;
-          for (int i = 0; i < ep.ncg; ++i) z += gp[i];
+#pragma unroll
+          for (int g = 0; g < MAX_NCG; ++g)
+            if (g < ep.ncg) z += raw.gp[s][g];
           p.g[s] = ep.gate_scale * sigmoid_fast(p.rs * z);
           if (p.tok >= 0) {
-            const bf16* row = ep.ve + static_cast<size_t>(p.tok) * kcols + static_cast<size_t>(hv) * D;
+            const bf16* row = ep.ve + static_cast<size_t>(p.tok) * kcols + static_cast<size_t>((c - vcol0) / D) * D;
 #pragma unroll
             for (int l = 0; l < D * 2 / 128; ++l) prefetch_l2(row + l * 64);
           }
@@ -277,8 +326,7 @@ __device__ __forceinline__ void epi_bf16(uint32_t taddr, uint32_t tempty, int la
 
 // cap * tanh(rs * acc / cap), fp32 (logit soft-cap of the lm_head).
 __device__ __forceinline__ void epi_softcap(uint32_t taddr, uint32_t tempty, int lane, int m0w, int n0, int M,
-                                            int N, const GemmEpi& ep, const OutMaps& om, Slab& sl, const EpiPre& pre,
-                                            uint64_t store_policy) {
+                                            int N, const GemmEpi& ep, Slab& sl, const EpiPre& pre) {
   const float cap = ep.cap;
   const float sc = pre.rs / cap;
 #pragma unroll 1
@@ -296,9 +344,20 @@ __device__ __forceinline__ void epi_softcap(uint32_t taddr, uint32_t tempty, int
                         __float_as_uint(cap * tanh_approx(__uint_as_float(r[c * 4 + 2]) * sc)),
                         __float_as_uint(cap * tanh_approx(__uint_as_float(r[c * 4 + 3]) * sc)));
     }
-    sl.acquire(lane);
+    // Through the slab to row-coalesced streaming stores (4 rows x 128 B per instruction):
+    // the logits are written once and never re-read, and leaving them to the load/store unit
+    // keeps the TMA unit free for the operand stream.
+    __syncwarp();
     sl.put_row(lane, o);
-    sl.store_hint(&om.o0, c0, m0w, lane, store_policy);
+    __syncwarp();
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int row = k * 4 + (lane >> 3), q = lane & 7;
+      const uint4 v = *slab_chunk(sl.buf(), row, q);
+      if (m0w + row < M)
+        __stcs(reinterpret_cast<uint4*>(static_cast<float*>(ep.out) + static_cast<size_t>(m0w + row) * ep.ldo + c0 + q * 4),
+               v);
+    }
   }
   release_acc(lane, tempty);
 }
@@ -306,15 +365,27 @@ __device__ __forceinline__ void epi_softcap(uint32_t taddr, uint32_t tempty, int
 // Residual stream update (attention and MLP output projections), with the next consumer's
 // inputs: the bf16 copy of the new stream and its partial sums of squares (the consumer's
 // RMSNorm row scale), and on request the next block's residual mix, the backout cache, the
-// final backout, and the value-embedding gate partial dot products.
+// final backout, and the value-embedding gate partial dot products.  Each warp stages the
+// gate weights of its 128 columns in its own shared buffer (gate_w) once per tile.
 __device__ __forceinline__ void epi_resid(uint32_t taddr, uint32_t tempty, int lane, int m0w, int n0, int M, int N,
-                                          const GemmEpi& ep, const OutMaps& om, Slab& sl, const EpiPre&) {
+                                          const GemmEpi& ep, const OutMaps& om, Slab& sl, bf16* gate_w) {
   if (n0 >= N) {
     release_acc(lane, tempty);
     return;
   }
   const int m = m0w + lane;
   const bool has_gate = ep.wg != nullptr;
+  if (has_gate) {
+    // W_g[:, n0 .. n0+128) (zero past c_g), 16 pieces of 16 B per head row
+    __syncwarp();   // every lane is done with the previous tile's copy
+    for (int i = lane; i < ep.Hkv * 16; i += 32) {
+      const int h = i >> 4, c = n0 + (i & 15) * 8;
+      uint4 w = make_uint4(0u, 0u, 0u, 0u);
+      if (c < ep.c_g) w = __ldg(reinterpret_cast<const uint4*>(ep.wg + static_cast<size_t>(h) * ep.c_g + c));
+      reinterpret_cast<uint4*>(gate_w)[i] = w;
+    }
+    __syncwarp();
+  }
   float ss = 0.f;
   float gacc[MAX_GATE_HEADS];
 #pragma unroll
@@ -335,22 +406,42 @@ __device__ __forceinline__ void epi_resid(uint32_t taddr, uint32_t tempty, int l
     if (ch == 3) release_acc(lane, tempty);
     float x[32];
     sl.acquire(lane);
-    sl.transpose_f32(lane, rv, x);
-#pragma unroll
-    for (int j = 0; j < 32; ++j) x[j] += __uint_as_float(r[j]);
     if (ep.xm_out != nullptr) {   // backout cache: the stream after this block, before mixing
+      sl.transpose_f32(lane, rv, x);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) x[j] += __uint_as_float(r[j]);
       sl.put_row_f32(lane, x);
       sl.store(&om.o1, c0, m0w, lane);
       sl.acquire(lane);
-    }
-    if (ep.Y != nullptr) {
-      float y[32];
-      sl.transpose_f32(lane, yv, y);
+      if (ep.Y != nullptr) {
+        float y[32];
+        sl.transpose_f32(lane, yv, y);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) x[j] = fmaf(ep.a, x[j], ep.b * y[j]);
-    } else if (ep.a != 1.f) {
+        for (int j = 0; j < 32; ++j) x[j] = fmaf(ep.a, x[j], ep.b * y[j]);
+      } else {
 #pragma unroll
-      for (int j = 0; j < 32; ++j) x[j] *= ep.a;
+        for (int j = 0; j < 32; ++j) x[j] *= ep.a;
+      }
+    } else {
+      // x' = a (resid + acc) + b Y: the a resid + b Y part is formed in the loaded layout, so
+      // one transpose serves both inputs
+      if (ep.Y != nullptr) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          rv[k].x = fmaf(ep.a, rv[k].x, ep.b * yv[k].x);
+          rv[k].y = fmaf(ep.a, rv[k].y, ep.b * yv[k].y);
+          rv[k].z = fmaf(ep.a, rv[k].z, ep.b * yv[k].z);
+          rv[k].w = fmaf(ep.a, rv[k].w, ep.b * yv[k].w);
+        }
+      } else if (ep.a != 1.f) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          rv[k].x *= ep.a; rv[k].y *= ep.a; rv[k].z *= ep.a; rv[k].w *= ep.a;
+        }
+      }
+      sl.transpose_f32(lane, rv, x);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) x[j] = fmaf(ep.a, __uint_as_float(r[j]), x[j]);
     }
 #pragma unroll
     for (int j = 0; j < 32; ++j) ss = fmaf(x[j], x[j], ss);
@@ -358,19 +449,17 @@ __device__ __forceinline__ void epi_resid(uint32_t taddr, uint32_t tempty, int l
 #pragma unroll
       for (int h = 0; h < MAX_GATE_HEADS; ++h) {
         if (h < ep.Hkv) {
-          const bf16* w = ep.wg + static_cast<size_t>(h) * ep.c_g + c0;
+          const uint4* w4 = reinterpret_cast<const uint4*>(gate_w + h * 128 + ch * 32);
           float acc = gacc[h];
 #pragma unroll
           for (int q8 = 0; q8 < 4; ++q8) {
-            if (c0 + q8 * 8 < ep.c_g) {
-              const uint4 u = __ldg(reinterpret_cast<const uint4*>(w + q8 * 8));
-              const __nv_bfloat162* w2 = reinterpret_cast<const __nv_bfloat162*>(&u);
+            const uint4 u = w4[q8];
+            const __nv_bfloat162* w2 = reinterpret_cast<const __nv_bfloat162*>(&u);
 #pragma unroll
-              for (int t = 0; t < 4; ++t) {
-                const float2 f = __bfloat1622float2(w2[t]);
-                acc = fmaf(x[q8 * 8 + 2 * t], f.x, acc);
-                acc = fmaf(x[q8 * 8 + 2 * t + 1], f.y, acc);
-              }
+            for (int t = 0; t < 4; ++t) {
+              const float2 f = __bfloat1622float2(w2[t]);
+              acc = fmaf(x[q8 * 8 + 2 * t], f.x, acc);
+              acc = fmaf(x[q8 * 8 + 2 * t + 1], f.y, acc);
             }
           }
           gacc[h] = acc;
@@ -415,14 +504,16 @@ __device__ __forceinline__ void epi_qkv(uint32_t taddr, uint32_t tempty, int lan
   const float rs = pre.rs;
   const int qcols = ep.H * D, kcols = ep.Hkv * D;
   const int pos = m < M ? m % ep.T : 0;
+  // A head is D/64 boxes of [32 rows][64 columns] bf16: results go straight into the staging
+  // buffers (box b in the buffer of the b-th store from now), then the boxes are stored.
 #pragma unroll
   for (int s = 0; s < 128 / D; ++s) {
     const int c = n0 + s * D;
     if (c >= N) break;
     const uint32_t tb = taddr + s * D;
-    uint32_t outp[D / 2];   // the head as packed bf16 pairs
     const CUtensorMap* map;
     int xcol;
+    sl.acquire_both(lane);
     if (c < qcols + kcols) {
       if (c < qcols) {
         map = &om.o0;
@@ -431,6 +522,11 @@ __device__ __forceinline__ void epi_qkv(uint32_t taddr, uint32_t tempty, int lan
         map = &om.o1;
         xcol = c - qcols;
       }
+      // the rotation table rows do not depend on the accumulator: load them first
+      const float2* rope = ep.rope + pos;
+      float2 cs[D / 2];
+#pragma unroll
+      for (int j = 0; j < D / 2; ++j) cs[j] = __ldg(rope + static_cast<size_t>(j) * ep.rope_ld);
       float ss = 0.f;
 #pragma unroll
       for (int ch = 0; ch < D / 32; ++ch) {
@@ -441,25 +537,28 @@ __device__ __forceinline__ void epi_qkv(uint32_t taddr, uint32_t tempty, int lan
         for (int j = 0; j < 32; ++j) ss = fmaf(__uint_as_float(r[j]), __uint_as_float(r[j]), ss);
       }
       const float sc = rs * rsqrtf(rs * rs * ss * (1.0f / D) + ep.eps);
-      const float2* rope = ep.rope + pos;
 #pragma unroll
       for (int hc = 0; hc < D / 64; ++hc) {
         uint32_t lo[32], hi[32];
         tmem_ld32(tb + hc * 32, lo);
         tmem_ld32(tb + D / 2 + hc * 32, hi);
-        float2 cs[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) cs[j] = __ldg(rope + static_cast<size_t>(hc * 32 + j) * ep.rope_ld);
         tmem_ld_wait(lo);
         tmem_ld_wait(hi);
 #pragma unroll
-        for (int j = 0; j < 32; j += 2) {
-          const float a0 = __uint_as_float(lo[j]), b0 = __uint_as_float(hi[j]);
-          const float a1 = __uint_as_float(lo[j + 1]), b1 = __uint_as_float(hi[j + 1]);
-          const float y0 = (a0 * cs[j].x + b0 * cs[j].y) * sc, z0 = (b0 * cs[j].x - a0 * cs[j].y) * sc;
-          const float y1 = (a1 * cs[j + 1].x + b1 * cs[j + 1].y) * sc, z1 = (b1 * cs[j + 1].x - a1 * cs[j + 1].y) * sc;
-          outp[(hc * 32 + j) / 2] = pack_bf16(y0, y1);
-          outp[(D / 2 + hc * 32 + j) / 2] = pack_bf16(z0, z1);
+        for (int j8 = 0; j8 < 32; j8 += 8) {
+          uint32_t py[4], pz[4];
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const int j = j8 + 2 * t;
+            const float2 c0 = cs[hc * 32 + j], c1 = cs[hc * 32 + j + 1];
+            const float a0 = __uint_as_float(lo[j]), b0 = __uint_as_float(hi[j]);
+            const float a1 = __uint_as_float(lo[j + 1]), b1 = __uint_as_float(hi[j + 1]);
+            py[t] = pack_bf16((a0 * c0.x + b0 * c0.y) * sc, (a1 * c1.x + b1 * c1.y) * sc);
+            pz[t] = pack_bf16((b0 * c0.x - a0 * c0.y) * sc, (b1 * c1.x - a1 * c1.y) * sc);
+          }
+          const int cy = hc * 32 + j8, cz = D / 2 + hc * 32 + j8;   // head columns
+          *slab_chunk(sl.buf_ahead(cy / 64), lane, (cy % 64) / 8) = make_uint4(py[0], py[1], py[2], py[3]);
+          *slab_chunk(sl.buf_ahead(cz / 64), lane, (cz % 64) / 8) = make_uint4(pz[0], pz[1], pz[2], pz[3]);
         }
       }
     } else {
@@ -483,35 +582,26 @@ __device__ __forceinline__ void epi_qkv(uint32_t taddr, uint32_t tempty, int lan
 #pragma unroll
         for (int c8 = 0; c8 < 8; ++c8) {
           const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&e[c8]);
+          uint32_t pv[4];
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int idx = c8 * 8 + 2 * j;
-            const float2 f = __bfloat1622float2(h2[j]);
+          for (int t = 0; t < 4; ++t) {
+            const int idx = c8 * 8 + 2 * t;
+            const float2 f = __bfloat1622float2(h2[t]);
             const float v0 = __uint_as_float(idx < 32 ? r0[idx] : r1[idx - 32]);
             const float v1 = __uint_as_float(idx + 1 < 32 ? r0[idx + 1] : r1[idx + 1 - 32]);
-            outp[(cc * 64 + idx) / 2] = pack_bf16(fmaf(g, f.x, v0 * rs), fmaf(g, f.y, v1 * rs));
+            pv[t] = pack_bf16(fmaf(g, f.x, v0 * rs), fmaf(g, f.y, v1 * rs));
           }
+          *slab_chunk(sl.buf_ahead(cc), lane, c8) = make_uint4(pv[0], pv[1], pv[2], pv[3]);
         }
       }
     }
 #pragma unroll
-    for (int cc = 0; cc < D / 64; ++cc) {
-      uint4 o[8];
-#pragma unroll
-      for (int c8 = 0; c8 < 8; ++c8)
-        o[c8] = make_uint4(outp[cc * 32 + 4 * c8], outp[cc * 32 + 4 * c8 + 1], outp[cc * 32 + 4 * c8 + 2],
-                           outp[cc * 32 + 4 * c8 + 3]);
-      sl.acquire(lane);
-      sl.put_row(lane, o);
-      sl.store(map, xcol + cc * 64, m0w, lane);
-    }
+    for (int cc = 0; cc < D / 64; ++cc) sl.store(map, xcol + cc * 64, m0w, lane);
   }
   release_acc(lane, tempty);
 }
 
 template <int KIND, int D>
-// 10 warps spread 3/3/2/2 over the four 16K-register SM sub-partitions: at most 168
-// registers per thread.
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ OutMaps om, int M, int N, int K, int n_fast,
@@ -519,9 +609,11 @@ __global__ void __launch_bounds__(THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
+  using L = Cfg<KIND>;
+  constexpr int STAGES = L::STAGES;
   const uint32_t sA = smem_u32(smem);
   const uint32_t sB = sA + STAGES * A_BYTES;
-  Ctrl* ctl = reinterpret_cast<Ctrl*>(smem + OFF_CTRL);
+  typename L::Ctrl* ctl = reinterpret_cast<typename L::Ctrl*>(smem + L::OFF_CTRL);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();            // 0: pair leader (issues the MMAs)
@@ -557,8 +649,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t tmem = ctl->tmem_base;
   volatile int* abort = &ctl->abort;
 
-  if (warp == 0) {
-    if (lane == 0) {
+  if (warp < EPI_WARP0) {
+    regs_dec<REGS_CTRL>();
+    if (warp == 0 && lane == 0) {
       // The operand shared by the pairs running at the same time is read once per wave; the
       // other one is re-read for every tile of the walk and should stay in L2.
       const uint64_t pol_a = n_fast ? policy_evict_first() : policy_evict_last();
@@ -586,10 +679,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (uint32_t j = (it > STAGES ? it - STAGES : 0); j < it; ++j)
           mbar_wait_cluster(smem_u32(&ctl->full[j % STAGES]), (j / STAGES) & 1, nullptr, status);
       }
-    }
-    __syncwarp();
-  } else if (warp == 1) {
-    if (lane == 0 && rank == 0) {
+    } else if (warp == 1 && lane == 0 && rank == 0) {
       constexpr uint32_t idesc = idesc_bf16_f32(PAIR_M, BN);
       uint32_t it = 0, tc = 0;
       bool ok = true;
@@ -621,25 +711,42 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     __syncwarp();
   } else {
-    const int ew = warp - 2;
-    const int quarter = warp & 3;
+    regs_inc<REGS_EPI>();
+    const int ew = warp - EPI_WARP0;
+    const int quarter = warp & 3;   // TMEM lanes 32*(warp % 4) .. +31 are this warp's
     const int group = ew >> 2;
-    Slab sl{smem + OFF_SLAB + ew * SLAB_BYTES, smem_u32(smem + OFF_SLAB + ew * SLAB_BYTES), 0u};
-    const uint64_t store_policy = policy_evict_first();   // logits are written once, never re-read
+    Slab sl{smem + L::OFF_SLAB + ew * SLAB_BYTES, smem_u32(smem + L::OFF_SLAB + ew * SLAB_BYTES), 0u};
+    bf16* gate_w = reinterpret_cast<bf16*>(smem + L::OFF_GATE + ew * GATE_BYTES);
+    auto coords = [&](int tile, int& m0w, int& n0) {
+      const int mb = n_fast ? tile / num_n : tile % num_m, nb = n_fast ? tile % num_n : tile / num_m;
+      m0w = mb * PAIR_M + static_cast<int>(rank) * BM + quarter * 32;
+      n0 = nb * BN + group * 128;
+    };
+    PreRaw<D> raw;
+    raw.tok = -1;
+    if (pair < num_tiles) {
+      int m0w, n0;
+      coords(pair, m0w, n0);
+      pre_issue<KIND, D>(raw, lane, m0w, n0, M, N, ep);
+    }
     uint32_t tc = 0;
     for (int tile = pair; tile < num_tiles; tile += npairs, ++tc) {
       const uint32_t a = tc & 1, aph = (tc >> 1) & 1;
-      const int mb = n_fast ? tile / num_n : tile % num_m, nb = n_fast ? tile % num_n : tile / num_m;
-      const int m0w = mb * PAIR_M + static_cast<int>(rank) * BM + quarter * 32, n0 = nb * BN + group * 128;
-      const EpiPre pre = epi_pre<KIND, D>(lane, m0w, n0, M, N, ep);
+      int m0w, n0;
+      coords(tile, m0w, n0);
+      const EpiPre pre = pre_finish<KIND, D>(raw, lane, m0w, n0, M, N, ep);
       const bool ok = mbar_wait_cluster(smem_u32(&ctl->tfull[a]), aph, abort, status);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
+      if (tile + npairs < num_tiles) {   // the next tile's row data is in flight during this epilogue
+        int m1, n1;
+        coords(tile + npairs, m1, n1);
+        pre_issue<KIND, D>(raw, lane, m1, n1, M, N, ep);
+      }
       const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + a * BN + group * 128;
       const uint32_t tempty = mapa_shared(smem_u32(&ctl->tempty[a]), 0);
-      if constexpr (KIND == EPI_RESID) epi_resid(taddr, tempty, lane, m0w, n0, M, N, ep, om, sl, pre);
-      else if constexpr (KIND == EPI_SOFTCAP_F32)
-        epi_softcap(taddr, tempty, lane, m0w, n0, M, N, ep, om, sl, pre, store_policy);
+      if constexpr (KIND == EPI_RESID) epi_resid(taddr, tempty, lane, m0w, n0, M, N, ep, om, sl, gate_w);
+      else if constexpr (KIND == EPI_SOFTCAP_F32) epi_softcap(taddr, tempty, lane, m0w, n0, M, N, ep, sl, pre);
       else if constexpr (KIND == EPI_QKV) epi_qkv<D>(taddr, tempty, lane, m0w, n0, M, N, ep, om, sl, pre);
       else epi_bf16<KIND == EPI_RELU2_BF16>(taddr, tempty, lane, m0w, n0, M, N, ep, om, sl, pre);
     }
@@ -668,12 +775,13 @@ cudaError_t launch_kind(const CUtensorMap& ta, const CUtensorMap& tb, const OutM
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.blockDim = dim3(THREADS);
-  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.dynamicSmemBytes = Cfg<KIND>::SMEM_BYTES;
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   std::call_once(once, [&] {
-    attr_err = cudaFuncSetAttribute(gemm_tc_kernel<KIND, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    attr_err = cudaFuncSetAttribute(gemm_tc_kernel<KIND, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    Cfg<KIND>::SMEM_BYTES);
     if (attr_err != cudaSuccess) return;
     cudaLaunchConfig_t q = cfg;
     q.gridDim = dim3(2 * (num_sms / 2));
@@ -715,8 +823,8 @@ cudaError_t launch_gemm(const bf16* A, const bf16* B, int M, int N, int K, const
       if (ok) ok = make_tmap_bf16_2d(&om.o2, epi.xb, N, Mu, static_cast<uint64_t>(N) * 2, 64, 32);
       break;
     }
-    case EPI_SOFTCAP_F32:
-      ok = make_tmap_2d(&om.o0, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, epi.out, N, Mu, static_cast<uint64_t>(epi.ldo) * 4, 32, 32);
+    case EPI_SOFTCAP_F32:   // written with plain coalesced stores (16-byte aligned rows)
+      ok = (reinterpret_cast<uintptr_t>(epi.out) % 16 == 0) && epi.ldo % 4 == 0;
       break;
     case EPI_BF16:
     case EPI_RELU2_BF16:

@@ -407,6 +407,19 @@ __device__ __forceinline__ void umma_commit_pair(uint32_t bar, uint16_t cta_mask
       : "memory");
 }
 
+// ---------------------------------------------------------------- register reallocation
+
+// Warpgroup-wide change of the per-thread register budget (all 128 threads execute it).  The
+// decreases and increases of a CTA must add up to its launch-time allocation.
+template <int N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(N) : "memory");
+}
+template <int N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(N) : "memory");
+}
+
 // ---------------------------------------------------------------- small helpers
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
