@@ -204,34 +204,51 @@ __global__ void __launch_bounds__(THREADS, 2)
       if (lane == 0) mbar_arrive(smem_u32(&ctl->s_free));
 
       const int key0 = (j0 + j) * BKV;
-      const int kmin = window < 0 ? 0 : i - window;
+      // Tiles inside every row's visible range need no per-element mask: the last key is at
+      // most the first query, the tile lies inside the sequence, and (with a window) its first
+      // key is within the window of the last query.  The test is the same for the whole CTA.
+      const bool interior = key0 + BKV - 1 <= q0 && key0 + BKV <= T &&
+                            (window < 0 || key0 >= q0 + BQ - 1 - window);
       float s[BKV];
-      float mt = -INFINITY;
+      if (interior) {
 #pragma unroll
-      for (int c = 0; c < BKV; ++c) {
-        const int key = key0 + c;
-        const bool vis = key <= i && key < T && key >= kmin;
-        const float v = __uint_as_float(c < 32 ? r0[c] : r1[c - 32]);
-        s[c] = vis ? v : -INFINITY;
-        mt = fmaxf(mt, s[c]);
+        for (int c = 0; c < BKV; ++c) s[c] = __uint_as_float(c < 32 ? r0[c] : r1[c - 32]);
+      } else {
+        const int kmin = window < 0 ? 0 : i - window;
+        const int kmax = min(i, T - 1);
+#pragma unroll
+        for (int c = 0; c < BKV; ++c) {
+          const int key = key0 + c;
+          const float v = __uint_as_float(c < 32 ? r0[c] : r1[c - 32]);
+          s[c] = (key <= kmax && key >= kmin) ? v : -INFINITY;
+        }
       }
+      // row max as 8 independent chains and a 3-level tree
+      float mx[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) mx[q] = s[q];
+#pragma unroll
+      for (int c = 8; c < BKV; ++c) mx[c & 7] = fmaxf(mx[c & 7], s[c]);
+      const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
       float alpha = 1.f;
       bool resc = false;
       if (mt > m_run + thr) {
-        alpha = exp2f((m_run - mt) * scale_log2);   // 0 when m_run = -inf
+        alpha = ex2_approx((m_run - mt) * scale_log2);   // 0 when m_run = -inf
         resc = m_run != -INFINITY;
         m_run = mt;
       }
       const float negm = (m_run == -INFINITY) ? 0.f : -m_run * scale_log2;
       uint32_t pk[BKV / 2];
-      float sum = 0.f;
+      float ps[4] = {0.f, 0.f, 0.f, 0.f};   // 4 independent partial sums
 #pragma unroll
       for (int c = 0; c < BKV; c += 2) {
-        const float p0 = exp2f(fmaf(s[c], scale_log2, negm));
-        const float p1 = exp2f(fmaf(s[c + 1], scale_log2, negm));
-        sum += p0 + p1;
+        const float p0 = ex2_approx(fmaf(s[c], scale_log2, negm));
+        const float p1 = ex2_approx(fmaf(s[c + 1], scale_log2, negm));
+        ps[(c >> 1) & 3] += p0 + p1;
         pk[c / 2] = pack_bf16(p0, p1);
       }
+      const float sum = (ps[0] + ps[1]) + (ps[2] + ps[3]);
       l_run = l_run * alpha + sum;
 
       if (j > 0) {   // P V of the previous tile must be done before P and O are touched

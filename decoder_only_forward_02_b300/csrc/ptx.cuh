@@ -427,6 +427,13 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// Hardware 2^x approximation (one MUFU operation; subnormal results flush to zero).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Hardware tanh approximation (one MUFU operation).
 __device__ __forceinline__ float tanh_approx(float x) {
   float y;
