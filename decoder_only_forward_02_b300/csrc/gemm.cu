@@ -68,14 +68,20 @@ constexpr int SLAB_BUF = 32 * 128;       // one staging buffer: 32 rows x 128 B
 constexpr int SLAB_BYTES = 2 * SLAB_BUF; // two per epilogue warp, used alternately
 constexpr int GATE_BYTES = MAX_GATE_HEADS * 128 * 2;   // gate weights of one 128-column group (per warp)
 
+// Shared memory per epilogue kind.  Kinds whose epilogue stores with TMA keep two staging
+// buffers per warp (a store drains from one while the next is filled); the squared-ReLU and
+// soft-cap epilogues store row-coalesced from one buffer, and the space saved deepens their
+// operand ring to 6 stages (their K is short, so operand latency is what starves the MMA).
 // The residual-update epilogue (whose K is the long one of the MLP down projection) takes a
-// 4-stage operand ring, and each of its warps keeps its own copy of the gate weights of its
-// column group in shared memory; the other kinds use 5 stages.
+// 4-stage ring, and each of its warps keeps its own copy of the gate weights of its column
+// group in shared memory.
 template <int KIND>
 struct Cfg {
-  static constexpr int STAGES = KIND == EPI_RESID ? 4 : 5;
+  static constexpr bool LSU_STORE = KIND == EPI_RELU2_BF16 || KIND == EPI_SOFTCAP_F32;
+  static constexpr int STAGES = KIND == EPI_RESID ? 4 : (LSU_STORE ? 6 : 5);
+  static constexpr int SLAB_WARP = LSU_STORE ? SLAB_BUF : SLAB_BYTES;   // staging bytes per warp
   static constexpr int OFF_SLAB = STAGES * (A_BYTES + B_BYTES);
-  static constexpr int OFF_GATE = OFF_SLAB + NUM_EPI_WARPS * SLAB_BYTES;
+  static constexpr int OFF_GATE = OFF_SLAB + NUM_EPI_WARPS * SLAB_WARP;
   static constexpr int OFF_CTRL = OFF_GATE + (KIND == EPI_RESID ? NUM_EPI_WARPS * GATE_BYTES : 0);
   struct __align__(8) Ctrl {
     uint64_t full[STAGES];
@@ -187,6 +193,20 @@ __device__ __forceinline__ void release_acc(int lane, uint32_t bar) {
   if (lane == 0) mbar_arrive_cluster(bar);
 }
 
+// ---------------------------------------------------------------- tile order
+// Pair tiles are walked in groups of `grp` row blocks: inside a group the row block is the
+// fastest index, then the column block.  grp = 1 walks the column blocks of one row block
+// together (the pairs of a wave share a row block of A); grp = num_m walks the row blocks of one
+// column block together (they share a block of B); a value in between shares B among grp pairs
+// and keeps the concurrently written output rows grp blocks tall.
+__device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int grp, int& mb, int& nb) {
+  const int per_group = grp * num_n;
+  const int group = tile / per_group, local = tile % per_group;
+  const int rows = min(grp, num_m - group * grp);   // the last group may be shorter
+  mb = group * grp + local % rows;
+  nb = local / rows;
+}
+
 // ---------------------------------------------------------------- per-tile prologue
 // Row data an epilogue needs that does not depend on the accumulator (the RMSNorm partial sums,
 // the value-embedding gate partials, the token id).  Its loads are issued one tile ahead, while
@@ -287,7 +307,26 @@ __device__ __forceinline__ EpiPre pre_finish(const PreRaw<D>& raw, int lane, int
 // [n0, n0 + 128) at TMEM address taddr (lane quarter applied).  Each releases the accumulator
 // after its last tcgen05.ld.
 
-// Plain bf16 store, or relu(rs * acc)^2 (MLP up projection, squared ReLU).
+// Row-coalesced stores of the staged [32 rows][128 B] box to rows m0w.. of `out` (row pitch
+// ld_bytes), starting at byte column col_bytes; rows at or beyond M are skipped.  Streaming
+// (evict-first) stores when `stream` is set.
+__device__ __forceinline__ void lsu_store_box(const uint8_t* buf, void* out, size_t ld_bytes, int m0w, size_t col_bytes,
+                                              int M, int lane, bool stream) {
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const int row = k * 4 + (lane >> 3), q = lane & 7;
+    const uint4 v = *slab_chunk(const_cast<uint8_t*>(buf), row, q);
+    if (m0w + row < M) {
+      uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(out) + static_cast<size_t>(m0w + row) * ld_bytes +
+                                            col_bytes + q * 16);
+      if (stream) __stcs(dst, v);
+      else *dst = v;
+    }
+  }
+}
+
+// Plain bf16 store (TMA), or relu(rs * acc)^2 (MLP up projection, squared ReLU; row-coalesced
+// stores from the single staging buffer).
 template <bool RELU2>
 __device__ __forceinline__ void epi_bf16(uint32_t taddr, uint32_t tempty, int lane, int m0w, int n0, int M, int N,
                                          const GemmEpi& ep, const OutMaps& om, Slab& sl, const EpiPre& pre) {
@@ -317,9 +356,27 @@ __device__ __forceinline__ void epi_bf16(uint32_t taddr, uint32_t tempty, int la
       }
       o[c] = pack8_bf16(a);
     }
-    sl.acquire(lane);
-    sl.put_row(lane, o);
-    sl.store(&om.o0, c0, m0w, lane);
+    if constexpr (RELU2) {
+      __syncwarp();   // every lane is done reading the previous box
+      sl.put_row(lane, o);
+      __syncwarp();
+      if (c0 + 64 <= N) {
+        lsu_store_box(sl.buf(), ep.out, static_cast<size_t>(ep.ldo) * 2, m0w, static_cast<size_t>(c0) * 2, M, lane,
+                      false);
+      } else {   // ragged last box: 32 valid columns (N % 32 == 0)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int row = k * 4 + (lane >> 3), q = lane & 7;
+          const uint4 v = *slab_chunk(sl.buf(), row, q);
+          if (m0w + row < M && c0 + q * 8 < N)
+            *reinterpret_cast<uint4*>(static_cast<bf16*>(ep.out) + static_cast<size_t>(m0w + row) * ep.ldo + c0 + q * 8) = v;
+        }
+      }
+    } else {
+      sl.acquire(lane);
+      sl.put_row(lane, o);
+      sl.store(&om.o0, c0, m0w, lane);
+    }
   }
   release_acc(lane, tempty);
 }
@@ -344,20 +401,13 @@ __device__ __forceinline__ void epi_softcap(uint32_t taddr, uint32_t tempty, int
                         __float_as_uint(cap * tanh_approx(__uint_as_float(r[c * 4 + 2]) * sc)),
                         __float_as_uint(cap * tanh_approx(__uint_as_float(r[c * 4 + 3]) * sc)));
     }
-    // Through the slab to row-coalesced streaming stores (4 rows x 128 B per instruction):
-    // the logits are written once and never re-read, and leaving them to the load/store unit
-    // keeps the TMA unit free for the operand stream.
+    // Through the staging buffer to row-coalesced streaming stores (4 rows x 128 B per
+    // instruction): the logits are written once and never re-read, and leaving them to the
+    // load/store unit keeps the TMA unit free for the operand stream.
     __syncwarp();
     sl.put_row(lane, o);
     __syncwarp();
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const int row = k * 4 + (lane >> 3), q = lane & 7;
-      const uint4 v = *slab_chunk(sl.buf(), row, q);
-      if (m0w + row < M)
-        __stcs(reinterpret_cast<uint4*>(static_cast<float*>(ep.out) + static_cast<size_t>(m0w + row) * ep.ldo + c0 + q * 4),
-               v);
-    }
+    lsu_store_box(sl.buf(), ep.out, static_cast<size_t>(ep.ldo) * 4, m0w, static_cast<size_t>(c0) * 4, M, lane, true);
   }
   release_acc(lane, tempty);
 }
@@ -604,7 +654,7 @@ __device__ __forceinline__ void epi_qkv(uint32_t taddr, uint32_t tempty, int lan
 template <int KIND, int D>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ OutMaps om, int M, int N, int K, int n_fast,
+                   const __grid_constant__ OutMaps om, int M, int N, int K, int grp,
                    const __grid_constant__ GemmEpi ep) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -654,12 +704,14 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (warp == 0 && lane == 0) {
       // The operand shared by the pairs running at the same time is read once per wave; the
       // other one is re-read for every tile of the walk and should stay in L2.
-      const uint64_t pol_a = n_fast ? policy_evict_first() : policy_evict_last();
-      const uint64_t pol_b = n_fast ? policy_evict_last() : policy_evict_first();
+      const bool share_a = grp == 1;
+      const uint64_t pol_a = share_a ? policy_evict_first() : policy_evict_last();
+      const uint64_t pol_b = share_a ? policy_evict_last() : policy_evict_first();
       uint32_t it = 0;
       bool ok = true;
       for (int tile = pair; tile < num_tiles && ok; tile += npairs) {
-        const int mb = n_fast ? tile / num_n : tile % num_m, nb = n_fast ? tile % num_n : tile / num_m;
+        int mb, nb;
+        tile_coords(tile, num_m, num_n, grp, mb, nb);
         for (int kb = 0; kb < kblocks; ++kb) {
           const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
           if (!mbar_wait_cluster(smem_u32(&ctl->empty[s]), ph ^ 1, abort, status)) {
@@ -715,10 +767,11 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int ew = warp - EPI_WARP0;
     const int quarter = warp & 3;   // TMEM lanes 32*(warp % 4) .. +31 are this warp's
     const int group = ew >> 2;
-    Slab sl{smem + L::OFF_SLAB + ew * SLAB_BYTES, smem_u32(smem + L::OFF_SLAB + ew * SLAB_BYTES), 0u};
+    Slab sl{smem + L::OFF_SLAB + ew * L::SLAB_WARP, smem_u32(smem + L::OFF_SLAB + ew * L::SLAB_WARP), 0u};
     bf16* gate_w = reinterpret_cast<bf16*>(smem + L::OFF_GATE + ew * GATE_BYTES);
     auto coords = [&](int tile, int& m0w, int& n0) {
-      const int mb = n_fast ? tile / num_n : tile % num_m, nb = n_fast ? tile % num_n : tile / num_m;
+      int mb, nb;
+      tile_coords(tile, num_m, num_n, grp, mb, nb);
       m0w = mb * PAIR_M + static_cast<int>(rank) * BM + quarter * 32;
       n0 = nb * BN + group * 128;
     };
@@ -792,10 +845,12 @@ cudaError_t launch_kind(const CUtensorMap& ta, const CUtensorMap& tb, const OutM
   const int tiles = ((M + PAIR_M - 1) / PAIR_M) * ((N + BN - 1) / BN);
   const int pairs = tiles < max_pairs ? tiles : max_pairs;
   cfg.gridDim = dim3(2 * pairs);
-  // Walk the column blocks fastest when A is the larger operand (the pairs of a wave then
-  // share one row block of A), the row blocks fastest otherwise (they share a block of B).
-  const int n_fast = M >= N ? 1 : 0;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<KIND, D>, ta, tb, om, M, N, K, n_fast, epi);
+  // When A is the larger operand the pairs of a wave share its row block (grp = 1); otherwise
+  // (the lm_head) they share a block of B (grp = every row block: on the d12 lm_head this beats
+  // groups of 8 row blocks, whose B tiles are re-read 8 times as often).
+  const int num_m = (M + PAIR_M - 1) / PAIR_M;
+  const int grp = M >= N ? 1 : num_m;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<KIND, D>, ta, tb, om, M, N, K, grp, epi);
   if (e != cudaSuccess) cudaGetLastError();   // a failed launch must not resurface in a later call
   return e;
 }
@@ -827,8 +882,10 @@ cudaError_t launch_gemm(const bf16* A, const bf16* B, int M, int N, int K, const
       ok = (reinterpret_cast<uintptr_t>(epi.out) % 16 == 0) && epi.ldo % 4 == 0;
       break;
     case EPI_BF16:
-    case EPI_RELU2_BF16:
       ok = make_tmap_bf16_2d(&om.o0, epi.out, N, Mu, static_cast<uint64_t>(epi.ldo) * 2, 64, 32);
+      break;
+    case EPI_RELU2_BF16:   // row-coalesced plain stores (16-byte aligned rows)
+      ok = (reinterpret_cast<uintptr_t>(epi.out) % 16 == 0) && epi.ldo % 8 == 0;
       break;
     case EPI_QKV: {
       const uint64_t qc = static_cast<uint64_t>(epi.H) * epi.D, kc = static_cast<uint64_t>(epi.Hkv) * epi.D;
