@@ -9,18 +9,29 @@
 // the reference's Blackwell path falls back to an attention without windows, so windows there
 // cost full causal work; here key tiles outside the window are never loaded.
 //
-// One CTA per (128-query tile, head, batch row), two CTAs per SM (112 KB shared memory and
-// 256 TMEM columns each).  Heaviest query tiles are dispatched first.
-//   warp 0      TMA: Q tile once, then 64-key K and V tiles into a 2-stage ring.
-//   warp 1      TMEM allocation; one lane issues S = Q K^T (128 x 64, fp32 in TMEM) and
-//               O += P V (128 x D, fp32 in TMEM; V read MN-major straight from its
-//               token-major layout).
-//   warps 2..5  softmax, one thread per query row: read its S row from TMEM, mask (causal,
-//               window, sequence end), online softmax in base 2 with the scale folded into
-//               one FMA, P as bf16 into a 128-byte-swizzled shared tile (the A operand of
-//               P V).  The running max moves only when a row's max grows by more than 2^8;
-//               only then is that row of O rescaled in TMEM (after the previous P V is done).
+// One CTA per (pair of 128-query tiles, head, batch row), one CTA per SM; heaviest pairs first.
+// Key tiles are 128 keys wide, so every tensor-core step is a full-rate 128 x 128 (x 16) or
+// 128 x D (x 16) MMA.  The two query tiles (Q0: rows q0..q0+127, Q1: the next 128 rows) walk
+// the same key tiles; a query tile skips the key tiles it does not see.
+//   tensor memory (512 columns): S_k for query tile k at columns 128k (fp32 scores); softmax k
+//               overwrites the first 64 of them with P_k (bf16, two per column), which the
+//               P V step reads as its A operand straight from tensor memory; O_k at 256 + k*D.
+//   warp 0      TMA: Q0 and Q1 once, then K and V tiles (128 keys) into a 2-stage ring.
+//   warp 1      TMEM allocation; one lane issues, for each key tile j:
+//                 O_0 += P_0(j) V(j), S_0(j+1) = Q_0 K(j+1)^T, O_1 += P_1(j) V(j), S_1(j+1) ...
+//               so that while softmax 0 works on its scores the tensor core runs query tile 1's
+//               steps and the other way round.  Tensor-core operations issued by one thread run
+//               in issue order, so S_k(j+1) overwrites P_k(j) only after O_k += P_k(j) V(j) has
+//               read it, and the completion of S_k(j+1) also tells softmax k that O_k is stable.
+//   warps 4..7  softmax of Q0, warps 8..11 softmax of Q1, one thread per query row: load the
+//               128 scores of its row, mask only on key tiles that cross the diagonal, the
+//               window edge or the sequence end, online softmax in base 2 (scale folded into one
+//               FMA, hardware exp2), P to tensor memory in two halves of 64 keys (the P V step
+//               of the first half starts while the second is computed).  The running max moves
+//               only when a row's max grows by more than 2^8; only then is that row of O
+//               rescaled.
 //               Final: O / l -> bf16 -> y.
+//   warps 2, 3  idle.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -29,35 +40,61 @@
 namespace nc {
 namespace {
 
-constexpr int BQ = 128, BKV = 64, STAGES = 2, THREADS = 192;
-constexpr uint32_t TMEM_COLS = 256;   // S: columns [0, 64); O: [64, 64 + D)
+constexpr int BQ = 128, BKV = 128, STAGES = 2;
+constexpr int SM_WARP0 = 4;                    // softmax warps 4..11
+constexpr int THREADS = 32 * (SM_WARP0 + 8);
+constexpr uint32_t TMEM_COLS = 512;
+constexpr int REGS_CTRL = 56, REGS_SOFTMAX = 224;   // 128*56 + 256*224 = 384*168
+static_assert(128 * REGS_CTRL + 256 * REGS_SOFTMAX <= THREADS * 168, "register split exceeds the launch");
 
 struct __align__(8) AttnCtrl {
   uint64_t q_full;
   uint64_t kv_full[STAGES];
   uint64_t kv_empty[STAGES];
-  uint64_t s_full, s_free, p_full, o_done, drain;
+  uint64_t s_full[2];   // S_k(j) (and every earlier tensor-core step) complete
+  uint64_t p_full[2][2];   // softmax k wrote keys [64 h, 64 h + 64) of P_k(j)  ([k][h])
+  uint64_t o_done[2];   // O_k final (its last P V step complete)
+  uint64_t drain;
   uint32_t tmem_base;
   int abort;
 };
 
 template <int D>
 struct Lay {
-  static constexpr int Q_BOX = BQ * 64 * 2;     // [128 rows][64 d] bf16, 16 KB
-  static constexpr int KV_BOX = BKV * 64 * 2;   // [64 keys][64 d] bf16, 8 KB
-  static constexpr int NB = D / 64;             // boxes along d
-  static constexpr int Q_BYTES = NB * Q_BOX;
+  static constexpr int Q_BOX = BQ * 64 * 2;      // [128 rows][64 d] bf16, 16 KB
+  static constexpr int KV_BOX = BKV * 64 * 2;    // [128 keys][64 d] bf16, 16 KB
+  static constexpr int NB = D / 64;              // boxes along d
+  static constexpr int Q_BYTES = NB * Q_BOX;     // one query tile
   static constexpr int K_BYTES = NB * KV_BOX;
-  static constexpr int P_BYTES = BQ * BKV * 2;  // [128 rows][64 keys] bf16, 16 KB
-  static constexpr int OFF_P = Q_BYTES;
-  static constexpr int OFF_KV = OFF_P + P_BYTES;
+  static constexpr int OFF_KV = 2 * Q_BYTES;
   static constexpr int STAGE_BYTES = 2 * K_BYTES;  // K then V
   static constexpr int OFF_CTRL = OFF_KV + STAGES * STAGE_BYTES;
   static constexpr int TOTAL = OFF_CTRL + 256;
+  static_assert(TOTAL <= 232448, "shared memory");
 };
 
+// Key-tile range [lo, hi] (128-key tiles) of query tile rows [q0, q0 + 127] (rows < T).
+__device__ __forceinline__ void key_tiles(int q0, int T, int window, int& lo, int& hi) {
+  lo = window < 0 ? 0 : max(0, q0 - window) / BKV;
+  hi = min(q0 + BQ - 1, T - 1) / BKV;
+}
+
+// 32 lanes x 32 consecutive 32-bit columns from registers (tcgen05.st.32x32b.x32).
+__device__ __forceinline__ void tmem_st32_u(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]),
+      "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]),
+      "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]),
+      "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+
 template <int D>
-__global__ void __launch_bounds__(THREADS, 2)
+__global__ void __launch_bounds__(THREADS, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, int T, int H, int Hkv, int B, int window,
                    float scale_log2, bf16* __restrict__ y, int* status) {
@@ -68,20 +105,21 @@ __global__ void __launch_bounds__(THREADS, 2)
     return;
   }
   AttnCtrl* ctl = reinterpret_cast<AttnCtrl*>(smem + L::OFF_CTRL);
-  const uint32_t sQ = smem_u32(smem), sP = sQ + L::OFF_P, sKV = sQ + L::OFF_KV;
+  const uint32_t sQ = smem_u32(smem), sKV = sQ + L::OFF_KV;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int HB = H * B;
-  const int nq = (T + BQ - 1) / BQ;
-  const int qt = nq - 1 - static_cast<int>(blockIdx.x) / HB;   // heaviest tiles first
+  const int npair = (T + 2 * BQ - 1) / (2 * BQ);
+  const int pr = npair - 1 - static_cast<int>(blockIdx.x) / HB;   // heaviest pairs first
   const int hb = static_cast<int>(blockIdx.x) % HB;
   const int h = hb % H, b = hb / H;
   const int g = h / (H / Hkv);
-  const int q0 = qt * BQ;
-  const int q_last = min(q0 + BQ - 1, T - 1);
-  const int k_lo = window < 0 ? 0 : max(0, q0 - window);
-  const int j0 = k_lo / BKV;
-  const int n = q_last / BKV - j0 + 1;
+  const int qbase = pr * 2 * BQ;
+  const bool has_q1 = qbase + BQ < T;
+  int lo0, hi0, lo1 = 1, hi1 = 0;   // Q1's range is empty unless it exists
+  key_tiles(qbase, T, window, lo0, hi0);
+  if (has_q1) key_tiles(qbase + BQ, T, window, lo1, hi1);
+  const int jlo = lo0, jhi = has_q1 ? hi1 : hi0;   // lo0 <= lo1 and hi0 <= hi1
 
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&ctl->q_full), 1);
@@ -89,10 +127,12 @@ __global__ void __launch_bounds__(THREADS, 2)
       mbar_init(smem_u32(&ctl->kv_full[s]), 1);
       mbar_init(smem_u32(&ctl->kv_empty[s]), 1);
     }
-    mbar_init(smem_u32(&ctl->s_full), 1);
-    mbar_init(smem_u32(&ctl->s_free), 4);
-    mbar_init(smem_u32(&ctl->p_full), 4);
-    mbar_init(smem_u32(&ctl->o_done), 1);
+    for (int k = 0; k < 2; ++k) {
+      mbar_init(smem_u32(&ctl->s_full[k]), 1);
+      mbar_init(smem_u32(&ctl->p_full[k][0]), 4);
+      mbar_init(smem_u32(&ctl->p_full[k][1]), 4);
+      mbar_init(smem_u32(&ctl->o_done[k]), 1);
+    }
     mbar_init(smem_u32(&ctl->drain), 1);
     ctl->abort = 0;
     fence_mbar_init();
@@ -105,26 +145,28 @@ __global__ void __launch_bounds__(THREADS, 2)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
-  const uint32_t tS = tmem, tO = tmem + BKV;
   volatile int* abort = &ctl->abort;
 
-  if (warp == 0) {
-    if (lane == 0) {
+  if (warp < SM_WARP0) {
+    regs_dec<REGS_CTRL>();
+    if (warp == 0 && lane == 0) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
       const uint32_t qb = smem_u32(&ctl->q_full);
-      mbar_arrive_expect_tx(qb, L::Q_BYTES);
+      mbar_arrive_expect_tx(qb, (has_q1 ? 2 : 1) * L::Q_BYTES);
 #pragma unroll
-      for (int c = 0; c < L::NB; ++c) tma_load_2d(sQ + c * L::Q_BOX, &tmQ, qb, h * D + c * 64, b * T + q0);
+      for (int c = 0; c < L::NB; ++c) {
+        tma_load_2d(sQ + c * L::Q_BOX, &tmQ, qb, h * D + c * 64, b * T + qbase);
+        if (has_q1) tma_load_2d(sQ + L::Q_BYTES + c * L::Q_BOX, &tmQ, qb, h * D + c * 64, b * T + qbase + BQ);
+      }
       int issued = 0;
-      for (int j = 0; j < n; ++j) {
-        const int s = j % STAGES;
-        const uint32_t ph = (j / STAGES) & 1;
-        if (!mbar_wait(smem_u32(&ctl->kv_empty[s]), ph ^ 1, abort, status)) break;
+      for (int j = jlo; j <= jhi; ++j) {
+        const int jj = j - jlo, s = jj % STAGES;
+        if (!mbar_wait(smem_u32(&ctl->kv_empty[s]), ((jj / STAGES) & 1) ^ 1, abort, status)) break;
         const uint32_t fb = smem_u32(&ctl->kv_full[s]);
         mbar_arrive_expect_tx(fb, L::STAGE_BYTES);
-        const int row = b * T + (j0 + j) * BKV;
+        const int row = b * T + j * BKV;
         const uint32_t sK = sKV + s * L::STAGE_BYTES, sV = sK + L::K_BYTES;
 #pragma unroll
         for (int c = 0; c < L::NB; ++c) {
@@ -135,100 +177,134 @@ __global__ void __launch_bounds__(THREADS, 2)
       }
       // every issued copy must land before the CTA may exit
       mbar_wait(qb, 0, nullptr, status);
-      for (int j = (issued > STAGES ? issued - STAGES : 0); j < issued; ++j)
-        mbar_wait(smem_u32(&ctl->kv_full[j % STAGES]), (j / STAGES) & 1, nullptr, status);
-    }
-    __syncwarp();
-  } else if (warp == 1) {
-    if (lane == 0) {
+      for (int jj = (issued > STAGES ? issued - STAGES : 0); jj < issued; ++jj)
+        mbar_wait(smem_u32(&ctl->kv_full[jj % STAGES]), (jj / STAGES) & 1, nullptr, status);
+    } else if (warp == 1 && lane == 0) {
       constexpr uint32_t idS = idesc_bf16_f32(BQ, BKV);
       constexpr uint32_t idO = idesc_bf16_f32_bmn(BQ, D);
+      const int lo[2] = {lo0, lo1}, hi[2] = {hi0, hi1};
       bool ok = mbar_wait(smem_u32(&ctl->q_full), 0, abort, status);
-      auto issue_s = [&](int j) -> bool {
-        const int s = j % STAGES;
-        if (!mbar_wait(smem_u32(&ctl->kv_full[s]), (j / STAGES) & 1, abort, status)) return false;
+      auto kv_ready = [&](int j) -> bool {
+        const int jj = j - jlo;
+        if (!mbar_wait(smem_u32(&ctl->kv_full[jj % STAGES]), (jj / STAGES) & 1, abort, status)) return false;
         tc_fence_after();
-        const uint32_t sK = sKV + s * L::STAGE_BYTES;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t a = sdesc_kmajor_sw128(sQ + (kk / 4) * L::Q_BOX + (kk % 4) * 32);
-          const uint64_t bd = sdesc_kmajor_sw128(sK + (kk / 4) * L::KV_BOX + (kk % 4) * 32);
-          umma_bf16(tS, a, bd, idS, kk > 0 ? 1u : 0u);
-        }
-        umma_commit(smem_u32(&ctl->s_full));
         return true;
       };
-      if (ok) ok = issue_s(0);
-      for (int j = 0; j < n && ok; ++j) {
-        if (j + 1 < n) {
-          if (!mbar_wait(smem_u32(&ctl->s_free), j & 1, abort, status)) break;
-          tc_fence_after();
-          if (!issue_s(j + 1)) break;
-        }
-        if (!mbar_wait(smem_u32(&ctl->p_full), j & 1, abort, status)) break;
-        tc_fence_after();
-        const int s = j % STAGES;
-        const uint32_t sV = sKV + s * L::STAGE_BYTES + L::K_BYTES;
+      auto issue_s = [&](int k, int j) {
+        const uint32_t sK = sKV + ((j - jlo) % STAGES) * L::STAGE_BYTES;
+        const uint32_t qk = sQ + k * L::Q_BYTES;
 #pragma unroll
-        for (int kk = 0; kk < BKV / 16; ++kk) {
-          const uint64_t a = sdesc_kmajor_sw128(sP + kk * 32);
-          const uint64_t bd = sdesc_mnmajor_sw128(sV + kk * 16 * 128, L::KV_BOX);
-          umma_bf16(tO, a, bd, idO, (j > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t a = sdesc_kmajor_sw128(qk + (kk / 4) * L::Q_BOX + (kk % 4) * 32);
+          const uint64_t bd = sdesc_kmajor_sw128(sK + (kk / 4) * L::KV_BOX + (kk % 4) * 32);
+          umma_bf16(tmem + 128 * k, a, bd, idS, kk > 0 ? 1u : 0u);
         }
-        umma_commit(smem_u32(&ctl->o_done));
-        umma_commit(smem_u32(&ctl->kv_empty[s]));
+        umma_commit(smem_u32(&ctl->s_full[k]));
+      };
+      if (ok) ok = kv_ready(jlo);
+      if (ok) {
+        for (int k = 0; k < 2; ++k)
+          if (jlo >= lo[k] && jlo <= hi[k]) issue_s(k, jlo);
+      }
+      for (int j = jlo; j <= jhi && ok; ++j) {
+        const uint32_t sV = sKV + ((j - jlo) % STAGES) * L::STAGE_BYTES + L::K_BYTES;
+        bool next_ready = false;
+#pragma unroll
+        for (int k = 0; k < 2 && ok; ++k) {
+          if (j >= lo[k] && j <= hi[k]) {
+            // P V in two halves of 64 keys: the first half runs while softmax k still
+            // computes the second
+#pragma unroll
+            for (int ph = 0; ph < 2; ++ph) {
+              if (!mbar_wait(smem_u32(&ctl->p_full[k][ph]), (j - lo[k]) & 1, abort, status)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+#pragma unroll
+              for (int kk = 4 * ph; kk < 4 * ph + 4; ++kk) {
+                const uint64_t bd = sdesc_mnmajor_sw128(sV + kk * 16 * 128, L::KV_BOX);
+                umma_bf16_ts(tmem + 256 + k * D, tmem + 128 * k + kk * 8, bd, idO, (j > lo[k] || kk > 0) ? 1u : 0u);
+              }
+            }
+            if (!ok) break;
+            if (j == hi[k]) umma_commit(smem_u32(&ctl->o_done[k]));   // O_k final
+          }
+          if (j + 1 <= jhi && j + 1 >= lo[k] && j + 1 <= hi[k]) {
+            if (!next_ready) {
+              if (!kv_ready(j + 1)) {
+                ok = false;
+                break;
+              }
+              next_ready = true;
+            }
+            issue_s(k, j + 1);
+          }
+        }
+        if (ok) umma_commit(smem_u32(&ctl->kv_empty[(j - jlo) % STAGES]));
       }
       umma_commit(smem_u32(&ctl->drain));
       mbar_wait(smem_u32(&ctl->drain), 0, nullptr, status);
     }
     __syncwarp();
   } else {
-    const int quarter = warp & 3;
+    regs_inc<REGS_SOFTMAX>();
+    const int k = (warp - SM_WARP0) >> 2;   // query tile of this warpgroup
+    const int quarter = warp & 3;          // TMEM lanes 32*(warp % 4) .. +31
     const int row = quarter * 32 + lane;
+    const int q0 = qbase + k * BQ;
     const int i = q0 + row;
+    const int lo = k == 0 ? lo0 : lo1, hi = k == 0 ? hi0 : hi1;
+    const int nk = hi - lo + 1;   // 0 when the CTA has no second query tile
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t tS = tmem + 128 * k + lane_off, tO = tmem + 256 + k * D + lane_off;
     const float thr = 8.0f / scale_log2;   // raw-score growth that triggers a rescale (2^8)
+    const int kmin = window < 0 ? 0 : i - window;
+    const int kmax = min(i, T - 1);
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
-    for (int j = 0; j < n; ++j) {
-      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl->s_full), j & 1, abort, status));
+    for (int t = 0; t < nk; ++t) {
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl->s_full[k]), t & 1, abort, status));
       if (!ok) break;
       tc_fence_after();
-      uint32_t r0[32], r1[32];
-      tmem_ld32(tS + lane_off, r0);
-      tmem_ld32(tS + lane_off + 32, r1);
-      tmem_ld_wait(r0);
-      tmem_ld_wait(r1);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&ctl->s_free));
-
-      const int key0 = (j0 + j) * BKV;
+      float sv[BKV];
+      {
+        uint32_t r0[32], r1[32], r2[32], r3[32];
+        tmem_ld32(tS, r0);
+        tmem_ld32(tS + 32, r1);
+        tmem_ld32(tS + 64, r2);
+        tmem_ld32(tS + 96, r3);
+        tmem_ld_wait(r0);
+        tmem_ld_wait(r1);
+        tmem_ld_wait(r2);
+        tmem_ld_wait(r3);
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          sv[c] = __uint_as_float(r0[c]);
+          sv[32 + c] = __uint_as_float(r1[c]);
+          sv[64 + c] = __uint_as_float(r2[c]);
+          sv[96 + c] = __uint_as_float(r3[c]);
+        }
+      }
+      const int key0 = (lo + t) * BKV;
       // Tiles inside every row's visible range need no per-element mask: the last key is at
       // most the first query, the tile lies inside the sequence, and (with a window) its first
-      // key is within the window of the last query.  The test is the same for the whole CTA.
+      // key is within the window of the last query.  The test is the same for the warpgroup.
       const bool interior = key0 + BKV - 1 <= q0 && key0 + BKV <= T &&
                             (window < 0 || key0 >= q0 + BQ - 1 - window);
-      float s[BKV];
-      if (interior) {
-#pragma unroll
-        for (int c = 0; c < BKV; ++c) s[c] = __uint_as_float(c < 32 ? r0[c] : r1[c - 32]);
-      } else {
-        const int kmin = window < 0 ? 0 : i - window;
-        const int kmax = min(i, T - 1);
+      if (!interior) {
 #pragma unroll
         for (int c = 0; c < BKV; ++c) {
           const int key = key0 + c;
-          const float v = __uint_as_float(c < 32 ? r0[c] : r1[c - 32]);
-          s[c] = (key <= kmax && key >= kmin) ? v : -INFINITY;
+          sv[c] = (key <= kmax && key >= kmin) ? sv[c] : -INFINITY;
         }
       }
       // row max as 8 independent chains and a 3-level tree
       float mx[8];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) mx[q] = s[q];
+      for (int q = 0; q < 8; ++q) mx[q] = sv[q];
 #pragma unroll
-      for (int c = 8; c < BKV; ++c) mx[c & 7] = fmaxf(mx[c & 7], s[c]);
+      for (int c = 8; c < BKV; ++c) mx[c & 7] = fmaxf(mx[c & 7], sv[c]);
       const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                              fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
       float alpha = 1.f;
@@ -239,56 +315,48 @@ __global__ void __launch_bounds__(THREADS, 2)
         m_run = mt;
       }
       const float negm = (m_run == -INFINITY) ? 0.f : -m_run * scale_log2;
-      uint32_t pk[BKV / 2];
-      float ps[4] = {0.f, 0.f, 0.f, 0.f};   // 4 independent partial sums
-#pragma unroll
-      for (int c = 0; c < BKV; c += 2) {
-        const float p0 = ex2_approx(fmaf(s[c], scale_log2, negm));
-        const float p1 = ex2_approx(fmaf(s[c + 1], scale_log2, negm));
-        ps[(c >> 1) & 3] += p0 + p1;
-        pk[c / 2] = pack_bf16(p0, p1);
-      }
-      const float sum = (ps[0] + ps[1]) + (ps[2] + ps[3]);
-      l_run = l_run * alpha + sum;
-
-      if (j > 0) {   // P V of the previous tile must be done before P and O are touched
-        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl->o_done), (j - 1) & 1, abort, status));
-        if (!ok) break;
-        tc_fence_after();
-      }
+      // S_k(j) complete implies O_k += P_k(j-1) V(j-1) complete: O_k may be rescaled now.
       if (__any_sync(0xffffffffu, resc)) {
         const float a = resc ? alpha : 1.f;
 #pragma unroll 1
         for (int ch = 0; ch < D / 32; ++ch) {
           uint32_t o[32];
-          tmem_ld32(tO + lane_off + ch * 32, o);
+          tmem_ld32(tO + ch * 32, o);
           tmem_ld_wait(o);
 #pragma unroll
           for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * a);
-          tmem_st32(tO + lane_off + ch * 32, o);
+          tmem_st32(tO + ch * 32, o);
         }
         tmem_st_wait();
       }
-      uint8_t* prow = smem + L::OFF_P + row * 128;
+      float ps[4] = {0.f, 0.f, 0.f, 0.f};   // 4 independent partial sums
 #pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
-        const uint4 v = make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
-        *reinterpret_cast<uint4*>(prow + ((ch ^ (row & 7)) << 4)) = v;
+      for (int half = 0; half < 2; ++half) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int c = 0; c < 64; c += 2) {
+          const float p0 = ex2_approx(fmaf(sv[half * 64 + c], scale_log2, negm));
+          const float p1 = ex2_approx(fmaf(sv[half * 64 + c + 1], scale_log2, negm));
+          ps[(c >> 1) & 3] += p0 + p1;
+          pk[c / 2] = pack_bf16(p0, p1);
+        }
+        tmem_st32_u(tS + half * 32, pk);   // keys 64 half .. 64 half + 63 -> columns 32 half ..
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&ctl->p_full[k][half]));
       }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&ctl->p_full));
+      l_run = l_run * alpha + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
     }
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl->o_done), (n - 1) & 1, abort, status));
-    if (ok) {
+    if (ok && nk > 0) ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl->o_done[k]), 0, abort, status));
+    if (ok && nk > 0) {
       tc_fence_after();
       const float inv = 1.f / l_run;
       bf16* dst = y + (static_cast<size_t>(b) * T + i) * (static_cast<size_t>(H) * D) + h * D;
 #pragma unroll 1
       for (int ch = 0; ch < D / 32; ++ch) {
         uint32_t o[32];
-        tmem_ld32(tO + lane_off + ch * 32, o);
+        tmem_ld32(tO + ch * 32, o);
         tmem_ld_wait(o);
         if (i < T) {
 #pragma unroll
@@ -326,10 +394,10 @@ cudaError_t launch_d(const bf16* q, const bf16* k, const bf16* v, int B, int T, 
       !make_tmap_bf16_2d(&tk, k, static_cast<uint64_t>(Hkv) * D, M, static_cast<uint64_t>(Hkv) * D * 2, 64, BKV) ||
       !make_tmap_bf16_2d(&tv, v, static_cast<uint64_t>(Hkv) * D, M, static_cast<uint64_t>(Hkv) * D * 2, 64, BKV))
     return cudaErrorInvalidValue;
-  const int nq = (T + BQ - 1) / BQ;
+  const int npair = (T + 2 * BQ - 1) / (2 * BQ);
   const float scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
-  attn_tc_kernel<D><<<nq * H * B, THREADS, Lt::TOTAL, stream>>>(tq, tk, tv, T, H, Hkv, B, window, scale_log2, y,
-                                                                 status);
+  attn_tc_kernel<D><<<npair * H * B, THREADS, Lt::TOTAL, stream>>>(tq, tk, tv, T, H, Hkv, B, window, scale_log2, y,
+                                                                    status);
   return cudaGetLastError();
 }
 
