@@ -144,6 +144,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  griddep_wait();     // the previous kernel's outputs are complete and visible
+  griddep_launch();
   const uint32_t tmem = ctl->tmem_base;
   volatile int* abort = &ctl->abort;
 
@@ -396,9 +398,18 @@ cudaError_t launch_d(const bf16* q, const bf16* k, const bf16* v, int B, int T, 
     return cudaErrorInvalidValue;
   const int npair = (T + 2 * BQ - 1) / (2 * BQ);
   const float scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
-  attn_tc_kernel<D><<<npair * H * B, THREADS, Lt::TOTAL, stream>>>(tq, tk, tv, T, H, Hkv, B, window, scale_log2, y,
-                                                                    status);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute lattr[1] = {pdl_attribute()};
+  cfg.gridDim = dim3(npair * H * B);
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = Lt::TOTAL;
+  cfg.stream = stream;
+  cfg.attrs = lattr;
+  cfg.numAttrs = 1;
+  const cudaError_t e =
+      cudaLaunchKernelEx(&cfg, attn_tc_kernel<D>, tq, tk, tv, T, H, Hkv, B, window, scale_log2, y, status);
+  if (e != cudaSuccess) cudaGetLastError();
+  return e;
 }
 
 }  // namespace

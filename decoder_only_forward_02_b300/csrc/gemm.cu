@@ -696,6 +696,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   tc_fence_before();
   cluster_sync();   // barriers of both CTAs initialised, TMEM allocated
   tc_fence_after();
+  griddep_wait();     // the previous kernel's outputs are complete and visible
+  griddep_launch();
   const uint32_t tmem = ctl->tmem_base;
   volatile int* abort = &ctl->abort;
 
@@ -822,16 +824,17 @@ cudaError_t launch_kind(const CUtensorMap& ta, const CUtensorMap& tb, const OutM
   static cudaError_t attr_err = cudaSuccess;
   static int max_pairs = 0;
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1] = pdl_attribute();
   cfg.blockDim = dim3(THREADS);
   cfg.dynamicSmemBytes = Cfg<KIND>::SMEM_BYTES;
   cfg.stream = stream;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 1;   // occupancy query without the PDL attribute
   std::call_once(once, [&] {
     attr_err = cudaFuncSetAttribute(gemm_tc_kernel<KIND, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     Cfg<KIND>::SMEM_BYTES);
@@ -850,6 +853,7 @@ cudaError_t launch_kind(const CUtensorMap& ta, const CUtensorMap& tb, const OutM
   // groups of 8 row blocks, whose B tiles are re-read 8 times as often).
   const int num_m = (M + PAIR_M - 1) / PAIR_M;
   const int grp = M >= N ? 1 : num_m;
+  cfg.numAttrs = 2;
   const cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<KIND, D>, ta, tb, om, M, N, K, grp, epi);
   if (e != cudaSuccess) cudaGetLastError();   // a failed launch must not resurface in a later call
   return e;

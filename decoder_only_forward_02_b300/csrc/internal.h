@@ -77,6 +77,15 @@ constexpr int MAX_GATE_HEADS = 16;
 nc_status cuda_status(cudaError_t e);
 const char* last_cuda_error_name();
 
+// Launch attribute that lets a kernel's CTAs start while the previous kernel on the stream
+// drains (each kernel waits for its predecessor before touching memory: griddep_wait()).
+inline cudaLaunchAttribute pdl_attribute() {
+  cudaLaunchAttribute a;
+  a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  a.val.programmaticStreamSerializationAllowed = 1;
+  return a;
+}
+
 // Encodes a 2-D TMA descriptor with 128-byte swizzling through the driver entry point
 // (no link-time libcuda).  inner/outer are extents in elements, row stride in bytes.
 bool make_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* ptr, uint64_t inner,

@@ -420,6 +420,14 @@ __device__ __forceinline__ void umma_commit_pair(uint32_t bar, uint16_t cta_mask
       : "memory");
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+// Kernels are launched so that the next kernel's CTAs may start while this one drains.  Every
+// kernel calls griddep_wait() before its first global-memory access (read or write): it returns
+// once the preceding kernel has completed and its writes are visible, so the order of the whole
+// launch sequence is kept.  griddep_launch() lets the next kernel's CTAs be scheduled.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---------------------------------------------------------------- register reallocation
 
 // Warpgroup-wide change of the per-thread register budget (all 128 threads execute it).  The

@@ -66,6 +66,8 @@ __global__ void __launch_bounds__(32 * ROWS_PER_BLOCK)
                        float* __restrict__ ssp, const bf16* __restrict__ wg, int Hkv, int c_g,
                        float* __restrict__ gp, int* status) {
   constexpr int C = NV4 * 128;
+  griddep_wait();   // the previous kernel on the stream (still reading xb, ssp, ...) has completed
+  griddep_launch();
   const int lane = threadIdx.x & 31;
   const int row = blockIdx.x * ROWS_PER_BLOCK + (threadIdx.x >> 5);
   if (row >= M) return;
@@ -140,10 +142,17 @@ struct EmbedLaunch {
                          const bf16* smear_gate, int c_s, int embed_norm, float eps, float a, float* x0,
                          float* x, bf16* xb, float* ssp, const bf16* wg, int Hkv, int c_g, float* gp,
                          int* status, cudaStream_t stream) {
-    const int grid = (M + ROWS_PER_BLOCK - 1) / ROWS_PER_BLOCK;
-    embed_smear_kernel<NV4><<<grid, 32 * ROWS_PER_BLOCK, 0, stream>>>(
-        tokens, M, T, wte, V, smear_gate, c_s, embed_norm, eps, a, x0, x, xb, ssp, wg, Hkv, c_g, gp, status);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1] = {pdl_attribute()};
+    cfg.gridDim = dim3((M + ROWS_PER_BLOCK - 1) / ROWS_PER_BLOCK);
+    cfg.blockDim = dim3(32 * ROWS_PER_BLOCK);
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, embed_smear_kernel<NV4>, tokens, M, T, wte, V, smear_gate, c_s,
+                                             embed_norm, eps, a, x0, x, xb, ssp, wg, Hkv, c_g, gp, status);
+    if (e != cudaSuccess) cudaGetLastError();
+    return e;
   }
 };
 
