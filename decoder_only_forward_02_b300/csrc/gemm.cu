@@ -199,7 +199,12 @@ __device__ __forceinline__ void release_acc(int lane, uint32_t bar) {
 // together (the pairs of a wave share a row block of A); grp = num_m walks the row blocks of one
 // column block together (they share a block of B); a value in between shares B among grp pairs
 // and keeps the concurrently written output rows grp blocks tall.
+// A negative grp walks the same order backwards (last tile first), with group size -grp.
 __device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int grp, int& mb, int& nb) {
+  if (grp < 0) {
+    tile = num_m * num_n - 1 - tile;
+    grp = -grp;
+  }
   const int per_group = grp * num_n;
   const int group = tile / per_group, local = tile % per_group;
   const int rows = min(grp, num_m - group * grp);   // the last group may be shorter
@@ -706,7 +711,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (warp == 0 && lane == 0) {
       // The operand shared by the pairs running at the same time is read once per wave; the
       // other one is re-read for every tile of the walk and should stay in L2.
-      const bool share_a = grp == 1;
+      const bool share_a = grp == 1 || grp == -1;
       const uint64_t pol_a = share_a ? policy_evict_first() : policy_evict_last();
       const uint64_t pol_b = share_a ? policy_evict_last() : policy_evict_first();
       uint32_t it = 0;
@@ -852,7 +857,10 @@ cudaError_t launch_kind(const CUtensorMap& ta, const CUtensorMap& tb, const OutM
   // (the lm_head) they share a block of B (grp = every row block: on the d12 lm_head this beats
   // groups of 8 row blocks, whose B tiles are re-read 8 times as often).
   const int num_m = (M + PAIR_M - 1) / PAIR_M;
-  const int grp = M >= N ? 1 : num_m;
+  int grp = M >= N ? 1 : num_m;
+  // The MLP down projection reads h, which the up projection has just written in ascending row
+  // order: walking its tiles backwards starts on the rows most likely still in L2.
+  if (KIND == EPI_RESID && K > 1024) grp = -grp;
   cfg.numAttrs = 2;
   const cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<KIND, D>, ta, tb, om, M, N, K, grp, epi);
   if (e != cudaSuccess) cudaGetLastError();   // a failed launch must not resurface in a later call
