@@ -44,11 +44,12 @@ constexpr int BQ = 128, BKV = 128, STAGES = 2;
 constexpr int SM_WARP0 = 4;                    // softmax warps 4..11
 constexpr int THREADS = 32 * (SM_WARP0 + 8);
 constexpr uint32_t TMEM_COLS = 512;
-constexpr int REGS_CTRL = 56, REGS_SOFTMAX = 224;   // 128*56 + 256*224 = 384*168
+constexpr int REGS_CTRL = 88, REGS_SOFTMAX = 200;   // 128*88 + 256*200 <= 384*168
 static_assert(128 * REGS_CTRL + 256 * REGS_SOFTMAX <= THREADS * 168, "register split exceeds the launch");
 
 struct __align__(8) AttnCtrl {
   uint64_t q_full;
+  uint64_t q_empty;     // the last S MMA of an item has run: its Q tiles may be replaced
   uint64_t kv_full[STAGES];
   uint64_t kv_empty[STAGES];
   uint64_t s_full[2];   // S_k(j) (and every earlier tensor-core step) complete
@@ -93,11 +94,43 @@ __device__ __forceinline__ void tmem_st32_u(uint32_t taddr, const uint32_t* r) {
       : "memory");
 }
 
+// One work item: a pair of query tiles of one (batch row, head).  Items are numbered heaviest
+// first (the pair index descends).  CTA c of G takes, in round r, item r*G + c when r is even and
+// r*G + G-1-c when r is odd: the heaviest items of one round meet the lightest of the next, which
+// evens out causal work (whose items shrink with the pair index).
+__device__ __forceinline__ int item_index(int c, int r, int G) { return r * G + ((r & 1) ? G - 1 - c : c); }
+
+struct Item {
+  int b, h, g, qbase;
+  bool has_q1;
+  int lo0, hi0, lo1, hi1, jlo, jhi;
+};
+
+__device__ __forceinline__ Item decode_item(int it, int T, int H, int Hkv, int B, int window) {
+  Item w;
+  const int HB = H * B;
+  const int npair = (T + 2 * BQ - 1) / (2 * BQ);
+  const int pr = npair - 1 - it / HB;
+  const int hb = it % HB;
+  w.h = hb % H;
+  w.b = hb / H;
+  w.g = w.h / (H / Hkv);
+  w.qbase = pr * 2 * BQ;
+  w.has_q1 = w.qbase + BQ < T;
+  w.lo1 = 1;
+  w.hi1 = 0;   // Q1's range is empty unless it exists
+  key_tiles(w.qbase, T, window, w.lo0, w.hi0);
+  if (w.has_q1) key_tiles(w.qbase + BQ, T, window, w.lo1, w.hi1);
+  w.jlo = w.lo0;
+  w.jhi = w.has_q1 ? w.hi1 : w.hi0;   // lo0 <= lo1 and hi0 <= hi1
+  return w;
+}
+
 template <int D>
 __global__ void __launch_bounds__(THREADS, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, int T, int H, int Hkv, int B, int window,
-                   float scale_log2, bf16* __restrict__ y, int* status) {
+                   int num_items, float scale_log2, bf16* __restrict__ y, int* status) {
   using L = Lay<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   if ((smem_u32(smem) & 1023u) != 0) {   // swizzled tiles need 1024-byte alignment
@@ -106,23 +139,12 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
   AttnCtrl* ctl = reinterpret_cast<AttnCtrl*>(smem + L::OFF_CTRL);
   const uint32_t sQ = smem_u32(smem), sKV = sQ + L::OFF_KV;
-
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int HB = H * B;
-  const int npair = (T + 2 * BQ - 1) / (2 * BQ);
-  const int pr = npair - 1 - static_cast<int>(blockIdx.x) / HB;   // heaviest pairs first
-  const int hb = static_cast<int>(blockIdx.x) % HB;
-  const int h = hb % H, b = hb / H;
-  const int g = h / (H / Hkv);
-  const int qbase = pr * 2 * BQ;
-  const bool has_q1 = qbase + BQ < T;
-  int lo0, hi0, lo1 = 1, hi1 = 0;   // Q1's range is empty unless it exists
-  key_tiles(qbase, T, window, lo0, hi0);
-  if (has_q1) key_tiles(qbase + BQ, T, window, lo1, hi1);
-  const int jlo = lo0, jhi = has_q1 ? hi1 : hi0;   // lo0 <= lo1 and hi0 <= hi1
+  const int first = static_cast<int>(blockIdx.x), stride = static_cast<int>(gridDim.x);
 
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&ctl->q_full), 1);
+    mbar_init(smem_u32(&ctl->q_empty), 1);
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(smem_u32(&ctl->kv_full[s]), 1);
       mbar_init(smem_u32(&ctl->kv_empty[s]), 1);
@@ -156,94 +178,120 @@ __global__ void __launch_bounds__(THREADS, 1)
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
       const uint32_t qb = smem_u32(&ctl->q_full);
-      mbar_arrive_expect_tx(qb, (has_q1 ? 2 : 1) * L::Q_BYTES);
-#pragma unroll
-      for (int c = 0; c < L::NB; ++c) {
-        tma_load_2d(sQ + c * L::Q_BOX, &tmQ, qb, h * D + c * 64, b * T + qbase);
-        if (has_q1) tma_load_2d(sQ + L::Q_BYTES + c * L::Q_BOX, &tmQ, qb, h * D + c * 64, b * T + qbase + BQ);
-      }
-      int issued = 0;
-      for (int j = jlo; j <= jhi; ++j) {
-        const int jj = j - jlo, s = jj % STAGES;
-        if (!mbar_wait(smem_u32(&ctl->kv_empty[s]), ((jj / STAGES) & 1) ^ 1, abort, status)) break;
-        const uint32_t fb = smem_u32(&ctl->kv_full[s]);
-        mbar_arrive_expect_tx(fb, L::STAGE_BYTES);
-        const int row = b * T + j * BKV;
-        const uint32_t sK = sKV + s * L::STAGE_BYTES, sV = sK + L::K_BYTES;
+      uint32_t gkv = 0;   // key tiles loaded so far (ring position)
+      int ic = 0;
+      bool ok = true;
+      for (int r = 0; ok; ++r, ++ic) {
+        const int it = item_index(first, r, stride);
+        if (it >= num_items) break;
+        const Item w = decode_item(it, T, H, Hkv, B, window);
+        if (ic > 0 && !mbar_wait(smem_u32(&ctl->q_empty), (ic - 1) & 1, abort, status)) break;
+        mbar_arrive_expect_tx(qb, (w.has_q1 ? 2 : 1) * L::Q_BYTES);
 #pragma unroll
         for (int c = 0; c < L::NB; ++c) {
-          tma_load_2d(sK + c * L::KV_BOX, &tmK, fb, g * D + c * 64, row);
-          tma_load_2d(sV + c * L::KV_BOX, &tmV, fb, g * D + c * 64, row);
+          tma_load_2d(sQ + c * L::Q_BOX, &tmQ, qb, w.h * D + c * 64, w.b * T + w.qbase);
+          if (w.has_q1)
+            tma_load_2d(sQ + L::Q_BYTES + c * L::Q_BOX, &tmQ, qb, w.h * D + c * 64, w.b * T + w.qbase + BQ);
         }
-        ++issued;
+        for (int j = w.jlo; j <= w.jhi; ++j, ++gkv) {
+          const uint32_t s = gkv % STAGES;
+          if (!mbar_wait(smem_u32(&ctl->kv_empty[s]), ((gkv / STAGES) & 1) ^ 1, abort, status)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = smem_u32(&ctl->kv_full[s]);
+          mbar_arrive_expect_tx(fb, L::STAGE_BYTES);
+          const int row = w.b * T + j * BKV;
+          const uint32_t sK = sKV + s * L::STAGE_BYTES, sV = sK + L::K_BYTES;
+#pragma unroll
+          for (int c = 0; c < L::NB; ++c) {
+            tma_load_2d(sK + c * L::KV_BOX, &tmK, fb, w.g * D + c * 64, row);
+            tma_load_2d(sV + c * L::KV_BOX, &tmV, fb, w.g * D + c * 64, row);
+          }
+        }
       }
       // every issued copy must land before the CTA may exit
-      mbar_wait(qb, 0, nullptr, status);
-      for (int jj = (issued > STAGES ? issued - STAGES : 0); jj < issued; ++jj)
-        mbar_wait(smem_u32(&ctl->kv_full[jj % STAGES]), (jj / STAGES) & 1, nullptr, status);
+      if (ic > 0) mbar_wait(qb, (ic - 1) & 1, nullptr, status);
+      for (uint32_t q = (gkv > STAGES ? gkv - STAGES : 0); q < gkv; ++q)
+        mbar_wait(smem_u32(&ctl->kv_full[q % STAGES]), (q / STAGES) & 1, nullptr, status);
     } else if (warp == 1 && lane == 0) {
       constexpr uint32_t idS = idesc_bf16_f32(BQ, BKV);
       constexpr uint32_t idO = idesc_bf16_f32_bmn(BQ, D);
-      const int lo[2] = {lo0, lo1}, hi[2] = {hi0, hi1};
-      bool ok = mbar_wait(smem_u32(&ctl->q_full), 0, abort, status);
-      auto kv_ready = [&](int j) -> bool {
-        const int jj = j - jlo;
-        if (!mbar_wait(smem_u32(&ctl->kv_full[jj % STAGES]), (jj / STAGES) & 1, abort, status)) return false;
-        tc_fence_after();
-        return true;
-      };
-      auto issue_s = [&](int k, int j) {
-        const uint32_t sK = sKV + ((j - jlo) % STAGES) * L::STAGE_BYTES;
-        const uint32_t qk = sQ + k * L::Q_BYTES;
+      uint32_t gkv = 0;                 // ring position of the current item's first key tile
+      uint32_t pv_cnt[2] = {0u, 0u};    // P V steps issued per query tile (p_full phases)
+      int ic = 0;
+      bool ok = true;
+      for (int r = 0; ok; ++r, ++ic) {
+        const int it = item_index(first, r, stride);
+        if (it >= num_items) break;
+        const Item w = decode_item(it, T, H, Hkv, B, window);
+        const int lo[2] = {w.lo0, w.lo1}, hi[2] = {w.hi0, w.hi1};
+        const int jlo = w.jlo, jhi = w.jhi;
+        if (!mbar_wait(smem_u32(&ctl->q_full), ic & 1, abort, status)) break;
+        auto kv_ready = [&](int j) -> bool {
+          const uint32_t q = gkv + static_cast<uint32_t>(j - jlo);
+          if (!mbar_wait(smem_u32(&ctl->kv_full[q % STAGES]), (q / STAGES) & 1, abort, status)) return false;
+          tc_fence_after();
+          return true;
+        };
+        auto stage_of = [&](int j) { return (gkv + static_cast<uint32_t>(j - jlo)) % STAGES; };
+        auto issue_s = [&](int k, int j) {
+          const uint32_t sK = sKV + stage_of(j) * L::STAGE_BYTES;
+          const uint32_t qk = sQ + k * L::Q_BYTES;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t a = sdesc_kmajor_sw128(qk + (kk / 4) * L::Q_BOX + (kk % 4) * 32);
-          const uint64_t bd = sdesc_kmajor_sw128(sK + (kk / 4) * L::KV_BOX + (kk % 4) * 32);
-          umma_bf16(tmem + 128 * k, a, bd, idS, kk > 0 ? 1u : 0u);
-        }
-        umma_commit(smem_u32(&ctl->s_full[k]));
-      };
-      if (ok) ok = kv_ready(jlo);
-      if (ok) {
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint64_t a = sdesc_kmajor_sw128(qk + (kk / 4) * L::Q_BOX + (kk % 4) * 32);
+            const uint64_t bd = sdesc_kmajor_sw128(sK + (kk / 4) * L::KV_BOX + (kk % 4) * 32);
+            umma_bf16(tmem + 128 * k, a, bd, idS, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(smem_u32(&ctl->s_full[k]));
+        };
+        if (!kv_ready(jlo)) break;
         for (int k = 0; k < 2; ++k)
           if (jlo >= lo[k] && jlo <= hi[k]) issue_s(k, jlo);
-      }
-      for (int j = jlo; j <= jhi && ok; ++j) {
-        const uint32_t sV = sKV + ((j - jlo) % STAGES) * L::STAGE_BYTES + L::K_BYTES;
-        bool next_ready = false;
+        if (jlo == jhi) umma_commit(smem_u32(&ctl->q_empty));   // no S step of this item is left
+        for (int j = jlo; j <= jhi && ok; ++j) {
+          const uint32_t sV = sKV + stage_of(j) * L::STAGE_BYTES + L::K_BYTES;
+          bool next_ready = false;
 #pragma unroll
-        for (int k = 0; k < 2 && ok; ++k) {
-          if (j >= lo[k] && j <= hi[k]) {
-            // P V in two halves of 64 keys: the first half runs while softmax k still
-            // computes the second
+          for (int k = 0; k < 2 && ok; ++k) {
+            if (j >= lo[k] && j <= hi[k]) {
+              // P V in two halves of 64 keys: the first half runs while softmax k still
+              // computes the second
 #pragma unroll
-            for (int ph = 0; ph < 2; ++ph) {
-              if (!mbar_wait(smem_u32(&ctl->p_full[k][ph]), (j - lo[k]) & 1, abort, status)) {
-                ok = false;
-                break;
+              for (int ph = 0; ph < 2; ++ph) {
+                if (!mbar_wait(smem_u32(&ctl->p_full[k][ph]), pv_cnt[k] & 1, abort, status)) {
+                  ok = false;
+                  break;
+                }
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 4 * ph; kk < 4 * ph + 4; ++kk) {
+                  const uint64_t bd = sdesc_mnmajor_sw128(sV + kk * 16 * 128, L::KV_BOX);
+                  umma_bf16_ts(tmem + 256 + k * D, tmem + 128 * k + kk * 8, bd, idO,
+                               (j > lo[k] || kk > 0) ? 1u : 0u);
+                }
               }
-              tc_fence_after();
-#pragma unroll
-              for (int kk = 4 * ph; kk < 4 * ph + 4; ++kk) {
-                const uint64_t bd = sdesc_mnmajor_sw128(sV + kk * 16 * 128, L::KV_BOX);
-                umma_bf16_ts(tmem + 256 + k * D, tmem + 128 * k + kk * 8, bd, idO, (j > lo[k] || kk > 0) ? 1u : 0u);
-              }
+              if (!ok) break;
+              ++pv_cnt[k];
+              if (j == hi[k]) umma_commit(smem_u32(&ctl->o_done[k]));   // O_k of this item final
             }
-            if (!ok) break;
-            if (j == hi[k]) umma_commit(smem_u32(&ctl->o_done[k]));   // O_k final
-          }
-          if (j + 1 <= jhi && j + 1 >= lo[k] && j + 1 <= hi[k]) {
-            if (!next_ready) {
-              if (!kv_ready(j + 1)) {
-                ok = false;
-                break;
+            if (j + 1 <= jhi && j + 1 >= lo[k] && j + 1 <= hi[k]) {
+              if (!next_ready) {
+                if (!kv_ready(j + 1)) {
+                  ok = false;
+                  break;
+                }
+                next_ready = true;
               }
-              next_ready = true;
+              issue_s(k, j + 1);
             }
-            issue_s(k, j + 1);
           }
+          if (!ok) break;
+          if (j + 1 == jhi) umma_commit(smem_u32(&ctl->q_empty));   // no S step of this item is left
+          umma_commit(smem_u32(&ctl->kv_empty[stage_of(j)]));
         }
-        if (ok) umma_commit(smem_u32(&ctl->kv_empty[(j - jlo) % STAGES]));
+        gkv += static_cast<uint32_t>(jhi - jlo + 1);
       }
       umma_commit(smem_u32(&ctl->drain));
       mbar_wait(smem_u32(&ctl->drain), 0, nullptr, status);
@@ -254,19 +302,25 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int k = (warp - SM_WARP0) >> 2;   // query tile of this warpgroup
     const int quarter = warp & 3;          // TMEM lanes 32*(warp % 4) .. +31
     const int row = quarter * 32 + lane;
-    const int q0 = qbase + k * BQ;
-    const int i = q0 + row;
-    const int lo = k == 0 ? lo0 : lo1, hi = k == 0 ? hi0 : hi1;
-    const int nk = hi - lo + 1;   // 0 when the CTA has no second query tile
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t tS = tmem + 128 * k + lane_off, tO = tmem + 256 + k * D + lane_off;
     const float thr = 8.0f / scale_log2;   // raw-score growth that triggers a rescale (2^8)
+    uint32_t tcnt = 0, icnt = 0;           // S tiles and items handled by this query tile slot
+    bool ok = true;
+    for (int r = 0; ok; ++r) {
+    const int it = item_index(first, r, stride);
+    if (it >= num_items) break;
+    const Item w = decode_item(it, T, H, Hkv, B, window);
+    const int q0 = w.qbase + k * BQ;
+    const int i = q0 + row;
+    const int lo = k == 0 ? w.lo0 : w.lo1, hi = k == 0 ? w.hi0 : w.hi1;
+    const int nk = hi - lo + 1;   // 0 when the item has no second query tile
+    if (nk <= 0) continue;
     const int kmin = window < 0 ? 0 : i - window;
     const int kmax = min(i, T - 1);
     float m_run = -INFINITY, l_run = 0.f;
-    bool ok = true;
-    for (int t = 0; t < nk; ++t) {
-      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl->s_full[k]), t & 1, abort, status));
+    for (int t = 0; t < nk; ++t, ++tcnt) {
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl->s_full[k]), tcnt & 1, abort, status));
       if (!ok) break;
       tc_fence_after();
       float sv[BKV];
@@ -350,11 +404,12 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       l_run = l_run * alpha + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
     }
-    if (ok && nk > 0) ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl->o_done[k]), 0, abort, status));
-    if (ok && nk > 0) {
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl->o_done[k]), icnt & 1, abort, status));
+    ++icnt;
+    if (ok) {
       tc_fence_after();
       const float inv = 1.f / l_run;
-      bf16* dst = y + (static_cast<size_t>(b) * T + i) * (static_cast<size_t>(H) * D) + h * D;
+      bf16* dst = y + (static_cast<size_t>(w.b) * T + i) * (static_cast<size_t>(H) * D) + w.h * D;
 #pragma unroll 1
       for (int ch = 0; ch < D / 32; ++ch) {
         uint32_t o[32];
@@ -372,6 +427,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
         }
       }
+    }
     }
   }
 
@@ -397,17 +453,25 @@ cudaError_t launch_d(const bf16* q, const bf16* k, const bf16* v, int B, int T, 
       !make_tmap_bf16_2d(&tv, v, static_cast<uint64_t>(Hkv) * D, M, static_cast<uint64_t>(Hkv) * D * 2, 64, BKV))
     return cudaErrorInvalidValue;
   const int npair = (T + 2 * BQ - 1) / (2 * BQ);
+  const int num_items = npair * H * B;
+  static int num_sms = 0;
+  if (num_sms == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || num_sms < 1)
+      num_sms = 148;
+  }
   const float scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute lattr[1] = {pdl_attribute()};
-  cfg.gridDim = dim3(npair * H * B);
+  cfg.gridDim = dim3(num_items < num_sms ? num_items : num_sms);   // persistent: one CTA per SM
   cfg.blockDim = dim3(THREADS);
   cfg.dynamicSmemBytes = Lt::TOTAL;
   cfg.stream = stream;
   cfg.attrs = lattr;
   cfg.numAttrs = 1;
   const cudaError_t e =
-      cudaLaunchKernelEx(&cfg, attn_tc_kernel<D>, tq, tk, tv, T, H, Hkv, B, window, scale_log2, y, status);
+      cudaLaunchKernelEx(&cfg, attn_tc_kernel<D>, tq, tk, tv, T, H, Hkv, B, window, num_items, scale_log2, y, status);
   if (e != cudaSuccess) cudaGetLastError();
   return e;
 }
