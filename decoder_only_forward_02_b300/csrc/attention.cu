@@ -9,7 +9,8 @@
 // the reference's Blackwell path falls back to an attention without windows, so windows there
 // cost full causal work; here key tiles outside the window are never loaded.
 //
-// One CTA per (pair of 128-query tiles, head, batch row), one CTA per SM; heaviest pairs first.
+// Persistent CTAs, one per SM, walk work items: a pair of 128-query tiles of one (head, batch
+// row), heaviest pairs first, in serpentine order across the grid.
 // Key tiles are 128 keys wide, so every tensor-core step is a full-rate 128 x 128 (x 16) or
 // 128 x D (x 16) MMA.  The two query tiles (Q0: rows q0..q0+127, Q1: the next 128 rows) walk
 // the same key tiles; a query tile skips the key tiles it does not see.
@@ -26,7 +27,8 @@
 //   warps 4..7  softmax of Q0, warps 8..11 softmax of Q1, one thread per query row: load the
 //               128 scores of its row, mask only on key tiles that cross the diagonal, the
 //               window edge or the sequence end, online softmax in base 2 (scale folded into one
-//               FMA, hardware exp2), P to tensor memory in two halves of 64 keys (the P V step
+//               FMA, hardware exp2; maxima, scaling and sums on packed two-lane fp32
+//               instructions), P to tensor memory in two halves of 64 keys (the P V step
 //               of the first half starts while the second is computed).  The running max moves
 //               only when a row's max grows by more than 2^8; only then is that row of O
 //               rescaled.
@@ -349,20 +351,24 @@ __global__ void __launch_bounds__(THREADS, 1)
       const bool interior = key0 + BKV - 1 <= q0 && key0 + BKV <= T &&
                             (window < 0 || key0 >= q0 + BQ - 1 - window);
       if (!interior) {
+        // visible columns [kmin - key0, kmax - key0] as four 32-bit masks: a select per column
+        // on a mask bit, with no branch (a per-column compare chain costs about three times as much)
+        const int clo = kmin - key0, chi = kmax - key0;
 #pragma unroll
-        for (int c = 0; c < BKV; ++c) {
-          const int key = key0 + c;
-          sv[c] = (key <= kmax && key >= kmin) ? sv[c] : -INFINITY;
+        for (int q = 0; q < 4; ++q) {
+          const int a = max(clo - 32 * q, 0), b = min(chi - 32 * q, 31);
+          const uint32_t m = a > b ? 0u : ((0xffffffffu >> (31 - (b - a))) << a);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) sv[32 * q + c] = ((m >> c) & 1u) ? sv[32 * q + c] : -INFINITY;
         }
       }
-      // row max as 8 independent chains and a 3-level tree
+      // row max: 8 independent chains of three-input maxima, then a tree
       float mx[8];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) mx[q] = sv[q];
+      for (int q = 0; q < 8; ++q) mx[q] = fmaxf(sv[2 * q], sv[2 * q + 1]);
 #pragma unroll
-      for (int c = 8; c < BKV; ++c) mx[c & 7] = fmaxf(mx[c & 7], sv[c]);
-      const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      for (int c = 16; c < BKV; c += 2) mx[(c >> 1) & 7] = fmax3(mx[(c >> 1) & 7], sv[c], sv[c + 1]);
+      const float mt = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
       float alpha = 1.f;
       bool resc = false;
       if (mt > m_run + thr) {
@@ -385,16 +391,19 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         tmem_st_wait();
       }
-      float ps[4] = {0.f, 0.f, 0.f, 0.f};   // 4 independent partial sums
+      // exponents two keys at a time with packed fp32 arithmetic; 4 independent partial sums
+      const float2 sc2 = make_float2(scale_log2, scale_log2), nm2 = make_float2(negm, negm);
+      float2 ps[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         uint32_t pk[32];
 #pragma unroll
         for (int c = 0; c < 64; c += 2) {
-          const float p0 = ex2_approx(fmaf(sv[half * 64 + c], scale_log2, negm));
-          const float p1 = ex2_approx(fmaf(sv[half * 64 + c + 1], scale_log2, negm));
-          ps[(c >> 1) & 3] += p0 + p1;
-          pk[c / 2] = pack_bf16(p0, p1);
+          float2 e = ffma2(make_float2(sv[half * 64 + c], sv[half * 64 + c + 1]), sc2, nm2);
+          e.x = ex2_approx(e.x);
+          e.y = ex2_approx(e.y);
+          ps[(c >> 1) & 3] = fadd2(ps[(c >> 1) & 3], e);
+          pk[c / 2] = pack_bf16(e.x, e.y);
         }
         tmem_st32_u(tS + half * 32, pk);   // keys 64 half .. 64 half + 63 -> columns 32 half ..
         tmem_st_wait();
@@ -402,7 +411,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&ctl->p_full[k][half]));
       }
-      l_run = l_run * alpha + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
+      const float2 pt = fadd2(fadd2(ps[0], ps[1]), fadd2(ps[2], ps[3]));
+      l_run = l_run * alpha + (pt.x + pt.y);
     }
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl->o_done[k]), icnt & 1, abort, status));
     ++icnt;
