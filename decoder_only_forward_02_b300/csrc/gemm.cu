@@ -417,20 +417,13 @@ __device__ __forceinline__ void epi_softcap(uint32_t taddr, uint32_t tempty, int
   release_acc(lane, tempty);
 }
 
-// Residual stream update (attention and MLP output projections), with the next consumer's
-// inputs: the bf16 copy of the new stream and its partial sums of squares (the consumer's
-// RMSNorm row scale), and on request the next block's residual mix, the backout cache, the
-// final backout, and the value-embedding gate partial dot products.  Each warp stages the
-// gate weights of its 128 columns in its own shared buffer (gate_w) once per tile.
-__device__ __forceinline__ void epi_resid(uint32_t taddr, uint32_t tempty, int lane, int m0w, int n0, int M, int N,
-                                          const GemmEpi& ep, const OutMaps& om, Slab& sl, bf16* gate_w) {
-  if (n0 >= N) {
-    release_acc(lane, tempty);
-    return;
-  }
-  const int m = m0w + lane;
-  const bool has_gate = ep.wg != nullptr;
-  if (has_gate) {
+// Start of a residual-update tile, issued before its accumulator is ready so that the
+// latency overlaps the wait: the gate weights of the warp's 128 columns go to its own shared
+// buffer (gate_w), and the first 32-column chunk of the residual (and of Y) is loaded.
+__device__ __forceinline__ void resid_begin(int lane, int m0w, int n0, int M, int N, const GemmEpi& ep,
+                                            bf16* gate_w, float4 (&rv)[8], float4 (&yv)[8]) {
+  if (n0 >= N) return;
+  if (ep.wg != nullptr) {
     // W_g[:, n0 .. n0+128) (zero past c_g), 16 pieces of 16 B per head row
     __syncwarp();   // every lane is done with the previous tile's copy
     for (int i = lane; i < ep.Hkv * 16; i += 32) {
@@ -439,8 +432,27 @@ __device__ __forceinline__ void epi_resid(uint32_t taddr, uint32_t tempty, int l
       if (c < ep.c_g) w = __ldg(reinterpret_cast<const uint4*>(ep.wg + static_cast<size_t>(h) * ep.c_g + c));
       reinterpret_cast<uint4*>(gate_w)[i] = w;
     }
-    __syncwarp();
   }
+  load_chunk_f32(ep.resid, N, m0w, n0, M, lane, rv);
+  if (ep.Y != nullptr) load_chunk_f32(ep.Y, N, m0w, n0, M, lane, yv);
+}
+
+// Residual stream update (attention and MLP output projections), with the next consumer's
+// inputs: the bf16 copy of the new stream and its partial sums of squares (the consumer's
+// RMSNorm row scale), and on request the next block's residual mix, the backout cache, the
+// final backout, and the value-embedding gate partial dot products.  rv / yv arrive holding
+// the first chunk (resid_begin); each later chunk is loaded as soon as the previous one has
+// been consumed, so its latency overlaps the previous chunk's gate and store work.
+__device__ __forceinline__ void epi_resid(uint32_t taddr, uint32_t tempty, int lane, int m0w, int n0, int M, int N,
+                                          const GemmEpi& ep, const OutMaps& om, Slab& sl, bf16* gate_w,
+                                          float4 (&rv)[8], float4 (&yv)[8]) {
+  if (n0 >= N) {
+    release_acc(lane, tempty);
+    return;
+  }
+  const int m = m0w + lane;
+  const bool has_gate = ep.wg != nullptr;
+  if (has_gate) __syncwarp();   // the gate weights staged by every lane are visible
   float ss = 0.f;
   float gacc[MAX_GATE_HEADS];
 #pragma unroll
@@ -454,9 +466,6 @@ __device__ __forceinline__ void epi_resid(uint32_t taddr, uint32_t tempty, int l
     const int c0 = n0 + ch * 32;
     uint32_t r[32];
     tmem_ld32(taddr + ch * 32, r);
-    float4 rv[8], yv[8];
-    load_chunk_f32(ep.resid, N, m0w, c0, M, lane, rv);
-    if (ep.Y != nullptr) load_chunk_f32(ep.Y, N, m0w, c0, M, lane, yv);
     tmem_ld_wait(r);
     if (ch == 3) release_acc(lane, tempty);
     float x[32];
@@ -477,6 +486,10 @@ __device__ __forceinline__ void epi_resid(uint32_t taddr, uint32_t tempty, int l
 #pragma unroll
         for (int j = 0; j < 32; ++j) x[j] *= ep.a;
       }
+      if (ch < 3) {
+        load_chunk_f32(ep.resid, N, m0w, c0 + 32, M, lane, rv);
+        if (ep.Y != nullptr) load_chunk_f32(ep.Y, N, m0w, c0 + 32, M, lane, yv);
+      }
     } else {
       // x' = a (resid + acc) + b Y: the a resid + b Y part is formed in the loaded layout, so
       // one transpose serves both inputs
@@ -495,6 +508,10 @@ __device__ __forceinline__ void epi_resid(uint32_t taddr, uint32_t tempty, int l
         }
       }
       sl.transpose_f32(lane, rv, x);
+      if (ch < 3) {
+        load_chunk_f32(ep.resid, N, m0w, c0 + 32, M, lane, rv);
+        if (ep.Y != nullptr) load_chunk_f32(ep.Y, N, m0w, c0 + 32, M, lane, yv);
+      }
 #pragma unroll
       for (int j = 0; j < 32; ++j) x[j] = fmaf(ep.a, __uint_as_float(r[j]), x[j]);
     }
@@ -795,6 +812,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       int m0w, n0;
       coords(tile, m0w, n0);
       const EpiPre pre = pre_finish<KIND, D>(raw, lane, m0w, n0, M, N, ep);
+      float4 rv[8], yv[8];   // residual-update epilogue: the first chunk of the residual (and Y)
+      if constexpr (KIND == EPI_RESID) resid_begin(lane, m0w, n0, M, N, ep, gate_w, rv, yv);
       const bool ok = mbar_wait_cluster(smem_u32(&ctl->tfull[a]), aph, abort, status);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
@@ -805,7 +824,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + a * BN + group * 128;
       const uint32_t tempty = mapa_shared(smem_u32(&ctl->tempty[a]), 0);
-      if constexpr (KIND == EPI_RESID) epi_resid(taddr, tempty, lane, m0w, n0, M, N, ep, om, sl, gate_w);
+      if constexpr (KIND == EPI_RESID) epi_resid(taddr, tempty, lane, m0w, n0, M, N, ep, om, sl, gate_w, rv, yv);
       else if constexpr (KIND == EPI_SOFTCAP_F32) epi_softcap(taddr, tempty, lane, m0w, n0, M, N, ep, sl, pre);
       else if constexpr (KIND == EPI_QKV) epi_qkv<D>(taddr, tempty, lane, m0w, n0, M, N, ep, om, sl, pre);
       else epi_bf16<KIND == EPI_RELU2_BF16>(taddr, tempty, lane, m0w, n0, M, N, ep, om, sl, pre);
