@@ -66,23 +66,28 @@ constexpr int MAX_NCG = 16;                     // column groups of a row (n_emb
 constexpr uint32_t TMEM_COLS = 2 * BN;
 constexpr int SLAB_BUF = 32 * 128;       // one staging buffer: 32 rows x 128 B
 constexpr int SLAB_BYTES = 2 * SLAB_BUF; // two per epilogue warp, used alternately
+
+// Second template argument of a residual-update launch whose epilogue also produces the
+// value-embedding gate partials (for the other kinds it is the head dimension, or 0).
+constexpr int RESID_GATE = 1;
 constexpr int GATE_BYTES = MAX_GATE_HEADS * 128 * 2;   // gate weights of one 128-column group (per warp)
 
 // Shared memory per epilogue kind.  Kinds whose epilogue stores with TMA keep two staging
-// buffers per warp (a store drains from one while the next is filled); the squared-ReLU and
-// soft-cap epilogues store row-coalesced from one buffer, and the space saved deepens their
-// operand ring to 6 stages (their K is short, so operand latency is what starves the MMA).
-// The residual-update epilogue (whose K is the long one of the MLP down projection) takes a
-// 4-stage ring, and each of its warps keeps its own copy of the gate weights of its column
-// group in shared memory.
-template <int KIND>
+// buffers per warp (a store drains from one while the next is filled) and a 5-stage operand
+// ring; the squared-ReLU and soft-cap epilogues store row-coalesced from one buffer, and the
+// space saved deepens their ring to 6 stages (operand latency is what starves the MMA).  A
+// residual update that produces gate partials keeps each warp's copy of the gate weights of
+// its column group in shared memory (read by every lane at the same address), which costs
+// one operand stage.
+template <int KIND, int D>
 struct Cfg {
   static constexpr bool LSU_STORE = KIND == EPI_RELU2_BF16 || KIND == EPI_SOFTCAP_F32;
-  static constexpr int STAGES = KIND == EPI_RESID ? 4 : (LSU_STORE ? 6 : 5);
+  static constexpr bool GATE = KIND == EPI_RESID && D == RESID_GATE;
+  static constexpr int STAGES = LSU_STORE ? 6 : (GATE ? 4 : 5);
   static constexpr int SLAB_WARP = LSU_STORE ? SLAB_BUF : SLAB_BYTES;   // staging bytes per warp
   static constexpr int OFF_SLAB = STAGES * (A_BYTES + B_BYTES);
   static constexpr int OFF_GATE = OFF_SLAB + NUM_EPI_WARPS * SLAB_WARP;
-  static constexpr int OFF_CTRL = OFF_GATE + (KIND == EPI_RESID ? NUM_EPI_WARPS * GATE_BYTES : 0);
+  static constexpr int OFF_CTRL = OFF_GATE + (GATE ? NUM_EPI_WARPS * GATE_BYTES : 0);
   struct __align__(8) Ctrl {
     uint64_t full[STAGES];
     uint64_t empty[STAGES];
@@ -418,12 +423,13 @@ __device__ __forceinline__ void epi_softcap(uint32_t taddr, uint32_t tempty, int
 }
 
 // Start of a residual-update tile, issued before its accumulator is ready so that the
-// latency overlaps the wait: the gate weights of the warp's 128 columns go to its own shared
-// buffer (gate_w), and the first 32-column chunk of the residual (and of Y) is loaded.
+// latency overlaps the wait: with GATE, the gate weights of the warp's 128 columns go to its
+// own shared buffer (gate_w); then the first 32-column chunk of the residual (and of Y).
+template <bool GATE>
 __device__ __forceinline__ void resid_begin(int lane, int m0w, int n0, int M, int N, const GemmEpi& ep,
                                             bf16* gate_w, float4 (&rv)[8], float4 (&yv)[8]) {
   if (n0 >= N) return;
-  if (ep.wg != nullptr) {
+  if constexpr (GATE) {
     // W_g[:, n0 .. n0+128) (zero past c_g), 16 pieces of 16 B per head row
     __syncwarp();   // every lane is done with the previous tile's copy
     for (int i = lane; i < ep.Hkv * 16; i += 32) {
@@ -440,19 +446,20 @@ __device__ __forceinline__ void resid_begin(int lane, int m0w, int n0, int M, in
 // Residual stream update (attention and MLP output projections), with the next consumer's
 // inputs: the bf16 copy of the new stream and its partial sums of squares (the consumer's
 // RMSNorm row scale), and on request the next block's residual mix, the backout cache, the
-// final backout, and the value-embedding gate partial dot products.  rv / yv arrive holding
+// final backout, and (GATE) the value-embedding gate partial dot products.  rv / yv arrive holding
 // the first chunk (resid_begin); each later chunk is loaded as soon as the previous one has
 // been consumed, so its latency overlaps the previous chunk's gate and store work.
+template <bool GATE>
 __device__ __forceinline__ void epi_resid(uint32_t taddr, uint32_t tempty, int lane, int m0w, int n0, int M, int N,
-                                          const GemmEpi& ep, const OutMaps& om, Slab& sl, bf16* gate_w,
+                                          const GemmEpi& ep, const OutMaps& om, Slab& sl, const bf16* gate_w,
                                           float4 (&rv)[8], float4 (&yv)[8]) {
   if (n0 >= N) {
     release_acc(lane, tempty);
     return;
   }
   const int m = m0w + lane;
-  const bool has_gate = ep.wg != nullptr;
-  if (has_gate) __syncwarp();   // the gate weights staged by every lane are visible
+  constexpr bool has_gate = GATE;
+  if constexpr (GATE) __syncwarp();   // the gate weights staged by every lane are visible
   float ss = 0.f;
   float gacc[MAX_GATE_HEADS];
 #pragma unroll
@@ -681,7 +688,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  using L = Cfg<KIND>;
+  using L = Cfg<KIND, D>;
+  constexpr int PD = KIND == EPI_QKV ? D : 0;   // head dimension of the prologue data (QKV only)
   constexpr int STAGES = L::STAGES;
   const uint32_t sA = smem_u32(smem);
   const uint32_t sB = sA + STAGES * A_BYTES;
@@ -792,39 +800,39 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int quarter = warp & 3;   // TMEM lanes 32*(warp % 4) .. +31 are this warp's
     const int group = ew >> 2;
     Slab sl{smem + L::OFF_SLAB + ew * L::SLAB_WARP, smem_u32(smem + L::OFF_SLAB + ew * L::SLAB_WARP), 0u};
-    bf16* gate_w = reinterpret_cast<bf16*>(smem + L::OFF_GATE + ew * GATE_BYTES);
+    bf16* gate_w = reinterpret_cast<bf16*>(smem + L::OFF_GATE + ew * GATE_BYTES);   // used with a gate only
     auto coords = [&](int tile, int& m0w, int& n0) {
       int mb, nb;
       tile_coords(tile, num_m, num_n, grp, mb, nb);
       m0w = mb * PAIR_M + static_cast<int>(rank) * BM + quarter * 32;
       n0 = nb * BN + group * 128;
     };
-    PreRaw<D> raw;
+    PreRaw<PD> raw;
     raw.tok = -1;
     if (pair < num_tiles) {
       int m0w, n0;
       coords(pair, m0w, n0);
-      pre_issue<KIND, D>(raw, lane, m0w, n0, M, N, ep);
+      pre_issue<KIND, PD>(raw, lane, m0w, n0, M, N, ep);
     }
     uint32_t tc = 0;
     for (int tile = pair; tile < num_tiles; tile += npairs, ++tc) {
       const uint32_t a = tc & 1, aph = (tc >> 1) & 1;
       int m0w, n0;
       coords(tile, m0w, n0);
-      const EpiPre pre = pre_finish<KIND, D>(raw, lane, m0w, n0, M, N, ep);
+      const EpiPre pre = pre_finish<KIND, PD>(raw, lane, m0w, n0, M, N, ep);
       float4 rv[8], yv[8];   // residual-update epilogue: the first chunk of the residual (and Y)
-      if constexpr (KIND == EPI_RESID) resid_begin(lane, m0w, n0, M, N, ep, gate_w, rv, yv);
+      if constexpr (KIND == EPI_RESID) resid_begin<L::GATE>(lane, m0w, n0, M, N, ep, gate_w, rv, yv);
       const bool ok = mbar_wait_cluster(smem_u32(&ctl->tfull[a]), aph, abort, status);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
       if (tile + npairs < num_tiles) {   // the next tile's row data is in flight during this epilogue
         int m1, n1;
         coords(tile + npairs, m1, n1);
-        pre_issue<KIND, D>(raw, lane, m1, n1, M, N, ep);
+        pre_issue<KIND, PD>(raw, lane, m1, n1, M, N, ep);
       }
       const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + a * BN + group * 128;
       const uint32_t tempty = mapa_shared(smem_u32(&ctl->tempty[a]), 0);
-      if constexpr (KIND == EPI_RESID) epi_resid(taddr, tempty, lane, m0w, n0, M, N, ep, om, sl, gate_w, rv, yv);
+      if constexpr (KIND == EPI_RESID) epi_resid<L::GATE>(taddr, tempty, lane, m0w, n0, M, N, ep, om, sl, gate_w, rv, yv);
       else if constexpr (KIND == EPI_SOFTCAP_F32) epi_softcap(taddr, tempty, lane, m0w, n0, M, N, ep, sl, pre);
       else if constexpr (KIND == EPI_QKV) epi_qkv<D>(taddr, tempty, lane, m0w, n0, M, N, ep, om, sl, pre);
       else epi_bf16<KIND == EPI_RELU2_BF16>(taddr, tempty, lane, m0w, n0, M, N, ep, om, sl, pre);
@@ -855,13 +863,13 @@ cudaError_t launch_kind(const CUtensorMap& ta, const CUtensorMap& tb, const OutM
   attr[0].val.clusterDim.z = 1;
   attr[1] = pdl_attribute();
   cfg.blockDim = dim3(THREADS);
-  cfg.dynamicSmemBytes = Cfg<KIND>::SMEM_BYTES;
+  cfg.dynamicSmemBytes = Cfg<KIND, D>::SMEM_BYTES;
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;   // occupancy query without the PDL attribute
   std::call_once(once, [&] {
     attr_err = cudaFuncSetAttribute(gemm_tc_kernel<KIND, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    Cfg<KIND>::SMEM_BYTES);
+                                    Cfg<KIND, D>::SMEM_BYTES);
     if (attr_err != cudaSuccess) return;
     cudaLaunchConfig_t q = cfg;
     q.gridDim = dim3(2 * (num_sms / 2));
@@ -932,7 +940,9 @@ cudaError_t launch_gemm(const bf16* A, const bf16* B, int M, int N, int K, const
   if (!ok) return cudaErrorInvalidValue;
   switch (epi.kind) {
     case EPI_BF16: return launch_kind<EPI_BF16, 0>(ta, tb, om, M, N, K, epi, num_sms, stream);
-    case EPI_RESID: return launch_kind<EPI_RESID, 0>(ta, tb, om, M, N, K, epi, num_sms, stream);
+    case EPI_RESID:
+      if (epi.wg != nullptr) return launch_kind<EPI_RESID, RESID_GATE>(ta, tb, om, M, N, K, epi, num_sms, stream);
+      return launch_kind<EPI_RESID, 0>(ta, tb, om, M, N, K, epi, num_sms, stream);
     case EPI_RELU2_BF16: return launch_kind<EPI_RELU2_BF16, 0>(ta, tb, om, M, N, K, epi, num_sms, stream);
     case EPI_SOFTCAP_F32: return launch_kind<EPI_SOFTCAP_F32, 0>(ta, tb, om, M, N, K, epi, num_sms, stream);
     case EPI_QKV:
