@@ -384,3 +384,66 @@ def test_positions_subset_matches_full():
     tok = make_tokens(wl).numpy()[1]
     full = O.forward_row(wl.model, W, tok)
     np.testing.assert_array_equal(O.forward_row(wl.model, W, tok, positions=[0, 5, 63]), full[[0, 5, 63]])
+
+
+# ---------------------------------------------------------------- cross-entropy / bits per byte
+
+def test_cross_entropy_equal_logits_is_ln_v():
+    for V in (2, 7, 512):
+        z = np.full((3, V), 1.25)
+        np.testing.assert_allclose(O.cross_entropy(z, np.array([0, V - 1, V // 2])), math.log(V), rtol=0, atol=1e-12)
+
+
+def test_cross_entropy_two_class_closed_form():
+    # z = (a, b): loss(target 0) = log(1 + e^(b - a)), loss(target 1) = log(1 + e^(a - b))
+    a, b = 0.7, -2.3
+    z = np.array([[a, b], [a, b]])
+    got = O.cross_entropy(z, np.array([0, 1]))
+    np.testing.assert_allclose(got, [math.log1p(math.exp(b - a)), math.log1p(math.exp(a - b))], rtol=1e-14)
+
+
+def test_cross_entropy_dominant_target_and_shift_invariance():
+    z = np.zeros((1, 4))
+    z[0, 2] = 30.0
+    assert O.cross_entropy(z, np.array([2]))[0] < 1e-12          # log(1 + 3 e^-30)
+    assert abs(O.cross_entropy(z, np.array([1]))[0] - 30.0) < 1e-9
+    zr = rng.normal(size=(5, 33)) * 4
+    t = rng.integers(0, 33, 5)
+    np.testing.assert_allclose(O.cross_entropy(zr + 17.5, t), O.cross_entropy(zr, t), rtol=1e-12)
+
+
+def test_cross_entropy_matches_torch_and_ignores_negative_targets():
+    z = rng.normal(size=(40, 97)) * 5
+    t = rng.integers(0, 97, 40)
+    t[[3, 11]] = -1
+    ref = F.cross_entropy(torch.from_numpy(z), torch.from_numpy(t), ignore_index=-1, reduction="none").numpy()
+    got = O.cross_entropy(z, t)
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-12)
+    assert got[3] == 0.0 and got[11] == 0.0
+    mean, bpb = O.loss_stats(got, t)
+    np.testing.assert_allclose(mean, got[t >= 0].mean(), rtol=1e-14)
+    assert math.isnan(bpb)
+
+
+def test_loss_stats_bits_per_byte_hand_case():
+    # losses ln2, 2 ln2, 3 ln2, 5; targets of byte lengths 1, 0 (special token), 2 and an ignored
+    # position: bpb = (ln2 + 3 ln2) / (ln 2 * (1 + 2)) = 4/3; the mean counts the first three
+    ln2 = math.log(2.0)
+    losses = np.array([ln2, 2 * ln2, 3 * ln2, 5.0])
+    targets = np.array([4, 0, 2, -1])
+    token_bytes = np.array([0, 3, 2, 9, 1])
+    mean, bpb = O.loss_stats(losses, targets, token_bytes)
+    np.testing.assert_allclose(mean, 2 * ln2, rtol=1e-15)
+    np.testing.assert_allclose(bpb, 4.0 / 3.0, rtol=1e-15)
+    assert math.isnan(O.loss_stats(losses, np.array([-1, -1, -1, -1]), token_bytes)[0])
+    assert math.isnan(O.loss_stats(losses, np.array([0, 0, -1, -1]), token_bytes)[1])   # no bytes
+
+
+def test_model_cross_entropy_near_ln_v():
+    # N(0, 0.02) weights: near-uniform predictions; the oracle's loss agrees with the direct formula
+    wl = get_workload("tiny_all")
+    cfg = wl.model
+    y = O.forward(cfg, _weights(cfg), make_tokens(wl).numpy())
+    tgt = np.random.default_rng(3).integers(0, cfg.vocab_size, y.shape[:2])
+    losses = O.cross_entropy(y.reshape(-1, cfg.vocab_size), tgt.reshape(-1))
+    assert abs(O.loss_stats(losses, tgt.reshape(-1))[0] - math.log(cfg.vocab_size)) < 0.5
