@@ -117,13 +117,14 @@ class ClockSampler:
                 "samples": len(sm), "reasons": sorted(reasons)}
 
 
-def oracle_sample(wl, wts, tok, n_tokens: int):
-    """Run the fp64 oracle on the first n_tokens positions of batch row 0; returns seconds."""
+def oracle_sample(wl, wts, tok, n_tokens: int, rows: int = 1):
+    """Run the fp64 oracle on the first n_tokens positions of batch rows 0..rows-1; returns seconds."""
     import numpy as np
     import oracle as O
     W = O.OracleWeights.from_synth(wl.model, wts)
     t0 = time.perf_counter()
-    O.forward_row(wl.model, W, tok[0, :n_tokens].numpy())
+    for r in range(rows):
+        O.forward_row(wl.model, W, tok[r, :n_tokens].numpy())
     return time.perf_counter() - t0
 
 
@@ -225,6 +226,40 @@ def run_ours(args, rank, world, local_rank):
     model.timing(False)
     ktimes = model.timing_read()
 
+    # The loss path (nc_forward_loss: the lm_head fused with the soft-cap and the next-token
+    # cross-entropy, no logits written), timed the same way on the same batch; targets are the
+    # next tokens, the last position of each row ignored.
+    loss_path = None
+    if not args.no_loss_path:
+        tgt = torch.full_like(tok, -1)
+        tgt[:, :-1] = tok[:, 1:]
+        lbuf = torch.empty((B, T), dtype=torch.float32, device=dev)
+        sbuf = torch.empty((2,), dtype=torch.float32, device=dev)
+        for _ in range(3):
+            model.forward_loss(tok, tgt, loss=lbuf, stats=sbuf)
+        n_loss = max(1, min(args.steps, 50))
+        barrier()
+        torch.cuda.synchronize()
+        e2 = torch.cuda.Event(enable_timing=True)
+        e3 = torch.cuda.Event(enable_timing=True)
+        e2.record(stream)
+        for _ in range(n_loss):
+            model.forward_loss(tok, tgt, loss=lbuf, stats=sbuf)
+        e3.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        if model.status() != 0:
+            raise RuntimeError("device status set on the loss path")
+        lt = torch.tensor([e2.elapsed_time(e3)], dtype=torch.float64, device=dev)
+        if world > 1:
+            dist.all_reduce(lt, op=dist.ReduceOp.MAX)
+        loss_ms = float(lt.item()) / n_loss
+        loss_path = {"metric": "forward + cross-entropy tokens/s", "value": world * B * T / (loss_ms / 1000.0),
+                     "unit": UNIT, "ms_per_step": loss_ms, "steps": n_loss,
+                     "gpu_launches_per_step": model.launch_count(loss=True),
+                     "mean_loss_nats": float(sbuf[0].item()),
+                     "note": "nc_forward_loss: lm_head fused with soft-cap and cross-entropy, no logits written"}
+
     t_max = torch.tensor([ms], dtype=torch.float64, device=dev)
     if world > 1:
         dist.all_reduce(t_max, op=dist.ReduceOp.MAX)
@@ -309,13 +344,16 @@ def run_ours(args, rank, world, local_rank):
         "gpu_launches": model.launch_count() * args.steps,
         "clocks": clk,
         "e2e": e2e,
+        "loss_path": loss_path,
     }
     if not args.no_cpu_baseline and world >= 1:
         n = min(args.cpu_tokens, T)
-        secs = oracle_sample(wl, wts_cpu, tok_cpu, n)
-        line["cpu_baseline"] = {"value": n / secs, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
-                                "sample": f"fp64 oracle on positions 0..{n - 1} of batch row 0 "
-                                          f"({secs:.1f} s, causal prefix: exact logits for those positions)"}
+        rows = max(1, min(args.cpu_rows, B))
+        secs = oracle_sample(wl, wts_cpu, tok_cpu, n, rows)
+        line["cpu_baseline"] = {"value": rows * n / secs, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+                                "sample": f"fp64 oracle on positions 0..{n - 1} of batch rows 0..{rows - 1} "
+                                          f"({secs:.1f} s; rows are independent and a causal prefix gives "
+                                          f"exact logits for its positions)"}
     print(json.dumps(line), flush=True)
 
 
@@ -410,8 +448,10 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-loss-path", action="store_true", help="skip timing the fused cross-entropy path")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-tokens", type=int, default=2048)
+    ap.add_argument("--cpu-rows", type=int, default=4, help="batch rows the CPU baseline times")
     ap.add_argument("--ref-tokens", type=int, default=512)
     ap.add_argument("--only-kernel", default=None,
                     help="launch one kernel class (qkv, attention, oproj, fc, proj, lmhead, embed) "

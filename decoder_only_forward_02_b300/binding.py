@@ -19,7 +19,7 @@ NC_OK = 0
 STATUS_NAMES = {0: "NC_OK", 1: "NC_ERR_INVALID_ARG", 2: "NC_ERR_UNSUPPORTED", 3: "NC_ERR_WORKSPACE",
                 4: "NC_ERR_CUDA", 5: "NC_ERR_DEVICE_TIMEOUT", 6: "NC_ERR_TOKEN_RANGE"}
 KERNEL_CLASSES = ["embed_smear", "qkv_rope_qknorm_ve", "attention", "oproj_residual", "fc_relu2",
-                  "proj_residual", "lmhead_softcap"]
+                  "proj_residual", "lmhead_softcap", "cross_entropy"]
 SS_GROUP = 128   # columns per partial sum of squares
 
 c_int_p = ctypes.POINTER(ctypes.c_int)
@@ -70,6 +70,11 @@ _SIGS = {
                                       ctypes.POINTER(ctypes.c_int)]),
     "nc_kernel_class_name": (ctypes.c_char_p, [ctypes.c_int]),
     "nc_forward_launch_count": (ctypes.c_int, [ctypes.c_void_p]),
+    "nc_forward_loss_launch_count": (ctypes.c_int, [ctypes.c_void_p]),
+    "nc_workspace_bytes_loss": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+                                               ctypes.POINTER(ctypes.c_size_t)]),
+    "nc_forward_loss": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int]
+                        + [ctypes.c_void_p] * 4 + [ctypes.c_size_t, ctypes.c_void_p]),
     # per-kernel entry points (include/nc_ops.h)
     "nc_op_gemm": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                   ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int,
@@ -88,6 +93,12 @@ _SIGS = {
                                          ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
                                          ctypes.c_float, ctypes.c_float] + [ctypes.c_void_p] * 5 +
                           [ctypes.c_int, ctypes.c_int] + [ctypes.c_void_p] * 3),
+    "nc_op_lmhead_ce": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                       ctypes.c_void_p, ctypes.c_float, ctypes.c_float] + [ctypes.c_void_p] * 5),
+    "nc_op_ce_scratch_bytes": (ctypes.c_size_t, [ctypes.c_int]),
+    "nc_op_ce_finalize": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+                                         ctypes.c_int] + [ctypes.c_void_p] * 4 + [ctypes.c_size_t, ctypes.c_void_p,
+                                                                                   ctypes.c_void_p]),
 }
 
 EPI = {"bf16": 0, "relu2_bf16": 2, "softcap_f32": 3}
@@ -168,6 +179,32 @@ class ops:
                                       ssp.data_ptr(), _ptr(wg), Hkv, c_g or C, _ptr(gp), _ptr(status),
                                       _stream_handle(None)), "nc_op_embed_smear")
         return x0, x, xb, ssp, gp
+
+    @staticmethod
+    def lmhead_ce(xf, wlm, targets, ssp=None, C=0, eps=1e-6, cap=15.0, status=None):
+        """Cross-entropy partials of the soft-capped lm_head: returns (part [ceil(V/128), M], zt [M])."""
+        M, K = xf.shape
+        V = wlm.shape[0]
+        part = torch.empty(((V + 127) // 128, M), dtype=torch.float32, device=xf.device)
+        zt = torch.zeros((M,), dtype=torch.float32, device=xf.device)
+        check(lib().nc_op_lmhead_ce(xf.data_ptr(), wlm.data_ptr(), M, V, K, _ptr(ssp), eps, cap, targets.data_ptr(),
+                                    part.data_ptr(), zt.data_ptr(), _ptr(status), _stream_handle(None)),
+              "nc_op_lmhead_ce")
+        return part, zt
+
+    @staticmethod
+    def ce_finalize(part, zt, targets, V, token_bytes=None, status=None):
+        """Returns (loss [M], stats [2] = mean loss, bits per byte)."""
+        M = zt.shape[0]
+        dev = zt.device
+        loss = torch.empty((M,), dtype=torch.float32, device=dev)
+        stats = torch.empty((2,), dtype=torch.float32, device=dev)
+        nbytes = lib().nc_op_ce_scratch_bytes(M)
+        scratch = torch.empty((max(nbytes, 8) // 8,), dtype=torch.float64, device=dev)
+        check(lib().nc_op_ce_finalize(part.data_ptr(), zt.data_ptr(), targets.data_ptr(), M, V, _ptr(token_bytes),
+                                      loss.data_ptr(), stats.data_ptr(), scratch.data_ptr(), nbytes, _ptr(status),
+                                      _stream_handle(None)), "nc_op_ce_finalize")
+        return loss, stats
 
 
 _lib: Optional[ctypes.CDLL] = None
@@ -293,16 +330,18 @@ class Model:
                 pass
             self.handle = None
 
-    def workspace_bytes(self, B: int, T: int, host: bool = False) -> int:
+    def workspace_bytes(self, B: int, T: int, host: bool = False, loss: bool = False) -> int:
         n = ctypes.c_size_t()
-        fn = lib().nc_workspace_bytes_host if host else lib().nc_workspace_bytes
+        fn = lib().nc_workspace_bytes_host if host else (lib().nc_workspace_bytes_loss if loss
+                                                         else lib().nc_workspace_bytes)
         check(fn(self.handle, B, T, ctypes.byref(n)), "nc_workspace_bytes")
         return n.value
 
-    def workspace(self, B: int, T: int, host: bool = False) -> torch.Tensor:
-        key = (B, T, host)
+    def workspace(self, B: int, T: int, host: bool = False, loss: bool = False) -> torch.Tensor:
+        key = (B, T, host, loss)
         if key not in self._ws:
-            self._ws[key] = torch.empty(self.workspace_bytes(B, T, host), dtype=torch.uint8, device=self.device)
+            self._ws[key] = torch.empty(self.workspace_bytes(B, T, host, loss), dtype=torch.uint8,
+                                        device=self.device)
         return self._ws[key]
 
     def forward(self, tokens: torch.Tensor, out: Optional[torch.Tensor] = None,
@@ -318,6 +357,28 @@ class Model:
         check(lib().nc_forward(self.handle, tokens.data_ptr(), B, T, out.data_ptr(), ws.data_ptr(), ws.numel(),
                                _stream_handle(stream)), "nc_forward")
         return out
+
+    def forward_loss(self, tokens: torch.Tensor, targets: torch.Tensor,
+                     token_bytes: Optional[torch.Tensor] = None, loss: Optional[torch.Tensor] = None,
+                     stats: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None):
+        """tokens, targets: device int32 [B, T] (target < 0: ignored) -> (loss fp32 [B, T] in nats,
+        stats fp32 [2] = mean loss, bits per byte); token_bytes: device int32 [V] or None.
+        The lm_head is fused with the soft-cap and the cross-entropy: no logits are written."""
+        for name, t in (("tokens", tokens), ("targets", targets)):
+            if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
+                raise ValueError(f"{name} must be a contiguous int32 CUDA tensor")
+        if targets.shape != tokens.shape:
+            raise ValueError("targets must have the shape of tokens")
+        B, T = tokens.shape
+        if loss is None:
+            loss = torch.empty((B, T), dtype=torch.float32, device=self.device)
+        if stats is None:
+            stats = torch.empty((2,), dtype=torch.float32, device=self.device)
+        ws = self.workspace(B, T, loss=True)
+        check(lib().nc_forward_loss(self.handle, tokens.data_ptr(), targets.data_ptr(), B, T, _ptr(token_bytes),
+                                    loss.data_ptr(), stats.data_ptr(), ws.data_ptr(), ws.numel(),
+                                    _stream_handle(stream)), "nc_forward_loss")
+        return loss, stats
 
     def forward_host(self, tokens: torch.Tensor, out: torch.Tensor,
                      stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
@@ -344,5 +405,6 @@ class Model:
             out[name] = (ms.value, n.value)
         return out
 
-    def launch_count(self) -> int:
-        return lib().nc_forward_launch_count(self.handle)
+    def launch_count(self, loss: bool = False) -> int:
+        fn = lib().nc_forward_loss_launch_count if loss else lib().nc_forward_launch_count
+        return fn(self.handle)

@@ -36,6 +36,8 @@
 //   EPI_RELU2_BF16   squared ReLU of the MLP up projection, input RMSNorm as a row scale
 //   EPI_SOFTCAP_F32  tanh soft-cap (+-cap) of the untied lm_head logits, final RMSNorm as a row
 //                    scale (hardware tanh)
+//   EPI_CE           the lm_head with soft-cap and cross-entropy: per row and 128-column group,
+//                    the sum of exp(logit) and the target's logit; no logits are stored
 //   EPI_QKV          split of the packed q|k|v projection, input RMSNorm as a row scale; RoPE
 //                    then per-head RMSNorm of q and k; on value-embedding layers
 //                    v += gate * ve[token] with gate = scale * sigmoid(rs * (x . w_gate))
@@ -79,12 +81,13 @@ constexpr int GATE_BYTES = MAX_GATE_HEADS * 128 * 2;   // gate weights of one 12
 // residual update that produces gate partials keeps each warp's copy of the gate weights of
 // its column group in shared memory (read by every lane at the same address), which costs
 // one operand stage.
+// The cross-entropy epilogue stores no tile at all: no staging buffers, a 7-stage ring.
 template <int KIND, int D>
 struct Cfg {
   static constexpr bool LSU_STORE = KIND == EPI_RELU2_BF16 || KIND == EPI_SOFTCAP_F32;
   static constexpr bool GATE = KIND == EPI_RESID && D == RESID_GATE;
-  static constexpr int STAGES = LSU_STORE ? 6 : (GATE ? 4 : 5);
-  static constexpr int SLAB_WARP = LSU_STORE ? SLAB_BUF : SLAB_BYTES;   // staging bytes per warp
+  static constexpr int STAGES = KIND == EPI_CE ? 7 : (LSU_STORE ? 6 : (GATE ? 4 : 5));
+  static constexpr int SLAB_WARP = KIND == EPI_CE ? 0 : (LSU_STORE ? SLAB_BUF : SLAB_BYTES);   // staging bytes per warp
   static constexpr int OFF_SLAB = STAGES * (A_BYTES + B_BYTES);
   static constexpr int OFF_GATE = OFF_SLAB + NUM_EPI_WARPS * SLAB_WARP;
   static constexpr int OFF_CTRL = OFF_GATE + (GATE ? NUM_EPI_WARPS * GATE_BYTES : 0);
@@ -233,7 +236,8 @@ struct PreRaw {
 struct EpiPre {
   float rs = 1.f;              // input RMSNorm row scale
   float g[2] = {0.f, 0.f};     // value-embedding gate per head of the column group (EPI_QKV)
-  int tok = -1;                // token id of the row when a gate applies, else -1
+  int tok = -1;                // EPI_QKV: token id of the row when a gate applies, else -1;
+                               // EPI_CE: the row's target
 };
 
 template <int KIND, int D>
@@ -248,13 +252,14 @@ __device__ __forceinline__ void pre_issue(PreRaw<D>& raw, int lane, int m0w, int
       prefetch_l2(ep.resid + off + l * 32);
       if (ep.Y != nullptr) prefetch_l2(ep.Y + off + l * 32);
     }
-  } else if constexpr (KIND == EPI_RELU2_BF16 || KIND == EPI_SOFTCAP_F32 || KIND == EPI_QKV) {
+  } else if constexpr (KIND == EPI_RELU2_BF16 || KIND == EPI_SOFTCAP_F32 || KIND == EPI_QKV || KIND == EPI_CE) {
     if (ep.ssp_in != nullptr) {
       const float* p = ep.ssp_in + static_cast<size_t>(m) * ep.ncg;
 #pragma unroll
       for (int g = 0; g < MAX_NCG; ++g)
         if (g < ep.ncg) raw.ss[g] = p[g];
     }
+    if constexpr (KIND == EPI_CE) raw.tok = ep.targets[m];
     if constexpr (KIND == EPI_QKV) {
       const int vcol0 = (ep.H + ep.Hkv) * D;
       if (ep.gp_in != nullptr && n0 + 128 > vcol0) {
@@ -279,7 +284,8 @@ __device__ __forceinline__ EpiPre pre_finish(const PreRaw<D>& raw, int lane, int
   EpiPre p;
   const int m = m0w + lane;
   if (n0 >= N || m >= M) return p;
-  if constexpr (KIND == EPI_RELU2_BF16 || KIND == EPI_SOFTCAP_F32 || KIND == EPI_QKV) {
+  if constexpr (KIND == EPI_RELU2_BF16 || KIND == EPI_SOFTCAP_F32 || KIND == EPI_QKV || KIND == EPI_CE) {
+    if constexpr (KIND == EPI_CE) p.tok = raw.tok;
     if (ep.ssp_in != nullptr) {
       float ss = 0.f;
 #pragma unroll
@@ -441,6 +447,46 @@ __device__ __forceinline__ void resid_begin(int lane, int m0w, int n0, int M, in
   }
   load_chunk_f32(ep.resid, N, m0w, n0, M, lane, rv);
   if (ep.Y != nullptr) load_chunk_f32(ep.Y, N, m0w, n0, M, lane, yv);
+}
+
+// Cross-entropy partials of the soft-capped lm_head, with no logits stored: per row, the sum
+// of exp(z) over the warp's 128 columns, z = cap * tanh(rs * acc / cap), and z at the row's
+// target column when the target lies in them.  |z| < cap bounds every term by e^cap, so the sum
+// needs no running maximum (cap = 15: under 2^22 per column, far inside fp32 for any vocabulary
+// this kernel can address).  The target's z is the same rounded value that entered the sum.
+__device__ __forceinline__ void epi_ce(uint32_t taddr, uint32_t tempty, int lane, int m0w, int n0, int M, int N,
+                                       const GemmEpi& ep, const EpiPre& pre) {
+  const float cap = ep.cap;
+  const float sc = pre.rs / cap;
+  const float l2e_cap = cap * 1.4426950408889634f;   // exp(cap * t) = 2^(log2(e) * cap * t)
+  const int tcol = pre.tok - n0;                      // the target's column among the warp's 128
+  float s0 = 0.f, s1 = 0.f, zt = 0.f;
+#pragma unroll 1
+  for (int ch = 0; ch < 4; ++ch) {
+    const int c0 = n0 + ch * 32;
+    if (c0 >= N) break;
+    uint32_t r[32];
+    tmem_ld32(taddr + ch * 32, r);
+    tmem_ld_wait(r);
+#pragma unroll
+    for (int j = 0; j < 32; j += 2) {
+      s0 += ex2_approx(tanh_approx(__uint_as_float(r[j]) * sc) * l2e_cap);
+      s1 += ex2_approx(tanh_approx(__uint_as_float(r[j + 1]) * sc) * l2e_cap);
+    }
+    const int tj = tcol - ch * 32;
+    if (static_cast<unsigned>(tj) < 32u) {   // rare: this chunk holds the row's target
+      float a = 0.f;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) a = j == tj ? __uint_as_float(r[j]) : a;
+      zt = cap * tanh_approx(a * sc);
+    }
+  }
+  release_acc(lane, tempty);
+  const int m = m0w + lane;
+  if (m < M && n0 < N) {
+    ep.ce_part[static_cast<size_t>(n0 / 128) * M + m] = s0 + s1;
+    if (tcol >= 0 && tcol < 128 && pre.tok < N) ep.ce_zt[m] = zt;
+  }
 }
 
 // Residual stream update (attention and MLP output projections), with the next consumer's
@@ -834,6 +880,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint32_t tempty = mapa_shared(smem_u32(&ctl->tempty[a]), 0);
       if constexpr (KIND == EPI_RESID) epi_resid<L::GATE>(taddr, tempty, lane, m0w, n0, M, N, ep, om, sl, gate_w, rv, yv);
       else if constexpr (KIND == EPI_SOFTCAP_F32) epi_softcap(taddr, tempty, lane, m0w, n0, M, N, ep, sl, pre);
+      else if constexpr (KIND == EPI_CE) epi_ce(taddr, tempty, lane, m0w, n0, M, N, ep, pre);
       else if constexpr (KIND == EPI_QKV) epi_qkv<D>(taddr, tempty, lane, m0w, n0, M, N, ep, om, sl, pre);
       else epi_bf16<KIND == EPI_RELU2_BF16>(taddr, tempty, lane, m0w, n0, M, N, ep, om, sl, pre);
     }
@@ -917,6 +964,9 @@ cudaError_t launch_gemm(const bf16* A, const bf16* B, int M, int N, int K, const
       if (ok) ok = make_tmap_bf16_2d(&om.o2, epi.xb, N, Mu, static_cast<uint64_t>(N) * 2, 64, 32);
       break;
     }
+    case EPI_CE:
+      ok = epi.targets != nullptr && epi.ce_part != nullptr && epi.ce_zt != nullptr && epi.cap > 0.f;
+      break;
     case EPI_SOFTCAP_F32:   // written with plain coalesced stores (16-byte aligned rows)
       ok = (reinterpret_cast<uintptr_t>(epi.out) % 16 == 0) && epi.ldo % 4 == 0;
       break;
@@ -945,6 +995,7 @@ cudaError_t launch_gemm(const bf16* A, const bf16* B, int M, int N, int K, const
       return launch_kind<EPI_RESID, 0>(ta, tb, om, M, N, K, epi, num_sms, stream);
     case EPI_RELU2_BF16: return launch_kind<EPI_RELU2_BF16, 0>(ta, tb, om, M, N, K, epi, num_sms, stream);
     case EPI_SOFTCAP_F32: return launch_kind<EPI_SOFTCAP_F32, 0>(ta, tb, om, M, N, K, epi, num_sms, stream);
+    case EPI_CE: return launch_kind<EPI_CE, 0>(ta, tb, om, M, N, K, epi, num_sms, stream);
     case EPI_QKV:
       if (epi.D == 128) return launch_kind<EPI_QKV, 128>(ta, tb, om, M, N, K, epi, num_sms, stream);
       if (epi.D == 64) return launch_kind<EPI_QKV, 64>(ta, tb, om, M, N, K, epi, num_sms, stream);

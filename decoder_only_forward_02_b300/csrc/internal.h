@@ -18,6 +18,7 @@ enum EpiKind : int {
   EPI_RELU2_BF16 = 2,   // out(bf16) = relu(rs * acc)^2
   EPI_SOFTCAP_F32 = 3,  // out(f32) = cap * tanh(rs * acc / cap)
   EPI_QKV = 4,          // q|k|v split, RoPE + RMSNorm on q and k, value-embedding gate on v
+  EPI_CE = 5,           // cross-entropy partials of z = cap * tanh(rs * acc / cap), no logits
 };
 
 // Columns covered by one partial sum of squares (one epilogue thread's share of a row).
@@ -67,6 +68,14 @@ struct GemmEpi {
   const bf16* ve = nullptr;       // [V, Hkv*D]
   const int32_t* tokens = nullptr;
   int V = 0;
+
+  // EPI_CE (uses ssp_in / cap): for each row m and 128-column group g (g = col / 128),
+  //   ce_part[g * M + m] = sum over the group's columns of exp(z[m, col])   (group-major);
+  //   ce_zt[m] = z[m, targets[m]], written by the group holding the target column (rows whose
+  //   target lies outside [0, N) are not written).
+  const int32_t* targets = nullptr;
+  float* ce_part = nullptr;
+  float* ce_zt = nullptr;
 };
 
 // Largest number of kv heads whose value-embedding gate partials one epilogue thread keeps.
@@ -111,6 +120,17 @@ cudaError_t launch_embed_smear(const int32_t* tokens, int B, int T, const bf16* 
 
 // table[i][t] = (cos, sin)(t * base^(-2i/D)), i < D/2, t < T (position fastest).
 cudaError_t launch_rope_table(float2* table, int T, int D, float base, cudaStream_t stream);
+
+// Cross-entropy from the EPI_CE partials: per row S = sum_g part[g * M + m] over G groups;
+// loss[m] = log S - zt[m] for targets in [0, V), 0 for ignored rows (target < 0; other targets
+// outside [0, V) record NC_ERR_TOKEN_RANGE and are ignored).  stats[0] = mean loss over the
+// counted rows, stats[1] = bits per byte (sum of the losses of rows whose target has a nonzero
+// byte count, over ln 2 times the sum of those byte counts; NaN without token_bytes or bytes).
+// scratch holds ce_scratch_doubles(M) doubles.  loss may be null.
+int ce_scratch_doubles(int M);
+cudaError_t launch_ce_finalize(const float* part, const float* zt, const int32_t* targets, int M, int G, int V,
+                               const int32_t* token_bytes, float* loss, float* stats, double* scratch,
+                               int* status, cudaStream_t stream);
 
 // y[M, H*D] = windowed causal GQA attention of q [M, H*D], k/v [M, Hkv*D].
 cudaError_t launch_attention(const bf16* q, const bf16* k, const bf16* v, int B, int T, int H,

@@ -231,7 +231,8 @@ const char* nc_last_cuda_error(void) { return nc::last_cuda_error_name(); }
 
 const char* nc_kernel_class_name(nc_kernel_class k) {
   static const char* names[NC_K_COUNT] = {"embed_smear", "qkv_rope_qknorm_ve", "attention", "oproj_residual",
-                                          "fc_relu2",    "proj_residual",      "lmhead_softcap"};
+                                          "fc_relu2",    "proj_residual",      "lmhead_softcap",
+                                          "cross_entropy"};
   return (k >= 0 && k < NC_K_COUNT) ? names[k] : "unknown";
 }
 
@@ -338,23 +339,37 @@ nc_status nc_workspace_bytes_host(const nc_model* m, int B, int T, size_t* bytes
   return NC_OK;
 }
 
-nc_status nc_forward(nc_model* m, const int32_t* tokens, int B, int T, float* logits,
-                     void* workspace, size_t ws_bytes, void* stream_) {
-  if (m == nullptr || tokens == nullptr || logits == nullptr || workspace == nullptr)
-    return NC_ERR_INVALID_ARG;
+}  // extern "C"
+
+namespace {
+
+// Argument checks shared by the forward entry points (before any device work).
+nc_status check_forward_args(const nc_model* m, const int32_t* tokens, int B, int T, const void* workspace) {
+  if (m == nullptr || tokens == nullptr || workspace == nullptr) return NC_ERR_INVALID_ARG;
   if (B < 1 || T < 1) return NC_ERR_INVALID_ARG;
   if (T > m->cfg.seq_len_ctx) return NC_ERR_UNSUPPORTED;
   if (static_cast<long long>(B) * T > (1LL << 30)) return NC_ERR_UNSUPPORTED;
-  if (!aligned(workspace, ALIGN) || !aligned(logits, 16) || !aligned(tokens, 4)) return NC_ERR_INVALID_ARG;
-  const Layout Lo = layout_for(m, B, T);
-  if (ws_bytes < Lo.end) return NC_ERR_WORKSPACE;
+  if (!aligned(workspace, ALIGN) || !aligned(tokens, 4)) return NC_ERR_INVALID_ARG;
+  return NC_OK;
+}
 
-  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+// Epilogue fields of a GEMM whose input is the residual stream's RMSNorm (row scale from ssp).
+void set_consumer(nc::GemmEpi& e, const nc_model* m, float* ssp) {
+  e.ssp_in = ssp;
+  e.ncg = m->C() / nc::SS_GROUP;
+  e.inv_ncols = 1.0f / static_cast<float>(m->C());
+  e.eps = m->cfg.rms_eps;
+  e.status = m->status;
+}
+
+// The embedding and every block, up to the final backout: leaves the lm_head's input (before
+// its RMSNorm) as xb with its partial sums of squares in ssp.
+cudaError_t run_blocks(nc_model* m, const int32_t* tokens, int B, int T, const Layout& Lo, uint8_t* ws,
+                       cudaStream_t stream) {
   const nc_config& c = m->cfg;
   const int M = B * T, C = c.n_embd, H = c.n_head, Hkv = c.n_kv_head, D = c.head_dim;
   const int F = c.mlp_hidden, V = c.vocab_size, L = c.n_layer;
   const int ncg = C / nc::SS_GROUP;
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
   float* x0 = reinterpret_cast<float*>(ws + Lo.x0);
   float* x = reinterpret_cast<float*>(ws + Lo.x);
   float* xm = reinterpret_cast<float*>(ws + Lo.xm);
@@ -370,14 +385,6 @@ nc_status nc_forward(nc_model* m, const int32_t* tokens, int B, int T, float* lo
   const int c_g = c.ve_gate_channels ? c.ve_gate_channels : C;
   const int mid = L / 2 - 1;
 
-  // Row-scale inputs shared by the consuming epilogues.
-  auto consumer = [&](nc::GemmEpi& e) {
-    e.ssp_in = ssp;
-    e.ncg = ncg;
-    e.inv_ncols = 1.0f / static_cast<float>(C);
-    e.eps = c.rms_eps;
-    e.status = m->status;
-  };
   // Residual-stream update of an output projection: x += acc, bf16 copy and partial sums.
   auto resid = [&](nc::GemmEpi& e) {
     e.kind = nc::EPI_RESID;
@@ -398,7 +405,7 @@ nc_status nc_forward(nc_model* m, const int32_t* tokens, int B, int T, float* lo
   for (int i = 0; i < L && e == cudaSuccess; ++i) {
     const bool ve = m->has_ve[i] != 0;
     nc::GemmEpi qe;
-    consumer(qe);
+    set_consumer(qe, m, ssp);
     qe.kind = nc::EPI_QKV;
     qe.q = q;
     qe.k = k;
@@ -428,7 +435,7 @@ nc_status nc_forward(nc_model* m, const int32_t* tokens, int B, int T, float* lo
     e = timed(m, NC_K_OPROJ, stream, [&] { return nc::launch_gemm(y, m->wo[i], M, C, H * D, oe, m->num_sms, stream); });
     if (e != cudaSuccess) break;
     nc::GemmEpi fe;
-    consumer(fe);
+    set_consumer(fe, m, ssp);
     fe.kind = nc::EPI_RELU2_BF16;
     fe.out = h;
     fe.ldo = F;
@@ -457,15 +464,97 @@ nc_status nc_forward(nc_model* m, const int32_t* tokens, int B, int T, float* lo
     }
     e = timed(m, NC_K_PROJ, stream, [&] { return nc::launch_gemm(h, m->wproj[i], M, C, F, pe, m->num_sms, stream); });
   }
+  return e;
+}
+
+// Loss-path buffers placed after the forward's layout: the cross-entropy partials
+// [ceil(V/128)][M], the target logits [M] and the reduction scratch.
+struct LossLayout {
+  size_t part, zt, scratch, end;
+};
+
+LossLayout loss_layout_for(const nc_model* m, const Layout& Lo, int B, int T) {
+  const size_t M = static_cast<size_t>(B) * T;
+  const size_t G = (m->cfg.vocab_size + 127) / 128;
+  LossLayout L{};
+  L.part = Lo.end;
+  L.zt = L.part + align_up(G * M * 4);
+  L.scratch = L.zt + align_up(M * 4);
+  L.end = L.scratch + align_up(static_cast<size_t>(nc::ce_scratch_doubles(static_cast<int>(M))) * sizeof(double));
+  return L;
+}
+
+}  // namespace
+
+extern "C" {
+
+nc_status nc_forward(nc_model* m, const int32_t* tokens, int B, int T, float* logits,
+                     void* workspace, size_t ws_bytes, void* stream_) {
+  nc_status s = check_forward_args(m, tokens, B, T, workspace);
+  if (s != NC_OK) return s;
+  if (logits == nullptr || !aligned(logits, 16)) return NC_ERR_INVALID_ARG;
+  const Layout Lo = layout_for(m, B, T);
+  if (ws_bytes < Lo.end) return NC_ERR_WORKSPACE;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  cudaError_t e = run_blocks(m, tokens, B, T, Lo, ws, stream);
   if (e == cudaSuccess) {
     nc::GemmEpi le;
-    consumer(le);
+    set_consumer(le, m, reinterpret_cast<float*>(ws + Lo.ssp));
     le.kind = nc::EPI_SOFTCAP_F32;
     le.out = logits;
-    le.ldo = V;
-    le.cap = c.softcap;
-    e = timed(m, NC_K_LMHEAD, stream, [&] { return nc::launch_gemm(xb, m->lm, M, V, C, le, m->num_sms, stream); });
+    le.ldo = m->cfg.vocab_size;
+    le.cap = m->cfg.softcap;
+    e = timed(m, NC_K_LMHEAD, stream, [&] {
+      return nc::launch_gemm(reinterpret_cast<bf16*>(ws + Lo.xb), m->lm, B * T, m->cfg.vocab_size, m->C(), le,
+                             m->num_sms, stream);
+    });
   }
+  return nc::cuda_status(e);
+}
+
+nc_status nc_workspace_bytes_loss(const nc_model* m, int B, int T, size_t* bytes) {
+  if (m == nullptr || bytes == nullptr || B < 1 || T < 1) return NC_ERR_INVALID_ARG;
+  if (T > m->cfg.seq_len_ctx) return NC_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * T > (1LL << 30)) return NC_ERR_UNSUPPORTED;
+  *bytes = loss_layout_for(m, layout_for(m, B, T), B, T).end;
+  return NC_OK;
+}
+
+nc_status nc_forward_loss(nc_model* m, const int32_t* tokens, const int32_t* targets, int B, int T,
+                          const int32_t* token_bytes, float* loss, float* stats, void* workspace,
+                          size_t ws_bytes, void* stream_) {
+  nc_status s = check_forward_args(m, tokens, B, T, workspace);
+  if (s != NC_OK) return s;
+  if (targets == nullptr || stats == nullptr || !aligned(targets, 4) || !aligned(stats, 4) ||
+      (loss != nullptr && !aligned(loss, 4)) || (token_bytes != nullptr && !aligned(token_bytes, 4)))
+    return NC_ERR_INVALID_ARG;
+  const Layout Lo = layout_for(m, B, T);
+  const LossLayout LL = loss_layout_for(m, Lo, B, T);
+  if (ws_bytes < LL.end) return NC_ERR_WORKSPACE;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const int M = B * T, V = m->cfg.vocab_size;
+  float* part = reinterpret_cast<float*>(ws + LL.part);
+  float* zt = reinterpret_cast<float*>(ws + LL.zt);
+  cudaError_t e = run_blocks(m, tokens, B, T, Lo, ws, stream);
+  if (e == cudaSuccess) {
+    nc::GemmEpi le;
+    set_consumer(le, m, reinterpret_cast<float*>(ws + Lo.ssp));
+    le.kind = nc::EPI_CE;
+    le.cap = m->cfg.softcap;
+    le.targets = targets;
+    le.ce_part = part;
+    le.ce_zt = zt;
+    e = timed(m, NC_K_LMHEAD, stream, [&] {
+      return nc::launch_gemm(reinterpret_cast<bf16*>(ws + Lo.xb), m->lm, M, V, m->C(), le, m->num_sms, stream);
+    });
+  }
+  if (e == cudaSuccess)
+    e = timed(m, NC_K_LOSS, stream, [&] {
+      return nc::launch_ce_finalize(part, zt, targets, M, (V + 127) / 128, V, token_bytes, loss, stats,
+                                    reinterpret_cast<double*>(ws + LL.scratch), m->status, stream);
+    });
   return nc::cuda_status(e);
 }
 
@@ -533,6 +622,11 @@ nc_status nc_timing_read(nc_model* m, nc_kernel_class k, double* total_ms, int* 
 int nc_forward_launch_count(const nc_model* m) {
   if (m == nullptr) return 0;
   return 2 + 5 * m->cfg.n_layer;
+}
+
+int nc_forward_loss_launch_count(const nc_model* m) {
+  if (m == nullptr) return 0;
+  return nc_forward_launch_count(m) + 2;   // + the two cross-entropy reduction kernels
 }
 
 }  // extern "C"

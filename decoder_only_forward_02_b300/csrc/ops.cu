@@ -145,4 +145,44 @@ nc_status nc_op_embed_smear(const int32_t* tokens, int B, int T, const void* wte
                                             Hkv, c_g, gp, status, static_cast<cudaStream_t>(stream)));
 }
 
+nc_status nc_op_lmhead_ce(const void* xf, const void* wlm, int M, int V, int C, const float* ssp, float eps,
+                          float cap, const int32_t* targets, float* part, float* zt, int* status, void* stream) {
+  if (!al(xf, 16) || !al(wlm, 16) || !al(part, 4) || !al(zt, 4) || targets == nullptr || M < 1 || V < 1 ||
+      C < 1 || !(cap > 0.f))
+    return NC_ERR_INVALID_ARG;
+  if (!al_or_null(ssp, 4) || (ssp != nullptr && C % nc::SS_GROUP != 0)) return NC_ERR_INVALID_ARG;
+  if (C % 64 != 0 || V % 32 != 0) return NC_ERR_UNSUPPORTED;
+  nc::GemmEpi e;
+  e.kind = nc::EPI_CE;
+  e.status = status;
+  e.cap = cap;
+  e.targets = targets;
+  e.ce_part = part;
+  e.ce_zt = zt;
+  if (ssp != nullptr) {
+    e.ssp_in = ssp;
+    e.ncg = C / nc::SS_GROUP;
+    e.inv_ncols = 1.0f / static_cast<float>(C);
+    e.eps = eps;
+  }
+  return cuda_status(nc::launch_gemm(static_cast<const nc::bf16*>(xf), static_cast<const nc::bf16*>(wlm), M, V, C,
+                                     e, device_sms(), static_cast<cudaStream_t>(stream)));
+}
+
+size_t nc_op_ce_scratch_bytes(int M) {
+  return M < 1 ? 0 : static_cast<size_t>(nc::ce_scratch_doubles(M)) * sizeof(double);
+}
+
+nc_status nc_op_ce_finalize(const float* part, const float* zt, const int32_t* targets, int M, int V,
+                            const int32_t* token_bytes, float* loss, float* stats, void* scratch,
+                            size_t scratch_bytes, int* status, void* stream) {
+  if (!al(part, 4) || !al(zt, 4) || targets == nullptr || !al(stats, 4) || !al(scratch, 8) ||
+      !al_or_null(loss, 4) || !al_or_null(token_bytes, 4) || M < 1 || V < 1)
+    return NC_ERR_INVALID_ARG;
+  if (scratch_bytes < nc_op_ce_scratch_bytes(M)) return NC_ERR_WORKSPACE;
+  return cuda_status(nc::launch_ce_finalize(part, zt, targets, M, (V + 127) / 128, V, token_bytes, loss, stats,
+                                            static_cast<double*>(scratch), status,
+                                            static_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"

@@ -174,6 +174,30 @@ NC_API nc_status nc_forward_host(nc_model *m, const int32_t *tokens_host, int B,
 NC_API nc_status nc_forward_static_scratch(nc_model *m, const int32_t *tokens, int B, int T,
                                            float *logits, void *stream);
 
+/* ---- loss path: fused lm_head + soft-cap + next-token cross-entropy, no logits ----
+ * "nanochat — 架构与原理", section 2 component table (metrics row: bits per byte from the
+ * loss evaluation) and "NanoChat基础训练报告", loss progression table (training loss and
+ * validation bits per byte).  The forward is that of nc_forward up to the final norm; the
+ * lm_head GEMM then keeps, per row and 128-column group, the sum of exp(logit) and the
+ * target's logit instead of writing the [B, T, V] logits, and two small kernels reduce them:
+ *   loss[b, t] = log(sum_v exp(z[b, t, v])) - z[b, t, targets[b, t]]      (nats)
+ * with z the soft-capped logits of nc_forward.  A negative target marks an ignored position
+ * (loss 0, not counted); a target >= V is recorded as NC_ERR_TOKEN_RANGE in the status word
+ * and ignored the same way.
+ *   stats[0] = mean loss over the counted positions (NaN if there are none);
+ *   stats[1] = bits per byte: the summed loss of the positions whose target has a nonzero
+ *              byte count, over ln 2 times the sum of those byte counts (NaN without
+ *              token_bytes or when no counted target has bytes).
+ * targets: device int32 [B, T], the token each position predicts (the caller shifts);
+ * token_bytes: device int32 [V] byte length of each vocabulary entry, or NULL;
+ * loss: device fp32 [B, T], or NULL; stats: device fp32 [2].  Both statistics are reduced in
+ * fp64 in a fixed order (bitwise repeatable).  workspace: device, >= nc_workspace_bytes_loss,
+ * 256-byte aligned, caller-owned.  Asynchronous on `stream`, errors as nc_forward. */
+NC_API nc_status nc_workspace_bytes_loss(const nc_model *m, int B, int T, size_t *bytes);
+NC_API nc_status nc_forward_loss(nc_model *m, const int32_t *tokens, const int32_t *targets, int B, int T,
+                                 const int32_t *token_bytes, float *loss, float *stats, void *workspace,
+                                 size_t ws_bytes, void *stream);
+
 /* Synchronise `stream`, read and clear the device status word. */
 NC_API nc_status nc_get_status(nc_model *m, void *stream);
 
@@ -196,8 +220,9 @@ typedef enum {
   NC_K_OPROJ = 3,     /* attention output projection + residual add (+ next norm's inputs) */
   NC_K_FC = 4,        /* MLP up projection: input RMSNorm + squared ReLU */
   NC_K_PROJ = 5,      /* MLP down projection + residual add, next block's mix / backout */
-  NC_K_LMHEAD = 6,    /* lm_head GEMM: final RMSNorm + tanh soft-cap */
-  NC_K_COUNT = 7
+  NC_K_LMHEAD = 6,    /* lm_head GEMM: final RMSNorm + tanh soft-cap (+ cross-entropy partials) */
+  NC_K_LOSS = 7,      /* cross-entropy reduction of the loss path */
+  NC_K_COUNT = 8
 } nc_kernel_class;
 
 /* enable != 0: every following nc_forward records an event pair around each
@@ -206,8 +231,9 @@ NC_API nc_status nc_timing_enable(nc_model *m, int enable);
 NC_API nc_status nc_timing_read(nc_model *m, nc_kernel_class k, double *total_ms, int *launches);
 NC_API const char *nc_kernel_class_name(nc_kernel_class k);
 
-/* Number of kernels one nc_forward launches for this model. */
+/* Number of kernels one nc_forward (nc_forward_loss) launches for this model. */
 NC_API int nc_forward_launch_count(const nc_model *m);
+NC_API int nc_forward_loss_launch_count(const nc_model *m);
 
 #ifdef __cplusplus
 }

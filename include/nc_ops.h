@@ -80,6 +80,25 @@ NC_API nc_status nc_op_embed_smear(const int32_t *tokens, int B, int T, const vo
                                    const void *wg, int Hkv, int c_g, float *gp, int *status,
                                    void *stream);
 
+/* Fused lm_head + soft-cap + cross-entropy partials (the loss path of nc_forward_loss): with
+ * z = cap * tanh(rs * (xf . wlm^T) / cap) (rs from ssp over C columns, as nc_op_gemm), for each
+ * row m and 128-column group g of the V columns:
+ *   part[g * M + m] = sum over the group's columns v of exp(z[m, v])     (group-major)
+ *   zt[m] = z[m, targets[m]] when 0 <= targets[m] < V (not written otherwise).
+ * xf bf16 [M, C], wlm bf16 [V, C]; part fp32 [ceil(V/128) * M]; zt, targets [M].  C % 64 == 0,
+ * V % 32 == 0. */
+NC_API nc_status nc_op_lmhead_ce(const void *xf, const void *wlm, int M, int V, int C, const float *ssp,
+                                 float eps, float cap, const int32_t *targets, float *part, float *zt,
+                                 int *status, void *stream);
+
+/* Cross-entropy from the partials of nc_op_lmhead_ce: loss[m] and stats[2] exactly as
+ * nc_forward_loss defines them (loss may be NULL; token_bytes device int32 [V] or NULL).
+ * scratch: device, >= nc_op_ce_scratch_bytes(M), 8-byte aligned. */
+NC_API size_t nc_op_ce_scratch_bytes(int M);
+NC_API nc_status nc_op_ce_finalize(const float *part, const float *zt, const int32_t *targets, int M, int V,
+                                   const int32_t *token_bytes, float *loss, float *stats, void *scratch,
+                                   size_t scratch_bytes, int *status, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

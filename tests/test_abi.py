@@ -92,9 +92,14 @@ def test_null_arguments_rejected_without_device_work():
     assert lib.nc_op_rope_table(None, 4, 8, 1e4, None) == 1
     assert lib.nc_op_embed_smear(None, 1, 1, None, 1, 128, None, 0, 0, 1e-6, 1.0, None, None, None, None, None, 0,
                                  0, None, None, None) == 1
+    assert lib.nc_op_lmhead_ce(None, None, 1, 32, 64, None, 1e-6, 15.0, None, None, None, None, None) == 1
+    assert lib.nc_op_ce_finalize(None, None, None, 1, 32, None, None, None, None, 0, None, None) == 1
+    assert lib.nc_op_ce_scratch_bytes(0) == 0 and lib.nc_op_ce_scratch_bytes(300) >= 16
+    assert lib.nc_forward_loss(None, None, None, 1, 1, None, None, None, None, 0, None) == 1
+    assert lib.nc_forward_loss_launch_count(None) == 0
 
 
 def test_kernel_class_names():
     lib = B.lib()
-    assert [lib.nc_kernel_class_name(i).decode() for i in range(7)] == B.KERNEL_CLASSES
-    assert lib.nc_kernel_class_name(7) == b"unknown"
+    assert [lib.nc_kernel_class_name(i).decode() for i in range(8)] == B.KERNEL_CLASSES
+    assert lib.nc_kernel_class_name(8) == b"unknown"

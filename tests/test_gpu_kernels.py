@@ -112,6 +112,59 @@ def test_gemm_relu2_and_softcap_row_scaled():
     assert float(z1.abs().max()) < 15.0
 
 
+# ------------------------------------------------------------------------ fused lm_head + cross-entropy
+
+@pytest.mark.parametrize("M,V,C,use_ssp", [(257, 1024, 768, True), (130, 992, 128, False)])
+def test_lmhead_cross_entropy(M, V, C, use_ssp):
+    A = _rand_bf16((M, C), seed=21)
+    Wl = _rand_bf16((V, C), scale=0.08, seed=22)
+    acc = bf16_np(A) @ bf16_np(Wl).T
+    ssp = torch.rand((M, C // 128), generator=torch.Generator().manual_seed(23)) * 200.0 if use_ssp else None
+    rs = 1.0 / np.sqrt(ssp.double().numpy().sum(1) / C + 1e-6) if use_ssp else np.ones(M)
+    g = torch.Generator().manual_seed(24)
+    tgt = torch.randint(0, V, (M,), generator=g, dtype=torch.int32)
+    tgt[:6] = torch.tensor([0, 127, 128, V - 1, -1, V - 97], dtype=torch.int32)   # group edges, ignored, last group
+    tb = torch.randint(0, 9, (V,), generator=g, dtype=torch.int32)
+    tb[:3] = 0
+    ops = _ops()
+    sspd = ssp.to(DEV) if use_ssp else None
+    part, zt = ops.lmhead_ce(A.to(DEV), Wl.to(DEV), tgt.to(DEV), ssp=sspd, C=C, cap=15.0)
+    loss, stats = ops.ce_finalize(part, zt, tgt.to(DEV), V, token_bytes=tb.to(DEV))
+    z_gpu = ops.gemm(A.to(DEV), Wl.to(DEV), "softcap_f32", ssp=sspd, C=C if use_ssp else 0, cap=15.0)
+    torch.cuda.synchronize()
+    got = loss.cpu().double().numpy()
+    t = tgt.numpy()
+    # against the oracle: each logit errs by at most cap * 2^-10 (hardware tanh, documented relative
+    # error below 2^-10), and the log-sum-exp is 1-Lipschitz in the largest logit error, so a loss
+    # errs by at most twice that
+    ref = O.cross_entropy(O.softcap(rs[:, None] * acc, 15.0), t)
+    np.testing.assert_allclose(got, ref, rtol=0, atol=2 * 15.0 * 2 ** -10)
+    # against fp64 cross-entropy of this GPU's own soft-capped logits (same tanh values): only the
+    # hardware exp2 (relative error near 2^-22) and fp32 sums differ
+    own = O.cross_entropy(z_gpu.cpu().double().numpy(), t)
+    np.testing.assert_allclose(got, own, rtol=0, atol=2e-4)
+    assert got[4] == 0.0
+    mean, bpb = O.loss_stats(own, t, tb.numpy())
+    st = stats.cpu().double().numpy()
+    np.testing.assert_allclose(st, [mean, bpb], rtol=1e-5)
+
+
+def test_cross_entropy_target_out_of_range_sets_status():
+    M, V, C = 64, 256, 128
+    A, Wl = _rand_bf16((M, C), seed=31), _rand_bf16((V, C), scale=0.05, seed=32)
+    tgt = torch.randint(0, V, (M,), generator=torch.Generator().manual_seed(33), dtype=torch.int32)
+    tgt[5] = V + 3
+    status = torch.zeros((1,), dtype=torch.int32, device=DEV)
+    part, zt = _ops().lmhead_ce(A.to(DEV), Wl.to(DEV), tgt.to(DEV), cap=15.0, status=status)
+    loss, stats = _ops().ce_finalize(part, zt, tgt.to(DEV), V, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 6   # NC_ERR_TOKEN_RANGE
+    assert float(loss[5]) == 0.0
+    own = O.cross_entropy(_ops().gemm(A.to(DEV), Wl.to(DEV), "softcap_f32", cap=15.0).cpu().double().numpy(),
+                          np.where(tgt.numpy() >= V, -1, tgt.numpy()))
+    np.testing.assert_allclose(float(stats[0]), own[np.arange(M) != 5].mean(), rtol=1e-5)
+
+
 # ------------------------------------------------------------------------ embedding
 
 @pytest.mark.parametrize("embed_norm,a,gate", [(False, 1.0, False), (True, 1.3, True)])

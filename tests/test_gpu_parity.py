@@ -113,3 +113,79 @@ def test_causality_bitwise():
     b = m.forward(tok2.to(DEV))
     assert torch.equal(a[:, :t], b[:, :t])
     assert not torch.equal(a[:, t:], b[:, t:])
+
+
+# ------------------------------------------------------------------------ loss path (fused lm_head + CE)
+
+def _targets_and_bytes(tok, V, seed=11):
+    """Next-token targets (the last position of each row ignored) and byte lengths of the
+    vocabulary (some zero, as for special tokens)."""
+    tgt = torch.full_like(tok, -1)
+    tgt[:, :-1] = tok[:, 1:]
+    tb = torch.randint(0, 9, (V,), generator=torch.Generator().manual_seed(seed), dtype=torch.int32)
+    tb[:5] = 0
+    return tgt, tb
+
+
+def _loss_bound():
+    # each loss errs by at most twice the largest logit error (log-sum-exp is 1-Lipschitz)
+    from tests.helpers import MAX_ABS
+    return 2 * MAX_ABS
+
+
+@pytest.mark.parametrize("name", ["tiny", "tiny_all"])
+def test_loss_path_tiny(name):
+    wl = get_workload(name)
+    cfg = wl.model
+    wts = make_weights(cfg, init="dense")
+    tok = make_tokens(wl)
+    tgt, tb = _targets_and_bytes(tok, cfg.vocab_size)
+    m, logits = _run(wl, wts, tok)
+    loss, stats = m.forward_loss(tok.to(DEV), tgt.to(DEV), token_bytes=tb.to(DEV))
+    assert m.status() == 0
+    got = loss.cpu().double().numpy().reshape(-1)
+    t = tgt.numpy().reshape(-1)
+    ref_logits = O.forward(cfg, O.OracleWeights.from_synth(cfg, wts), tok.numpy())
+    ref = O.cross_entropy(ref_logits.reshape(-1, cfg.vocab_size), t)
+    np.testing.assert_allclose(got, ref, rtol=0, atol=_loss_bound())
+    mean, bpb = O.loss_stats(ref, t, tb.numpy())
+    np.testing.assert_allclose(stats.cpu().double().numpy(), [mean, bpb], rtol=0, atol=_loss_bound())
+    # the logits path on this GPU gives the same losses up to exp2 rounding and summation order
+    own = O.cross_entropy(logits.cpu().double().numpy().reshape(-1, cfg.vocab_size), t)
+    np.testing.assert_allclose(got, own, rtol=0, atol=2e-4)
+
+
+def test_loss_path_d12_sampled_rows_and_batch_mean():
+    wl = get_workload("d12")
+    cfg = wl.model
+    wts = make_weights(cfg, seed=wl.seed, init=wl.init)
+    tok = make_tokens(wl)
+    tgt, tb = _targets_and_bytes(tok, cfg.vocab_size)
+    m, logits = _run(wl, wts, tok)
+    loss, stats = m.forward_loss(tok.to(DEV), tgt.to(DEV), token_bytes=tb.to(DEV))
+    assert m.status() == 0
+    W = O.OracleWeights.from_synth(cfg, wts)
+    for r in (0, 7):
+        ref_logits = O.forward_row(cfg, W, tok[r].numpy())
+        ref = O.cross_entropy(ref_logits, tgt[r].numpy())
+        np.testing.assert_allclose(loss[r].cpu().double().numpy(), ref, rtol=0, atol=_loss_bound())
+    # whole batch: the statistics agree with fp64 cross-entropy of the logits path
+    t = tgt.reshape(-1).numpy()
+    own = np.concatenate([O.cross_entropy(logits[b].cpu().double().numpy(), tgt[b].numpy())
+                          for b in range(tok.shape[0])])
+    np.testing.assert_allclose(loss.cpu().double().numpy().reshape(-1), own, rtol=0, atol=2e-4)
+    mean, bpb = O.loss_stats(own, t, tb.numpy())
+    np.testing.assert_allclose(stats.cpu().double().numpy(), [mean, bpb], rtol=1e-5)
+
+
+def test_loss_path_repeatable_and_launch_count():
+    wl = get_workload("tiny_all")
+    cfg = replace(wl.model, seq_len_ctx=256, window_left=(64,))
+    wts = make_weights(cfg, init="dense")
+    tok = torch.randint(0, cfg.vocab_size, (4, 256), generator=torch.Generator().manual_seed(9), dtype=torch.int32)
+    tgt, tb = _targets_and_bytes(tok, cfg.vocab_size)
+    m, _ = _run(cfg, wts, tok)
+    a = m.forward_loss(tok.to(DEV), tgt.to(DEV), token_bytes=tb.to(DEV))
+    b = m.forward_loss(tok.to(DEV), tgt.to(DEV), token_bytes=tb.to(DEV))
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+    assert m.launch_count(loss=True) == m.launch_count() + 2
