@@ -407,6 +407,11 @@ def run_single_kernel(args):
         ssp = torch.rand((M, C // 128), generator=g, device=dev) * 100
         out = torch.empty((M, V), dtype=torch.float32, device=dev)
         fn = lambda: ops.gemm(a, w, "softcap_f32", out=out, ssp=ssp, C=C, cap=c.softcap)
+    elif k == "lmhead_ce":   # the loss path's lm_head: soft-cap + cross-entropy partials, no logits
+        a, w = rnd((M, C)), rnd((V, C), 0.02)
+        ssp = torch.rand((M, C // 128), generator=g, device=dev) * 100
+        tgt = torch.randint(0, V, (M,), generator=g, device=dev, dtype=torch.int32)
+        fn = lambda: ops.lmhead_ce(a, w, tgt, ssp=ssp, C=C, cap=c.softcap)
     elif k == "embed":
         tok = torch.randint(0, V, (wl.B, wl.T), generator=g, device=dev, dtype=torch.int32)
         wte, sg = rnd((V, C), 0.02), rnd((C,), 0.02)
@@ -454,7 +459,7 @@ def main():
     ap.add_argument("--cpu-rows", type=int, default=4, help="batch rows the CPU baseline times")
     ap.add_argument("--ref-tokens", type=int, default=512)
     ap.add_argument("--only-kernel", default=None,
-                    help="launch one kernel class (qkv, attention, oproj, fc, proj, lmhead, embed) "
+                    help="launch one kernel class (qkv, attention, oproj, fc, proj, lmhead, lmhead_ce, embed) "
                          "at the workload's shapes, for profiler captures")
     ap.add_argument("--launches", type=int, default=3)
     ap.add_argument("--window", type=int, default=None)
