@@ -319,7 +319,8 @@ def run_ours(args, rank, world, local_rank):
     tpath = os.path.join(ROOT, "profiles", "traffic.json")
     if os.path.exists(tpath):
         t = json.load(open(tpath))
-        if t.get("kernel") == dom and t.get("workload") == wl.name and t.get("source_hash") == _src_hash():
+        if t.get("kernel") == dom and t.get("workload") == wl.name and \
+                t.get("source_hash") == _src_hash(t.get("sources")):
             traffic = t.get("bytes_per_launch")
     flops = model_flops(cfg, B, T)
     tflops = flops / (ms_step / 1000.0) / 1e12
@@ -424,19 +425,18 @@ def run_single_kernel(args):
     print(json.dumps({"kernel": k, "workload": wl.name, "launches": args.launches, "ok": True}))
 
 
-_HASH = None
-
-
-def _src_hash():
-    global _HASH
-    if _HASH is None:
-        import hashlib
-        h = hashlib.sha1()
-        d = os.path.join(ROOT, "decoder_only_forward_02_b300", "csrc")
-        for f in sorted(os.listdir(d)):
-            h.update(open(os.path.join(d, f), "rb").read())
-        _HASH = h.hexdigest()[:12]
-    return _HASH
+def _src_hash(files=None):
+    """sha1 (12 hex digits) of the named csrc files (all of csrc when None), in sorted order: the
+    sources the recorded DRAM traffic of a kernel depends on."""
+    import hashlib
+    h = hashlib.sha1()
+    d = os.path.join(ROOT, "decoder_only_forward_02_b300", "csrc")
+    for f in sorted(files if files else os.listdir(d)):
+        p = os.path.join(d, f)
+        if not os.path.isfile(p):
+            return None
+        h.update(open(p, "rb").read())
+    return h.hexdigest()[:12]
 
 
 def _weight_bytes(w):
