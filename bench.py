@@ -260,6 +260,42 @@ def run_ours(args, rank, world, local_rank):
                      "mean_loss_nats": float(sbuf[0].item()),
                      "note": "nc_forward_loss: lm_head fused with soft-cap and cross-entropy, no logits written"}
 
+    # The decode path (nc_prefill of T-1 tokens, then nc_decode_step: one new token per batch row
+    # at position T-1, the longest context, read from the KV cache), repeated at that position.
+    decode_path = None
+    if not args.no_decode_path:
+        T0 = T - 1
+        cache = model.kv_cache(B, T)
+        model.prefill(tok[:, :T0].contiguous(), cache, T)
+        prev, cur = tok[:, T0 - 1].contiguous(), tok[:, T0].contiguous()
+        lg = torch.empty((B, V), dtype=torch.float32, device=dev)
+        for _ in range(3):
+            model.decode_step(prev, cur, T0, cache, T, out=lg)
+        n_dec = max(1, min(args.steps, 50))
+        barrier()
+        torch.cuda.synchronize()
+        e4 = torch.cuda.Event(enable_timing=True)
+        e5 = torch.cuda.Event(enable_timing=True)
+        e4.record(stream)
+        for _ in range(n_dec):
+            model.decode_step(prev, cur, T0, cache, T, out=lg)
+        e5.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        if model.status() != 0:
+            raise RuntimeError("device status set on the decode path")
+        dt = torch.tensor([e4.elapsed_time(e5)], dtype=torch.float64, device=dev)
+        if world > 1:
+            dist.all_reduce(dt, op=dist.ReduceOp.MAX)
+        dec_ms = float(dt.item()) / n_dec
+        decode_path = {"metric": "decode tokens/s (one new token per batch row)", "value": world * B / (dec_ms / 1e3),
+                       "unit": UNIT, "ms_per_step": dec_ms, "steps": n_dec, "batch": B, "context": T,
+                       "gpu_launches_per_step": model.launch_count(kv=True),
+                       "note": "nc_decode_step at position T-1 after nc_prefill of T-1 tokens, repeated at that "
+                               "position; the GEMMs run at M = 2B rows (row pairs), so this is launch- and "
+                               "weight-read-bound, not tuned"}
+        del cache
+
     t_max = torch.tensor([ms], dtype=torch.float64, device=dev)
     if world > 1:
         dist.all_reduce(t_max, op=dist.ReduceOp.MAX)
@@ -346,6 +382,7 @@ def run_ours(args, rank, world, local_rank):
         "clocks": clk,
         "e2e": e2e,
         "loss_path": loss_path,
+        "decode_path": decode_path,
     }
     if not args.no_cpu_baseline and world >= 1:
         n = min(args.cpu_tokens, T)
@@ -454,6 +491,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-loss-path", action="store_true", help="skip timing the fused cross-entropy path")
+    ap.add_argument("--no-decode-path", action="store_true", help="skip timing the KV-cache decode step")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-tokens", type=int, default=2048)
     ap.add_argument("--cpu-rows", type=int, default=4, help="batch rows the CPU baseline times")

@@ -71,6 +71,15 @@ _SIGS = {
     "nc_kernel_class_name": (ctypes.c_char_p, [ctypes.c_int]),
     "nc_forward_launch_count": (ctypes.c_int, [ctypes.c_void_p]),
     "nc_forward_loss_launch_count": (ctypes.c_int, [ctypes.c_void_p]),
+    "nc_kv_launch_count": (ctypes.c_int, [ctypes.c_void_p]),
+    "nc_kv_cache_bytes": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)]),
+    "nc_workspace_bytes_decode": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)]),
+    "nc_prefill": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                                  ctypes.c_size_t, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
+                                  ctypes.c_void_p]),
+    "nc_decode_step": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+                                      ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_void_p,
+                                      ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "nc_workspace_bytes_loss": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
                                                ctypes.POINTER(ctypes.c_size_t)]),
     "nc_forward_loss": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int]
@@ -380,6 +389,47 @@ class Model:
                                     _stream_handle(stream)), "nc_forward_loss")
         return loss, stats
 
+    def kv_cache(self, B: int, T_max: int) -> torch.Tensor:
+        """A device buffer for the KV cache of B rows and up to T_max positions."""
+        n = ctypes.c_size_t()
+        check(lib().nc_kv_cache_bytes(self.handle, B, T_max, ctypes.byref(n)), "nc_kv_cache_bytes")
+        return torch.empty(n.value, dtype=torch.uint8, device=self.device)
+
+    def prefill(self, tokens: torch.Tensor, cache: torch.Tensor, T_max: int, out: Optional[torch.Tensor] = None,
+                stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+        """tokens: device int32 [B, T] -> logits fp32 [B, T, V]; fills the cache with positions 0..T-1."""
+        if tokens.dtype != torch.int32 or not tokens.is_cuda or not tokens.is_contiguous():
+            raise ValueError("tokens must be a contiguous int32 CUDA tensor")
+        B, T = tokens.shape
+        if out is None:
+            out = torch.empty((B, T, self.cfg.vocab_size), dtype=torch.float32, device=self.device)
+        ws = self.workspace(B, T)
+        check(lib().nc_prefill(self.handle, tokens.data_ptr(), B, T, cache.data_ptr(), cache.numel(), T_max,
+                               out.data_ptr(), ws.data_ptr(), ws.numel(), _stream_handle(stream)), "nc_prefill")
+        return out
+
+    def decode_step(self, prev_tokens: torch.Tensor, tokens: torch.Tensor, pos: int, cache: torch.Tensor,
+                    T_max: int, out: Optional[torch.Tensor] = None,
+                    stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+        """tokens / prev_tokens: device int32 [B] (positions pos and pos - 1) -> logits fp32 [B, V] of
+        position pos; appends the new keys and values to the cache."""
+        for name, t in (("tokens", tokens), ("prev_tokens", prev_tokens)):
+            if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
+                raise ValueError(f"{name} must be a contiguous int32 CUDA tensor")
+        B = tokens.shape[0]
+        if out is None:
+            out = torch.empty((B, self.cfg.vocab_size), dtype=torch.float32, device=self.device)
+        key = ("decode", B)
+        if key not in self._ws:
+            n = ctypes.c_size_t()
+            check(lib().nc_workspace_bytes_decode(self.handle, B, ctypes.byref(n)), "nc_workspace_bytes_decode")
+            self._ws[key] = torch.empty(n.value, dtype=torch.uint8, device=self.device)
+        ws = self._ws[key]
+        check(lib().nc_decode_step(self.handle, prev_tokens.data_ptr(), tokens.data_ptr(), B, pos, cache.data_ptr(),
+                                   cache.numel(), T_max, out.data_ptr(), ws.data_ptr(), ws.numel(),
+                                   _stream_handle(stream)), "nc_decode_step")
+        return out
+
     def forward_host(self, tokens: torch.Tensor, out: torch.Tensor,
                      stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
         """tokens: host int32 [B, T] (pinned for full speed) -> out: host fp32 [B, T, V]; synchronous."""
@@ -405,6 +455,7 @@ class Model:
             out[name] = (ms.value, n.value)
         return out
 
-    def launch_count(self, loss: bool = False) -> int:
-        fn = lib().nc_forward_loss_launch_count if loss else lib().nc_forward_launch_count
+    def launch_count(self, loss: bool = False, kv: bool = False) -> int:
+        fn = lib().nc_forward_loss_launch_count if loss else (lib().nc_kv_launch_count if kv
+                                                              else lib().nc_forward_launch_count)
         return fn(self.handle)

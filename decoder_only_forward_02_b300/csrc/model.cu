@@ -16,10 +16,12 @@
 //                then x = lr_{i+1} x + l0_{i+1} x0 for the next block (+ its VE gate partials),
 //                or after the last layer x - lb * x_mid (final norm's input)
 //   lm_head GEMM (row scale, soft-cap)
+#include "decode.h"
 #include "internal.h"
 
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -362,10 +364,47 @@ void set_consumer(nc::GemmEpi& e, const nc_model* m, float* ssp) {
   e.status = m->status;
 }
 
+// KV cache of the prefill / decode path: per layer, keys then values, each [B][cap][Hkv*D]
+// bf16, cap = T_max on full layers and min(T_max, W + 1) on a layer with window W (position j in
+// slot j % cap).
+int kv_cap(const nc_model* m, int layer, int T_max) {
+  const int w = m->window[layer];
+  return w < 0 ? T_max : std::min(T_max, w + 1);
+}
+
+size_t kv_tensor_bytes(const nc_model* m, int B, int cap) {
+  return align_up(static_cast<size_t>(B) * cap * m->cfg.n_kv_head * m->cfg.head_dim * sizeof(bf16));
+}
+
+size_t kv_cache_bytes(const nc_model* m, int B, int T_max) {
+  size_t n = 0;
+  for (int i = 0; i < m->cfg.n_layer; ++i) n += 2 * kv_tensor_bytes(m, B, kv_cap(m, i, T_max));
+  return n;
+}
+
+// Where a forward writes its keys and values and which attention it runs.
+struct KvCtx {
+  uint8_t* cache = nullptr;
+  int T_max = 0;
+  bool decode = false;   // rows come in (pos - 1, pos) pairs; only the second of each pair is real
+  int pos = 0;           // decode: the position of the new token
+  float* scratch = nullptr;   // decode: split partials of the attention
+  size_t scratch_floats = 0;
+};
+
+// Decode workspace: the forward's layout for B row pairs, then the pair tokens [B][2], the
+// pair logits [B][2][V] and the decode attention's split partials.
+size_t decode_scratch_floats(const nc_model* m, int B) {
+  return static_cast<size_t>(B) * m->cfg.n_head * nc::decode_attention_splits(m->cfg.seq_len_ctx) *
+         (m->cfg.head_dim + 2);
+}
+
 // The embedding and every block, up to the final backout: leaves the lm_head's input (before
-// its RMSNorm) as xb with its partial sums of squares in ssp.
+// its RMSNorm) as xb with its partial sums of squares in ssp.  With kv, each layer's keys and
+// values also go to the cache (prefill: the positions the layer's window can still see; decode:
+// the new position), and a decode step attends over the cache.
 cudaError_t run_blocks(nc_model* m, const int32_t* tokens, int B, int T, const Layout& Lo, uint8_t* ws,
-                       cudaStream_t stream) {
+                       cudaStream_t stream, const KvCtx* kv = nullptr) {
   const nc_config& c = m->cfg;
   const int M = B * T, C = c.n_embd, H = c.n_head, Hkv = c.n_kv_head, D = c.head_dim;
   const int F = c.mlp_hidden, V = c.vocab_size, L = c.n_layer;
@@ -384,6 +423,7 @@ cudaError_t run_blocks(nc_model* m, const int32_t* tokens, int B, int T, const L
   const int c_s = c.smear_gate_channels ? c.smear_gate_channels : C;
   const int c_g = c.ve_gate_channels ? c.ve_gate_channels : C;
   const int mid = L / 2 - 1;
+  uint8_t* kv_next = kv != nullptr ? kv->cache : nullptr;   // the current layer's keys, then values
 
   // Residual-stream update of an output projection: x += acc, bf16 copy and partial sums.
   auto resid = [&](nc::GemmEpi& e) {
@@ -416,6 +456,7 @@ cudaError_t run_blocks(nc_model* m, const int32_t* tokens, int B, int T, const L
     qe.T = T;
     qe.rope = m->rope;
     qe.rope_ld = c.seq_len_ctx;
+    if (kv != nullptr && kv->decode) qe.rope = m->rope + (kv->pos - 1);   // row pair at positions pos-1, pos
     qe.gp_in = ve ? gp : nullptr;
     qe.gate_scale = c.ve_gate_scale;
     qe.ve = m->ve[i];
@@ -426,9 +467,29 @@ cudaError_t run_blocks(nc_model* m, const int32_t* tokens, int B, int T, const L
                              qe, m->num_sms, stream);
     });
     if (e != cudaSuccess) break;
-    e = timed(m, NC_K_ATTN, stream, [&] {
-      return nc::launch_attention(q, k, v, B, T, H, Hkv, D, m->window[i], y, m->status, stream);
-    });
+    if (kv != nullptr) {
+      const int cap = kv_cap(m, i, kv->T_max);
+      bf16* kc = reinterpret_cast<bf16*>(kv_next);
+      bf16* vc = reinterpret_cast<bf16*>(kv_next + kv_tensor_bytes(m, B, cap));
+      kv_next += 2 * kv_tensor_bytes(m, B, cap);
+      e = timed(m, NC_K_ATTN, stream, [&] {
+        if (kv->decode) return nc::launch_kv_append(k, v, B, 2, 1, 1, kv->pos - 1, Hkv * D, kc, vc, cap, stream);
+        const int first = std::max(0, T - cap);
+        return nc::launch_kv_append(k, v, B, T, first, T - first, 0, Hkv * D, kc, vc, cap, stream);
+      });
+      if (e != cudaSuccess) break;
+      if (kv->decode) {
+        e = timed(m, NC_K_ATTN, stream, [&] {
+          return nc::launch_decode_attention(q, B, 2, 1, H, Hkv, D, kc, vc, cap, kv->pos, m->window[i], y, kv->scratch,
+                                             kv->scratch_floats, stream);
+        });
+        if (e != cudaSuccess) break;
+      }
+    }
+    if (kv == nullptr || !kv->decode)
+      e = timed(m, NC_K_ATTN, stream, [&] {
+        return nc::launch_attention(q, k, v, B, T, H, Hkv, D, m->window[i], y, m->status, stream);
+      });
     if (e != cudaSuccess) break;
     nc::GemmEpi oe;
     resid(oe);
@@ -558,6 +619,109 @@ nc_status nc_forward_loss(nc_model* m, const int32_t* tokens, const int32_t* tar
   return nc::cuda_status(e);
 }
 
+nc_status nc_kv_cache_bytes(const nc_model* m, int B, int T_max, size_t* bytes) {
+  if (m == nullptr || bytes == nullptr || B < 1 || T_max < 1) return NC_ERR_INVALID_ARG;
+  if (T_max > m->cfg.seq_len_ctx) return NC_ERR_UNSUPPORTED;
+  *bytes = kv_cache_bytes(m, B, T_max);
+  return NC_OK;
+}
+
+nc_status nc_prefill(nc_model* m, const int32_t* tokens, int B, int T, void* kv_cache, size_t cache_bytes,
+                     int T_max, float* logits, void* workspace, size_t ws_bytes, void* stream_) {
+  nc_status s = check_forward_args(m, tokens, B, T, workspace);
+  if (s != NC_OK) return s;
+  if (logits == nullptr || !aligned(logits, 16) || kv_cache == nullptr || !aligned(kv_cache, ALIGN))
+    return NC_ERR_INVALID_ARG;
+  if (T_max < T) return NC_ERR_INVALID_ARG;
+  if (T_max > m->cfg.seq_len_ctx) return NC_ERR_UNSUPPORTED;
+  if (cache_bytes < kv_cache_bytes(m, B, T_max)) return NC_ERR_WORKSPACE;
+  const Layout Lo = layout_for(m, B, T);
+  if (ws_bytes < Lo.end) return NC_ERR_WORKSPACE;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  KvCtx kv;
+  kv.cache = static_cast<uint8_t*>(kv_cache);
+  kv.T_max = T_max;
+  cudaError_t e = run_blocks(m, tokens, B, T, Lo, ws, stream, &kv);
+  if (e == cudaSuccess) {
+    nc::GemmEpi le;
+    set_consumer(le, m, reinterpret_cast<float*>(ws + Lo.ssp));
+    le.kind = nc::EPI_SOFTCAP_F32;
+    le.out = logits;
+    le.ldo = m->cfg.vocab_size;
+    le.cap = m->cfg.softcap;
+    e = timed(m, NC_K_LMHEAD, stream, [&] {
+      return nc::launch_gemm(reinterpret_cast<bf16*>(ws + Lo.xb), m->lm, B * T, m->cfg.vocab_size, m->C(), le,
+                             m->num_sms, stream);
+    });
+  }
+  return nc::cuda_status(e);
+}
+
+nc_status nc_workspace_bytes_decode(const nc_model* m, int B, size_t* bytes) {
+  if (m == nullptr || bytes == nullptr || B < 1) return NC_ERR_INVALID_ARG;
+  if (m->cfg.seq_len_ctx < 2) return NC_ERR_UNSUPPORTED;
+  const size_t rows = 2 * static_cast<size_t>(B);
+  *bytes = layout_for(m, B, 2).end + align_up(rows * 4) + align_up(rows * m->cfg.vocab_size * 4) +
+           align_up(decode_scratch_floats(m, B) * 4);
+  return NC_OK;
+}
+
+nc_status nc_decode_step(nc_model* m, const int32_t* prev_tokens, const int32_t* tokens, int B, int pos,
+                         void* kv_cache, size_t cache_bytes, int T_max, float* logits, void* workspace,
+                         size_t ws_bytes, void* stream_) {
+  if (m == nullptr || prev_tokens == nullptr || tokens == nullptr || logits == nullptr || kv_cache == nullptr ||
+      workspace == nullptr || B < 1)
+    return NC_ERR_INVALID_ARG;
+  if (!aligned(prev_tokens, 4) || !aligned(tokens, 4) || !aligned(logits, 16) || !aligned(kv_cache, ALIGN) ||
+      !aligned(workspace, ALIGN))
+    return NC_ERR_INVALID_ARG;
+  if (pos < 1 || pos >= T_max) return NC_ERR_INVALID_ARG;
+  if (T_max > m->cfg.seq_len_ctx) return NC_ERR_UNSUPPORTED;
+  if (cache_bytes < kv_cache_bytes(m, B, T_max)) return NC_ERR_WORKSPACE;
+  size_t need = 0;
+  nc_status s = nc_workspace_bytes_decode(m, B, &need);
+  if (s != NC_OK) return s;
+  if (ws_bytes < need) return NC_ERR_WORKSPACE;
+  const Layout Lo = layout_for(m, B, 2);
+  const int V = m->cfg.vocab_size;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int32_t* pair = reinterpret_cast<int32_t*>(ws + Lo.end);                        // [B][2] (prev, token)
+  float* logits2 = reinterpret_cast<float*>(ws + Lo.end + align_up(2 * static_cast<size_t>(B) * 4));   // [B][2][V]
+  float* attn_scratch = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(logits2) +
+                                                 align_up(2 * static_cast<size_t>(B) * V * 4));
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  // Each row becomes the pair (previous token, new token): the embedding's smear then sees the
+  // previous token, and with the rotary table offset by pos - 1 the pair sits at positions
+  // pos - 1, pos.  Only the second row of a pair is used; every kernel but attention treats
+  // rows independently, and the decode attention reads the cache for the second rows only.
+  cudaError_t e = cudaMemcpy2DAsync(pair, 8, prev_tokens, 4, 4, B, cudaMemcpyDeviceToDevice, stream);
+  if (e == cudaSuccess) e = cudaMemcpy2DAsync(pair + 1, 8, tokens, 4, 4, B, cudaMemcpyDeviceToDevice, stream);
+  KvCtx kv;
+  kv.cache = static_cast<uint8_t*>(kv_cache);
+  kv.T_max = T_max;
+  kv.decode = true;
+  kv.pos = pos;
+  kv.scratch = attn_scratch;
+  kv.scratch_floats = decode_scratch_floats(m, B);
+  if (e == cudaSuccess) e = run_blocks(m, pair, B, 2, Lo, ws, stream, &kv);
+  if (e == cudaSuccess) {
+    nc::GemmEpi le;
+    set_consumer(le, m, reinterpret_cast<float*>(ws + Lo.ssp));
+    le.kind = nc::EPI_SOFTCAP_F32;
+    le.out = logits2;
+    le.ldo = V;
+    le.cap = m->cfg.softcap;
+    e = timed(m, NC_K_LMHEAD, stream, [&] {
+      return nc::launch_gemm(reinterpret_cast<bf16*>(ws + Lo.xb), m->lm, 2 * B, V, m->C(), le, m->num_sms, stream);
+    });
+  }
+  if (e == cudaSuccess)   // the second row of each pair
+    e = cudaMemcpy2DAsync(logits, static_cast<size_t>(V) * 4, logits2 + V, 2 * static_cast<size_t>(V) * 4,
+                          static_cast<size_t>(V) * 4, B, cudaMemcpyDeviceToDevice, stream);
+  return nc::cuda_status(e);
+}
+
 nc_status nc_forward_host(nc_model* m, const int32_t* tokens_host, int B, int T, float* logits_host,
                           void* workspace, size_t ws_bytes, void* stream_) {
   if (m == nullptr || tokens_host == nullptr || logits_host == nullptr || workspace == nullptr)
@@ -622,6 +786,12 @@ nc_status nc_timing_read(nc_model* m, nc_kernel_class k, double* total_ms, int* 
 int nc_forward_launch_count(const nc_model* m) {
   if (m == nullptr) return 0;
   return 2 + 5 * m->cfg.n_layer;
+}
+
+int nc_kv_launch_count(const nc_model* m) {
+  if (m == nullptr) return 0;
+  return 2 + 7 * m->cfg.n_layer;   // a decode step: per layer q|k|v, cache append, the two attention
+                                   // passes, out-projection, fc, down projection (a prefill: one fewer)
 }
 
 int nc_forward_loss_launch_count(const nc_model* m) {

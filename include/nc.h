@@ -198,6 +198,36 @@ NC_API nc_status nc_forward_loss(nc_model *m, const int32_t *tokens, const int32
                                  const int32_t *token_bytes, float *loss, float *stats, void *workspace,
                                  size_t ws_bytes, void *stream);
 
+/* ---- KV cache: prefill + single-token decode ----
+ * "nanochat — 架构与原理", section 2 component table (inference engine: KV cache and sampling)
+ * and section 7 code map (Engine, KVCache); "Nanochat在nanoGPT之上的新增功能", section 1 table
+ * and notes (per-layer sliding windows, GQA).  The cache keeps, per layer and batch row, the
+ * post-RoPE, post-QK-norm keys and the values (value embedding included) of the positions the
+ * layer can still attend to: all T_max positions on full layers, the last W+1 on a layer with
+ * window W (position j in slot j % (W+1)).  Layout per layer: keys then values, each
+ * [B][cap][Hkv*D] bf16, 256-byte aligned; the caller owns the buffer (>= nc_kv_cache_bytes,
+ * 256-byte aligned) and T_max <= seq_len_ctx.
+ *
+ * nc_prefill: nc_forward over tokens [B, T] (T <= T_max) that also fills the cache with
+ * positions 0..T-1; logits fp32 [B, T, V]; workspace as nc_forward (nc_workspace_bytes(B, T)).
+ *
+ * nc_decode_step: one new token per batch row, all at position pos (1 <= pos < T_max):
+ * tokens (device int32 [B]) are the tokens at pos, prev_tokens those at pos - 1 (the smear
+ * reads the previous token's embedding); appends the new keys and values at pos and writes the
+ * logits of position pos, fp32 [B, V].  The result equals row pos of nc_forward over the whole
+ * sequence (up to rounding: the decode attention keeps p in fp32 where the batched one rounds
+ * it to bf16).  workspace: >= nc_workspace_bytes_decode(B), 256-byte aligned.
+ * Both are asynchronous on `stream`; errors as nc_forward.  nc_kv_launch_count gives the kernels a
+ * decode step launches (2 + 7 * n_layer; a prefill launches 2 + 6 * n_layer). */
+NC_API nc_status nc_kv_cache_bytes(const nc_model *m, int B, int T_max, size_t *bytes);
+NC_API nc_status nc_prefill(nc_model *m, const int32_t *tokens, int B, int T, void *kv_cache, size_t cache_bytes,
+                            int T_max, float *logits, void *workspace, size_t ws_bytes, void *stream);
+NC_API nc_status nc_workspace_bytes_decode(const nc_model *m, int B, size_t *bytes);
+NC_API nc_status nc_decode_step(nc_model *m, const int32_t *prev_tokens, const int32_t *tokens, int B, int pos,
+                                void *kv_cache, size_t cache_bytes, int T_max, float *logits, void *workspace,
+                                size_t ws_bytes, void *stream);
+NC_API int nc_kv_launch_count(const nc_model *m);
+
 /* Synchronise `stream`, read and clear the device status word. */
 NC_API nc_status nc_get_status(nc_model *m, void *stream);
 

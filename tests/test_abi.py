@@ -97,6 +97,10 @@ def test_null_arguments_rejected_without_device_work():
     assert lib.nc_op_ce_scratch_bytes(0) == 0 and lib.nc_op_ce_scratch_bytes(300) >= 16
     assert lib.nc_forward_loss(None, None, None, 1, 1, None, None, None, None, 0, None) == 1
     assert lib.nc_forward_loss_launch_count(None) == 0
+    assert lib.nc_kv_launch_count(None) == 0
+    assert lib.nc_kv_cache_bytes(None, 1, 1, None) == 1
+    assert lib.nc_prefill(None, None, 1, 1, None, 0, 1, None, None, 0, None) == 1
+    assert lib.nc_decode_step(None, None, None, 1, 1, None, 0, 2, None, None, 0, None) == 1
 
 
 def test_kernel_class_names():

@@ -1,0 +1,80 @@
+"""KV-cache prefill + single-token decode (C ABI, CUDA kernels) against the fp64 oracle.
+
+The forward is causal, so the logits a decode step produces at position p must equal row p of
+the oracle's forward over the whole sequence; prefill logits must equal rows 0..T0-1.  The
+tiny case covers GQA (H = 2, Hkv = 1), D = 64 and windows shorter than the prefill (the
+layer's cache ring wraps); d12 covers D = 128 and the window-512 ring at full size."""
+from dataclasses import replace
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from synth import get_workload, make_tokens, make_weights
+from tests.helpers import assert_parity, binding, to_device
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _decode_run(m, tok, T0, T_max, positions):
+    cache = m.kv_cache(tok.shape[0], T_max)
+    pre = m.prefill(tok[:, :T0].contiguous().to(DEV), cache, T_max)
+    steps = []
+    for p in positions:
+        steps.append(m.decode_step(tok[:, p - 1].contiguous().to(DEV), tok[:, p].contiguous().to(DEV), p, cache,
+                                   T_max).clone())
+    assert m.status() == 0
+    return pre, torch.stack(steps, 1)
+
+
+def test_decode_tiny_gqa_windows_wrap():
+    wl = get_workload("tiny_all")
+    cfg = replace(wl.model, n_layer=3, window_left=(16, 16, -1), has_ve=(1, 0, 1), seq_len_ctx=64)
+    wts = make_weights(cfg, init="dense")
+    tok = torch.randint(0, cfg.vocab_size, (2, 64), generator=torch.Generator().manual_seed(21), dtype=torch.int32)
+    m = binding().Model(cfg, to_device(wts))
+    T0 = 20
+    pos = list(range(T0, 64))
+    pre, dec = _decode_run(m, tok, T0, 64, pos)
+    ref = O.forward(cfg, O.OracleWeights.from_synth(cfg, wts), tok.numpy())
+    assert_parity(pre.cpu().numpy(), ref[:, :T0], "prefill")
+    assert_parity(dec.cpu().numpy(), ref[:, T0:], "decode")
+    full = m.forward(tok.to(DEV)).cpu().numpy()
+    np.testing.assert_allclose(dec.cpu().numpy(), full[:, T0:], rtol=0, atol=2e-2)
+    np.testing.assert_array_equal(pre.cpu().numpy(), full[:, :T0])   # prefill is the forward itself
+
+
+def test_decode_d12_tail_positions():
+    wl = get_workload("d12")
+    cfg = wl.model
+    wts = make_weights(cfg, seed=wl.seed, init=wl.init)
+    tok = make_tokens(wl)
+    m = binding().Model(cfg, to_device(wts))
+    T0 = wl.T - 8
+    pos = list(range(T0, wl.T))
+    _, dec = _decode_run(m, tok, T0, wl.T, pos)
+    full = m.forward(tok.to(DEV))
+    got = dec.cpu().numpy()
+    assert_parity(got, full[:, T0:].cpu().numpy(), "decode vs forward")
+    ref = O.forward_row(cfg, O.OracleWeights.from_synth(cfg, wts), tok[0].numpy(), positions=pos)
+    assert_parity(got[0], ref, "decode vs oracle row 0")
+
+
+def test_decode_argument_errors():
+    wl = get_workload("tiny_all")
+    cfg = replace(wl.model, seq_len_ctx=64)
+    m = binding().Model(cfg, to_device(make_weights(cfg, init="dense")))
+    tok = torch.zeros((1,), dtype=torch.int32, device=DEV)
+    cache = m.kv_cache(1, 32)
+    lib = binding().lib()
+    ws = torch.empty(1 << 20, dtype=torch.uint8, device=DEV)
+    out = torch.empty((1, cfg.vocab_size), device=DEV)
+    args = lambda pos, cap_bytes, T_max: (m.handle, tok.data_ptr(), tok.data_ptr(), 1, pos, cache.data_ptr(),
+                                          cap_bytes, T_max, out.data_ptr(), ws.data_ptr(), ws.numel(), None)
+    assert lib.nc_decode_step(*args(0, cache.numel(), 32)) == 1          # pos must be >= 1
+    assert lib.nc_decode_step(*args(32, cache.numel(), 32)) == 1         # pos < T_max
+    assert lib.nc_decode_step(*args(5, cache.numel(), 65)) == 2          # T_max > seq_len_ctx
+    assert lib.nc_decode_step(*args(5, cache.numel() - 1, 32)) == 3      # cache too small
+    assert m.launch_count(kv=True) == 2 + 7 * cfg.n_layer
