@@ -29,6 +29,23 @@ UNIT = "tokens/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 
 
+def max_over_ranks(ms: float, world: int, device=None) -> float:
+    """The largest of the ranks' times: the job ends with its slowest rank (an all-reduce MAX
+    over the default process group when world > 1)."""
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(world: int, units_per_rank: float, ms: float) -> float:
+    """Units per second over the whole job: every rank processes units_per_rank (a replica of the
+    full workload, weak scaling) within the slowest rank's ms."""
+    return world * units_per_rank / (ms / 1000.0)
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -250,11 +267,8 @@ def run_ours(args, rank, world, local_rank):
         barrier()
         if model.status() != 0:
             raise RuntimeError("device status set on the loss path")
-        lt = torch.tensor([e2.elapsed_time(e3)], dtype=torch.float64, device=dev)
-        if world > 1:
-            dist.all_reduce(lt, op=dist.ReduceOp.MAX)
-        loss_ms = float(lt.item()) / n_loss
-        loss_path = {"metric": "forward + cross-entropy tokens/s", "value": world * B * T / (loss_ms / 1000.0),
+        loss_ms = max_over_ranks(e2.elapsed_time(e3), world, dev) / n_loss
+        loss_path = {"metric": "forward + cross-entropy tokens/s", "value": job_rate(world, B * T, loss_ms),
                      "unit": UNIT, "ms_per_step": loss_ms, "steps": n_loss,
                      "gpu_launches_per_step": model.launch_count(loss=True),
                      "mean_loss_nats": float(sbuf[0].item()),
@@ -284,11 +298,8 @@ def run_ours(args, rank, world, local_rank):
         barrier()
         if model.status() != 0:
             raise RuntimeError("device status set on the decode path")
-        dt = torch.tensor([e4.elapsed_time(e5)], dtype=torch.float64, device=dev)
-        if world > 1:
-            dist.all_reduce(dt, op=dist.ReduceOp.MAX)
-        dec_ms = float(dt.item()) / n_dec
-        decode_path = {"metric": "decode tokens/s (one new token per batch row)", "value": world * B / (dec_ms / 1e3),
+        dec_ms = max_over_ranks(e4.elapsed_time(e5), world, dev) / n_dec
+        decode_path = {"metric": "decode tokens/s (one new token per batch row)", "value": job_rate(world, B, dec_ms),
                        "unit": UNIT, "ms_per_step": dec_ms, "steps": n_dec, "batch": B, "context": T,
                        "gpu_launches_per_step": model.launch_count(kv=True),
                        "note": "nc_decode_step at position T-1 after nc_prefill of T-1 tokens, repeated at that "
@@ -296,12 +307,9 @@ def run_ours(args, rank, world, local_rank):
                                "weight-read-bound, not tuned"}
         del cache
 
-    t_max = torch.tensor([ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t_max, op=dist.ReduceOp.MAX)
-    ms_max = float(t_max.item())
+    ms_max = max_over_ranks(ms, world, dev)
     ms_step = ms_max / args.steps
-    value = world * B * T * args.steps / (ms_max / 1000.0)
+    value = job_rate(world, B * T * args.steps, ms_max)
 
     # end to end through host buffers
     e2e = None
@@ -318,10 +326,7 @@ def run_ours(args, rank, world, local_rank):
             model.forward_host(tok_h, out_h)
         torch.cuda.synchronize()
         h_ms = 1000 * (time.perf_counter() - h0)
-        tm = torch.tensor([h_ms], dtype=torch.float64, device=dev)
-        if world > 1:
-            dist.all_reduce(tm, op=dist.ReduceOp.MAX)
-        e2e = {"value": world * B * T * e2e_steps / (float(tm.item()) / 1000.0), "unit": UNIT,
+        e2e = {"value": job_rate(world, B * T * e2e_steps, max_over_ranks(h_ms, world, dev)), "unit": UNIT,
                "h2d_bytes_per_step": int(tok_h.numel() * 4), "d2h_bytes_per_step": int(out_h.numel() * 4),
                "steps": e2e_steps}
         del out_h
