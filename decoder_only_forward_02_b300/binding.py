@@ -61,6 +61,8 @@ _SIGS = {
                                   ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "nc_forward_host": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
                                        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "nc_forward_static_scratch": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+                                                 ctypes.c_void_p, ctypes.c_void_p]),
     "nc_get_status": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
     "nc_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "nc_last_cuda_error": (ctypes.c_char_p, []),
