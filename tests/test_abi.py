@@ -107,3 +107,30 @@ def test_kernel_class_names():
     lib = B.lib()
     assert [lib.nc_kernel_class_name(i).decode() for i in range(8)] == B.KERNEL_CLASSES
     assert lib.nc_kernel_class_name(8) == b"unknown"
+
+
+def test_headers_are_plain_c_and_link(tmp_path):
+    """The boundary is a C ABI: both headers compile as pedantic C99 and as C++, and a C program
+    links against the library and calls its host-only entry points."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "use_nc.c"
+    src.write_text(
+        '#include "nc.h"\n#include "nc_ops.h"\n#include <string.h>\n'
+        "int main(void) {\n"
+        '  if (strcmp(nc_status_string(NC_ERR_WORKSPACE), "buffer smaller than required") != 0) return 1;\n'
+        "  if (nc_forward_launch_count(0) != 0 || nc_op_ce_scratch_bytes(0) != 0) return 2;\n"
+        "  size_t n = 0;\n"
+        "  if (nc_model_packed_bytes(0, &n) != NC_ERR_INVALID_ARG) return 3;\n"
+        "  return 0;\n}\n")
+    inc = os.path.join(ROOT, "include")
+    lib = os.path.dirname(B.LIB_PATH)
+    exe = tmp_path / "use_nc"
+    subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", "-I", inc, str(src), "-o", str(exe),
+                    "-L", lib, "-lnc", f"-Wl,-rpath,{lib}"], check=True, capture_output=True)
+    subprocess.run(["g++", "-std=c++17", "-Wall", "-Werror", "-I", inc, "-x", "c++", "-fsyntax-only", str(src)],
+                   check=True, capture_output=True)
+    assert subprocess.run([str(exe)]).returncode == 0
