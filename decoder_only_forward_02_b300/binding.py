@@ -250,6 +250,13 @@ def check(code: int, what: str) -> None:
         raise NcError(code, what)
 
 
+def _check_out(t: torch.Tensor, shape: tuple, dtype: torch.dtype, device, name: str) -> None:
+    """A caller-provided output buffer must match exactly what the kernels write into it."""
+    if tuple(t.shape) != tuple(shape) or t.dtype != dtype or not t.is_contiguous() or t.device != device:
+        raise ValueError(f"{name} must be a contiguous {dtype} tensor of shape {tuple(shape)} on {device}, "
+                         f"got {t.dtype} {tuple(t.shape)} on {t.device}")
+
+
 def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
     return None if t is None else t.data_ptr()
 
@@ -364,6 +371,7 @@ class Model:
         V = self.cfg.vocab_size
         if out is None:
             out = torch.empty((B, T, V), dtype=torch.float32, device=self.device)
+        _check_out(out, (B, T, V), torch.float32, tokens.device, "out")
         ws = self.workspace(B, T)
         check(lib().nc_forward(self.handle, tokens.data_ptr(), B, T, out.data_ptr(), ws.data_ptr(), ws.numel(),
                                _stream_handle(stream)), "nc_forward")
@@ -385,6 +393,10 @@ class Model:
             loss = torch.empty((B, T), dtype=torch.float32, device=self.device)
         if stats is None:
             stats = torch.empty((2,), dtype=torch.float32, device=self.device)
+        _check_out(loss, (B, T), torch.float32, tokens.device, "loss")
+        _check_out(stats, (2,), torch.float32, tokens.device, "stats")
+        if token_bytes is not None:
+            _check_out(token_bytes, (self.cfg.vocab_size,), torch.int32, tokens.device, "token_bytes")
         ws = self.workspace(B, T, loss=True)
         check(lib().nc_forward_loss(self.handle, tokens.data_ptr(), targets.data_ptr(), B, T, _ptr(token_bytes),
                                     loss.data_ptr(), stats.data_ptr(), ws.data_ptr(), ws.numel(),
@@ -405,6 +417,7 @@ class Model:
         B, T = tokens.shape
         if out is None:
             out = torch.empty((B, T, self.cfg.vocab_size), dtype=torch.float32, device=self.device)
+        _check_out(out, (B, T, self.cfg.vocab_size), torch.float32, tokens.device, "out")
         ws = self.workspace(B, T)
         check(lib().nc_prefill(self.handle, tokens.data_ptr(), B, T, cache.data_ptr(), cache.numel(), T_max,
                                out.data_ptr(), ws.data_ptr(), ws.numel(), _stream_handle(stream)), "nc_prefill")
@@ -419,8 +432,11 @@ class Model:
             if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
                 raise ValueError(f"{name} must be a contiguous int32 CUDA tensor")
         B = tokens.shape[0]
+        if prev_tokens.shape != tokens.shape or tokens.dim() != 1:
+            raise ValueError("tokens and prev_tokens must both have shape [B]")
         if out is None:
             out = torch.empty((B, self.cfg.vocab_size), dtype=torch.float32, device=self.device)
+        _check_out(out, (B, self.cfg.vocab_size), torch.float32, tokens.device, "out")
         key = ("decode", B)
         if key not in self._ws:
             n = ctypes.c_size_t()

@@ -134,3 +134,14 @@ def test_headers_are_plain_c_and_link(tmp_path):
     subprocess.run(["g++", "-std=c++17", "-Wall", "-Werror", "-I", inc, "-x", "c++", "-fsyntax-only", str(src)],
                    check=True, capture_output=True)
     assert subprocess.run([str(exe)]).returncode == 0
+
+
+def test_output_buffer_checks():
+    import torch
+    dev = torch.device("cpu")
+    ok = torch.empty((2, 3), dtype=torch.float32)
+    B._check_out(ok, (2, 3), torch.float32, dev, "out")
+    for bad in (torch.empty((3, 2), dtype=torch.float32), torch.empty((2, 3), dtype=torch.float64),
+                torch.empty((3, 2), dtype=torch.float32).t()):
+        with pytest.raises(ValueError):
+            B._check_out(bad, (2, 3), torch.float32, dev, "out")
