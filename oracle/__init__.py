@@ -1,6 +1,7 @@
 """fp64 CPU oracle for the nanochat-style decoder-only GPT forward pass (``forward``), its
 next-token cross-entropy and bits per byte (``loss``), and the gradient of that loss with
-respect to every weight (``backward``).
+respect to every weight (``backward``), and the forward with FP8 (e4m3) tensorwise-scaled
+linear layers (``fp8``).
 
 TEST INFRASTRUCTURE ONLY.  Nothing on the product path may import, call or
 execute anything in this package; only ``tests/``, ``__graft_entry__.smoke()``
