@@ -145,3 +145,20 @@ def test_output_buffer_checks():
                 torch.empty((3, 2), dtype=torch.float32).t()):
         with pytest.raises(ValueError):
             B._check_out(bad, (2, 3), torch.float32, dev, "out")
+
+
+def test_loss_ops_validate_before_launch():
+    """Every case here fails validation, so nothing is launched (fake pointers are never used)."""
+    lib = B.lib()
+    a = 4096   # an aligned address that is never dereferenced
+    # nc_op_lmhead_ce(xf, wlm, M, V, C, ssp, eps, cap, targets, part, zt, status, stream)
+    assert lib.nc_op_lmhead_ce(a + 8, a, 4, 64, 64, None, 1e-6, 15.0, a, a, a, None, None) == 1    # misaligned xf
+    assert lib.nc_op_lmhead_ce(a, a, 4, 64, 64, None, 1e-6, 0.0, a, a, a, None, None) == 1        # cap <= 0
+    assert lib.nc_op_lmhead_ce(a, a, 4, 48, 64, None, 1e-6, 15.0, a, a, a, None, None) == 2       # V % 32
+    assert lib.nc_op_lmhead_ce(a, a, 4, 64, 96, None, 1e-6, 15.0, a, a, a, None, None) == 2       # C % 64
+    assert lib.nc_op_lmhead_ce(a, a, 4, 64, 64, a, 1e-6, 15.0, a, a, a, None, None) == 1          # ssp, C % 128
+    # nc_op_ce_finalize(part, zt, targets, M, V, token_bytes, loss, stats, scratch, bytes, status, stream)
+    need = lib.nc_op_ce_scratch_bytes(300)
+    assert lib.nc_op_ce_finalize(a, a, a, 300, 64, None, None, a, a, need - 8, None, None) == 3   # scratch too small
+    assert lib.nc_op_ce_finalize(a, a, a, 300, 64, None, None, a, a + 4, need, None, None) == 1   # misaligned scratch
+    assert lib.nc_op_ce_finalize(a, a, a, 0, 64, None, None, a, a, need, None, None) == 1         # M < 1
