@@ -500,7 +500,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-tokens", type=int, default=2048)
     ap.add_argument("--cpu-rows", type=int, default=4, help="batch rows the CPU baseline times")
-    ap.add_argument("--ref-tokens", type=int, default=512)
+    ap.add_argument("--ref-tokens", type=int, default=256,
+                    help="positions of batch row 0 the reference arm runs per step (a bounded sample)")
     ap.add_argument("--only-kernel", default=None,
                     help="launch one kernel class (qkv, attention, oproj, fc, proj, lmhead, lmhead_ce, embed) "
                          "at the workload's shapes, for profiler captures")
