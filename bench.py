@@ -185,6 +185,92 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def roofline(ktimes, work, peaks, peak_src):
+    """Per-kernel achieved rates and the roofline entry of the dominant kernel class (largest summed
+    event time).  A contraction is compared with the burst bf16 figure, since each launch runs for
+    tens of microseconds to a millisecond inside a sub-second timed region (the sustained figure,
+    from seconds of back-to-back GEMMs at a power-capped clock, is reported beside the model
+    rate); a memory-bound kernel with the measured copy bandwidth."""
+    kern = {}
+    total = max(1e-9, sum(t for t, _ in ktimes.values()))
+    for name, (tot, n) in ktimes.items():
+        if n and name in work:
+            b, wk = work[name]
+            s = tot / n / 1000.0
+            kern[name] = {"ms_total": tot, "launches": n, "ms_per_launch": tot / n, "share": tot / total,
+                          "achieved": wk / s / (1e12 if b == "tensor" else 1e9),
+                          "unit": "TFLOP/s" if b == "tensor" else "GB/s"}
+    dom = max(kern, key=lambda k: kern[k]["ms_total"])
+    bound = work[dom][0]
+    key = "bf16_tflops" if bound == "tensor" else "hbm_gbs"
+    peak = float(peaks.get(key, FALLBACK_PEAKS[key]))
+    for name in kern:
+        pk = float(peaks.get("bf16_tflops" if work[name][0] == "tensor" else "hbm_gbs", FALLBACK_PEAKS[key]))
+        kern[name]["frac"] = kern[name]["achieved"] / pk
+    achieved = kern[dom]["achieved"]
+    return kern, dom, {"kernel": dom, "bound": bound, "achieved": achieved, "peak": peak,
+                       "unit": kern[dom]["unit"], "frac": achieved / peak, "traffic": None,
+                       "peak_source": f"{peak_src} ({key}, of measured)" if peak_src == "measured"
+                       else f"{peak_src} ({key}, of fallback)"}
+
+
+def measure_workload(name, steps, dev, world, peaks, peak_src, cpu_tokens, do_cpu):
+    """One of the other full-size workloads: forward tokens/s (CUDA events over `steps` forwards
+    after 3 warm-up ones), the model FLOP rate against the burst peak, the per-kernel breakdown
+    with the dominant kernel's roofline entry, and an oracle sample on the host cores."""
+    import torch
+    import torch.distributed as dist
+    from synth import get_workload, make_tokens, make_weights
+    from decoder_only_forward_02_b300 import binding as NB
+    wl = get_workload(name)
+    cfg = wl.model
+    wts_cpu = make_weights(cfg, seed=wl.seed, init=wl.init)
+    wts = {k: (v.to(dev) if torch.is_tensor(v) else v) for k, v in wts_cpu.items()}
+    tok_cpu = make_tokens(wl)
+    tok = tok_cpu.to(dev)
+    model = NB.Model(cfg, wts, device=dev)
+    B, T, V = wl.B, wl.T, cfg.vocab_size
+    logits = torch.empty((B, T, V), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(3):
+        model.forward(tok, out=logits)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        model.forward(tok, out=logits)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    if model.status() != 0:
+        raise RuntimeError(f"device status set on the {name} workload")
+    ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    model.timing(True)
+    for _ in range(steps):
+        model.forward(tok, out=logits)
+    torch.cuda.synchronize()
+    model.timing(False)
+    ktimes = model.timing_read()
+    ms_step = ms / steps
+    tflops = model_flops(cfg, B, T) / (ms_step / 1000.0) / 1e12
+    kern, dom, roof = roofline(ktimes, kernel_work(cfg, B, T), peaks, peak_src)
+    out = {"workload": name, "B": B, "T": T, "value": job_rate(world, B * T * steps, ms), "unit": UNIT,
+           "ms_per_step": ms_step, "steps": steps, "model_tflops": tflops,
+           "pct_bf16_peak": 100.0 * tflops / float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])),
+           "gpu_launches_per_step": model.launch_count(), "roofline": roof, "kernels": kern}
+    del model, logits, wts
+    torch.cuda.empty_cache()
+    if do_cpu:
+        n = min(cpu_tokens, T)
+        secs = oracle_sample(wl, wts_cpu, tok_cpu, n, 1)
+        out["cpu_baseline"] = {"value": n / secs, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+                               "sample": f"fp64 oracle on positions 0..{n - 1} of batch row 0 ({secs:.1f} s)"}
+    return out
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -331,31 +417,22 @@ def run_ours(args, rank, world, local_rank):
                "steps": e2e_steps}
         del out_h
 
+    # the other full-size workloads (d20 with grouped-query attention, the long-context d12 whose
+    # short windows skip most key tiles, d24), each measured the same way on a shorter loop (every
+    # rank runs them: the timing takes the max over ranks)
+    peaks, peak_src = load_peaks()
+    launches = model.launch_count() * args.steps
+    workloads = []
+    extra = [w for w in args.extra_workloads.split(",") if w and w != wl.name]
+    if extra:
+        del logits, model, wts
+        torch.cuda.empty_cache()
+        workloads = [measure_workload(w, args.extra_steps, dev, world, peaks, peak_src, args.extra_cpu_tokens,
+                                      rank == 0 and not args.no_cpu_baseline) for w in extra]
     if rank != 0:
         return
-    peaks, peak_src = load_peaks()
     work = kernel_work(cfg, B, T)
-    kern = {}
-    for name, (tot, n) in ktimes.items():
-        if n:
-            kern[name] = {"ms_total": tot, "launches": n, "ms_per_launch": tot / n,
-                          "share": tot / max(1e-9, sum(t for t, _ in ktimes.values()))}
-    dom = max(kern, key=lambda k: kern[k]["ms_total"])
-    bound, per_launch = work[dom]
-    avg_s = kern[dom]["ms_per_launch"] / 1000.0
-    if bound == "tensor":
-        achieved = per_launch / avg_s / 1e12
-        peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
-        unit = "TFLOP/s"
-    else:
-        achieved = per_launch / avg_s / 1e9
-        peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
-        unit = "GB/s"
-    for name in kern:
-        b, wk = work[name]
-        s = kern[name]["ms_per_launch"] / 1000.0
-        kern[name]["achieved"] = wk / s / (1e12 if b == "tensor" else 1e9)
-        kern[name]["unit"] = "TFLOP/s" if b == "tensor" else "GB/s"
+    kern, dom, roof = roofline(ktimes, work, peaks, peak_src)
     traffic = None
     tpath = os.path.join(ROOT, "profiles", "traffic.json")
     if os.path.exists(tpath):
@@ -365,6 +442,7 @@ def run_ours(args, rank, world, local_rank):
             traffic = t.get("bytes_per_launch")
     flops = model_flops(cfg, B, T)
     tflops = flops / (ms_step / 1000.0) / 1e12
+    roof["traffic"] = traffic
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": max(args.warmup, 3), "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
@@ -379,16 +457,16 @@ def run_ours(args, rank, world, local_rank):
         "pct_bf16_peak": 100.0 * tflops / float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])),
         "pct_bf16_peak_sustained": 100.0 * tflops / float(
             peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])),
-        "roofline": {"kernel": dom, "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
-                     "frac": achieved / peak, "traffic": traffic,
-                     "peak_source": f"{peak_src} ({'bf16_tflops_sustained' if bound == 'tensor' else 'hbm_gbs'})"},
+        "roofline": roof,
         "kernels": kern,
-        "gpu_launches": model.launch_count() * args.steps,
+        "gpu_launches": launches,
         "clocks": clk,
         "e2e": e2e,
         "loss_path": loss_path,
         "decode_path": decode_path,
     }
+    if workloads:
+        line["workloads"] = workloads
     if not args.no_cpu_baseline and world >= 1:
         n = min(args.cpu_tokens, T)
         rows = max(1, min(args.cpu_rows, B))
@@ -502,6 +580,11 @@ def main():
     ap.add_argument("--cpu-rows", type=int, default=4, help="batch rows the CPU baseline times")
     ap.add_argument("--ref-tokens", type=int, default=256,
                     help="positions of batch row 0 the reference arm runs per step (a bounded sample)")
+    ap.add_argument("--extra-workloads", default="d20,d12_long,d24",
+                    help="other full-size workloads measured after the headline one (comma list; empty: none)")
+    ap.add_argument("--extra-steps", type=int, default=20)
+    ap.add_argument("--extra-cpu-tokens", type=int, default=128,
+                    help="positions of batch row 0 the oracle runs for each extra workload's CPU baseline")
     ap.add_argument("--only-kernel", default=None,
                     help="launch one kernel class (qkv, attention, oproj, fc, proj, lmhead, lmhead_ce, embed) "
                          "at the workload's shapes, for profiler captures")

@@ -453,9 +453,26 @@ template <int D>
 cudaError_t launch_d(const bf16* q, const bf16* k, const bf16* v, int B, int T, int H, int Hkv, int window,
                      bf16* y, int* status, cudaStream_t stream) {
   using Lt = Lay<D>;
-  static cudaError_t attr =
-      cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lt::TOTAL);
-  if (attr != cudaSuccess) return attr;
+  struct State {
+    int num_sms = 0;
+  };
+  static State states[MAX_DEVICES];
+  static bool ready[MAX_DEVICES];
+  static std::mutex mu;
+  State* st = nullptr;
+  const cudaError_t init_err = per_device(states, ready, mu, [](State& s) {
+    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lt::TOTAL);
+    if (e != cudaSuccess) return e;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&s.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || s.num_sms < 1) {
+      cudaGetLastError();
+      s.num_sms = 148;
+    }
+    return cudaSuccess;
+  }, &st);
+  if (init_err != cudaSuccess) return init_err;
+  const int num_sms = st->num_sms;
   const uint64_t M = static_cast<uint64_t>(B) * T;
   CUtensorMap tq, tk, tv;
   if (!make_tmap_bf16_2d(&tq, q, static_cast<uint64_t>(H) * D, M, static_cast<uint64_t>(H) * D * 2, 64, BQ) ||
@@ -464,13 +481,6 @@ cudaError_t launch_d(const bf16* q, const bf16* k, const bf16* v, int B, int T, 
     return cudaErrorInvalidValue;
   const int npair = (T + 2 * BQ - 1) / (2 * BQ);
   const int num_items = npair * H * B;
-  static int num_sms = 0;
-  if (num_sms == 0) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || num_sms < 1)
-      num_sms = 148;
-  }
   const float scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute lattr[1] = {pdl_attribute()};

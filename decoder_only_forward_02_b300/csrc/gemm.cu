@@ -10,18 +10,22 @@
 // half of B from the peer.  Persistent grid: min(pair tiles, co-resident pairs); pair tiles
 // are taken round-robin with the column-block index fastest, so the pairs running at the same
 // time share one row block of A (read from DRAM once) and the weights stay in L2.
-// Roles (320 threads per CTA):
+// Roles (384 threads = 12 warps per CTA; warpgroup 0 runs at 56 registers per thread and the two
+// epilogue warpgroups at 224, moved with setmaxnreg within the launch's 384 x 168):
 //   warp 0       TMA producer (both CTAs): its A box (128x64) and B half (128x64) per stage,
-//                128-byte swizzle, 5-stage ring; both CTAs' copies complete on the leader
-//                CTA's full barrier, which the leader arms with the pair's byte count.
+//                128-byte swizzle, a 4- to 7-stage ring (the depth depends on how much shared
+//                memory the epilogue kind keeps: Cfg::STAGES); both CTAs' copies complete on
+//                the leader CTA's full barrier, which the leader arms with the pair's byte count.
 //   warp 1       allocates 512 TMEM columns in both CTAs (two 128x256 fp32 accumulators);
 //                in the leader one lane issues tcgen05.mma (M=256, N=256, K=16) for the pair;
 //                pair commits free each stage in both CTAs and publish each finished
 //                accumulator to both CTAs' epilogues.
-//   warps 2..9   epilogue: two warpgroups, each owns 128 accumulator columns; every thread
-//                owns one output row (TMEM lane).  A warp reads its 32 rows with tcgen05.ld,
-//                applies the fused epilogue, writes 32-row x 128-byte boxes into one of its two
-//                128-byte-swizzled shared buffers and stores each box with one TMA store.
+//   warps 2, 3   idle (they complete warpgroup 0 for the register reallocation).
+//   warps 4..11  epilogue: two warpgroups, each owns 128 accumulator columns; every thread
+//                owns one output row (TMEM lane).  A warp reads its 32 rows with tcgen05.ld and
+//                applies the fused epilogue; depending on the kind it stores 32-row x 128-byte
+//                boxes with TMA from two alternating 128-byte-swizzled shared buffers, stores
+//                row-coalesced from one staging buffer, or stores nothing (cross-entropy).
 // The double-buffered accumulator lets the epilogue of tile i overlap the MMAs of tile i+1.
 //
 // Fused epilogues (the operations are those of "Nanochat在nanoGPT之上的新增功能", section 1
@@ -899,9 +903,12 @@ __global__ void __launch_bounds__(THREADS, 1)
 template <int KIND, int D>
 cudaError_t launch_kind(const CUtensorMap& ta, const CUtensorMap& tb, const OutMaps& om, int M, int N, int K,
                         const GemmEpi& epi, int num_sms, cudaStream_t stream) {
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  static int max_pairs = 0;
+  struct State {
+    int max_pairs = 0;
+  };
+  static State states[MAX_DEVICES];
+  static bool ready[MAX_DEVICES];
+  static std::mutex mu;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -914,16 +921,21 @@ cudaError_t launch_kind(const CUtensorMap& ta, const CUtensorMap& tb, const OutM
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;   // occupancy query without the PDL attribute
-  std::call_once(once, [&] {
-    attr_err = cudaFuncSetAttribute(gemm_tc_kernel<KIND, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    Cfg<KIND, D>::SMEM_BYTES);
-    if (attr_err != cudaSuccess) return;
+  State* st = nullptr;
+  const cudaError_t init_err = per_device(states, ready, mu, [&](State& s) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<KIND, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Cfg<KIND, D>::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t q = cfg;
     q.gridDim = dim3(2 * (num_sms / 2));
-    if (cudaOccupancyMaxActiveClusters(&max_pairs, gemm_tc_kernel<KIND, D>, &q) != cudaSuccess || max_pairs < 1)
-      max_pairs = num_sms / 2;
-  });
-  if (attr_err != cudaSuccess) return attr_err;
+    if (cudaOccupancyMaxActiveClusters(&s.max_pairs, gemm_tc_kernel<KIND, D>, &q) != cudaSuccess || s.max_pairs < 1) {
+      cudaGetLastError();
+      s.max_pairs = num_sms / 2;
+    }
+    return cudaSuccess;
+  }, &st);
+  if (init_err != cudaSuccess) return init_err;
+  const int max_pairs = st->max_pairs;
   const int tiles = ((M + PAIR_M - 1) / PAIR_M) * ((N + BN - 1) / BN);
   const int pairs = tiles < max_pairs ? tiles : max_pairs;
   cfg.gridDim = dim3(2 * pairs);

@@ -6,6 +6,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include "nc.h"
 
 namespace nc {
@@ -85,6 +87,30 @@ constexpr int MAX_GATE_HEADS = 16;
 // to a status: NC_OK for cudaSuccess, NC_ERR_CUDA otherwise.
 nc_status cuda_status(cudaError_t e);
 const char* last_cuda_error_name();
+
+// One-time per-device set-up of a kernel (its shared-memory attribute, its occupancy), done with
+// that device current, so that a process running models on several GPUs sets each one up.
+constexpr int MAX_DEVICES = 64;
+
+// Kernel state for the current device (states[dev]), initialised on first use on that device by
+// init(State&) -> cudaError_t; a failed init is retried on the next call.
+template <typename State, typename Init>
+cudaError_t per_device(State (&states)[MAX_DEVICES], bool (&ready)[MAX_DEVICES], std::mutex& mu, Init init,
+                       State** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) {
+    cudaGetLastError();
+    return cudaErrorInvalidDevice;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ready[dev]) {
+    const cudaError_t e = init(states[dev]);
+    if (e != cudaSuccess) return e;
+    ready[dev] = true;
+  }
+  *out = &states[dev];
+  return cudaSuccess;
+}
 
 // Launch attribute that lets a kernel's CTAs start while the previous kernel on the stream
 // drains (each kernel waits for its predecessor before touching memory: griddep_wait()).

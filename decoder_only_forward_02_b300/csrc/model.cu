@@ -108,6 +108,7 @@ struct nc_model {
   bf16* wqkv = nullptr;     // packed [L][(H+2Hkv)*D][C]
   float2* rope = nullptr;   // [seq_len_ctx][D/2]
   int* status = nullptr;    // device status word
+  int device = 0;           // the device current at creation (where packed_buf lives)
   int num_sms = 148;
   bool timing = false;
   std::vector<TimedLaunch> pending;
@@ -303,6 +304,7 @@ nc_status nc_model_create(const nc_config* cfg, const nc_weights* w, void* packe
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
+  m->device = dev;
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&m->num_sms, cudaDevAttrMultiProcessorCount, dev);
   const size_t C = cfg->n_embd, qd = static_cast<size_t>(cfg->n_head) * cfg->head_dim,
                kd = static_cast<size_t>(cfg->n_kv_head) * cfg->head_dim;
@@ -345,9 +347,20 @@ nc_status nc_workspace_bytes_host(const nc_model* m, int B, int T, size_t* bytes
 
 namespace {
 
+// The calling thread's current device is the model's (checked before any device work).
+bool on_model_device(const nc_model* m) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return dev == m->device;
+}
+
 // Argument checks shared by the forward entry points (before any device work).
 nc_status check_forward_args(const nc_model* m, const int32_t* tokens, int B, int T, const void* workspace) {
   if (m == nullptr || tokens == nullptr || workspace == nullptr) return NC_ERR_INVALID_ARG;
+  if (!on_model_device(m)) return NC_ERR_INVALID_ARG;
   if (B < 1 || T < 1) return NC_ERR_INVALID_ARG;
   if (T > m->cfg.seq_len_ctx) return NC_ERR_UNSUPPORTED;
   if (static_cast<long long>(B) * T > (1LL << 30)) return NC_ERR_UNSUPPORTED;
@@ -673,6 +686,7 @@ nc_status nc_decode_step(nc_model* m, const int32_t* prev_tokens, const int32_t*
   if (m == nullptr || prev_tokens == nullptr || tokens == nullptr || logits == nullptr || kv_cache == nullptr ||
       workspace == nullptr || B < 1)
     return NC_ERR_INVALID_ARG;
+  if (!on_model_device(m)) return NC_ERR_INVALID_ARG;
   if (!aligned(prev_tokens, 4) || !aligned(tokens, 4) || !aligned(logits, 16) || !aligned(kv_cache, ALIGN) ||
       !aligned(workspace, ALIGN))
     return NC_ERR_INVALID_ARG;

@@ -12,6 +12,9 @@
 // Host code must not hand the array's name to a kernel (on the host it names a shadow
 // variable, not device memory); the device address is looked up once per device with
 // cudaGetSymbolAddress, with that device current, on the first call made on that device.
+// Under CUDA's lazy module loading that lookup is also what loads this library's device code
+// on the device and reserves the array, so the first call can fail with NC_ERR_CUDA when the
+// device is short of memory; callers make it at set-up time.
 #include <mutex>
 
 #include "internal.h"

@@ -45,6 +45,12 @@
  * accumulation, fp32 residual stream, fp32 softmax statistics.
  *
  * Threading: a model is not re-entrant; calls on one model must not overlap.
+ *
+ * Devices: a model belongs to the device that was current when nc_model_create ran (its
+ * packed buffer lives there); every call that launches work on it must be made with that
+ * device current, else it returns NC_ERR_INVALID_ARG before any device work.  Kernel set-up
+ * (shared-memory limits, occupancy) is done once per device, so one process may run models
+ * on several GPUs.
  */
 #ifndef NC_H
 #define NC_H
@@ -166,10 +172,14 @@ NC_API nc_status nc_forward_host(nc_model *m, const int32_t *tokens_host, int B,
  *  - Allocates nothing: no cudaMalloc, cudaFree or allocating library routine.  Keep
  *    per-kernel timing (nc_timing_enable) off, since it creates CUDA events.
  *  - The first call on each device looks up the array's device address with that device
- *    current; make that first call before any stream capture.
+ *    current.  With CUDA's lazy module loading (the default) that first call is also when
+ *    the library's device code is loaded on the device and the array is reserved, so it can
+ *    fail with NC_ERR_CUDA if the device is short of memory: make it at set-up time, and
+ *    before any stream capture.
  *  - All calls share the one array, which keeps the previous call's contents (nothing in it
- *    needs to start at zero).  Calls that overlap on the GPU (other streams, other models,
- *    other threads) race on it: serialise them. */
+ *    needs to start at zero: every region is written before it is read within one call).
+ *    Calls that overlap on the GPU (other streams, other models, other threads) race on it:
+ *    serialise them. */
 #define NC_STATIC_SCRATCH_BYTES (32u * 1024u * 1024u)
 NC_API nc_status nc_forward_static_scratch(nc_model *m, const int32_t *tokens, int B, int T,
                                            float *logits, void *stream);

@@ -11,12 +11,11 @@ CUDA path.
 from .forward import (
     OracleWeights, rms_norm, rope_tables, apply_rope, attention, relu2, softcap,
     sigmoid, embed_smear, block, forward_row, forward, param_shapes, param_count,
-    visible,
 )
 from .loss import cross_entropy, loss_stats
 
 __all__ = [
     "OracleWeights", "rms_norm", "rope_tables", "apply_rope", "attention", "relu2",
     "softcap", "sigmoid", "embed_smear", "block", "forward_row", "forward",
-    "param_shapes", "param_count", "visible", "cross_entropy", "loss_stats",
+    "param_shapes", "param_count", "cross_entropy", "loss_stats",
 ]

@@ -164,16 +164,6 @@ def apply_rope(x: np.ndarray, cos: np.ndarray, sin: np.ndarray) -> np.ndarray:
 # attention
 # ----------------------------------------------------------------------------
 
-def visible(i: int, j: int, window: int) -> bool:
-    """Query i sees key j: causal, and within the left window when one is set.
-
-    READING: window W means keys max(0, i - W) .. i (the FlashAttention
-    window_size=(W, 0) convention of the backend the architecture guide names);
-    W < 0 means plain causal.
-    """
-    return j <= i and (window < 0 or j >= i - window)
-
-
 def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, window: int, block: int = 256) -> np.ndarray:
     """Causal grouped-query softmax attention with an optional left window.
 

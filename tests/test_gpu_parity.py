@@ -89,6 +89,26 @@ def test_full_size_workloads_sampled(name, rows, stride):
         assert_parity(got, ref, f"{name} row {r}")
 
 
+def test_d24_error_growth_with_depth():
+    """How the logit error grows through the bf16 stack: the d24 weights cut to their first 6, 12,
+    18 and 24 blocks (the same windows and value-embedding layers; backout at the cut model's
+    middle), one row of 1,024 tokens, every logit against the oracle.  The margins table printed
+    at the end of the run shows the headroom at each depth."""
+    wl = get_workload("d24")
+    cfg = wl.model
+    wts = make_weights(cfg, seed=wl.seed, init=wl.init)
+    tok = make_tokens(wl)[15:16, :1024].contiguous()
+    for depth in (6, 12, 18, 24):
+        c = replace(cfg, n_layer=depth, window_left=cfg.window_left[:depth], has_ve=cfg.has_ve[:depth])
+        w = {k: v for k, v in wts.items() if "." not in k or int(k.split(".")[1]) < depth}
+        w["resid_lambdas"] = wts["resid_lambdas"][:depth]
+        w["x0_lambdas"] = wts["x0_lambdas"][:depth]
+        _, out = _run(c, w, tok)
+        ref = O.forward(c, O.OracleWeights.from_synth(c, w), tok.numpy())
+        assert_parity(out.cpu().numpy(), ref, f"d24 first {depth} blocks, T=1024")
+        del out
+
+
 def test_bitwise_repeatable_and_row_independent():
     wl = get_workload("tiny_all")
     cfg = replace(wl.model, seq_len_ctx=256, window_left=(64,))

@@ -269,6 +269,127 @@ def test_ve_gate_special_cases():
                                O.block(c2, Wh, 0, x0, x0, tok, cos, sin), atol=1e-13)
 
 
+def _gate_pin_case(cfg, T, seed):
+    """Inputs for the value-embedding gate pins: one VE layer, block input x with an RMS far from
+    1 (so a gate taken from un-normed x differs from one taken from a = rms(x)), and the normed
+    input a computed by torch's rms_norm (a library routine, not the oracle)."""
+    W = _weights(cfg, seed=seed)
+    g = np.random.default_rng(seed)
+    x = g.standard_normal((T, cfg.n_embd)) * 0.05
+    x0 = g.standard_normal((T, cfg.n_embd)) * 0.02
+    tok = g.integers(0, cfg.vocab_size, T)
+    mixed = W.resid_lambdas[0] * x + W.x0_lambdas[0] * x0
+    a = F.rms_norm(torch.from_numpy(mixed), (cfg.n_embd,), eps=cfg.rms_eps).numpy()
+    assert np.all(np.abs(np.sqrt(np.mean(mixed ** 2, -1)) - 1.0) > 0.5)
+    return W, x, x0, tok, a
+
+
+def _fold_gated_ve_into_wv(cfg, W, a, tok, Z):
+    """Value weights W_v' with a W_v'^T = a W_v^T + gate * ve[tok] on every kv head, where
+    gate[t, g] = sigmoid(Z[t, g]) (ve_gate_scale = 1): with T <= C and the rows of a independent,
+    the least-squares solution reproduces the gated table rows exactly (up to rounding)."""
+    T, Hkv, D = len(tok), cfg.n_kv_head, cfg.head_dim
+    ve = W.m("ve.0")[tok].reshape(T, Hkv, D)
+    target = (1.0 / (1.0 + np.exp(-Z)))[:, :, None] * ve          # [T, Hkv, D]
+    dWv_t, *_ = np.linalg.lstsq(a, target.reshape(T, Hkv * D), rcond=None)
+    return W.m("wv.0") + dWv_t.T
+
+
+@pytest.mark.parametrize("shape", ["gqa_h4_kv2", "d20_width"])
+def test_ve_gate_per_head_from_normed_input(shape):
+    """The gate of kv head g is sigmoid(a . W_g[g]) with a the block's RMS-normed input, and it
+    scales kv head g's slice of the value-embedding row of the token.  Gate weights are solved so
+    that a . W_g[g] equals chosen pre-activations Z[:, g] (some saturating at +-40, some not);
+    the value-embedding layer must then equal a layer without value embeddings whose value
+    projection is shifted to add exactly sigmoid(Z) * ve[tok] per head.  Fails if the gate is
+    taken from the un-normed x, if gate rows are paired with the wrong kv head, or if the table
+    row is split into heads in another order."""
+    if shape == "gqa_h4_kv2":
+        cfg = replace(get_workload("tiny_all").model, n_head=4, n_kv_head=2, head_dim=32, has_ve=(1,),
+                      use_smear=False, use_backout=False)
+        T = 12
+    else:   # the d20 attention shape (10 heads of 128, 5 kv heads) on one layer, small vocabulary
+        cfg = replace(get_workload("d20").model, n_layer=1, vocab_size=512, seq_len_ctx=16,
+                      window_left=(-1,), has_ve=(1,))
+        T = 16
+    W, x, x0, tok, a = _gate_pin_case(cfg, T, seed=7)
+    g = np.random.default_rng(11)
+    Z = g.standard_normal((T, cfg.n_kv_head)) * 1.5
+    Z[:, 0] = 40.0                      # kv head 0: gate 1 (saturated)
+    Z[:, 1] = -40.0                     # kv head 1: gate 0 (saturated)
+    Z[: T // 2, -1] = g.uniform(-2, 2, T // 2) if cfg.n_kv_head > 2 else Z[: T // 2, -1]
+    Wg, *_ = np.linalg.lstsq(a, Z, rcond=None)                  # a @ Wg = Z
+    np.testing.assert_allclose(a @ Wg, Z, atol=1e-9)
+    W.mats["veg.0"] = Wg.T.copy()
+    cos, sin = O.rope_tables(T, cfg.head_dim, cfg.rope_base)
+    got = O.block(cfg, W, 0, x, x0, tok, cos, sin)
+    Wf = _weights(cfg, seed=7)
+    Wf.mats["wv.0"] = _fold_gated_ve_into_wv(cfg, W, a, tok, Z)
+    expect = O.block(replace(cfg, has_ve=(0,)), Wf, 0, x, x0, tok, cos, sin)
+    np.testing.assert_allclose(got, expect, atol=1e-9, rtol=1e-9)
+
+
+def test_ve_gate_hand_element():
+    """T = 2, two kv heads: gate pre-activations 0 and ln 3 give gates 1/2 and 3/4, so the value
+    of kv head 1 at token t gains exactly 3/4 of columns D..2D of that token's table row."""
+    cfg = replace(get_workload("tiny_all").model, n_head=2, n_kv_head=2, head_dim=64, has_ve=(1,),
+                  use_smear=False, use_backout=False)
+    T = 2
+    W, x, x0, tok, a = _gate_pin_case(cfg, T, seed=3)
+    Z = np.array([[0.0, math.log(3.0)], [0.0, math.log(3.0)]])
+    Wg, *_ = np.linalg.lstsq(a, Z, rcond=None)
+    W.mats["veg.0"] = Wg.T.copy()
+    gates = 1.0 / (1.0 + np.exp(-Z))
+    np.testing.assert_allclose(gates[0], [0.5, 0.75], rtol=1e-15)
+    # with a zero value projection the values are the gated table rows; with every query and key
+    # zero (zero q/k projections: after QK-norm they stay 0, eps > 0) attention averages the values
+    # uniformly over the visible keys: y[1, head 1] = (v[0, 1] + v[1, 1]) / 2
+    for k in ("wq.0", "wk.0", "wv.0"):
+        W.mats[k] = np.zeros_like(W.mats[k])
+    W.mats["wo.0"] = np.eye(cfg.n_embd, dtype=np.float64)       # y lands in the residual unchanged
+    W.mats["wproj.0"] = np.zeros_like(W.mats["wproj.0"])        # no MLP contribution
+    cos, sin = O.rope_tables(T, cfg.head_dim, cfg.rope_base)
+    out = O.block(cfg, W, 0, x, x0, tok, cos, sin)
+    mixed = W.resid_lambdas[0] * x + W.x0_lambdas[0] * x0
+    D = cfg.head_dim
+    ve = W.m("ve.0")
+    y1_head1 = 0.75 * (ve[tok[0], D:2 * D] + ve[tok[1], D:2 * D]) / 2.0
+    y1_head0 = 0.5 * (ve[tok[0], :D] + ve[tok[1], :D]) / 2.0
+    np.testing.assert_allclose(out[1, D:2 * D] - mixed[1, D:2 * D], y1_head1, atol=1e-14)
+    np.testing.assert_allclose(out[1, :D] - mixed[1, :D], y1_head0, atol=1e-14)
+    np.testing.assert_allclose(out[0, :D] - mixed[0, :D], 0.5 * ve[tok[0], :D], atol=1e-14)
+
+
+def test_ve_gate_kv_head_permutation_equivariance():
+    """Relabelling the kv heads (their q-head groups, key and value rows, gate rows and table
+    column blocks together, and the output projection's columns to match) leaves the block's
+    output unchanged."""
+    cfg = replace(get_workload("tiny_all").model, n_head=6, n_kv_head=3, head_dim=32, n_embd=192,
+                  mlp_hidden=256, has_ve=(1,), use_smear=False, use_backout=False)
+    T = 10
+    W, x, x0, tok, a = _gate_pin_case(cfg, T, seed=5)
+    W.mats["veg.0"] = np.random.default_rng(2).standard_normal(W.mats["veg.0"].shape) * 3.0
+    H, Hkv, D = cfg.n_head, cfg.n_kv_head, cfg.head_dim
+    grp = H // Hkv
+    perm = [2, 0, 1]                                    # new kv head g is old kv head perm[g]
+    qperm = [perm[h // grp] * grp + h % grp for h in range(H)]
+
+    def rows(m, order):
+        return np.concatenate([m[o * D:(o + 1) * D] for o in order], 0)
+
+    P = _weights(cfg, seed=5)
+    P.mats = dict(W.mats)
+    P.mats["wq.0"] = rows(W.m("wq.0"), qperm)
+    P.mats["wk.0"] = rows(W.m("wk.0"), perm)
+    P.mats["wv.0"] = rows(W.m("wv.0"), perm)
+    P.mats["wo.0"] = rows(W.m("wo.0").T, qperm).T
+    P.mats["veg.0"] = W.m("veg.0")[perm]
+    P.mats["ve.0"] = rows(W.m("ve.0").T, perm).T
+    cos, sin = O.rope_tables(T, D, cfg.rope_base)
+    np.testing.assert_allclose(O.block(cfg, P, 0, x, x0, tok, cos, sin), O.block(cfg, W, 0, x, x0, tok, cos, sin),
+                               atol=1e-13)
+
+
 def _plain_gpt_torch(cfg, W, tok):
     """Pre-norm GPT from library routines: rms_norm, linear, complex-rotation RoPE, causal SDPA."""
     t = lambda a: torch.from_numpy(np.asarray(a, dtype=np.float64))
