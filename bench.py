@@ -501,24 +501,24 @@ def run_single_kernel(args):
 
     k = args.only_kernel
     window = max(c.window_left) if args.window is None else args.window
-    if k == "qkv":
-        xb, w = rnd((M, C)), rnd(((H + 2 * Hkv) * D, C), 0.02)
+    if k == "qkv":   # a value-embedding layer's q|k|v projection (gate rows packed after each kv head's v)
+        xb = rnd((M, C))
+        w = ops.pack_qkv(rnd((H * D, C), 0.02), rnd((Hkv * D, C), 0.02), rnd((Hkv * D, C), 0.02),
+                         rnd((Hkv, C), 0.02), D)
         ssp = torch.rand((M, C // 128), generator=g, device=dev) * 100
-        gp = torch.randn((M, Hkv, C // 128), generator=g, device=dev)
         rope = ops.rope_table(wl.T, D, c.rope_base, dev)
         ve, tok = rnd((V, Hkv * D), 0.02), torch.randint(0, V, (M,), generator=g, device=dev, dtype=torch.int32)
-        fn = lambda: ops.qkv(xb, w, wl.T, H, Hkv, D, rope, c.rms_eps, ssp, gp, 1.0, ve, tok, V)
+        fn = lambda: ops.qkv(xb, w, wl.T, H, Hkv, D, rope, c.rms_eps, ssp, True, 1.0, ve, tok, V)
     elif k == "attention":
         q, kk, v = unit(rnd((M, H, D))).reshape(M, -1), unit(rnd((M, Hkv, D))).reshape(M, -1), rnd((M, Hkv * D))
         fn = lambda: ops.attention(q, kk, v, wl.B, wl.T, H, Hkv, D, window)
     elif k in ("oproj", "proj"):
         K = H * D if k == "oproj" else F
         a, w, x, x0 = rnd((M, K)), rnd((C, K), 0.02), rnd((M, C), 1.0, torch.float32), rnd((M, C), 1.0, torch.float32)
-        wg = rnd((Hkv, C), 0.02)
         if k == "oproj":
             fn = lambda: ops.gemm_residual(a, w, x, x_out=x)
-        else:   # the MLP down projection with the next block's mix and value-embedding gate partials
-            fn = lambda: ops.gemm_residual(a, w, x, 0.9, 0.1, x0, x, None, wg, C)
+        else:   # the MLP down projection with the next block's mix
+            fn = lambda: ops.gemm_residual(a, w, x, 0.9, 0.1, x0, x, None)
     elif k == "fc":
         a, w = rnd((M, C)), rnd((F, C), 0.02)
         ssp = torch.rand((M, C // 128), generator=g, device=dev) * 100

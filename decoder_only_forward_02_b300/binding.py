@@ -21,6 +21,7 @@ STATUS_NAMES = {0: "NC_OK", 1: "NC_ERR_INVALID_ARG", 2: "NC_ERR_UNSUPPORTED", 3:
 KERNEL_CLASSES = ["embed_smear", "qkv_rope_qknorm_ve", "attention", "oproj_residual", "fc_relu2",
                   "proj_residual", "lmhead_softcap", "cross_entropy"]
 SS_GROUP = 128   # columns per partial sum of squares
+QKV_GATE_ROWS = 16   # rows after each kv head's v rows in a value-embedding layer's packed q|k|v weight
 
 c_int_p = ctypes.POINTER(ctypes.c_int)
 c_void_pp = ctypes.POINTER(ctypes.c_void_p)
@@ -92,9 +93,9 @@ _SIGS = {
                                   ctypes.c_float, ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p]),
     "nc_op_gemm_residual": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
                                            ctypes.c_int, ctypes.c_void_p, ctypes.c_float, ctypes.c_float]
-                            + [ctypes.c_void_p] * 6 + [ctypes.c_int, ctypes.c_int] + [ctypes.c_void_p] * 3),
+                            + [ctypes.c_void_p] * 7),
     "nc_op_qkv": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p] + [ctypes.c_int] * 6 +
-                  [ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_float,
+                  [ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_void_p, ctypes.c_int, ctypes.c_float,
                    ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int] + [ctypes.c_void_p] * 5),
     "nc_op_rope_table": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_float,
                                         ctypes.c_void_p]),
@@ -102,8 +103,7 @@ _SIGS = {
                         [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     "nc_op_embed_smear": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
                                          ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
-                                         ctypes.c_float, ctypes.c_float] + [ctypes.c_void_p] * 5 +
-                          [ctypes.c_int, ctypes.c_int] + [ctypes.c_void_p] * 3),
+                                         ctypes.c_float, ctypes.c_float] + [ctypes.c_void_p] * 6),
     "nc_op_lmhead_ce": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                        ctypes.c_void_p, ctypes.c_float, ctypes.c_float] + [ctypes.c_void_p] * 5),
     "nc_op_ce_scratch_bytes": (ctypes.c_size_t, [ctypes.c_int]),
@@ -130,19 +130,17 @@ class ops:
         return out
 
     @staticmethod
-    def gemm_residual(A, B, resid, a=1.0, b=0.0, Y=None, x_out=None, xm_out=None, wg=None, c_g=0, status=None):
-        """Returns (xb, ssp, gp); x_out / xm_out are written in place when given."""
+    def gemm_residual(A, B, resid, a=1.0, b=0.0, Y=None, x_out=None, xm_out=None, status=None):
+        """Returns (xb, ssp); x_out / xm_out are written in place when given."""
         M, K = A.shape
         N = B.shape[0]
         dev = A.device
         xb = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
         ssp = torch.empty((M, N // SS_GROUP), dtype=torch.float32, device=dev)
-        Hkv = 0 if wg is None else wg.shape[0]
-        gp = None if wg is None else torch.empty((M, Hkv, N // SS_GROUP), dtype=torch.float32, device=dev)
         check(lib().nc_op_gemm_residual(A.data_ptr(), B.data_ptr(), M, N, K, resid.data_ptr(), a, b, _ptr(Y),
-                                        _ptr(x_out), _ptr(xm_out), xb.data_ptr(), ssp.data_ptr(), _ptr(wg), Hkv,
-                                        c_g, _ptr(gp), _ptr(status), _stream_handle(None)), "nc_op_gemm_residual")
-        return xb, ssp, gp
+                                        _ptr(x_out), _ptr(xm_out), xb.data_ptr(), ssp.data_ptr(), _ptr(status),
+                                        _stream_handle(None)), "nc_op_gemm_residual")
+        return xb, ssp
 
     @staticmethod
     def rope_table(T, D, base, device):
@@ -152,17 +150,34 @@ class ops:
         return t
 
     @staticmethod
-    def qkv(xb, wqkv, T, H, Hkv, D, rope, eps, ssp, gp=None, gate_scale=1.0, ve=None, tokens=None, V=0,
+    def qkv(xb, wqkv, T, H, Hkv, D, rope, eps, ssp, vgate=False, gate_scale=1.0, ve=None, tokens=None, V=0,
             status=None):
+        """wqkv: the packed weight (see pack_qkv); vgate: it holds each kv head's gate rows."""
         M, C = xb.shape
         dev = xb.device
         q = torch.empty((M, H * D), dtype=torch.bfloat16, device=dev)
         k = torch.empty((M, Hkv * D), dtype=torch.bfloat16, device=dev)
         v = torch.empty((M, Hkv * D), dtype=torch.bfloat16, device=dev)
         check(lib().nc_op_qkv(xb.data_ptr(), wqkv.data_ptr(), M, T, C, H, Hkv, D, rope.data_ptr(), rope.shape[1],
-                              eps, ssp.data_ptr(), _ptr(gp), gate_scale, _ptr(ve), _ptr(tokens), V, q.data_ptr(),
-                              k.data_ptr(), v.data_ptr(), _ptr(status), _stream_handle(None)), "nc_op_qkv")
+                              eps, ssp.data_ptr(), int(bool(vgate)), gate_scale, _ptr(ve), _ptr(tokens), V,
+                              q.data_ptr(), k.data_ptr(), v.data_ptr(), _ptr(status), _stream_handle(None)),
+              "nc_op_qkv")
         return q, k, v
+
+    @staticmethod
+    def pack_qkv(wq, wk, wv, wg=None, D=128):
+        """The packed q|k|v weight nc_op_qkv takes: W_q, W_k, then W_v, or (wg [Hkv, c_g] given) for
+        each kv head its D rows of W_v, its gate row (zero beyond c_g) and NC_QKV_GATE_ROWS - 1 zero rows."""
+        if wg is None:
+            return torch.cat([wq, wk, wv]).contiguous()
+        Hkv, c_g = wg.shape
+        C = wq.shape[1]
+        parts = [wq, wk]
+        for g in range(Hkv):
+            gate = torch.zeros((QKV_GATE_ROWS, C), dtype=wq.dtype, device=wq.device)
+            gate[0, :c_g] = wg[g]
+            parts += [wv[g * D:(g + 1) * D], gate]
+        return torch.cat(parts).contiguous()
 
     @staticmethod
     def attention(q, k, v, B, T, H, Hkv, D, window, status=None):
@@ -172,9 +187,8 @@ class ops:
         return y
 
     @staticmethod
-    def embed_smear(tokens, wte, smear_gate=None, c_s=0, embed_norm=False, eps=1e-6, a=1.0, wg=None, c_g=0,
-                    status=None):
-        """Returns (x0, x, xb, ssp, gp)."""
+    def embed_smear(tokens, wte, smear_gate=None, c_s=0, embed_norm=False, eps=1e-6, a=1.0, status=None):
+        """Returns (x0, x, xb, ssp)."""
         B, T = tokens.shape
         V, C = wte.shape
         dev = wte.device
@@ -183,13 +197,10 @@ class ops:
         x = torch.empty((M, C), dtype=torch.float32, device=dev)
         xb = torch.empty((M, C), dtype=torch.bfloat16, device=dev)
         ssp = torch.empty((M, C // SS_GROUP), dtype=torch.float32, device=dev)
-        Hkv = 0 if wg is None else wg.shape[0]
-        gp = None if wg is None else torch.empty((M, Hkv, C // SS_GROUP), dtype=torch.float32, device=dev)
         check(lib().nc_op_embed_smear(tokens.data_ptr(), B, T, wte.data_ptr(), V, C, _ptr(smear_gate), c_s or C,
                                       int(embed_norm), eps, a, x0.data_ptr(), x.data_ptr(), xb.data_ptr(),
-                                      ssp.data_ptr(), _ptr(wg), Hkv, c_g or C, _ptr(gp), _ptr(status),
-                                      _stream_handle(None)), "nc_op_embed_smear")
-        return x0, x, xb, ssp, gp
+                                      ssp.data_ptr(), _ptr(status), _stream_handle(None)), "nc_op_embed_smear")
+        return x0, x, xb, ssp
 
     @staticmethod
     def lmhead_ce(xf, wlm, targets, ssp=None, C=0, eps=1e-6, cap=15.0, status=None):

@@ -31,21 +31,20 @@
 // Fused epilogues (the operations are those of "Nanochat在nanoGPT之上的新增功能", section 1
 // feature table and notes; RMSNorm has no weight, so norm(x) W^T = diag(1/rms(x)) (x W^T) and
 // the normalisation of a GEMM's input becomes a per-row scale of its accumulator):
-//   EPI_RESID        residual update of an output projection (attention c_proj, MLP c_proj):
-//                    x += acc, then optionally the backout cache, the next block's
-//                    resid_lambdas/x0_lambdas mix or the final backout subtraction; writes the
-//                    stream (fp32), its bf16 copy (the next GEMM's A operand), per-row partial
-//                    sums of squares over 128-column groups (the next RMSNorm) and, before a
-//                    value-embedding layer, partial dot products with its gate weights
 //   EPI_RELU2_BF16   squared ReLU of the MLP up projection, input RMSNorm as a row scale
 //   EPI_SOFTCAP_F32  tanh soft-cap (+-cap) of the untied lm_head logits, final RMSNorm as a row
 //                    scale (hardware tanh)
 //   EPI_CE           the lm_head with soft-cap and cross-entropy: per row and 128-column group,
 //                    the sum of exp(logit) and the target's logit; no logits are stored
 //   EPI_QKV          split of the packed q|k|v projection, input RMSNorm as a row scale; RoPE
-//                    then per-head RMSNorm of q and k; on value-embedding layers
-//                    v += gate * ve[token] with gate = scale * sigmoid(rs * (x . w_gate))
+//                    then per-head RMSNorm of q and k; on value-embedding layers each kv head's
+//                    v rows are followed in the packed weight by its gate row (and 15 zero rows),
+//                    so the head's tile (N = D + 16) also yields the gate's pre-activation
+//                    x . w_gate and the epilogue adds gate * ve[token] with
+//                    gate = scale * sigmoid(rs * (x . w_gate)) -- the gate is a contraction, so it
+//                    runs on the tensor cores with the projection it belongs to
 //   EPI_BF16         plain store (used by tests of the mainloop)
+// The residual-stream updates of the output projections are in gemm_resid.cu.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -73,28 +72,19 @@ constexpr uint32_t TMEM_COLS = 2 * BN;
 constexpr int SLAB_BUF = 32 * 128;       // one staging buffer: 32 rows x 128 B
 constexpr int SLAB_BYTES = 2 * SLAB_BUF; // two per epilogue warp, used alternately
 
-// Second template argument of a residual-update launch whose epilogue also produces the
-// value-embedding gate partials (for the other kinds it is the head dimension, or 0).
-constexpr int RESID_GATE = 1;
-constexpr int GATE_BYTES = MAX_GATE_HEADS * 128 * 2;   // gate weights of one 128-column group (per warp)
 
 // Shared memory per epilogue kind.  Kinds whose epilogue stores with TMA keep two staging
 // buffers per warp (a store drains from one while the next is filled) and a 5-stage operand
 // ring; the squared-ReLU and soft-cap epilogues store row-coalesced from one buffer, and the
-// space saved deepens their ring to 6 stages (operand latency is what starves the MMA).  A
-// residual update that produces gate partials keeps each warp's copy of the gate weights of
-// its column group in shared memory (read by every lane at the same address), which costs
-// one operand stage.
+// space saved deepens their ring to 6 stages (operand latency is what starves the MMA).
 // The cross-entropy epilogue stores no tile at all: no staging buffers, a 7-stage ring.
 template <int KIND, int D>
 struct Cfg {
   static constexpr bool LSU_STORE = KIND == EPI_RELU2_BF16 || KIND == EPI_SOFTCAP_F32;
-  static constexpr bool GATE = KIND == EPI_RESID && D == RESID_GATE;
-  static constexpr int STAGES = KIND == EPI_CE ? 7 : (LSU_STORE ? 6 : (GATE ? 4 : 5));
+  static constexpr int STAGES = KIND == EPI_CE ? 7 : (LSU_STORE ? 6 : 5);
   static constexpr int SLAB_WARP = KIND == EPI_CE ? 0 : (LSU_STORE ? SLAB_BUF : SLAB_BYTES);   // staging bytes per warp
   static constexpr int OFF_SLAB = STAGES * (A_BYTES + B_BYTES);
-  static constexpr int OFF_GATE = OFF_SLAB + NUM_EPI_WARPS * SLAB_WARP;
-  static constexpr int OFF_CTRL = OFF_GATE + (GATE ? NUM_EPI_WARPS * GATE_BYTES : 0);
+  static constexpr int OFF_CTRL = OFF_SLAB + NUM_EPI_WARPS * SLAB_WARP;
   struct __align__(8) Ctrl {
     uint64_t full[STAGES];
     uint64_t empty[STAGES];
@@ -151,41 +141,7 @@ struct Slab {
 #pragma unroll
     for (int c = 0; c < 8; ++c) *slab_chunk(buf(), lane, c) = x[c];
   }
-  __device__ __forceinline__ void put_row_f32(int lane, const float (&x)[32]) const {
-#pragma unroll
-    for (int c = 0; c < 8; ++c)
-      *reinterpret_cast<float4*>(slab_chunk(buf(), lane, c)) = make_float4(x[4 * c], x[4 * c + 1], x[4 * c + 2], x[4 * c + 3]);
-  }
-  // Transpose a [32 rows][32 fp32] chunk loaded row-coalesced (load k of lane l holds row
-  // 4k + l/8, columns 4(l%8)..+3) into row `lane` of this thread.
-  __device__ __forceinline__ void transpose_f32(int lane, const float4 (&v)[8], float (&row)[32]) const {
-    __syncwarp();
-#pragma unroll
-    for (int k = 0; k < 8; ++k) *reinterpret_cast<float4*>(slab_chunk(buf(), k * 4 + (lane >> 3), lane & 7)) = v[k];
-    __syncwarp();
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      const float4 t = *reinterpret_cast<const float4*>(slab_chunk(buf(), lane, c));
-      row[4 * c] = t.x;
-      row[4 * c + 1] = t.y;
-      row[4 * c + 2] = t.z;
-      row[4 * c + 3] = t.w;
-    }
-    __syncwarp();
-  }
 };
-
-// Row-coalesced load of the [32 rows][32 fp32] chunk at (m0w, c0) of a row-major matrix.
-__device__ __forceinline__ void load_chunk_f32(const float* p, int ld, int m0w, int c0, int M, int lane,
-                                               float4 (&v)[8]) {
-  const int rsub = lane >> 3, csub = (lane & 7) * 4;
-#pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    const int gm = m0w + k * 4 + rsub;
-    v[k] = gm < M ? *reinterpret_cast<const float4*>(p + static_cast<size_t>(gm) * ld + c0 + csub)
-                  : make_float4(0.f, 0.f, 0.f, 0.f);
-  }
-}
 
 __device__ __forceinline__ uint4 pack8_bf16(const float* a) {
   return make_uint4(pack_bf16(a[0], a[1]), pack_bf16(a[2], a[3]), pack_bf16(a[4], a[5]), pack_bf16(a[6], a[7]));
@@ -194,7 +150,7 @@ __device__ __forceinline__ uint4 pack8_bf16(const float* a) {
 __device__ __forceinline__ float sigmoid_fast(float z) { return 1.0f / (1.0f + __expf(-z)); }
 
 struct OutMaps {
-  CUtensorMap o0, o1, o2;   // EPI_RESID: x_out, xm_out, xb;  EPI_QKV: q, k, v;  else: out
+  CUtensorMap o0, o1, o2;   // EPI_QKV: q, k, v;  else: o0 = out
 };
 
 // Release an accumulator buffer to the pair's MMA thread (after this warp's last tcgen05.ld
@@ -224,98 +180,96 @@ __device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int 
   nb = local / rows;
 }
 
+// ---------------------------------------------------------------- column tiles
+// Column tile nb of a launch: its first column (a row of B), its width (the MMA's N) and, for a
+// value-embedding head's tile of the q|k|v projection, that kv head (else -1).  Without gate rows
+// every tile is BN wide (the epilogue skips columns at or beyond `end`).  With them, the q|k
+// columns are cut into BN-wide tiles (the last one narrower) and each kv head gets one tile of
+// its D v rows and VGATE_ROWS gate rows.
+struct ColTile {
+  int col0, width, end, vhead;
+};
+
+template <int KIND>
+__device__ __forceinline__ ColTile col_tile(int nb, int N, const GemmEpi& ep) {
+  ColTile t;
+  t.vhead = -1;
+  if (KIND == EPI_QKV && ep.vgate) {
+    const int qk = (ep.H + ep.Hkv) * ep.D, nqk = (qk + BN - 1) / BN;
+    if (nb >= nqk) {
+      t.vhead = nb - nqk;
+      t.width = ep.D + VGATE_ROWS;
+      t.col0 = qk + t.vhead * t.width;
+      t.end = t.col0 + t.width;
+      return t;
+    }
+    t.col0 = nb * BN;
+    t.width = min(BN, qk - t.col0);
+    t.end = t.col0 + t.width;
+    return t;
+  }
+  t.col0 = nb * BN;
+  t.width = BN;
+  t.end = N;
+  return t;
+}
+
+__host__ __device__ __forceinline__ int num_col_tiles(int kind, int N, int H, int Hkv, int D, int vgate) {
+  if (kind == EPI_QKV && vgate) return ((H + Hkv) * D + BN - 1) / BN + Hkv;
+  return (N + BN - 1) / BN;
+}
+
 // ---------------------------------------------------------------- per-tile prologue
 // Row data an epilogue needs that does not depend on the accumulator (the RMSNorm partial sums,
-// the value-embedding gate partials, the token id).  Its loads are issued one tile ahead, while
-// the epilogue of the previous tile runs, and reduced just before the tile's epilogue, so their
-// latency is off the epilogue's critical path.  Residual-update tiles instead prefetch their
-// residual rows into L2 one tile ahead.
-template <int D>
+// the token id).  Its loads are issued one tile ahead, while the epilogue of the previous tile
+// runs, and reduced just before the tile's epilogue, so their latency is off the epilogue's
+// critical path.
 struct PreRaw {
   float ss[MAX_NCG];
-  float gp[128 / (D > 0 ? D : 128)][MAX_NCG];
   int tok;
 };
 
 struct EpiPre {
   float rs = 1.f;              // input RMSNorm row scale
-  float g[2] = {0.f, 0.f};     // value-embedding gate per head of the column group (EPI_QKV)
-  int tok = -1;                // EPI_QKV: token id of the row when a gate applies, else -1;
+  int tok = -1;                // EPI_QKV: token id of the row on a value-embedding head's tile, else -1;
                                // EPI_CE: the row's target
 };
 
-template <int KIND, int D>
-__device__ __forceinline__ void pre_issue(PreRaw<D>& raw, int lane, int m0w, int n0, int M, int N,
-                                          const GemmEpi& ep) {
+template <int KIND>
+__device__ __forceinline__ void pre_issue(PreRaw& raw, int lane, int m0w, int M, const GemmEpi& ep,
+                                          const ColTile& ct) {
   const int m = m0w + lane;
-  if (n0 >= N || m >= M) return;
-  if constexpr (KIND == EPI_RESID) {
-    const size_t off = static_cast<size_t>(m) * N + n0;
+  if (m >= M) return;
+  if (ep.ssp_in != nullptr) {
+    const float* p = ep.ssp_in + static_cast<size_t>(m) * ep.ncg;
 #pragma unroll
-    for (int l = 0; l < 4; ++l) {
-      prefetch_l2(ep.resid + off + l * 32);
-      if (ep.Y != nullptr) prefetch_l2(ep.Y + off + l * 32);
-    }
-  } else if constexpr (KIND == EPI_RELU2_BF16 || KIND == EPI_SOFTCAP_F32 || KIND == EPI_QKV || KIND == EPI_CE) {
-    if (ep.ssp_in != nullptr) {
-      const float* p = ep.ssp_in + static_cast<size_t>(m) * ep.ncg;
-#pragma unroll
-      for (int g = 0; g < MAX_NCG; ++g)
-        if (g < ep.ncg) raw.ss[g] = p[g];
-    }
-    if constexpr (KIND == EPI_CE) raw.tok = ep.targets[m];
-    if constexpr (KIND == EPI_QKV) {
-      const int vcol0 = (ep.H + ep.Hkv) * D;
-      if (ep.gp_in != nullptr && n0 + 128 > vcol0) {
-        raw.tok = ep.tokens[m];
-#pragma unroll
-        for (int s = 0; s < 128 / D; ++s) {
-          const int c = n0 + s * D;
-          if (c < vcol0 || c >= N) continue;
-          const float* gp = ep.gp_in + (static_cast<size_t>(m) * ep.Hkv + (c - vcol0) / D) * ep.ncg;
-#pragma unroll
-          for (int g = 0; g < MAX_NCG; ++g)
-            if (g < ep.ncg) raw.gp[s][g] = gp[g];
-        }
-      }
-    }
+    for (int g = 0; g < MAX_NCG; ++g)
+      if (g < ep.ncg) raw.ss[g] = p[g];
   }
+  if constexpr (KIND == EPI_CE) raw.tok = ep.targets[m];
+  if constexpr (KIND == EPI_QKV) raw.tok = ct.vhead >= 0 ? ep.tokens[m] : -1;
 }
 
-template <int KIND, int D>
-__device__ __forceinline__ EpiPre pre_finish(const PreRaw<D>& raw, int lane, int m0w, int n0, int M, int N,
-                                             const GemmEpi& ep) {
+template <int KIND>
+__device__ __forceinline__ EpiPre pre_finish(const PreRaw& raw, int lane, int m0w, int M, const GemmEpi& ep,
+                                             const ColTile& ct) {
   EpiPre p;
   const int m = m0w + lane;
-  if (n0 >= N || m >= M) return p;
-  if constexpr (KIND == EPI_RELU2_BF16 || KIND == EPI_SOFTCAP_F32 || KIND == EPI_QKV || KIND == EPI_CE) {
-    if constexpr (KIND == EPI_CE) p.tok = raw.tok;
-    if (ep.ssp_in != nullptr) {
-      float ss = 0.f;
+  if (m >= M) return p;
+  if constexpr (KIND == EPI_CE) p.tok = raw.tok;
+  if (ep.ssp_in != nullptr) {
+    float ss = 0.f;
 #pragma unroll
-      for (int g = 0; g < MAX_NCG; ++g)
-        if (g < ep.ncg) ss += raw.ss[g];
-      p.rs = rsqrtf(ss * ep.inv_ncols + ep.eps);
-    }
-    if constexpr (KIND == EPI_QKV) {
-      const int vcol0 = (ep.H + ep.Hkv) * D, kcols = ep.Hkv * D;
-      if (ep.gp_in != nullptr && n0 + 128 > vcol0) {
-        p.tok = (raw.tok >= 0 && raw.tok < ep.V) ? raw.tok : -1;
-#pragma unroll
-        for (int s = 0; s < 128 / D; ++s) {
-          const int c = n0 + s * D;
-          if (c < vcol0 || c >= N) continue;
-          float z = 0.f;
-#pragma unroll
-          for (int g = 0; g < MAX_NCG; ++g)
-            if (g < ep.ncg) z += raw.gp[s][g];
-          p.g[s] = ep.gate_scale * sigmoid_fast(p.rs * z);
-          if (p.tok >= 0) {
-            const bf16* row = ep.ve + static_cast<size_t>(p.tok) * kcols + static_cast<size_t>((c - vcol0) / D) * D;
-#pragma unroll
-            for (int l = 0; l < D * 2 / 128; ++l) prefetch_l2(row + l * 64);
-          }
-        }
+    for (int g = 0; g < MAX_NCG; ++g)
+      if (g < ep.ncg) ss += raw.ss[g];
+    p.rs = rsqrtf(ss * ep.inv_ncols + ep.eps);
+  }
+  if constexpr (KIND == EPI_QKV) {
+    if (ct.vhead >= 0) {
+      p.tok = (raw.tok >= 0 && raw.tok < ep.V) ? raw.tok : -1;
+      if (p.tok >= 0) {   // the head's slice of the token's value-embedding row, into L2
+        const bf16* row = ep.ve + static_cast<size_t>(p.tok) * ep.Hkv * ep.D + static_cast<size_t>(ct.vhead) * ep.D;
+        for (int l = 0; l < ep.D * 2 / 128; ++l) prefetch_l2(row + l * 64);
       }
     }
   }
@@ -432,27 +386,6 @@ __device__ __forceinline__ void epi_softcap(uint32_t taddr, uint32_t tempty, int
   release_acc(lane, tempty);
 }
 
-// Start of a residual-update tile, issued before its accumulator is ready so that the
-// latency overlaps the wait: with GATE, the gate weights of the warp's 128 columns go to its
-// own shared buffer (gate_w); then the first 32-column chunk of the residual (and of Y).
-template <bool GATE>
-__device__ __forceinline__ void resid_begin(int lane, int m0w, int n0, int M, int N, const GemmEpi& ep,
-                                            bf16* gate_w, float4 (&rv)[8], float4 (&yv)[8]) {
-  if (n0 >= N) return;
-  if constexpr (GATE) {
-    // W_g[:, n0 .. n0+128) (zero past c_g), 16 pieces of 16 B per head row
-    __syncwarp();   // every lane is done with the previous tile's copy
-    for (int i = lane; i < ep.Hkv * 16; i += 32) {
-      const int h = i >> 4, c = n0 + (i & 15) * 8;
-      uint4 w = make_uint4(0u, 0u, 0u, 0u);
-      if (c < ep.c_g) w = __ldg(reinterpret_cast<const uint4*>(ep.wg + static_cast<size_t>(h) * ep.c_g + c));
-      reinterpret_cast<uint4*>(gate_w)[i] = w;
-    }
-  }
-  load_chunk_f32(ep.resid, N, m0w, n0, M, lane, rv);
-  if (ep.Y != nullptr) load_chunk_f32(ep.Y, N, m0w, n0, M, lane, yv);
-}
-
 // Cross-entropy partials of the soft-capped lm_head, with no logits stored: per row, the sum
 // of exp(z) over the warp's 128 columns, z = cap * tanh(rs * acc / cap), and z at the row's
 // target column when the target lies in them.  |z| < cap bounds every term by e^cap, so the sum
@@ -493,141 +426,12 @@ __device__ __forceinline__ void epi_ce(uint32_t taddr, uint32_t tempty, int lane
   }
 }
 
-// Residual stream update (attention and MLP output projections), with the next consumer's
-// inputs: the bf16 copy of the new stream and its partial sums of squares (the consumer's
-// RMSNorm row scale), and on request the next block's residual mix, the backout cache, the
-// final backout, and (GATE) the value-embedding gate partial dot products.  rv / yv arrive holding
-// the first chunk (resid_begin); each later chunk is loaded as soon as the previous one has
-// been consumed, so its latency overlaps the previous chunk's gate and store work.
-template <bool GATE>
-__device__ __forceinline__ void epi_resid(uint32_t taddr, uint32_t tempty, int lane, int m0w, int n0, int M, int N,
-                                          const GemmEpi& ep, const OutMaps& om, Slab& sl, const bf16* gate_w,
-                                          float4 (&rv)[8], float4 (&yv)[8]) {
-  if (n0 >= N) {
-    release_acc(lane, tempty);
-    return;
-  }
-  const int m = m0w + lane;
-  constexpr bool has_gate = GATE;
-  if constexpr (GATE) __syncwarp();   // the gate weights staged by every lane are visible
-  float ss = 0.f;
-  float gacc[MAX_GATE_HEADS];
-#pragma unroll
-  for (int h = 0; h < MAX_GATE_HEADS; ++h) gacc[h] = 0.f;
-  uint32_t xbp[32];
-#pragma unroll 1
-  for (int cp = 0; cp < 2; ++cp) {
-#pragma unroll
-  for (int hf = 0; hf < 2; ++hf) {
-    const int ch = cp * 2 + hf;
-    const int c0 = n0 + ch * 32;
-    uint32_t r[32];
-    tmem_ld32(taddr + ch * 32, r);
-    tmem_ld_wait(r);
-    if (ch == 3) release_acc(lane, tempty);
-    float x[32];
-    sl.acquire(lane);
-    if (ep.xm_out != nullptr) {   // backout cache: the stream after this block, before mixing
-      sl.transpose_f32(lane, rv, x);
-#pragma unroll
-      for (int j = 0; j < 32; ++j) x[j] += __uint_as_float(r[j]);
-      sl.put_row_f32(lane, x);
-      sl.store(&om.o1, c0, m0w, lane);
-      sl.acquire(lane);
-      if (ep.Y != nullptr) {
-        float y[32];
-        sl.transpose_f32(lane, yv, y);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) x[j] = fmaf(ep.a, x[j], ep.b * y[j]);
-      } else {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) x[j] *= ep.a;
-      }
-      if (ch < 3) {
-        load_chunk_f32(ep.resid, N, m0w, c0 + 32, M, lane, rv);
-        if (ep.Y != nullptr) load_chunk_f32(ep.Y, N, m0w, c0 + 32, M, lane, yv);
-      }
-    } else {
-      // x' = a (resid + acc) + b Y: the a resid + b Y part is formed in the loaded layout, so
-      // one transpose serves both inputs
-      if (ep.Y != nullptr) {
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          rv[k].x = fmaf(ep.a, rv[k].x, ep.b * yv[k].x);
-          rv[k].y = fmaf(ep.a, rv[k].y, ep.b * yv[k].y);
-          rv[k].z = fmaf(ep.a, rv[k].z, ep.b * yv[k].z);
-          rv[k].w = fmaf(ep.a, rv[k].w, ep.b * yv[k].w);
-        }
-      } else if (ep.a != 1.f) {
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          rv[k].x *= ep.a; rv[k].y *= ep.a; rv[k].z *= ep.a; rv[k].w *= ep.a;
-        }
-      }
-      sl.transpose_f32(lane, rv, x);
-      if (ch < 3) {
-        load_chunk_f32(ep.resid, N, m0w, c0 + 32, M, lane, rv);
-        if (ep.Y != nullptr) load_chunk_f32(ep.Y, N, m0w, c0 + 32, M, lane, yv);
-      }
-#pragma unroll
-      for (int j = 0; j < 32; ++j) x[j] = fmaf(ep.a, __uint_as_float(r[j]), x[j]);
-    }
-#pragma unroll
-    for (int j = 0; j < 32; ++j) ss = fmaf(x[j], x[j], ss);
-    if (has_gate) {
-#pragma unroll
-      for (int h = 0; h < MAX_GATE_HEADS; ++h) {
-        if (h < ep.Hkv) {
-          const uint4* w4 = reinterpret_cast<const uint4*>(gate_w + h * 128 + ch * 32);
-          float acc = gacc[h];
-#pragma unroll
-          for (int q8 = 0; q8 < 4; ++q8) {
-            const uint4 u = w4[q8];
-            const __nv_bfloat162* w2 = reinterpret_cast<const __nv_bfloat162*>(&u);
-#pragma unroll
-            for (int t = 0; t < 4; ++t) {
-              const float2 f = __bfloat1622float2(w2[t]);
-              acc = fmaf(x[q8 * 8 + 2 * t], f.x, acc);
-              acc = fmaf(x[q8 * 8 + 2 * t + 1], f.y, acc);
-            }
-          }
-          gacc[h] = acc;
-        }
-      }
-    }
-    if (ep.x_out != nullptr) {
-      sl.put_row_f32(lane, x);
-      sl.store(&om.o0, c0, m0w, lane);
-    }
-#pragma unroll
-    for (int j = 0; j < 16; ++j) xbp[hf * 16 + j] = pack_bf16(x[2 * j], x[2 * j + 1]);
-    if (hf == 1) {
-      uint4 o[8];
-#pragma unroll
-      for (int c = 0; c < 8; ++c) o[c] = make_uint4(xbp[4 * c], xbp[4 * c + 1], xbp[4 * c + 2], xbp[4 * c + 3]);
-      sl.acquire(lane);
-      sl.put_row(lane, o);
-      sl.store(&om.o2, c0 - 32, m0w, lane);
-    }
-  }
-  }
-  if (m < M) {
-    const int g = n0 / SS_GROUP;
-    ep.ssp_out[static_cast<size_t>(m) * ep.ncg + g] = ss;
-    if (has_gate) {
-#pragma unroll
-      for (int h = 0; h < MAX_GATE_HEADS; ++h)
-        if (h < ep.Hkv) ep.gp_out[(static_cast<size_t>(m) * ep.Hkv + h) * ep.ncg + g] = gacc[h];
-    }
-  }
-}
-
-// Packed q|k|v projection: q and k heads are rotated (RoPE) and RMS-normalised per head, v
-// heads get the value-embedding gate term.  rs (the block's input RMSNorm) scales every
-// column; for q and k the head norm is taken from the unrotated accumulator, since the
-// rotation keeps each head's norm.
+// Packed q|k|v projection: q and k heads are rotated (RoPE) and RMS-normalised per head; v heads
+// (of a layer without value embeddings) are stored as they are.  rs (the block's input RMSNorm)
+// scales every column; for q and k the head norm is taken from the unrotated accumulator, since
+// the rotation keeps each head's norm.  Columns at or beyond `end` belong to no output.
 template <int D>
-__device__ __forceinline__ void epi_qkv(uint32_t taddr, uint32_t tempty, int lane, int m0w, int n0, int M, int N,
+__device__ __forceinline__ void epi_qkv(uint32_t taddr, uint32_t tempty, int lane, int m0w, int n0, int end, int M,
                                         const GemmEpi& ep, const OutMaps& om, Slab& sl, const EpiPre& pre) {
   const int m = m0w + lane;
   const float rs = pre.rs;
@@ -638,7 +442,7 @@ __device__ __forceinline__ void epi_qkv(uint32_t taddr, uint32_t tempty, int lan
 #pragma unroll
   for (int s = 0; s < 128 / D; ++s) {
     const int c = n0 + s * D;
-    if (c >= N) break;
+    if (c >= end) break;
     const uint32_t tb = taddr + s * D;
     const CUtensorMap* map;
     int xcol;
@@ -693,32 +497,22 @@ __device__ __forceinline__ void epi_qkv(uint32_t taddr, uint32_t tempty, int lan
     } else {
       xcol = c - qcols - kcols;
       map = &om.o2;
-      const int hv = xcol / D;
-      const float g = pre.g[s];
-      const uint4* vr = pre.tok >= 0 ? reinterpret_cast<const uint4*>(ep.ve + static_cast<size_t>(pre.tok) * kcols +
-                                                                      static_cast<size_t>(hv) * D)
-                                     : nullptr;
 #pragma unroll
       for (int cc = 0; cc < D / 64; ++cc) {
         uint32_t r0[32], r1[32];
         tmem_ld32(tb + cc * 64, r0);
         tmem_ld32(tb + cc * 64 + 32, r1);
-        uint4 e[8];
-#pragma unroll
-        for (int c8 = 0; c8 < 8; ++c8) e[c8] = vr ? __ldg(vr + cc * 8 + c8) : make_uint4(0u, 0u, 0u, 0u);
         tmem_ld_wait(r0);
         tmem_ld_wait(r1);
 #pragma unroll
         for (int c8 = 0; c8 < 8; ++c8) {
-          const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&e[c8]);
           uint32_t pv[4];
 #pragma unroll
           for (int t = 0; t < 4; ++t) {
             const int idx = c8 * 8 + 2 * t;
-            const float2 f = __bfloat1622float2(h2[t]);
             const float v0 = __uint_as_float(idx < 32 ? r0[idx] : r1[idx - 32]);
             const float v1 = __uint_as_float(idx + 1 < 32 ? r0[idx + 1] : r1[idx + 1 - 32]);
-            pv[t] = pack_bf16(fmaf(g, f.x, v0 * rs), fmaf(g, f.y, v1 * rs));
+            pv[t] = pack_bf16(v0 * rs, v1 * rs);
           }
           *slab_chunk(sl.buf_ahead(cc), lane, c8) = make_uint4(pv[0], pv[1], pv[2], pv[3]);
         }
@@ -730,16 +524,62 @@ __device__ __forceinline__ void epi_qkv(uint32_t taddr, uint32_t tempty, int lan
   release_acc(lane, tempty);
 }
 
+// A value-embedding head's tile of the packed q|k|v projection: accumulator columns [0, D) are the
+// head's v, column D the gate's pre-activation x . w_gate (columns D+1.. are zero rows).
+//   v = rs * acc + gate * ve[token, head],  gate = gate_scale * sigmoid(rs * acc[D])
+// With D = 128 the two warpgroups take 64 columns each; with D = 64 the first takes the head.
+template <int D>
+__device__ __forceinline__ void epi_vgate(uint32_t taddr, uint32_t tempty, int lane, int m0w, int group, int vhead,
+                                          const GemmEpi& ep, const OutMaps& om, Slab& sl, const EpiPre& pre) {
+  const int c0 = D == 128 ? group * 64 : 0;
+  if (D == 64 && group == 1) {
+    release_acc(lane, tempty);
+    return;
+  }
+  const float rs = pre.rs;
+  uint32_t gz[1];
+  tmem_ld1(taddr + D, gz);
+  uint32_t r0[32], r1[32];
+  tmem_ld32(taddr + c0, r0);
+  tmem_ld32(taddr + c0 + 32, r1);
+  uint4 e[8];
+  const uint4* vr = pre.tok >= 0 ? reinterpret_cast<const uint4*>(ep.ve + static_cast<size_t>(pre.tok) * ep.Hkv * D +
+                                                                  static_cast<size_t>(vhead) * D + c0)
+                                 : nullptr;
+#pragma unroll
+  for (int c8 = 0; c8 < 8; ++c8) e[c8] = vr ? __ldg(vr + c8) : make_uint4(0u, 0u, 0u, 0u);
+  tmem_ld_wait(gz);
+  tmem_ld_wait(r0);
+  tmem_ld_wait(r1);
+  release_acc(lane, tempty);
+  const float g = ep.gate_scale * sigmoid_fast(rs * __uint_as_float(gz[0]));
+  sl.acquire(lane);
+#pragma unroll
+  for (int c8 = 0; c8 < 8; ++c8) {
+    const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&e[c8]);
+    uint32_t pv[4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const int idx = c8 * 8 + 2 * t;
+      const float2 f = __bfloat1622float2(h2[t]);
+      const float v0 = __uint_as_float(idx < 32 ? r0[idx] : r1[idx - 32]);
+      const float v1 = __uint_as_float(idx + 1 < 32 ? r0[idx + 1] : r1[idx + 1 - 32]);
+      pv[t] = pack_bf16(fmaf(g, f.x, v0 * rs), fmaf(g, f.y, v1 * rs));
+    }
+    *slab_chunk(sl.buf(), lane, c8) = make_uint4(pv[0], pv[1], pv[2], pv[3]);
+  }
+  sl.store(&om.o2, vhead * D + c0, m0w, lane);
+}
+
 template <int KIND, int D>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ OutMaps om, int M, int N, int K, int grp,
-                   const __grid_constant__ GemmEpi ep) {
+                   const __grid_constant__ CUtensorMap tmBv, const __grid_constant__ OutMaps om, int M, int N, int K,
+                   int grp, const __grid_constant__ GemmEpi ep) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   using L = Cfg<KIND, D>;
-  constexpr int PD = KIND == EPI_QKV ? D : 0;   // head dimension of the prologue data (QKV only)
   constexpr int STAGES = L::STAGES;
   const uint32_t sA = smem_u32(smem);
   const uint32_t sB = sA + STAGES * A_BYTES;
@@ -748,7 +588,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();            // 0: pair leader (issues the MMAs)
   const int pair = static_cast<int>(blockIdx.x) >> 1, npairs = static_cast<int>(gridDim.x) >> 1;
-  const int num_m = (M + PAIR_M - 1) / PAIR_M, num_n = (N + BN - 1) / BN;
+  const int num_m = (M + PAIR_M - 1) / PAIR_M, num_n = num_col_tiles(KIND, N, ep.H, ep.Hkv, ep.D, ep.vgate);
   const int num_tiles = num_m * num_n, kblocks = K / BK;
   int* status = ep.status;
 
@@ -768,6 +608,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    if (KIND == EPI_QKV && ep.vgate) tma_prefetch_desc(&tmBv);
   }
   if (warp == 1) {
     tmem_alloc_pair(smem_u32(&ctl->tmem_base), TMEM_COLS);
@@ -794,6 +635,11 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int tile = pair; tile < num_tiles && ok; tile += npairs) {
         int mb, nb;
         tile_coords(tile, num_m, num_n, grp, mb, nb);
+        const ColTile ct = col_tile<KIND>(nb, N, ep);
+        // a value-embedding head's tile loads its D + VGATE_ROWS rows of B through the map whose box
+        // is half of that; every other tile loads BN / 2 rows per CTA (the MMA uses width / 2)
+        const bool vt = ct.vhead >= 0;
+        const uint32_t b_bytes = vt ? static_cast<uint32_t>(ct.width / 2) * BK * 2 : static_cast<uint32_t>(B_BYTES);
         for (int kb = 0; kb < kblocks; ++kb) {
           const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
           if (!mbar_wait_cluster(smem_u32(&ctl->empty[s]), ph ^ 1, abort, status)) {
@@ -801,9 +647,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             break;
           }
           const uint32_t fb = mapa_shared(smem_u32(&ctl->full[s]), 0);   // the leader's barrier
-          if (rank == 0) mbar_arrive_expect_tx(smem_u32(&ctl->full[s]), 2 * (A_BYTES + B_BYTES));
+          if (rank == 0) mbar_arrive_expect_tx(smem_u32(&ctl->full[s]), 2 * (A_BYTES + b_bytes));
           tma_load_2d_pair_hint(sA + s * A_BYTES, &tmA, fb, kb * BK, mb * PAIR_M + static_cast<int>(rank) * BM, pol_a);
-          tma_load_2d_pair_hint(sB + s * B_BYTES, &tmB, fb, kb * BK, nb * BN + static_cast<int>(rank) * B_ROWS, pol_b);
+          tma_load_2d_pair_hint(sB + s * B_BYTES, vt ? &tmBv : &tmB, fb, kb * BK,
+                                ct.col0 + static_cast<int>(rank) * (ct.width / 2), pol_b);
           ++it;
         }
       }
@@ -814,10 +661,12 @@ __global__ void __launch_bounds__(THREADS, 1)
           mbar_wait_cluster(smem_u32(&ctl->full[j % STAGES]), (j / STAGES) & 1, nullptr, status);
       }
     } else if (warp == 1 && lane == 0 && rank == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(PAIR_M, BN);
       uint32_t it = 0, tc = 0;
       bool ok = true;
       for (int tile = pair; tile < num_tiles && ok; tile += npairs, ++tc) {
+        int mb, nb;
+        tile_coords(tile, num_m, num_n, grp, mb, nb);
+        const uint32_t idesc = idesc_bf16_f32(PAIR_M, col_tile<KIND>(nb, N, ep).width);
         const uint32_t a = tc & 1, aph = (tc >> 1) & 1;
         if (!mbar_wait_cluster(smem_u32(&ctl->tempty[a]), aph ^ 1, abort, status)) break;
         tc_fence_after();
@@ -850,43 +699,46 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int quarter = warp & 3;   // TMEM lanes 32*(warp % 4) .. +31 are this warp's
     const int group = ew >> 2;
     Slab sl{smem + L::OFF_SLAB + ew * L::SLAB_WARP, smem_u32(smem + L::OFF_SLAB + ew * L::SLAB_WARP), 0u};
-    bf16* gate_w = reinterpret_cast<bf16*>(smem + L::OFF_GATE + ew * GATE_BYTES);   // used with a gate only
-    auto coords = [&](int tile, int& m0w, int& n0) {
+    auto coords = [&](int tile, int& m0w, ColTile& ct) {
       int mb, nb;
       tile_coords(tile, num_m, num_n, grp, mb, nb);
       m0w = mb * PAIR_M + static_cast<int>(rank) * BM + quarter * 32;
-      n0 = nb * BN + group * 128;
+      ct = col_tile<KIND>(nb, N, ep);
     };
-    PreRaw<PD> raw;
+    PreRaw raw;
     raw.tok = -1;
     if (pair < num_tiles) {
-      int m0w, n0;
-      coords(pair, m0w, n0);
-      pre_issue<KIND, PD>(raw, lane, m0w, n0, M, N, ep);
+      int m0w;
+      ColTile ct;
+      coords(pair, m0w, ct);
+      pre_issue<KIND>(raw, lane, m0w, M, ep, ct);
     }
     uint32_t tc = 0;
     for (int tile = pair; tile < num_tiles; tile += npairs, ++tc) {
       const uint32_t a = tc & 1, aph = (tc >> 1) & 1;
-      int m0w, n0;
-      coords(tile, m0w, n0);
-      const EpiPre pre = pre_finish<KIND, PD>(raw, lane, m0w, n0, M, N, ep);
-      float4 rv[8], yv[8];   // residual-update epilogue: the first chunk of the residual (and Y)
-      if constexpr (KIND == EPI_RESID) resid_begin<L::GATE>(lane, m0w, n0, M, N, ep, gate_w, rv, yv);
+      int m0w;
+      ColTile ct;
+      coords(tile, m0w, ct);
+      const int n0 = ct.col0 + group * 128;
+      const EpiPre pre = pre_finish<KIND>(raw, lane, m0w, M, ep, ct);
       const bool ok = mbar_wait_cluster(smem_u32(&ctl->tfull[a]), aph, abort, status);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
       if (tile + npairs < num_tiles) {   // the next tile's row data is in flight during this epilogue
-        int m1, n1;
-        coords(tile + npairs, m1, n1);
-        pre_issue<KIND, PD>(raw, lane, m1, n1, M, N, ep);
+        int m1;
+        ColTile c1;
+        coords(tile + npairs, m1, c1);
+        pre_issue<KIND>(raw, lane, m1, M, ep, c1);
       }
-      const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + a * BN + group * 128;
+      const uint32_t tbase = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + a * BN;
+      const uint32_t taddr = tbase + group * 128;
       const uint32_t tempty = mapa_shared(smem_u32(&ctl->tempty[a]), 0);
-      if constexpr (KIND == EPI_RESID) epi_resid<L::GATE>(taddr, tempty, lane, m0w, n0, M, N, ep, om, sl, gate_w, rv, yv);
-      else if constexpr (KIND == EPI_SOFTCAP_F32) epi_softcap(taddr, tempty, lane, m0w, n0, M, N, ep, sl, pre);
+      if constexpr (KIND == EPI_SOFTCAP_F32) epi_softcap(taddr, tempty, lane, m0w, n0, M, N, ep, sl, pre);
       else if constexpr (KIND == EPI_CE) epi_ce(taddr, tempty, lane, m0w, n0, M, N, ep, pre);
-      else if constexpr (KIND == EPI_QKV) epi_qkv<D>(taddr, tempty, lane, m0w, n0, M, N, ep, om, sl, pre);
-      else epi_bf16<KIND == EPI_RELU2_BF16>(taddr, tempty, lane, m0w, n0, M, N, ep, om, sl, pre);
+      else if constexpr (KIND == EPI_QKV) {
+        if (ct.vhead >= 0) epi_vgate<D>(tbase, tempty, lane, m0w, group, ct.vhead, ep, om, sl, pre);
+        else epi_qkv<D>(taddr, tempty, lane, m0w, n0, ct.end, M, ep, om, sl, pre);
+      } else epi_bf16<KIND == EPI_RELU2_BF16>(taddr, tempty, lane, m0w, n0, M, N, ep, om, sl, pre);
     }
     if (lane == 0) bulk_wait<0>();   // stores complete before the CTA exits
     __syncwarp();
@@ -901,8 +753,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 }
 
 template <int KIND, int D>
-cudaError_t launch_kind(const CUtensorMap& ta, const CUtensorMap& tb, const OutMaps& om, int M, int N, int K,
-                        const GemmEpi& epi, int num_sms, cudaStream_t stream) {
+cudaError_t launch_kind(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tbv, const OutMaps& om,
+                        int M, int N, int K, const GemmEpi& epi, int num_sms, cudaStream_t stream) {
   struct State {
     int max_pairs = 0;
   };
@@ -936,19 +788,16 @@ cudaError_t launch_kind(const CUtensorMap& ta, const CUtensorMap& tb, const OutM
   }, &st);
   if (init_err != cudaSuccess) return init_err;
   const int max_pairs = st->max_pairs;
-  const int tiles = ((M + PAIR_M - 1) / PAIR_M) * ((N + BN - 1) / BN);
+  const int num_m = (M + PAIR_M - 1) / PAIR_M;
+  const int tiles = num_m * num_col_tiles(KIND, N, epi.H, epi.Hkv, epi.D, epi.vgate);
   const int pairs = tiles < max_pairs ? tiles : max_pairs;
   cfg.gridDim = dim3(2 * pairs);
   // When A is the larger operand the pairs of a wave share its row block (grp = 1); otherwise
   // (the lm_head) they share a block of B (grp = every row block: on the d12 lm_head this beats
   // groups of 8 row blocks, whose B tiles are re-read 8 times as often).
-  const int num_m = (M + PAIR_M - 1) / PAIR_M;
-  int grp = M >= N ? 1 : num_m;
-  // The MLP down projection reads h, which the up projection has just written in ascending row
-  // order: walking its tiles backwards starts on the rows most likely still in L2.
-  if (KIND == EPI_RESID && K > 1024) grp = -grp;
+  const int grp = M >= N ? 1 : num_m;
   cfg.numAttrs = 2;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<KIND, D>, ta, tb, om, M, N, K, grp, epi);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<KIND, D>, ta, tb, tbv, om, M, N, K, grp, epi);
   if (e != cudaSuccess) cudaGetLastError();   // a failed launch must not resurface in a later call
   return e;
 }
@@ -957,25 +806,16 @@ cudaError_t launch_kind(const CUtensorMap& ta, const CUtensorMap& tb, const OutM
 
 cudaError_t launch_gemm(const bf16* A, const bf16* B, int M, int N, int K, const GemmEpi& epi,
                         int num_sms, cudaStream_t stream) {
-  if (M <= 0 || N <= 0 || K <= 0 || K % BK != 0 || N % 32 != 0) return cudaErrorInvalidValue;
-  CUtensorMap ta, tb;
+  const bool vgate = epi.kind == EPI_QKV && epi.vgate;
+  if (M <= 0 || N <= 0 || K <= 0 || K % BK != 0 || N % (vgate ? 16 : 32) != 0) return cudaErrorInvalidValue;
+  CUtensorMap ta, tb, tbv;
   if (!make_tmap_bf16_2d(&ta, A, K, M, static_cast<uint64_t>(K) * 2, BK, BM)) return cudaErrorInvalidValue;
   if (!make_tmap_bf16_2d(&tb, B, K, N, static_cast<uint64_t>(K) * 2, BK, B_ROWS)) return cudaErrorInvalidValue;
+  tbv = tb;
   OutMaps om;
   const uint64_t Mu = static_cast<uint64_t>(M);
   bool ok = true;
   switch (epi.kind) {
-    case EPI_RESID: {
-      if (N % SS_GROUP != 0 || epi.resid == nullptr || epi.xb == nullptr || epi.ssp_out == nullptr ||
-          epi.ncg != N / SS_GROUP || (epi.wg != nullptr && (epi.gp_out == nullptr || epi.Hkv < 1 ||
-                                                           epi.Hkv > MAX_GATE_HEADS || epi.c_g % 8 != 0)))
-        return cudaErrorInvalidValue;
-      const uint64_t ld4 = static_cast<uint64_t>(N) * 4;
-      if (epi.x_out) ok = make_tmap_2d(&om.o0, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, epi.x_out, N, Mu, ld4, 32, 32);
-      if (ok && epi.xm_out) ok = make_tmap_2d(&om.o1, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, epi.xm_out, N, Mu, ld4, 32, 32);
-      if (ok) ok = make_tmap_bf16_2d(&om.o2, epi.xb, N, Mu, static_cast<uint64_t>(N) * 2, 64, 32);
-      break;
-    }
     case EPI_CE:
       ok = epi.targets != nullptr && epi.ce_part != nullptr && epi.ce_zt != nullptr && epi.cap > 0.f;
       break;
@@ -990,28 +830,30 @@ cudaError_t launch_gemm(const bf16* A, const bf16* B, int M, int N, int K, const
       break;
     case EPI_QKV: {
       const uint64_t qc = static_cast<uint64_t>(epi.H) * epi.D, kc = static_cast<uint64_t>(epi.Hkv) * epi.D;
-      if (epi.rope == nullptr || epi.rope_ld < 1 || (epi.gp_in != nullptr && (epi.ve == nullptr || epi.tokens == nullptr)))
+      if (epi.rope == nullptr || epi.rope_ld < 1 || (epi.D != 64 && epi.D != 128)) return cudaErrorInvalidValue;
+      if (vgate && (epi.ve == nullptr || epi.tokens == nullptr ||
+                    N != static_cast<int>(qc + kc) + epi.Hkv * (epi.D + VGATE_ROWS)))
         return cudaErrorInvalidValue;
+      if (!vgate && N != static_cast<int>(qc + 2 * kc)) return cudaErrorInvalidValue;
       ok = make_tmap_bf16_2d(&om.o0, epi.q, qc, Mu, qc * 2, 64, 32) &&
            make_tmap_bf16_2d(&om.o1, epi.k, kc, Mu, kc * 2, 64, 32) &&
            make_tmap_bf16_2d(&om.o2, epi.v, kc, Mu, kc * 2, 64, 32);
+      // a value-embedding head's tile: D + VGATE_ROWS rows of B, half per CTA
+      if (ok && vgate)
+        ok = make_tmap_bf16_2d(&tbv, B, K, N, static_cast<uint64_t>(K) * 2, BK, (epi.D + VGATE_ROWS) / 2);
       break;
     }
     default: return cudaErrorInvalidValue;
   }
   if (!ok) return cudaErrorInvalidValue;
   switch (epi.kind) {
-    case EPI_BF16: return launch_kind<EPI_BF16, 0>(ta, tb, om, M, N, K, epi, num_sms, stream);
-    case EPI_RESID:
-      if (epi.wg != nullptr) return launch_kind<EPI_RESID, RESID_GATE>(ta, tb, om, M, N, K, epi, num_sms, stream);
-      return launch_kind<EPI_RESID, 0>(ta, tb, om, M, N, K, epi, num_sms, stream);
-    case EPI_RELU2_BF16: return launch_kind<EPI_RELU2_BF16, 0>(ta, tb, om, M, N, K, epi, num_sms, stream);
-    case EPI_SOFTCAP_F32: return launch_kind<EPI_SOFTCAP_F32, 0>(ta, tb, om, M, N, K, epi, num_sms, stream);
-    case EPI_CE: return launch_kind<EPI_CE, 0>(ta, tb, om, M, N, K, epi, num_sms, stream);
+    case EPI_BF16: return launch_kind<EPI_BF16, 0>(ta, tb, tbv, om, M, N, K, epi, num_sms, stream);
+    case EPI_RELU2_BF16: return launch_kind<EPI_RELU2_BF16, 0>(ta, tb, tbv, om, M, N, K, epi, num_sms, stream);
+    case EPI_SOFTCAP_F32: return launch_kind<EPI_SOFTCAP_F32, 0>(ta, tb, tbv, om, M, N, K, epi, num_sms, stream);
+    case EPI_CE: return launch_kind<EPI_CE, 0>(ta, tb, tbv, om, M, N, K, epi, num_sms, stream);
     case EPI_QKV:
-      if (epi.D == 128) return launch_kind<EPI_QKV, 128>(ta, tb, om, M, N, K, epi, num_sms, stream);
-      if (epi.D == 64) return launch_kind<EPI_QKV, 64>(ta, tb, om, M, N, K, epi, num_sms, stream);
-      return cudaErrorInvalidValue;
+      if (epi.D == 128) return launch_kind<EPI_QKV, 128>(ta, tb, tbv, om, M, N, K, epi, num_sms, stream);
+      return launch_kind<EPI_QKV, 64>(ta, tb, tbv, om, M, N, K, epi, num_sms, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -26,6 +26,11 @@ enum EpiKind : int {
 // Columns covered by one partial sum of squares (one epilogue thread's share of a row).
 constexpr int SS_GROUP = 128;
 
+// Rows that follow each kv head's v rows in a value-embedding layer's packed q|k|v weight: the
+// head's gate row, then zero rows (the MMA's N must be a multiple of 16), so that the head's
+// GEMM tile, D + VGATE_ROWS columns wide, also yields the gate's pre-activation.
+constexpr int VGATE_ROWS = 16;
+
 struct GemmEpi {
   int kind = EPI_BF16;
   int* status = nullptr;
@@ -42,11 +47,10 @@ struct GemmEpi {
   int ldo = 0;
   float cap = 15.f;
 
-  // EPI_RESID (N = ncols of the stream, N % 128 == 0):
+  // EPI_RESID (launch_gemm_resid; N = ncols of the stream, N % 128 == 0):
   //   xr = resid + acc;  xm_out <- xr (if set);  x' = a * xr + b * Y (Y may be null);
   //   x_out <- x' (if set, may alias resid);  xb <- bf16(x');
-  //   ssp_out[m, g] = sum of x'^2 over columns [128 g, 128 g + 128);
-  //   if wg: gp_out[m, h, g] = sum over those columns c < c_g of x'[c] * wg[h, c], h < Hkv.
+  //   ssp_out[m, g] = sum of x'^2 over columns [128 g, 128 g + 128).
   const float* resid = nullptr;
   float a = 1.f, b = 0.f;
   const float* Y = nullptr;
@@ -54,9 +58,6 @@ struct GemmEpi {
   float* xm_out = nullptr;
   bf16* xb = nullptr;
   float* ssp_out = nullptr;
-  const bf16* wg = nullptr;
-  int c_g = 0;
-  float* gp_out = nullptr;
 
   // EPI_QKV
   bf16* q = nullptr;
@@ -65,7 +66,10 @@ struct GemmEpi {
   int H = 0, Hkv = 0, D = 0, T = 1;
   int rope_ld = 0;                // row length (positions) of the rotary table
   const float2* rope = nullptr;   // [D/2][rope_ld] (cos, sin), position fastest
-  const float* gp_in = nullptr;   // [M, Hkv, ncg] gate pre-activation partials, or null (no VE)
+  // vgate != 0 (a value-embedding layer): B holds the q and k rows, then for each kv head its D v
+  // rows followed by its gate row and VGATE_ROWS - 1 zero rows; v += gate * ve[token] with
+  // gate = gate_scale * sigmoid(rs * (x . gate row)).
+  int vgate = 0;
   float gate_scale = 1.f;
   const bf16* ve = nullptr;       // [V, Hkv*D]
   const int32_t* tokens = nullptr;
@@ -80,8 +84,6 @@ struct GemmEpi {
   float* ce_zt = nullptr;
 };
 
-// Largest number of kv heads whose value-embedding gate partials one epilogue thread keeps.
-constexpr int MAX_GATE_HEADS = 16;
 
 // Records `e` as the calling thread's last CUDA error (read by nc_last_cuda_error) and maps it
 // to a status: NC_OK for cudaSuccess, NC_ERR_CUDA otherwise.
@@ -121,10 +123,12 @@ inline cudaLaunchAttribute pdl_attribute() {
   return a;
 }
 
-// Encodes a 2-D TMA descriptor with 128-byte swizzling through the driver entry point
-// (no link-time libcuda).  inner/outer are extents in elements, row stride in bytes.
+// Encodes a 2-D TMA descriptor through the driver entry point (no link-time libcuda), with
+// 128-byte swizzling unless swizzle128 is false (then the box is a dense row-major array in shared
+// memory).  inner/outer are extents in elements, row stride in bytes.
 bool make_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* ptr, uint64_t inner,
-                  uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer);
+                  uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer,
+                  bool swizzle128 = true);
 
 inline bool make_tmap_bf16_2d(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer,
                               uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer) {
@@ -137,12 +141,17 @@ inline bool make_tmap_bf16_2d(CUtensorMap* map, const void* ptr, uint64_t inner,
 cudaError_t launch_gemm(const bf16* A, const bf16* B, int M, int N, int K, const GemmEpi& epi,
                         int num_sms, cudaStream_t stream);
 
-// x0 = smear(wte[tokens]); x = a * x0; xb = bf16(x); ssp[m, g] = sum of x^2 over column group g;
-// if wg: gp[m, h, g] = sum over group g columns c < c_g of x[c] * wg[h, c].
+// Residual-stream update of an output projection (EPI_RESID fields of `epi`), computed as the
+// transposed product W . A^T so that the epilogue's loads and stores of the stream are coalesced
+// from registers: xr = resid + A[M, K] . W[N, K]^T, then the updates listed at GemmEpi.
+// Requires K % 64 == 0, N % 128 == 0, 16-byte aligned rows of A and W.
+cudaError_t launch_gemm_resid(const bf16* A, const bf16* W, int M, int N, int K, const GemmEpi& epi,
+                              int num_sms, cudaStream_t stream);
+
+// x0 = smear(wte[tokens]); x = a * x0; xb = bf16(x); ssp[m, g] = sum of x^2 over column group g.
 cudaError_t launch_embed_smear(const int32_t* tokens, int B, int T, const bf16* wte, int V, int C,
                                const bf16* smear_gate, int c_s, int embed_norm, float eps, float a,
-                               float* x0, float* x, bf16* xb, float* ssp, const bf16* wg, int Hkv,
-                               int c_g, float* gp, int* status, cudaStream_t stream);
+                               float* x0, float* x, bf16* xb, float* ssp, int* status, cudaStream_t stream);
 
 // table[i][t] = (cos, sin)(t * base^(-2i/D)), i < D/2, t < T (position fastest).
 cudaError_t launch_rope_table(float2* table, int T, int D, float base, cudaStream_t stream);

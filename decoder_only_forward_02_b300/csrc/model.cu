@@ -6,15 +6,16 @@
 // norm is split: the kernel that writes the residual stream also writes its bf16 copy and
 // per-row partial sums of squares, and the GEMM that consumes it scales its accumulator rows
 // by 1 / rms.
-//   embed: x0 = smear(wte[tok]); x = (lr_0 + l0_0) x0 (+ bf16 copy, partial sums, VE gate partials)
+//   embed: x0 = smear(wte[tok]); x = (lr_0 + l0_0) x0 (+ bf16 copy, partial sums)
 //   per layer i:
-//     QKV GEMM  (row scale, RoPE, QK-norm, v += gate * ve)
+//     QKV GEMM  (row scale, RoPE, QK-norm; on VE layers the gate rows packed after each kv head's
+//               v rows give the gate, and v += gate * ve)
 //     attention
 //     out-proj GEMM: x += y Wo^T (+ bf16 copy, partial sums)
 //     fc GEMM   (row scale, ReLU^2)
 //     proj GEMM: x += h Wproj^T; after layer L/2-1 that result is also the backout cache;
-//                then x = lr_{i+1} x + l0_{i+1} x0 for the next block (+ its VE gate partials),
-//                or after the last layer x - lb * x_mid (final norm's input)
+//                then x = lr_{i+1} x + l0_{i+1} x0 for the next block, or after the last layer
+//                x - lb * x_mid (final norm's input)
 //   lm_head GEMM (row scale, soft-cap)
 #include "decode.h"
 #include "internal.h"
@@ -61,7 +62,8 @@ nc_status cuda_status(cudaError_t e) {
 const char* last_cuda_error_name() { return cudaGetErrorName(g_last_cuda_error); }
 
 bool make_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* ptr, uint64_t inner,
-                  uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer) {
+                  uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer,
+                  bool swizzle128) {
   auto fn = get_encode_fn();
   if (fn == nullptr) return false;
   cuuint64_t dims[2] = {inner, outer};
@@ -69,7 +71,8 @@ bool make_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* ptr, 
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(map, dtype, 2, const_cast<void*>(ptr), dims, strides, box,
-                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -90,8 +93,10 @@ struct TimedLaunch {
 };
 
 struct Layout {
-  size_t x0, x, xm, xb, q, k, v, y, h, ssp, gp, end;
+  size_t x0, x, xm, xb, q, k, v, y, h, ssp, end;
 };
+
+using nc::VGATE_ROWS;
 
 }  // namespace
 
@@ -104,8 +109,9 @@ struct nc_model {
   const bf16* wte = nullptr;
   const bf16* smear = nullptr;
   const bf16* lm = nullptr;
-  std::vector<const bf16*> wo, wfc, wproj, ve, veg;
-  bf16* wqkv = nullptr;     // packed [L][(H+2Hkv)*D][C]
+  std::vector<const bf16*> wo, wfc, wproj, ve;
+  bf16* wqkv = nullptr;     // packed per layer: [q rows | k rows | v rows (+ gate rows on VE layers)][C]
+  std::vector<size_t> qkv_off;   // element offset of each layer's packed weight
   float2* rope = nullptr;   // [seq_len_ctx][D/2]
   int* status = nullptr;    // device status word
   int device = 0;           // the device current at creation (where packed_buf lives)
@@ -117,8 +123,10 @@ struct nc_model {
   int acc_n[NC_K_COUNT] = {};
 
   int C() const { return cfg.n_embd; }
-  int Nqkv() const { return (cfg.n_head + 2 * cfg.n_kv_head) * cfg.head_dim; }
-  size_t qkv_layer_elems() const { return static_cast<size_t>(Nqkv()) * C(); }
+  // rows of layer i's packed q|k|v weight
+  int Nqkv(int i) const {
+    return (cfg.n_head + 2 * cfg.n_kv_head) * cfg.head_dim + (has_ve[i] ? cfg.n_kv_head * VGATE_ROWS : 0);
+  }
 };
 
 namespace {
@@ -138,17 +146,16 @@ nc_status validate_config(const nc_config* c) {
   if (c->n_embd % 128 != 0 || c->n_embd > 2048) return NC_ERR_UNSUPPORTED;
   if (c->mlp_hidden % 64 != 0 || c->vocab_size % 64 != 0) return NC_ERR_UNSUPPORTED;
   if (c->smear_gate_channels % 4 != 0 || c->ve_gate_channels % 8 != 0) return NC_ERR_UNSUPPORTED;
-  for (int i = 0; i < c->n_layer; ++i)
-    if (c->has_ve[i] && c->n_kv_head > nc::MAX_GATE_HEADS) return NC_ERR_UNSUPPORTED;
   return NC_OK;
 }
 
 size_t packed_bytes_for(const nc_config* c) {
   const size_t status = ALIGN;
   const size_t rope = align_up(static_cast<size_t>(c->seq_len_ctx) * (c->head_dim / 2) * sizeof(float2));
-  const size_t qkv = static_cast<size_t>(c->n_layer) * (c->n_head + 2 * c->n_kv_head) * c->head_dim *
-                     c->n_embd * sizeof(bf16);
-  return status + rope + align_up(qkv);
+  size_t rows = 0;
+  for (int i = 0; i < c->n_layer; ++i)
+    rows += (c->n_head + 2 * c->n_kv_head) * c->head_dim + (c->has_ve[i] ? c->n_kv_head * VGATE_ROWS : 0);
+  return status + rope + align_up(rows * c->n_embd * sizeof(bf16));
 }
 
 Layout layout_for(const nc_model* m, int B, int T) {
@@ -171,7 +178,6 @@ Layout layout_for(const nc_model* m, int B, int T) {
   L.y = take(M * c.n_head * c.head_dim * 2);
   L.h = take(M * c.mlp_hidden * 2);
   L.ssp = take(M * (c.n_embd / nc::SS_GROUP) * 4);
-  L.gp = take(M * c.n_kv_head * (c.n_embd / nc::SS_GROUP) * 4);
   L.end = off;
   return L;
 }
@@ -268,7 +274,7 @@ nc_status nc_model_create(const nc_config* cfg, const nc_weights* w, void* packe
       if (p == nullptr || !aligned(p, 16)) return NC_ERR_INVALID_ARG;
     if (cfg->has_ve[i]) {
       if (w->ve_table == nullptr || w->ve_gate == nullptr || w->ve_table[i] == nullptr ||
-          w->ve_gate[i] == nullptr || !aligned(w->ve_table[i], 16) || !aligned(w->ve_gate[i], 16))
+          w->ve_gate[i] == nullptr || !aligned(w->ve_table[i], 16) || !aligned(w->ve_gate[i], 2))
         return NC_ERR_INVALID_ARG;
     }
   }
@@ -293,7 +299,6 @@ nc_status nc_model_create(const nc_config* cfg, const nc_weights* w, void* packe
     m->wfc.push_back(static_cast<const bf16*>(w->wfc[i]));
     m->wproj.push_back(static_cast<const bf16*>(w->wproj[i]));
     m->ve.push_back(cfg->has_ve[i] ? static_cast<const bf16*>(w->ve_table[i]) : nullptr);
-    m->veg.push_back(cfg->has_ve[i] ? static_cast<const bf16*>(w->ve_gate[i]) : nullptr);
   }
   uint8_t* base = static_cast<uint8_t*>(packed_buf);
   m->status = reinterpret_cast<int*>(base);
@@ -306,15 +311,36 @@ nc_status nc_model_create(const nc_config* cfg, const nc_weights* w, void* packe
   cudaError_t e = cudaGetDevice(&dev);
   m->device = dev;
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&m->num_sms, cudaDevAttrMultiProcessorCount, dev);
-  const size_t C = cfg->n_embd, qd = static_cast<size_t>(cfg->n_head) * cfg->head_dim,
-               kd = static_cast<size_t>(cfg->n_kv_head) * cfg->head_dim;
+  const size_t C = cfg->n_embd, D = cfg->head_dim, qd = static_cast<size_t>(cfg->n_head) * D,
+               kd = static_cast<size_t>(cfg->n_kv_head) * D;
+  const size_t c_g = cfg->ve_gate_channels ? cfg->ve_gate_channels : C;
+  size_t off = 0;
+  for (int i = 0; i < L; ++i) {
+    m->qkv_off.push_back(off);
+    off += static_cast<size_t>(m->Nqkv(i)) * C;
+  }
   for (int i = 0; i < L && e == cudaSuccess; ++i) {
-    bf16* dst = m->wqkv + static_cast<size_t>(i) * m->qkv_layer_elems();
+    bf16* dst = m->wqkv + m->qkv_off[i];
     e = cudaMemcpyAsync(dst, w->wq[i], qd * C * 2, cudaMemcpyDeviceToDevice, stream);
     if (e == cudaSuccess)
       e = cudaMemcpyAsync(dst + qd * C, w->wk[i], kd * C * 2, cudaMemcpyDeviceToDevice, stream);
-    if (e == cudaSuccess)
-      e = cudaMemcpyAsync(dst + (qd + kd) * C, w->wv[i], kd * C * 2, cudaMemcpyDeviceToDevice, stream);
+    if (e != cudaSuccess) break;
+    bf16* v0 = dst + (qd + kd) * C;
+    if (!cfg->has_ve[i]) {
+      e = cudaMemcpyAsync(v0, w->wv[i], kd * C * 2, cudaMemcpyDeviceToDevice, stream);
+      continue;
+    }
+    // per kv head g: its D v rows, its gate row (the first c_g columns, zeros after), 15 zero rows
+    const size_t head_rows = D + VGATE_ROWS;
+    e = cudaMemsetAsync(v0, 0, static_cast<size_t>(cfg->n_kv_head) * head_rows * C * 2, stream);
+    for (int g = 0; g < cfg->n_kv_head && e == cudaSuccess; ++g) {
+      bf16* hd = v0 + g * head_rows * C;
+      e = cudaMemcpyAsync(hd, static_cast<const bf16*>(w->wv[i]) + g * D * C, D * C * 2, cudaMemcpyDeviceToDevice,
+                          stream);
+      if (e == cudaSuccess)
+        e = cudaMemcpyAsync(hd + D * C, static_cast<const bf16*>(w->ve_gate[i]) + g * c_g, c_g * 2,
+                            cudaMemcpyDeviceToDevice, stream);
+    }
   }
   if (e == cudaSuccess) e = cudaMemsetAsync(m->status, 0, sizeof(int), stream);
   if (e == cudaSuccess)
@@ -432,9 +458,7 @@ cudaError_t run_blocks(nc_model* m, const int32_t* tokens, int B, int T, const L
   bf16* y = reinterpret_cast<bf16*>(ws + Lo.y);
   bf16* h = reinterpret_cast<bf16*>(ws + Lo.h);
   float* ssp = reinterpret_cast<float*>(ws + Lo.ssp);
-  float* gp = reinterpret_cast<float*>(ws + Lo.gp);
   const int c_s = c.smear_gate_channels ? c.smear_gate_channels : C;
-  const int c_g = c.ve_gate_channels ? c.ve_gate_channels : C;
   const int mid = L / 2 - 1;
   uint8_t* kv_next = kv != nullptr ? kv->cache : nullptr;   // the current layer's keys, then values
 
@@ -450,10 +474,8 @@ cudaError_t run_blocks(nc_model* m, const int32_t* tokens, int B, int T, const L
   };
 
   cudaError_t e = timed(m, NC_K_EMBED, stream, [&] {
-    const bool ve0 = m->has_ve[0] != 0;
     return nc::launch_embed_smear(tokens, B, T, m->wte, V, C, m->smear, c_s, c.embed_norm, c.rms_eps,
-                                  m->lr[0] + m->l0[0], x0, x, xb, ssp, ve0 ? m->veg[0] : nullptr, Hkv, c_g,
-                                  ve0 ? gp : nullptr, m->status, stream);
+                                  m->lr[0] + m->l0[0], x0, x, xb, ssp, m->status, stream);
   });
   for (int i = 0; i < L && e == cudaSuccess; ++i) {
     const bool ve = m->has_ve[i] != 0;
@@ -470,14 +492,13 @@ cudaError_t run_blocks(nc_model* m, const int32_t* tokens, int B, int T, const L
     qe.rope = m->rope;
     qe.rope_ld = c.seq_len_ctx;
     if (kv != nullptr && kv->decode) qe.rope = m->rope + (kv->pos - 1);   // row pair at positions pos-1, pos
-    qe.gp_in = ve ? gp : nullptr;
+    qe.vgate = ve ? 1 : 0;
     qe.gate_scale = c.ve_gate_scale;
     qe.ve = m->ve[i];
     qe.tokens = tokens;
     qe.V = V;
     e = timed(m, NC_K_QKV, stream, [&] {
-      return nc::launch_gemm(xb, m->wqkv + static_cast<size_t>(i) * m->qkv_layer_elems(), M, m->Nqkv(), C,
-                             qe, m->num_sms, stream);
+      return nc::launch_gemm(xb, m->wqkv + m->qkv_off[i], M, m->Nqkv(i), C, qe, m->num_sms, stream);
     });
     if (e != cudaSuccess) break;
     if (kv != nullptr) {
@@ -506,7 +527,7 @@ cudaError_t run_blocks(nc_model* m, const int32_t* tokens, int B, int T, const L
     if (e != cudaSuccess) break;
     nc::GemmEpi oe;
     resid(oe);
-    e = timed(m, NC_K_OPROJ, stream, [&] { return nc::launch_gemm(y, m->wo[i], M, C, H * D, oe, m->num_sms, stream); });
+    e = timed(m, NC_K_OPROJ, stream, [&] { return nc::launch_gemm_resid(y, m->wo[i], M, C, H * D, oe, m->num_sms, stream); });
     if (e != cudaSuccess) break;
     nc::GemmEpi fe;
     set_consumer(fe, m, ssp);
@@ -518,16 +539,10 @@ cudaError_t run_blocks(nc_model* m, const int32_t* tokens, int B, int T, const L
     nc::GemmEpi pe;
     resid(pe);
     if (c.use_backout && i == mid) pe.xm_out = xm;
-    if (i + 1 < L) {   // the next block's residual mix and, on a VE layer, its gate partials
+    if (i + 1 < L) {   // the next block's residual mix
       pe.a = m->lr[i + 1];
       pe.b = m->l0[i + 1];
       pe.Y = x0;
-      if (m->has_ve[i + 1]) {
-        pe.wg = m->veg[i + 1];
-        pe.Hkv = Hkv;
-        pe.c_g = c_g;
-        pe.gp_out = gp;
-      }
     } else {           // final: backout, then only the lm_head's inputs are needed
       pe.x_out = nullptr;
       if (c.use_backout) {
@@ -536,7 +551,7 @@ cudaError_t run_blocks(nc_model* m, const int32_t* tokens, int B, int T, const L
         pe.Y = mid < 0 ? x0 : xm;
       }
     }
-    e = timed(m, NC_K_PROJ, stream, [&] { return nc::launch_gemm(h, m->wproj[i], M, C, F, pe, m->num_sms, stream); });
+    e = timed(m, NC_K_PROJ, stream, [&] { return nc::launch_gemm_resid(h, m->wproj[i], M, C, F, pe, m->num_sms, stream); });
   }
   return e;
 }

@@ -13,6 +13,7 @@ int device_sms() {
 inline bool al(const void* p, size_t a) { return p != nullptr && reinterpret_cast<uintptr_t>(p) % a == 0; }
 inline bool al_or_null(const void* p, size_t a) { return p == nullptr || reinterpret_cast<uintptr_t>(p) % a == 0; }
 using nc::cuda_status;
+static_assert(NC_QKV_GATE_ROWS == nc::VGATE_ROWS, "packed gate rows of the public header and the kernels");
 
 }  // namespace
 
@@ -49,13 +50,11 @@ nc_status nc_op_gemm(const void* A, const void* B, int M, int N, int K, nc_epilo
 
 nc_status nc_op_gemm_residual(const void* A, const void* B, int M, int N, int K, const float* resid, float a,
                               float b, const float* Y, float* x_out, float* xm_out, void* xb, float* ssp,
-                              const void* wg, int Hkv, int c_g, float* gp, int* status, void* stream) {
-  if (!al(A, 16) || !al(B, 16) || !al(resid, 16) || !al(xb, 16) || !al(ssp, 4) || M < 1 || N < 1 || K < 1)
+                              int* status, void* stream) {
+  if (!al(A, 16) || !al(B, 16) || !al(resid, 4) || !al(xb, 2) || !al(ssp, 4) || M < 1 || N < 1 || K < 1)
     return NC_ERR_INVALID_ARG;
-  if (!al_or_null(Y, 16) || !al_or_null(x_out, 16) || !al_or_null(xm_out, 16)) return NC_ERR_INVALID_ARG;
-  if (wg != nullptr && (!al(wg, 16) || !al(gp, 4) || Hkv < 1 || c_g < 8 || c_g > N)) return NC_ERR_INVALID_ARG;
+  if (!al_or_null(Y, 4) || !al_or_null(x_out, 4) || !al_or_null(xm_out, 4)) return NC_ERR_INVALID_ARG;
   if (K % 64 != 0 || N % nc::SS_GROUP != 0) return NC_ERR_UNSUPPORTED;
-  if (wg != nullptr && (Hkv > nc::MAX_GATE_HEADS || c_g % 8 != 0)) return NC_ERR_UNSUPPORTED;
   nc::GemmEpi e;
   e.kind = nc::EPI_RESID;
   e.status = status;
@@ -68,23 +67,17 @@ nc_status nc_op_gemm_residual(const void* A, const void* B, int M, int N, int K,
   e.xb = static_cast<nc::bf16*>(xb);
   e.ssp_out = ssp;
   e.ncg = N / nc::SS_GROUP;
-  if (wg != nullptr) {
-    e.wg = static_cast<const nc::bf16*>(wg);
-    e.Hkv = Hkv;
-    e.c_g = c_g;
-    e.gp_out = gp;
-  }
-  return cuda_status(nc::launch_gemm(static_cast<const nc::bf16*>(A), static_cast<const nc::bf16*>(B), M, N, K,
-                                     e, device_sms(), static_cast<cudaStream_t>(stream)));
+  return cuda_status(nc::launch_gemm_resid(static_cast<const nc::bf16*>(A), static_cast<const nc::bf16*>(B), M, N,
+                                           K, e, device_sms(), static_cast<cudaStream_t>(stream)));
 }
 
 nc_status nc_op_qkv(const void* xb, const void* wqkv, int M, int T, int C, int H, int Hkv, int D, const float* rope,
-                    int rope_ld, float eps, const float* ssp, const float* gp, float gate_scale, const void* ve,
+                    int rope_ld, float eps, const float* ssp, int vgate, float gate_scale, const void* ve,
                     const int32_t* tokens, int V, void* q, void* k, void* v, int* status, void* stream) {
   if (!al(xb, 16) || !al(wqkv, 16) || !al(rope, 16) || !al(q, 16) || !al(k, 16) || !al(v, 16) || !al(ssp, 4) ||
       M < 1 || T < 1 || C < 1 || H < 1 || Hkv < 1 || H % Hkv != 0 || rope_ld < T)
     return NC_ERR_INVALID_ARG;
-  if (gp != nullptr && (!al(gp, 4) || !al(ve, 16) || tokens == nullptr || V < 1)) return NC_ERR_INVALID_ARG;
+  if (vgate && (!al(ve, 16) || tokens == nullptr || V < 1)) return NC_ERR_INVALID_ARG;
   if ((D != 64 && D != 128) || C % nc::SS_GROUP != 0) return NC_ERR_UNSUPPORTED;
   nc::GemmEpi e;
   e.kind = nc::EPI_QKV;
@@ -102,13 +95,14 @@ nc_status nc_op_qkv(const void* xb, const void* wqkv, int M, int T, int C, int H
   e.T = T;
   e.rope = reinterpret_cast<const float2*>(rope);
   e.rope_ld = rope_ld;
-  e.gp_in = gp;
+  e.vgate = vgate ? 1 : 0;
   e.gate_scale = gate_scale;
   e.ve = static_cast<const nc::bf16*>(ve);
   e.tokens = tokens;
   e.V = V;
-  return cuda_status(nc::launch_gemm(static_cast<const nc::bf16*>(xb), static_cast<const nc::bf16*>(wqkv), M,
-                                     (H + 2 * Hkv) * D, C, e, device_sms(), static_cast<cudaStream_t>(stream)));
+  const int N = (H + 2 * Hkv) * D + (vgate ? Hkv * nc::VGATE_ROWS : 0);
+  return cuda_status(nc::launch_gemm(static_cast<const nc::bf16*>(xb), static_cast<const nc::bf16*>(wqkv), M, N, C,
+                                     e, device_sms(), static_cast<cudaStream_t>(stream)));
 }
 
 nc_status nc_op_rope_table(float* rope, int T, int D, float base, void* stream) {
@@ -130,19 +124,16 @@ nc_status nc_op_attention(const void* q, const void* k, const void* v, int B, in
 
 nc_status nc_op_embed_smear(const int32_t* tokens, int B, int T, const void* wte, int V, int C,
                             const void* smear_gate, int c_s, int embed_norm, float eps, float a, float* x0, float* x,
-                            void* xb, float* ssp, const void* wg, int Hkv, int c_g, float* gp, int* status,
-                            void* stream) {
+                            void* xb, float* ssp, int* status, void* stream) {
   if (tokens == nullptr || !al(wte, 16) || !al(x0, 16) || !al(x, 16) || !al(xb, 16) || !al(ssp, 4) || B < 1 ||
       T < 1 || V < 1 || C < 1)
     return NC_ERR_INVALID_ARG;
   if (smear_gate != nullptr && (!al(smear_gate, 8) || c_s < 4 || c_s > C)) return NC_ERR_INVALID_ARG;
-  if (wg != nullptr && (!al(wg, 8) || !al(gp, 4) || Hkv < 1 || c_g < 4 || c_g > C)) return NC_ERR_INVALID_ARG;
-  if (C % 128 != 0 || C > 2048 || (smear_gate != nullptr && c_s % 4 != 0) || (wg != nullptr && c_g % 4 != 0))
-    return NC_ERR_UNSUPPORTED;
+  if (C % 128 != 0 || C > 2048 || (smear_gate != nullptr && c_s % 4 != 0)) return NC_ERR_UNSUPPORTED;
   return cuda_status(nc::launch_embed_smear(tokens, B, T, static_cast<const nc::bf16*>(wte), V, C,
                                             static_cast<const nc::bf16*>(smear_gate), c_s, embed_norm, eps, a, x0,
-                                            x, static_cast<nc::bf16*>(xb), ssp, static_cast<const nc::bf16*>(wg),
-                                            Hkv, c_g, gp, status, static_cast<cudaStream_t>(stream)));
+                                            x, static_cast<nc::bf16*>(xb), ssp, status,
+                                            static_cast<cudaStream_t>(stream)));
 }
 
 nc_status nc_op_lmhead_ce(const void* xf, const void* wlm, int M, int V, int C, const float* ssp, float eps,

@@ -10,7 +10,7 @@
 // Definitions ("Nanochat在nanoGPT之上的新增功能", section 1 table and notes): smear adds
 // sigmoid(gate(x)) times the previous token's embedding; blocks rescale the residual stream by
 // resid_lambdas and add x0_lambdas * x0 (for the first block x = x0, so x = (l_r + l_0) x0);
-// RMSNorm has no learned weight, and the value-embedding gate reads the normalised block input.
+// RMSNorm has no learned weight.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -63,8 +63,7 @@ __global__ void __launch_bounds__(32 * ROWS_PER_BLOCK)
     embed_smear_kernel(const int32_t* __restrict__ tokens, int M, int T, const bf16* __restrict__ wte,
                        int V, const bf16* __restrict__ smear_gate, int c_s, int embed_norm, float eps,
                        float a, float* __restrict__ x0, float* __restrict__ x, bf16* __restrict__ xb,
-                       float* __restrict__ ssp, const bf16* __restrict__ wg, int Hkv, int c_g,
-                       float* __restrict__ gp, int* status) {
+                       float* __restrict__ ssp, int* status) {
   constexpr int C = NV4 * 128;
   griddep_wait();   // the previous kernel on the stream (still reading xb, ssp, ...) has completed
   griddep_launch();
@@ -103,13 +102,6 @@ __global__ void __launch_bounds__(32 * ROWS_PER_BLOCK)
     st_bf16x4(xb + base + i * 128 + lane * 4, v);
     const float s = warp_sum(dot4(v, v));
     if (lane == 0) ssp[static_cast<size_t>(row) * NV4 + i] = s;
-    if (wg != nullptr) {
-      const int c = i * 128 + lane * 4;
-      for (int h = 0; h < Hkv; ++h) {
-        const float d = warp_sum(c < c_g ? dot4(v, ld_bf16x4(wg + static_cast<size_t>(h) * c_g + c)) : 0.f);
-        if (lane == 0) gp[(static_cast<size_t>(row) * Hkv + h) * NV4 + i] = d;
-      }
-    }
   }
 }
 
@@ -140,8 +132,7 @@ template <int NV4>
 struct EmbedLaunch {
   static cudaError_t run(const int32_t* tokens, int M, int T, const bf16* wte, int V,
                          const bf16* smear_gate, int c_s, int embed_norm, float eps, float a, float* x0,
-                         float* x, bf16* xb, float* ssp, const bf16* wg, int Hkv, int c_g, float* gp,
-                         int* status, cudaStream_t stream) {
+                         float* x, bf16* xb, float* ssp, int* status, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1] = {pdl_attribute()};
     cfg.gridDim = dim3((M + ROWS_PER_BLOCK - 1) / ROWS_PER_BLOCK);
@@ -150,7 +141,7 @@ struct EmbedLaunch {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     const cudaError_t e = cudaLaunchKernelEx(&cfg, embed_smear_kernel<NV4>, tokens, M, T, wte, V, smear_gate, c_s,
-                                             embed_norm, eps, a, x0, x, xb, ssp, wg, Hkv, c_g, gp, status);
+                                             embed_norm, eps, a, x0, x, xb, ssp, status);
     if (e != cudaSuccess) cudaGetLastError();
     return e;
   }
@@ -160,12 +151,10 @@ struct EmbedLaunch {
 
 cudaError_t launch_embed_smear(const int32_t* tokens, int B, int T, const bf16* wte, int V, int C,
                                const bf16* smear_gate, int c_s, int embed_norm, float eps, float a,
-                               float* x0, float* x, bf16* xb, float* ssp, const bf16* wg, int Hkv,
-                               int c_g, float* gp, int* status, cudaStream_t stream) {
-  if (C % 128 != 0 || c_s % 4 != 0 || (wg != nullptr && (c_g % 4 != 0 || gp == nullptr)))
-    return cudaErrorInvalidValue;
+                               float* x0, float* x, bf16* xb, float* ssp, int* status, cudaStream_t stream) {
+  if (C % 128 != 0 || c_s % 4 != 0) return cudaErrorInvalidValue;
   return dispatch_nv4<EmbedLaunch>(C, tokens, B * T, T, wte, V, smear_gate, c_s, embed_norm, eps, a, x0,
-                                   x, xb, ssp, wg, Hkv, c_g, gp, status, stream);
+                                   x, xb, ssp, status, stream);
 }
 
 cudaError_t launch_rope_table(float2* table, int T, int D, float base, cudaStream_t stream) {

@@ -37,7 +37,9 @@
  *    row is unchanged.  The smeared embedding is x0.
  *  - Value-embedding gate: ve_gate_scale * sigmoid(a_t[:c_g] . ve_gate[g])
  *    per token and kv head g, a_t the block's normalised input;
- *    v <- v + gate * ve_table[token].
+ *    v <- v + gate * ve_table[token].  The product a_t . ve_gate[g] runs on
+ *    the tensor cores with the q|k|v projection, from the same bf16 copy of
+ *    the block input as q, k and v.
  *  - x <- resid_lambdas[i] * x + x0_lambdas[i] * x0 at the start of block i.
  *  - Backout caches x after block n_layer/2 - 1 (x0 when n_layer == 1).
  *
@@ -114,7 +116,7 @@ typedef struct {
   const void *const *wfc;             /* [F, C] */
   const void *const *wproj;           /* [C, F] */
   const void *const *ve_table;        /* [V, Hkv*D] */
-  const void *const *ve_gate;         /* [Hkv, c_g], 16-byte aligned */
+  const void *const *ve_gate;         /* [Hkv, c_g] */
   const void *smear_gate;             /* [c_s]; unused if !use_smear */
   const void *lm_head;                /* [V, C] */
   const float *resid_lambdas;         /* host [n_layer], copied */

@@ -39,26 +39,29 @@ NC_API nc_status nc_op_gemm(const void *A, const void *B, int M, int N, int K, n
 
 /* Residual-stream update of an output projection, N = C columns (C % 128 == 0):
  *   xr = resid + A . B^T;  xm_out <- xr (if non-NULL);  x' = a * xr + b * Y (Y may be NULL);
- *   x_out <- x' (if non-NULL; may equal resid);  xb <- bf16(x');  ssp <- partial sums of x'^2;
- *   if wg != NULL: gp[m, h, g] = sum over group-g columns c < c_g of x'[c] * wg[h, c], h < Hkv
- *   (gp fp32 [M, Hkv, C/128], wg bf16 [Hkv, c_g] 16-byte aligned, Hkv <= 16, c_g % 8 == 0).
+ *   x_out <- x' (if non-NULL; may equal resid);  xb <- bf16(x');  ssp <- partial sums of x'^2.
  * resid, Y, x_out, xm_out fp32 [M, C]; xb bf16 [M, C]. */
 NC_API nc_status nc_op_gemm_residual(const void *A, const void *B, int M, int N, int K,
                                      const float *resid, float a, float b, const float *Y,
-                                     float *x_out, float *xm_out, void *xb, float *ssp,
-                                     const void *wg, int Hkv, int c_g, float *gp, int *status,
+                                     float *x_out, float *xm_out, void *xb, float *ssp, int *status,
                                      void *stream);
 
-/* Packed q|k|v projection of a block: acc = xb[M, C] . wqkv[(H+2Hkv)*D, C]^T scaled by the input
- * RMSNorm row scale rs (from ssp), split into q [M, H*D], k [M, Hkv*D], v [M, Hkv*D] (bf16).
+/* Rows that follow each kv head's v rows in a value-embedding layer's packed q|k|v weight. */
+#define NC_QKV_GATE_ROWS 16
+
+/* Packed q|k|v projection of a block: acc = xb[M, C] . wqkv[N, C]^T scaled by the input RMSNorm
+ * row scale rs (from ssp), split into q [M, H*D], k [M, Hkv*D], v [M, Hkv*D] (bf16).
  * q and k: RoPE at position (row % T) from `rope` (see nc_op_rope_table; rope_ld = its
- * position count, >= T), then RMSNorm over each head (eps).  v: if gp != NULL (fp32
- * [M, Hkv, C/128], see nc_op_gemm_residual), v += gate_scale * sigmoid(rs * sum_g gp[m, g', g])
- * * ve[tokens[m], g'*D:(g'+1)*D] for kv head g' (ve bf16 [V, Hkv*D]); out-of-range tokens add
- * nothing. */
+ * position count, >= T), then RMSNorm over each head (eps).
+ * vgate == 0: wqkv rows are W_q (H*D), W_k (Hkv*D), W_v (Hkv*D); N = (H + 2 Hkv) D.
+ * vgate != 0 (a value-embedding layer): wqkv rows are W_q, W_k, then for each kv head g its D rows
+ * of W_v, then one row holding the gate weights ve_gate[g] (zero beyond c_g) and
+ * NC_QKV_GATE_ROWS - 1 zero rows; N = (H + Hkv) D + Hkv (D + NC_QKV_GATE_ROWS).  Then
+ * v[:, g] += gate_scale * sigmoid(rs * (xb . gate row g)) * ve[tokens[m], g*D:(g+1)*D]
+ * (ve bf16 [V, Hkv*D]); out-of-range tokens add nothing. */
 NC_API nc_status nc_op_qkv(const void *xb, const void *wqkv, int M, int T, int C, int H, int Hkv,
                            int D, const float *rope, int rope_ld, float eps, const float *ssp,
-                           const float *gp, float gate_scale, const void *ve, const int32_t *tokens,
+                           int vgate, float gate_scale, const void *ve, const int32_t *tokens,
                            int V, void *q, void *k, void *v, int *status, void *stream);
 
 /* rope[i][t] = (cos, sin)(t * base^(-2i/D)), i < D/2, t < T, fp32 pairs, position fastest
@@ -71,14 +74,13 @@ NC_API nc_status nc_op_attention(const void *q, const void *k, const void *v, in
                                  int Hkv, int D, int window, void *y, int *status, void *stream);
 
 /* x0[b*T+t] = e_t + sigmoid(e_t[:c_s] . smear_gate) * e_{t-1} (t >= 1, same row b), e = wte[token]
- * (RMS-normalised first if embed_norm); smear_gate NULL = no smear.  Then x = a * x0, xb = bf16(x),
- * ssp = partial sums of x^2 and, if wg != NULL, gp as in nc_op_gemm_residual.  Out-of-range tokens
- * give a zero embedding and NC_ERR_TOKEN_RANGE in *status.  x0, x fp32 [B*T, C]. */
+ * (RMS-normalised first if embed_norm); smear_gate NULL = no smear.  Then x = a * x0, xb = bf16(x)
+ * and ssp = partial sums of x^2.  Out-of-range tokens give a zero embedding and NC_ERR_TOKEN_RANGE
+ * in *status.  x0, x fp32 [B*T, C]. */
 NC_API nc_status nc_op_embed_smear(const int32_t *tokens, int B, int T, const void *wte, int V,
                                    int C, const void *smear_gate, int c_s, int embed_norm,
                                    float eps, float a, float *x0, float *x, void *xb, float *ssp,
-                                   const void *wg, int Hkv, int c_g, float *gp, int *status,
-                                   void *stream);
+                                   int *status, void *stream);
 
 /* Fused lm_head + soft-cap + cross-entropy partials (the loss path of nc_forward_loss): with
  * z = cap * tanh(rs * (xf . wlm^T) / cap) (rs from ssp over C columns, as nc_op_gemm), for each

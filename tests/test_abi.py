@@ -47,7 +47,9 @@ def test_packed_bytes_formula():
     cfg = get_workload("d12").model
     code, n = _packed(cfg)
     assert code == 0
-    qkv = 12 * (6 + 12) * 128 * 768 * 2
+    # q|k|v rows per layer, plus, on the 6 value-embedding layers, 16 rows per kv head (its gate row
+    # and 15 zero rows)
+    qkv = (12 * (6 + 12) * 128 + 6 * 6 * 16) * 768 * 2
     rope = 2048 * 64 * 8
     assert n == 256 + rope + qkv
 
@@ -60,7 +62,7 @@ def test_packed_bytes_formula():
     (dict(vocab_size=32769), 2),
     (dict(smear_gate_channels=6), 2),
     (dict(ve_gate_channels=1000), 1),
-    (dict(ve_gate_channels=12), 2),  # gate rows are read 8 channels at a time
+    (dict(ve_gate_channels=12), 2),  # c_g must be a multiple of 8 (nc.h)
     (dict(n_layer=0, window_left=(), has_ve=()), 1),
 ])
 def test_config_validation(change, code):
@@ -86,12 +88,12 @@ def test_null_arguments_rejected_without_device_work():
     lib.nc_model_destroy(None)
     # per-kernel entry points validate before launching
     assert lib.nc_op_gemm(None, None, 1, 32, 64, 0, None, 32, None, 0, 1e-6, 15.0, None, None) == 1
-    assert lib.nc_op_gemm_residual(None, None, 1, 128, 64, None, 1.0, 0.0, None, None, None, None, None, None, 0,
-                                   0, None, None, None) == 1
+    assert lib.nc_op_gemm_residual(None, None, 1, 128, 64, None, 1.0, 0.0, None, None, None, None, None, None,
+                                   None) == 1
     assert lib.nc_op_attention(None, None, None, 1, 1, 1, 1, 128, -1, None, None, None) == 1
     assert lib.nc_op_rope_table(None, 4, 8, 1e4, None) == 1
-    assert lib.nc_op_embed_smear(None, 1, 1, None, 1, 128, None, 0, 0, 1e-6, 1.0, None, None, None, None, None, 0,
-                                 0, None, None, None) == 1
+    assert lib.nc_op_embed_smear(None, 1, 1, None, 1, 128, None, 0, 0, 1e-6, 1.0, None, None, None, None, None,
+                                 None) == 1
     assert lib.nc_op_lmhead_ce(None, None, 1, 32, 64, None, 1e-6, 15.0, None, None, None, None, None) == 1
     assert lib.nc_op_ce_finalize(None, None, None, 1, 32, None, None, None, None, 0, None, None) == 1
     assert lib.nc_op_ce_scratch_bytes(0) == 0 and lib.nc_op_ce_scratch_bytes(300) >= 16
