@@ -107,6 +107,9 @@ _SIGS = {
     "nc_op_lmhead_ce": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                        ctypes.c_void_p, ctypes.c_float, ctypes.c_float] + [ctypes.c_void_p] * 5),
     "nc_op_ce_scratch_bytes": (ctypes.c_size_t, [ctypes.c_int]),
+    "nc_op_test_wait_timeout": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p] + [ctypes.c_int] * 3 +
+                                [ctypes.c_void_p, ctypes.c_int, ctypes.c_ulonglong, ctypes.c_int, ctypes.c_void_p,
+                                 ctypes.c_void_p]),
     "nc_op_ce_finalize": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
                                          ctypes.c_int] + [ctypes.c_void_p] * 4 + [ctypes.c_size_t, ctypes.c_void_p,
                                                                                    ctypes.c_void_p]),
@@ -128,6 +131,15 @@ class ops:
         check(lib().nc_op_gemm(A.data_ptr(), B.data_ptr(), M, N, K, EPI[epi], out.data_ptr(), out.shape[1],
                                _ptr(ssp), C, eps, cap, _ptr(status), _stream_handle(None)), "nc_op_gemm")
         return out
+
+    @staticmethod
+    def test_wait_timeout(A, B, out, limit_ns, skip_tile, status):
+        """nc_op_test_wait_timeout: the bf16 GEMM with a short wait limit and one tile's accumulator
+        signal withheld; returns the launch status code (the device status lands in `status`)."""
+        M, K = A.shape
+        N = B.shape[0]
+        return lib().nc_op_test_wait_timeout(A.data_ptr(), B.data_ptr(), M, N, K, out.data_ptr(), out.shape[1],
+                                             int(limit_ns), int(skip_tile), status.data_ptr(), _stream_handle(None))
 
     @staticmethod
     def gemm_residual(A, B, resid, a=1.0, b=0.0, Y=None, x_out=None, xm_out=None, status=None):

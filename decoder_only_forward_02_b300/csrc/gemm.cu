@@ -591,6 +591,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int num_m = (M + PAIR_M - 1) / PAIR_M, num_n = num_col_tiles(KIND, N, ep.H, ep.Hkv, ep.D, ep.vgate);
   const int num_tiles = num_m * num_n, kblocks = K / BK;
   int* status = ep.status;
+  const uint64_t wlim = ep.wait_ns;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -642,7 +643,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint32_t b_bytes = vt ? static_cast<uint32_t>(ct.width / 2) * BK * 2 : static_cast<uint32_t>(B_BYTES);
         for (int kb = 0; kb < kblocks; ++kb) {
           const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
-          if (!mbar_wait_cluster(smem_u32(&ctl->empty[s]), ph ^ 1, abort, status)) {
+          if (!mbar_wait_cluster(smem_u32(&ctl->empty[s]), ph ^ 1, abort, status, wlim)) {
             ok = false;
             break;
           }
@@ -658,7 +659,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       // every copy issued by the pair has landed (the peer exits only after the final sync).
       if (rank == 0) {
         for (uint32_t j = (it > STAGES ? it - STAGES : 0); j < it; ++j)
-          mbar_wait_cluster(smem_u32(&ctl->full[j % STAGES]), (j / STAGES) & 1, nullptr, status);
+          mbar_wait_cluster(smem_u32(&ctl->full[j % STAGES]), (j / STAGES) & 1, nullptr, status, wlim);
       }
     } else if (warp == 1 && lane == 0 && rank == 0) {
       uint32_t it = 0, tc = 0;
@@ -668,12 +669,12 @@ __global__ void __launch_bounds__(THREADS, 1)
         tile_coords(tile, num_m, num_n, grp, mb, nb);
         const uint32_t idesc = idesc_bf16_f32(PAIR_M, col_tile<KIND>(nb, N, ep).width);
         const uint32_t a = tc & 1, aph = (tc >> 1) & 1;
-        if (!mbar_wait_cluster(smem_u32(&ctl->tempty[a]), aph ^ 1, abort, status)) break;
+        if (!mbar_wait_cluster(smem_u32(&ctl->tempty[a]), aph ^ 1, abort, status, wlim)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem + a * BN;
         for (int kb = 0; kb < kblocks; ++kb) {
           const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
-          if (!mbar_wait_cluster(smem_u32(&ctl->full[s]), ph, abort, status)) {
+          if (!mbar_wait_cluster(smem_u32(&ctl->full[s]), ph, abort, status, wlim)) {
             ok = false;
             break;
           }
@@ -687,10 +688,10 @@ __global__ void __launch_bounds__(THREADS, 1)
           ++it;
         }
         if (!ok) break;
-        umma_commit_pair(smem_u32(&ctl->tfull[a]), 0x3);
+        if (tile != ep.test_skip_tile) umma_commit_pair(smem_u32(&ctl->tfull[a]), 0x3);
       }
       umma_commit_pair(smem_u32(&ctl->drain), 0x1);
-      mbar_wait(smem_u32(&ctl->drain), 0, nullptr, status);
+      mbar_wait(smem_u32(&ctl->drain), 0, nullptr, status, wlim);
     }
     __syncwarp();
   } else {
@@ -721,7 +722,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       coords(tile, m0w, ct);
       const int n0 = ct.col0 + group * 128;
       const EpiPre pre = pre_finish<KIND>(raw, lane, m0w, M, ep, ct);
-      const bool ok = mbar_wait_cluster(smem_u32(&ctl->tfull[a]), aph, abort, status);
+      const bool ok = mbar_wait_cluster(smem_u32(&ctl->tfull[a]), aph, abort, status, wlim);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
       if (tile + npairs < num_tiles) {   // the next tile's row data is in flight during this epilogue

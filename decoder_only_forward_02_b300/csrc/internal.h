@@ -34,6 +34,11 @@ constexpr int VGATE_ROWS = 16;
 struct GemmEpi {
   int kind = EPI_BF16;
   int* status = nullptr;
+  // Limit of every bounded wait of the launch, and a test hook: the MMA issuer withholds the
+  // "accumulator ready" signal of pair tile test_skip_tile (< 0: none), so that its epilogue's
+  // wait runs out and the launch takes its abort path (see nc_op_test_wait_timeout).
+  unsigned long long wait_ns = 2000000000ull;
+  int test_skip_tile = -1;
 
   // Row scale of the consuming epilogues (RELU2, SOFTCAP, QKV): rs[m] = 1 / sqrt(sum_g
   // ssp[m, g] / ncols + eps), ssp fp32 [M, ncg] partial sums of squares; ssp == null -> rs = 1.

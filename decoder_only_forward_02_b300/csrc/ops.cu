@@ -176,4 +176,23 @@ nc_status nc_op_ce_finalize(const float* part, const float* zt, const int32_t* t
                                             static_cast<cudaStream_t>(stream)));
 }
 
+nc_status nc_op_test_wait_timeout(const void* A, const void* B, int M, int N, int K, void* out, int ldo,
+                                  unsigned long long limit_ns, int skip_tile, int* status, void* stream) {
+  if (!al(A, 16) || !al(B, 16) || !al(out, 16) || status == nullptr || M < 1 || N < 1 || K < 1 || ldo < N ||
+      ldo % 8 != 0 || skip_tile < 0)
+    return NC_ERR_INVALID_ARG;
+  if (K % 64 != 0 || N % 32 != 0) return NC_ERR_UNSUPPORTED;
+  // a limit long enough for the tiles that do run, short enough to end the test quickly
+  if (limit_ns < 100000ull || limit_ns > 100000000ull) return NC_ERR_INVALID_ARG;
+  nc::GemmEpi e;
+  e.kind = nc::EPI_BF16;
+  e.out = out;
+  e.ldo = ldo;
+  e.status = status;
+  e.wait_ns = limit_ns;
+  e.test_skip_tile = skip_tile;
+  return cuda_status(nc::launch_gemm(static_cast<const nc::bf16*>(A), static_cast<const nc::bf16*>(B), M, N, K,
+                                     e, device_sms(), static_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"

@@ -62,11 +62,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait until the phase with the given parity has completed.  Bounded: gives up after
-// NC_WAIT_LIMIT_NS or as soon as another role of the CTA has raised *abort (abort may be
-// null for teardown waits that must not be cut short).
+// Wait until the phase with the given parity has completed.  Bounded: gives up after limit_ns
+// (NC_WAIT_LIMIT_NS unless a caller passes a shorter limit) or as soon as another role of the CTA
+// has raised *abort (abort may be null for teardown waits that must not be cut short).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
-                                          int* status) {
+                                          int* status, uint64_t limit_ns = NC_WAIT_LIMIT_NS) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
@@ -74,7 +74,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (abort != nullptr && *abort) return false;
-    if (globaltimer_ns() - t0 > NC_WAIT_LIMIT_NS) {
+    if (globaltimer_ns() - t0 > limit_ns) {
       record_error(status, NC_ERR_DEVICE_TIMEOUT);
       if (abort != nullptr) *abort = 1;
       return false;
@@ -405,7 +405,7 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
 
 // mbar_wait with cluster-scope acquire (for barriers that peer CTAs arrive on).
 __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, volatile int* abort,
-                                                  int* status) {
+                                                  int* status, uint64_t limit_ns = NC_WAIT_LIMIT_NS) {
   if (mbar_try_wait_cluster(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
@@ -413,7 +413,7 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait_cluster(bar, parity)) return true;
     if (abort != nullptr && *abort) return false;
-    if (globaltimer_ns() - t0 > NC_WAIT_LIMIT_NS) {
+    if (globaltimer_ns() - t0 > limit_ns) {
       record_error(status, NC_ERR_DEVICE_TIMEOUT);
       if (abort != nullptr) *abort = 1;
       return false;

@@ -101,6 +101,19 @@ NC_API nc_status nc_op_ce_finalize(const float *part, const float *zt, const int
                                    const int32_t *token_bytes, float *loss, float *stats, void *scratch,
                                    size_t scratch_bytes, int *status, void *stream);
 
+/* Test of the bounded device-side waits (failure detection without a GPU fault): the GEMM of
+ * nc_op_gemm with NC_EPI_BF16, every wait of the launch limited to limit_ns (1e5 .. 1e8 ns), and the
+ * tensor-core issuer withholding the "accumulator ready" signal of pair tile skip_tile (pair tiles
+ * are 256 x 256 output blocks, numbered along the columns first).  The epilogue waiting for that
+ * tile runs out of time: the kernel records NC_ERR_DEVICE_TIMEOUT in *status (device int32,
+ * required), every role of the CTA pair leaves its loop, drains the copies and tensor-core work in
+ * flight, frees its tensor memory and returns, so the context stays usable.  The other tiles are
+ * computed as by nc_op_gemm; the skipped tile's part of `out` is left unwritten.  Returns the launch
+ * status. */
+NC_API nc_status nc_op_test_wait_timeout(const void *A, const void *B, int M, int N, int K, void *out,
+                                         int ldo, unsigned long long limit_ns, int skip_tile,
+                                         int *status, void *stream);
+
 #ifdef __cplusplus
 }
 #endif
