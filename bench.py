@@ -393,6 +393,52 @@ def run_ours(args, rank, world, local_rank):
                                "weight-read-bound, not tuned"}
         del cache
 
+    # The same forward writing bf16 logits (nc_config.logits_bf16: the soft-capped values rounded to
+    # nearest even, half the 2.15 GB write), on device and end to end through host buffers.
+    logits_bf16 = None
+    if not args.no_bf16_logits:
+        m16 = NB.Model(cfg, wts, device=dev, logits_bf16=True)
+        z16 = torch.empty((B, T, V), dtype=torch.bfloat16, device=dev)
+        for _ in range(3):
+            m16.forward(tok, out=z16)
+        n16 = max(1, min(args.steps, 50))
+        barrier()
+        torch.cuda.synchronize()
+        e6 = torch.cuda.Event(enable_timing=True)
+        e7 = torch.cuda.Event(enable_timing=True)
+        e6.record(stream)
+        for _ in range(n16):
+            m16.forward(tok, out=z16)
+        e7.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        if m16.status() != 0:
+            raise RuntimeError("device status set on the bf16-logits forward")
+        ms16 = max_over_ranks(e6.elapsed_time(e7), world, dev) / n16
+        logits_bf16 = {"metric": "forward tokens/s, bf16 logits", "value": job_rate(world, B * T, ms16), "unit": UNIT,
+                       "ms_per_step": ms16, "steps": n16, "gpu_launches_per_step": m16.launch_count(),
+                       "note": "nc_forward with logits_bf16: the same logits rounded to nearest even "
+                               "(bitwise the rounding of the fp32 output)"}
+        if not args.no_e2e:
+            tok_h = tok_cpu.pin_memory()
+            out_h = torch.empty((B, T, V), dtype=torch.bfloat16).pin_memory()
+            for _ in range(2):
+                m16.forward_host(tok_h, out_h)
+            k = max(1, min(args.steps, args.e2e_steps))
+            barrier()
+            torch.cuda.synchronize()
+            h0 = time.perf_counter()
+            for _ in range(k):
+                m16.forward_host(tok_h, out_h)
+            torch.cuda.synchronize()
+            h_ms = 1000 * (time.perf_counter() - h0)
+            logits_bf16["e2e"] = {"value": job_rate(world, B * T * k, max_over_ranks(h_ms, world, dev)), "unit": UNIT,
+                                  "h2d_bytes_per_step": int(tok_h.numel() * 4),
+                                  "d2h_bytes_per_step": int(out_h.numel() * 2), "steps": k}
+            del out_h
+        del m16, z16
+        torch.cuda.empty_cache()
+
     ms_max = max_over_ranks(ms, world, dev)
     ms_step = ms_max / args.steps
     value = job_rate(world, B * T * args.steps, ms_max)
@@ -464,6 +510,7 @@ def run_ours(args, rank, world, local_rank):
         "e2e": e2e,
         "loss_path": loss_path,
         "decode_path": decode_path,
+        "logits_bf16": logits_bf16,
     }
     if workloads:
         line["workloads"] = workloads
@@ -567,7 +614,7 @@ def _weight_bytes(w):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default="d12")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
@@ -575,6 +622,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-loss-path", action="store_true", help="skip timing the fused cross-entropy path")
     ap.add_argument("--no-decode-path", action="store_true", help="skip timing the KV-cache decode step")
+    ap.add_argument("--no-bf16-logits", action="store_true", help="skip timing the forward with bf16 logits")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-tokens", type=int, default=2048)
     ap.add_argument("--cpu-rows", type=int, default=4, help="batch rows the CPU baseline times")

@@ -36,7 +36,7 @@ class NcConfig(ctypes.Structure):
         ("use_smear", ctypes.c_int), ("use_backout", ctypes.c_int), ("embed_norm", ctypes.c_int),
         ("smear_gate_channels", ctypes.c_int), ("ve_gate_channels", ctypes.c_int),
         ("ve_gate_scale", ctypes.c_float), ("rms_eps", ctypes.c_float), ("rope_base", ctypes.c_float),
-        ("softcap", ctypes.c_float),
+        ("softcap", ctypes.c_float), ("logits_bf16", ctypes.c_int),
     ]
 
 
@@ -115,7 +115,7 @@ _SIGS = {
                                                                                    ctypes.c_void_p]),
 }
 
-EPI = {"bf16": 0, "relu2_bf16": 2, "softcap_f32": 3}
+EPI = {"bf16": 0, "relu2_bf16": 2, "softcap_f32": 3, "softcap_bf16": 6}
 
 
 class ops:
@@ -126,7 +126,7 @@ class ops:
         M, K = A.shape
         N = B.shape[0]
         if out is None:
-            dt = torch.bfloat16 if epi in ("bf16", "relu2_bf16") else torch.float32
+            dt = torch.bfloat16 if epi in ("bf16", "relu2_bf16", "softcap_bf16") else torch.float32
             out = torch.empty((M, N), dtype=dt, device=A.device)
         check(lib().nc_op_gemm(A.data_ptr(), B.data_ptr(), M, N, K, EPI[epi], out.data_ptr(), out.shape[1],
                                _ptr(ssp), C, eps, cap, _ptr(status), _stream_handle(None)), "nc_op_gemm")
@@ -289,8 +289,9 @@ def _stream_handle(stream: Optional[torch.cuda.Stream]) -> int:
     return s.cuda_stream
 
 
-def make_config(cfg) -> tuple:
-    """Build an NcConfig from any object with the model's attribute names.
+def make_config(cfg, logits_bf16: bool = False) -> tuple:
+    """Build an NcConfig from any object with the model's attribute names (logits_bf16: the
+    forward writes bf16 logits instead of fp32).
 
     Returns (struct, keepalive) - the per-layer arrays must stay alive while the struct is used.
     """
@@ -306,7 +307,8 @@ def make_config(cfg) -> tuple:
         smear_gate_channels=int(getattr(cfg, "smear_gate_channels", 0)),
         ve_gate_channels=int(getattr(cfg, "ve_gate_channels", 0)),
         ve_gate_scale=float(getattr(cfg, "ve_gate_scale", 1.0)), rms_eps=float(getattr(cfg, "rms_eps", 1e-6)),
-        rope_base=float(getattr(cfg, "rope_base", 10000.0)), softcap=float(getattr(cfg, "softcap", 15.0)))
+        rope_base=float(getattr(cfg, "rope_base", 10000.0)), softcap=float(getattr(cfg, "softcap", 15.0)),
+        logits_bf16=int(bool(logits_bf16)))
     return c, (win, ve)
 
 
@@ -323,10 +325,11 @@ class Model:
     float lists resid_lambdas, x0_lambdas and the float backout_lambda."""
 
     def __init__(self, cfg, weights: Dict[str, object], device: Optional[torch.device] = None,
-                 stream: Optional[torch.cuda.Stream] = None):
+                 stream: Optional[torch.cuda.Stream] = None, logits_bf16: bool = False):
         self.cfg = cfg
         self.device = torch.device(device) if device is not None else weights["wte"].device
-        self._cstruct, self._keep = make_config(cfg)
+        self.logits_dtype = torch.bfloat16 if logits_bf16 else torch.float32
+        self._cstruct, self._keep = make_config(cfg, logits_bf16)
         L = cfg.n_layer
 
         def arr(name, optional=False):
@@ -387,14 +390,14 @@ class Model:
 
     def forward(self, tokens: torch.Tensor, out: Optional[torch.Tensor] = None,
                 stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
-        """tokens: device int32 [B, T] -> fp32 logits [B, T, V] (asynchronous)."""
+        """tokens: device int32 [B, T] -> logits [B, T, V], fp32 or bf16 (logits_dtype; asynchronous)."""
         if tokens.dtype != torch.int32 or not tokens.is_cuda or not tokens.is_contiguous():
             raise ValueError("tokens must be a contiguous int32 CUDA tensor")
         B, T = tokens.shape
         V = self.cfg.vocab_size
         if out is None:
-            out = torch.empty((B, T, V), dtype=torch.float32, device=self.device)
-        _check_out(out, (B, T, V), torch.float32, tokens.device, "out")
+            out = torch.empty((B, T, V), dtype=self.logits_dtype, device=self.device)
+        _check_out(out, (B, T, V), self.logits_dtype, tokens.device, "out")
         ws = self.workspace(B, T)
         check(lib().nc_forward(self.handle, tokens.data_ptr(), B, T, out.data_ptr(), ws.data_ptr(), ws.numel(),
                                _stream_handle(stream)), "nc_forward")
@@ -434,13 +437,13 @@ class Model:
 
     def prefill(self, tokens: torch.Tensor, cache: torch.Tensor, T_max: int, out: Optional[torch.Tensor] = None,
                 stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
-        """tokens: device int32 [B, T] -> logits fp32 [B, T, V]; fills the cache with positions 0..T-1."""
+        """tokens: device int32 [B, T] -> logits [B, T, V] (logits_dtype); fills the cache with positions 0..T-1."""
         if tokens.dtype != torch.int32 or not tokens.is_cuda or not tokens.is_contiguous():
             raise ValueError("tokens must be a contiguous int32 CUDA tensor")
         B, T = tokens.shape
         if out is None:
-            out = torch.empty((B, T, self.cfg.vocab_size), dtype=torch.float32, device=self.device)
-        _check_out(out, (B, T, self.cfg.vocab_size), torch.float32, tokens.device, "out")
+            out = torch.empty((B, T, self.cfg.vocab_size), dtype=self.logits_dtype, device=self.device)
+        _check_out(out, (B, T, self.cfg.vocab_size), self.logits_dtype, tokens.device, "out")
         ws = self.workspace(B, T)
         check(lib().nc_prefill(self.handle, tokens.data_ptr(), B, T, cache.data_ptr(), cache.numel(), T_max,
                                out.data_ptr(), ws.data_ptr(), ws.numel(), _stream_handle(stream)), "nc_prefill")
@@ -449,7 +452,7 @@ class Model:
     def decode_step(self, prev_tokens: torch.Tensor, tokens: torch.Tensor, pos: int, cache: torch.Tensor,
                     T_max: int, out: Optional[torch.Tensor] = None,
                     stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
-        """tokens / prev_tokens: device int32 [B] (positions pos and pos - 1) -> logits fp32 [B, V] of
+        """tokens / prev_tokens: device int32 [B] (positions pos and pos - 1) -> logits [B, V] (logits_dtype) of
         position pos; appends the new keys and values to the cache."""
         for name, t in (("tokens", tokens), ("prev_tokens", prev_tokens)):
             if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
@@ -458,8 +461,8 @@ class Model:
         if prev_tokens.shape != tokens.shape or tokens.dim() != 1:
             raise ValueError("tokens and prev_tokens must both have shape [B]")
         if out is None:
-            out = torch.empty((B, self.cfg.vocab_size), dtype=torch.float32, device=self.device)
-        _check_out(out, (B, self.cfg.vocab_size), torch.float32, tokens.device, "out")
+            out = torch.empty((B, self.cfg.vocab_size), dtype=self.logits_dtype, device=self.device)
+        _check_out(out, (B, self.cfg.vocab_size), self.logits_dtype, tokens.device, "out")
         key = ("decode", B)
         if key not in self._ws:
             n = ctypes.c_size_t()
@@ -473,8 +476,10 @@ class Model:
 
     def forward_host(self, tokens: torch.Tensor, out: torch.Tensor,
                      stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
-        """tokens: host int32 [B, T] (pinned for full speed) -> out: host fp32 [B, T, V]; synchronous."""
+        """tokens: host int32 [B, T] (pinned for full speed) -> out: host [B, T, V] (logits_dtype);
+        synchronous."""
         B, T = tokens.shape
+        _check_out(out, (B, T, self.cfg.vocab_size), self.logits_dtype, torch.device("cpu"), "out")
         ws = self.workspace(B, T, host=True)
         check(lib().nc_forward_host(self.handle, tokens.data_ptr(), B, T, out.data_ptr(), ws.data_ptr(),
                                     ws.numel(), _stream_handle(stream)), "nc_forward_host")

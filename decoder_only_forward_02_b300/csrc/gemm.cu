@@ -33,7 +33,7 @@
 // the normalisation of a GEMM's input becomes a per-row scale of its accumulator):
 //   EPI_RELU2_BF16   squared ReLU of the MLP up projection, input RMSNorm as a row scale
 //   EPI_SOFTCAP_F32  tanh soft-cap (+-cap) of the untied lm_head logits, final RMSNorm as a row
-//                    scale (hardware tanh)
+//                    scale (hardware tanh); EPI_SOFTCAP_BF16 the same logits rounded to bf16
 //   EPI_CE           the lm_head with soft-cap and cross-entropy: per row and 128-column group,
 //                    the sum of exp(logit) and the target's logit; no logits are stored
 //   EPI_QKV          split of the packed q|k|v projection, input RMSNorm as a row scale; RoPE
@@ -80,7 +80,7 @@ constexpr int SLAB_BYTES = 2 * SLAB_BUF; // two per epilogue warp, used alternat
 // The cross-entropy epilogue stores no tile at all: no staging buffers, a 7-stage ring.
 template <int KIND, int D>
 struct Cfg {
-  static constexpr bool LSU_STORE = KIND == EPI_RELU2_BF16 || KIND == EPI_SOFTCAP_F32;
+  static constexpr bool LSU_STORE = KIND == EPI_RELU2_BF16 || KIND == EPI_SOFTCAP_F32 || KIND == EPI_SOFTCAP_BF16;
   static constexpr int STAGES = KIND == EPI_CE ? 7 : (LSU_STORE ? 6 : 5);
   static constexpr int SLAB_WARP = KIND == EPI_CE ? 0 : (LSU_STORE ? SLAB_BUF : SLAB_BYTES);   // staging bytes per warp
   static constexpr int OFF_SLAB = STAGES * (A_BYTES + B_BYTES);
@@ -299,12 +299,16 @@ __device__ __forceinline__ void lsu_store_box(const uint8_t* buf, void* out, siz
   }
 }
 
-// Plain bf16 store (TMA), or relu(rs * acc)^2 (MLP up projection, squared ReLU; row-coalesced
-// stores from the single staging buffer).
-template <bool RELU2>
+// bf16 outputs of 64-column boxes: plain (TMA store), relu(rs * acc)^2 (MLP up projection, squared
+// ReLU) or cap * tanh(rs * acc / cap) (the lm_head's soft-capped logits in bf16); the last two are
+// stored row-coalesced from the single staging buffer, the logits with streaming stores.
+enum Bf16Mode { BF16_PLAIN = 0, BF16_RELU2 = 1, BF16_SOFTCAP = 2 };
+
+template <int MODE>
 __device__ __forceinline__ void epi_bf16(uint32_t taddr, uint32_t tempty, int lane, int m0w, int n0, int M, int N,
                                          const GemmEpi& ep, const OutMaps& om, Slab& sl, const EpiPre& pre) {
   const float rs = pre.rs;
+  const float cap = ep.cap, sc = rs / cap;
 #pragma unroll 1
   for (int ch = 0; ch < 2; ++ch) {
     const int c0 = n0 + ch * 64;
@@ -322,21 +326,24 @@ __device__ __forceinline__ void epi_bf16(uint32_t taddr, uint32_t tempty, int la
       for (int j = 0; j < 8; ++j) {
         const int e = c * 8 + j;
         float t = __uint_as_float(e < 32 ? r[e] : r2[e - 32]);
-        if constexpr (RELU2) {
+        if constexpr (MODE == BF16_RELU2) {
           t = fmaxf(t * rs, 0.f);
           t = t * t;
+        } else if constexpr (MODE == BF16_SOFTCAP) {
+          t = cap * tanh_approx(t * sc);
         }
         a[j] = t;
       }
       o[c] = pack8_bf16(a);
     }
-    if constexpr (RELU2) {
+    if constexpr (MODE != BF16_PLAIN) {
+      constexpr bool stream = MODE == BF16_SOFTCAP;
       __syncwarp();   // every lane is done reading the previous box
       sl.put_row(lane, o);
       __syncwarp();
       if (c0 + 64 <= N) {
         lsu_store_box(sl.buf(), ep.out, static_cast<size_t>(ep.ldo) * 2, m0w, static_cast<size_t>(c0) * 2, M, lane,
-                      false);
+                      stream);
       } else {   // ragged last box: 32 valid columns (N % 32 == 0)
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
@@ -739,7 +746,11 @@ __global__ void __launch_bounds__(THREADS, 1)
       else if constexpr (KIND == EPI_QKV) {
         if (ct.vhead >= 0) epi_vgate<D>(tbase, tempty, lane, m0w, group, ct.vhead, ep, om, sl, pre);
         else epi_qkv<D>(taddr, tempty, lane, m0w, n0, ct.end, M, ep, om, sl, pre);
-      } else epi_bf16<KIND == EPI_RELU2_BF16>(taddr, tempty, lane, m0w, n0, M, N, ep, om, sl, pre);
+      } else if constexpr (KIND == EPI_SOFTCAP_BF16) {
+        epi_bf16<BF16_SOFTCAP>(taddr, tempty, lane, m0w, n0, M, N, ep, om, sl, pre);
+      } else {
+        epi_bf16<KIND == EPI_RELU2_BF16 ? BF16_RELU2 : BF16_PLAIN>(taddr, tempty, lane, m0w, n0, M, N, ep, om, sl, pre);
+      }
     }
     if (lane == 0) bulk_wait<0>();   // stores complete before the CTA exits
     __syncwarp();
@@ -827,7 +838,9 @@ cudaError_t launch_gemm(const bf16* A, const bf16* B, int M, int N, int K, const
       ok = make_tmap_bf16_2d(&om.o0, epi.out, N, Mu, static_cast<uint64_t>(epi.ldo) * 2, 64, 32);
       break;
     case EPI_RELU2_BF16:   // row-coalesced plain stores (16-byte aligned rows)
-      ok = (reinterpret_cast<uintptr_t>(epi.out) % 16 == 0) && epi.ldo % 8 == 0;
+    case EPI_SOFTCAP_BF16:
+      ok = (reinterpret_cast<uintptr_t>(epi.out) % 16 == 0) && epi.ldo % 8 == 0 &&
+           (epi.kind != EPI_SOFTCAP_BF16 || epi.cap > 0.f);
       break;
     case EPI_QKV: {
       const uint64_t qc = static_cast<uint64_t>(epi.H) * epi.D, kc = static_cast<uint64_t>(epi.Hkv) * epi.D;
@@ -851,6 +864,7 @@ cudaError_t launch_gemm(const bf16* A, const bf16* B, int M, int N, int K, const
     case EPI_BF16: return launch_kind<EPI_BF16, 0>(ta, tb, tbv, om, M, N, K, epi, num_sms, stream);
     case EPI_RELU2_BF16: return launch_kind<EPI_RELU2_BF16, 0>(ta, tb, tbv, om, M, N, K, epi, num_sms, stream);
     case EPI_SOFTCAP_F32: return launch_kind<EPI_SOFTCAP_F32, 0>(ta, tb, tbv, om, M, N, K, epi, num_sms, stream);
+    case EPI_SOFTCAP_BF16: return launch_kind<EPI_SOFTCAP_BF16, 0>(ta, tb, tbv, om, M, N, K, epi, num_sms, stream);
     case EPI_CE: return launch_kind<EPI_CE, 0>(ta, tb, tbv, om, M, N, K, epi, num_sms, stream);
     case EPI_QKV:
       if (epi.D == 128) return launch_kind<EPI_QKV, 128>(ta, tb, tbv, om, M, N, K, epi, num_sms, stream);

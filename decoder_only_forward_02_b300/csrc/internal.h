@@ -21,6 +21,7 @@ enum EpiKind : int {
   EPI_SOFTCAP_F32 = 3,  // out(f32) = cap * tanh(rs * acc / cap)
   EPI_QKV = 4,          // q|k|v split, RoPE + RMSNorm on q and k, value-embedding gate on v
   EPI_CE = 5,           // cross-entropy partials of z = cap * tanh(rs * acc / cap), no logits
+  EPI_SOFTCAP_BF16 = 6, // out(bf16) = cap * tanh(rs * acc / cap)
 };
 
 // Columns covered by one partial sum of squares (one epilogue thread's share of a row).
@@ -47,7 +48,7 @@ struct GemmEpi {
   float inv_ncols = 0.f;  // 1 / ncols
   float eps = 1e-6f;
 
-  // EPI_BF16 / EPI_RELU2_BF16 / EPI_SOFTCAP_F32
+  // EPI_BF16 / EPI_RELU2_BF16 / EPI_SOFTCAP_F32 / EPI_SOFTCAP_BF16
   void* out = nullptr;
   int ldo = 0;
   float cap = 15.f;

@@ -142,6 +142,7 @@ nc_status validate_config(const nc_config* c) {
   if (c->smear_gate_channels < 0 || c->smear_gate_channels > c->n_embd) return NC_ERR_INVALID_ARG;
   if (c->ve_gate_channels < 0 || c->ve_gate_channels > c->n_embd) return NC_ERR_INVALID_ARG;
   if (!(c->rms_eps >= 0.f) || !(c->softcap > 0.f) || !(c->rope_base > 0.f)) return NC_ERR_INVALID_ARG;
+  if (c->logits_bf16 != 0 && c->logits_bf16 != 1) return NC_ERR_INVALID_ARG;
   if (c->head_dim != 64 && c->head_dim != 128) return NC_ERR_UNSUPPORTED;
   if (c->n_embd % 128 != 0 || c->n_embd > 2048) return NC_ERR_UNSUPPORTED;
   if (c->mlp_hidden % 64 != 0 || c->vocab_size % 64 != 0) return NC_ERR_UNSUPPORTED;
@@ -365,7 +366,7 @@ nc_status nc_workspace_bytes_host(const nc_model* m, int B, int T, size_t* bytes
   nc_status s = nc_workspace_bytes(m, B, T, &base);
   if (s != NC_OK) return s;
   const size_t M = static_cast<size_t>(B) * T;
-  *bytes = base + align_up(M * 4) + align_up(M * m->cfg.vocab_size * 4);
+  *bytes = base + align_up(M * 4) + align_up(M * m->cfg.vocab_size * (m->cfg.logits_bf16 ? 2 : 4));
   return NC_OK;
 }
 
@@ -577,7 +578,28 @@ LossLayout loss_layout_for(const nc_model* m, const Layout& Lo, int B, int T) {
 
 extern "C" {
 
-nc_status nc_forward(nc_model* m, const int32_t* tokens, int B, int T, float* logits,
+namespace {
+
+// Bytes of one logit in the caller's output.
+size_t logit_bytes(const nc_model* m) { return m->cfg.logits_bf16 ? 2 : 4; }
+
+// The lm_head with the final RMSNorm (row scale from ssp) and the soft-cap, writing fp32 or bf16
+// logits [M, V] as the config asks.
+cudaError_t launch_lm_head(nc_model* m, const bf16* xb, float* ssp, int M, void* logits, cudaStream_t stream) {
+  nc::GemmEpi le;
+  set_consumer(le, m, ssp);
+  le.kind = m->cfg.logits_bf16 ? nc::EPI_SOFTCAP_BF16 : nc::EPI_SOFTCAP_F32;
+  le.out = logits;
+  le.ldo = m->cfg.vocab_size;
+  le.cap = m->cfg.softcap;
+  return timed(m, NC_K_LMHEAD, stream, [&] {
+    return nc::launch_gemm(xb, m->lm, M, m->cfg.vocab_size, m->C(), le, m->num_sms, stream);
+  });
+}
+
+}  // namespace
+
+nc_status nc_forward(nc_model* m, const int32_t* tokens, int B, int T, void* logits,
                      void* workspace, size_t ws_bytes, void* stream_) {
   nc_status s = check_forward_args(m, tokens, B, T, workspace);
   if (s != NC_OK) return s;
@@ -587,18 +609,9 @@ nc_status nc_forward(nc_model* m, const int32_t* tokens, int B, int T, float* lo
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   cudaError_t e = run_blocks(m, tokens, B, T, Lo, ws, stream);
-  if (e == cudaSuccess) {
-    nc::GemmEpi le;
-    set_consumer(le, m, reinterpret_cast<float*>(ws + Lo.ssp));
-    le.kind = nc::EPI_SOFTCAP_F32;
-    le.out = logits;
-    le.ldo = m->cfg.vocab_size;
-    le.cap = m->cfg.softcap;
-    e = timed(m, NC_K_LMHEAD, stream, [&] {
-      return nc::launch_gemm(reinterpret_cast<bf16*>(ws + Lo.xb), m->lm, B * T, m->cfg.vocab_size, m->C(), le,
-                             m->num_sms, stream);
-    });
-  }
+  if (e == cudaSuccess)
+    e = launch_lm_head(m, reinterpret_cast<bf16*>(ws + Lo.xb), reinterpret_cast<float*>(ws + Lo.ssp), B * T, logits,
+                       stream);
   return nc::cuda_status(e);
 }
 
@@ -655,7 +668,7 @@ nc_status nc_kv_cache_bytes(const nc_model* m, int B, int T_max, size_t* bytes) 
 }
 
 nc_status nc_prefill(nc_model* m, const int32_t* tokens, int B, int T, void* kv_cache, size_t cache_bytes,
-                     int T_max, float* logits, void* workspace, size_t ws_bytes, void* stream_) {
+                     int T_max, void* logits, void* workspace, size_t ws_bytes, void* stream_) {
   nc_status s = check_forward_args(m, tokens, B, T, workspace);
   if (s != NC_OK) return s;
   if (logits == nullptr || !aligned(logits, 16) || kv_cache == nullptr || !aligned(kv_cache, ALIGN))
@@ -671,18 +684,9 @@ nc_status nc_prefill(nc_model* m, const int32_t* tokens, int B, int T, void* kv_
   kv.cache = static_cast<uint8_t*>(kv_cache);
   kv.T_max = T_max;
   cudaError_t e = run_blocks(m, tokens, B, T, Lo, ws, stream, &kv);
-  if (e == cudaSuccess) {
-    nc::GemmEpi le;
-    set_consumer(le, m, reinterpret_cast<float*>(ws + Lo.ssp));
-    le.kind = nc::EPI_SOFTCAP_F32;
-    le.out = logits;
-    le.ldo = m->cfg.vocab_size;
-    le.cap = m->cfg.softcap;
-    e = timed(m, NC_K_LMHEAD, stream, [&] {
-      return nc::launch_gemm(reinterpret_cast<bf16*>(ws + Lo.xb), m->lm, B * T, m->cfg.vocab_size, m->C(), le,
-                             m->num_sms, stream);
-    });
-  }
+  if (e == cudaSuccess)
+    e = launch_lm_head(m, reinterpret_cast<bf16*>(ws + Lo.xb), reinterpret_cast<float*>(ws + Lo.ssp), B * T, logits,
+                       stream);
   return nc::cuda_status(e);
 }
 
@@ -690,13 +694,13 @@ nc_status nc_workspace_bytes_decode(const nc_model* m, int B, size_t* bytes) {
   if (m == nullptr || bytes == nullptr || B < 1) return NC_ERR_INVALID_ARG;
   if (m->cfg.seq_len_ctx < 2) return NC_ERR_UNSUPPORTED;
   const size_t rows = 2 * static_cast<size_t>(B);
-  *bytes = layout_for(m, B, 2).end + align_up(rows * 4) + align_up(rows * m->cfg.vocab_size * 4) +
+  *bytes = layout_for(m, B, 2).end + align_up(rows * 4) + align_up(rows * m->cfg.vocab_size * logit_bytes(m)) +
            align_up(decode_scratch_floats(m, B) * 4);
   return NC_OK;
 }
 
 nc_status nc_decode_step(nc_model* m, const int32_t* prev_tokens, const int32_t* tokens, int B, int pos,
-                         void* kv_cache, size_t cache_bytes, int T_max, float* logits, void* workspace,
+                         void* kv_cache, size_t cache_bytes, int T_max, void* logits, void* workspace,
                          size_t ws_bytes, void* stream_) {
   if (m == nullptr || prev_tokens == nullptr || tokens == nullptr || logits == nullptr || kv_cache == nullptr ||
       workspace == nullptr || B < 1)
@@ -716,9 +720,9 @@ nc_status nc_decode_step(nc_model* m, const int32_t* prev_tokens, const int32_t*
   const int V = m->cfg.vocab_size;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   int32_t* pair = reinterpret_cast<int32_t*>(ws + Lo.end);                        // [B][2] (prev, token)
-  float* logits2 = reinterpret_cast<float*>(ws + Lo.end + align_up(2 * static_cast<size_t>(B) * 4));   // [B][2][V]
-  float* attn_scratch = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(logits2) +
-                                                 align_up(2 * static_cast<size_t>(B) * V * 4));
+  const size_t lb = logit_bytes(m);
+  uint8_t* logits2 = ws + Lo.end + align_up(2 * static_cast<size_t>(B) * 4);   // [B][2][V]
+  float* attn_scratch = reinterpret_cast<float*>(logits2 + align_up(2 * static_cast<size_t>(B) * V * lb));
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   // Each row becomes the pair (previous token, new token): the embedding's smear then sees the
   // previous token, and with the rotary table offset by pos - 1 the pair sits at positions
@@ -734,24 +738,16 @@ nc_status nc_decode_step(nc_model* m, const int32_t* prev_tokens, const int32_t*
   kv.scratch = attn_scratch;
   kv.scratch_floats = decode_scratch_floats(m, B);
   if (e == cudaSuccess) e = run_blocks(m, pair, B, 2, Lo, ws, stream, &kv);
-  if (e == cudaSuccess) {
-    nc::GemmEpi le;
-    set_consumer(le, m, reinterpret_cast<float*>(ws + Lo.ssp));
-    le.kind = nc::EPI_SOFTCAP_F32;
-    le.out = logits2;
-    le.ldo = V;
-    le.cap = m->cfg.softcap;
-    e = timed(m, NC_K_LMHEAD, stream, [&] {
-      return nc::launch_gemm(reinterpret_cast<bf16*>(ws + Lo.xb), m->lm, 2 * B, V, m->C(), le, m->num_sms, stream);
-    });
-  }
+  if (e == cudaSuccess)
+    e = launch_lm_head(m, reinterpret_cast<bf16*>(ws + Lo.xb), reinterpret_cast<float*>(ws + Lo.ssp), 2 * B, logits2,
+                       stream);
   if (e == cudaSuccess)   // the second row of each pair
-    e = cudaMemcpy2DAsync(logits, static_cast<size_t>(V) * 4, logits2 + V, 2 * static_cast<size_t>(V) * 4,
-                          static_cast<size_t>(V) * 4, B, cudaMemcpyDeviceToDevice, stream);
+    e = cudaMemcpy2DAsync(logits, static_cast<size_t>(V) * lb, logits2 + V * lb, 2 * static_cast<size_t>(V) * lb,
+                          static_cast<size_t>(V) * lb, B, cudaMemcpyDeviceToDevice, stream);
   return nc::cuda_status(e);
 }
 
-nc_status nc_forward_host(nc_model* m, const int32_t* tokens_host, int B, int T, float* logits_host,
+nc_status nc_forward_host(nc_model* m, const int32_t* tokens_host, int B, int T, void* logits_host,
                           void* workspace, size_t ws_bytes, void* stream_) {
   if (m == nullptr || tokens_host == nullptr || logits_host == nullptr || workspace == nullptr)
     return NC_ERR_INVALID_ARG;
@@ -765,14 +761,14 @@ nc_status nc_forward_host(nc_model* m, const int32_t* tokens_host, int B, int T,
   const size_t M = static_cast<size_t>(B) * T;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   int32_t* tok_dev = reinterpret_cast<int32_t*>(ws + base);
-  float* logits_dev = reinterpret_cast<float*>(ws + base + align_up(M * 4));
+  void* logits_dev = ws + base + align_up(M * 4);
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   s = nc::cuda_status(cudaMemcpyAsync(tok_dev, tokens_host, M * 4, cudaMemcpyHostToDevice, stream));
   if (s != NC_OK) return s;
   s = nc_forward(m, tok_dev, B, T, logits_dev, workspace, base, stream_);
   if (s != NC_OK) return s;
   s = nc::cuda_status(
-      cudaMemcpyAsync(logits_host, logits_dev, M * m->cfg.vocab_size * 4, cudaMemcpyDeviceToHost, stream));
+      cudaMemcpyAsync(logits_host, logits_dev, M * m->cfg.vocab_size * logit_bytes(m), cudaMemcpyDeviceToHost, stream));
   if (s != NC_OK) return s;
   return nc::cuda_status(cudaStreamSynchronize(stream));
 }

@@ -49,7 +49,7 @@ nc_status scratch_for_current_device(void** out) {
 }  // namespace
 
 extern "C" nc_status nc_forward_static_scratch(nc_model* m, const int32_t* tokens, int B, int T,
-                                               float* logits, void* stream) {
+                                               void* logits, void* stream) {
   if (m == nullptr || tokens == nullptr || logits == nullptr) return NC_ERR_INVALID_ARG;
   size_t need = 0;
   nc_status s = nc_workspace_bytes(m, B, T, &need);

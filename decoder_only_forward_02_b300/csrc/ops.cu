@@ -26,12 +26,13 @@ nc_status nc_op_gemm(const void* A, const void* B, int M, int N, int K, nc_epilo
   if (!al_or_null(ssp, 4) || (ssp != nullptr && (C < nc::SS_GROUP || C % nc::SS_GROUP != 0)))
     return NC_ERR_INVALID_ARG;
   if (K % 64 != 0 || N % 32 != 0) return NC_ERR_UNSUPPORTED;
-  if (epi == NC_EPI_SOFTCAP_F32 && !(cap > 0.f)) return NC_ERR_INVALID_ARG;
+  if ((epi == NC_EPI_SOFTCAP_F32 || epi == NC_EPI_SOFTCAP_BF16) && !(cap > 0.f)) return NC_ERR_INVALID_ARG;
   nc::GemmEpi e;
   switch (epi) {
     case NC_EPI_BF16: e.kind = nc::EPI_BF16; break;
     case NC_EPI_RELU2_BF16: e.kind = nc::EPI_RELU2_BF16; break;
     case NC_EPI_SOFTCAP_F32: e.kind = nc::EPI_SOFTCAP_F32; break;
+    case NC_EPI_SOFTCAP_BF16: e.kind = nc::EPI_SOFTCAP_BF16; break;
     default: return NC_ERR_INVALID_ARG;
   }
   e.out = out;

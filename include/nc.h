@@ -101,6 +101,8 @@ typedef struct {
   float rms_eps;              /* default 1e-6 */
   float rope_base;            /* default 10000 */
   float softcap;              /* default 15 */
+  int logits_bf16;            /* 0: logits are fp32 (default); 1: bf16 (the same soft-capped values
+                                 rounded to nearest even: half the bytes to write and to copy out) */
 } nc_config;
 
 /* Weights.  Matrices are bf16, row-major in the nn.Linear layout [out, in],
@@ -142,22 +144,22 @@ NC_API nc_status nc_model_create(const nc_config *cfg, const nc_weights *w, void
 /* Device workspace needed by nc_forward for a [B, T] batch.  Host-only. */
 NC_API nc_status nc_workspace_bytes(const nc_model *m, int B, int T, size_t *bytes);
 
-/* Forward pass: tokens (device int32 [B, T]) -> logits (device fp32
- * [B, T, V], row-major), soft-capped.  Asynchronous on `stream`; argument
+/* Forward pass: tokens (device int32 [B, T]) -> logits (device [B, T, V], row-major, fp32 or,
+ * with cfg.logits_bf16, bf16), soft-capped.  Asynchronous on `stream`; argument
  * errors are returned synchronously before any device work; device-side
  * errors (token range, wait timeout) are recorded in the status word and
  * returned by nc_get_status.  workspace: device, >= nc_workspace_bytes,
  * 256-byte aligned, caller-owned; T <= seq_len_ctx. */
-NC_API nc_status nc_forward(nc_model *m, const int32_t *tokens, int B, int T, float *logits,
+NC_API nc_status nc_forward(nc_model *m, const int32_t *tokens, int B, int T, void *logits,
                      void *workspace, size_t ws_bytes, void *stream);
 
 /* Same forward with HOST buffers: copies tokens (host int32 [B, T]) in,
- * runs nc_forward, copies logits (host fp32 [B, T, V]) out and synchronises
+ * runs nc_forward, copies logits (host [B, T, V], fp32 or bf16 as nc_forward) out and synchronises
  * `stream`.  Staging areas live in `workspace`, sized by
  * nc_workspace_bytes_host.  Pinned host memory gives full copy bandwidth. */
 NC_API nc_status nc_workspace_bytes_host(const nc_model *m, int B, int T, size_t *bytes);
 NC_API nc_status nc_forward_host(nc_model *m, const int32_t *tokens_host, int B, int T,
-                          float *logits_host, void *workspace, size_t ws_bytes, void *stream);
+                          void *logits_host, void *workspace, size_t ws_bytes, void *stream);
 
 /* Forward pass for callers that cannot allocate device memory when they run the model
  * (for example code hosted by a framework that owns all device memory through its own pool
@@ -168,7 +170,7 @@ NC_API nc_status nc_forward_host(nc_model *m, const int32_t *tokens_host, int B,
  * Identical to nc_forward, except that the activation scratch is a fixed array of
  * NC_STATIC_SCRATCH_BYTES built into the library (every GPU that loads the library keeps
  * it reserved until the process exits) instead of a caller workspace.  The caller passes
- * only the model, tokens (device int32 [B, T]) and logits (device fp32 [B, T, V]).
+ * only the model, tokens (device int32 [B, T]) and logits (device [B, T, V], as nc_forward).
  *  - Limit: returns NC_ERR_WORKSPACE, before any device work, when nc_workspace_bytes(B, T)
  *    exceeds NC_STATIC_SCRATCH_BYTES (at d12 width that is roughly 1,400 tokens per call).
  *  - Allocates nothing: no cudaMalloc, cudaFree or allocating library routine.  Keep
@@ -184,7 +186,7 @@ NC_API nc_status nc_forward_host(nc_model *m, const int32_t *tokens_host, int B,
  *    serialise them. */
 #define NC_STATIC_SCRATCH_BYTES (32u * 1024u * 1024u)
 NC_API nc_status nc_forward_static_scratch(nc_model *m, const int32_t *tokens, int B, int T,
-                                           float *logits, void *stream);
+                                           void *logits, void *stream);
 
 /* ---- loss path: fused lm_head + soft-cap + next-token cross-entropy, no logits ----
  * "nanochat — 架构与原理", section 2 component table (metrics row: bits per byte from the
@@ -221,22 +223,23 @@ NC_API nc_status nc_forward_loss(nc_model *m, const int32_t *tokens, const int32
  * 256-byte aligned) and T_max <= seq_len_ctx.
  *
  * nc_prefill: nc_forward over tokens [B, T] (T <= T_max) that also fills the cache with
- * positions 0..T-1; logits fp32 [B, T, V]; workspace as nc_forward (nc_workspace_bytes(B, T)).
+ * positions 0..T-1; logits [B, T, V] (fp32 or bf16 as nc_forward); workspace as nc_forward
+ * (nc_workspace_bytes(B, T)).
  *
  * nc_decode_step: one new token per batch row, all at position pos (1 <= pos < T_max):
  * tokens (device int32 [B]) are the tokens at pos, prev_tokens those at pos - 1 (the smear
  * reads the previous token's embedding); appends the new keys and values at pos and writes the
- * logits of position pos, fp32 [B, V].  The result equals row pos of nc_forward over the whole
+ * logits of position pos, [B, V] (fp32 or bf16 as nc_forward).  The result equals row pos of nc_forward over the whole
  * sequence (up to rounding: the decode attention keeps p in fp32 where the batched one rounds
  * it to bf16).  workspace: >= nc_workspace_bytes_decode(B), 256-byte aligned.
  * Both are asynchronous on `stream`; errors as nc_forward.  nc_kv_launch_count gives the kernels a
  * decode step launches (2 + 7 * n_layer; a prefill launches 2 + 6 * n_layer). */
 NC_API nc_status nc_kv_cache_bytes(const nc_model *m, int B, int T_max, size_t *bytes);
 NC_API nc_status nc_prefill(nc_model *m, const int32_t *tokens, int B, int T, void *kv_cache, size_t cache_bytes,
-                            int T_max, float *logits, void *workspace, size_t ws_bytes, void *stream);
+                            int T_max, void *logits, void *workspace, size_t ws_bytes, void *stream);
 NC_API nc_status nc_workspace_bytes_decode(const nc_model *m, int B, size_t *bytes);
 NC_API nc_status nc_decode_step(nc_model *m, const int32_t *prev_tokens, const int32_t *tokens, int B, int pos,
-                                void *kv_cache, size_t cache_bytes, int T_max, float *logits, void *workspace,
+                                void *kv_cache, size_t cache_bytes, int T_max, void *logits, void *workspace,
                                 size_t ws_bytes, void *stream);
 NC_API int nc_kv_launch_count(const nc_model *m);
 

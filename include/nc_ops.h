@@ -23,7 +23,8 @@ extern "C" {
 typedef enum {
   NC_EPI_BF16 = 0,        /* out bf16 [M, ldo] = acc */
   NC_EPI_RELU2_BF16 = 2,  /* out bf16 = relu(rs * acc)^2     (squared-ReLU row of the feature table) */
-  NC_EPI_SOFTCAP_F32 = 3  /* out fp32 = cap*tanh(rs * acc/cap) (logit soft-cap row of the feature table) */
+  NC_EPI_SOFTCAP_F32 = 3, /* out fp32 = cap*tanh(rs * acc/cap) (logit soft-cap row of the feature table) */
+  NC_EPI_SOFTCAP_BF16 = 6 /* out bf16 = the same, rounded to nearest even */
 } nc_epilogue;
 
 /* Partial sums of squares ("ssp"): fp32 [M, C/128]; ssp[m, g] = sum of x[m, c]^2 over the 128

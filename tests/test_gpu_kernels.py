@@ -125,6 +125,10 @@ def test_gemm_relu2_and_softcap_row_scaled():
     np.testing.assert_allclose(z.cpu().double().numpy(), O.softcap(rs[:, None] * acc, 15.0), rtol=0,
                                atol=15.0 * 2 ** -10)
     np.testing.assert_allclose(z1.cpu().double().numpy(), O.softcap(acc, 15.0), rtol=0, atol=15.0 * 2 ** -10)
+    # bf16 logits: the same values rounded to nearest even, bit for bit
+    zb = _ops().gemm(A.to(DEV), Bm.to(DEV), "softcap_bf16", ssp=ssp.to(DEV), C=K, cap=15.0)
+    torch.cuda.synchronize()
+    assert torch.equal(zb, z.to(torch.bfloat16))
     assert float(z1.abs().max()) < 15.0
 
 

@@ -209,3 +209,55 @@ def test_loss_path_repeatable_and_launch_count():
     b = m.forward_loss(tok.to(DEV), tgt.to(DEV), token_bytes=tb.to(DEV))
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
     assert m.launch_count(loss=True) == m.launch_count() + 2
+
+
+# ------------------------------------------------------------------------ bf16 logits (opt-in output)
+
+# bf16 keeps 8 significant bits: rounding to nearest moves a logit |z| < cap by at most cap * 2^-9
+BF16_LOGIT_ULP = 15.0 * 2 ** -9
+
+
+@pytest.mark.parametrize("name,B,T", [("tiny_all", 2, 64), ("d12", 1, 512)])
+def test_logits_bf16_is_the_rounded_fp32_forward(name, B, T):
+    """With logits_bf16 the forward writes the same soft-capped values rounded to nearest even:
+    bit for bit the rounding of the fp32 forward's logits (same kernels, same accumulation), and
+    within the oracle bound plus the rounding bound."""
+    wl = get_workload(name)
+    cfg = wl.model
+    wts = make_weights(cfg, seed=wl.seed, init=wl.init)
+    tok = make_tokens(wl)[:B, :T].contiguous()
+    Bn = binding()
+    w = to_device(wts)
+    m32 = Bn.Model(cfg, w)
+    m16 = Bn.Model(cfg, w, logits_bf16=True)
+    z32 = m32.forward(tok.to(DEV))
+    z16 = m16.forward(tok.to(DEV))
+    assert m16.status() == 0 and z16.dtype == torch.bfloat16
+    assert torch.equal(z16, z32.to(torch.bfloat16))
+    ref = O.forward(cfg, O.OracleWeights.from_synth(cfg, wts), tok.numpy())
+    g = z16.float().cpu().numpy()
+    d = np.abs(g - ref)
+    assert d.max() <= 5e-2 + BF16_LOGIT_ULP and d.sum() / np.abs(ref).sum() <= 1e-2 + 2 ** -9
+    # the host entry point copies half the bytes out
+    out_h = torch.empty((B, T, cfg.vocab_size), dtype=torch.bfloat16).pin_memory()
+    m16.forward_host(tok.pin_memory(), out_h)
+    assert torch.equal(out_h, z16.cpu())
+
+
+def test_logits_bf16_prefill_and_decode():
+    wl = get_workload("tiny_all")
+    cfg = wl.model
+    w = to_device(make_weights(cfg, init="dense"))
+    tok = make_tokens(wl).to(DEV)
+    Bn = binding()
+    outs = {}
+    for bf in (False, True):
+        m = Bn.Model(cfg, w, logits_bf16=bf)
+        cache = m.kv_cache(tok.shape[0], 64)
+        pre = m.prefill(tok[:, :40].contiguous(), cache, 64)
+        dec = m.decode_step(tok[:, 39].contiguous(), tok[:, 40].contiguous(), 40, cache, 64)
+        assert m.status() == 0
+        outs[bf] = (pre, dec)
+    assert outs[True][0].dtype == torch.bfloat16 and outs[True][1].dtype == torch.bfloat16
+    assert torch.equal(outs[True][0], outs[False][0].to(torch.bfloat16))
+    assert torch.equal(outs[True][1], outs[False][1].to(torch.bfloat16))
