@@ -584,6 +584,16 @@ def run_single_kernel(args):
         tok = torch.randint(0, V, (wl.B, wl.T), generator=g, device=dev, dtype=torch.int32)
         wte, sg = rnd((V, C), 0.02), rnd((C,), 0.02)
         fn = lambda: ops.embed_smear(tok, wte, sg, C)
+    elif k == "decode":   # decode steps at the last position after a prefill of T-1 tokens (cache append, split attention)
+        from synth import make_tokens, make_weights
+        wts = {n: (v.to(dev) if torch.is_tensor(v) else v) for n, v in make_weights(c, seed=wl.seed, init=wl.init).items()}
+        model = NB.Model(c, wts, device=dev)
+        tokd = make_tokens(wl).to(dev)
+        T0 = wl.T - 1
+        cache = model.kv_cache(wl.B, wl.T)
+        model.prefill(tokd[:, :T0].contiguous(), cache, wl.T)
+        prev, cur = tokd[:, T0 - 1].contiguous(), tokd[:, T0].contiguous()
+        fn = lambda: model.decode_step(prev, cur, T0, cache, wl.T)
     else:
         raise SystemExit(f"unknown kernel {k}")
     for _ in range(args.launches):
@@ -634,7 +644,7 @@ def main():
     ap.add_argument("--extra-cpu-tokens", type=int, default=128,
                     help="positions of batch row 0 the oracle runs for each extra workload's CPU baseline")
     ap.add_argument("--only-kernel", default=None,
-                    help="launch one kernel class (qkv, attention, oproj, fc, proj, lmhead, lmhead_ce, embed) "
+                    help="launch one kernel class (qkv, attention, oproj, fc, proj, lmhead, lmhead_ce, embed, decode) "
                          "at the workload's shapes, for profiler captures")
     ap.add_argument("--launches", type=int, default=3)
     ap.add_argument("--window", type=int, default=None)

@@ -17,7 +17,10 @@
 //   tensor memory (512 columns): S_k for query tile k at columns 128k (fp32 scores); softmax k
 //               overwrites the first 64 of them with P_k (bf16, two per column), which the
 //               P V step reads as its A operand straight from tensor memory; O_k at 256 + k*D.
-//   warp 0      TMA: Q0 and Q1 once, then K and V tiles (128 keys) into a 2-stage ring.
+//   warp 0      TMA: Q0 and Q1 once per item (and an L2 prefetch of the next item's, so that its
+//               load at the item transition hits L2), then the key tiles (128 keys) into a ring
+//               (2 stages at D = 128, 3 at D = 64).
+//   warp 2      TMA: the value tiles into a 3-stage ring of their own.
 //   warp 1      TMEM allocation; one lane issues, for each key tile j:
 //                 O_0 += P_0(j) V(j), S_0(j+1) = Q_0 K(j+1)^T, O_1 += P_1(j) V(j), S_1(j+1) ...
 //               so that while softmax 0 works on its scores the tensor core runs query tile 1's
@@ -33,7 +36,7 @@
 //               only when a row's max grows by more than 2^8; only then is that row of O
 //               rescaled.
 //               Final: O / l -> bf16 -> y.
-//   warps 2, 3  idle.
+//   warp 3      idle.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -42,18 +45,22 @@
 namespace nc {
 namespace {
 
-constexpr int BQ = 128, BKV = 128, STAGES = 2;
+constexpr int BQ = 128, BKV = 128;
 constexpr int SM_WARP0 = 4;                    // softmax warps 4..11
 constexpr int THREADS = 32 * (SM_WARP0 + 8);
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int REGS_CTRL = 88, REGS_SOFTMAX = 200;   // 128*88 + 256*200 <= 384*168
 static_assert(128 * REGS_CTRL + 256 * REGS_SOFTMAX <= THREADS * 168, "register split exceeds the launch");
 
+constexpr int MAX_KS = 3, MAX_VS = 3;
+
 struct __align__(8) AttnCtrl {
   uint64_t q_full;
   uint64_t q_empty;     // the last S MMA of an item has run: its Q tiles may be replaced
-  uint64_t kv_full[STAGES];
-  uint64_t kv_empty[STAGES];
+  uint64_t k_full[MAX_KS];
+  uint64_t k_empty[MAX_KS];   // both query tiles' S steps on this key tile have run
+  uint64_t v_full[MAX_VS];
+  uint64_t v_empty[MAX_VS];   // both query tiles' P V steps on this key tile have run
   uint64_t s_full[2];   // S_k(j) (and every earlier tensor-core step) complete
   uint64_t p_full[2][2];   // softmax k wrote keys [64 h, 64 h + 64) of P_k(j)  ([k][h])
   uint64_t o_done[2];   // O_k final (its last P V step complete)
@@ -62,18 +69,27 @@ struct __align__(8) AttnCtrl {
   int abort;
 };
 
+// Keys and values have rings of their own: a key tile is free once both query tiles' S steps on
+// it have run, a value tile only after their P V steps.  A commit fires when every tensor-core
+// step issued before it is done, so a V slot is handed back only at the end of a key tile's
+// work; with two V slots the P V step of the next key tile waited for its value tile to arrive
+// and held back the S steps queued behind it.  At D = 128 shared memory holds two query tiles
+// (64 KB), two K stages and three V stages (32 KB each).
 template <int D>
 struct Lay {
   static constexpr int Q_BOX = BQ * 64 * 2;      // [128 rows][64 d] bf16, 16 KB
   static constexpr int KV_BOX = BKV * 64 * 2;    // [128 keys][64 d] bf16, 16 KB
   static constexpr int NB = D / 64;              // boxes along d
   static constexpr int Q_BYTES = NB * Q_BOX;     // one query tile
-  static constexpr int K_BYTES = NB * KV_BOX;
-  static constexpr int OFF_KV = 2 * Q_BYTES;
-  static constexpr int STAGE_BYTES = 2 * K_BYTES;  // K then V
-  static constexpr int OFF_CTRL = OFF_KV + STAGES * STAGE_BYTES;
+  static constexpr int K_BYTES = NB * KV_BOX;    // one key (or value) tile
+  static constexpr int KS = D == 128 ? 2 : 3, VS = 3;
+  static constexpr int OFF_K = 2 * Q_BYTES;
+  static constexpr int OFF_V = OFF_K + KS * K_BYTES;
+  static constexpr int OFF_CTRL = OFF_V + VS * K_BYTES;
   static constexpr int TOTAL = OFF_CTRL + 256;
+  static_assert(KS <= MAX_KS && VS <= MAX_VS, "ring depth");
   static_assert(TOTAL <= 232448, "shared memory");
+  static_assert(sizeof(AttnCtrl) <= 256, "control block");
 };
 
 // Key-tile range [lo, hi] (128-key tiles) of query tile rows [q0, q0 + 127] (rows < T).
@@ -140,16 +156,20 @@ __global__ void __launch_bounds__(THREADS, 1)
     return;
   }
   AttnCtrl* ctl = reinterpret_cast<AttnCtrl*>(smem + L::OFF_CTRL);
-  const uint32_t sQ = smem_u32(smem), sKV = sQ + L::OFF_KV;
+  const uint32_t sQ = smem_u32(smem), sK0 = sQ + L::OFF_K, sV0 = sQ + L::OFF_V;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int first = static_cast<int>(blockIdx.x), stride = static_cast<int>(gridDim.x);
 
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&ctl->q_full), 1);
     mbar_init(smem_u32(&ctl->q_empty), 1);
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(smem_u32(&ctl->kv_full[s]), 1);
-      mbar_init(smem_u32(&ctl->kv_empty[s]), 1);
+    for (int s = 0; s < L::KS; ++s) {
+      mbar_init(smem_u32(&ctl->k_full[s]), 1);
+      mbar_init(smem_u32(&ctl->k_empty[s]), 1);
+    }
+    for (int s = 0; s < L::VS; ++s) {
+      mbar_init(smem_u32(&ctl->v_full[s]), 1);
+      mbar_init(smem_u32(&ctl->v_empty[s]), 1);
     }
     for (int k = 0; k < 2; ++k) {
       mbar_init(smem_u32(&ctl->s_full[k]), 1);
@@ -187,6 +207,17 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int it = item_index(first, r, stride);
         if (it >= num_items) break;
         const Item w = decode_item(it, T, H, Hkv, B, window);
+        {   // the next item's query tiles into L2 while this item runs
+          const int nx = item_index(first, r + 1, stride);
+          if (nx < num_items) {
+            const Item wn = decode_item(nx, T, H, Hkv, B, window);
+#pragma unroll
+            for (int c = 0; c < L::NB; ++c) {
+              tma_prefetch_l2_2d(&tmQ, wn.h * D + c * 64, wn.b * T + wn.qbase);
+              if (wn.has_q1) tma_prefetch_l2_2d(&tmQ, wn.h * D + c * 64, wn.b * T + wn.qbase + BQ);
+            }
+          }
+        }
         if (ic > 0 && !mbar_wait(smem_u32(&ctl->q_empty), (ic - 1) & 1, abort, status)) break;
         mbar_arrive_expect_tx(qb, (w.has_q1 ? 2 : 1) * L::Q_BYTES);
 #pragma unroll
@@ -196,26 +227,44 @@ __global__ void __launch_bounds__(THREADS, 1)
             tma_load_2d(sQ + L::Q_BYTES + c * L::Q_BOX, &tmQ, qb, w.h * D + c * 64, w.b * T + w.qbase + BQ);
         }
         for (int j = w.jlo; j <= w.jhi; ++j, ++gkv) {
-          const uint32_t s = gkv % STAGES;
-          if (!mbar_wait(smem_u32(&ctl->kv_empty[s]), ((gkv / STAGES) & 1) ^ 1, abort, status)) {
+          const uint32_t s = gkv % L::KS;
+          if (!mbar_wait(smem_u32(&ctl->k_empty[s]), ((gkv / L::KS) & 1) ^ 1, abort, status)) {
             ok = false;
             break;
           }
-          const uint32_t fb = smem_u32(&ctl->kv_full[s]);
-          mbar_arrive_expect_tx(fb, L::STAGE_BYTES);
-          const int row = w.b * T + j * BKV;
-          const uint32_t sK = sKV + s * L::STAGE_BYTES, sV = sK + L::K_BYTES;
+          const uint32_t fb = smem_u32(&ctl->k_full[s]);
+          mbar_arrive_expect_tx(fb, L::K_BYTES);
 #pragma unroll
-          for (int c = 0; c < L::NB; ++c) {
-            tma_load_2d(sK + c * L::KV_BOX, &tmK, fb, w.g * D + c * 64, row);
-            tma_load_2d(sV + c * L::KV_BOX, &tmV, fb, w.g * D + c * 64, row);
-          }
+          for (int c = 0; c < L::NB; ++c)
+            tma_load_2d(sK0 + s * L::K_BYTES + c * L::KV_BOX, &tmK, fb, w.g * D + c * 64, w.b * T + j * BKV);
         }
       }
       // every issued copy must land before the CTA may exit
       if (ic > 0) mbar_wait(qb, (ic - 1) & 1, nullptr, status);
-      for (uint32_t q = (gkv > STAGES ? gkv - STAGES : 0); q < gkv; ++q)
-        mbar_wait(smem_u32(&ctl->kv_full[q % STAGES]), (q / STAGES) & 1, nullptr, status);
+      for (uint32_t q = (gkv > L::KS ? gkv - L::KS : 0); q < gkv; ++q)
+        mbar_wait(smem_u32(&ctl->k_full[q % L::KS]), (q / L::KS) & 1, nullptr, status);
+    } else if (warp == 2 && lane == 0) {   // value tiles, in the same item and key-tile order
+      uint32_t gkv = 0;
+      bool ok = true;
+      for (int r = 0; ok; ++r) {
+        const int it = item_index(first, r, stride);
+        if (it >= num_items) break;
+        const Item w = decode_item(it, T, H, Hkv, B, window);
+        for (int j = w.jlo; j <= w.jhi; ++j, ++gkv) {
+          const uint32_t s = gkv % L::VS;
+          if (!mbar_wait(smem_u32(&ctl->v_empty[s]), ((gkv / L::VS) & 1) ^ 1, abort, status)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = smem_u32(&ctl->v_full[s]);
+          mbar_arrive_expect_tx(fb, L::K_BYTES);
+#pragma unroll
+          for (int c = 0; c < L::NB; ++c)
+            tma_load_2d(sV0 + s * L::K_BYTES + c * L::KV_BOX, &tmV, fb, w.g * D + c * 64, w.b * T + j * BKV);
+        }
+      }
+      for (uint32_t q = (gkv > L::VS ? gkv - L::VS : 0); q < gkv; ++q)
+        mbar_wait(smem_u32(&ctl->v_full[q % L::VS]), (q / L::VS) & 1, nullptr, status);
     } else if (warp == 1 && lane == 0) {
       constexpr uint32_t idS = idesc_bf16_f32(BQ, BKV);
       constexpr uint32_t idO = idesc_bf16_f32_bmn(BQ, D);
@@ -230,15 +279,21 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int lo[2] = {w.lo0, w.lo1}, hi[2] = {w.hi0, w.hi1};
         const int jlo = w.jlo, jhi = w.jhi;
         if (!mbar_wait(smem_u32(&ctl->q_full), ic & 1, abort, status)) break;
-        auto kv_ready = [&](int j) -> bool {
-          const uint32_t q = gkv + static_cast<uint32_t>(j - jlo);
-          if (!mbar_wait(smem_u32(&ctl->kv_full[q % STAGES]), (q / STAGES) & 1, abort, status)) return false;
+        auto pos_of = [&](int j) { return gkv + static_cast<uint32_t>(j - jlo); };   // ring position of key tile j
+        auto k_ready = [&](int j) -> bool {
+          const uint32_t q = pos_of(j);
+          if (!mbar_wait(smem_u32(&ctl->k_full[q % L::KS]), (q / L::KS) & 1, abort, status)) return false;
           tc_fence_after();
           return true;
         };
-        auto stage_of = [&](int j) { return (gkv + static_cast<uint32_t>(j - jlo)) % STAGES; };
+        auto v_ready = [&](int j) -> bool {
+          const uint32_t q = pos_of(j);
+          if (!mbar_wait(smem_u32(&ctl->v_full[q % L::VS]), (q / L::VS) & 1, abort, status)) return false;
+          tc_fence_after();
+          return true;
+        };
         auto issue_s = [&](int k, int j) {
-          const uint32_t sK = sKV + stage_of(j) * L::STAGE_BYTES;
+          const uint32_t sK = sK0 + (pos_of(j) % L::KS) * L::K_BYTES;
           const uint32_t qk = sQ + k * L::Q_BYTES;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
@@ -248,12 +303,17 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           umma_commit(smem_u32(&ctl->s_full[k]));
         };
-        if (!kv_ready(jlo)) break;
+        if (!k_ready(jlo)) break;
         for (int k = 0; k < 2; ++k)
           if (jlo >= lo[k] && jlo <= hi[k]) issue_s(k, jlo);
+        umma_commit(smem_u32(&ctl->k_empty[pos_of(jlo) % L::KS]));   // both S steps on key tile jlo issued
         if (jlo == jhi) umma_commit(smem_u32(&ctl->q_empty));   // no S step of this item is left
         for (int j = jlo; j <= jhi && ok; ++j) {
-          const uint32_t sV = sKV + stage_of(j) * L::STAGE_BYTES + L::K_BYTES;
+          if (!v_ready(j)) {
+            ok = false;
+            break;
+          }
+          const uint32_t sV = sV0 + (pos_of(j) % L::VS) * L::K_BYTES;
           bool next_ready = false;
 #pragma unroll
           for (int k = 0; k < 2 && ok; ++k) {
@@ -280,7 +340,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             if (j + 1 <= jhi && j + 1 >= lo[k] && j + 1 <= hi[k]) {
               if (!next_ready) {
-                if (!kv_ready(j + 1)) {
+                if (!k_ready(j + 1)) {
                   ok = false;
                   break;
                 }
@@ -290,8 +350,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
           }
           if (!ok) break;
+          if (j + 1 <= jhi) umma_commit(smem_u32(&ctl->k_empty[pos_of(j + 1) % L::KS]));   // its S steps issued
           if (j + 1 == jhi) umma_commit(smem_u32(&ctl->q_empty));   // no S step of this item is left
-          umma_commit(smem_u32(&ctl->kv_empty[stage_of(j)]));
+          umma_commit(smem_u32(&ctl->v_empty[pos_of(j) % L::VS]));
         }
         gkv += static_cast<uint32_t>(jhi - jlo + 1);
       }
