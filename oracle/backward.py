@@ -142,3 +142,45 @@ def loss_and_grads(cfg, W: OracleWeights, tokens: np.ndarray,
     loss = mean_loss(cfg, P, tokens, targets)
     loss.backward()
     return float(loss.item()), {k: p.grad.detach().numpy().copy() for k, p in P.items()}
+
+
+# ---------------------------------------------------------------- step backwards (closed forms)
+# The backward of single steps of the forward, written out from calculus, in fp64 NumPy: the
+# references of the GPU's backward kernels, each pinned by ``tests/test_oracle_backward.py``
+# against central finite differences of its own forward step and against a property of it.
+
+def rms_norm_backward(x: np.ndarray, g: np.ndarray, eps: float) -> np.ndarray:
+    """dL/dx of the weightless RMSNorm xn = x / sqrt(mean(x^2) + eps) over the last axis, given
+    g = dL/dxn ([ADD] RMSNorm row: no learned weight).  With r = (mean(x^2) + eps)^(-1/2) and
+    dr/dx_j = -r^3 x_j / C:  dL/dx_j = r g_j - r^3 x_j mean_i(g_i x_i)."""
+    x = np.asarray(x, dtype=np.float64)
+    g = np.asarray(g, dtype=np.float64)
+    r = 1.0 / np.sqrt((x * x).mean(-1, keepdims=True) + eps)
+    return r * g - r ** 3 * x * (g * x).mean(-1, keepdims=True)
+
+
+def softcap_ce_grad(u: np.ndarray, targets: np.ndarray, cap: float) -> np.ndarray:
+    """d/du of the mean over counted rows (target in [0, V)) of log sum_v exp z_v - z_target, with
+    z = cap * tanh(u / cap) ([ADD] logit soft-cap row; the loss as in ``oracle/loss.py``):
+    (softmax(z) - onehot(target)) * (1 - (z / cap)^2) / (rows counted); ignored rows are zero."""
+    u = np.asarray(u, dtype=np.float64)
+    t = np.asarray(targets).reshape(-1)
+    M, V = u.shape
+    z = cap * np.tanh(u / cap)
+    keep = (t >= 0) & (t < V)
+    n = int(keep.sum())
+    out = np.zeros_like(z)
+    if n == 0:
+        return out
+    zk = z[keep]
+    p = np.exp(zk - zk.max(-1, keepdims=True))
+    p /= p.sum(-1, keepdims=True)
+    p[np.arange(n), t[keep]] -= 1.0
+    out[keep] = p * (1.0 - (zk / cap) ** 2) / n
+    return out
+
+
+def relu2_backward(u: np.ndarray, g: np.ndarray) -> np.ndarray:
+    """d/du of relu(u)^2 times the upstream gradient g ([ADD] ReLU^2 row): 2 relu(u) g."""
+    u = np.asarray(u, dtype=np.float64)
+    return 2.0 * np.maximum(u, 0.0) * np.asarray(g, dtype=np.float64)

@@ -77,3 +77,76 @@ def test_gradient_is_zero_on_embedding_rows_of_absent_tokens():
     last_only = np.setdiff1d(np.unique(tok[:, -1]), present)
     assert np.all(grads["wte"][last_only] == 0.0)
     assert np.all(np.abs(grads["lm_head"]).sum(1) > 0)   # every vocabulary row enters the softmax
+
+
+# ---------------------------------------------------------------- step backwards
+
+def _central(f, x, h=1e-6):
+    """Central differences of the scalar f at every entry of x (fp64)."""
+    g = np.zeros_like(x)
+    for idx in np.ndindex(x.shape):
+        e = np.zeros_like(x)
+        e[idx] = h
+        g[idx] = (f(x + e) - f(x - e)) / (2 * h)
+    return g
+
+
+@pytest.mark.parametrize("eps", [0.0, 1e-6, 0.5])
+def test_rms_norm_backward_matches_central_differences(eps):
+    rng = np.random.default_rng(11)
+    x = rng.normal(size=(3, 16)) * np.array([[0.1], [1.0], [7.0]])   # RMS far from 1 in every row
+    w = rng.normal(size=(3, 16))                                      # L = sum(w * rms(x)): g = w
+    loss = lambda xx: float((w * (xx / np.sqrt((xx * xx).mean(-1, keepdims=True) + eps))).sum())
+    got = OB.rms_norm_backward(x, w, eps)
+    np.testing.assert_allclose(got, _central(loss, x), rtol=1e-6, atol=1e-8)
+
+
+def test_rms_norm_backward_is_orthogonal_to_x_without_eps():
+    """At eps = 0 the norm is invariant to scaling x, so its gradient has no component along x."""
+    rng = np.random.default_rng(12)
+    x, g = rng.normal(size=(5, 64)) * 3.0, rng.normal(size=(5, 64))
+    dx = OB.rms_norm_backward(x, g, 0.0)
+    np.testing.assert_allclose((dx * x).sum(-1), 0.0, atol=1e-12)
+    assert np.abs(dx).max() > 0.1
+
+
+def test_softcap_ce_grad_matches_central_differences_and_ignores_rows():
+    rng = np.random.default_rng(13)
+    M, V, cap = 5, 9, 15.0
+    u = rng.normal(size=(M, V)) * 8.0          # some logits well into the cap's curve
+    t = np.array([2, -1, 8, 0, 9])             # one ignored (negative), one out of range
+    def loss(uu):
+        z = cap * np.tanh(uu / cap)
+        keep = (t >= 0) & (t < V)
+        lse = np.log(np.exp(z[keep]).sum(-1))
+        return float((lse - z[keep, t[keep]]).mean())
+    got = OB.softcap_ce_grad(u, t, cap)
+    # the differences' rounding floor: 2 * 2^-52 * |loss| (about 3) / h (1e-6), about 1.3e-9
+    np.testing.assert_allclose(got, _central(loss, u), rtol=1e-6, atol=3e-9)
+    assert np.all(got[1] == 0) and np.all(got[4] == 0)
+
+
+def test_softcap_ce_grad_rows_balance_and_large_cap_limit():
+    """Each counted row of (grad / (1 - (z/cap)^2)) sums to zero (softmax minus one-hot); with the
+    cap far above the logits the factor is 1 and the gradient is (softmax - onehot) / n."""
+    rng = np.random.default_rng(14)
+    u = rng.normal(size=(4, 7))
+    t = np.array([1, 3, 0, 6])
+    g = OB.softcap_ce_grad(u, t, 15.0)
+    z = 15.0 * np.tanh(u / 15.0)
+    np.testing.assert_allclose((g / (1 - (z / 15.0) ** 2)).sum(-1), 0.0, atol=1e-15)
+    big = OB.softcap_ce_grad(u, t, 1e8)
+    p = np.exp(u) / np.exp(u).sum(-1, keepdims=True)
+    p[np.arange(4), t] -= 1
+    np.testing.assert_allclose(big, p / 4, rtol=1e-9, atol=1e-12)
+
+
+def test_relu2_backward_matches_central_differences():
+    rng = np.random.default_rng(15)
+    u = rng.normal(size=(4, 6))
+    u[u.__abs__() < 1e-3] = 0.5   # keep away from the kink at 0
+    w = rng.normal(size=(4, 6))
+    got = OB.relu2_backward(u, w)
+    np.testing.assert_allclose(got, _central(lambda v: float((w * np.maximum(v, 0) ** 2).sum()), u), rtol=1e-6,
+                               atol=1e-9)
+    assert np.all(got[u < 0] == 0)
