@@ -360,6 +360,50 @@ def run_ours(args, rank, world, local_rank):
                      "mean_loss_nats": float(sbuf[0].item()),
                      "note": "nc_forward_loss: lm_head fused with soft-cap and cross-entropy, no logits written"}
 
+    # The backward's first part (nc_forward_loss_grad_tail): the loss path, then the gradient of the
+    # mean loss with respect to the lm_head and the last block's MLP and attention output projection,
+    # timed the same way; a second pass with per-kernel events gives each backward class its rate.
+    grad_tail = None
+    if not args.no_grad_tail:
+        tgt = torch.full_like(tok, -1)
+        tgt[:, :-1] = tok[:, 1:]
+        for _ in range(3):
+            model.loss_grad_tail(tok, tgt)
+        n_bw = max(1, min(args.steps, 20))
+        barrier()
+        torch.cuda.synchronize()
+        e4 = torch.cuda.Event(enable_timing=True)
+        e5 = torch.cuda.Event(enable_timing=True)
+        e4.record(stream)
+        for _ in range(n_bw):
+            st_bw, _ = model.loss_grad_tail(tok, tgt)
+        e5.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        if model.status() != 0:
+            raise RuntimeError("device status set on the backward path")
+        bw_ms = max_over_ranks(e4.elapsed_time(e5), world, dev) / n_bw
+        model.timing(True)
+        model.loss_grad_tail(tok, tgt)
+        torch.cuda.synchronize()
+        bt = model.timing_read()
+        model.timing(False)
+        M = B * T
+        C, F, V, HD = cfg.n_embd, cfg.mlp_hidden, cfg.vocab_size, cfg.n_head * cfg.head_dim
+        bw_work = {"lmhead_grad": ("tensor", 2.0 * M * C * V), "mlp_grad": ("tensor", 2.0 * M * C * F),
+                   "oproj_grad": ("tensor", 2.0 * M * C * HD),
+                   # G and x read (fp32), the residual gradient or the fp32 copy, the bf16 copy
+                   "rmsnorm_grad": ("hbm", 14.0 * M * C)}
+        bw_peaks, bw_src = load_peaks()
+        bw_k, _, _ = roofline({k: v for k, v in bt.items() if k in bw_work}, bw_work, bw_peaks, bw_src)
+        grad_tail = {"metric": "forward + loss + tail gradients tokens/s", "value": job_rate(world, M, bw_ms),
+                     "unit": UNIT, "ms_per_step": bw_ms, "steps": n_bw,
+                     "gpu_launches_per_step": model.grad_tail_launch_count(),
+                     "mean_loss_nats": float(st_bw[0].item()), "kernels": bw_k,
+                     "note": "nc_forward_loss_grad_tail: loss path, then d(mean loss)/d(lm_head, last block's "
+                             "c_proj, c_fc, attention c_proj); the lm_head runs three times (loss, gradient "
+                             "at its output, recomputed; input and weight gradients)"}
+
     # The decode path (nc_prefill of T-1 tokens, then nc_decode_step: one new token per batch row
     # at position T-1, the longest context, read from the KV cache), repeated at that position.
     decode_path = None
@@ -510,6 +554,7 @@ def run_ours(args, rank, world, local_rank):
         "e2e": e2e,
         "loss_path": loss_path,
         "decode_path": decode_path,
+        "grad_tail": grad_tail,
         "logits_bf16": logits_bf16,
     }
     if workloads:
@@ -631,6 +676,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-loss-path", action="store_true", help="skip timing the fused cross-entropy path")
+    ap.add_argument("--no-grad-tail", action="store_true", help="skip timing the tail backward")
     ap.add_argument("--no-decode-path", action="store_true", help="skip timing the KV-cache decode step")
     ap.add_argument("--no-bf16-logits", action="store_true", help="skip timing the forward with bf16 logits")
     ap.add_argument("--e2e-steps", type=int, default=5)

@@ -19,7 +19,8 @@ NC_OK = 0
 STATUS_NAMES = {0: "NC_OK", 1: "NC_ERR_INVALID_ARG", 2: "NC_ERR_UNSUPPORTED", 3: "NC_ERR_WORKSPACE",
                 4: "NC_ERR_CUDA", 5: "NC_ERR_DEVICE_TIMEOUT", 6: "NC_ERR_TOKEN_RANGE"}
 KERNEL_CLASSES = ["embed_smear", "qkv_rope_qknorm_ve", "attention", "oproj_residual", "fc_relu2",
-                  "proj_residual", "lmhead_softcap", "cross_entropy"]
+                  "proj_residual", "lmhead_softcap", "cross_entropy", "lmhead_grad", "mlp_grad", "oproj_grad",
+                  "rmsnorm_grad"]
 SS_GROUP = 128   # columns per partial sum of squares
 QKV_GATE_ROWS = 16   # rows after each kv head's v rows in a value-embedding layer's packed q|k|v weight
 
@@ -87,6 +88,12 @@ _SIGS = {
                                                ctypes.POINTER(ctypes.c_size_t)]),
     "nc_forward_loss": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int]
                         + [ctypes.c_void_p] * 4 + [ctypes.c_size_t, ctypes.c_void_p]),
+    "nc_workspace_bytes_grad_tail": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+                                                    ctypes.POINTER(ctypes.c_size_t)]),
+    "nc_forward_loss_grad_tail": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+                                                 ctypes.c_int] + [ctypes.c_void_p] * 7 + [ctypes.c_size_t,
+                                                                                         ctypes.c_void_p]),
+    "nc_grad_tail_launch_count": (ctypes.c_int, [ctypes.c_void_p]),
     # per-kernel entry points (include/nc_ops.h)
     "nc_op_gemm": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                   ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int,
@@ -111,11 +118,21 @@ _SIGS = {
                                 [ctypes.c_void_p, ctypes.c_int, ctypes.c_ulonglong, ctypes.c_int, ctypes.c_void_p,
                                  ctypes.c_void_p]),
     "nc_op_ce_finalize": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
-                                         ctypes.c_int] + [ctypes.c_void_p] * 4 + [ctypes.c_size_t, ctypes.c_void_p,
-                                                                                   ctypes.c_void_p]),
+                                         ctypes.c_int] + [ctypes.c_void_p] * 4 + [ctypes.c_size_t] +
+                          [ctypes.c_void_p] * 4),
+    "nc_op_gemm_t": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p] + [ctypes.c_int] * 6 +
+                     [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_float,
+                      ctypes.c_void_p, ctypes.c_void_p]),
+    "nc_op_lmhead_ce_grad": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+                                            ctypes.c_int, ctypes.c_void_p, ctypes.c_float, ctypes.c_float] +
+                             [ctypes.c_void_p] * 4 + [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]),
+    "nc_op_mlp_hidden_grad": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+                                             ctypes.c_int, ctypes.c_void_p, ctypes.c_float] + [ctypes.c_void_p] * 4),
+    "nc_op_rms_backward": (ctypes.c_int, [ctypes.c_void_p] * 4 + [ctypes.c_int, ctypes.c_int, ctypes.c_float] +
+                           [ctypes.c_void_p] * 3),
 }
 
-EPI = {"bf16": 0, "relu2_bf16": 2, "softcap_f32": 3, "softcap_bf16": 6}
+EPI = {"bf16": 0, "relu2_bf16": 2, "softcap_f32": 3, "softcap_bf16": 6, "f32": 7}
 
 
 class ops:
@@ -131,6 +148,53 @@ class ops:
         check(lib().nc_op_gemm(A.data_ptr(), B.data_ptr(), M, N, K, EPI[epi], out.data_ptr(), out.shape[1],
                                _ptr(ssp), C, eps, cap, _ptr(status), _stream_handle(None)), "nc_op_gemm")
         return out
+
+    @staticmethod
+    def gemm_t(A, B, a_mn=False, b_mn=False, epi="f32", out=None, ssp=None, C=0, eps=1e-6, cap=15.0, status=None):
+        """nc_op_gemm_t: A is [M, K] (a_mn False) or stored [K, M] (a_mn True); B is [N, K] or stored
+        [K, N]; returns epi(A . B^T) [M, N]."""
+        K, M = A.shape if a_mn else A.shape[::-1]
+        KB, N = B.shape if b_mn else B.shape[::-1]
+        if KB != K:
+            raise ValueError("A and B disagree on K")
+        if out is None:
+            dt = torch.bfloat16 if epi in ("bf16", "relu2_bf16", "softcap_bf16") else torch.float32
+            out = torch.empty((M, N), dtype=dt, device=A.device)
+        check(lib().nc_op_gemm_t(A.data_ptr(), B.data_ptr(), M, N, K, int(a_mn), int(b_mn), EPI[epi], out.data_ptr(),
+                                 out.shape[1], _ptr(ssp), C, eps, cap, _ptr(status), _stream_handle(None)),
+              "nc_op_gemm_t")
+        return out
+
+    @staticmethod
+    def lmhead_ce_grad(xf, wlm, targets, lse, inv_count, ssp=None, C=0, eps=1e-6, cap=15.0, status=None):
+        """bf16 [M, V]: rs * inv_count * (softmax(z) - onehot(target)) * (1 - (z/cap)^2)."""
+        M, K = xf.shape
+        V = wlm.shape[0]
+        out = torch.empty((M, V), dtype=torch.bfloat16, device=xf.device)
+        check(lib().nc_op_lmhead_ce_grad(xf.data_ptr(), wlm.data_ptr(), M, V, K, _ptr(ssp), eps, cap,
+                                         targets.data_ptr(), lse.data_ptr(), inv_count.data_ptr(), out.data_ptr(), V,
+                                         _ptr(status), _stream_handle(None)), "nc_op_lmhead_ce_grad")
+        return out
+
+    @staticmethod
+    def mlp_hidden_grad(dy, w, h, ssp=None, eps=1e-6, status=None):
+        """bf16 [M, F]: rs * (dy . w) * 2 sqrt(h), w the down projection's weight [C, F]."""
+        M, C = dy.shape
+        F = w.shape[1]
+        out = torch.empty((M, F), dtype=torch.bfloat16, device=dy.device)
+        check(lib().nc_op_mlp_hidden_grad(dy.data_ptr(), w.data_ptr(), M, F, C, _ptr(ssp), eps, h.data_ptr(),
+                                          out.data_ptr(), _ptr(status), _stream_handle(None)), "nc_op_mlp_hidden_grad")
+        return out
+
+    @staticmethod
+    def rms_backward(G, x, ssp, eps=1e-6, add=None):
+        """Returns (dx fp32, dx bf16) = G - rs^2 x mean(G x) (+ add)."""
+        M, C = G.shape
+        dxf = torch.empty((M, C), dtype=torch.float32, device=G.device)
+        dxb = torch.empty((M, C), dtype=torch.bfloat16, device=G.device)
+        check(lib().nc_op_rms_backward(G.data_ptr(), x.data_ptr(), ssp.data_ptr(), _ptr(add), M, C, eps,
+                                       dxf.data_ptr(), dxb.data_ptr(), _stream_handle(None)), "nc_op_rms_backward")
+        return dxf, dxb
 
     @staticmethod
     def test_wait_timeout(A, B, out, limit_ns, skip_tile, status):
@@ -227,18 +291,21 @@ class ops:
         return part, zt
 
     @staticmethod
-    def ce_finalize(part, zt, targets, V, token_bytes=None, status=None):
-        """Returns (loss [M], stats [2] = mean loss, bits per byte)."""
+    def ce_finalize(part, zt, targets, V, token_bytes=None, status=None, with_lse=False):
+        """Returns (loss [M], stats [2] = mean loss, bits per byte), and with with_lse also
+        (lse [M], inv_count [1])."""
         M = zt.shape[0]
         dev = zt.device
         loss = torch.empty((M,), dtype=torch.float32, device=dev)
         stats = torch.empty((2,), dtype=torch.float32, device=dev)
+        lse = torch.empty((M,), dtype=torch.float32, device=dev) if with_lse else None
+        invc = torch.empty((1,), dtype=torch.float32, device=dev) if with_lse else None
         nbytes = lib().nc_op_ce_scratch_bytes(M)
         scratch = torch.empty((max(nbytes, 8) // 8,), dtype=torch.float64, device=dev)
         check(lib().nc_op_ce_finalize(part.data_ptr(), zt.data_ptr(), targets.data_ptr(), M, V, _ptr(token_bytes),
-                                      loss.data_ptr(), stats.data_ptr(), scratch.data_ptr(), nbytes, _ptr(status),
-                                      _stream_handle(None)), "nc_op_ce_finalize")
-        return loss, stats
+                                      loss.data_ptr(), stats.data_ptr(), scratch.data_ptr(), nbytes, _ptr(lse),
+                                      _ptr(invc), _ptr(status), _stream_handle(None)), "nc_op_ce_finalize")
+        return (loss, stats, lse, invc) if with_lse else (loss, stats)
 
 
 _lib: Optional[ctypes.CDLL] = None
@@ -429,6 +496,41 @@ class Model:
                                     _stream_handle(stream)), "nc_forward_loss")
         return loss, stats
 
+    def loss_grad_tail(self, tokens: torch.Tensor, targets: torch.Tensor,
+                       token_bytes: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None):
+        """nc_forward_loss_grad_tail: the loss path, then the gradient of the mean loss with respect to
+        the lm_head and the last block's MLP down/up projections and attention output projection.
+        Returns (stats fp32 [2], {"lm_head", "wproj", "wfc", "wo"}: fp32 gradients shaped like the
+        weights)."""
+        for name, t in (("tokens", tokens), ("targets", targets)):
+            if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
+                raise ValueError(f"{name} must be a contiguous int32 CUDA tensor")
+        if targets.shape != tokens.shape:
+            raise ValueError("targets must have the shape of tokens")
+        B, T = tokens.shape
+        c = self.cfg
+        C, F, V, HD = c.n_embd, c.mlp_hidden, c.vocab_size, c.n_head * c.head_dim
+        dev = self.device
+        stats = torch.empty((2,), dtype=torch.float32, device=dev)
+        g = {"lm_head": torch.empty((V, C), dtype=torch.float32, device=dev),
+             "wproj": torch.empty((C, F), dtype=torch.float32, device=dev),
+             "wfc": torch.empty((F, C), dtype=torch.float32, device=dev),
+             "wo": torch.empty((C, HD), dtype=torch.float32, device=dev)}
+        if token_bytes is not None:
+            _check_out(token_bytes, (V,), torch.int32, tokens.device, "token_bytes")
+        key = (B, T, "grad_tail")
+        if key not in self._ws:
+            n = ctypes.c_size_t()
+            check(lib().nc_workspace_bytes_grad_tail(self.handle, B, T, ctypes.byref(n)), "nc_workspace_bytes_grad_tail")
+            self._ws[key] = torch.empty(n.value, dtype=torch.uint8, device=dev)
+        ws = self._ws[key]
+        check(lib().nc_forward_loss_grad_tail(self.handle, tokens.data_ptr(), targets.data_ptr(), B, T,
+                                              _ptr(token_bytes), stats.data_ptr(), g["lm_head"].data_ptr(),
+                                              g["wproj"].data_ptr(), g["wfc"].data_ptr(), g["wo"].data_ptr(),
+                                              ws.data_ptr(), ws.numel(), _stream_handle(stream)),
+              "nc_forward_loss_grad_tail")
+        return stats, g
+
     def kv_cache(self, B: int, T_max: int) -> torch.Tensor:
         """A device buffer for the KV cache of B rows and up to T_max positions."""
         n = ctypes.c_size_t()
@@ -500,6 +602,9 @@ class Model:
             check(lib().nc_timing_read(self.handle, k, ctypes.byref(ms), ctypes.byref(n)), "nc_timing_read")
             out[name] = (ms.value, n.value)
         return out
+
+    def grad_tail_launch_count(self) -> int:
+        return lib().nc_grad_tail_launch_count(self.handle)
 
     def launch_count(self, loss: bool = False, kv: bool = False) -> int:
         fn = lib().nc_forward_loss_launch_count if loss else (lib().nc_kv_launch_count if kv

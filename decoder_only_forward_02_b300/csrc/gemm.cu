@@ -44,6 +44,22 @@
 //                    gate = scale * sigmoid(rs * (x . w_gate)) -- the gate is a contraction, so it
 //                    runs on the tensor cores with the projection it belongs to
 //   EPI_BF16         plain store (used by tests of the mainloop)
+// and the backward of the loss and the MLP (the gradient of the mean next-token cross-entropy,
+// "NanoChat基础训练报告", loss progression table: the training loss):
+//   EPI_F32          rs * acc in fp32: weight gradients and input gradients before their RMSNorm
+//   EPI_CE_GRAD      the lm_head recomputed with the forward's row scale and soft-cap, written as
+//                    rs * (softmax(z) - onehot(target)) * (1 - (z/cap)^2) / (rows counted) in bf16:
+//                    the gradient at its pre-cap output, with the row scale the weight gradient needs
+//   EPI_DRELU2       rs * acc * 2 sqrt(h): the squared ReLU's derivative, from the forward's h
+//
+// Operand layouts: A and B are K-contiguous (nn.Linear weights, token-major activations) unless
+// GemmEpi::a_mn / b_mn mark one as MN-contiguous (stored [K][M] or [K][N]), as the backward's
+// products need: a weight gradient dW = G^T X contracts over tokens, so both of its operands are
+// token-major [K][rows]; an input gradient dX = G W multiplies by the weight itself, [K][N].  An
+// MN-contiguous stage is two TMA boxes [64 k][64 rows] with 128-byte swizzle, described to the
+// MMA with the MN-major descriptor (8-row groups 1024 B apart, 64-row blocks 8 KB apart) and the
+// instruction descriptor's transpose bit for that operand.  K may be ragged: TMA fills the k
+// positions past the end with zeros.
 // The residual-stream updates of the output projections are in gemm_resid.cu.
 #include "internal.h"
 #include "ptx.cuh"
@@ -60,6 +76,8 @@ constexpr int B_ROWS = BN / 2;     // rows of B (columns of D) loaded by each CT
 constexpr int BK = 64;
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = B_ROWS * BK * 2;
+constexpr int MN_BLOCK = 64 * BK * 2;   // an MN-contiguous operand's [64 k][64 rows] box (8 KB)
+static_assert(A_BYTES == 2 * MN_BLOCK && B_BYTES == 2 * MN_BLOCK, "two MN boxes per operand stage");
 constexpr int NUM_EPI_WARPS = 8;
 constexpr int EPI_WARP0 = 4;                    // epilogue warps 4..11 (warpgroups 1 and 2)
 constexpr int THREADS = 32 * (EPI_WARP0 + NUM_EPI_WARPS);
@@ -80,7 +98,8 @@ constexpr int SLAB_BYTES = 2 * SLAB_BUF; // two per epilogue warp, used alternat
 // The cross-entropy epilogue stores no tile at all: no staging buffers, a 7-stage ring.
 template <int KIND, int D>
 struct Cfg {
-  static constexpr bool LSU_STORE = KIND == EPI_RELU2_BF16 || KIND == EPI_SOFTCAP_F32 || KIND == EPI_SOFTCAP_BF16;
+  static constexpr bool LSU_STORE = KIND == EPI_RELU2_BF16 || KIND == EPI_SOFTCAP_F32 || KIND == EPI_SOFTCAP_BF16 ||
+                                    KIND == EPI_F32 || KIND == EPI_CE_GRAD || KIND == EPI_DRELU2;
   static constexpr int STAGES = KIND == EPI_CE ? 7 : (LSU_STORE ? 6 : 5);
   static constexpr int SLAB_WARP = KIND == EPI_CE ? 0 : (LSU_STORE ? SLAB_BUF : SLAB_BYTES);   // staging bytes per warp
   static constexpr int OFF_SLAB = STAGES * (A_BYTES + B_BYTES);
@@ -227,12 +246,14 @@ __host__ __device__ __forceinline__ int num_col_tiles(int kind, int N, int H, in
 struct PreRaw {
   float ss[MAX_NCG];
   int tok;
+  float lse;
 };
 
 struct EpiPre {
   float rs = 1.f;              // input RMSNorm row scale
   int tok = -1;                // EPI_QKV: token id of the row on a value-embedding head's tile, else -1;
-                               // EPI_CE: the row's target
+                               // EPI_CE, EPI_CE_GRAD: the row's target
+  float lse = 0.f;             // EPI_CE_GRAD: log sum exp of the row's logits
 };
 
 template <int KIND>
@@ -246,7 +267,8 @@ __device__ __forceinline__ void pre_issue(PreRaw& raw, int lane, int m0w, int M,
     for (int g = 0; g < MAX_NCG; ++g)
       if (g < ep.ncg) raw.ss[g] = p[g];
   }
-  if constexpr (KIND == EPI_CE) raw.tok = ep.targets[m];
+  if constexpr (KIND == EPI_CE || KIND == EPI_CE_GRAD) raw.tok = ep.targets[m];
+  if constexpr (KIND == EPI_CE_GRAD) raw.lse = ep.ce_lse[m];
   if constexpr (KIND == EPI_QKV) raw.tok = ct.vhead >= 0 ? ep.tokens[m] : -1;
 }
 
@@ -256,7 +278,8 @@ __device__ __forceinline__ EpiPre pre_finish(const PreRaw& raw, int lane, int m0
   EpiPre p;
   const int m = m0w + lane;
   if (m >= M) return p;
-  if constexpr (KIND == EPI_CE) p.tok = raw.tok;
+  if constexpr (KIND == EPI_CE || KIND == EPI_CE_GRAD) p.tok = raw.tok;
+  if constexpr (KIND == EPI_CE_GRAD) p.lse = raw.lse;
   if (ep.ssp_in != nullptr) {
     float ss = 0.f;
 #pragma unroll
@@ -300,15 +323,27 @@ __device__ __forceinline__ void lsu_store_box(const uint8_t* buf, void* out, siz
 }
 
 // bf16 outputs of 64-column boxes: plain (TMA store), relu(rs * acc)^2 (MLP up projection, squared
-// ReLU) or cap * tanh(rs * acc / cap) (the lm_head's soft-capped logits in bf16); the last two are
-// stored row-coalesced from the single staging buffer, the logits with streaming stores.
-enum Bf16Mode { BF16_PLAIN = 0, BF16_RELU2 = 1, BF16_SOFTCAP = 2 };
+// ReLU), cap * tanh(rs * acc / cap) (the lm_head's soft-capped logits in bf16), the cross-entropy
+// gradient at the lm_head's pre-cap output (EPI_CE_GRAD) or the squared ReLU's backward
+// rs * acc * 2 sqrt(h) (EPI_DRELU2); all but the first are stored row-coalesced from the single
+// staging buffer, the logits with streaming stores.
+enum Bf16Mode { BF16_PLAIN = 0, BF16_RELU2 = 1, BF16_SOFTCAP = 2, BF16_CEGRAD = 3, BF16_DRELU2 = 4 };
 
 template <int MODE>
 __device__ __forceinline__ void epi_bf16(uint32_t taddr, uint32_t tempty, int lane, int m0w, int n0, int M, int N,
                                          const GemmEpi& ep, const OutMaps& om, Slab& sl, const EpiPre& pre) {
   const float rs = pre.rs;
   const float cap = ep.cap, sc = rs / cap;
+  const int m = m0w + lane;
+  // EPI_CE_GRAD: exp(z - lse) = 2^(log2(e) * (cap * th - lse)); rows without a counted target
+  // get scale 0.  The exponential and tanh are the approximations the cross-entropy pass used.
+  float gscale = 0.f, l2e_cap = 0.f, lse_l2 = 0.f;
+  if constexpr (MODE == BF16_CEGRAD) {
+    const bool counted = m < M && pre.tok >= 0 && pre.tok < N;
+    gscale = counted ? rs * __ldg(ep.inv_count) : 0.f;
+    l2e_cap = cap * 1.4426950408889634f;
+    lse_l2 = pre.lse * 1.4426950408889634f;
+  }
 #pragma unroll 1
   for (int ch = 0; ch < 2; ++ch) {
     const int c0 = n0 + ch * 64;
@@ -316,8 +351,16 @@ __device__ __forceinline__ void epi_bf16(uint32_t taddr, uint32_t tempty, int la
     uint32_t r[32], r2[32];
     tmem_ld32(taddr + ch * 64, r);
     tmem_ld32(taddr + ch * 64 + 32, r2);
+    uint4 hv[8];
+    if constexpr (MODE == BF16_DRELU2) {   // the forward's relu(u)^2 of this row's 64 columns
+      const uint4* hp = reinterpret_cast<const uint4*>(ep.h_in + static_cast<size_t>(m) * ep.ldo + c0);
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        hv[c] = (m < M && c0 + c * 8 < N) ? __ldg(hp + c) : make_uint4(0u, 0u, 0u, 0u);
+    }
     tmem_ld_wait(r);
     tmem_ld_wait(r2);
+    const int tcol = pre.tok - c0;   // EPI_CE_GRAD: the target's column within this box
     uint4 o[8];
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
@@ -331,6 +374,14 @@ __device__ __forceinline__ void epi_bf16(uint32_t taddr, uint32_t tempty, int la
           t = t * t;
         } else if constexpr (MODE == BF16_SOFTCAP) {
           t = cap * tanh_approx(t * sc);
+        } else if constexpr (MODE == BF16_CEGRAD) {
+          const float th = tanh_approx(t * sc);
+          const float p = ex2_approx(fmaf(th, l2e_cap, -lse_l2));
+          t = (p - (e == tcol ? 1.f : 0.f)) * fmaf(-th, th, 1.f) * gscale;
+        } else if constexpr (MODE == BF16_DRELU2) {
+          const __nv_bfloat162 h2 = reinterpret_cast<const __nv_bfloat162*>(&hv[c])[j >> 1];
+          const float hval = (j & 1) ? __high2float(h2) : __low2float(h2);
+          t = t * rs * 2.f * sqrtf(hval);
         }
         a[j] = t;
       }
@@ -362,11 +413,13 @@ __device__ __forceinline__ void epi_bf16(uint32_t taddr, uint32_t tempty, int la
   release_acc(lane, tempty);
 }
 
-// cap * tanh(rs * acc / cap), fp32 (logit soft-cap of the lm_head).
-__device__ __forceinline__ void epi_softcap(uint32_t taddr, uint32_t tempty, int lane, int m0w, int n0, int M,
-                                            int N, const GemmEpi& ep, Slab& sl, const EpiPre& pre) {
+// fp32 outputs: cap * tanh(rs * acc / cap) (logit soft-cap of the lm_head, streaming stores) or
+// rs * acc (EPI_F32: the backward's weight and input gradients).
+template <bool SOFTCAP>
+__device__ __forceinline__ void epi_f32out(uint32_t taddr, uint32_t tempty, int lane, int m0w, int n0, int M,
+                                           int N, const GemmEpi& ep, Slab& sl, const EpiPre& pre) {
   const float cap = ep.cap;
-  const float sc = pre.rs / cap;
+  const float sc = SOFTCAP ? pre.rs / cap : pre.rs;
 #pragma unroll 1
   for (int ch = 0; ch < 4; ++ch) {
     const int c0 = n0 + ch * 32;
@@ -377,10 +430,13 @@ __device__ __forceinline__ void epi_softcap(uint32_t taddr, uint32_t tempty, int
     uint4 o[8];
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
-      o[c] = make_uint4(__float_as_uint(cap * tanh_approx(__uint_as_float(r[c * 4 + 0]) * sc)),
-                        __float_as_uint(cap * tanh_approx(__uint_as_float(r[c * 4 + 1]) * sc)),
-                        __float_as_uint(cap * tanh_approx(__uint_as_float(r[c * 4 + 2]) * sc)),
-                        __float_as_uint(cap * tanh_approx(__uint_as_float(r[c * 4 + 3]) * sc)));
+      float v[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float a = __uint_as_float(r[c * 4 + j]) * sc;
+        v[j] = SOFTCAP ? cap * tanh_approx(a) : a;
+      }
+      o[c] = make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]), __float_as_uint(v[3]));
     }
     // Through the staging buffer to row-coalesced streaming stores (4 rows x 128 B per
     // instruction): the logits are written once and never re-read, and leaving them to the
@@ -388,7 +444,8 @@ __device__ __forceinline__ void epi_softcap(uint32_t taddr, uint32_t tempty, int
     __syncwarp();
     sl.put_row(lane, o);
     __syncwarp();
-    lsu_store_box(sl.buf(), ep.out, static_cast<size_t>(ep.ldo) * 4, m0w, static_cast<size_t>(c0) * 4, M, lane, true);
+    lsu_store_box(sl.buf(), ep.out, static_cast<size_t>(ep.ldo) * 4, m0w, static_cast<size_t>(c0) * 4, M, lane,
+                  SOFTCAP);
   }
   release_acc(lane, tempty);
 }
@@ -596,7 +653,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t rank = cluster_ctarank();            // 0: pair leader (issues the MMAs)
   const int pair = static_cast<int>(blockIdx.x) >> 1, npairs = static_cast<int>(gridDim.x) >> 1;
   const int num_m = (M + PAIR_M - 1) / PAIR_M, num_n = num_col_tiles(KIND, N, ep.H, ep.Hkv, ep.D, ep.vgate);
-  const int num_tiles = num_m * num_n, kblocks = K / BK;
+  const int num_tiles = num_m * num_n, kblocks = (K + BK - 1) / BK;   // a ragged last k-block is zero-filled
+  const bool a_mn = ep.a_mn != 0, b_mn = ep.b_mn != 0;
   int* status = ep.status;
   const uint64_t wlim = ep.wait_ns;
 
@@ -656,9 +714,22 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           const uint32_t fb = mapa_shared(smem_u32(&ctl->full[s]), 0);   // the leader's barrier
           if (rank == 0) mbar_arrive_expect_tx(smem_u32(&ctl->full[s]), 2 * (A_BYTES + b_bytes));
-          tma_load_2d_pair_hint(sA + s * A_BYTES, &tmA, fb, kb * BK, mb * PAIR_M + static_cast<int>(rank) * BM, pol_a);
-          tma_load_2d_pair_hint(sB + s * B_BYTES, vt ? &tmBv : &tmB, fb, kb * BK,
-                                ct.col0 + static_cast<int>(rank) * (ct.width / 2), pol_b);
+          const int a_row = mb * PAIR_M + static_cast<int>(rank) * BM;
+          const int b_row = ct.col0 + static_cast<int>(rank) * (ct.width / 2);
+          // K-contiguous: one box [rows][64 k].  MN-contiguous: two boxes [64 k][64 rows], the
+          // second (rows 64..127) MN_BLOCK bytes after the first.
+          if (!a_mn) {
+            tma_load_2d_pair_hint(sA + s * A_BYTES, &tmA, fb, kb * BK, a_row, pol_a);
+          } else {
+            tma_load_2d_pair_hint(sA + s * A_BYTES, &tmA, fb, a_row, kb * BK, pol_a);
+            tma_load_2d_pair_hint(sA + s * A_BYTES + MN_BLOCK, &tmA, fb, a_row + 64, kb * BK, pol_a);
+          }
+          if (!b_mn) {
+            tma_load_2d_pair_hint(sB + s * B_BYTES, vt ? &tmBv : &tmB, fb, kb * BK, b_row, pol_b);
+          } else {
+            tma_load_2d_pair_hint(sB + s * B_BYTES, &tmB, fb, b_row, kb * BK, pol_b);
+            tma_load_2d_pair_hint(sB + s * B_BYTES + MN_BLOCK, &tmB, fb, b_row + 64, kb * BK, pol_b);
+          }
           ++it;
         }
       }
@@ -674,7 +745,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int tile = pair; tile < num_tiles && ok; tile += npairs, ++tc) {
         int mb, nb;
         tile_coords(tile, num_m, num_n, grp, mb, nb);
-        const uint32_t idesc = idesc_bf16_f32(PAIR_M, col_tile<KIND>(nb, N, ep).width);
+        const uint32_t idesc = idesc_bf16_f32(PAIR_M, col_tile<KIND>(nb, N, ep).width) | (a_mn ? 1u << 15 : 0u) |
+                               (b_mn ? 1u << 16 : 0u);
         const uint32_t a = tc & 1, aph = (tc >> 1) & 1;
         if (!mbar_wait_cluster(smem_u32(&ctl->tempty[a]), aph ^ 1, abort, status, wlim)) break;
         tc_fence_after();
@@ -688,8 +760,12 @@ __global__ void __launch_bounds__(THREADS, 1)
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
-            umma_bf16_pair(d_tmem, sdesc_kmajor_sw128(sA + s * A_BYTES + kk * 32),
-                           sdesc_kmajor_sw128(sB + s * B_BYTES + kk * 32), idesc, (kb | kk) != 0 ? 1u : 0u);
+            // a k-step of 16: 32 B along a K-contiguous row, or 16 rows of 128 B of an MN-contiguous box
+            const uint64_t ad = a_mn ? sdesc_mnmajor_sw128(sA + s * A_BYTES + kk * 16 * 128, MN_BLOCK)
+                                     : sdesc_kmajor_sw128(sA + s * A_BYTES + kk * 32);
+            const uint64_t bd = b_mn ? sdesc_mnmajor_sw128(sB + s * B_BYTES + kk * 16 * 128, MN_BLOCK)
+                                     : sdesc_kmajor_sw128(sB + s * B_BYTES + kk * 32);
+            umma_bf16_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
           }
           umma_commit_pair(smem_u32(&ctl->empty[s]), 0x3);
           ++it;
@@ -741,7 +817,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint32_t tbase = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + a * BN;
       const uint32_t taddr = tbase + group * 128;
       const uint32_t tempty = mapa_shared(smem_u32(&ctl->tempty[a]), 0);
-      if constexpr (KIND == EPI_SOFTCAP_F32) epi_softcap(taddr, tempty, lane, m0w, n0, M, N, ep, sl, pre);
+      if constexpr (KIND == EPI_SOFTCAP_F32) epi_f32out<true>(taddr, tempty, lane, m0w, n0, M, N, ep, sl, pre);
+      else if constexpr (KIND == EPI_F32) epi_f32out<false>(taddr, tempty, lane, m0w, n0, M, N, ep, sl, pre);
+      else if constexpr (KIND == EPI_CE_GRAD) epi_bf16<BF16_CEGRAD>(taddr, tempty, lane, m0w, n0, M, N, ep, om, sl, pre);
+      else if constexpr (KIND == EPI_DRELU2) epi_bf16<BF16_DRELU2>(taddr, tempty, lane, m0w, n0, M, N, ep, om, sl, pre);
       else if constexpr (KIND == EPI_CE) epi_ce(taddr, tempty, lane, m0w, n0, M, N, ep, pre);
       else if constexpr (KIND == EPI_QKV) {
         if (ct.vhead >= 0) epi_vgate<D>(tbase, tempty, lane, m0w, group, ct.vhead, ep, om, sl, pre);
@@ -819,10 +898,20 @@ cudaError_t launch_kind(const CUtensorMap& ta, const CUtensorMap& tb, const CUte
 cudaError_t launch_gemm(const bf16* A, const bf16* B, int M, int N, int K, const GemmEpi& epi,
                         int num_sms, cudaStream_t stream) {
   const bool vgate = epi.kind == EPI_QKV && epi.vgate;
-  if (M <= 0 || N <= 0 || K <= 0 || K % BK != 0 || N % (vgate ? 16 : 32) != 0) return cudaErrorInvalidValue;
+  const bool a_mn = epi.a_mn != 0, b_mn = epi.b_mn != 0;
+  if (M <= 0 || N <= 0 || K <= 0 || N % (vgate ? 16 : 32) != 0) return cudaErrorInvalidValue;
+  if ((epi.a_mn != 0 && epi.a_mn != 1) || (epi.b_mn != 0 && epi.b_mn != 1)) return cudaErrorInvalidValue;
+  // rows of a stored operand are 16-byte multiples (TMA strides); the q|k|v layout is K-contiguous
+  if ((!a_mn || !b_mn) && K % 8 != 0) return cudaErrorInvalidValue;
+  if ((a_mn && M % 8 != 0) || (b_mn && N % 8 != 0) || (epi.kind == EPI_QKV && (a_mn || b_mn)))
+    return cudaErrorInvalidValue;
+  const uint64_t Ku = static_cast<uint64_t>(K);
   CUtensorMap ta, tb, tbv;
-  if (!make_tmap_bf16_2d(&ta, A, K, M, static_cast<uint64_t>(K) * 2, BK, BM)) return cudaErrorInvalidValue;
-  if (!make_tmap_bf16_2d(&tb, B, K, N, static_cast<uint64_t>(K) * 2, BK, B_ROWS)) return cudaErrorInvalidValue;
+  const bool ok_a = a_mn ? make_tmap_bf16_2d(&ta, A, M, Ku, static_cast<uint64_t>(M) * 2, 64, BK)
+                         : make_tmap_bf16_2d(&ta, A, Ku, M, Ku * 2, BK, BM);
+  const bool ok_b = b_mn ? make_tmap_bf16_2d(&tb, B, N, Ku, static_cast<uint64_t>(N) * 2, 64, BK)
+                         : make_tmap_bf16_2d(&tb, B, Ku, N, Ku * 2, BK, B_ROWS);
+  if (!ok_a || !ok_b) return cudaErrorInvalidValue;
   tbv = tb;
   OutMaps om;
   const uint64_t Mu = static_cast<uint64_t>(M);
@@ -832,7 +921,16 @@ cudaError_t launch_gemm(const bf16* A, const bf16* B, int M, int N, int K, const
       ok = epi.targets != nullptr && epi.ce_part != nullptr && epi.ce_zt != nullptr && epi.cap > 0.f;
       break;
     case EPI_SOFTCAP_F32:   // written with plain coalesced stores (16-byte aligned rows)
-      ok = (reinterpret_cast<uintptr_t>(epi.out) % 16 == 0) && epi.ldo % 4 == 0;
+    case EPI_F32:
+      ok = (reinterpret_cast<uintptr_t>(epi.out) % 16 == 0) && epi.ldo % 4 == 0 && epi.ldo >= N;
+      break;
+    case EPI_CE_GRAD:
+      ok = epi.targets != nullptr && epi.ce_lse != nullptr && epi.inv_count != nullptr && epi.cap > 0.f &&
+           (reinterpret_cast<uintptr_t>(epi.out) % 16 == 0) && epi.ldo % 8 == 0 && epi.ldo >= N;
+      break;
+    case EPI_DRELU2:
+      ok = epi.h_in != nullptr && (reinterpret_cast<uintptr_t>(epi.h_in) % 16 == 0) &&
+           (reinterpret_cast<uintptr_t>(epi.out) % 16 == 0) && epi.ldo % 8 == 0 && epi.ldo >= N;
       break;
     case EPI_BF16:
       ok = make_tmap_bf16_2d(&om.o0, epi.out, N, Mu, static_cast<uint64_t>(epi.ldo) * 2, 64, 32);
@@ -866,6 +964,9 @@ cudaError_t launch_gemm(const bf16* A, const bf16* B, int M, int N, int K, const
     case EPI_SOFTCAP_F32: return launch_kind<EPI_SOFTCAP_F32, 0>(ta, tb, tbv, om, M, N, K, epi, num_sms, stream);
     case EPI_SOFTCAP_BF16: return launch_kind<EPI_SOFTCAP_BF16, 0>(ta, tb, tbv, om, M, N, K, epi, num_sms, stream);
     case EPI_CE: return launch_kind<EPI_CE, 0>(ta, tb, tbv, om, M, N, K, epi, num_sms, stream);
+    case EPI_F32: return launch_kind<EPI_F32, 0>(ta, tb, tbv, om, M, N, K, epi, num_sms, stream);
+    case EPI_CE_GRAD: return launch_kind<EPI_CE_GRAD, 0>(ta, tb, tbv, om, M, N, K, epi, num_sms, stream);
+    case EPI_DRELU2: return launch_kind<EPI_DRELU2, 0>(ta, tb, tbv, om, M, N, K, epi, num_sms, stream);
     case EPI_QKV:
       if (epi.D == 128) return launch_kind<EPI_QKV, 128>(ta, tb, tbv, om, M, N, K, epi, num_sms, stream);
       return launch_kind<EPI_QKV, 64>(ta, tb, tbv, om, M, N, K, epi, num_sms, stream);

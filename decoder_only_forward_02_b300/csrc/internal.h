@@ -22,6 +22,9 @@ enum EpiKind : int {
   EPI_QKV = 4,          // q|k|v split, RoPE + RMSNorm on q and k, value-embedding gate on v
   EPI_CE = 5,           // cross-entropy partials of z = cap * tanh(rs * acc / cap), no logits
   EPI_SOFTCAP_BF16 = 6, // out(bf16) = cap * tanh(rs * acc / cap)
+  EPI_F32 = 7,          // out(f32) = rs * acc
+  EPI_CE_GRAD = 8,      // out(bf16) = gradient of the mean cross-entropy at the lm_head's pre-cap output
+  EPI_DRELU2 = 9,       // out(bf16) = rs * acc * 2 sqrt(h)   (the squared ReLU's derivative)
 };
 
 // Columns covered by one partial sum of squares (one epilogue thread's share of a row).
@@ -41,14 +44,20 @@ struct GemmEpi {
   unsigned long long wait_ns = 2000000000ull;
   int test_skip_tile = -1;
 
-  // Row scale of the consuming epilogues (RELU2, SOFTCAP, QKV): rs[m] = 1 / sqrt(sum_g
+  // Operand layouts.  0: K contiguous, A[M][K] and B[N][K] (nn.Linear weights and activations);
+  // 1: M (or N) contiguous, A stored as [K][M], B as [K][N] -- the transposed operands of the
+  // backward's products (a weight gradient contracts over tokens, an input gradient multiplies
+  // by the weight itself).  Both stored densely (row pitch = the contiguous extent).
+  int a_mn = 0, b_mn = 0;
+
+  // Row scale of the consuming epilogues (RELU2, SOFTCAP, QKV, F32, CE_GRAD, DRELU2): rs[m] = 1 / sqrt(sum_g
   // ssp[m, g] / ncols + eps), ssp fp32 [M, ncg] partial sums of squares; ssp == null -> rs = 1.
   const float* ssp_in = nullptr;
   int ncg = 0;            // partial sums per row (ncols / SS_GROUP)
   float inv_ncols = 0.f;  // 1 / ncols
   float eps = 1e-6f;
 
-  // EPI_BF16 / EPI_RELU2_BF16 / EPI_SOFTCAP_F32 / EPI_SOFTCAP_BF16
+  // EPI_BF16 / EPI_RELU2_BF16 / EPI_SOFTCAP_F32 / EPI_SOFTCAP_BF16 / EPI_F32 / EPI_CE_GRAD / EPI_DRELU2
   void* out = nullptr;
   int ldo = 0;
   float cap = 15.f;
@@ -88,6 +97,17 @@ struct GemmEpi {
   const int32_t* targets = nullptr;
   float* ce_part = nullptr;
   float* ce_zt = nullptr;
+
+  // EPI_CE_GRAD (uses ssp_in / cap / targets): with z = cap * tanh(u / cap), u = rs * acc,
+  //   out[m, n] = rs * inv_count * (exp(z - ce_lse[m]) - [n == targets[m]]) * (1 - (z / cap)^2)
+  // -- d(mean loss)/du times the row's RMSNorm scale, which the weight gradient needs -- and 0 on
+  // rows whose target lies outside [0, N).  ce_lse[m] = log sum_n exp(z[m, n]); inv_count: one
+  // float in device memory, 1 / (rows counted).
+  const float* ce_lse = nullptr;
+  const float* inv_count = nullptr;
+  // EPI_DRELU2 (uses ssp_in): h_in bf16 [M, ldo] holds relu(u)^2 of the forward, so relu(u) =
+  // sqrt(h) and out = rs * acc * 2 sqrt(h).
+  const bf16* h_in = nullptr;
 };
 
 
@@ -142,8 +162,9 @@ inline bool make_tmap_bf16_2d(CUtensorMap* map, const void* ptr, uint64_t inner,
                       box_inner, box_outer);
 }
 
-// C[M, N] = epi(A[M, K] . B[N, K]^T); A, B bf16 row-major (K contiguous).
-// Requires K % 64 == 0, N % 32 == 0, 16-byte aligned rows.
+// C[M, N] = epi(A[M, K] . B[N, K]^T); A, B bf16, K contiguous unless epi.a_mn / epi.b_mn.
+// Requires N % 32 == 0, 16-byte aligned rows (K % 8 == 0 for a K-contiguous operand, M % 8 or
+// N % 8 == 0 for an MN-contiguous one); K may be ragged (the last k-block is zero-filled).
 cudaError_t launch_gemm(const bf16* A, const bf16* B, int M, int N, int K, const GemmEpi& epi,
                         int num_sms, cudaStream_t stream);
 
@@ -168,10 +189,19 @@ cudaError_t launch_rope_table(float2* table, int T, int D, float base, cudaStrea
 // counted rows, stats[1] = bits per byte (sum of the losses of rows whose target has a nonzero
 // byte count, over ln 2 times the sum of those byte counts; NaN without token_bytes or bytes).
 // scratch holds ce_scratch_doubles(M) doubles.  loss may be null.
+// lse (optional) receives log S per counted row (0 on ignored rows) and inv_count (optional, one
+// float) 1 / (rows counted), 0 when none is counted: the inputs of EPI_CE_GRAD.
 int ce_scratch_doubles(int M);
 cudaError_t launch_ce_finalize(const float* part, const float* zt, const int32_t* targets, int M, int G, int V,
                                const int32_t* token_bytes, float* loss, float* stats, double* scratch,
-                               int* status, cudaStream_t stream);
+                               int* status, cudaStream_t stream, float* lse = nullptr,
+                               float* inv_count = nullptr);
+
+// Backward of the weightless RMSNorm xn = rs * x (rs = 1 / sqrt(mean x^2 + eps), from the partial
+// sums ssp [M, C / 128]) given G = rs * dL/dxn:  dx = G - rs^2 * x * mean(G * x)  (+ add, if set).
+// dx goes to dx_f32 (if set) and as bf16 to dx_b16 (if set); rows of C fp32 elements, C % 128 == 0.
+cudaError_t launch_rms_backward(const float* G, const float* x, const float* ssp, const float* add, int M, int C,
+                                float eps, float* dx_f32, bf16* dx_b16, cudaStream_t stream);
 
 // y[M, H*D] = windowed causal GQA attention of q [M, H*D], k/v [M, Hkv*D].
 cudaError_t launch_attention(const bf16* q, const bf16* k, const bf16* v, int B, int T, int H,

@@ -9,7 +9,8 @@
 //   ce_rows   one thread per row: S = sum over the G partial sums (group-major, so a warp
 //             reads 32 consecutive rows of one group), loss = log S - z[target]; per block,
 //             the sums needed by the statistics, reduced in a fixed order.
-//   ce_stats  one block: the per-block sums, in a fixed order -> mean loss and bits per byte.
+//   ce_stats  one block: the per-block sums, in a fixed order -> mean loss and bits per byte
+//             (and 1 / rows counted, for the gradient pass).
 // Both reductions run in fp64 and in a fixed order, so the statistics are bitwise repeatable.
 #include "internal.h"
 #include "ptx.cuh"
@@ -45,7 +46,7 @@ __device__ __forceinline__ void block_sum(double (&v)[NSTAT], double (*sh)[CE_TH
 __global__ void __launch_bounds__(CE_THREADS)
     ce_rows_kernel(const float* __restrict__ part, const float* __restrict__ zt, const int32_t* __restrict__ targets,
                    int M, int G, int V, const int32_t* __restrict__ token_bytes, float* __restrict__ loss,
-                   double* __restrict__ block_stats, int* status) {
+                   double* __restrict__ block_stats, int* status, float* __restrict__ lse) {
   __shared__ double sh[NSTAT][CE_THREADS / 32];
   griddep_wait();   // the lm_head's partials are complete and visible
   griddep_launch();
@@ -53,7 +54,7 @@ __global__ void __launch_bounds__(CE_THREADS)
   double v[NSTAT] = {0.0, 0.0, 0.0, 0.0};
   if (m < M) {
     const int t = targets[m];
-    float l = 0.f;
+    float l = 0.f, ls = 0.f;
     if (t >= 0 && t < V) {
       float s[4] = {0.f, 0.f, 0.f, 0.f};
       int g = 0;
@@ -61,7 +62,8 @@ __global__ void __launch_bounds__(CE_THREADS)
 #pragma unroll
         for (int u = 0; u < 4; ++u) s[u] += part[static_cast<size_t>(g + u) * M + m];
       for (; g < G; ++g) s[0] += part[static_cast<size_t>(g) * M + m];
-      l = logf((s[0] + s[1]) + (s[2] + s[3])) - zt[m];
+      ls = logf((s[0] + s[1]) + (s[2] + s[3]));
+      l = ls - zt[m];
       v[0] = l;
       v[1] = 1.0;
       if (token_bytes != nullptr) {
@@ -75,6 +77,7 @@ __global__ void __launch_bounds__(CE_THREADS)
       record_error(status, NC_ERR_TOKEN_RANGE);   // ignored like a negative target
     }
     if (loss != nullptr) loss[m] = l;
+    if (lse != nullptr) lse[m] = ls;
   }
   block_sum(v, sh);
   if (threadIdx.x == 0)
@@ -83,7 +86,8 @@ __global__ void __launch_bounds__(CE_THREADS)
 }
 
 __global__ void __launch_bounds__(CE_THREADS)
-    ce_stats_kernel(const double* __restrict__ block_stats, int nblocks, float* __restrict__ stats) {
+    ce_stats_kernel(const double* __restrict__ block_stats, int nblocks, float* __restrict__ stats,
+                    float* __restrict__ inv_count) {
   __shared__ double sh[NSTAT][CE_THREADS / 32];
   griddep_wait();
   griddep_launch();
@@ -95,6 +99,7 @@ __global__ void __launch_bounds__(CE_THREADS)
   if (threadIdx.x == 0) {
     stats[0] = v[1] > 0.0 ? static_cast<float>(v[0] / v[1]) : NAN;
     stats[1] = v[3] > 0.0 ? static_cast<float>(v[2] / (0.69314718055994530942 * v[3])) : NAN;
+    if (inv_count != nullptr) *inv_count = v[1] > 0.0 ? static_cast<float>(1.0 / v[1]) : 0.f;
   }
 }
 
@@ -118,15 +123,15 @@ int ce_scratch_doubles(int M) { return NSTAT * ((M + CE_THREADS - 1) / CE_THREAD
 
 cudaError_t launch_ce_finalize(const float* part, const float* zt, const int32_t* targets, int M, int G, int V,
                                const int32_t* token_bytes, float* loss, float* stats, double* scratch,
-                               int* status, cudaStream_t stream) {
+                               int* status, cudaStream_t stream, float* lse, float* inv_count) {
   if (part == nullptr || zt == nullptr || targets == nullptr || stats == nullptr || scratch == nullptr || M < 1 ||
       G < 1 || V < 1)
     return cudaErrorInvalidValue;
   const int nblocks = (M + CE_THREADS - 1) / CE_THREADS;
   cudaError_t e = launch_pdl(ce_rows_kernel, nblocks, stream, part, zt, targets, M, G, V, token_bytes, loss,
-                             scratch, status);
+                             scratch, status, lse);
   if (e != cudaSuccess) return e;
-  return launch_pdl(ce_stats_kernel, 1, stream, static_cast<const double*>(scratch), nblocks, stats);
+  return launch_pdl(ce_stats_kernel, 1, stream, static_cast<const double*>(scratch), nblocks, stats, inv_count);
 }
 
 }  // namespace nc

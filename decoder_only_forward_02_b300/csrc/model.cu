@@ -96,6 +96,14 @@ struct Layout {
   size_t x0, x, xm, xb, q, k, v, y, h, ssp, end;
 };
 
+// Where the last block's MLP down projection writes the lm_head's input when the backward runs:
+// its own buffers, so that the last block's MLP input (x, xb, ssp) survives the forward.
+struct TailOut {
+  float* xf;     // fp32 [M, C] x after the final backout (the final RMSNorm's input)
+  nc::bf16* xbf; // its bf16 copy (the lm_head's operand)
+  float* sspf;   // its partial sums of squares
+};
+
 using nc::VGATE_ROWS;
 
 }  // namespace
@@ -240,9 +248,9 @@ const char* nc_status_string(nc_status s) {
 const char* nc_last_cuda_error(void) { return nc::last_cuda_error_name(); }
 
 const char* nc_kernel_class_name(nc_kernel_class k) {
-  static const char* names[NC_K_COUNT] = {"embed_smear", "qkv_rope_qknorm_ve", "attention", "oproj_residual",
-                                          "fc_relu2",    "proj_residual",      "lmhead_softcap",
-                                          "cross_entropy"};
+  static const char* names[NC_K_COUNT] = {"embed_smear",   "qkv_rope_qknorm_ve", "attention",  "oproj_residual",
+                                          "fc_relu2",      "proj_residual",      "lmhead_softcap", "cross_entropy",
+                                          "lmhead_grad",   "mlp_grad",           "oproj_grad",     "rmsnorm_grad"};
   return (k >= 0 && k < NC_K_COUNT) ? names[k] : "unknown";
 }
 
@@ -444,7 +452,7 @@ size_t decode_scratch_floats(const nc_model* m, int B) {
 // values also go to the cache (prefill: the positions the layer's window can still see; decode:
 // the new position), and a decode step attends over the cache.
 cudaError_t run_blocks(nc_model* m, const int32_t* tokens, int B, int T, const Layout& Lo, uint8_t* ws,
-                       cudaStream_t stream, const KvCtx* kv = nullptr) {
+                       cudaStream_t stream, const KvCtx* kv = nullptr, const TailOut* tail = nullptr) {
   const nc_config& c = m->cfg;
   const int M = B * T, C = c.n_embd, H = c.n_head, Hkv = c.n_kv_head, D = c.head_dim;
   const int F = c.mlp_hidden, V = c.vocab_size, L = c.n_layer;
@@ -551,6 +559,11 @@ cudaError_t run_blocks(nc_model* m, const int32_t* tokens, int B, int T, const L
         pe.b = -m->lb;
         pe.Y = mid < 0 ? x0 : xm;
       }
+      if (tail != nullptr) {   // keep the last block's MLP input for the backward
+        pe.x_out = tail->xf;
+        pe.xb = tail->xbf;
+        pe.ssp_out = tail->sspf;
+      }
     }
     e = timed(m, NC_K_PROJ, stream, [&] { return nc::launch_gemm_resid(h, m->wproj[i], M, C, F, pe, m->num_sms, stream); });
   }
@@ -571,6 +584,40 @@ LossLayout loss_layout_for(const nc_model* m, const Layout& Lo, int B, int T) {
   L.zt = L.part + align_up(G * M * 4);
   L.scratch = L.zt + align_up(M * 4);
   L.end = L.scratch + align_up(static_cast<size_t>(nc::ce_scratch_doubles(static_cast<int>(M))) * sizeof(double));
+  return L;
+}
+
+// Backward buffers placed after the loss path's: the final stream and its bf16 copy and partials
+// (TailOut), the per-row log-sum-exp and 1 / rows counted, the lm_head's output gradient
+// dlt bf16 [M, V], the pre-norm input gradient G fp32 [M, C] (reused for both norms), the
+// gradient at the last block's output (fp32 and bf16), the MLP's hidden gradient du bf16 [M, F]
+// and the gradient at the last block's MLP input (bf16).
+struct TailLayout {
+  size_t xf, xbf, sspf, lse, invc, dlt, G, dxl, dxlb, du, dxa, end;
+};
+
+TailLayout tail_layout_for(const nc_model* m, const LossLayout& LL, int B, int T) {
+  const nc_config& c = m->cfg;
+  const size_t M = static_cast<size_t>(B) * T, C = c.n_embd;
+  TailLayout L{};
+  size_t off = LL.end;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off += align_up(bytes);
+    return o;
+  };
+  L.xf = take(M * C * 4);
+  L.xbf = take(M * C * 2);
+  L.sspf = take(M * (C / nc::SS_GROUP) * 4);
+  L.lse = take(M * 4);
+  L.invc = take(4);
+  L.dlt = take(M * c.vocab_size * 2);
+  L.G = take(M * C * 4);
+  L.dxl = take(M * C * 4);
+  L.dxlb = take(M * C * 2);
+  L.du = take(M * c.mlp_hidden * 2);
+  L.dxa = take(M * C * 2);
+  L.end = off;
   return L;
 }
 
@@ -657,6 +704,158 @@ nc_status nc_forward_loss(nc_model* m, const int32_t* tokens, const int32_t* tar
       return nc::launch_ce_finalize(part, zt, targets, M, (V + 127) / 128, V, token_bytes, loss, stats,
                                     reinterpret_cast<double*>(ws + LL.scratch), m->status, stream);
     });
+  return nc::cuda_status(e);
+}
+
+nc_status nc_workspace_bytes_grad_tail(const nc_model* m, int B, int T, size_t* bytes) {
+  if (m == nullptr || bytes == nullptr || B < 1 || T < 1) return NC_ERR_INVALID_ARG;
+  if (T > m->cfg.seq_len_ctx) return NC_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * T > (1LL << 30)) return NC_ERR_UNSUPPORTED;
+  const Layout Lo = layout_for(m, B, T);
+  *bytes = tail_layout_for(m, loss_layout_for(m, Lo, B, T), B, T).end;
+  return NC_OK;
+}
+
+nc_status nc_forward_loss_grad_tail(nc_model* m, const int32_t* tokens, const int32_t* targets, int B, int T,
+                                    const int32_t* token_bytes, float* stats, float* grad_lm_head,
+                                    float* grad_wproj, float* grad_wfc, float* grad_wo, void* workspace,
+                                    size_t ws_bytes, void* stream_) {
+  nc_status s = check_forward_args(m, tokens, B, T, workspace);
+  if (s != NC_OK) return s;
+  if (targets == nullptr || stats == nullptr || !aligned(targets, 4) || !aligned(stats, 4) ||
+      (token_bytes != nullptr && !aligned(token_bytes, 4)))
+    return NC_ERR_INVALID_ARG;
+  for (const float* g : {grad_lm_head, grad_wproj, grad_wfc, grad_wo})
+    if (g == nullptr || !aligned(g, 16)) return NC_ERR_INVALID_ARG;
+  const Layout Lo = layout_for(m, B, T);
+  const LossLayout LL = loss_layout_for(m, Lo, B, T);
+  const TailLayout TL = tail_layout_for(m, LL, B, T);
+  if (ws_bytes < TL.end) return NC_ERR_WORKSPACE;
+  const nc_config& c = m->cfg;
+  const int M = B * T, V = c.vocab_size, C = c.n_embd, F = c.mlp_hidden, HD = c.n_head * c.head_dim;
+  const int last = c.n_layer - 1;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  auto f32 = [&](size_t off) { return reinterpret_cast<float*>(ws + off); };
+  auto b16 = [&](size_t off) { return reinterpret_cast<nc::bf16*>(ws + off); };
+  const TailOut tail{f32(TL.xf), b16(TL.xbf), f32(TL.sspf)};
+  float* part = f32(LL.part);
+  float* zt = f32(LL.zt);
+
+  // forward, keeping the last block's MLP input (x, xb, ssp) and its h and y
+  cudaError_t e = run_blocks(m, tokens, B, T, Lo, ws, stream, nullptr, &tail);
+  if (e == cudaSuccess) {   // loss: cross-entropy partials, then log-sum-exp, 1 / count, mean loss
+    nc::GemmEpi le;
+    set_consumer(le, m, tail.sspf);
+    le.kind = nc::EPI_CE;
+    le.cap = c.softcap;
+    le.targets = targets;
+    le.ce_part = part;
+    le.ce_zt = zt;
+    e = timed(m, NC_K_LMHEAD, stream, [&] { return nc::launch_gemm(tail.xbf, m->lm, M, V, C, le, m->num_sms, stream); });
+  }
+  if (e == cudaSuccess)
+    e = timed(m, NC_K_LOSS, stream, [&] {
+      return nc::launch_ce_finalize(part, zt, targets, M, (V + 127) / 128, V, token_bytes, nullptr, stats,
+                                    reinterpret_cast<double*>(ws + LL.scratch), m->status, stream, f32(TL.lse),
+                                    f32(TL.invc));
+    });
+  // the lm_head's output gradient (the logits recomputed), then its input and weight gradients
+  auto gemm = [&](int cls, const nc::bf16* A, const nc::bf16* Bm, int Mg, int Ng, int Kg, nc::GemmEpi& ge) {
+    ge.status = m->status;
+    return timed(m, cls, stream, [&] { return nc::launch_gemm(A, Bm, Mg, Ng, Kg, ge, m->num_sms, stream); });
+  };
+  if (e == cudaSuccess) {
+    nc::GemmEpi ge;
+    set_consumer(ge, m, tail.sspf);
+    ge.kind = nc::EPI_CE_GRAD;
+    ge.cap = c.softcap;
+    ge.targets = targets;
+    ge.ce_lse = f32(TL.lse);
+    ge.inv_count = f32(TL.invc);
+    ge.out = b16(TL.dlt);
+    ge.ldo = V;
+    e = gemm(NC_K_LMHEAD_GRAD, tail.xbf, m->lm, M, V, C, ge);
+  }
+  if (e == cudaSuccess) {   // G = dlt . W_lm   (W_lm [V][C]: N-contiguous B)
+    nc::GemmEpi ge;
+    ge.kind = nc::EPI_F32;
+    ge.b_mn = 1;
+    ge.out = f32(TL.G);
+    ge.ldo = C;
+    e = gemm(NC_K_LMHEAD_GRAD, b16(TL.dlt), m->lm, M, C, V, ge);
+  }
+  if (e == cudaSuccess) {   // dW_lm = dlt^T . xbf   (both token-major)
+    nc::GemmEpi ge;
+    ge.kind = nc::EPI_F32;
+    ge.a_mn = 1;
+    ge.b_mn = 1;
+    ge.out = grad_lm_head;
+    ge.ldo = C;
+    e = gemm(NC_K_LMHEAD_GRAD, b16(TL.dlt), tail.xbf, V, C, M, ge);
+  }
+  // the final RMSNorm's backward: the gradient at the last block's output (the backout
+  // subtracts a stream that does not depend on the last block)
+  if (e == cudaSuccess)
+    e = timed(m, NC_K_RMS_GRAD, stream, [&] {
+      return nc::launch_rms_backward(f32(TL.G), tail.xf, tail.sspf, nullptr, M, C, c.rms_eps, f32(TL.dxl),
+                                     b16(TL.dxlb), stream);
+    });
+  const nc::bf16* h = b16(Lo.h);
+  const nc::bf16* xb = b16(Lo.xb);
+  float* ssp = f32(Lo.ssp);
+  if (e == cudaSuccess) {   // du' = rs . (dxl . W_proj) * 2 sqrt(h)   (W_proj [C][F]: N-contiguous B)
+    nc::GemmEpi ge;
+    set_consumer(ge, m, ssp);
+    ge.kind = nc::EPI_DRELU2;
+    ge.b_mn = 1;
+    ge.h_in = h;
+    ge.out = b16(TL.du);
+    ge.ldo = F;
+    e = gemm(NC_K_MLP_GRAD, b16(TL.dxlb), m->wproj[last], M, F, C, ge);
+  }
+  if (e == cudaSuccess) {   // dW_proj = dxl^T . h
+    nc::GemmEpi ge;
+    ge.kind = nc::EPI_F32;
+    ge.a_mn = 1;
+    ge.b_mn = 1;
+    ge.out = grad_wproj;
+    ge.ldo = F;
+    e = gemm(NC_K_MLP_GRAD, b16(TL.dxlb), h, C, F, M, ge);
+  }
+  if (e == cudaSuccess) {   // dW_fc = du'^T . xb   (du' carries the MLP input's row scale)
+    nc::GemmEpi ge;
+    ge.kind = nc::EPI_F32;
+    ge.a_mn = 1;
+    ge.b_mn = 1;
+    ge.out = grad_wfc;
+    ge.ldo = C;
+    e = gemm(NC_K_MLP_GRAD, b16(TL.du), xb, F, C, M, ge);
+  }
+  if (e == cudaSuccess) {   // G = du' . W_fc   (W_fc [F][C]: N-contiguous B)
+    nc::GemmEpi ge;
+    ge.kind = nc::EPI_F32;
+    ge.b_mn = 1;
+    ge.out = f32(TL.G);
+    ge.ldo = C;
+    e = gemm(NC_K_MLP_GRAD, b16(TL.du), m->wfc[last], M, C, F, ge);
+  }
+  // the MLP input's RMSNorm backward plus the residual path: the gradient at the stream after the
+  // attention's output projection, then that projection's weight gradient
+  if (e == cudaSuccess)
+    e = timed(m, NC_K_RMS_GRAD, stream, [&] {
+      return nc::launch_rms_backward(f32(TL.G), f32(Lo.x), ssp, f32(TL.dxl), M, C, c.rms_eps, nullptr, b16(TL.dxa),
+                                     stream);
+    });
+  if (e == cudaSuccess) {   // dW_o = dxa^T . y
+    nc::GemmEpi ge;
+    ge.kind = nc::EPI_F32;
+    ge.a_mn = 1;
+    ge.b_mn = 1;
+    ge.out = grad_wo;
+    ge.ldo = HD;
+    e = gemm(NC_K_OPROJ_GRAD, b16(TL.dxa), b16(Lo.y), C, HD, M, ge);
+  }
   return nc::cuda_status(e);
 }
 
@@ -822,6 +1021,13 @@ int nc_kv_launch_count(const nc_model* m) {
 int nc_forward_loss_launch_count(const nc_model* m) {
   if (m == nullptr) return 0;
   return nc_forward_launch_count(m) + 2;   // + the two cross-entropy reduction kernels
+}
+
+int nc_grad_tail_launch_count(const nc_model* m) {
+  if (m == nullptr) return 0;
+  // the loss path, then the lm_head's output, input and weight gradients, two RMSNorm backwards,
+  // four MLP gradient products and the attention output projection's weight gradient
+  return nc_forward_loss_launch_count(m) + 3 + 2 + 4 + 1;
 }
 
 }  // extern "C"

@@ -49,6 +49,100 @@ nc_status nc_op_gemm(const void* A, const void* B, int M, int N, int K, nc_epilo
                                      e, device_sms(), static_cast<cudaStream_t>(stream)));
 }
 
+nc_status nc_op_gemm_t(const void* A, const void* B, int M, int N, int K, int a_mn, int b_mn, nc_epilogue epi,
+                       void* out, int ldo, const float* ssp, int C, float eps, float cap, int* status, void* stream) {
+  if (!al(A, 16) || !al(B, 16) || !al(out, 16) || M < 1 || N < 1 || K < 1 || ldo < N || ldo % 8 != 0)
+    return NC_ERR_INVALID_ARG;
+  if ((a_mn != 0 && a_mn != 1) || (b_mn != 0 && b_mn != 1)) return NC_ERR_INVALID_ARG;
+  if (!al_or_null(ssp, 4) || (ssp != nullptr && (C < nc::SS_GROUP || C % nc::SS_GROUP != 0)))
+    return NC_ERR_INVALID_ARG;
+  if (N % 32 != 0 || ((!a_mn || !b_mn) && K % 8 != 0) || (a_mn && M % 8 != 0) || (b_mn && N % 8 != 0))
+    return NC_ERR_UNSUPPORTED;
+  if ((epi == NC_EPI_SOFTCAP_F32 || epi == NC_EPI_SOFTCAP_BF16) && !(cap > 0.f)) return NC_ERR_INVALID_ARG;
+  nc::GemmEpi e;
+  switch (epi) {
+    case NC_EPI_BF16: e.kind = nc::EPI_BF16; break;
+    case NC_EPI_RELU2_BF16: e.kind = nc::EPI_RELU2_BF16; break;
+    case NC_EPI_SOFTCAP_F32: e.kind = nc::EPI_SOFTCAP_F32; break;
+    case NC_EPI_SOFTCAP_BF16: e.kind = nc::EPI_SOFTCAP_BF16; break;
+    case NC_EPI_F32: e.kind = nc::EPI_F32; break;
+    default: return NC_ERR_INVALID_ARG;
+  }
+  e.a_mn = a_mn;
+  e.b_mn = b_mn;
+  e.out = out;
+  e.ldo = ldo;
+  e.cap = cap;
+  e.status = status;
+  if (ssp != nullptr && epi != NC_EPI_BF16) {
+    e.ssp_in = ssp;
+    e.ncg = C / nc::SS_GROUP;
+    e.inv_ncols = 1.0f / static_cast<float>(C);
+    e.eps = eps;
+  }
+  return cuda_status(nc::launch_gemm(static_cast<const nc::bf16*>(A), static_cast<const nc::bf16*>(B), M, N, K,
+                                     e, device_sms(), static_cast<cudaStream_t>(stream)));
+}
+
+nc_status nc_op_lmhead_ce_grad(const void* xf, const void* wlm, int M, int V, int C, const float* ssp, float eps,
+                               float cap, const int32_t* targets, const float* lse, const float* inv_count, void* out,
+                               int ldo, int* status, void* stream) {
+  if (!al(xf, 16) || !al(wlm, 16) || !al(out, 16) || !al(lse, 4) || !al(inv_count, 4) || targets == nullptr ||
+      M < 1 || V < 1 || C < 1 || ldo < V || ldo % 8 != 0 || !(cap > 0.f))
+    return NC_ERR_INVALID_ARG;
+  if (!al_or_null(ssp, 4) || (ssp != nullptr && C % nc::SS_GROUP != 0)) return NC_ERR_INVALID_ARG;
+  if (C % 8 != 0 || V % 32 != 0) return NC_ERR_UNSUPPORTED;
+  nc::GemmEpi e;
+  e.kind = nc::EPI_CE_GRAD;
+  e.status = status;
+  e.cap = cap;
+  e.targets = targets;
+  e.ce_lse = lse;
+  e.inv_count = inv_count;
+  e.out = out;
+  e.ldo = ldo;
+  if (ssp != nullptr) {
+    e.ssp_in = ssp;
+    e.ncg = C / nc::SS_GROUP;
+    e.inv_ncols = 1.0f / static_cast<float>(C);
+    e.eps = eps;
+  }
+  return cuda_status(nc::launch_gemm(static_cast<const nc::bf16*>(xf), static_cast<const nc::bf16*>(wlm), M, V, C,
+                                     e, device_sms(), static_cast<cudaStream_t>(stream)));
+}
+
+nc_status nc_op_mlp_hidden_grad(const void* dy, const void* w, int M, int F, int C, const float* ssp, float eps,
+                                const void* h, void* out, int* status, void* stream) {
+  if (!al(dy, 16) || !al(w, 16) || !al(h, 16) || !al(out, 16) || M < 1 || F < 1 || C < 1) return NC_ERR_INVALID_ARG;
+  if (!al_or_null(ssp, 4) || (ssp != nullptr && C % nc::SS_GROUP != 0)) return NC_ERR_INVALID_ARG;
+  if (C % 8 != 0 || F % 32 != 0) return NC_ERR_UNSUPPORTED;
+  nc::GemmEpi e;
+  e.kind = nc::EPI_DRELU2;
+  e.status = status;
+  e.b_mn = 1;   // w [C][F]: the product's K = C rows, its N = F columns contiguous
+  e.h_in = static_cast<const nc::bf16*>(h);
+  e.out = out;
+  e.ldo = F;
+  if (ssp != nullptr) {
+    e.ssp_in = ssp;
+    e.ncg = C / nc::SS_GROUP;
+    e.inv_ncols = 1.0f / static_cast<float>(C);
+    e.eps = eps;
+  }
+  return cuda_status(nc::launch_gemm(static_cast<const nc::bf16*>(dy), static_cast<const nc::bf16*>(w), M, F, C, e,
+                                     device_sms(), static_cast<cudaStream_t>(stream)));
+}
+
+nc_status nc_op_rms_backward(const float* G, const float* x, const float* ssp, const float* add, int M, int C,
+                             float eps, float* dx_f32, void* dx_b16, void* stream) {
+  if (!al(G, 16) || !al(x, 16) || !al(ssp, 4) || !al_or_null(add, 16) || !al_or_null(dx_f32, 16) ||
+      !al_or_null(dx_b16, 8) || (dx_f32 == nullptr && dx_b16 == nullptr) || M < 1 || C < 1 || !(eps >= 0.f))
+    return NC_ERR_INVALID_ARG;
+  if (C % nc::SS_GROUP != 0 || C > 2048) return NC_ERR_UNSUPPORTED;
+  return cuda_status(nc::launch_rms_backward(G, x, ssp, add, M, C, eps, dx_f32, static_cast<nc::bf16*>(dx_b16),
+                                             static_cast<cudaStream_t>(stream)));
+}
+
 nc_status nc_op_gemm_residual(const void* A, const void* B, int M, int N, int K, const float* resid, float a,
                               float b, const float* Y, float* x_out, float* xm_out, void* xb, float* ssp,
                               int* status, void* stream) {
@@ -167,14 +261,15 @@ size_t nc_op_ce_scratch_bytes(int M) {
 
 nc_status nc_op_ce_finalize(const float* part, const float* zt, const int32_t* targets, int M, int V,
                             const int32_t* token_bytes, float* loss, float* stats, void* scratch,
-                            size_t scratch_bytes, int* status, void* stream) {
+                            size_t scratch_bytes, float* lse, float* inv_count, int* status, void* stream) {
   if (!al(part, 4) || !al(zt, 4) || targets == nullptr || !al(stats, 4) || !al(scratch, 8) ||
-      !al_or_null(loss, 4) || !al_or_null(token_bytes, 4) || M < 1 || V < 1)
+      !al_or_null(loss, 4) || !al_or_null(token_bytes, 4) || !al_or_null(lse, 4) || !al_or_null(inv_count, 4) ||
+      M < 1 || V < 1)
     return NC_ERR_INVALID_ARG;
   if (scratch_bytes < nc_op_ce_scratch_bytes(M)) return NC_ERR_WORKSPACE;
   return cuda_status(nc::launch_ce_finalize(part, zt, targets, M, (V + 127) / 128, V, token_bytes, loss, stats,
                                             static_cast<double*>(scratch), status,
-                                            static_cast<cudaStream_t>(stream)));
+                                            static_cast<cudaStream_t>(stream), lse, inv_count));
 }
 
 nc_status nc_op_test_wait_timeout(const void* A, const void* B, int M, int N, int K, void* out, int ldo,

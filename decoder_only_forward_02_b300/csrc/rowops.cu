@@ -1,5 +1,5 @@
 // rowops.cu -- memory-bound per-row kernels: the token embedding with smear and the first
-// block's residual mix, and the rotary-angle table.
+// block's residual mix, the rotary-angle table, and the backward of the weightless RMSNorm.
 //
 // One warp per row, 8 rows per 256-thread block; each lane owns C/128 groups of 4
 // consecutive channels (offset 128*i + 4*lane), so every load and store is a coalesced
@@ -105,6 +105,49 @@ __global__ void __launch_bounds__(32 * ROWS_PER_BLOCK)
   }
 }
 
+// Backward of xn = rs * x, rs = 1 / sqrt(mean(x^2) + eps), given G = rs * dL/dxn (the gradient
+// GEMMs fold the forward's row scale into their operand):  dL/dx_j = rs g_j - rs^3 x_j mean(g x)
+// = G_j - rs^2 x_j mean(G x).  rs^2 comes from the forward's partial sums of squares (the same
+// value the forward's consumers used); `add` is a gradient reaching x by another path (the
+// residual connection), added before the bf16 rounding.
+template <int NV4>
+__global__ void __launch_bounds__(32 * ROWS_PER_BLOCK)
+    rms_backward_kernel(const float* __restrict__ G, const float* __restrict__ x, const float* __restrict__ ssp,
+                        const float* __restrict__ add, int M, float eps, float* __restrict__ dx_f32,
+                        bf16* __restrict__ dx_b16) {
+  constexpr int C = NV4 * 128;
+  griddep_wait();
+  griddep_launch();
+  const int lane = threadIdx.x & 31;
+  const int row = blockIdx.x * ROWS_PER_BLOCK + (threadIdx.x >> 5);
+  if (row >= M) return;
+  const size_t base = static_cast<size_t>(row) * C;
+  float ss = lane < NV4 ? ssp[static_cast<size_t>(row) * NV4 + lane] : 0.f;
+  float4 g[NV4], xv[NV4];
+  float gx = 0.f;
+#pragma unroll
+  for (int i = 0; i < NV4; ++i) {
+    g[i] = *reinterpret_cast<const float4*>(G + base + i * 128 + lane * 4);
+    xv[i] = *reinterpret_cast<const float4*>(x + base + i * 128 + lane * 4);
+    gx += dot4(g[i], xv[i]);
+  }
+  ss = warp_sum(ss);
+  gx = warp_sum(gx);
+  const float rs2 = 1.0f / (ss * (1.0f / C) + eps);
+  const float k = rs2 * gx * (1.0f / C);
+#pragma unroll
+  for (int i = 0; i < NV4; ++i) {
+    float4 d = make_float4(fmaf(-k, xv[i].x, g[i].x), fmaf(-k, xv[i].y, g[i].y), fmaf(-k, xv[i].z, g[i].z),
+                           fmaf(-k, xv[i].w, g[i].w));
+    if (add != nullptr) {
+      const float4 a = *reinterpret_cast<const float4*>(add + base + i * 128 + lane * 4);
+      d.x += a.x; d.y += a.y; d.z += a.z; d.w += a.w;
+    }
+    if (dx_f32 != nullptr) *reinterpret_cast<float4*>(dx_f32 + base + i * 128 + lane * 4) = d;
+    if (dx_b16 != nullptr) st_bf16x4(dx_b16 + base + i * 128 + lane * 4, d);
+  }
+}
+
 // table[i * T + t] = (cos, sin)(t * base^(-2i/D)): position fastest, so the threads of a warp
 // (consecutive rows, i.e. consecutive positions) read one contiguous run per pair index i.
 __global__ void rope_table_kernel(float2* table, int T, int half, double base) {
@@ -147,7 +190,32 @@ struct EmbedLaunch {
   }
 };
 
+template <int NV4>
+struct RmsBackwardLaunch {
+  static cudaError_t run(const float* G, const float* x, const float* ssp, const float* add, int M, float eps,
+                         float* dx_f32, bf16* dx_b16, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1] = {pdl_attribute()};
+    cfg.gridDim = dim3((M + ROWS_PER_BLOCK - 1) / ROWS_PER_BLOCK);
+    cfg.blockDim = dim3(32 * ROWS_PER_BLOCK);
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, rms_backward_kernel<NV4>, G, x, ssp, add, M, eps, dx_f32, dx_b16);
+    if (e != cudaSuccess) cudaGetLastError();
+    return e;
+  }
+};
+
 }  // namespace
+
+cudaError_t launch_rms_backward(const float* G, const float* x, const float* ssp, const float* add, int M, int C,
+                                float eps, float* dx_f32, bf16* dx_b16, cudaStream_t stream) {
+  if (G == nullptr || x == nullptr || ssp == nullptr || M < 1 || C % 128 != 0 || C > 16 * 128 ||
+      (dx_f32 == nullptr && dx_b16 == nullptr))
+    return cudaErrorInvalidValue;
+  return dispatch_nv4<RmsBackwardLaunch>(C, G, x, ssp, add, M, eps, dx_f32, dx_b16, stream);
+}
 
 cudaError_t launch_embed_smear(const int32_t* tokens, int B, int T, const bf16* wte, int V, int C,
                                const bf16* smear_gate, int c_s, int embed_norm, float eps, float a,

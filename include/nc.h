@@ -212,6 +212,34 @@ NC_API nc_status nc_forward_loss(nc_model *m, const int32_t *tokens, const int32
                                  const int32_t *token_bytes, float *loss, float *stats, void *workspace,
                                  size_t ws_bytes, void *stream);
 
+/* ---- Backward, first part: the gradient of the mean loss at the tail of the network ----
+ * "NanoChat基础训练报告", performance section (the training step the pages measure) and loss
+ * progression table (the training loss); "Nanochat在nanoGPT之上的新增功能", section 1 table and
+ * notes (untied lm_head, logit soft-cap, final RMSNorm, backout, ReLU^2 MLP).  The loss is that of
+ * nc_forward_loss: the mean over counted positions (target in [0, V)) of the cross-entropy of the
+ * soft-capped logits.  nc_forward_loss_grad_tail runs that loss path and then the backward as far
+ * as the last block's attention output projection, writing the exact gradient of the mean loss
+ * (up to rounding) with respect to four weights, fp32, row-major like the weights themselves:
+ *   grad_lm_head [V, C]        the lm_head
+ *   grad_wproj   [C, F]        the last block's MLP down projection (c_proj)
+ *   grad_wfc     [F, C]        the last block's MLP up projection (c_fc)
+ *   grad_wo      [C, H * D]    the last block's attention output projection (c_proj)
+ * Each is overwritten (not accumulated).  The last block's weights get no gradient through the
+ * backout term: the backed-out stream is that of block n_layer/2 - 1 (or x0), never the last
+ * block's.  stats: device fp32 [2] as nc_forward_loss (mean loss, bits per byte with token_bytes);
+ * token_bytes may be NULL.  The lm_head is evaluated twice (once for the log-sum-exp of each row,
+ * once for the gradient), so no logits are stored; the gradient at the lm_head's pre-cap output is
+ * rounded to bf16 before the two products that use it, as the forward's activations are.  tokens,
+ * targets: device int32 [B, T]; gradients: device, 16-byte aligned, caller-owned; workspace: device,
+ * >= nc_workspace_bytes_grad_tail (the loss path's plus about M * (2 V + 2 F + 18 C) bytes), 256-byte
+ * aligned.  Asynchronous on `stream`; errors as nc_forward.  nc_grad_tail_launch_count gives the
+ * kernels one call launches (5 * n_layer + 14). */
+NC_API nc_status nc_workspace_bytes_grad_tail(const nc_model *m, int B, int T, size_t *bytes);
+NC_API nc_status nc_forward_loss_grad_tail(nc_model *m, const int32_t *tokens, const int32_t *targets, int B, int T,
+                                           const int32_t *token_bytes, float *stats, float *grad_lm_head,
+                                           float *grad_wproj, float *grad_wfc, float *grad_wo, void *workspace,
+                                           size_t ws_bytes, void *stream);
+
 /* ---- KV cache: prefill + single-token decode ----
  * "nanochat — 架构与原理", section 2 component table (inference engine: KV cache and sampling)
  * and section 7 code map (Engine, KVCache); "Nanochat在nanoGPT之上的新增功能", section 1 table
@@ -267,7 +295,11 @@ typedef enum {
   NC_K_PROJ = 5,      /* MLP down projection + residual add, next block's mix / backout */
   NC_K_LMHEAD = 6,    /* lm_head GEMM: final RMSNorm + tanh soft-cap (+ cross-entropy partials) */
   NC_K_LOSS = 7,      /* cross-entropy reduction of the loss path */
-  NC_K_COUNT = 8
+  NC_K_LMHEAD_GRAD = 8, /* backward: lm_head output gradient, its input and weight gradients */
+  NC_K_MLP_GRAD = 9,  /* backward: the last block's MLP gradient products */
+  NC_K_OPROJ_GRAD = 10, /* backward: the last block's attention output projection weight gradient */
+  NC_K_RMS_GRAD = 11, /* backward: RMSNorm backward (+ residual gradient) */
+  NC_K_COUNT = 12
 } nc_kernel_class;
 
 /* enable != 0: every following nc_forward records an event pair around each
@@ -279,6 +311,7 @@ NC_API const char *nc_kernel_class_name(nc_kernel_class k);
 /* Number of kernels one nc_forward (nc_forward_loss) launches for this model. */
 NC_API int nc_forward_launch_count(const nc_model *m);
 NC_API int nc_forward_loss_launch_count(const nc_model *m);
+NC_API int nc_grad_tail_launch_count(const nc_model *m);
 
 #ifdef __cplusplus
 }

@@ -24,7 +24,8 @@ typedef enum {
   NC_EPI_BF16 = 0,        /* out bf16 [M, ldo] = acc */
   NC_EPI_RELU2_BF16 = 2,  /* out bf16 = relu(rs * acc)^2     (squared-ReLU row of the feature table) */
   NC_EPI_SOFTCAP_F32 = 3, /* out fp32 = cap*tanh(rs * acc/cap) (logit soft-cap row of the feature table) */
-  NC_EPI_SOFTCAP_BF16 = 6 /* out bf16 = the same, rounded to nearest even */
+  NC_EPI_SOFTCAP_BF16 = 6, /* out bf16 = the same, rounded to nearest even */
+  NC_EPI_F32 = 7           /* out fp32 = rs * acc (the backward's weight and input gradients) */
 } nc_epilogue;
 
 /* Partial sums of squares ("ssp"): fp32 [M, C/128]; ssp[m, g] = sum of x[m, c]^2 over the 128
@@ -33,7 +34,7 @@ typedef enum {
 
 /* acc[M, N] = A[M, K] . B[N, K]^T (tcgen05, fp32 accumulation), then the epilogue; rs from
  * `ssp` over C columns (ssp == NULL: rs = 1).  K % 64 == 0, N % 32 == 0, ldo >= N, rows 16-byte
- * aligned. */
+ * aligned.  (nc_op_gemm_t below adds operand layouts and ragged K.) */
 NC_API nc_status nc_op_gemm(const void *A, const void *B, int M, int N, int K, nc_epilogue epi,
                             void *out, int ldo, const float *ssp, int C, float eps, float cap,
                             int *status, void *stream);
@@ -96,11 +97,52 @@ NC_API nc_status nc_op_lmhead_ce(const void *xf, const void *wlm, int M, int V, 
 
 /* Cross-entropy from the partials of nc_op_lmhead_ce: loss[m] and stats[2] exactly as
  * nc_forward_loss defines them (loss may be NULL; token_bytes device int32 [V] or NULL).
- * scratch: device, >= nc_op_ce_scratch_bytes(M), 8-byte aligned. */
+ * lse (NULL or fp32 [M]) receives log sum_v exp(z[m, v]) of each counted row (0 on ignored rows),
+ * inv_count (NULL or one fp32) 1 / (rows counted), 0 when none is: the inputs of
+ * nc_op_lmhead_ce_grad.  scratch: device, >= nc_op_ce_scratch_bytes(M), 8-byte aligned. */
 NC_API size_t nc_op_ce_scratch_bytes(int M);
 NC_API nc_status nc_op_ce_finalize(const float *part, const float *zt, const int32_t *targets, int M, int V,
                                    const int32_t *token_bytes, float *loss, float *stats, void *scratch,
-                                   size_t scratch_bytes, int *status, void *stream);
+                                   size_t scratch_bytes, float *lse, float *inv_count, int *status, void *stream);
+
+/* ---- Backward pieces (nc_forward_loss_grad_tail chains them) ---- */
+
+/* nc_op_gemm with operand layouts: a_mn = 0 reads A as [M][K] (K contiguous), a_mn = 1 as [K][M]
+ * (M contiguous, i.e. A^T stored row-major); b_mn likewise for B ([N][K] or [K][N]).  A weight
+ * gradient dW = G^T X of token-major G [T][N_out] and X [T][N_in] is (a_mn, b_mn) = (1, 1) with
+ * K = T; an input gradient dX = G W of a weight W [N_out][N_in] is (0, 1).  K need not be a
+ * multiple of 64; K % 8 == 0 when either operand is K-contiguous, M % 8 (N % 8) == 0 for an
+ * M- (N-) contiguous one.  Epilogues as nc_op_gemm (bf16, relu2_bf16, softcap_f32, softcap_bf16,
+ * f32). */
+NC_API nc_status nc_op_gemm_t(const void *A, const void *B, int M, int N, int K, int a_mn, int b_mn,
+                              nc_epilogue epi, void *out, int ldo, const float *ssp, int C, float eps, float cap,
+                              int *status, void *stream);
+
+/* Gradient of the mean cross-entropy at the lm_head's pre-cap output, the logits recomputed
+ * (nothing stored between the passes): with u = rs * (xf . wlm^T) (rs from ssp over C columns, as
+ * nc_op_lmhead_ce) and z = cap * tanh(u / cap),
+ *   out[m, v] = rs * inv_count * (exp(z[m, v] - lse[m]) - [v == targets[m]]) * (1 - (z[m, v] / cap)^2)
+ * in bf16 [M, ldo]; rows whose target lies outside [0, V) are zero.  lse and inv_count as written
+ * by nc_op_ce_finalize.  The row scale rs is kept in the output because the weight gradient
+ * needs it: dW_lm = out^T . xf, and dL/dxf-hat = out . wlm / rs. */
+NC_API nc_status nc_op_lmhead_ce_grad(const void *xf, const void *wlm, int M, int V, int C, const float *ssp,
+                                      float eps, float cap, const int32_t *targets, const float *lse,
+                                      const float *inv_count, void *out, int ldo, int *status, void *stream);
+
+/* Backward of the MLP's squared ReLU through its down projection: with w the down projection's
+ * weight [C][F] (nn.Linear [out][in]) and h = relu(u)^2 [M, F] bf16 the forward's hidden layer,
+ *   out[m, f] = rs[m] * (dy[m, :] . w[:, f]) * 2 sqrt(h[m, f])        (bf16 [M, F])
+ * i.e. the gradient at u scaled by the MLP input's RMSNorm row scale rs (from ssp over C columns;
+ * NULL: 1), the operand of the up projection's weight gradient. dy bf16 [M, C]. */
+NC_API nc_status nc_op_mlp_hidden_grad(const void *dy, const void *w, int M, int F, int C, const float *ssp,
+                                       float eps, const void *h, void *out, int *status, void *stream);
+
+/* Backward of the weightless RMSNorm xn = rs * x, rs = 1 / sqrt(mean(x^2) + eps) (from the
+ * forward's partial sums ssp [M, C / 128] of x^2): given G = rs * dL/dxn (fp32 [M, C]),
+ *   dx = G - rs^2 * x * mean(G * x)  (+ add [M, C] fp32 if non-NULL),
+ * written to dx_f32 (fp32, if non-NULL) and dx_b16 (bf16, if non-NULL).  C % 128 == 0, C <= 2048. */
+NC_API nc_status nc_op_rms_backward(const float *G, const float *x, const float *ssp, const float *add, int M,
+                                    int C, float eps, float *dx_f32, void *dx_b16, void *stream);
 
 /* Test of the bounded device-side waits (failure detection without a GPU fault): the GEMM of
  * nc_op_gemm with NC_EPI_BF16, every wait of the launch limited to limit_ns (1e5 .. 1e8 ns), and the

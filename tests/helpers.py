@@ -42,6 +42,11 @@ def parity(g: np.ndarray, o: np.ndarray):
 MARGINS = []
 
 
+# (label, value, bound) of every backward comparison (relative errors of gradients, or the largest
+# ratio of an error to its per-element bound), printed as a second table.
+GRAD_MARGINS = []
+
+
 def assert_parity(g, o, what=""):
     max_abs, mean_rel = parity(g, o)
     MARGINS.append((what, max_abs, mean_rel))

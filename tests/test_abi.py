@@ -95,7 +95,7 @@ def test_null_arguments_rejected_without_device_work():
     assert lib.nc_op_embed_smear(None, 1, 1, None, 1, 128, None, 0, 0, 1e-6, 1.0, None, None, None, None, None,
                                  None) == 1
     assert lib.nc_op_lmhead_ce(None, None, 1, 32, 64, None, 1e-6, 15.0, None, None, None, None, None) == 1
-    assert lib.nc_op_ce_finalize(None, None, None, 1, 32, None, None, None, None, 0, None, None) == 1
+    assert lib.nc_op_ce_finalize(None, None, None, 1, 32, None, None, None, None, 0, None, None, None, None) == 1
     assert lib.nc_op_ce_scratch_bytes(0) == 0 and lib.nc_op_ce_scratch_bytes(300) >= 16
     assert lib.nc_forward_loss(None, None, None, 1, 1, None, None, None, None, 0, None) == 1
     assert lib.nc_forward_loss_launch_count(None) == 0
@@ -103,12 +103,16 @@ def test_null_arguments_rejected_without_device_work():
     assert lib.nc_kv_cache_bytes(None, 1, 1, None) == 1
     assert lib.nc_prefill(None, None, 1, 1, None, 0, 1, None, None, 0, None) == 1
     assert lib.nc_decode_step(None, None, None, 1, 1, None, 0, 2, None, None, 0, None) == 1
+    assert lib.nc_workspace_bytes_grad_tail(None, 1, 1, ctypes.byref(n)) == 1
+    assert lib.nc_forward_loss_grad_tail(None, None, None, 1, 1, None, None, None, None, None, None, None, 0,
+                                         None) == 1
+    assert lib.nc_grad_tail_launch_count(None) == 0
 
 
 def test_kernel_class_names():
     lib = B.lib()
-    assert [lib.nc_kernel_class_name(i).decode() for i in range(8)] == B.KERNEL_CLASSES
-    assert lib.nc_kernel_class_name(8) == b"unknown"
+    assert [lib.nc_kernel_class_name(i).decode() for i in range(12)] == B.KERNEL_CLASSES
+    assert lib.nc_kernel_class_name(12) == b"unknown"
 
 
 def test_headers_are_plain_c_and_link(tmp_path):
@@ -159,8 +163,38 @@ def test_loss_ops_validate_before_launch():
     assert lib.nc_op_lmhead_ce(a, a, 4, 48, 64, None, 1e-6, 15.0, a, a, a, None, None) == 2       # V % 32
     assert lib.nc_op_lmhead_ce(a, a, 4, 64, 96, None, 1e-6, 15.0, a, a, a, None, None) == 2       # C % 64
     assert lib.nc_op_lmhead_ce(a, a, 4, 64, 64, a, 1e-6, 15.0, a, a, a, None, None) == 1          # ssp, C % 128
-    # nc_op_ce_finalize(part, zt, targets, M, V, token_bytes, loss, stats, scratch, bytes, status, stream)
+    # nc_op_ce_finalize(part, zt, targets, M, V, token_bytes, loss, stats, scratch, bytes, lse, inv_count,
+    #                   status, stream)
     need = lib.nc_op_ce_scratch_bytes(300)
-    assert lib.nc_op_ce_finalize(a, a, a, 300, 64, None, None, a, a, need - 8, None, None) == 3   # scratch too small
-    assert lib.nc_op_ce_finalize(a, a, a, 300, 64, None, None, a, a + 4, need, None, None) == 1   # misaligned scratch
-    assert lib.nc_op_ce_finalize(a, a, a, 0, 64, None, None, a, a, need, None, None) == 1         # M < 1
+    assert lib.nc_op_ce_finalize(a, a, a, 300, 64, None, None, a, a, need - 8, None, None, None, None) == 3
+    assert lib.nc_op_ce_finalize(a, a, a, 300, 64, None, None, a, a + 4, need, None, None, None, None) == 1
+    assert lib.nc_op_ce_finalize(a, a, a, 0, 64, None, None, a, a, need, None, None, None, None) == 1     # M < 1
+    assert lib.nc_op_ce_finalize(a, a, a, 300, 64, None, None, a, a, need, a + 2, None, None, None) == 1  # lse
+
+
+def test_backward_ops_validate_before_launch():
+    """Every case here fails validation, so nothing is launched (fake pointers are never used)."""
+    lib = B.lib()
+    a = 4096
+    # nc_op_gemm_t(A, B, M, N, K, a_mn, b_mn, epi, out, ldo, ssp, C, eps, cap, status, stream)
+    assert lib.nc_op_gemm_t(a, a, 64, 64, 64, 2, 0, 7, a, 64, None, 0, 1e-6, 15.0, None, None) == 1   # a_mn not 0/1
+    assert lib.nc_op_gemm_t(a, a, 64, 64, 60, 0, 1, 7, a, 64, None, 0, 1e-6, 15.0, None, None) == 2   # K % 8, K-major A
+    assert lib.nc_op_gemm_t(a, a, 60, 64, 64, 1, 1, 7, a, 64, None, 0, 1e-6, 15.0, None, None) == 2   # M % 8, MN-major A
+    assert lib.nc_op_gemm_t(a, a, 64, 48, 64, 1, 1, 7, a, 64, None, 0, 1e-6, 15.0, None, None) == 2   # N % 32
+    assert lib.nc_op_gemm_t(a, a, 64, 64, 64, 1, 1, 7, a, 32, None, 0, 1e-6, 15.0, None, None) == 1   # ldo < N
+    assert lib.nc_op_gemm_t(a, a, 64, 64, 64, 1, 1, 5, a, 64, None, 0, 1e-6, 15.0, None, None) == 1   # epilogue kind
+    assert lib.nc_op_gemm_t(a + 8, a, 64, 64, 64, 1, 1, 7, a, 64, None, 0, 1e-6, 15.0, None, None) == 1
+    # nc_op_lmhead_ce_grad(xf, wlm, M, V, C, ssp, eps, cap, targets, lse, inv_count, out, ldo, status, stream)
+    assert lib.nc_op_lmhead_ce_grad(a, a, 4, 64, 64, None, 1e-6, 15.0, a, a, None, a, 64, None, None) == 1  # inv_count
+    assert lib.nc_op_lmhead_ce_grad(a, a, 4, 64, 64, None, 1e-6, 0.0, a, a, a, a, 64, None, None) == 1      # cap
+    assert lib.nc_op_lmhead_ce_grad(a, a, 4, 64, 64, None, 1e-6, 15.0, a, a, a, a, 60, None, None) == 1     # ldo
+    assert lib.nc_op_lmhead_ce_grad(a, a, 4, 48, 64, None, 1e-6, 15.0, a, a, a, a, 48, None, None) == 2     # V % 32
+    # nc_op_mlp_hidden_grad(dy, w, M, F, C, ssp, eps, h, out, status, stream)
+    assert lib.nc_op_mlp_hidden_grad(a, a, 4, 64, 128, None, 1e-6, None, a, None, None) == 1   # h missing
+    assert lib.nc_op_mlp_hidden_grad(a, a, 4, 48, 128, None, 1e-6, a, a, None, None) == 2      # F % 32
+    assert lib.nc_op_mlp_hidden_grad(a, a, 4, 64, 100, None, 1e-6, a, a, None, None) == 2      # C % 8
+    # nc_op_rms_backward(G, x, ssp, add, M, C, eps, dx_f32, dx_b16, stream)
+    assert lib.nc_op_rms_backward(a, a, a, None, 4, 128, 1e-6, None, None, None) == 1          # no output
+    assert lib.nc_op_rms_backward(a, a, a, None, 4, 192, 1e-6, a, None, None) == 2             # C % 128
+    assert lib.nc_op_rms_backward(a, a, a, None, 4, 4096, 1e-6, a, None, None) == 2            # C > 2048
+    assert lib.nc_op_rms_backward(a + 4, a, a, None, 4, 128, 1e-6, a, None, None) == 1         # misaligned G

@@ -213,8 +213,9 @@ def test_loss_path_repeatable_and_launch_count():
 
 # ------------------------------------------------------------------------ bf16 logits (opt-in output)
 
-# bf16 keeps 8 significant bits: rounding to nearest moves a logit |z| < cap by at most cap * 2^-9
-BF16_LOGIT_ULP = 15.0 * 2 ** -9
+# bf16 keeps 8 significant bits: rounding to nearest moves a value by at most half an ulp, 2^-8 of its
+# binade's lower end; a logit |z| < cap = 15 lies below 16, whose binade [8, 16) has half-ulp 2^-5
+BF16_LOGIT_ULP = 2.0 ** -5
 
 
 @pytest.mark.parametrize("name,B,T", [("tiny_all", 2, 64), ("d12", 1, 512)])
@@ -237,7 +238,7 @@ def test_logits_bf16_is_the_rounded_fp32_forward(name, B, T):
     ref = O.forward(cfg, O.OracleWeights.from_synth(cfg, wts), tok.numpy())
     g = z16.float().cpu().numpy()
     d = np.abs(g - ref)
-    assert d.max() <= 5e-2 + BF16_LOGIT_ULP and d.sum() / np.abs(ref).sum() <= 1e-2 + 2 ** -9
+    assert d.max() <= 5e-2 + BF16_LOGIT_ULP and d.sum() / np.abs(ref).sum() <= 1e-2 + 2 ** -8
     # the host entry point copies half the bytes out
     out_h = torch.empty((B, T, cfg.vocab_size), dtype=torch.bfloat16).pin_memory()
     m16.forward_host(tok.pin_memory(), out_h)
