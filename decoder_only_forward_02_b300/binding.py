@@ -122,7 +122,8 @@ _SIGS = {
                           [ctypes.c_void_p] * 4),
     "nc_op_gemm_t": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p] + [ctypes.c_int] * 6 +
                      [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_float,
-                      ctypes.c_void_p, ctypes.c_void_p]),
+                      ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p]),
+    "nc_op_gemm_split_ws_bytes": (ctypes.c_size_t, [ctypes.c_int] * 4),
     "nc_op_lmhead_ce_grad": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
                                             ctypes.c_int, ctypes.c_void_p, ctypes.c_float, ctypes.c_float] +
                              [ctypes.c_void_p] * 4 + [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]),
@@ -150,9 +151,10 @@ class ops:
         return out
 
     @staticmethod
-    def gemm_t(A, B, a_mn=False, b_mn=False, epi="f32", out=None, ssp=None, C=0, eps=1e-6, cap=15.0, status=None):
+    def gemm_t(A, B, a_mn=False, b_mn=False, epi="f32", out=None, ssp=None, C=0, eps=1e-6, cap=15.0, status=None,
+               split=False):
         """nc_op_gemm_t: A is [M, K] (a_mn False) or stored [K, M] (a_mn True); B is [N, K] or stored
-        [K, N]; returns epi(A . B^T) [M, N]."""
+        [K, N]; returns epi(A . B^T) [M, N].  split: give the call a K-split workspace (fp32 output)."""
         K, M = A.shape if a_mn else A.shape[::-1]
         KB, N = B.shape if b_mn else B.shape[::-1]
         if KB != K:
@@ -160,9 +162,13 @@ class ops:
         if out is None:
             dt = torch.bfloat16 if epi in ("bf16", "relu2_bf16", "softcap_bf16") else torch.float32
             out = torch.empty((M, N), dtype=dt, device=A.device)
+        ws, nws = None, 0
+        if split:
+            nws = lib().nc_op_gemm_split_ws_bytes(M, N, K, out.shape[1])
+            ws = torch.empty((max(nws, 16) // 4,), dtype=torch.float32, device=A.device)
         check(lib().nc_op_gemm_t(A.data_ptr(), B.data_ptr(), M, N, K, int(a_mn), int(b_mn), EPI[epi], out.data_ptr(),
-                                 out.shape[1], _ptr(ssp), C, eps, cap, _ptr(status), _stream_handle(None)),
-              "nc_op_gemm_t")
+                                 out.shape[1], _ptr(ssp), C, eps, cap, _ptr(ws), nws, _ptr(status),
+                                 _stream_handle(None)), "nc_op_gemm_t")
         return out
 
     @staticmethod

@@ -417,7 +417,7 @@ __device__ __forceinline__ void epi_bf16(uint32_t taddr, uint32_t tempty, int la
 // rs * acc (EPI_F32: the backward's weight and input gradients).
 template <bool SOFTCAP>
 __device__ __forceinline__ void epi_f32out(uint32_t taddr, uint32_t tempty, int lane, int m0w, int n0, int M,
-                                           int N, const GemmEpi& ep, Slab& sl, const EpiPre& pre) {
+                                           int N, const GemmEpi& ep, Slab& sl, const EpiPre& pre, void* out) {
   const float cap = ep.cap;
   const float sc = SOFTCAP ? pre.rs / cap : pre.rs;
 #pragma unroll 1
@@ -444,7 +444,7 @@ __device__ __forceinline__ void epi_f32out(uint32_t taddr, uint32_t tempty, int 
     __syncwarp();
     sl.put_row(lane, o);
     __syncwarp();
-    lsu_store_box(sl.buf(), ep.out, static_cast<size_t>(ep.ldo) * 4, m0w, static_cast<size_t>(c0) * 4, M, lane,
+    lsu_store_box(sl.buf(), out, static_cast<size_t>(ep.ldo) * 4, m0w, static_cast<size_t>(c0) * 4, M, lane,
                   SOFTCAP);
   }
   release_acc(lane, tempty);
@@ -653,7 +653,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t rank = cluster_ctarank();            // 0: pair leader (issues the MMAs)
   const int pair = static_cast<int>(blockIdx.x) >> 1, npairs = static_cast<int>(gridDim.x) >> 1;
   const int num_m = (M + PAIR_M - 1) / PAIR_M, num_n = num_col_tiles(KIND, N, ep.H, ep.Hkv, ep.D, ep.vgate);
-  const int num_tiles = num_m * num_n, kblocks = (K + BK - 1) / BK;   // a ragged last k-block is zero-filled
+  const int kblocks = (K + BK - 1) / BK;   // a ragged last k-block is zero-filled
+  // split over K (EPI_F32): tile = s * out_tiles + output tile, k-blocks [s * kps, (s + 1) * kps)
+  const int out_tiles = num_m * num_n, ksplit = ep.ksplit > 1 ? ep.ksplit : 1;
+  const int num_tiles = out_tiles * ksplit, kps = (kblocks + ksplit - 1) / ksplit;
   const bool a_mn = ep.a_mn != 0, b_mn = ep.b_mn != 0;
   int* status = ep.status;
   const uint64_t wlim = ep.wait_ns;
@@ -700,13 +703,14 @@ __global__ void __launch_bounds__(THREADS, 1)
       bool ok = true;
       for (int tile = pair; tile < num_tiles && ok; tile += npairs) {
         int mb, nb;
-        tile_coords(tile, num_m, num_n, grp, mb, nb);
+        tile_coords(tile % out_tiles, num_m, num_n, grp, mb, nb);
+        const int kb0 = (tile / out_tiles) * kps, kb1 = min(kblocks, kb0 + kps);
         const ColTile ct = col_tile<KIND>(nb, N, ep);
         // a value-embedding head's tile loads its D + VGATE_ROWS rows of B through the map whose box
         // is half of that; every other tile loads BN / 2 rows per CTA (the MMA uses width / 2)
         const bool vt = ct.vhead >= 0;
         const uint32_t b_bytes = vt ? static_cast<uint32_t>(ct.width / 2) * BK * 2 : static_cast<uint32_t>(B_BYTES);
-        for (int kb = 0; kb < kblocks; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
           if (!mbar_wait_cluster(smem_u32(&ctl->empty[s]), ph ^ 1, abort, status, wlim)) {
             ok = false;
@@ -744,14 +748,15 @@ __global__ void __launch_bounds__(THREADS, 1)
       bool ok = true;
       for (int tile = pair; tile < num_tiles && ok; tile += npairs, ++tc) {
         int mb, nb;
-        tile_coords(tile, num_m, num_n, grp, mb, nb);
+        tile_coords(tile % out_tiles, num_m, num_n, grp, mb, nb);
+        const int kb0 = (tile / out_tiles) * kps, kb1 = min(kblocks, kb0 + kps);
         const uint32_t idesc = idesc_bf16_f32(PAIR_M, col_tile<KIND>(nb, N, ep).width) | (a_mn ? 1u << 15 : 0u) |
                                (b_mn ? 1u << 16 : 0u);
         const uint32_t a = tc & 1, aph = (tc >> 1) & 1;
         if (!mbar_wait_cluster(smem_u32(&ctl->tempty[a]), aph ^ 1, abort, status, wlim)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem + a * BN;
-        for (int kb = 0; kb < kblocks; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
           if (!mbar_wait_cluster(smem_u32(&ctl->full[s]), ph, abort, status, wlim)) {
             ok = false;
@@ -765,7 +770,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                                      : sdesc_kmajor_sw128(sA + s * A_BYTES + kk * 32);
             const uint64_t bd = b_mn ? sdesc_mnmajor_sw128(sB + s * B_BYTES + kk * 16 * 128, MN_BLOCK)
                                      : sdesc_kmajor_sw128(sB + s * B_BYTES + kk * 32);
-            umma_bf16_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+            umma_bf16_pair(d_tmem, ad, bd, idesc, (kb != kb0 || kk != 0) ? 1u : 0u);
           }
           umma_commit_pair(smem_u32(&ctl->empty[s]), 0x3);
           ++it;
@@ -785,7 +790,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     Slab sl{smem + L::OFF_SLAB + ew * L::SLAB_WARP, smem_u32(smem + L::OFF_SLAB + ew * L::SLAB_WARP), 0u};
     auto coords = [&](int tile, int& m0w, ColTile& ct) {
       int mb, nb;
-      tile_coords(tile, num_m, num_n, grp, mb, nb);
+      tile_coords(tile % out_tiles, num_m, num_n, grp, mb, nb);
       m0w = mb * PAIR_M + static_cast<int>(rank) * BM + quarter * 32;
       ct = col_tile<KIND>(nb, N, ep);
     };
@@ -817,8 +822,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint32_t tbase = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + a * BN;
       const uint32_t taddr = tbase + group * 128;
       const uint32_t tempty = mapa_shared(smem_u32(&ctl->tempty[a]), 0);
-      if constexpr (KIND == EPI_SOFTCAP_F32) epi_f32out<true>(taddr, tempty, lane, m0w, n0, M, N, ep, sl, pre);
-      else if constexpr (KIND == EPI_F32) epi_f32out<false>(taddr, tempty, lane, m0w, n0, M, N, ep, sl, pre);
+      if constexpr (KIND == EPI_SOFTCAP_F32) epi_f32out<true>(taddr, tempty, lane, m0w, n0, M, N, ep, sl, pre, ep.out);
+      else if constexpr (KIND == EPI_F32)   // a split tile writes its K range's slab
+        epi_f32out<false>(taddr, tempty, lane, m0w, n0, M, N, ep, sl, pre,
+                          ksplit > 1 ? ep.split_ws + static_cast<size_t>(tile / out_tiles) * M * ep.ldo : ep.out);
       else if constexpr (KIND == EPI_CE_GRAD) epi_bf16<BF16_CEGRAD>(taddr, tempty, lane, m0w, n0, M, N, ep, om, sl, pre);
       else if constexpr (KIND == EPI_DRELU2) epi_bf16<BF16_DRELU2>(taddr, tempty, lane, m0w, n0, M, N, ep, om, sl, pre);
       else if constexpr (KIND == EPI_CE) epi_ce(taddr, tempty, lane, m0w, n0, M, N, ep, pre);
@@ -880,7 +887,7 @@ cudaError_t launch_kind(const CUtensorMap& ta, const CUtensorMap& tb, const CUte
   if (init_err != cudaSuccess) return init_err;
   const int max_pairs = st->max_pairs;
   const int num_m = (M + PAIR_M - 1) / PAIR_M;
-  const int tiles = num_m * num_col_tiles(KIND, N, epi.H, epi.Hkv, epi.D, epi.vgate);
+  const int tiles = num_m * num_col_tiles(KIND, N, epi.H, epi.Hkv, epi.D, epi.vgate) * (epi.ksplit > 1 ? epi.ksplit : 1);
   const int pairs = tiles < max_pairs ? tiles : max_pairs;
   cfg.gridDim = dim3(2 * pairs);
   // When A is the larger operand the pairs of a wave share its row block (grp = 1); otherwise
@@ -893,10 +900,68 @@ cudaError_t launch_kind(const CUtensorMap& ta, const CUtensorMap& tb, const CUte
   return e;
 }
 
+// out[m, c] = sum over s = 0, 1, ... of ws[s][m, c]: the K ranges of a split product, added in a
+// fixed order (4 columns per thread, 128-bit loads and stores).
+__global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restrict__ ws, int S, size_t slab, int M,
+                                                            int N, int ldo, float* __restrict__ out) {
+  griddep_wait();   // the partial slabs are complete and visible
+  griddep_launch();
+  const int q = N / 4;
+  const size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= static_cast<size_t>(M) * q) return;
+  const size_t off = (i / q) * static_cast<size_t>(ldo) + (i % q) * 4;
+  float4 acc = *reinterpret_cast<const float4*>(ws + off);
+  for (int s = 1; s < S; ++s) {
+    const float4 v = *reinterpret_cast<const float4*>(ws + static_cast<size_t>(s) * slab + off);
+    acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+  }
+  *reinterpret_cast<float4*>(out + off) = acc;
+}
+
+cudaError_t launch_splitk_reduce(const GemmEpi& e, int M, int N, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1] = {pdl_attribute()};
+  const size_t n = static_cast<size_t>(M) * (N / 4);
+  cfg.gridDim = dim3(static_cast<unsigned>((n + 255) / 256));
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t err = cudaLaunchKernelEx(&cfg, splitk_reduce_kernel, static_cast<const float*>(e.split_ws), e.ksplit,
+                                             static_cast<size_t>(M) * e.ldo, M, N, e.ldo, static_cast<float*>(e.out));
+  if (err != cudaSuccess) cudaGetLastError();
+  return err;
+}
+
 }  // namespace
 
-cudaError_t launch_gemm(const bf16* A, const bf16* B, int M, int N, int K, const GemmEpi& epi,
+int gemm_ksplit(int M, int N, int K, int num_sms) {
+  if (M < 1 || N < 1 || K < 1) return 1;
+  const int tiles = ((M + PAIR_M - 1) / PAIR_M) * ((N + BN - 1) / BN);
+  const int pairs = num_sms / 2 > 0 ? num_sms / 2 : 1;
+  const int kblocks = (K + BK - 1) / BK;
+  if (2 * tiles >= pairs) return 1;
+  int s = pairs / tiles;
+  s = s < kblocks ? s : kblocks;
+  s = s < 16 ? s : 16;
+  if (s < 2) return 1;
+  const int kps = (kblocks + s - 1) / s;   // every range non-empty
+  return (kblocks + kps - 1) / kps;
+}
+
+size_t gemm_split_ws_bytes(int M, int N, int K, int ldo, int num_sms) {
+  const int s = gemm_ksplit(M, N, K, num_sms);
+  return s > 1 ? static_cast<size_t>(s) * M * ldo * sizeof(float) : 0;
+}
+
+cudaError_t launch_gemm(const bf16* A, const bf16* B, int M, int N, int K, const GemmEpi& epi_in,
                         int num_sms, cudaStream_t stream) {
+  GemmEpi epi = epi_in;
+  epi.ksplit = 1;
+  if (epi.kind == EPI_F32 && epi.split_ws != nullptr) {
+    epi.ksplit = gemm_ksplit(M, N, K, num_sms);
+    if (epi.ksplit > 1 && reinterpret_cast<uintptr_t>(epi.split_ws) % 16 != 0) return cudaErrorInvalidValue;
+  }
   const bool vgate = epi.kind == EPI_QKV && epi.vgate;
   const bool a_mn = epi.a_mn != 0, b_mn = epi.b_mn != 0;
   if (M <= 0 || N <= 0 || K <= 0 || N % (vgate ? 16 : 32) != 0) return cudaErrorInvalidValue;
@@ -964,7 +1029,11 @@ cudaError_t launch_gemm(const bf16* A, const bf16* B, int M, int N, int K, const
     case EPI_SOFTCAP_F32: return launch_kind<EPI_SOFTCAP_F32, 0>(ta, tb, tbv, om, M, N, K, epi, num_sms, stream);
     case EPI_SOFTCAP_BF16: return launch_kind<EPI_SOFTCAP_BF16, 0>(ta, tb, tbv, om, M, N, K, epi, num_sms, stream);
     case EPI_CE: return launch_kind<EPI_CE, 0>(ta, tb, tbv, om, M, N, K, epi, num_sms, stream);
-    case EPI_F32: return launch_kind<EPI_F32, 0>(ta, tb, tbv, om, M, N, K, epi, num_sms, stream);
+    case EPI_F32: {
+      const cudaError_t e = launch_kind<EPI_F32, 0>(ta, tb, tbv, om, M, N, K, epi, num_sms, stream);
+      if (e != cudaSuccess || epi.ksplit < 2) return e;
+      return launch_splitk_reduce(epi, M, N, stream);
+    }
     case EPI_CE_GRAD: return launch_kind<EPI_CE_GRAD, 0>(ta, tb, tbv, om, M, N, K, epi, num_sms, stream);
     case EPI_DRELU2: return launch_kind<EPI_DRELU2, 0>(ta, tb, tbv, om, M, N, K, epi, num_sms, stream);
     case EPI_QKV:

@@ -108,7 +108,21 @@ struct GemmEpi {
   // EPI_DRELU2 (uses ssp_in): h_in bf16 [M, ldo] holds relu(u)^2 of the forward, so relu(u) =
   // sqrt(h) and out = rs * acc * 2 sqrt(h).
   const bf16* h_in = nullptr;
+
+  // EPI_F32 split over K (launch_gemm sets these from split_ws / gemm_ksplit): the k-blocks are cut
+  // into ksplit consecutive ranges, each computed by its own tiles into the fp32 slab
+  // split_ws + s * M * ldo, then added in the order s = 0, 1, ... into out by a second kernel, so
+  // the result does not depend on which tiles ran first.
+  int ksplit = 1;
+  float* split_ws = nullptr;
 };
+
+// How many K ranges an EPI_F32 product of this shape is split into: enough that its tiles fill
+// the CTA pairs of the device (a weight gradient has few output tiles and a long K), at least one
+// 64-deep k-block per range, at most 16.  1 when the output tiles alone fill half the pairs.
+int gemm_ksplit(int M, int N, int K, int num_sms);
+// Bytes of split_ws such a product needs (0 when it is not split).
+size_t gemm_split_ws_bytes(int M, int N, int K, int ldo, int num_sms);
 
 
 // Records `e` as the calling thread's last CUDA error (read by nc_last_cuda_error) and maps it
@@ -163,6 +177,8 @@ inline bool make_tmap_bf16_2d(CUtensorMap* map, const void* ptr, uint64_t inner,
 }
 
 // C[M, N] = epi(A[M, K] . B[N, K]^T); A, B bf16, K contiguous unless epi.a_mn / epi.b_mn.
+// An EPI_F32 product with epi.split_ws set (>= gemm_split_ws_bytes) is split over K as described
+// at GemmEpi::ksplit (two launches); without split_ws it runs unsplit.
 // Requires N % 32 == 0, 16-byte aligned rows (K % 8 == 0 for a K-contiguous operand, M % 8 or
 // N % 8 == 0 for an MN-contiguous one); K may be ragged (the last k-block is zero-filled).
 cudaError_t launch_gemm(const bf16* A, const bf16* B, int M, int N, int K, const GemmEpi& epi,

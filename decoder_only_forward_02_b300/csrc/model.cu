@@ -593,7 +593,7 @@ LossLayout loss_layout_for(const nc_model* m, const Layout& Lo, int B, int T) {
 // gradient at the last block's output (fp32 and bf16), the MLP's hidden gradient du bf16 [M, F]
 // and the gradient at the last block's MLP input (bf16).
 struct TailLayout {
-  size_t xf, xbf, sspf, lse, invc, dlt, G, dxl, dxlb, du, dxa, end;
+  size_t xf, xbf, sspf, lse, invc, dlt, G, dxl, dxlb, du, dxa, split, end;
 };
 
 TailLayout tail_layout_for(const nc_model* m, const LossLayout& LL, int B, int T) {
@@ -617,6 +617,13 @@ TailLayout tail_layout_for(const nc_model* m, const LossLayout& LL, int B, int T
   L.dxlb = take(M * C * 2);
   L.du = take(M * c.mlp_hidden * 2);
   L.dxa = take(M * C * 2);
+  // the K-range slabs of the weight gradients split over tokens (one product at a time)
+  const int Mi = static_cast<int>(M), Ci = static_cast<int>(C), F = c.mlp_hidden, HD = c.n_head * c.head_dim;
+  size_t split = nc::gemm_split_ws_bytes(c.vocab_size, Ci, Mi, Ci, m->num_sms);
+  split = std::max(split, nc::gemm_split_ws_bytes(Ci, F, Mi, F, m->num_sms));
+  split = std::max(split, nc::gemm_split_ws_bytes(F, Ci, Mi, Ci, m->num_sms));
+  split = std::max(split, nc::gemm_split_ws_bytes(Ci, HD, Mi, HD, m->num_sms));
+  L.split = take(split);
   L.end = off;
   return L;
 }
@@ -791,6 +798,7 @@ nc_status nc_forward_loss_grad_tail(nc_model* m, const int32_t* tokens, const in
     ge.a_mn = 1;
     ge.b_mn = 1;
     ge.out = grad_lm_head;
+    ge.split_ws = f32(TL.split);
     ge.ldo = C;
     e = gemm(NC_K_LMHEAD_GRAD, b16(TL.dlt), tail.xbf, V, C, M, ge);
   }
@@ -820,6 +828,7 @@ nc_status nc_forward_loss_grad_tail(nc_model* m, const int32_t* tokens, const in
     ge.a_mn = 1;
     ge.b_mn = 1;
     ge.out = grad_wproj;
+    ge.split_ws = f32(TL.split);
     ge.ldo = F;
     e = gemm(NC_K_MLP_GRAD, b16(TL.dxlb), h, C, F, M, ge);
   }
@@ -829,6 +838,7 @@ nc_status nc_forward_loss_grad_tail(nc_model* m, const int32_t* tokens, const in
     ge.a_mn = 1;
     ge.b_mn = 1;
     ge.out = grad_wfc;
+    ge.split_ws = f32(TL.split);
     ge.ldo = C;
     e = gemm(NC_K_MLP_GRAD, b16(TL.du), xb, F, C, M, ge);
   }
@@ -853,6 +863,7 @@ nc_status nc_forward_loss_grad_tail(nc_model* m, const int32_t* tokens, const in
     ge.a_mn = 1;
     ge.b_mn = 1;
     ge.out = grad_wo;
+    ge.split_ws = f32(TL.split);
     ge.ldo = HD;
     e = gemm(NC_K_OPROJ_GRAD, b16(TL.dxa), b16(Lo.y), C, HD, M, ge);
   }

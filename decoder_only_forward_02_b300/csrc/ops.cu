@@ -49,8 +49,14 @@ nc_status nc_op_gemm(const void* A, const void* B, int M, int N, int K, nc_epilo
                                      e, device_sms(), static_cast<cudaStream_t>(stream)));
 }
 
+size_t nc_op_gemm_split_ws_bytes(int M, int N, int K, int ldo) {
+  if (M < 1 || N < 1 || K < 1 || ldo < N) return 0;
+  return nc::gemm_split_ws_bytes(M, N, K, ldo, device_sms());
+}
+
 nc_status nc_op_gemm_t(const void* A, const void* B, int M, int N, int K, int a_mn, int b_mn, nc_epilogue epi,
-                       void* out, int ldo, const float* ssp, int C, float eps, float cap, int* status, void* stream) {
+                       void* out, int ldo, const float* ssp, int C, float eps, float cap, void* split_ws,
+                       size_t split_ws_bytes, int* status, void* stream) {
   if (!al(A, 16) || !al(B, 16) || !al(out, 16) || M < 1 || N < 1 || K < 1 || ldo < N || ldo % 8 != 0)
     return NC_ERR_INVALID_ARG;
   if ((a_mn != 0 && a_mn != 1) || (b_mn != 0 && b_mn != 1)) return NC_ERR_INVALID_ARG;
@@ -70,6 +76,11 @@ nc_status nc_op_gemm_t(const void* A, const void* B, int M, int N, int K, int a_
   }
   e.a_mn = a_mn;
   e.b_mn = b_mn;
+  if (split_ws != nullptr) {   // split over K when the shape calls for it (fp32 output only)
+    if (epi != NC_EPI_F32 || !al(split_ws, 16)) return NC_ERR_INVALID_ARG;
+    if (split_ws_bytes < nc::gemm_split_ws_bytes(M, N, K, ldo, device_sms())) return NC_ERR_WORKSPACE;
+    e.split_ws = static_cast<float*>(split_ws);
+  }
   e.out = out;
   e.ldo = ldo;
   e.cap = cap;

@@ -116,7 +116,14 @@ NC_API nc_status nc_op_ce_finalize(const float *part, const float *zt, const int
  * f32). */
 NC_API nc_status nc_op_gemm_t(const void *A, const void *B, int M, int N, int K, int a_mn, int b_mn,
                               nc_epilogue epi, void *out, int ldo, const float *ssp, int C, float eps, float cap,
-                              int *status, void *stream);
+                              void *split_ws, size_t split_ws_bytes, int *status, void *stream);
+
+/* Split over K of an NC_EPI_F32 product (weight gradients: few output tiles, K = tokens): with
+ * split_ws non-NULL (device, 16-byte aligned, >= nc_op_gemm_split_ws_bytes bytes, which is 0 when
+ * the shape is not split) nc_op_gemm_t cuts the k-blocks into ranges that fill the device, writes
+ * each range's fp32 partial product to its own slab of split_ws and adds the slabs in a fixed order
+ * into out (a second kernel), so repeated calls are bit-identical. */
+NC_API size_t nc_op_gemm_split_ws_bytes(int M, int N, int K, int ldo);
 
 /* Gradient of the mean cross-entropy at the lm_head's pre-cap output, the logits recomputed
  * (nothing stored between the passes): with u = rs * (xf . wlm^T) (rs from ssp over C columns, as

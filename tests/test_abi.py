@@ -176,14 +176,17 @@ def test_backward_ops_validate_before_launch():
     """Every case here fails validation, so nothing is launched (fake pointers are never used)."""
     lib = B.lib()
     a = 4096
-    # nc_op_gemm_t(A, B, M, N, K, a_mn, b_mn, epi, out, ldo, ssp, C, eps, cap, status, stream)
-    assert lib.nc_op_gemm_t(a, a, 64, 64, 64, 2, 0, 7, a, 64, None, 0, 1e-6, 15.0, None, None) == 1   # a_mn not 0/1
-    assert lib.nc_op_gemm_t(a, a, 64, 64, 60, 0, 1, 7, a, 64, None, 0, 1e-6, 15.0, None, None) == 2   # K % 8, K-major A
-    assert lib.nc_op_gemm_t(a, a, 60, 64, 64, 1, 1, 7, a, 64, None, 0, 1e-6, 15.0, None, None) == 2   # M % 8, MN-major A
-    assert lib.nc_op_gemm_t(a, a, 64, 48, 64, 1, 1, 7, a, 64, None, 0, 1e-6, 15.0, None, None) == 2   # N % 32
-    assert lib.nc_op_gemm_t(a, a, 64, 64, 64, 1, 1, 7, a, 32, None, 0, 1e-6, 15.0, None, None) == 1   # ldo < N
-    assert lib.nc_op_gemm_t(a, a, 64, 64, 64, 1, 1, 5, a, 64, None, 0, 1e-6, 15.0, None, None) == 1   # epilogue kind
-    assert lib.nc_op_gemm_t(a + 8, a, 64, 64, 64, 1, 1, 7, a, 64, None, 0, 1e-6, 15.0, None, None) == 1
+    # nc_op_gemm_t(A, B, M, N, K, a_mn, b_mn, epi, out, ldo, ssp, C, eps, cap, split_ws, bytes, status, stream)
+    assert lib.nc_op_gemm_t(a, a, 64, 64, 64, 2, 0, 7, a, 64, None, 0, 1e-6, 15.0, None, 0, None, None) == 1   # a_mn not 0/1
+    assert lib.nc_op_gemm_t(a, a, 64, 64, 60, 0, 1, 7, a, 64, None, 0, 1e-6, 15.0, None, 0, None, None) == 2   # K % 8, K-major A
+    assert lib.nc_op_gemm_t(a, a, 60, 64, 64, 1, 1, 7, a, 64, None, 0, 1e-6, 15.0, None, 0, None, None) == 2   # M % 8, MN-major A
+    assert lib.nc_op_gemm_t(a, a, 64, 48, 64, 1, 1, 7, a, 64, None, 0, 1e-6, 15.0, None, 0, None, None) == 2   # N % 32
+    assert lib.nc_op_gemm_t(a, a, 64, 64, 64, 1, 1, 7, a, 32, None, 0, 1e-6, 15.0, None, 0, None, None) == 1   # ldo < N
+    assert lib.nc_op_gemm_t(a, a, 64, 64, 64, 1, 1, 5, a, 64, None, 0, 1e-6, 15.0, None, 0, None, None) == 1   # epilogue kind
+    assert lib.nc_op_gemm_t(a + 8, a, 64, 64, 64, 1, 1, 7, a, 64, None, 0, 1e-6, 15.0, None, 0, None, None) == 1
+    assert lib.nc_op_gemm_t(a, a, 64, 64, 64, 1, 1, 0, a, 64, None, 0, 1e-6, 15.0, a, 1 << 20, None, None) == 1  # split, bf16
+    assert lib.nc_op_gemm_t(a, a, 64, 64, 64, 1, 1, 7, a, 64, None, 0, 1e-6, 15.0, a + 4, 1 << 20, None, None) == 1
+    assert lib.nc_op_gemm_split_ws_bytes(0, 64, 64, 64) == 0
     # nc_op_lmhead_ce_grad(xf, wlm, M, V, C, ssp, eps, cap, targets, lse, inv_count, out, ldo, status, stream)
     assert lib.nc_op_lmhead_ce_grad(a, a, 4, 64, 64, None, 1e-6, 15.0, a, a, None, a, 64, None, None) == 1  # inv_count
     assert lib.nc_op_lmhead_ce_grad(a, a, 4, 64, 64, None, 1e-6, 0.0, a, a, a, a, 64, None, None) == 1      # cap

@@ -55,6 +55,27 @@ def test_gemm_operand_layouts(M, N, K, a_mn, b_mn):
     assert np.all(err <= bound), f"max err/bound {np.max(err / bound):.3f}"
 
 
+@pytest.mark.parametrize("M,N,K", [(256, 256, 4096), (520, 384, 200), (768, 768, 16384), (64, 32, 1000)])
+def test_gemm_split_k(M, N, K):
+    """A weight-gradient shape (few output tiles, long K over tokens, both operands token-major)
+    split over K: the ranges' fp32 slabs added in a fixed order match the fp64 product, and
+    repeated calls are bit-identical."""
+    ops = _ops()
+    n = binding().lib().nc_op_gemm_split_ws_bytes(M, N, K, N)
+    assert n > 0   # these shapes are split
+    A = _rand_bf16((K, M), seed=3)
+    B = _rand_bf16((K, N), seed=4)
+    a, b = bf16_np(A).T, bf16_np(B).T
+    got = ops.gemm_t(A.to(DEV), B.to(DEV), a_mn=True, b_mn=True, epi="f32", split=True)
+    got2 = ops.gemm_t(A.to(DEV), B.to(DEV), a_mn=True, b_mn=True, epi="f32", split=True)
+    torch.cuda.synchronize()
+    assert torch.equal(got, got2)
+    # fp32 accumulation within each range and across the (at most 16) ranges
+    bound = ((K + 16) * 2.0 ** -24 + 2.0 ** -22) * (np.abs(a) @ np.abs(b).T) + 1e-30
+    err = np.abs(got.cpu().double().numpy() - a @ b.T)
+    assert np.all(err <= bound), f"max err/bound {np.max(err / bound):.3f}"
+
+
 def test_gemm_layout_rejects_unaligned_extent():
     A = torch.zeros((64, 60), dtype=torch.bfloat16, device=DEV)   # [K][M] with M = 60: rows not 16-byte multiples
     B = torch.zeros((64, 64), dtype=torch.bfloat16, device=DEV)
