@@ -625,6 +625,33 @@ def run_single_kernel(args):
         ssp = torch.rand((M, C // 128), generator=g, device=dev) * 100
         tgt = torch.randint(0, V, (M,), generator=g, device=dev, dtype=torch.int32)
         fn = lambda: ops.lmhead_ce(a, w, tgt, ssp=ssp, C=C, cap=c.softcap)
+    elif k == "ce_grad":   # the gradient at the lm_head's output (the logits recomputed; lse from the loss pass)
+        a, w = rnd((M, C)), rnd((V, C), 0.02)
+        ssp = torch.rand((M, C // 128), generator=g, device=dev) * 100
+        tgt = torch.randint(0, V, (M,), generator=g, device=dev, dtype=torch.int32)
+        part, zt = ops.lmhead_ce(a, w, tgt, ssp=ssp, C=C, cap=c.softcap)
+        _, _, lse, invc = ops.ce_finalize(part, zt, tgt, V, with_lse=True)
+        fn = lambda: ops.lmhead_ce_grad(a, w, tgt, lse, invc, ssp=ssp, C=C, cap=c.softcap)
+    elif k == "lmhead_dgrad":   # G = dlt . W_lm: the lm_head's input gradient (W_lm read N-contiguous)
+        dlt, w = rnd((M, V), 1e-6), rnd((V, C), 0.02)
+        out = torch.empty((M, C), dtype=torch.float32, device=dev)
+        fn = lambda: ops.gemm_t(dlt, w, a_mn=False, b_mn=True, epi="f32", out=out)
+    elif k == "lmhead_wgrad":   # dW_lm = dlt^T . xb: both operands token-major
+        dlt, xb = rnd((M, V), 1e-6), rnd((M, C))
+        out = torch.empty((V, C), dtype=torch.float32, device=dev)
+        fn = lambda: ops.gemm_t(dlt, xb, a_mn=True, b_mn=True, epi="f32", out=out, split=True)
+    elif k == "mlp_wgrad":      # dW_proj = dxl^T . h, split over the tokens
+        dxl, h = rnd((M, C)), rnd((M, F))
+        out = torch.empty((C, F), dtype=torch.float32, device=dev)
+        fn = lambda: ops.gemm_t(dxl, h, a_mn=True, b_mn=True, epi="f32", out=out, split=True)
+    elif k == "mlp_hidden_grad":   # rs * (dxl . W_proj) * 2 sqrt(h)
+        dxl, w, h = rnd((M, C)), rnd((C, F), 0.02), rnd((M, F)).abs()
+        ssp = torch.rand((M, C // 128), generator=g, device=dev) * 100
+        fn = lambda: ops.mlp_hidden_grad(dxl, w, h, ssp=ssp)
+    elif k == "rms_backward":
+        G, x = rnd((M, C), 1.0, torch.float32), rnd((M, C), 1.0, torch.float32)
+        ssp = torch.rand((M, C // 128), generator=g, device=dev) * 100
+        fn = lambda: ops.rms_backward(G, x, ssp, add=G)
     elif k == "embed":
         tok = torch.randint(0, V, (wl.B, wl.T), generator=g, device=dev, dtype=torch.int32)
         wte, sg = rnd((V, C), 0.02), rnd((C,), 0.02)
@@ -690,7 +717,8 @@ def main():
     ap.add_argument("--extra-cpu-tokens", type=int, default=128,
                     help="positions of batch row 0 the oracle runs for each extra workload's CPU baseline")
     ap.add_argument("--only-kernel", default=None,
-                    help="launch one kernel class (qkv, attention, oproj, fc, proj, lmhead, lmhead_ce, embed, decode) "
+                    help="launch one kernel class (qkv, attention, oproj, fc, proj, lmhead, lmhead_ce, embed, decode, "
+                         "ce_grad, lmhead_dgrad, lmhead_wgrad, mlp_wgrad, mlp_hidden_grad, rms_backward) "
                          "at the workload's shapes, for profiler captures")
     ap.add_argument("--launches", type=int, default=3)
     ap.add_argument("--window", type=int, default=None)

@@ -270,6 +270,10 @@ __device__ __forceinline__ void pre_issue(PreRaw& raw, int lane, int m0w, int M,
   if constexpr (KIND == EPI_CE || KIND == EPI_CE_GRAD) raw.tok = ep.targets[m];
   if constexpr (KIND == EPI_CE_GRAD) raw.lse = ep.ce_lse[m];
   if constexpr (KIND == EPI_QKV) raw.tok = ct.vhead >= 0 ? ep.tokens[m] : -1;
+  if constexpr (KIND == EPI_DRELU2) {   // the tile's h rows (both column halves), into L2 a tile ahead
+    const bf16* hr = ep.h_in + static_cast<size_t>(m) * ep.ldo + ct.col0;
+    for (int l = 0; l < 4 && ct.col0 + l * 64 < ct.end; ++l) prefetch_l2(hr + l * 64);   // ct.end = N
+  }
 }
 
 template <int KIND>
@@ -332,7 +336,7 @@ enum Bf16Mode { BF16_PLAIN = 0, BF16_RELU2 = 1, BF16_SOFTCAP = 2, BF16_CEGRAD = 
 template <int MODE>
 __device__ __forceinline__ void epi_bf16(uint32_t taddr, uint32_t tempty, int lane, int m0w, int n0, int M, int N,
                                          const GemmEpi& ep, const OutMaps& om, Slab& sl, const EpiPre& pre) {
-  const float rs = pre.rs;
+  const float rs = pre.rs, rs2 = 2.f * pre.rs;
   const float cap = ep.cap, sc = rs / cap;
   const int m = m0w + lane;
   // EPI_CE_GRAD: exp(z - lse) = 2^(log2(e) * (cap * th - lse)); rows without a counted target
@@ -352,11 +356,23 @@ __device__ __forceinline__ void epi_bf16(uint32_t taddr, uint32_t tempty, int la
     tmem_ld32(taddr + ch * 64, r);
     tmem_ld32(taddr + ch * 64 + 32, r2);
     uint4 hv[8];
-    if constexpr (MODE == BF16_DRELU2) {   // the forward's relu(u)^2 of this row's 64 columns
-      const uint4* hp = reinterpret_cast<const uint4*>(ep.h_in + static_cast<size_t>(m) * ep.ldo + c0);
+    if constexpr (MODE == BF16_DRELU2) {
+      // The forward's relu(u)^2 of the warp's 32 rows x 64 columns, read row-coalesced (each load
+      // instruction covers four whole 128-byte rows), then handed to the owning lanes through the
+      // staging buffer: lane l holds chunk l % 8 of rows 4 k + l / 8.
 #pragma unroll
-      for (int c = 0; c < 8; ++c)
-        hv[c] = (m < M && c0 + c * 8 < N) ? __ldg(hp + c) : make_uint4(0u, 0u, 0u, 0u);
+      for (int k = 0; k < 8; ++k) {
+        const int row = k * 4 + (lane >> 3), q = lane & 7;
+        const bool in = m0w + row < M && c0 + q * 8 < N;
+        hv[k] = in ? __ldg(reinterpret_cast<const uint4*>(ep.h_in + static_cast<size_t>(m0w + row) * ep.ldo + c0) + q)
+                   : make_uint4(0u, 0u, 0u, 0u);
+      }
+      __syncwarp();   // every lane is done reading the previous box from the staging buffer
+#pragma unroll
+      for (int k = 0; k < 8; ++k) *slab_chunk(sl.buf(), k * 4 + (lane >> 3), lane & 7) = hv[k];
+      __syncwarp();
+#pragma unroll
+      for (int c = 0; c < 8; ++c) hv[c] = *slab_chunk(sl.buf(), lane, c);
     }
     tmem_ld_wait(r);
     tmem_ld_wait(r2);
@@ -381,7 +397,7 @@ __device__ __forceinline__ void epi_bf16(uint32_t taddr, uint32_t tempty, int la
         } else if constexpr (MODE == BF16_DRELU2) {
           const __nv_bfloat162 h2 = reinterpret_cast<const __nv_bfloat162*>(&hv[c])[j >> 1];
           const float hval = (j & 1) ? __high2float(h2) : __low2float(h2);
-          t = t * rs * 2.f * sqrtf(hval);
+          t = t * rs2 * sqrt_approx(hval);
         }
         a[j] = t;
       }

@@ -530,6 +530,14 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// Hardware square root approximation (one MUFU operation, subnormals flushed to zero): the
+// squared ReLU's backward needs sqrt(h) only to the precision of the bf16 h it is taken of.
+__device__ __forceinline__ float sqrt_approx(float x) {
+  float y;
+  asm("sqrt.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Hardware 2^x approximation (one MUFU operation; subnormal results flush to zero).
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
