@@ -20,7 +20,7 @@ STATUS_NAMES = {0: "NC_OK", 1: "NC_ERR_INVALID_ARG", 2: "NC_ERR_UNSUPPORTED", 3:
                 4: "NC_ERR_CUDA", 5: "NC_ERR_DEVICE_TIMEOUT", 6: "NC_ERR_TOKEN_RANGE"}
 KERNEL_CLASSES = ["embed_smear", "qkv_rope_qknorm_ve", "attention", "oproj_residual", "fc_relu2",
                   "proj_residual", "lmhead_softcap", "cross_entropy", "lmhead_grad", "mlp_grad", "oproj_grad",
-                  "rmsnorm_grad"]
+                  "rmsnorm_grad", "fp8_quantize"]
 SS_GROUP = 128   # columns per partial sum of squares
 QKV_GATE_ROWS = 16   # rows after each kv head's v rows in a value-embedding layer's packed q|k|v weight
 
@@ -37,7 +37,7 @@ class NcConfig(ctypes.Structure):
         ("use_smear", ctypes.c_int), ("use_backout", ctypes.c_int), ("embed_norm", ctypes.c_int),
         ("smear_gate_channels", ctypes.c_int), ("ve_gate_channels", ctypes.c_int),
         ("ve_gate_scale", ctypes.c_float), ("rms_eps", ctypes.c_float), ("rope_base", ctypes.c_float),
-        ("softcap", ctypes.c_float), ("logits_bf16", ctypes.c_int),
+        ("softcap", ctypes.c_float), ("logits_bf16", ctypes.c_int), ("fp8", ctypes.c_int),
     ]
 
 
@@ -124,6 +124,12 @@ _SIGS = {
                      [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_float,
                       ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p]),
     "nc_op_gemm_split_ws_bytes": (ctypes.c_size_t, [ctypes.c_int] * 4),
+    "nc_op_fp8_scratch_bytes": (ctypes.c_size_t, []),
+    "nc_op_fp8_quantize": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                                          ctypes.c_float] + [ctypes.c_void_p] * 4),
+    "nc_op_gemm_fp8": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p] + [ctypes.c_int] * 4 +
+                       [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_float,
+                        ctypes.c_void_p, ctypes.c_void_p]),
     "nc_op_lmhead_ce_grad": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
                                             ctypes.c_int, ctypes.c_void_p, ctypes.c_float, ctypes.c_float] +
                              [ctypes.c_void_p] * 4 + [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]),
@@ -169,6 +175,30 @@ class ops:
         check(lib().nc_op_gemm_t(A.data_ptr(), B.data_ptr(), M, N, K, int(a_mn), int(b_mn), EPI[epi], out.data_ptr(),
                                  out.shape[1], _ptr(ssp), C, eps, cap, _ptr(ws), nws, _ptr(status),
                                  _stream_handle(None)), "nc_op_gemm_t")
+        return out
+
+    @staticmethod
+    def fp8_quantize(src, ssp=None, eps=1e-6):
+        """e4m3 codes (torch.float8_e4m3fn [M, C]) of src at its tensorwise scale, and 1 / scale (fp32 [1])."""
+        M, C = src.shape
+        dst = torch.empty((M, C), dtype=torch.float8_e4m3fn, device=src.device)
+        inv = torch.empty((1,), dtype=torch.float32, device=src.device)
+        scratch = torch.empty((lib().nc_op_fp8_scratch_bytes() // 4,), dtype=torch.float32, device=src.device)
+        check(lib().nc_op_fp8_quantize(src.data_ptr(), int(src.dtype == torch.float32), M, C, _ptr(ssp), eps,
+                                       dst.data_ptr(), inv.data_ptr(), scratch.data_ptr(), _stream_handle(None)),
+              "nc_op_fp8_quantize")
+        return dst, inv
+
+    @staticmethod
+    def gemm_fp8(A8, B8, inv_sa, inv_sb, epi="f32", cap=15.0, status=None):
+        """epi((A8 . B8^T) * inv_sa * inv_sb) of e4m3 operands A8 [M, K], B8 [N, K]."""
+        M, K = A8.shape
+        N = B8.shape[0]
+        dt = torch.bfloat16 if epi in ("bf16", "relu2_bf16", "softcap_bf16") else torch.float32
+        out = torch.empty((M, N), dtype=dt, device=A8.device)
+        check(lib().nc_op_gemm_fp8(A8.data_ptr(), B8.data_ptr(), M, N, K, EPI[epi], out.data_ptr(), N,
+                                   inv_sa.data_ptr(), inv_sb.data_ptr(), cap, _ptr(status), _stream_handle(None)),
+              "nc_op_gemm_fp8")
         return out
 
     @staticmethod
@@ -362,9 +392,9 @@ def _stream_handle(stream: Optional[torch.cuda.Stream]) -> int:
     return s.cuda_stream
 
 
-def make_config(cfg, logits_bf16: bool = False) -> tuple:
+def make_config(cfg, logits_bf16: bool = False, fp8: bool = False) -> tuple:
     """Build an NcConfig from any object with the model's attribute names (logits_bf16: the
-    forward writes bf16 logits instead of fp32).
+    forward writes bf16 logits instead of fp32; fp8: the linear layers run on e4m3 copies).
 
     Returns (struct, keepalive) - the per-layer arrays must stay alive while the struct is used.
     """
@@ -381,7 +411,7 @@ def make_config(cfg, logits_bf16: bool = False) -> tuple:
         ve_gate_channels=int(getattr(cfg, "ve_gate_channels", 0)),
         ve_gate_scale=float(getattr(cfg, "ve_gate_scale", 1.0)), rms_eps=float(getattr(cfg, "rms_eps", 1e-6)),
         rope_base=float(getattr(cfg, "rope_base", 10000.0)), softcap=float(getattr(cfg, "softcap", 15.0)),
-        logits_bf16=int(bool(logits_bf16)))
+        logits_bf16=int(bool(logits_bf16)), fp8=int(bool(fp8)))
     return c, (win, ve)
 
 
@@ -398,11 +428,11 @@ class Model:
     float lists resid_lambdas, x0_lambdas and the float backout_lambda."""
 
     def __init__(self, cfg, weights: Dict[str, object], device: Optional[torch.device] = None,
-                 stream: Optional[torch.cuda.Stream] = None, logits_bf16: bool = False):
+                 stream: Optional[torch.cuda.Stream] = None, logits_bf16: bool = False, fp8: bool = False):
         self.cfg = cfg
         self.device = torch.device(device) if device is not None else weights["wte"].device
         self.logits_dtype = torch.bfloat16 if logits_bf16 else torch.float32
-        self._cstruct, self._keep = make_config(cfg, logits_bf16)
+        self._cstruct, self._keep = make_config(cfg, logits_bf16, fp8)
         L = cfg.n_layer
 
         def arr(name, optional=False):

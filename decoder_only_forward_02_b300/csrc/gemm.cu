@@ -250,7 +250,8 @@ struct PreRaw {
 };
 
 struct EpiPre {
-  float rs = 1.f;              // input RMSNorm row scale
+  float rs = 1.f;              // input RMSNorm row scale (8-bit: the dequantisation; EPI_QKV: of the q columns)
+  float rs_k = 1.f, rs_v = 1.f;   // EPI_QKV: the same for the k and v columns (they differ on the 8-bit path)
   int tok = -1;                // EPI_QKV: token id of the row on a value-embedding head's tile, else -1;
                                // EPI_CE, EPI_CE_GRAD: the row's target
   float lse = 0.f;             // EPI_CE_GRAD: log sum exp of the row's logits
@@ -284,12 +285,22 @@ __device__ __forceinline__ EpiPre pre_finish(const PreRaw& raw, int lane, int m0
   if (m >= M) return p;
   if constexpr (KIND == EPI_CE || KIND == EPI_CE_GRAD) p.tok = raw.tok;
   if constexpr (KIND == EPI_CE_GRAD) p.lse = raw.lse;
-  if (ep.ssp_in != nullptr) {
-    float ss = 0.f;
+  if (ep.fp8) {   // dequantisation: the input's and the weight's 1 / scale (q, k, v ranges of the packed weight)
+    const float sa = __ldg(ep.fp8_sa);
+    p.rs = sa * __ldg(ep.fp8_sw);
+    if constexpr (KIND == EPI_QKV) {   // q, k and v weights each have their own scale
+      p.rs_k = sa * __ldg(ep.fp8_sw + 1);
+      p.rs_v = sa * __ldg(ep.fp8_sw + 2);
+    }
+  } else {
+    if (ep.ssp_in != nullptr) {
+      float ss = 0.f;
 #pragma unroll
-    for (int g = 0; g < MAX_NCG; ++g)
-      if (g < ep.ncg) ss += raw.ss[g];
-    p.rs = rsqrtf(ss * ep.inv_ncols + ep.eps);
+      for (int g = 0; g < MAX_NCG; ++g)
+        if (g < ep.ncg) ss += raw.ss[g];
+      p.rs = rsqrtf(ss * ep.inv_ncols + ep.eps);
+    }
+    p.rs_k = p.rs_v = p.rs;
   }
   if constexpr (KIND == EPI_QKV) {
     if (ct.vhead >= 0) {
@@ -385,7 +396,9 @@ __device__ __forceinline__ void epi_bf16(uint32_t taddr, uint32_t tempty, int la
       for (int j = 0; j < 8; ++j) {
         const int e = c * 8 + j;
         float t = __uint_as_float(e < 32 ? r[e] : r2[e - 32]);
-        if constexpr (MODE == BF16_RELU2) {
+        if constexpr (MODE == BF16_PLAIN) {
+          t = t * rs;   // 1 without a row scale; the 8-bit path's dequantisation
+        } else if constexpr (MODE == BF16_RELU2) {
           t = fmaxf(t * rs, 0.f);
           t = t * t;
         } else if constexpr (MODE == BF16_SOFTCAP) {
@@ -514,7 +527,6 @@ template <int D>
 __device__ __forceinline__ void epi_qkv(uint32_t taddr, uint32_t tempty, int lane, int m0w, int n0, int end, int M,
                                         const GemmEpi& ep, const OutMaps& om, Slab& sl, const EpiPre& pre) {
   const int m = m0w + lane;
-  const float rs = pre.rs;
   const int qcols = ep.H * D, kcols = ep.Hkv * D;
   const int pos = m < M ? m % ep.T : 0;
   // A head is D/64 boxes of [32 rows][64 columns] bf16: results go straight into the staging
@@ -526,6 +538,8 @@ __device__ __forceinline__ void epi_qkv(uint32_t taddr, uint32_t tempty, int lan
     const uint32_t tb = taddr + s * D;
     const CUtensorMap* map;
     int xcol;
+    // the head's scale: the input RMSNorm, or on the 8-bit path the q, k or v weight's dequantisation
+    const float rs = c < qcols ? pre.rs : (c < qcols + kcols ? pre.rs_k : pre.rs_v);
     sl.acquire_both(lane);
     if (c < qcols + kcols) {
       if (c < qcols) {
@@ -609,16 +623,20 @@ __device__ __forceinline__ void epi_qkv(uint32_t taddr, uint32_t tempty, int lan
 //   v = rs * acc + gate * ve[token, head],  gate = gate_scale * sigmoid(rs * acc[D])
 // With D = 128 the two warpgroups take 64 columns each; with D = 64 the first takes the head.
 template <int D>
-__device__ __forceinline__ void epi_vgate(uint32_t taddr, uint32_t tempty, int lane, int m0w, int group, int vhead,
-                                          const GemmEpi& ep, const OutMaps& om, Slab& sl, const EpiPre& pre) {
+__device__ __forceinline__ void epi_vgate(uint32_t taddr, uint32_t tempty, int lane, int m0w, int M, int group,
+                                          int vhead, const GemmEpi& ep, const OutMaps& om, Slab& sl,
+                                          const EpiPre& pre) {
   const int c0 = D == 128 ? group * 64 : 0;
   if (D == 64 && group == 1) {
     release_acc(lane, tempty);
     return;
   }
-  const float rs = pre.rs;
+  const float rs = pre.rs_v;
   uint32_t gz[1];
   tmem_ld1(taddr + D, gz);
+  // the 8-bit path: the gate's pre-activation (already row-scaled) from its own bf16 product
+  const int m = m0w + lane;
+  const float gpre = (ep.gpre != nullptr && m < M) ? ep.gpre[static_cast<size_t>(m) * ep.gpre_ld + vhead] : 0.f;
   uint32_t r0[32], r1[32];
   tmem_ld32(taddr + c0, r0);
   tmem_ld32(taddr + c0 + 32, r1);
@@ -632,7 +650,7 @@ __device__ __forceinline__ void epi_vgate(uint32_t taddr, uint32_t tempty, int l
   tmem_ld_wait(r0);
   tmem_ld_wait(r1);
   release_acc(lane, tempty);
-  const float g = ep.gate_scale * sigmoid_fast(rs * __uint_as_float(gz[0]));
+  const float g = ep.gate_scale * sigmoid_fast(ep.gpre != nullptr ? gpre : rs * __uint_as_float(gz[0]));
   sl.acquire(lane);
 #pragma unroll
   for (int c8 = 0; c8 < 8; ++c8) {
@@ -669,7 +687,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t rank = cluster_ctarank();            // 0: pair leader (issues the MMAs)
   const int pair = static_cast<int>(blockIdx.x) >> 1, npairs = static_cast<int>(gridDim.x) >> 1;
   const int num_m = (M + PAIR_M - 1) / PAIR_M, num_n = num_col_tiles(KIND, N, ep.H, ep.Hkv, ep.D, ep.vgate);
-  const int kblocks = (K + BK - 1) / BK;   // a ragged last k-block is zero-filled
+  // a stage holds 128 bytes of K per row: 64 bf16 or 128 e4m3 elements; a ragged last k-block is zero-filled
+  const int kstep = ep.fp8 ? 2 * BK : BK;
+  const int kblocks = (K + kstep - 1) / kstep;
   // split over K (EPI_F32): tile = s * out_tiles + output tile, k-blocks [s * kps, (s + 1) * kps)
   const int out_tiles = num_m * num_n, ksplit = ep.ksplit > 1 ? ep.ksplit : 1;
   const int num_tiles = out_tiles * ksplit, kps = (kblocks + ksplit - 1) / ksplit;
@@ -739,13 +759,13 @@ __global__ void __launch_bounds__(THREADS, 1)
           // K-contiguous: one box [rows][64 k].  MN-contiguous: two boxes [64 k][64 rows], the
           // second (rows 64..127) MN_BLOCK bytes after the first.
           if (!a_mn) {
-            tma_load_2d_pair_hint(sA + s * A_BYTES, &tmA, fb, kb * BK, a_row, pol_a);
+            tma_load_2d_pair_hint(sA + s * A_BYTES, &tmA, fb, kb * kstep, a_row, pol_a);
           } else {
             tma_load_2d_pair_hint(sA + s * A_BYTES, &tmA, fb, a_row, kb * BK, pol_a);
             tma_load_2d_pair_hint(sA + s * A_BYTES + MN_BLOCK, &tmA, fb, a_row + 64, kb * BK, pol_a);
           }
           if (!b_mn) {
-            tma_load_2d_pair_hint(sB + s * B_BYTES, vt ? &tmBv : &tmB, fb, kb * BK, b_row, pol_b);
+            tma_load_2d_pair_hint(sB + s * B_BYTES, vt ? &tmBv : &tmB, fb, kb * kstep, b_row, pol_b);
           } else {
             tma_load_2d_pair_hint(sB + s * B_BYTES, &tmB, fb, b_row, kb * BK, pol_b);
             tma_load_2d_pair_hint(sB + s * B_BYTES + MN_BLOCK, &tmB, fb, b_row + 64, kb * BK, pol_b);
@@ -766,8 +786,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         int mb, nb;
         tile_coords(tile % out_tiles, num_m, num_n, grp, mb, nb);
         const int kb0 = (tile / out_tiles) * kps, kb1 = min(kblocks, kb0 + kps);
-        const uint32_t idesc = idesc_bf16_f32(PAIR_M, col_tile<KIND>(nb, N, ep).width) | (a_mn ? 1u << 15 : 0u) |
-                               (b_mn ? 1u << 16 : 0u);
+        const int width = col_tile<KIND>(nb, N, ep).width;
+        const uint32_t idesc = ep.fp8 ? idesc_e4m3_f32(PAIR_M, width)
+                                      : idesc_bf16_f32(PAIR_M, width) | (a_mn ? 1u << 15 : 0u) | (b_mn ? 1u << 16 : 0u);
         const uint32_t a = tc & 1, aph = (tc >> 1) & 1;
         if (!mbar_wait_cluster(smem_u32(&ctl->tempty[a]), aph ^ 1, abort, status, wlim)) break;
         tc_fence_after();
@@ -786,7 +807,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                                      : sdesc_kmajor_sw128(sA + s * A_BYTES + kk * 32);
             const uint64_t bd = b_mn ? sdesc_mnmajor_sw128(sB + s * B_BYTES + kk * 16 * 128, MN_BLOCK)
                                      : sdesc_kmajor_sw128(sB + s * B_BYTES + kk * 32);
-            umma_bf16_pair(d_tmem, ad, bd, idesc, (kb != kb0 || kk != 0) ? 1u : 0u);
+            if (ep.fp8) umma_f8_pair(d_tmem, ad, bd, idesc, (kb != kb0 || kk != 0) ? 1u : 0u);
+            else umma_bf16_pair(d_tmem, ad, bd, idesc, (kb != kb0 || kk != 0) ? 1u : 0u);
           }
           umma_commit_pair(smem_u32(&ctl->empty[s]), 0x3);
           ++it;
@@ -846,7 +868,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       else if constexpr (KIND == EPI_DRELU2) epi_bf16<BF16_DRELU2>(taddr, tempty, lane, m0w, n0, M, N, ep, om, sl, pre);
       else if constexpr (KIND == EPI_CE) epi_ce(taddr, tempty, lane, m0w, n0, M, N, ep, pre);
       else if constexpr (KIND == EPI_QKV) {
-        if (ct.vhead >= 0) epi_vgate<D>(tbase, tempty, lane, m0w, group, ct.vhead, ep, om, sl, pre);
+        if (ct.vhead >= 0) epi_vgate<D>(tbase, tempty, lane, m0w, M, group, ct.vhead, ep, om, sl, pre);
         else epi_qkv<D>(taddr, tempty, lane, m0w, n0, ct.end, M, ep, om, sl, pre);
       } else if constexpr (KIND == EPI_SOFTCAP_BF16) {
         epi_bf16<BF16_SOFTCAP>(taddr, tempty, lane, m0w, n0, M, N, ep, om, sl, pre);
@@ -987,11 +1009,23 @@ cudaError_t launch_gemm(const bf16* A, const bf16* B, int M, int N, int K, const
   if ((a_mn && M % 8 != 0) || (b_mn && N % 8 != 0) || (epi.kind == EPI_QKV && (a_mn || b_mn)))
     return cudaErrorInvalidValue;
   const uint64_t Ku = static_cast<uint64_t>(K);
+  const bool f8 = epi.fp8 != 0;
+  // 8-bit operands: K-contiguous only, rows of K bytes (16-byte multiples), the dequantisation
+  // scales given, and no epilogue of the backward
+  if (f8 && (a_mn || b_mn || K % 16 != 0 || epi.fp8_sa == nullptr || epi.fp8_sw == nullptr ||
+             epi.kind == EPI_CE_GRAD || epi.kind == EPI_DRELU2))
+    return cudaErrorInvalidValue;
   CUtensorMap ta, tb, tbv;
-  const bool ok_a = a_mn ? make_tmap_bf16_2d(&ta, A, M, Ku, static_cast<uint64_t>(M) * 2, 64, BK)
-                         : make_tmap_bf16_2d(&ta, A, Ku, M, Ku * 2, BK, BM);
-  const bool ok_b = b_mn ? make_tmap_bf16_2d(&tb, B, N, Ku, static_cast<uint64_t>(N) * 2, 64, BK)
-                         : make_tmap_bf16_2d(&tb, B, Ku, N, Ku * 2, BK, B_ROWS);
+  bool ok_a, ok_b;
+  if (f8) {   // one 128-byte row of a stage = 128 e4m3 elements of K
+    ok_a = make_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, Ku, M, Ku, 2 * BK, BM);
+    ok_b = make_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, Ku, N, Ku, 2 * BK, B_ROWS);
+  } else {
+    ok_a = a_mn ? make_tmap_bf16_2d(&ta, A, M, Ku, static_cast<uint64_t>(M) * 2, 64, BK)
+                : make_tmap_bf16_2d(&ta, A, Ku, M, Ku * 2, BK, BM);
+    ok_b = b_mn ? make_tmap_bf16_2d(&tb, B, N, Ku, static_cast<uint64_t>(N) * 2, 64, BK)
+                : make_tmap_bf16_2d(&tb, B, Ku, N, Ku * 2, BK, B_ROWS);
+  }
   if (!ok_a || !ok_b) return cudaErrorInvalidValue;
   tbv = tb;
   OutMaps om;
@@ -1033,7 +1067,8 @@ cudaError_t launch_gemm(const bf16* A, const bf16* B, int M, int N, int K, const
            make_tmap_bf16_2d(&om.o2, epi.v, kc, Mu, kc * 2, 64, 32);
       // a value-embedding head's tile: D + VGATE_ROWS rows of B, half per CTA
       if (ok && vgate)
-        ok = make_tmap_bf16_2d(&tbv, B, K, N, static_cast<uint64_t>(K) * 2, BK, (epi.D + VGATE_ROWS) / 2);
+        ok = f8 ? make_tmap_2d(&tbv, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, Ku, N, Ku, 2 * BK, (epi.D + VGATE_ROWS) / 2)
+                : make_tmap_bf16_2d(&tbv, B, K, N, static_cast<uint64_t>(K) * 2, BK, (epi.D + VGATE_ROWS) / 2);
       break;
     }
     default: return cudaErrorInvalidValue;

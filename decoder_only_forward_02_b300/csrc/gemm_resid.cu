@@ -146,7 +146,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int half = NT / 2;
   const int nsteps = half / CH;                       // epilogue slots per tile and warpgroup (even)
   const int num_n = (N + PAIR_N - 1) / PAIR_N, num_t = (M + NT - 1) / NT;
-  const int num_tiles = num_n * num_t, kblocks = K / BK;
+  // a stage holds 128 bytes of K per row: 64 bf16 or 128 e4m3 elements
+  const int kstep = ep.fp8 ? 2 * BK : BK;
+  const int num_tiles = num_n * num_t, kblocks = K / kstep;
   const bool has_y = ep.Y != nullptr;
   int* status = ep.status;
 
@@ -204,8 +206,9 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           const uint32_t fb = mapa_shared(smem_u32(&ctl->full[s]), 0);   // the leader's barrier
           if (rank == 0) mbar_arrive_expect_tx(smem_u32(&ctl->full[s]), stage_tx);
-          tma_load_2d_pair_hint(sW + s * W_BYTES, &tmW, fb, kb * BK, nb * PAIR_N + static_cast<int>(rank) * BM, pol_w);
-          tma_load_2d_pair_hint(sA + s * A_SLOT, &tmA, fb, kb * BK, tb * NT + static_cast<int>(rank) * half, pol_a);
+          tma_load_2d_pair_hint(sW + s * W_BYTES, &tmW, fb, kb * kstep, nb * PAIR_N + static_cast<int>(rank) * BM,
+                                pol_w);
+          tma_load_2d_pair_hint(sA + s * A_SLOT, &tmA, fb, kb * kstep, tb * NT + static_cast<int>(rank) * half, pol_a);
           ++it;
         }
       }
@@ -216,7 +219,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           mbar_wait_cluster(smem_u32(&ctl->full[j % STAGES]), (j / STAGES) & 1, nullptr, status);
       }
     } else if (warp == 1 && lane == 0 && rank == 0) {
-      const uint32_t idesc = idesc_bf16_f32(2 * BM, NT);
+      const uint32_t idesc = ep.fp8 ? idesc_e4m3_f32(2 * BM, NT) : idesc_bf16_f32(2 * BM, NT);
       uint32_t it = 0, tc = 0;
       bool ok = true;
       for (int tile = pair; tile < num_tiles && ok; tile += npairs, ++tc) {
@@ -233,8 +236,10 @@ __global__ void __launch_bounds__(THREADS, 1)
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
-            umma_bf16_pair(d_tmem, sdesc_kmajor_sw128(sW + s * W_BYTES + kk * 32),
-                           sdesc_kmajor_sw128(sA + s * A_SLOT + kk * 32), idesc, (kb | kk) != 0 ? 1u : 0u);
+            const uint64_t wd = sdesc_kmajor_sw128(sW + s * W_BYTES + kk * 32);
+            const uint64_t ad = sdesc_kmajor_sw128(sA + s * A_SLOT + kk * 32);
+            if (ep.fp8) umma_f8_pair(d_tmem, wd, ad, idesc, (kb | kk) != 0 ? 1u : 0u);
+            else umma_bf16_pair(d_tmem, wd, ad, idesc, (kb | kk) != 0 ? 1u : 0u);
           }
           umma_commit_pair(smem_u32(&ctl->empty[s]), 0x3);
           ++it;
@@ -289,6 +294,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int tq = q * 32 + lane;               // thread index within the warpgroup
     const int bar_id = 1 + wg;
     const float ea = ep.a, eb = ep.b;
+    // 8-bit operands: the accumulator times the input's and the weight's 1 / scale (exactly xv + acc
+    // for bf16, where dq = 1)
+    const float dq = ep.fp8 ? __ldg(ep.fp8_sa) * __ldg(ep.fp8_sw) : 1.f;
     const bool has_xm = ep.xm_out != nullptr, has_x = ep.x_out != nullptr;
     uint8_t* ring = smem + OFF_RING + wg * RING * SLOT;
     uint32_t k = 0;    // steps handled (ring position)
@@ -340,7 +348,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         float sq[16], xrv[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
-          const float xr = xv[j] + __uint_as_float(r[j]);
+          const float xr = fmaf(dq, __uint_as_float(r[j]), xv[j]);
           const float x = has_y ? fmaf(ea, xr, eb * yv[j]) : ea * xr;
           xrv[j] = xr;
           sq[j] = x * x;
@@ -425,7 +433,8 @@ int choose_nt(int M, int N, int max_pairs) {
 
 cudaError_t launch_gemm_resid(const bf16* A, const bf16* W, int M, int N, int K, const GemmEpi& ep, int num_sms,
                               cudaStream_t stream) {
-  if (M <= 0 || N <= 0 || K <= 0 || K % BK != 0 || N % SS_GROUP != 0) return cudaErrorInvalidValue;
+  if (M <= 0 || N <= 0 || K <= 0 || K % (ep.fp8 ? 2 * BK : BK) != 0 || N % SS_GROUP != 0) return cudaErrorInvalidValue;
+  if (ep.fp8 && (ep.fp8_sa == nullptr || ep.fp8_sw == nullptr)) return cudaErrorInvalidValue;
   if (ep.resid == nullptr || ep.xb == nullptr || ep.ssp_out == nullptr || ep.ncg != N / SS_GROUP)
     return cudaErrorInvalidValue;
   // the TMA boxes of the stream start on 16-byte boundaries
@@ -466,8 +475,14 @@ cudaError_t launch_gemm_resid(const bf16* A, const bf16* W, int M, int N, int K,
   CUtensorMap tw, ta;
   ResidMaps rm;
   const uint64_t Mu = static_cast<uint64_t>(M), Nu = static_cast<uint64_t>(N);
-  if (!make_tmap_bf16_2d(&tw, W, K, N, static_cast<uint64_t>(K) * 2, BK, BM)) return cudaErrorInvalidValue;
-  if (!make_tmap_bf16_2d(&ta, A, K, M, static_cast<uint64_t>(K) * 2, BK, NT / 2)) return cudaErrorInvalidValue;
+  if (ep.fp8) {   // e4m3 operands: rows of K bytes, one 128-byte stage row = 128 elements of K
+    const uint64_t Ku = static_cast<uint64_t>(K);
+    if (!make_tmap_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, W, Ku, N, Ku, 2 * BK, BM)) return cudaErrorInvalidValue;
+    if (!make_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, Ku, M, Ku, 2 * BK, NT / 2)) return cudaErrorInvalidValue;
+  } else {
+    if (!make_tmap_bf16_2d(&tw, W, K, N, static_cast<uint64_t>(K) * 2, BK, BM)) return cudaErrorInvalidValue;
+    if (!make_tmap_bf16_2d(&ta, A, K, M, static_cast<uint64_t>(K) * 2, BK, NT / 2)) return cudaErrorInvalidValue;
+  }
   auto f32map = [&](CUtensorMap* m, const float* p) {
     return make_tmap_2d(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p, Nu, Mu, Nu * 4, 32, CH, false);
   };

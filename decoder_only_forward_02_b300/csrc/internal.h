@@ -50,6 +50,15 @@ struct GemmEpi {
   // by the weight itself).  Both stored densely (row pitch = the contiguous extent).
   int a_mn = 0, b_mn = 0;
 
+  // 8-bit operands: A and B e4m3 (one byte per element, K-contiguous, K % 16 == 0), the tensor
+  // cores' kind::f8f6f4; the accumulator is dequantised by multiplying it by fp8_sa[0] (the input's
+  // 1 / scale) times fp8_sw[j] (the weight's), j = 0 except for EPI_QKV, where the q, k and v
+  // column ranges use fp8_sw[0], [1], [2].  The row scale of ssp_in does not apply (the quantised
+  // input already carries its RMSNorm).
+  int fp8 = 0;
+  const float* fp8_sa = nullptr;
+  const float* fp8_sw = nullptr;
+
   // Row scale of the consuming epilogues (RELU2, SOFTCAP, QKV, F32, CE_GRAD, DRELU2): rs[m] = 1 / sqrt(sum_g
   // ssp[m, g] / ncols + eps), ssp fp32 [M, ncg] partial sums of squares; ssp == null -> rs = 1.
   const float* ssp_in = nullptr;
@@ -86,6 +95,11 @@ struct GemmEpi {
   // gate = gate_scale * sigmoid(rs * (x . gate row)).
   int vgate = 0;
   float gate_scale = 1.f;
+  // With gpre set, a value-embedding head's gate pre-activation is read from gpre[m * gpre_ld + g]
+  // (already scaled by the row's RMSNorm) instead of the tile's gate column: the 8-bit path keeps
+  // the gate's dot product in bf16 (its packed gate rows are zero).
+  const float* gpre = nullptr;
+  int gpre_ld = 0;
   const bf16* ve = nullptr;       // [V, Hkv*D]
   const int32_t* tokens = nullptr;
   int V = 0;
@@ -212,6 +226,19 @@ cudaError_t launch_ce_finalize(const float* part, const float* zt, const int32_t
                                const int32_t* token_bytes, float* loss, float* stats, double* scratch,
                                int* status, cudaStream_t stream, float* lse = nullptr,
                                float* inv_count = nullptr);
+
+// ---- 8-bit (e4m3) tensorwise quantisation: q = e4m3(v * s), s = 448 / max|v| over the whole tensor
+// (1 when it is all zero), round to nearest even, saturating at +-448.  v = src[m, c], times the
+// row's RMSNorm scale rs[m] = 1 / sqrt(sum_g ssp[m, g] / C + eps) when ssp is given.  Two launches:
+// fp8_amax writes per-block maxima to partial[FP8_AMAX_BLOCKS]; fp8_quantize reduces them in every
+// block, writes q [M, ld_dst] and inv_scale[0] = 1 / s.  Rows of src are `ld` elements apart; dst
+// row r goes to r + (r / group) * gap (group = 0: no remap), for the packed q|k|v weight's v heads.
+constexpr int FP8_AMAX_BLOCKS = 296;
+cudaError_t launch_fp8_amax(const void* src, int src_f32, int M, int C, int ld, const float* ssp, float eps,
+                            float* partial, cudaStream_t stream);
+cudaError_t launch_fp8_quantize(const void* src, int src_f32, int M, int C, int ld, const float* ssp, float eps,
+                                const float* partial, uint8_t* dst, int ld_dst, int group, int gap,
+                                float* inv_scale, cudaStream_t stream);
 
 // Backward of the weightless RMSNorm xn = rs * x (rs = 1 / sqrt(mean x^2 + eps), from the partial
 // sums ssp [M, C / 128]) given G = rs * dL/dxn:  dx = G - rs^2 * x * mean(G * x)  (+ add, if set).

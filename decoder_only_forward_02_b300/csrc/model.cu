@@ -93,7 +93,12 @@ struct TimedLaunch {
 };
 
 struct Layout {
-  size_t x0, x, xm, xb, q, k, v, y, h, ssp, end;
+  size_t x0, x, xm, xb, q, k, v, y, h, ssp;
+  // 8-bit path only (zero-sized otherwise): quantised activations (the normed stream, the
+  // attention output, the MLP hidden layer), the bf16 gate pre-activations [M, 32], the amax
+  // scratch and the 1 / scale of each quantised activation
+  size_t a8, y8, h8, gpre, qpart, qscale;
+  size_t end;
 };
 
 // Where the last block's MLP down projection writes the lm_head's input when the backward runs:
@@ -120,6 +125,15 @@ struct nc_model {
   std::vector<const bf16*> wo, wfc, wproj, ve;
   bf16* wqkv = nullptr;     // packed per layer: [q rows | k rows | v rows (+ gate rows on VE layers)][C]
   std::vector<size_t> qkv_off;   // element offset of each layer's packed weight
+  // 8-bit weights (fp8 configs): e4m3 q|k|v at the same element offsets as wqkv, per-layer
+  // W_o, W_fc, W_proj and W_lm; bf16 gate matrices [GATE_PAD][C] per layer; 1 / scale per weight
+  uint8_t* wqkv8 = nullptr;
+  uint8_t* wo8 = nullptr;
+  uint8_t* wfc8 = nullptr;
+  uint8_t* wproj8 = nullptr;
+  uint8_t* lm8 = nullptr;
+  bf16* wg = nullptr;
+  float* wscale = nullptr;
   float2* rope = nullptr;   // [seq_len_ctx][D/2]
   int* status = nullptr;    // device status word
   int device = 0;           // the device current at creation (where packed_buf lives)
@@ -151,6 +165,8 @@ nc_status validate_config(const nc_config* c) {
   if (c->ve_gate_channels < 0 || c->ve_gate_channels > c->n_embd) return NC_ERR_INVALID_ARG;
   if (!(c->rms_eps >= 0.f) || !(c->softcap > 0.f) || !(c->rope_base > 0.f)) return NC_ERR_INVALID_ARG;
   if (c->logits_bf16 != 0 && c->logits_bf16 != 1) return NC_ERR_INVALID_ARG;
+  if (c->fp8 != 0 && c->fp8 != 1) return NC_ERR_INVALID_ARG;
+  if (c->fp8 && c->mlp_hidden % 128 != 0) return NC_ERR_UNSUPPORTED;   // the 8-bit down projection's K
   if (c->head_dim != 64 && c->head_dim != 128) return NC_ERR_UNSUPPORTED;
   if (c->n_embd % 128 != 0 || c->n_embd > 2048) return NC_ERR_UNSUPPORTED;
   if (c->mlp_hidden % 64 != 0 || c->vocab_size % 64 != 0) return NC_ERR_UNSUPPORTED;
@@ -158,13 +174,106 @@ nc_status validate_config(const nc_config* c) {
   return NC_OK;
 }
 
-size_t packed_bytes_for(const nc_config* c) {
-  const size_t status = ALIGN;
-  const size_t rope = align_up(static_cast<size_t>(c->seq_len_ctx) * (c->head_dim / 2) * sizeof(float2));
+size_t qkv_rows_total(const nc_config* c) {
   size_t rows = 0;
   for (int i = 0; i < c->n_layer; ++i)
     rows += (c->n_head + 2 * c->n_kv_head) * c->head_dim + (c->has_ve[i] ? c->n_kv_head * VGATE_ROWS : 0);
-  return status + rope + align_up(rows * c->n_embd * sizeof(bf16));
+  return rows;
+}
+
+// The 8-bit weights after the bf16 packed q|k|v (fp8 configs only), byte offsets from the start of
+// the packed buffer: e4m3 q|k|v in the bf16 one's row layout (gate rows zero), per layer W_o, W_fc,
+// W_proj, then W_lm; per layer a bf16 [GATE_PAD, C] matrix of the value-embedding gate rows (the
+// gate's dot product stays bf16); 1 / scale of every quantised weight ([6 L + 1] floats: q, k, v,
+// o, fc, proj per layer, then the lm_head); the amax scratch of the weight quantisation.
+constexpr int GATE_PAD = 32;
+struct Fp8Pack {
+  size_t qkv8, wo8, wfc8, wproj8, lm8, wg, wscale, part, end;
+};
+
+Fp8Pack fp8_pack_for(const nc_config* c, size_t start) {
+  const size_t C = c->n_embd, HD = static_cast<size_t>(c->n_head) * c->head_dim, F = c->mlp_hidden;
+  const size_t L = c->n_layer;
+  Fp8Pack p{};
+  size_t off = start;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off += align_up(bytes);
+    return o;
+  };
+  p.qkv8 = take(qkv_rows_total(c) * C);
+  p.wo8 = take(L * C * HD);
+  p.wfc8 = take(L * F * C);
+  p.wproj8 = take(L * C * F);
+  p.lm8 = take(static_cast<size_t>(c->vocab_size) * C);
+  p.wg = take(L * GATE_PAD * C * sizeof(bf16));
+  p.wscale = take((6 * L + 1) * sizeof(float));
+  p.part = take(nc::FP8_AMAX_BLOCKS * sizeof(float));
+  p.end = off;
+  return p;
+}
+
+size_t packed_bf16_end(const nc_config* c) {
+  const size_t status = ALIGN;
+  const size_t rope = align_up(static_cast<size_t>(c->seq_len_ctx) * (c->head_dim / 2) * sizeof(float2));
+  return status + rope + align_up(qkv_rows_total(c) * c->n_embd * sizeof(bf16));
+}
+
+size_t packed_bytes_for(const nc_config* c) {
+  const size_t end = packed_bf16_end(c);
+  return c->fp8 ? fp8_pack_for(c, end).end : end;
+}
+
+// Quantises one weight tensor [rows, cols] (bf16) to e4m3 at its own tensorwise scale, into dst
+// (rows remapped as launch_fp8_quantize describes), 1 / scale into *inv.
+cudaError_t quantize_weight(const void* src, int rows, int cols, uint8_t* dst, int group, int gap, float* inv,
+                            float* part, cudaStream_t stream) {
+  cudaError_t e = nc::launch_fp8_amax(src, 0, rows, cols, cols, nullptr, 0.f, part, stream);
+  if (e == cudaSuccess)
+    e = nc::launch_fp8_quantize(src, 0, rows, cols, cols, nullptr, 0.f, part, dst, cols, group, gap, inv, stream);
+  return e;
+}
+
+// The 8-bit copies of every linear layer's weight and the bf16 gate matrices (fp8 configs).
+cudaError_t pack_fp8(nc_model* m, const nc_weights* w, uint8_t* base, cudaStream_t stream) {
+  const nc_config* c = &m->cfg;
+  const Fp8Pack p = fp8_pack_for(c, packed_bf16_end(c));
+  const int L = c->n_layer, C = c->n_embd, D = c->head_dim, F = c->mlp_hidden;
+  const int qd = c->n_head * D, kd = c->n_kv_head * D;
+  const size_t c_g = c->ve_gate_channels ? c->ve_gate_channels : C;
+  m->wqkv8 = base + p.qkv8;
+  m->wo8 = base + p.wo8;
+  m->wfc8 = base + p.wfc8;
+  m->wproj8 = base + p.wproj8;
+  m->lm8 = base + p.lm8;
+  m->wg = reinterpret_cast<bf16*>(base + p.wg);
+  m->wscale = reinterpret_cast<float*>(base + p.wscale);
+  float* part = reinterpret_cast<float*>(base + p.part);
+  cudaError_t e = cudaMemsetAsync(m->wqkv8, 0, p.wo8 - p.qkv8, stream);   // gate rows stay zero
+  if (e == cudaSuccess) e = cudaMemsetAsync(m->wg, 0, p.wscale - p.wg, stream);
+  for (int i = 0; i < L && e == cudaSuccess; ++i) {
+    uint8_t* q8 = m->wqkv8 + m->qkv_off[i];
+    float* s = m->wscale + 6 * i;
+    const bool ve = m->has_ve[i] != 0;
+    e = quantize_weight(w->wq[i], qd, C, q8, 0, 0, s + 0, part, stream);
+    if (e == cudaSuccess) e = quantize_weight(w->wk[i], kd, C, q8 + static_cast<size_t>(qd) * C, 0, 0, s + 1, part, stream);
+    if (e == cudaSuccess)   // v heads: D rows each, followed by VGATE_ROWS (zero) rows on value-embedding layers
+      e = quantize_weight(w->wv[i], kd, C, q8 + static_cast<size_t>(qd + kd) * C, ve ? D : 0, ve ? VGATE_ROWS : 0,
+                          s + 2, part, stream);
+    if (e == cudaSuccess)
+      e = quantize_weight(w->wo[i], C, qd, m->wo8 + static_cast<size_t>(i) * C * qd, 0, 0, s + 3, part, stream);
+    if (e == cudaSuccess)
+      e = quantize_weight(w->wfc[i], F, C, m->wfc8 + static_cast<size_t>(i) * F * C, 0, 0, s + 4, part, stream);
+    if (e == cudaSuccess)
+      e = quantize_weight(w->wproj[i], C, F, m->wproj8 + static_cast<size_t>(i) * C * F, 0, 0, s + 5, part, stream);
+    for (int g = 0; ve && g < c->n_kv_head && e == cudaSuccess; ++g)   // gate row g: first c_g columns
+      e = cudaMemcpyAsync(m->wg + (static_cast<size_t>(i) * GATE_PAD + g) * C,
+                          static_cast<const bf16*>(w->ve_gate[i]) + g * c_g, c_g * 2, cudaMemcpyDeviceToDevice,
+                          stream);
+  }
+  if (e == cudaSuccess)
+    e = quantize_weight(w->lm_head, c->vocab_size, C, m->lm8, 0, 0, m->wscale + 6 * L, part, stream);
+  return e;
 }
 
 Layout layout_for(const nc_model* m, int B, int T) {
@@ -187,6 +296,13 @@ Layout layout_for(const nc_model* m, int B, int T) {
   L.y = take(M * c.n_head * c.head_dim * 2);
   L.h = take(M * c.mlp_hidden * 2);
   L.ssp = take(M * (c.n_embd / nc::SS_GROUP) * 4);
+  const size_t f8 = c.fp8 ? 1 : 0;
+  L.a8 = take(f8 * M * c.n_embd);
+  L.y8 = take(f8 * M * c.n_head * c.head_dim);
+  L.h8 = take(f8 * M * c.mlp_hidden);
+  L.gpre = take(f8 * M * 32 * 4);
+  L.qpart = take(f8 * nc::FP8_AMAX_BLOCKS * 4);
+  L.qscale = take(f8 * 8 * 4);
   L.end = off;
   return L;
 }
@@ -250,7 +366,8 @@ const char* nc_last_cuda_error(void) { return nc::last_cuda_error_name(); }
 const char* nc_kernel_class_name(nc_kernel_class k) {
   static const char* names[NC_K_COUNT] = {"embed_smear",   "qkv_rope_qknorm_ve", "attention",  "oproj_residual",
                                           "fc_relu2",      "proj_residual",      "lmhead_softcap", "cross_entropy",
-                                          "lmhead_grad",   "mlp_grad",           "oproj_grad",     "rmsnorm_grad"};
+                                          "lmhead_grad",   "mlp_grad",           "oproj_grad",     "rmsnorm_grad",
+                                          "fp8_quantize"};
   return (k >= 0 && k < NC_K_COUNT) ? names[k] : "unknown";
 }
 
@@ -351,6 +468,7 @@ nc_status nc_model_create(const nc_config* cfg, const nc_weights* w, void* packe
                             cudaMemcpyDeviceToDevice, stream);
     }
   }
+  if (e == cudaSuccess && cfg->fp8) e = pack_fp8(m, w, base, stream);
   if (e == cudaSuccess) e = cudaMemsetAsync(m->status, 0, sizeof(int), stream);
   if (e == cudaSuccess)
     e = nc::launch_rope_table(m->rope, cfg->seq_len_ctx, cfg->head_dim, cfg->rope_base, stream);
@@ -482,6 +600,29 @@ cudaError_t run_blocks(nc_model* m, const int32_t* tokens, int B, int T, const L
     e.status = m->status;
   };
 
+  // 8-bit path: every linear layer's input is quantised as one tensor over the batch (its amax,
+  // then its e4m3 codes; the normed stream from the fp32 x with its RMSNorm row scale), and its
+  // GEMM runs on the e4m3 copies of input and weight, dequantised in the epilogue.
+  const bool f8 = c.fp8 != 0;
+  uint8_t* a8 = ws + Lo.a8;
+  uint8_t* y8 = ws + Lo.y8;
+  uint8_t* h8 = ws + Lo.h8;
+  float* gpre = reinterpret_cast<float*>(ws + Lo.gpre);
+  float* qpart = reinterpret_cast<float*>(ws + Lo.qpart);
+  float* qscale = reinterpret_cast<float*>(ws + Lo.qscale);   // 1 / scale: [0] q|k|v input, [1] y, [2] fc input, [3] h
+  auto quant = [&](const void* src, int f32, int cols, const float* row_ssp, uint8_t* dst, float* inv) {
+    cudaError_t r = timed(m, NC_K_QUANT, stream, [&] {
+      return nc::launch_fp8_amax(src, f32, M, cols, cols, row_ssp, c.rms_eps, qpart, stream);
+    });
+    if (r == cudaSuccess)
+      r = timed(m, NC_K_QUANT, stream, [&] {
+        return nc::launch_fp8_quantize(src, f32, M, cols, cols, row_ssp, c.rms_eps, qpart, dst, cols, 0, 0, inv,
+                                       stream);
+      });
+    return r;
+  };
+  auto as8 = [](const void* p) { return static_cast<const bf16*>(p); };   // e4m3 operands travel as untyped bytes
+
   cudaError_t e = timed(m, NC_K_EMBED, stream, [&] {
     return nc::launch_embed_smear(tokens, B, T, m->wte, V, C, m->smear, c_s, c.embed_norm, c.rms_eps,
                                   m->lr[0] + m->l0[0], x0, x, xb, ssp, m->status, stream);
@@ -506,8 +647,30 @@ cudaError_t run_blocks(nc_model* m, const int32_t* tokens, int B, int T, const L
     qe.ve = m->ve[i];
     qe.tokens = tokens;
     qe.V = V;
+    if (f8) {
+      e = quant(x, 1, C, ssp, a8, qscale + 0);
+      if (e == cudaSuccess && ve) {   // the value-embedding gates' dot products, bf16: rs * (xb . W_g^T)
+        nc::GemmEpi ge;
+        set_consumer(ge, m, ssp);
+        ge.kind = nc::EPI_F32;
+        ge.out = gpre;
+        ge.ldo = 32;
+        e = timed(m, NC_K_QKV, stream, [&] {
+          return nc::launch_gemm(xb, m->wg + static_cast<size_t>(i) * GATE_PAD * C, M, GATE_PAD, C, ge, m->num_sms,
+                                 stream);
+        });
+      }
+      if (e != cudaSuccess) break;
+      qe.ssp_in = nullptr;
+      qe.fp8 = 1;
+      qe.fp8_sa = qscale + 0;
+      qe.fp8_sw = m->wscale + 6 * i;
+      qe.gpre = ve ? gpre : nullptr;
+      qe.gpre_ld = 32;
+    }
     e = timed(m, NC_K_QKV, stream, [&] {
-      return nc::launch_gemm(xb, m->wqkv + m->qkv_off[i], M, m->Nqkv(i), C, qe, m->num_sms, stream);
+      return f8 ? nc::launch_gemm(as8(a8), as8(m->wqkv8 + m->qkv_off[i]), M, m->Nqkv(i), C, qe, m->num_sms, stream)
+                : nc::launch_gemm(xb, m->wqkv + m->qkv_off[i], M, m->Nqkv(i), C, qe, m->num_sms, stream);
     });
     if (e != cudaSuccess) break;
     if (kv != nullptr) {
@@ -536,14 +699,37 @@ cudaError_t run_blocks(nc_model* m, const int32_t* tokens, int B, int T, const L
     if (e != cudaSuccess) break;
     nc::GemmEpi oe;
     resid(oe);
-    e = timed(m, NC_K_OPROJ, stream, [&] { return nc::launch_gemm_resid(y, m->wo[i], M, C, H * D, oe, m->num_sms, stream); });
+    if (f8) {
+      e = quant(y, 0, H * D, nullptr, y8, qscale + 1);
+      if (e != cudaSuccess) break;
+      oe.fp8 = 1;
+      oe.fp8_sa = qscale + 1;
+      oe.fp8_sw = m->wscale + 6 * i + 3;
+    }
+    e = timed(m, NC_K_OPROJ, stream, [&] {
+      return f8 ? nc::launch_gemm_resid(as8(y8), as8(m->wo8 + static_cast<size_t>(i) * C * H * D), M, C, H * D, oe,
+                                        m->num_sms, stream)
+                : nc::launch_gemm_resid(y, m->wo[i], M, C, H * D, oe, m->num_sms, stream);
+    });
     if (e != cudaSuccess) break;
     nc::GemmEpi fe;
     set_consumer(fe, m, ssp);
     fe.kind = nc::EPI_RELU2_BF16;
     fe.out = h;
     fe.ldo = F;
-    e = timed(m, NC_K_FC, stream, [&] { return nc::launch_gemm(xb, m->wfc[i], M, F, C, fe, m->num_sms, stream); });
+    if (f8) {
+      e = quant(x, 1, C, ssp, a8, qscale + 2);
+      if (e != cudaSuccess) break;
+      fe.ssp_in = nullptr;
+      fe.fp8 = 1;
+      fe.fp8_sa = qscale + 2;
+      fe.fp8_sw = m->wscale + 6 * i + 4;
+    }
+    e = timed(m, NC_K_FC, stream, [&] {
+      return f8 ? nc::launch_gemm(as8(a8), as8(m->wfc8 + static_cast<size_t>(i) * F * C), M, F, C, fe, m->num_sms,
+                                  stream)
+                : nc::launch_gemm(xb, m->wfc[i], M, F, C, fe, m->num_sms, stream);
+    });
     if (e != cudaSuccess) break;
     nc::GemmEpi pe;
     resid(pe);
@@ -564,8 +750,20 @@ cudaError_t run_blocks(nc_model* m, const int32_t* tokens, int B, int T, const L
         pe.xb = tail->xbf;
         pe.ssp_out = tail->sspf;
       }
+      if (f8) pe.x_out = x;   // the lm_head's input is quantised from the fp32 stream
     }
-    e = timed(m, NC_K_PROJ, stream, [&] { return nc::launch_gemm_resid(h, m->wproj[i], M, C, F, pe, m->num_sms, stream); });
+    if (f8) {
+      e = quant(h, 0, F, nullptr, h8, qscale + 3);
+      if (e != cudaSuccess) break;
+      pe.fp8 = 1;
+      pe.fp8_sa = qscale + 3;
+      pe.fp8_sw = m->wscale + 6 * i + 5;
+    }
+    e = timed(m, NC_K_PROJ, stream, [&] {
+      return f8 ? nc::launch_gemm_resid(as8(h8), as8(m->wproj8 + static_cast<size_t>(i) * C * F), M, C, F, pe,
+                                        m->num_sms, stream)
+                : nc::launch_gemm_resid(h, m->wproj[i], M, C, F, pe, m->num_sms, stream);
+    });
   }
   return e;
 }
@@ -637,17 +835,52 @@ namespace {
 // Bytes of one logit in the caller's output.
 size_t logit_bytes(const nc_model* m) { return m->cfg.logits_bf16 ? 2 : 4; }
 
-// The lm_head with the final RMSNorm (row scale from ssp) and the soft-cap, writing fp32 or bf16
-// logits [M, V] as the config asks.
-cudaError_t launch_lm_head(nc_model* m, const bf16* xb, float* ssp, int M, void* logits, cudaStream_t stream) {
-  nc::GemmEpi le;
+// The lm_head's operands: the bf16 final stream xb with the final RMSNorm as the epilogue's row
+// scale, or on the 8-bit path the e4m3 quantisation of the normed final stream (from the fp32 x)
+// and the e4m3 W_lm, dequantised in the epilogue.
+cudaError_t lm_head_operands(nc_model* m, uint8_t* ws, const Layout& Lo, int M, cudaStream_t stream, nc::GemmEpi& le,
+                             const bf16** A, const bf16** W) {
+  float* ssp = reinterpret_cast<float*>(ws + Lo.ssp);
   set_consumer(le, m, ssp);
+  if (!m->cfg.fp8) {
+    *A = reinterpret_cast<const bf16*>(ws + Lo.xb);
+    *W = m->lm;
+    return cudaSuccess;
+  }
+  const int C = m->C();
+  const float* x = reinterpret_cast<const float*>(ws + Lo.x);
+  float* qpart = reinterpret_cast<float*>(ws + Lo.qpart);
+  float* inv = reinterpret_cast<float*>(ws + Lo.qscale) + 4;
+  uint8_t* a8 = ws + Lo.a8;
+  cudaError_t e = timed(m, NC_K_QUANT, stream, [&] {
+    return nc::launch_fp8_amax(x, 1, M, C, C, ssp, m->cfg.rms_eps, qpart, stream);
+  });
+  if (e == cudaSuccess)
+    e = timed(m, NC_K_QUANT, stream, [&] {
+      return nc::launch_fp8_quantize(x, 1, M, C, C, ssp, m->cfg.rms_eps, qpart, a8, C, 0, 0, inv, stream);
+    });
+  le.ssp_in = nullptr;
+  le.fp8 = 1;
+  le.fp8_sa = inv;
+  le.fp8_sw = m->wscale + 6 * m->cfg.n_layer;
+  *A = reinterpret_cast<const bf16*>(a8);
+  *W = reinterpret_cast<const bf16*>(m->lm8);
+  return e;
+}
+
+// The lm_head with the final RMSNorm and the soft-cap, writing fp32 or bf16 logits [M, V] as the
+// config asks.
+cudaError_t launch_lm_head(nc_model* m, uint8_t* ws, const Layout& Lo, int M, void* logits, cudaStream_t stream) {
+  nc::GemmEpi le;
+  const bf16 *A = nullptr, *W = nullptr;
+  cudaError_t e = lm_head_operands(m, ws, Lo, M, stream, le, &A, &W);
+  if (e != cudaSuccess) return e;
   le.kind = m->cfg.logits_bf16 ? nc::EPI_SOFTCAP_BF16 : nc::EPI_SOFTCAP_F32;
   le.out = logits;
   le.ldo = m->cfg.vocab_size;
   le.cap = m->cfg.softcap;
   return timed(m, NC_K_LMHEAD, stream, [&] {
-    return nc::launch_gemm(xb, m->lm, M, m->cfg.vocab_size, m->C(), le, m->num_sms, stream);
+    return nc::launch_gemm(A, W, M, m->cfg.vocab_size, m->C(), le, m->num_sms, stream);
   });
 }
 
@@ -664,8 +897,7 @@ nc_status nc_forward(nc_model* m, const int32_t* tokens, int B, int T, void* log
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   cudaError_t e = run_blocks(m, tokens, B, T, Lo, ws, stream);
   if (e == cudaSuccess)
-    e = launch_lm_head(m, reinterpret_cast<bf16*>(ws + Lo.xb), reinterpret_cast<float*>(ws + Lo.ssp), B * T, logits,
-                       stream);
+    e = launch_lm_head(m, ws, Lo, B * T, logits, stream);
   return nc::cuda_status(e);
 }
 
@@ -696,15 +928,15 @@ nc_status nc_forward_loss(nc_model* m, const int32_t* tokens, const int32_t* tar
   cudaError_t e = run_blocks(m, tokens, B, T, Lo, ws, stream);
   if (e == cudaSuccess) {
     nc::GemmEpi le;
-    set_consumer(le, m, reinterpret_cast<float*>(ws + Lo.ssp));
+    const bf16 *A = nullptr, *W = nullptr;
+    e = lm_head_operands(m, ws, Lo, M, stream, le, &A, &W);
     le.kind = nc::EPI_CE;
     le.cap = m->cfg.softcap;
     le.targets = targets;
     le.ce_part = part;
     le.ce_zt = zt;
-    e = timed(m, NC_K_LMHEAD, stream, [&] {
-      return nc::launch_gemm(reinterpret_cast<bf16*>(ws + Lo.xb), m->lm, M, V, m->C(), le, m->num_sms, stream);
-    });
+    if (e == cudaSuccess)
+      e = timed(m, NC_K_LMHEAD, stream, [&] { return nc::launch_gemm(A, W, M, V, m->C(), le, m->num_sms, stream); });
   }
   if (e == cudaSuccess)
     e = timed(m, NC_K_LOSS, stream, [&] {
@@ -716,6 +948,7 @@ nc_status nc_forward_loss(nc_model* m, const int32_t* tokens, const int32_t* tar
 
 nc_status nc_workspace_bytes_grad_tail(const nc_model* m, int B, int T, size_t* bytes) {
   if (m == nullptr || bytes == nullptr || B < 1 || T < 1) return NC_ERR_INVALID_ARG;
+  if (m->cfg.fp8) return NC_ERR_UNSUPPORTED;   // the backward runs on the bf16 path
   if (T > m->cfg.seq_len_ctx) return NC_ERR_UNSUPPORTED;
   if (static_cast<long long>(B) * T > (1LL << 30)) return NC_ERR_UNSUPPORTED;
   const Layout Lo = layout_for(m, B, T);
@@ -729,6 +962,7 @@ nc_status nc_forward_loss_grad_tail(nc_model* m, const int32_t* tokens, const in
                                     size_t ws_bytes, void* stream_) {
   nc_status s = check_forward_args(m, tokens, B, T, workspace);
   if (s != NC_OK) return s;
+  if (m->cfg.fp8) return NC_ERR_UNSUPPORTED;
   if (targets == nullptr || stats == nullptr || !aligned(targets, 4) || !aligned(stats, 4) ||
       (token_bytes != nullptr && !aligned(token_bytes, 4)))
     return NC_ERR_INVALID_ARG;
@@ -872,6 +1106,9 @@ nc_status nc_forward_loss_grad_tail(nc_model* m, const int32_t* tokens, const in
 
 nc_status nc_kv_cache_bytes(const nc_model* m, int B, int T_max, size_t* bytes) {
   if (m == nullptr || bytes == nullptr || B < 1 || T_max < 1) return NC_ERR_INVALID_ARG;
+  // the 8-bit path's scales span the whole batch of a call, so a decode step could not reproduce
+  // the full forward: the cache paths run bf16 only
+  if (m->cfg.fp8) return NC_ERR_UNSUPPORTED;
   if (T_max > m->cfg.seq_len_ctx) return NC_ERR_UNSUPPORTED;
   *bytes = kv_cache_bytes(m, B, T_max);
   return NC_OK;
@@ -881,6 +1118,7 @@ nc_status nc_prefill(nc_model* m, const int32_t* tokens, int B, int T, void* kv_
                      int T_max, void* logits, void* workspace, size_t ws_bytes, void* stream_) {
   nc_status s = check_forward_args(m, tokens, B, T, workspace);
   if (s != NC_OK) return s;
+  if (m->cfg.fp8) return NC_ERR_UNSUPPORTED;
   if (logits == nullptr || !aligned(logits, 16) || kv_cache == nullptr || !aligned(kv_cache, ALIGN))
     return NC_ERR_INVALID_ARG;
   if (T_max < T) return NC_ERR_INVALID_ARG;
@@ -895,13 +1133,13 @@ nc_status nc_prefill(nc_model* m, const int32_t* tokens, int B, int T, void* kv_
   kv.T_max = T_max;
   cudaError_t e = run_blocks(m, tokens, B, T, Lo, ws, stream, &kv);
   if (e == cudaSuccess)
-    e = launch_lm_head(m, reinterpret_cast<bf16*>(ws + Lo.xb), reinterpret_cast<float*>(ws + Lo.ssp), B * T, logits,
-                       stream);
+    e = launch_lm_head(m, ws, Lo, B * T, logits, stream);
   return nc::cuda_status(e);
 }
 
 nc_status nc_workspace_bytes_decode(const nc_model* m, int B, size_t* bytes) {
   if (m == nullptr || bytes == nullptr || B < 1) return NC_ERR_INVALID_ARG;
+  if (m->cfg.fp8) return NC_ERR_UNSUPPORTED;
   if (m->cfg.seq_len_ctx < 2) return NC_ERR_UNSUPPORTED;
   const size_t rows = 2 * static_cast<size_t>(B);
   *bytes = layout_for(m, B, 2).end + align_up(rows * 4) + align_up(rows * m->cfg.vocab_size * logit_bytes(m)) +
@@ -916,6 +1154,7 @@ nc_status nc_decode_step(nc_model* m, const int32_t* prev_tokens, const int32_t*
       workspace == nullptr || B < 1)
     return NC_ERR_INVALID_ARG;
   if (!on_model_device(m)) return NC_ERR_INVALID_ARG;
+  if (m->cfg.fp8) return NC_ERR_UNSUPPORTED;
   if (!aligned(prev_tokens, 4) || !aligned(tokens, 4) || !aligned(logits, 16) || !aligned(kv_cache, ALIGN) ||
       !aligned(workspace, ALIGN))
     return NC_ERR_INVALID_ARG;
@@ -949,8 +1188,7 @@ nc_status nc_decode_step(nc_model* m, const int32_t* prev_tokens, const int32_t*
   kv.scratch_floats = decode_scratch_floats(m, B);
   if (e == cudaSuccess) e = run_blocks(m, pair, B, 2, Lo, ws, stream, &kv);
   if (e == cudaSuccess)
-    e = launch_lm_head(m, reinterpret_cast<bf16*>(ws + Lo.xb), reinterpret_cast<float*>(ws + Lo.ssp), 2 * B, logits2,
-                       stream);
+    e = launch_lm_head(m, ws, Lo, 2 * B, logits2, stream);
   if (e == cudaSuccess)   // the second row of each pair
     e = cudaMemcpy2DAsync(logits, static_cast<size_t>(V) * lb, logits2 + V * lb, 2 * static_cast<size_t>(V) * lb,
                           static_cast<size_t>(V) * lb, B, cudaMemcpyDeviceToDevice, stream);
@@ -1020,7 +1258,12 @@ nc_status nc_timing_read(nc_model* m, nc_kernel_class k, double* total_ms, int* 
 
 int nc_forward_launch_count(const nc_model* m) {
   if (m == nullptr) return 0;
-  return 2 + 5 * m->cfg.n_layer;
+  if (!m->cfg.fp8) return 2 + 5 * m->cfg.n_layer;
+  // 8-bit: per block four quantisations (two launches each) and the gate product on
+  // value-embedding layers; the lm_head's input quantisation
+  int ve = 0;
+  for (int i = 0; i < m->cfg.n_layer; ++i) ve += m->has_ve[i] ? 1 : 0;
+  return 2 + 5 * m->cfg.n_layer + 8 * m->cfg.n_layer + ve + 2;
 }
 
 int nc_kv_launch_count(const nc_model* m) {

@@ -283,6 +283,50 @@ nc_status nc_op_ce_finalize(const float* part, const float* zt, const int32_t* t
                                             static_cast<cudaStream_t>(stream), lse, inv_count));
 }
 
+size_t nc_op_fp8_scratch_bytes(void) { return static_cast<size_t>(nc::FP8_AMAX_BLOCKS) * sizeof(float); }
+
+nc_status nc_op_fp8_quantize(const void* src, int src_f32, int M, int C, const float* ssp, float eps, void* dst,
+                             float* inv_scale, void* scratch, void* stream) {
+  if (!al(src, 16) || !al(dst, 8) || !al(inv_scale, 4) || !al(scratch, 4) || M < 1 || C < 8 ||
+      (src_f32 != 0 && src_f32 != 1) || !al_or_null(ssp, 4) || !(eps >= 0.f))
+    return NC_ERR_INVALID_ARG;
+  if (C % 8 != 0 || (ssp != nullptr && C % nc::SS_GROUP != 0)) return NC_ERR_UNSUPPORTED;
+  float* part = static_cast<float*>(scratch);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = nc::launch_fp8_amax(src, src_f32, M, C, C, ssp, eps, part, s);
+  if (e == cudaSuccess)
+    e = nc::launch_fp8_quantize(src, src_f32, M, C, C, ssp, eps, part, static_cast<uint8_t*>(dst), C, 0, 0, inv_scale,
+                                s);
+  return cuda_status(e);
+}
+
+nc_status nc_op_gemm_fp8(const void* A8, const void* B8, int M, int N, int K, nc_epilogue epi, void* out, int ldo,
+                         const float* inv_sa, const float* inv_sb, float cap, int* status, void* stream) {
+  if (!al(A8, 16) || !al(B8, 16) || !al(out, 16) || !al(inv_sa, 4) || !al(inv_sb, 4) || M < 1 || N < 1 || K < 1 ||
+      ldo < N || ldo % 8 != 0)
+    return NC_ERR_INVALID_ARG;
+  if (K % 16 != 0 || N % 32 != 0) return NC_ERR_UNSUPPORTED;
+  nc::GemmEpi e;
+  switch (epi) {
+    case NC_EPI_BF16: e.kind = nc::EPI_BF16; break;
+    case NC_EPI_RELU2_BF16: e.kind = nc::EPI_RELU2_BF16; break;
+    case NC_EPI_SOFTCAP_F32: e.kind = nc::EPI_SOFTCAP_F32; break;
+    case NC_EPI_SOFTCAP_BF16: e.kind = nc::EPI_SOFTCAP_BF16; break;
+    case NC_EPI_F32: e.kind = nc::EPI_F32; break;
+    default: return NC_ERR_INVALID_ARG;
+  }
+  if ((epi == NC_EPI_SOFTCAP_F32 || epi == NC_EPI_SOFTCAP_BF16) && !(cap > 0.f)) return NC_ERR_INVALID_ARG;
+  e.fp8 = 1;
+  e.fp8_sa = inv_sa;
+  e.fp8_sw = inv_sb;
+  e.out = out;
+  e.ldo = ldo;
+  e.cap = cap;
+  e.status = status;
+  return cuda_status(nc::launch_gemm(static_cast<const nc::bf16*>(A8), static_cast<const nc::bf16*>(B8), M, N, K, e,
+                                     device_sms(), static_cast<cudaStream_t>(stream)));
+}
+
 nc_status nc_op_test_wait_timeout(const void* A, const void* B, int M, int N, int K, void* out, int ldo,
                                   unsigned long long limit_ns, int skip_tile, int* status, void* stream) {
   if (!al(A, 16) || !al(B, 16) || !al(out, 16) || status == nullptr || M < 1 || N < 1 || K < 1 || ldo < N ||

@@ -103,6 +103,9 @@ typedef struct {
   float softcap;              /* default 15 */
   int logits_bf16;            /* 0: logits are fp32 (default); 1: bf16 (the same soft-capped values
                                  rounded to nearest even: half the bytes to write and to copy out) */
+  int fp8;                    /* 0: bf16 linear layers (default); 1: every linear layer (q, k, v, output
+                                 projection, MLP up and down projections, lm_head) in e4m3 with
+                                 tensorwise scales, see nc_forward; needs mlp_hidden % 128 == 0 */
 } nc_config;
 
 /* Weights.  Matrices are bf16, row-major in the nn.Linear layout [out, in],
@@ -299,7 +302,8 @@ typedef enum {
   NC_K_MLP_GRAD = 9,  /* backward: the last block's MLP gradient products */
   NC_K_OPROJ_GRAD = 10, /* backward: the last block's attention output projection weight gradient */
   NC_K_RMS_GRAD = 11, /* backward: RMSNorm backward (+ residual gradient) */
-  NC_K_COUNT = 12
+  NC_K_QUANT = 12,    /* 8-bit path: tensorwise amax and e4m3 quantisation of a layer's input */
+  NC_K_COUNT = 13
 } nc_kernel_class;
 
 /* enable != 0: every following nc_forward records an event pair around each

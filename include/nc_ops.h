@@ -151,6 +151,25 @@ NC_API nc_status nc_op_mlp_hidden_grad(const void *dy, const void *w, int M, int
 NC_API nc_status nc_op_rms_backward(const float *G, const float *x, const float *ssp, const float *add, int M,
                                     int C, float eps, float *dx_f32, void *dx_b16, void *stream);
 
+/* ---- 8-bit (e4m3) tensorwise quantisation and product (the fp8 path of nc_forward) ---- */
+
+/* q = e4m3(v * s) with s = 448 / max|v| over the whole [M, C] tensor (s = 1 if it is all zero),
+ * round to nearest even, saturating at +-448; v = src[m, c] (bf16, or fp32 with src_f32), times the
+ * row's RMSNorm scale 1 / sqrt(sum_g ssp[m, g] / C + eps) when ssp (fp32 [M, C / 128]) is given.
+ * dst: e4m3 bytes [M, C], 8-byte aligned; inv_scale: one fp32, receives 1 / s.  scratch: device,
+ * >= nc_op_fp8_scratch_bytes() bytes, 4-byte aligned.  C % 8 == 0 (C % 128 == 0 with ssp). */
+NC_API size_t nc_op_fp8_scratch_bytes(void);
+NC_API nc_status nc_op_fp8_quantize(const void *src, int src_f32, int M, int C, const float *ssp, float eps,
+                                    void *dst, float *inv_scale, void *scratch, void *stream);
+
+/* acc[M, N] = A8[M, K] . B8[N, K]^T of e4m3 operands (tcgen05 kind::f8f6f4, fp32 accumulation),
+ * dequantised by inv_sa[0] * inv_sb[0] (device fp32 scalars), then the epilogue (NC_EPI_BF16,
+ * NC_EPI_RELU2_BF16, NC_EPI_SOFTCAP_F32, NC_EPI_SOFTCAP_BF16 or NC_EPI_F32; no row scale).
+ * K % 16 == 0, N % 32 == 0, ldo >= N, 16-byte aligned rows. */
+NC_API nc_status nc_op_gemm_fp8(const void *A8, const void *B8, int M, int N, int K, nc_epilogue epi, void *out,
+                                int ldo, const float *inv_sa, const float *inv_sb, float cap, int *status,
+                                void *stream);
+
 /* Test of the bounded device-side waits (failure detection without a GPU fault): the GEMM of
  * nc_op_gemm with NC_EPI_BF16, every wait of the launch limited to limit_ns (1e5 .. 1e8 ns), and the
  * tensor-core issuer withholding the "accumulator ready" signal of pair tile skip_tile (pair tiles

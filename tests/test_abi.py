@@ -111,8 +111,8 @@ def test_null_arguments_rejected_without_device_work():
 
 def test_kernel_class_names():
     lib = B.lib()
-    assert [lib.nc_kernel_class_name(i).decode() for i in range(12)] == B.KERNEL_CLASSES
-    assert lib.nc_kernel_class_name(12) == b"unknown"
+    assert [lib.nc_kernel_class_name(i).decode() for i in range(13)] == B.KERNEL_CLASSES
+    assert lib.nc_kernel_class_name(13) == b"unknown"
 
 
 def test_headers_are_plain_c_and_link(tmp_path):
