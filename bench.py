@@ -483,6 +483,55 @@ def run_ours(args, rank, world, local_rank):
         del m16, z16
         torch.cuda.empty_cache()
 
+    # The 8-bit path (every linear layer in e4m3 at tensorwise scales, activations quantised on the
+    # fly): the same forward timed the same way, with per-kernel rates; contractions against the
+    # e4m3 peak (the measured bf16 figure times 2, the nominal dense ratio), quantisation against HBM.
+    fp8_path = None
+    if not args.no_fp8:
+        m8 = NB.Model(cfg, wts, device=dev, fp8=True)
+        z8 = torch.empty((B, T, V), dtype=torch.float32, device=dev)
+        for _ in range(3):
+            m8.forward(tok, out=z8)
+        n8 = max(1, min(args.steps, 50))
+        barrier()
+        torch.cuda.synchronize()
+        e8 = torch.cuda.Event(enable_timing=True)
+        e9 = torch.cuda.Event(enable_timing=True)
+        e8.record(stream)
+        for _ in range(n8):
+            m8.forward(tok, out=z8)
+        e9.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        if m8.status() != 0:
+            raise RuntimeError("device status set on the 8-bit forward")
+        ms8 = max_over_ranks(e8.elapsed_time(e9), world, dev) / n8
+        m8.timing(True)
+        for _ in range(3):
+            m8.forward(tok, out=z8)
+        torch.cuda.synchronize()
+        t8 = m8.timing_read()
+        m8.timing(False)
+        pk8, src8 = load_peaks()
+        pk8 = dict(pk8)
+        pk8["bf16_tflops"] = 2.0 * float(pk8.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+        w8 = dict(kernel_work(cfg, B, T))
+        M_ = B * T
+        # per quantisation launch (amax or codes): the mean tensor read, plus the 1-byte codes on half
+        # the launches: (the normed stream fp32 twice, y and h bf16) / 4 layer inputs
+        C_, HD_, F_ = cfg.n_embd, cfg.n_head * cfg.head_dim, cfg.mlp_hidden
+        w8["fp8_quantize"] = ("hbm", M_ * (2 * C_ * 4 + HD_ * 2 + F_ * 2) / 4.0 + M_ * (2 * C_ + HD_ + F_) / 8.0)
+        k8, _, _ = roofline({k: v for k, v in t8.items() if k in w8}, w8, pk8, src8)
+        fp8_path = {"metric": "forward tokens/s, e4m3 linear layers", "value": job_rate(world, B * T, ms8),
+                    "unit": UNIT, "ms_per_step": ms8, "steps": n8, "gpu_launches_per_step": m8.launch_count(),
+                    "tflops_model": model_flops(cfg, B, T) / (ms8 / 1000.0) / 1e12,
+                    "peak_e4m3_tflops": pk8["bf16_tflops"], "kernels": k8,
+                    "note": "nc_forward with fp8: q, k, v, output projection, MLP and lm_head on e4m3 copies "
+                            "(weights quantised at model creation, each layer input per call over the whole "
+                            "batch), fp32 accumulation; attention, norms and gates in bf16/fp32"}
+        del m8, z8
+        torch.cuda.empty_cache()
+
     ms_max = max_over_ranks(ms, world, dev)
     ms_step = ms_max / args.steps
     value = job_rate(world, B * T * args.steps, ms_max)
@@ -556,6 +605,7 @@ def run_ours(args, rank, world, local_rank):
         "decode_path": decode_path,
         "grad_tail": grad_tail,
         "logits_bf16": logits_bf16,
+        "fp8_path": fp8_path,
     }
     if workloads:
         line["workloads"] = workloads
@@ -648,6 +698,14 @@ def run_single_kernel(args):
         dxl, w, h = rnd((M, C)), rnd((C, F), 0.02), rnd((M, F)).abs()
         ssp = torch.rand((M, C // 128), generator=g, device=dev) * 100
         fn = lambda: ops.mlp_hidden_grad(dxl, w, h, ssp=ssp)
+    elif k == "fc_fp8":   # the MLP up projection on e4m3 copies (squared ReLU epilogue)
+        a8 = rnd((M, C), 30.0, torch.float32).to(torch.float8_e4m3fn)
+        w8 = rnd((F, C), 30.0, torch.float32).to(torch.float8_e4m3fn)
+        sa, sw = torch.full((1,), 1e-3, device=dev), torch.full((1,), 1e-3, device=dev)
+        fn = lambda: ops.gemm_fp8(a8, w8, sa, sw, epi="relu2_bf16")
+    elif k == "fp8_quantize":   # the MLP hidden layer's tensorwise quantisation (amax, then codes)
+        h = rnd((M, F)).abs()
+        fn = lambda: ops.fp8_quantize(h)
     elif k == "rms_backward":
         G, x = rnd((M, C), 1.0, torch.float32), rnd((M, C), 1.0, torch.float32)
         ssp = torch.rand((M, C // 128), generator=g, device=dev) * 100
@@ -704,6 +762,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-loss-path", action="store_true", help="skip timing the fused cross-entropy path")
     ap.add_argument("--no-grad-tail", action="store_true", help="skip timing the tail backward")
+    ap.add_argument("--no-fp8", action="store_true", help="skip timing the e4m3 forward")
     ap.add_argument("--no-decode-path", action="store_true", help="skip timing the KV-cache decode step")
     ap.add_argument("--no-bf16-logits", action="store_true", help="skip timing the forward with bf16 logits")
     ap.add_argument("--e2e-steps", type=int, default=5)
@@ -718,7 +777,8 @@ def main():
                     help="positions of batch row 0 the oracle runs for each extra workload's CPU baseline")
     ap.add_argument("--only-kernel", default=None,
                     help="launch one kernel class (qkv, attention, oproj, fc, proj, lmhead, lmhead_ce, embed, decode, "
-                         "ce_grad, lmhead_dgrad, lmhead_wgrad, mlp_wgrad, mlp_hidden_grad, rms_backward) "
+                         "ce_grad, lmhead_dgrad, lmhead_wgrad, mlp_wgrad, mlp_hidden_grad, rms_backward, fc_fp8, "
+                         "fp8_quantize) "
                          "at the workload's shapes, for profiler captures")
     ap.add_argument("--launches", type=int, default=3)
     ap.add_argument("--window", type=int, default=None)

@@ -669,7 +669,7 @@ __device__ __forceinline__ void epi_vgate(uint32_t taddr, uint32_t tempty, int l
   sl.store(&om.o2, vhead * D + c0, m0w, lane);
 }
 
-template <int KIND, int D>
+template <int KIND, int D, bool F8>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmBv, const __grid_constant__ OutMaps om, int M, int N, int K,
@@ -688,7 +688,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int pair = static_cast<int>(blockIdx.x) >> 1, npairs = static_cast<int>(gridDim.x) >> 1;
   const int num_m = (M + PAIR_M - 1) / PAIR_M, num_n = num_col_tiles(KIND, N, ep.H, ep.Hkv, ep.D, ep.vgate);
   // a stage holds 128 bytes of K per row: 64 bf16 or 128 e4m3 elements; a ragged last k-block is zero-filled
-  const int kstep = ep.fp8 ? 2 * BK : BK;
+  constexpr int kstep = F8 ? 2 * BK : BK;   // F8: e4m3 operands (the bf16 instantiations are unchanged)
   const int kblocks = (K + kstep - 1) / kstep;
   // split over K (EPI_F32): tile = s * out_tiles + output tile, k-blocks [s * kps, (s + 1) * kps)
   const int out_tiles = num_m * num_n, ksplit = ep.ksplit > 1 ? ep.ksplit : 1;
@@ -787,8 +787,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         tile_coords(tile % out_tiles, num_m, num_n, grp, mb, nb);
         const int kb0 = (tile / out_tiles) * kps, kb1 = min(kblocks, kb0 + kps);
         const int width = col_tile<KIND>(nb, N, ep).width;
-        const uint32_t idesc = ep.fp8 ? idesc_e4m3_f32(PAIR_M, width)
-                                      : idesc_bf16_f32(PAIR_M, width) | (a_mn ? 1u << 15 : 0u) | (b_mn ? 1u << 16 : 0u);
+        const uint32_t idesc = F8 ? idesc_e4m3_f32(PAIR_M, width)
+                                  : idesc_bf16_f32(PAIR_M, width) | (a_mn ? 1u << 15 : 0u) | (b_mn ? 1u << 16 : 0u);
         const uint32_t a = tc & 1, aph = (tc >> 1) & 1;
         if (!mbar_wait_cluster(smem_u32(&ctl->tempty[a]), aph ^ 1, abort, status, wlim)) break;
         tc_fence_after();
@@ -807,7 +807,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                                      : sdesc_kmajor_sw128(sA + s * A_BYTES + kk * 32);
             const uint64_t bd = b_mn ? sdesc_mnmajor_sw128(sB + s * B_BYTES + kk * 16 * 128, MN_BLOCK)
                                      : sdesc_kmajor_sw128(sB + s * B_BYTES + kk * 32);
-            if (ep.fp8) umma_f8_pair(d_tmem, ad, bd, idesc, (kb != kb0 || kk != 0) ? 1u : 0u);
+            if constexpr (F8) umma_f8_pair(d_tmem, ad, bd, idesc, (kb != kb0 || kk != 0) ? 1u : 0u);
             else umma_bf16_pair(d_tmem, ad, bd, idesc, (kb != kb0 || kk != 0) ? 1u : 0u);
           }
           umma_commit_pair(smem_u32(&ctl->empty[s]), 0x3);
@@ -888,7 +888,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
-template <int KIND, int D>
+template <int KIND, int D, bool F8 = false>
 cudaError_t launch_kind(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tbv, const OutMaps& om,
                         int M, int N, int K, const GemmEpi& epi, int num_sms, cudaStream_t stream) {
   struct State {
@@ -911,12 +911,12 @@ cudaError_t launch_kind(const CUtensorMap& ta, const CUtensorMap& tb, const CUte
   cfg.numAttrs = 1;   // occupancy query without the PDL attribute
   State* st = nullptr;
   const cudaError_t init_err = per_device(states, ready, mu, [&](State& s) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<KIND, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<KIND, D, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Cfg<KIND, D>::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t q = cfg;
     q.gridDim = dim3(2 * (num_sms / 2));
-    if (cudaOccupancyMaxActiveClusters(&s.max_pairs, gemm_tc_kernel<KIND, D>, &q) != cudaSuccess || s.max_pairs < 1) {
+    if (cudaOccupancyMaxActiveClusters(&s.max_pairs, gemm_tc_kernel<KIND, D, F8>, &q) != cudaSuccess || s.max_pairs < 1) {
       cudaGetLastError();
       s.max_pairs = num_sms / 2;
     }
@@ -933,7 +933,7 @@ cudaError_t launch_kind(const CUtensorMap& ta, const CUtensorMap& tb, const CUte
   // groups of 8 row blocks, whose B tiles are re-read 8 times as often).
   const int grp = M >= N ? 1 : num_m;
   cfg.numAttrs = 2;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<KIND, D>, ta, tb, tbv, om, M, N, K, grp, epi);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<KIND, D, F8>, ta, tb, tbv, om, M, N, K, grp, epi);
   if (e != cudaSuccess) cudaGetLastError();   // a failed launch must not resurface in a later call
   return e;
 }
@@ -1075,21 +1075,25 @@ cudaError_t launch_gemm(const bf16* A, const bf16* B, int M, int N, int K, const
   }
   if (!ok) return cudaErrorInvalidValue;
   switch (epi.kind) {
-    case EPI_BF16: return launch_kind<EPI_BF16, 0>(ta, tb, tbv, om, M, N, K, epi, num_sms, stream);
-    case EPI_RELU2_BF16: return launch_kind<EPI_RELU2_BF16, 0>(ta, tb, tbv, om, M, N, K, epi, num_sms, stream);
-    case EPI_SOFTCAP_F32: return launch_kind<EPI_SOFTCAP_F32, 0>(ta, tb, tbv, om, M, N, K, epi, num_sms, stream);
-    case EPI_SOFTCAP_BF16: return launch_kind<EPI_SOFTCAP_BF16, 0>(ta, tb, tbv, om, M, N, K, epi, num_sms, stream);
-    case EPI_CE: return launch_kind<EPI_CE, 0>(ta, tb, tbv, om, M, N, K, epi, num_sms, stream);
+#define NC_KIND(K_, D_)                                                                      \
+  (f8 ? launch_kind<K_, D_, true>(ta, tb, tbv, om, M, N, K, epi, num_sms, stream)            \
+      : launch_kind<K_, D_, false>(ta, tb, tbv, om, M, N, K, epi, num_sms, stream))
+    case EPI_BF16: return NC_KIND(EPI_BF16, 0);
+    case EPI_RELU2_BF16: return NC_KIND(EPI_RELU2_BF16, 0);
+    case EPI_SOFTCAP_F32: return NC_KIND(EPI_SOFTCAP_F32, 0);
+    case EPI_SOFTCAP_BF16: return NC_KIND(EPI_SOFTCAP_BF16, 0);
+    case EPI_CE: return NC_KIND(EPI_CE, 0);
     case EPI_F32: {
-      const cudaError_t e = launch_kind<EPI_F32, 0>(ta, tb, tbv, om, M, N, K, epi, num_sms, stream);
+      const cudaError_t e = NC_KIND(EPI_F32, 0);
       if (e != cudaSuccess || epi.ksplit < 2) return e;
       return launch_splitk_reduce(epi, M, N, stream);
     }
     case EPI_CE_GRAD: return launch_kind<EPI_CE_GRAD, 0>(ta, tb, tbv, om, M, N, K, epi, num_sms, stream);
     case EPI_DRELU2: return launch_kind<EPI_DRELU2, 0>(ta, tb, tbv, om, M, N, K, epi, num_sms, stream);
     case EPI_QKV:
-      if (epi.D == 128) return launch_kind<EPI_QKV, 128>(ta, tb, tbv, om, M, N, K, epi, num_sms, stream);
-      return launch_kind<EPI_QKV, 64>(ta, tb, tbv, om, M, N, K, epi, num_sms, stream);
+      if (epi.D == 128) return NC_KIND(EPI_QKV, 128);
+      return NC_KIND(EPI_QKV, 64);
+#undef NC_KIND
     default: return cudaErrorInvalidValue;
   }
 }

@@ -128,6 +128,7 @@ __device__ __forceinline__ float lane_reduce16(const float (&v)[16], int lane) {
   return w + __shfl_xor_sync(0xffffffffu, w, 1);
 }
 
+template <bool F8>   // F8: e4m3 operands (the bf16 instantiation is unchanged)
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_resid_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ ResidMaps rm, int M, int N, int K, int NT, int reverse,
@@ -147,7 +148,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int nsteps = half / CH;                       // epilogue slots per tile and warpgroup (even)
   const int num_n = (N + PAIR_N - 1) / PAIR_N, num_t = (M + NT - 1) / NT;
   // a stage holds 128 bytes of K per row: 64 bf16 or 128 e4m3 elements
-  const int kstep = ep.fp8 ? 2 * BK : BK;
+  constexpr int kstep = F8 ? 2 * BK : BK;
   const int num_tiles = num_n * num_t, kblocks = K / kstep;
   const bool has_y = ep.Y != nullptr;
   int* status = ep.status;
@@ -219,7 +220,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           mbar_wait_cluster(smem_u32(&ctl->full[j % STAGES]), (j / STAGES) & 1, nullptr, status);
       }
     } else if (warp == 1 && lane == 0 && rank == 0) {
-      const uint32_t idesc = ep.fp8 ? idesc_e4m3_f32(2 * BM, NT) : idesc_bf16_f32(2 * BM, NT);
+      const uint32_t idesc = F8 ? idesc_e4m3_f32(2 * BM, NT) : idesc_bf16_f32(2 * BM, NT);
       uint32_t it = 0, tc = 0;
       bool ok = true;
       for (int tile = pair; tile < num_tiles && ok; tile += npairs, ++tc) {
@@ -238,7 +239,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           for (int kk = 0; kk < BK / 16; ++kk) {
             const uint64_t wd = sdesc_kmajor_sw128(sW + s * W_BYTES + kk * 32);
             const uint64_t ad = sdesc_kmajor_sw128(sA + s * A_SLOT + kk * 32);
-            if (ep.fp8) umma_f8_pair(d_tmem, wd, ad, idesc, (kb | kk) != 0 ? 1u : 0u);
+            if constexpr (F8) umma_f8_pair(d_tmem, wd, ad, idesc, (kb | kk) != 0 ? 1u : 0u);
             else umma_bf16_pair(d_tmem, wd, ad, idesc, (kb | kk) != 0 ? 1u : 0u);
           }
           umma_commit_pair(smem_u32(&ctl->empty[s]), 0x3);
@@ -296,7 +297,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const float ea = ep.a, eb = ep.b;
     // 8-bit operands: the accumulator times the input's and the weight's 1 / scale (exactly xv + acc
     // for bf16, where dq = 1)
-    const float dq = ep.fp8 ? __ldg(ep.fp8_sa) * __ldg(ep.fp8_sw) : 1.f;
+    const float dq = F8 ? __ldg(ep.fp8_sa) * __ldg(ep.fp8_sw) : 1.f;
     const bool has_xm = ep.xm_out != nullptr, has_x = ep.x_out != nullptr;
     uint8_t* ring = smem + OFF_RING + wg * RING * SLOT;
     uint32_t k = 0;    // steps handled (ring position)
@@ -460,11 +461,14 @@ cudaError_t launch_gemm_resid(const bf16* A, const bf16* W, int M, int N, int K,
   cfg.numAttrs = 1;   // occupancy query without the PDL attribute
   State* st = nullptr;
   const cudaError_t init_err = per_device(states, ready, mu, [&](State& s) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_resid_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    cudaError_t e = cudaFuncSetAttribute(gemm_resid_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         SMEM_BYTES);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(gemm_resid_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t q = cfg;
     q.gridDim = dim3(2 * (num_sms / 2));
-    if (cudaOccupancyMaxActiveClusters(&s.max_pairs, gemm_resid_kernel, &q) != cudaSuccess || s.max_pairs < 1) {
+    if (cudaOccupancyMaxActiveClusters(&s.max_pairs, gemm_resid_kernel<false>, &q) != cudaSuccess || s.max_pairs < 1) {
       cudaGetLastError();
       s.max_pairs = num_sms / 2;
     }
@@ -498,7 +502,8 @@ cudaError_t launch_gemm_resid(const bf16* A, const bf16* W, int M, int N, int K,
   // The MLP down projection reads h, which the up projection has just written in ascending token
   // order: walking its tiles from the last one starts on the rows most likely still in L2.
   const int reverse = K > 1024 ? 1 : 0;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_resid_kernel, tw, ta, rm, M, N, K, NT, reverse, ep);
+  const cudaError_t e = ep.fp8 ? cudaLaunchKernelEx(&cfg, gemm_resid_kernel<true>, tw, ta, rm, M, N, K, NT, reverse, ep)
+                              : cudaLaunchKernelEx(&cfg, gemm_resid_kernel<false>, tw, ta, rm, M, N, K, NT, reverse, ep);
   if (e != cudaSuccess) cudaGetLastError();
   return e;
 }
