@@ -233,7 +233,7 @@ cudaError_t launch_ce_finalize(const float* part, const float* zt, const int32_t
 // fp8_amax writes per-block maxima to partial[FP8_AMAX_BLOCKS]; fp8_quantize reduces them in every
 // block, writes q [M, ld_dst] and inv_scale[0] = 1 / s.  Rows of src are `ld` elements apart; dst
 // row r goes to r + (r / group) * gap (group = 0: no remap), for the packed q|k|v weight's v heads.
-constexpr int FP8_AMAX_BLOCKS = 296;
+constexpr int FP8_AMAX_BLOCKS = 592;
 cudaError_t launch_fp8_amax(const void* src, int src_f32, int M, int C, int ld, const float* ssp, float eps,
                             float* partial, cudaStream_t stream);
 cudaError_t launch_fp8_quantize(const void* src, int src_f32, int M, int C, int ld, const float* ssp, float eps,

@@ -11,10 +11,16 @@
 //                 scale when the input is a normed residual stream) -> partial[FP8_AMAX_BLOCKS]
 //   fp8_quantize  every block first reduces the partial maxima (the same fixed order in every
 //                 block), then one warp per row converts 8 elements per lane-step to e4m3.  The
-//                 scaled value is (v * 448) / amax with a correctly rounded division, not
-//                 v * (448 / amax): for bf16 v the product is exact, so a value that the exact
-//                 scaling puts on a rounding tie of the e4m3 grid (frequent: bf16 values have few
-//                 significant bits) stays exactly on it and rounds to even, as in exact arithmetic.
+//                 scaled value is (v * 448) / amax, not v * (448 / amax): for bf16 v the product
+//                 is exact, so a value that the exact scaling puts on a rounding tie of the e4m3
+//                 grid (frequent: bf16 values have few significant bits) stays exactly on it and
+//                 rounds to even, as in exact arithmetic.  The quotient takes one reciprocal per
+//                 thread and a residual correction per element (q0 = p r, e = p - q0 a exactly by
+//                 fma, q = q0 + e r), which returns the exact quotient whenever it is representable
+//                 (every rounding tie is) and the correctly rounded one otherwise but for rare
+//                 boundary cases; no per-element division.
+// Both kernels keep four 16- or 32-byte loads per lane in flight (a row's chunks are loaded before
+// they are reduced or converted).
 // No atomics: the scale and the codes are the same on every run.
 #include "internal.h"
 #include "ptx.cuh"
@@ -59,6 +65,8 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
+constexpr int UNR = 4;   // chunks of 8 elements per lane loaded before use
+
 __global__ void __launch_bounds__(QT) fp8_amax_kernel(const void* __restrict__ src, int f32, int M, int C, int ld,
                                                       const float* __restrict__ ssp, float eps,
                                                       float* __restrict__ partial) {
@@ -71,11 +79,19 @@ __global__ void __launch_bounds__(QT) fp8_amax_kernel(const void* __restrict__ s
   for (int row = blockIdx.x * (QT / 32) + warp; row < M; row += nw) {
     const float rs = row_scale(ssp, row, C, eps, lane);
     float m = 0.f;
-    for (int c = lane * 8; c < C; c += 256) {
-      float v[8];
-      load8(src, f32, static_cast<size_t>(row) * ld + c, v);
+    for (int c0 = lane * 8; c0 < C; c0 += 256 * UNR) {
+      float v[UNR][8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(v[j]));
+      for (int u = 0; u < UNR; ++u) {
+        if (c0 + u * 256 < C) load8(src, f32, static_cast<size_t>(row) * ld + c0 + u * 256, v[u]);
+        else
+#pragma unroll
+          for (int j = 0; j < 8; ++j) v[u][j] = 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < UNR; ++u)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(v[u][j]));
     }
     mx = fmaxf(mx, m * rs);
   }
@@ -108,24 +124,38 @@ __global__ void __launch_bounds__(QT) fp8_quantize_kernel(const void* __restrict
   for (int w = 0; w < QT / 32; ++w) amax = fmaxf(amax, sh[w]);
   const bool scaled = amax > 0.f;   // an all-zero tensor keeps scale 1
   if (blockIdx.x == 0 && threadIdx.x == 0) *inv_scale = scaled ? amax / 448.0f : 1.0f;
+  const float den = scaled ? amax : 1.0f;
+  const float rden = 1.0f / den;   // one reciprocal per thread
   const int nw = gridDim.x * (QT / 32);
   for (int row = blockIdx.x * (QT / 32) + warp; row < M; row += nw) {
     const float k = row_scale(ssp, row, C, eps, lane) * (scaled ? 448.0f : 1.0f);
-    const float den = scaled ? amax : 1.0f;
     const int drow = group > 0 ? row + (row / group) * gap : row;
-    for (int c = lane * 8; c < C; c += 256) {
-      float v[8];
-      load8(src, f32, static_cast<size_t>(row) * ld + c, v);
-      uint32_t w[2];
+    for (int c0 = lane * 8; c0 < C; c0 += 256 * UNR) {
+      float v[UNR][8];
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const float2 p0 = make_float2(__fdiv_rn(v[4 * h] * k, den), __fdiv_rn(v[4 * h + 1] * k, den));
-        const float2 p1 = make_float2(__fdiv_rn(v[4 * h + 2] * k, den), __fdiv_rn(v[4 * h + 3] * k, den));
-        const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(p0, __NV_SATFINITE, __NV_E4M3);
-        const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(p1, __NV_SATFINITE, __NV_E4M3);
-        w[h] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+      for (int u = 0; u < UNR; ++u)
+        if (c0 + u * 256 < C) load8(src, f32, static_cast<size_t>(row) * ld + c0 + u * 256, v[u]);
+#pragma unroll
+      for (int u = 0; u < UNR; ++u) {
+        if (c0 + u * 256 >= C) break;
+        float p[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {   // (v k) / den: q0 = p r, exact residual, one correction
+          const float n = v[u][j] * k;
+          const float q0 = n * rden;
+          p[j] = fmaf(fmaf(-q0, den, n), rden, q0);
+        }
+        uint32_t w[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const __nv_fp8x2_storage_t lo =
+              __nv_cvt_float2_to_fp8x2(make_float2(p[4 * h], p[4 * h + 1]), __NV_SATFINITE, __NV_E4M3);
+          const __nv_fp8x2_storage_t hi =
+              __nv_cvt_float2_to_fp8x2(make_float2(p[4 * h + 2], p[4 * h + 3]), __NV_SATFINITE, __NV_E4M3);
+          w[h] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+        }
+        *reinterpret_cast<uint2*>(dst + static_cast<size_t>(drow) * ld_dst + c0 + u * 256) = make_uint2(w[0], w[1]);
       }
-      *reinterpret_cast<uint2*>(dst + static_cast<size_t>(drow) * ld_dst + c) = make_uint2(w[0], w[1]);
     }
   }
 }
