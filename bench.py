@@ -329,6 +329,37 @@ def run_ours(args, rank, world, local_rank):
     model.timing(False)
     ktimes = model.timing_read()
 
+    # The same forward captured once in a CUDA graph and replayed (reported beside the eager value,
+    # which is the call a user makes; the difference is the host's launch work)
+    fwd_graph = None
+    try:
+        gf = torch.cuda.CUDAGraph()
+        gfs = torch.cuda.Stream()
+        gfs.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(gfs):
+            with torch.cuda.graph(gf, stream=gfs):
+                model.forward(tok, out=logits)
+        torch.cuda.current_stream().wait_stream(gfs)
+        for _ in range(3):
+            gf.replay()
+        n_g = max(1, min(args.steps, 50))
+        barrier()
+        torch.cuda.synchronize()
+        g0 = torch.cuda.Event(enable_timing=True)
+        g1 = torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
+        for _ in range(n_g):
+            gf.replay()
+        g1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        g_ms = max_over_ranks(g0.elapsed_time(g1), world, dev) / n_g
+        fwd_graph = {"value": job_rate(world, B * T, g_ms), "unit": UNIT, "ms_per_step": g_ms, "steps": n_g,
+                     "note": "nc_forward captured once in a CUDA graph and replayed"}
+        del gf
+    except RuntimeError as exc:   # a capture the runtime refuses leaves the eager numbers standing
+        fwd_graph = {"unavailable": str(exc).splitlines()[0][:200]}
+
     # The loss path (nc_forward_loss: the lm_head fused with the soft-cap and the next-token
     # cross-entropy, no logits written), timed the same way on the same batch; targets are the
     # next tokens, the last position of each row ignored.
@@ -429,9 +460,34 @@ def run_ours(args, rank, world, local_rank):
         if model.status() != 0:
             raise RuntimeError("device status set on the decode path")
         dec_ms = max_over_ranks(e4.elapsed_time(e5), world, dev) / n_dec
+        # the same step captured once in a CUDA graph and replayed (no per-launch host work)
+        gph = torch.cuda.CUDAGraph()
+        gs = torch.cuda.Stream()
+        gs.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(gs):
+            with torch.cuda.graph(gph, stream=gs):
+                model.decode_step(prev, cur, T0, cache, T, out=lg)
+        torch.cuda.current_stream().wait_stream(gs)
+        for _ in range(3):
+            gph.replay()
+        barrier()
+        torch.cuda.synchronize()
+        e4.record(stream)
+        for _ in range(n_dec):
+            gph.replay()
+        e5.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        if model.status() != 0:
+            raise RuntimeError("device status set on the decode path (graph)")
+        dec_graph_ms = max_over_ranks(e4.elapsed_time(e5), world, dev) / n_dec
+        del gph
         decode_path = {"metric": "decode tokens/s (one new token per batch row)", "value": job_rate(world, B, dec_ms),
                        "unit": UNIT, "ms_per_step": dec_ms, "steps": n_dec, "batch": B, "context": T,
                        "gpu_launches_per_step": model.launch_count(kv=True),
+                       "graph": {"value": job_rate(world, B, dec_graph_ms), "unit": UNIT,
+                                 "ms_per_step": dec_graph_ms,
+                                 "note": "the same nc_decode_step captured once in a CUDA graph and replayed"},
                        "note": "nc_decode_step at position T-1 after nc_prefill of T-1 tokens, repeated at that "
                                "position; the GEMMs run at M = 2B rows (row pairs), so this is launch- and "
                                "weight-read-bound, not tuned"}
@@ -602,6 +658,7 @@ def run_ours(args, rank, world, local_rank):
         "clocks": clk,
         "e2e": e2e,
         "loss_path": loss_path,
+        "graph": fwd_graph,
         "decode_path": decode_path,
         "grad_tail": grad_tail,
         "logits_bf16": logits_bf16,

@@ -78,3 +78,35 @@ def test_decode_argument_errors():
     assert lib.nc_decode_step(*args(5, cache.numel(), 65)) == 2          # T_max > seq_len_ctx
     assert lib.nc_decode_step(*args(5, cache.numel() - 1, 32)) == 3      # cache too small
     assert m.launch_count(kv=True) == 2 + 7 * cfg.n_layer
+
+
+def test_decode_step_replays_from_a_cuda_graph():
+    """After a first call on the device (per-device kernel set-up), a decode step makes no host
+    synchronisation or allocation, so a caller can capture it in a CUDA graph: replays give the
+    eager step's logits bit for bit (the cache append at the position rewrites the same rows)."""
+    wl = get_workload("tiny_all")
+    cfg = replace(wl.model, n_layer=3, window_left=(16, 16, -1), has_ve=(1, 0, 1), seq_len_ctx=64)
+    wts = make_weights(cfg, init="dense")
+    tok = torch.randint(0, cfg.vocab_size, (2, 64), generator=torch.Generator().manual_seed(22), dtype=torch.int32)
+    m = binding().Model(cfg, to_device(wts))
+    T0, p = 40, 40
+    cache = m.kv_cache(2, 64)
+    m.prefill(tok[:, :T0].contiguous().to(DEV), cache, 64)
+    prev, cur = tok[:, p - 1].contiguous().to(DEV), tok[:, p].contiguous().to(DEV)
+    out = torch.empty((2, cfg.vocab_size), dtype=torch.float32, device=DEV)
+    m.decode_step(prev, cur, p, cache, 64, out=out)
+    eager = out.clone()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            m.decode_step(prev, cur, p, cache, 64, out=out)
+    torch.cuda.current_stream().wait_stream(s)
+    for _ in range(3):
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, eager)
+    assert m.status() == 0
