@@ -9,10 +9,12 @@
 //
 //   kv_append      copies keys and values of new positions into their slots (16 B per thread).
 //   decode_attn    one query position per batch row, split over the keys: one CTA per (row, head,
-//                  128 visible keys), 4 warps of 8 key slots (4 lanes per key, each a quarter of
-//                  the head dimension), online softmax in base 2 per slot, slots combined through
-//                  shared memory; a second kernel combines the splits in a fixed order.  fp32
-//                  throughout; GQA reads kv head h / (H/Hkv).
+//                  64 visible keys), 4 warps of 8 key slots (4 lanes per key, each a quarter of
+//                  the head dimension), online softmax in base 2 per slot (hardware exp2), slots
+//                  combined through shared memory; a second kernel combines the splits in a fixed
+//                  order.  A key's value row is loaded with its key row (not after its score) and
+//                  two keys per slot are in flight, so the loads' latencies overlap.  fp32
+//                  arithmetic; GQA reads kv head h / (H/Hkv).
 #include "decode.h"
 #include "ptx.cuh"
 
@@ -24,7 +26,7 @@ namespace {
 
 constexpr int APPEND_THREADS = 256;
 constexpr int DA_WARPS = 4;
-constexpr int DA_KPS = 128;   // keys per split (4 steps of 32 keys for a CTA)
+constexpr int DA_KPS = 64;    // keys per split (2 steps of 32 keys for a CTA)
 
 __global__ void __launch_bounds__(APPEND_THREADS)
     kv_append_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v, int B, int Tsrc, int t_first,
@@ -87,15 +89,23 @@ __global__ void __launch_bounds__(32 * DA_WARPS)
 #pragma unroll
   for (int e = 0; e < EL; ++e) o[e] = 0.f;
   const size_t rowbase = static_cast<size_t>(b) * cap * kvcols + g * D + quarter * EL;
+#pragma unroll 2
   for (int jb = j0 + warp * 8; jb < j1; jb += SLOTS) {   // uniform across the warp
     const int j = jb + kk;
     const bool valid = j < j1;
     const size_t off = rowbase + static_cast<size_t>((valid ? j : jb) % cap) * kvcols;
     const uint4* kp = reinterpret_cast<const uint4*>(kc + off);
+    const uint4* vp = reinterpret_cast<const uint4*>(vc + off);
+    uint4 kw[EL / 8], vw[EL / 8];   // the key's and the value's rows, loaded together
+#pragma unroll
+    for (int u = 0; u < EL / 8; ++u) {
+      kw[u] = __ldg(kp + u);
+      vw[u] = __ldg(vp + u);
+    }
     float sc = 0.f;
 #pragma unroll
     for (int u = 0; u < EL / 8; ++u) {
-      const uint4 w = __ldg(kp + u);
+      const uint4 w = kw[u];
       const __nv_bfloat162* w2 = reinterpret_cast<const __nv_bfloat162*>(&w);
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
@@ -108,13 +118,12 @@ __global__ void __launch_bounds__(32 * DA_WARPS)
     sc += __shfl_xor_sync(0xffffffffu, sc, 2);   // the key's full score, in base-2 units
     if (valid) {
       const float mn = fmaxf(m, sc);
-      const float corr = exp2f(m - mn);   // 0 on the slot's first key (m = -inf, sc finite)
-      const float p = exp2f(sc - mn);
+      const float corr = ex2_approx(m - mn);   // 0 on the slot's first key (m = -inf, sc finite)
+      const float p = ex2_approx(sc - mn);
       l = fmaf(l, corr, p);
-      const uint4* vp = reinterpret_cast<const uint4*>(vc + off);
 #pragma unroll
       for (int u = 0; u < EL / 8; ++u) {
-        const uint4 w = __ldg(vp + u);
+        const uint4 w = vw[u];
         const __nv_bfloat162* w2 = reinterpret_cast<const __nv_bfloat162*>(&w);
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
