@@ -482,9 +482,17 @@ def run_ours(args, rank, world, local_rank):
             raise RuntimeError("device status set on the decode path (graph)")
         dec_graph_ms = max_over_ranks(e4.elapsed_time(e5), world, dev) / n_dec
         del gph
+        model.timing(True)   # per-kernel-class times of the step (events around every launch)
+        for _ in range(10):
+            model.decode_step(prev, cur, T0, cache, T, out=lg)
+        torch.cuda.synchronize()
+        dk = model.timing_read()
+        model.timing(False)
+        dec_kernels = {k: {"launches_per_step": n // 10, "us_per_step": 1000.0 * ms / 10} for k, (ms, n) in dk.items() if n}
         decode_path = {"metric": "decode tokens/s (one new token per batch row)", "value": job_rate(world, B, dec_ms),
                        "unit": UNIT, "ms_per_step": dec_ms, "steps": n_dec, "batch": B, "context": T,
                        "gpu_launches_per_step": model.launch_count(kv=True),
+                       "kernels": dec_kernels,
                        "graph": {"value": job_rate(world, B, dec_graph_ms), "unit": UNIT,
                                  "ms_per_step": dec_graph_ms,
                                  "note": "the same nc_decode_step captured once in a CUDA graph and replayed"},

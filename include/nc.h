@@ -264,7 +264,9 @@ NC_API nc_status nc_forward_loss_grad_tail(nc_model *m, const int32_t *tokens, c
  * sequence (up to rounding: the decode attention keeps p in fp32 where the batched one rounds
  * it to bf16).  workspace: >= nc_workspace_bytes_decode(B), 256-byte aligned.
  * Both are asynchronous on `stream`; errors as nc_forward.  nc_kv_launch_count gives the kernels a
- * decode step launches (2 + 7 * n_layer; a prefill launches 2 + 6 * n_layer). */
+ * decode step launches (2 + 7 * n_layer; a prefill launches 2 + 6 * n_layer).  After a first call on
+ * the device (per-device kernel set-up), nc_forward and nc_decode_step make no host synchronisation
+ * or allocation, so a caller can capture them in a CUDA graph. */
 NC_API nc_status nc_kv_cache_bytes(const nc_model *m, int B, int T_max, size_t *bytes);
 NC_API nc_status nc_prefill(nc_model *m, const int32_t *tokens, int B, int T, void *kv_cache, size_t cache_bytes,
                             int T_max, void *logits, void *workspace, size_t ws_bytes, void *stream);

@@ -110,3 +110,20 @@ def test_decode_step_replays_from_a_cuda_graph():
         torch.cuda.synchronize()
         assert torch.equal(out, eager)
     assert m.status() == 0
+
+
+def test_decode_twelve_rows():
+    """B = 12 (24 rows per step, a window that wraps on the first layer): the steps equal the
+    forward's rows and the oracle's."""
+    wl = get_workload("tiny_all")
+    cfg = replace(wl.model, n_layer=2, window_left=(8, -1), has_ve=(0, 1), seq_len_ctx=64)
+    wts = make_weights(cfg, init="dense")
+    tok = torch.randint(0, cfg.vocab_size, (12, 40), generator=torch.Generator().manual_seed(23), dtype=torch.int32)
+    m = binding().Model(cfg, to_device(wts))
+    T0 = 30
+    pos = list(range(T0, 40))
+    _, dec = _decode_run(m, tok, T0, 64, pos)
+    ref = O.forward(cfg, O.OracleWeights.from_synth(cfg, wts), tok.numpy())
+    assert_parity(dec.cpu().numpy(), ref[:, T0:], "decode, 24 rows per step")
+    full = m.forward(tok.to(DEV)).cpu().numpy()
+    np.testing.assert_allclose(dec.cpu().numpy(), full[:, T0:], rtol=0, atol=2e-2)
