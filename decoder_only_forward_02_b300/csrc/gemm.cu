@@ -25,7 +25,8 @@
 //                owns one output row (TMEM lane).  A warp reads its 32 rows with tcgen05.ld and
 //                applies the fused epilogue; depending on the kind it stores 32-row x 128-byte
 //                boxes with TMA from two alternating 128-byte-swizzled shared buffers, stores
-//                row-coalesced from one staging buffer, or stores nothing (cross-entropy).
+//                row-coalesced from one staging buffer, stores whole sectors straight from the
+//                registers (fp32 outputs), or stores nothing (cross-entropy).
 // The double-buffered accumulator lets the epilogue of tile i overlap the MMAs of tile i+1.
 //
 // Fused epilogues (the operations are those of "Nanochat在nanoGPT之上的新增功能", section 1
@@ -93,15 +94,19 @@ constexpr int SLAB_BYTES = 2 * SLAB_BUF; // two per epilogue warp, used alternat
 
 // Shared memory per epilogue kind.  Kinds whose epilogue stores with TMA keep two staging
 // buffers per warp (a store drains from one while the next is filled) and a 5-stage operand
-// ring; the squared-ReLU and soft-cap epilogues store row-coalesced from one buffer, and the
-// space saved deepens their ring to 6 stages (operand latency is what starves the MMA).
-// The cross-entropy epilogue stores no tile at all: no staging buffers, a 7-stage ring.
+// ring; the bf16 epilogues that store row-coalesced use one buffer, and the space saved
+// deepens their ring to 6 stages (operand latency is what starves the MMA).  The fp32 outputs
+// (stored from registers) and the cross-entropy epilogue (no tile stored) keep no staging
+// buffers and a 7-stage ring.
 template <int KIND, int D>
 struct Cfg {
-  static constexpr bool LSU_STORE = KIND == EPI_RELU2_BF16 || KIND == EPI_SOFTCAP_F32 || KIND == EPI_SOFTCAP_BF16 ||
-                                    KIND == EPI_F32 || KIND == EPI_CE_GRAD || KIND == EPI_DRELU2;
-  static constexpr int STAGES = KIND == EPI_CE ? 7 : (LSU_STORE ? 6 : 5);
-  static constexpr int SLAB_WARP = KIND == EPI_CE ? 0 : (LSU_STORE ? SLAB_BUF : SLAB_BYTES);   // staging bytes per warp
+  // fp32 outputs and the cross-entropy partials need no staging; the other kinds stored by
+  // plain instructions stage one [32 rows][128 B] buffer per warp, the TMA-stored ones two
+  static constexpr bool NO_SLAB = KIND == EPI_CE || KIND == EPI_SOFTCAP_F32 || KIND == EPI_F32;
+  static constexpr bool LSU_STORE = KIND == EPI_RELU2_BF16 || KIND == EPI_SOFTCAP_BF16 || KIND == EPI_CE_GRAD ||
+                                    KIND == EPI_DRELU2;
+  static constexpr int STAGES = NO_SLAB ? 7 : (LSU_STORE ? 6 : 5);
+  static constexpr int SLAB_WARP = NO_SLAB ? 0 : (LSU_STORE ? SLAB_BUF : SLAB_BYTES);   // staging bytes per warp
   static constexpr int OFF_SLAB = STAGES * (A_BYTES + B_BYTES);
   static constexpr int OFF_CTRL = OFF_SLAB + NUM_EPI_WARPS * SLAB_WARP;
   struct __align__(8) Ctrl {
@@ -173,11 +178,13 @@ struct OutMaps {
 };
 
 // Release an accumulator buffer to the pair's MMA thread (after this warp's last tcgen05.ld
-// of it); `bar` is the leader CTA's barrier as a shared::cluster address.
+// of it); `bar` is the leader CTA's barrier as a shared::cluster address.  The arrive is relaxed:
+// the MMA thread reads nothing this warp wrote to memory, and a release would first wait for
+// every global store the warp has issued (the lm_head's logits: 6% of its time).
 __device__ __forceinline__ void release_acc(int lane, uint32_t bar) {
   tc_fence_before();
   __syncwarp();
-  if (lane == 0) mbar_arrive_cluster(bar);
+  if (lane == 0) mbar_arrive_cluster_relaxed(bar);
 }
 
 // ---------------------------------------------------------------- tile order
@@ -443,38 +450,54 @@ __device__ __forceinline__ void epi_bf16(uint32_t taddr, uint32_t tempty, int la
 }
 
 // fp32 outputs: cap * tanh(rs * acc / cap) (logit soft-cap of the lm_head, streaming stores) or
-// rs * acc (EPI_F32: the backward's weight and input gradients).
+// rs * acc (EPI_F32: the backward's weight and input gradients).  The accumulator is read in the
+// 16x256b shape, in which four consecutive threads hold 8 consecutive columns of one row, so
+// each 8-byte store instruction writes whole 32-byte sectors (8 rows x 32 B) straight from the
+// registers: no staging through shared memory, whose bytes go to a deeper operand ring instead.
 template <bool SOFTCAP>
 __device__ __forceinline__ void epi_f32out(uint32_t taddr, uint32_t tempty, int lane, int m0w, int n0, int M,
-                                           int N, const GemmEpi& ep, Slab& sl, const EpiPre& pre, void* out) {
+                                           int N, const GemmEpi& ep, const EpiPre& pre, void* out) {
   const float cap = ep.cap;
-  const float sc = SOFTCAP ? pre.rs / cap : pre.rs;
+  const int rq = lane >> 2, cq = lane & 3;
+  // the row scales of this thread's four rows m0w + 16 h + 8 e + lane / 4 (lane l holds row m0w + l's)
+  float sc[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float r = __shfl_sync(0xffffffffu, pre.rs, (i >> 1) * 16 + (i & 1) * 8 + rq);
+    sc[i] = SOFTCAP ? r / cap : r;
+  }
+  uint8_t* const obase = static_cast<uint8_t*>(out);
+  const size_t ld_bytes = static_cast<size_t>(ep.ldo) * 4;
 #pragma unroll 1
   for (int ch = 0; ch < 4; ++ch) {
     const int c0 = n0 + ch * 32;
     if (c0 >= N) break;
-    uint32_t r[32];
-    tmem_ld32(taddr + ch * 32, r);
-    tmem_ld_wait(r);
-    uint4 o[8];
+    uint32_t r[2][16];
+    tmem_ld16x256_x4(taddr + ch * 32, r[0]);               // lanes 0..15 of the warp's quarter
+    tmem_ld16x256_x4(taddr + (16u << 16) + ch * 32, r[1]);   // lanes 16..31
+    tmem_ld_wait(r[0]);
+    tmem_ld_wait(r[1]);
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      float v[4];
+    for (int h = 0; h < 2; ++h) {
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float a = __uint_as_float(r[c * 4 + j]) * sc;
-        v[j] = SOFTCAP ? cap * tanh_approx(a) : a;
+      for (int e = 0; e < 2; ++e) {
+        const int row = m0w + h * 16 + e * 8 + rq;
+        if (row >= M) continue;
+        uint8_t* const orow = obase + static_cast<size_t>(row) * ld_bytes;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          float v0 = __uint_as_float(r[h][4 * j + 2 * e]) * sc[2 * h + e];
+          float v1 = __uint_as_float(r[h][4 * j + 2 * e + 1]) * sc[2 * h + e];
+          if (SOFTCAP) {
+            v0 = cap * tanh_approx(v0);
+            v1 = cap * tanh_approx(v1);
+          }
+          float2* dst = reinterpret_cast<float2*>(orow + static_cast<size_t>(c0 + 8 * j + 2 * cq) * 4);
+          if (SOFTCAP) __stcs(dst, make_float2(v0, v1));   // written once, never re-read
+          else *dst = make_float2(v0, v1);
+        }
       }
-      o[c] = make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]), __float_as_uint(v[3]));
     }
-    // Through the staging buffer to row-coalesced streaming stores (4 rows x 128 B per
-    // instruction): the logits are written once and never re-read, and leaving them to the
-    // load/store unit keeps the TMA unit free for the operand stream.
-    __syncwarp();
-    sl.put_row(lane, o);
-    __syncwarp();
-    lsu_store_box(sl.buf(), out, static_cast<size_t>(ep.ldo) * 4, m0w, static_cast<size_t>(c0) * 4, M, lane,
-                  SOFTCAP);
   }
   release_acc(lane, tempty);
 }
@@ -860,9 +883,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint32_t tbase = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + a * BN;
       const uint32_t taddr = tbase + group * 128;
       const uint32_t tempty = mapa_shared(smem_u32(&ctl->tempty[a]), 0);
-      if constexpr (KIND == EPI_SOFTCAP_F32) epi_f32out<true>(taddr, tempty, lane, m0w, n0, M, N, ep, sl, pre, ep.out);
+      if constexpr (KIND == EPI_SOFTCAP_F32) epi_f32out<true>(taddr, tempty, lane, m0w, n0, M, N, ep, pre, ep.out);
       else if constexpr (KIND == EPI_F32)   // a split tile writes its K range's slab
-        epi_f32out<false>(taddr, tempty, lane, m0w, n0, M, N, ep, sl, pre,
+        epi_f32out<false>(taddr, tempty, lane, m0w, n0, M, N, ep, pre,
                           ksplit > 1 ? ep.split_ws + static_cast<size_t>(tile / out_tiles) * M * ep.ldo : ep.out);
       else if constexpr (KIND == EPI_CE_GRAD) epi_bf16<BF16_CEGRAD>(taddr, tempty, lane, m0w, n0, M, N, ep, om, sl, pre);
       else if constexpr (KIND == EPI_DRELU2) epi_bf16<BF16_DRELU2>(taddr, tempty, lane, m0w, n0, M, N, ep, om, sl, pre);
@@ -1035,7 +1058,7 @@ cudaError_t launch_gemm(const bf16* A, const bf16* B, int M, int N, int K, const
     case EPI_CE:
       ok = epi.targets != nullptr && epi.ce_part != nullptr && epi.ce_zt != nullptr && epi.cap > 0.f;
       break;
-    case EPI_SOFTCAP_F32:   // written with plain coalesced stores (16-byte aligned rows)
+    case EPI_SOFTCAP_F32:   // written with plain 8-byte stores from the registers (16-byte aligned rows)
     case EPI_F32:
       ok = (reinterpret_cast<uintptr_t>(epi.out) % 16 == 0) && epi.ldo % 4 == 0 && epi.ldo >= N;
       break;

@@ -273,6 +273,19 @@ __device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32]) {
       : "memory");
 }
 
+// 16 lanes x 32 fp32 columns in the 16x256b shape (four 8-column blocks): thread t receives
+// lane base + t/4 in registers 4j, 4j+1 and lane base + 8 + t/4 in 4j+2, 4j+3, each the columns
+// 8j + 2(t%4) and 8j + 2(t%4) + 1.
+__device__ __forceinline__ void tmem_ld16x256_x4(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x4.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+
 // 32 lanes x 1 fp32 column: thread i of the warp receives lane (base + i).
 __device__ __forceinline__ void tmem_ld1(uint32_t taddr, uint32_t (&r)[1]) {
   asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r[0]) : "r"(taddr));
