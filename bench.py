@@ -497,8 +497,8 @@ def run_ours(args, rank, world, local_rank):
                                  "ms_per_step": dec_graph_ms,
                                  "note": "the same nc_decode_step captured once in a CUDA graph and replayed"},
                        "note": "nc_decode_step at position T-1 after nc_prefill of T-1 tokens, repeated at that "
-                               "position; the GEMMs run at M = 2B rows (row pairs), so this is launch- and "
-                               "weight-read-bound, not tuned"}
+                               "position; small-row weight-streaming products and a one-launch attention per "
+                               "layer, bound by the chain of dependent launches"}
         del cache
 
     # The same forward writing bf16 logits (nc_config.logits_bf16: the soft-capped values rounded to

@@ -7,14 +7,17 @@
 // window can still see: all positions on full layers, the last W+1 on a layer with window W
 // (position j lives in slot j % cap, a ring).
 //
-//   kv_append      copies keys and values of new positions into their slots (16 B per thread).
-//   decode_attn    one query position per batch row, split over the keys: one CTA per (row, head,
-//                  64 visible keys), 4 warps of 8 key slots (4 lanes per key, each a quarter of
-//                  the head dimension), online softmax in base 2 per slot (hardware exp2), slots
-//                  combined through shared memory; a second kernel combines the splits in a fixed
-//                  order.  A key's value row is loaded with its key row (not after its score) and
-//                  two keys per slot are in flight, so the loads' latencies overlap.  fp32
-//                  arithmetic; GQA reads kv head h / (H/Hkv).
+//   kv_append      copies keys and values of new positions into their slots (16 B per thread);
+//                  the prefill's append.
+//   decode_attn    a decode step's attention, one launch per layer: the q|k|v epilogue of the new
+//                  token (RoPE, QK-norm, gated value embedding) and its cache append, then one
+//                  query position per batch row split over the keys: one CTA per (row, head, 64
+//                  visible keys), 4 warps of 8 key slots (4 lanes per key, each a quarter of the
+//                  head dimension), online softmax in base 2 per slot (hardware exp2), slots
+//                  combined through shared memory; the last CTA of a (row, head) combines its
+//                  splits in a fixed order.  A key's value row is loaded with its key row (not
+//                  after its score) and two keys per slot are in flight, so the loads' latencies
+//                  overlap.  fp32 arithmetic; GQA reads kv head h / (H/Hkv).
 #include "decode.h"
 #include "ptx.cuh"
 
@@ -45,62 +48,126 @@ __global__ void __launch_bounds__(APPEND_THREADS)
   vc[dst] = v[src];
 }
 
-// Split-key decode attention, pass 1: CTA (row b, head h, split) takes the visible keys
-// [jlo + split * KPS, ...) (at most KPS); each warp scores 8 keys per step, 4 lanes per key (each
-// lane a quarter of the head dimension), with an online softmax in base 2 per key slot; the 32
-// slots of the CTA are combined through shared memory into (sum_j 2^(s_j - M) v_j, M, sum_j
-// 2^(s_j - M)) for the split, written to part[(b*H + h) * nsplit + split][0 .. D+1].
+// The decode step's attention for one (batch row b, head h, split) CTA: the split takes the visible
+// keys [jlo + split * KPS, ...) (at most KPS).
+//   Prologue, from the q|k|v products raw = rs * (x . W^T) of row b: the head's q rotated at pos
+//   and RMS-normed (threads 0 .. D/2-1, each the columns j and j + D/2), rounded to bf16 as the
+//   cache keeps k; on the split that holds position pos also the new key (rotated, normed) and
+//   value (+ gate * ve[token] on value-embedding layers) of kv head g = h / (H / Hkv), kept in
+//   shared memory for this CTA's own use; the CTA of the group's first q head writes them into
+//   the cache slot pos % cap.  No CTA reads that slot from memory in this launch.
+//   Keys: each warp scores 8 keys per step, 4 lanes per key (each lane a quarter of the head
+//   dimension), with an online softmax in base 2 per key slot (hardware exp2); a key's value row
+//   is loaded with its key row and two keys per slot are in flight.  The CTA's 32 slots are
+//   combined through shared memory into (sum_j 2^(s_j - M) v_j, M, sum_j 2^(s_j - M)), written to
+//   part[(b*H + h) * nsplit + split][0 .. D+1].
+//   The last CTA of (b, h) to finish (a counter, after a memory fence) combines the splits in
+//   split order: y = sum_s 2^(M_s - M) O_s / sum_s 2^(M_s - M) L_s, rounded to bf16.
+// fp32 arithmetic throughout.
 template <int D>
 __global__ void __launch_bounds__(32 * DA_WARPS)
-    decode_attn_split_kernel(const bf16* __restrict__ q, int Tq, int tq, int H, int Hkv, const bf16* __restrict__ kc,
-                             const bf16* __restrict__ vc, int cap, int pos, int window, float scale_log2, int nsplit,
-                             float* __restrict__ part) {
+    decode_attn_kernel(const __grid_constant__ DecodeAttn a, float scale_log2, int nsplit) {
   constexpr int EL = D / 4;        // head-dimension elements per lane
   constexpr int SLOTS = DA_WARPS * 8;
+  constexpr int HALF = D / 2;
   __shared__ float s_m[SLOTS], s_l[SLOTS];
   __shared__ float s_o[SLOTS][D];
-  griddep_wait();   // the cache append (and the q projection) have completed
+  __shared__ float s_q[D];
+  __shared__ __align__(16) bf16 s_kn[D];
+  __shared__ __align__(16) bf16 s_vn[D];
+  __shared__ float s_red[2][2];
+  __shared__ float s_mv[DA_MAX_SPLITS], s_lv[DA_MAX_SPLITS], s_f[DA_MAX_SPLITS];
+  __shared__ int s_last;
+  griddep_wait();   // the q|k|v products come from the preceding kernel
   griddep_launch();
+  const int H = a.H, Hkv = a.Hkv;
   const int bh = blockIdx.x, split = blockIdx.y;
   const int b = bh / H, h = bh % H;
   const int g = h / (H / Hkv);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int kk = lane >> 2, quarter = lane & 3;   // key slot within the warp, quarter of the head dim
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int kvcols = Hkv * D;
-  float qv[EL];
+  const int pos = a.pos;
+  const int jlo = a.window < 0 ? 0 : max(0, pos - a.window);
+  const int j0 = jlo + split * DA_KPS, j1 = min(pos + 1, j0 + DA_KPS);
+  const bool has_new = j1 == pos + 1;   // this split holds the new position
+  const size_t slot = (static_cast<size_t>(b) * a.cap + pos % a.cap) * kvcols + static_cast<size_t>(g) * D;
+  const float* r = a.raw + static_cast<size_t>(b) * a.ldraw;
   {
-    const uint4* qp = reinterpret_cast<const uint4*>(q + (static_cast<size_t>(b) * Tq + tq) * (static_cast<size_t>(H) * D) +
-                                                     h * D + quarter * EL);
-#pragma unroll
-    for (int u = 0; u < EL / 8; ++u) {
-      const uint4 w = __ldg(qp + u);
-      const __nv_bfloat162* w2 = reinterpret_cast<const __nv_bfloat162*>(&w);
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        const float2 f = __bfloat1622float2(w2[t]);
-        qv[u * 8 + 2 * t] = f.x * scale_log2;
-        qv[u * 8 + 2 * t + 1] = f.y * scale_log2;
+    // role 0: q head h; role 1 (on the new key's split): k and v of kv head g
+    const int role = tid / HALF, j = tid % HALF;
+    float c0 = 0.f, c1 = 0.f, ss = 0.f;
+    if (role == 0 || (role == 1 && has_new)) {
+      const int col = role == 0 ? h * D : (H + g) * D;
+      c0 = r[col + j];
+      c1 = r[col + j + HALF];
+      ss = c0 * c0 + c1 * c1;
+    }
+    if (role < 2) {
+      ss = warp_sum(ss);
+      if (HALF > 32) {
+        if (lane == 0) s_red[role][(tid % HALF) >> 5] = ss;
       }
     }
+    __syncthreads();
+    if (role == 0 || (role == 1 && has_new)) {
+      if (HALF > 32) ss = s_red[role][0] + s_red[role][1];
+      const float sc = rsqrtf(ss * (1.0f / D) + a.eps);
+      const float2 cs = a.rope[static_cast<size_t>(j) * a.rope_ld + pos];
+      const bf16 y1 = __float2bfloat16((c0 * cs.x + c1 * cs.y) * sc);
+      const bf16 y2 = __float2bfloat16((c1 * cs.x - c0 * cs.y) * sc);
+      if (role == 0) {
+        s_q[j] = __bfloat162float(y1) * scale_log2;
+        s_q[j + HALF] = __bfloat162float(y2) * scale_log2;
+      } else {
+        s_kn[j] = y1;
+        s_kn[j + HALF] = y2;
+        const int vcol = (H + Hkv) * D + g * (a.vgate ? D + VGATE_ROWS : D);
+        float v0 = r[vcol + j], v1 = r[vcol + j + HALF];
+        if (a.vgate) {
+          const int tok = a.tokens[b];
+          if (tok >= 0 && tok < a.V) {
+            const float gg = a.gate_scale * (1.0f / (1.0f + __expf(-r[vcol + D])));
+            const bf16* e = a.ve + static_cast<size_t>(tok) * kvcols + g * D;
+            v0 = fmaf(gg, __bfloat162float(e[j]), v0);
+            v1 = fmaf(gg, __bfloat162float(e[j + HALF]), v1);
+          }
+        }
+        s_vn[j] = __float2bfloat16(v0);
+        s_vn[j + HALF] = __float2bfloat16(v1);
+        if (h % (H / Hkv) == 0) {   // one writer per kv head: the group's first q head
+          a.kc[slot + j] = y1;
+          a.kc[slot + j + HALF] = y2;
+          a.vc[slot + j] = s_vn[j];
+          a.vc[slot + j + HALF] = s_vn[j + HALF];
+        }
+      }
+    }
+    __syncthreads();
   }
-  const int jlo = window < 0 ? 0 : max(0, pos - window);
-  const int j0 = jlo + split * DA_KPS, j1 = min(pos + 1, j0 + DA_KPS);
+  const int kk = lane >> 2, quarter = lane & 3;   // key slot within the warp, quarter of the head dim
+  float qv[EL];
+#pragma unroll
+  for (int e = 0; e < EL; ++e) qv[e] = s_q[quarter * EL + e];
   float m = -INFINITY, l = 0.f, o[EL];
 #pragma unroll
   for (int e = 0; e < EL; ++e) o[e] = 0.f;
-  const size_t rowbase = static_cast<size_t>(b) * cap * kvcols + g * D + quarter * EL;
+  const size_t rowbase = static_cast<size_t>(b) * a.cap * kvcols + g * D + quarter * EL;
+  const uint4* kn = reinterpret_cast<const uint4*>(s_kn + quarter * EL);
+  const uint4* vn = reinterpret_cast<const uint4*>(s_vn + quarter * EL);
 #pragma unroll 2
   for (int jb = j0 + warp * 8; jb < j1; jb += SLOTS) {   // uniform across the warp
     const int j = jb + kk;
     const bool valid = j < j1;
-    const size_t off = rowbase + static_cast<size_t>((valid ? j : jb) % cap) * kvcols;
-    const uint4* kp = reinterpret_cast<const uint4*>(kc + off);
-    const uint4* vp = reinterpret_cast<const uint4*>(vc + off);
+    const bool isnew = valid && j == pos;   // the new key: from shared memory
+    const bool ld = valid && !isnew;
+    const size_t off = rowbase + static_cast<size_t>(j % a.cap) * kvcols;
+    const uint4* kp = reinterpret_cast<const uint4*>(a.kc + off);
+    const uint4* vp = reinterpret_cast<const uint4*>(a.vc + off);
     uint4 kw[EL / 8], vw[EL / 8];   // the key's and the value's rows, loaded together
 #pragma unroll
     for (int u = 0; u < EL / 8; ++u) {
-      kw[u] = __ldg(kp + u);
-      vw[u] = __ldg(vp + u);
+      kw[u] = ld ? __ldg(kp + u) : (isnew ? kn[u] : make_uint4(0u, 0u, 0u, 0u));
+      vw[u] = ld ? __ldg(vp + u) : (isnew ? vn[u] : make_uint4(0u, 0u, 0u, 0u));
     }
     float sc = 0.f;
 #pragma unroll
@@ -135,26 +202,27 @@ __global__ void __launch_bounds__(32 * DA_WARPS)
       m = mn;
     }
   }
-  const int slot = warp * 8 + kk;
+  const int kslot = warp * 8 + kk;
   if (quarter == 0) {
-    s_m[slot] = m;
-    s_l[slot] = l;
+    s_m[kslot] = m;
+    s_l[kslot] = l;
   }
 #pragma unroll
-  for (int e = 0; e < EL; ++e) s_o[slot][quarter * EL + e] = o[e];
+  for (int e = 0; e < EL; ++e) s_o[kslot][quarter * EL + e] = o[e];
   __syncthreads();
-  float* dst = part + (static_cast<size_t>(bh) * nsplit + split) * (D + 2);
+  float* part = a.scratch + static_cast<size_t>(bh) * nsplit * (D + 2);
+  float* dst = part + static_cast<size_t>(split) * (D + 2);
   float M = -INFINITY;
 #pragma unroll
   for (int w = 0; w < SLOTS; ++w) M = fmaxf(M, s_m[w]);
-  for (int d = threadIdx.x; d < D; d += 32 * DA_WARPS) {
+  for (int d = tid; d < D; d += 32 * DA_WARPS) {
     float O = 0.f;
 #pragma unroll
     for (int w = 0; w < SLOTS; ++w)
       if (s_m[w] != -INFINITY) O = fmaf(s_o[w][d], exp2f(s_m[w] - M), O);
     dst[d] = O;
   }
-  if (threadIdx.x == 0) {
+  if (tid == 0) {
     float L = 0.f;
 #pragma unroll
     for (int w = 0; w < SLOTS; ++w)
@@ -162,26 +230,30 @@ __global__ void __launch_bounds__(32 * DA_WARPS)
     dst[D] = M;
     dst[D + 1] = L;
   }
-}
-
-// Pass 2: y[b, h] = sum_s 2^(M_s - M) O_s / sum_s 2^(M_s - M) L_s over the splits, in split order.
-template <int D>
-__global__ void __launch_bounds__(D)
-    decode_attn_combine_kernel(const float* __restrict__ part, int nsplit, int Tq, int tq, int H,
-                               bf16* __restrict__ y) {
-  griddep_wait();
-  griddep_launch();
-  const int bh = blockIdx.x, b = bh / H, h = bh % H, d = threadIdx.x;
-  const float* p = part + static_cast<size_t>(bh) * nsplit * (D + 2);
-  float M = -INFINITY;
-  for (int s2 = 0; s2 < nsplit; ++s2) M = fmaxf(M, p[s2 * (D + 2) + D]);
-  float L = 0.f, O = 0.f;
-  for (int s2 = 0; s2 < nsplit; ++s2) {
-    const float f = exp2f(p[s2 * (D + 2) + D] - M);
-    L = fmaf(p[s2 * (D + 2) + D + 1], f, L);
-    O = fmaf(p[s2 * (D + 2) + d], f, O);
+  // the last CTA of (b, h) combines the splits
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) s_last = atomicAdd(a.counters + bh, 1u) == static_cast<unsigned>(nsplit - 1);
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  for (int s2 = tid; s2 < nsplit; s2 += 32 * DA_WARPS) {
+    s_mv[s2] = __ldcg(part + static_cast<size_t>(s2) * (D + 2) + D);
+    s_lv[s2] = __ldcg(part + static_cast<size_t>(s2) * (D + 2) + D + 1);
   }
-  y[(static_cast<size_t>(b) * Tq + tq) * (static_cast<size_t>(H) * D) + h * D + d] = __float2bfloat16(O / L);
+  __syncthreads();
+  float Mx = -INFINITY;
+  for (int s2 = 0; s2 < nsplit; ++s2) Mx = fmaxf(Mx, s_mv[s2]);
+  for (int s2 = tid; s2 < nsplit; s2 += 32 * DA_WARPS) s_f[s2] = exp2f(s_mv[s2] - Mx);
+  __syncthreads();
+  float L = 0.f;
+  for (int s2 = 0; s2 < nsplit; ++s2) L = fmaf(s_lv[s2], s_f[s2], L);
+  for (int d = tid; d < D; d += 32 * DA_WARPS) {
+    float O = 0.f;
+#pragma unroll 8
+    for (int s2 = 0; s2 < nsplit; ++s2) O = fmaf(__ldcg(part + static_cast<size_t>(s2) * (D + 2) + d), s_f[s2], O);
+    a.y[static_cast<size_t>(b) * a.ldy + h * D + d] = __float2bfloat16(O / L);
+  }
 }
 
 template <typename K, typename... Args>
@@ -215,38 +287,31 @@ cudaError_t launch_kv_append(const bf16* k, const bf16* v, int B, int Tsrc, int 
 
 int decode_attention_splits(int T_max) { return (T_max + DA_KPS - 1) / DA_KPS; }
 
-cudaError_t launch_decode_attention(const bf16* q, int B, int Tq, int tq, int H, int Hkv, int D, const bf16* kcache,
-                                    const bf16* vcache, int cap, int pos, int window, bf16* y, float* scratch,
-                                    size_t scratch_floats, cudaStream_t stream) {
-  if (q == nullptr || kcache == nullptr || vcache == nullptr || y == nullptr || scratch == nullptr || B < 1 ||
-      Tq < 1 || tq < 0 || tq >= Tq || H < 1 || Hkv < 1 || H % Hkv != 0 || pos < 0 || cap < 1 ||
-      (window < 0 ? cap <= pos : cap <= window && cap <= pos))
+cudaError_t launch_decode_attention(const DecodeAttn& a, cudaStream_t stream) {
+  if (a.raw == nullptr || a.kc == nullptr || a.vc == nullptr || a.y == nullptr || a.scratch == nullptr ||
+      a.counters == nullptr || a.rope == nullptr || a.B < 1 || a.H < 1 || a.Hkv < 1 || a.H % a.Hkv != 0 ||
+      a.pos < 0 || a.pos >= a.rope_ld || a.cap < 1 || a.ldy < a.H * a.D ||
+      (a.window < 0 ? a.cap <= a.pos : a.cap <= a.window && a.cap <= a.pos) ||
+      (a.vgate && (a.ve == nullptr || a.tokens == nullptr)) ||
+      a.ldraw < (a.H + a.Hkv) * a.D + a.Hkv * (a.vgate ? a.D + VGATE_ROWS : a.D))
     return cudaErrorInvalidValue;
-  if (D != 64 && D != 128) return cudaErrorInvalidValue;
-  const int jlo = window < 0 ? 0 : std::max(0, pos - window);
-  const int nsplit = (pos - jlo + 1 + DA_KPS - 1) / DA_KPS;
-  if (static_cast<size_t>(B) * H * nsplit * (D + 2) > scratch_floats) return cudaErrorInvalidValue;
-  const float scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
+  if (a.D != 64 && a.D != 128) return cudaErrorInvalidValue;
+  const int jlo = a.window < 0 ? 0 : std::max(0, a.pos - a.window);
+  const int nsplit = (a.pos - jlo + 1 + DA_KPS - 1) / DA_KPS;
+  if (nsplit > DA_MAX_SPLITS || static_cast<size_t>(a.B) * a.H * nsplit * (a.D + 2) > a.scratch_floats)
+    return cudaErrorInvalidValue;
+  const float scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(a.D)));
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1] = {pdl_attribute()};
-  cfg.gridDim = dim3(B * H, nsplit);
+  cfg.gridDim = dim3(a.B * a.H, nsplit);
   cfg.blockDim = dim3(32 * DA_WARPS);
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = D == 128 ? cudaLaunchKernelEx(&cfg, decode_attn_split_kernel<128>, q, Tq, tq, H, Hkv, kcache, vcache,
-                                                cap, pos, window, scale_log2, nsplit, scratch)
-                           : cudaLaunchKernelEx(&cfg, decode_attn_split_kernel<64>, q, Tq, tq, H, Hkv, kcache, vcache,
-                                                cap, pos, window, scale_log2, nsplit, scratch);
-  if (e != cudaSuccess) {
-    cudaGetLastError();
-    return e;
-  }
-  if (D == 128)
-    return launch_pdl(decode_attn_combine_kernel<128>, B * H, 128, stream, static_cast<const float*>(scratch), nsplit,
-                      Tq, tq, H, y);
-  return launch_pdl(decode_attn_combine_kernel<64>, B * H, 64, stream, static_cast<const float*>(scratch), nsplit, Tq,
-                    tq, H, y);
+  const cudaError_t e = a.D == 128 ? cudaLaunchKernelEx(&cfg, decode_attn_kernel<128>, a, scale_log2, nsplit)
+                                   : cudaLaunchKernelEx(&cfg, decode_attn_kernel<64>, a, scale_log2, nsplit);
+  if (e != cudaSuccess) cudaGetLastError();
+  return e;
 }
 
 }  // namespace nc

@@ -134,7 +134,7 @@ struct nc_model {
   uint8_t* lm8 = nullptr;
   bf16* wg = nullptr;
   float* wscale = nullptr;
-  float2* rope = nullptr;   // [seq_len_ctx][D/2]
+  float2* rope = nullptr;   // [D/2][seq_len_ctx] (cos, sin), position fastest
   int* status = nullptr;    // device status word
   int device = 0;           // the device current at creation (where packed_buf lives)
   int num_sms = 148;
@@ -552,14 +552,11 @@ size_t kv_cache_bytes(const nc_model* m, int B, int T_max) {
 struct KvCtx {
   uint8_t* cache = nullptr;
   int T_max = 0;
-  bool decode = false;   // rows come in (pos - 1, pos) pairs; only the second of each pair is real
-  int pos = 0;           // decode: the position of the new token
-  float* scratch = nullptr;   // decode: split partials of the attention
-  size_t scratch_floats = 0;
 };
 
 // Decode workspace: the forward's layout for B row pairs, then the pair tokens [B][2], the
-// pair logits [B][2][V] and the decode attention's split partials.
+// q|k|v products [B][max Nqkv] fp32, the per-8-column partial sums of squares [B][C/8] and the
+// decode attention's split partials.
 size_t decode_scratch_floats(const nc_model* m, int B) {
   return static_cast<size_t>(B) * m->cfg.n_head * nc::decode_attention_splits(m->cfg.seq_len_ctx) *
          (m->cfg.head_dim + 2);
@@ -641,7 +638,6 @@ cudaError_t run_blocks(nc_model* m, const int32_t* tokens, int B, int T, const L
     qe.T = T;
     qe.rope = m->rope;
     qe.rope_ld = c.seq_len_ctx;
-    if (kv != nullptr && kv->decode) qe.rope = m->rope + (kv->pos - 1);   // row pair at positions pos-1, pos
     qe.vgate = ve ? 1 : 0;
     qe.gate_scale = c.ve_gate_scale;
     qe.ve = m->ve[i];
@@ -679,23 +675,14 @@ cudaError_t run_blocks(nc_model* m, const int32_t* tokens, int B, int T, const L
       bf16* vc = reinterpret_cast<bf16*>(kv_next + kv_tensor_bytes(m, B, cap));
       kv_next += 2 * kv_tensor_bytes(m, B, cap);
       e = timed(m, NC_K_ATTN, stream, [&] {
-        if (kv->decode) return nc::launch_kv_append(k, v, B, 2, 1, 1, kv->pos - 1, Hkv * D, kc, vc, cap, stream);
         const int first = std::max(0, T - cap);
         return nc::launch_kv_append(k, v, B, T, first, T - first, 0, Hkv * D, kc, vc, cap, stream);
       });
       if (e != cudaSuccess) break;
-      if (kv->decode) {
-        e = timed(m, NC_K_ATTN, stream, [&] {
-          return nc::launch_decode_attention(q, B, 2, 1, H, Hkv, D, kc, vc, cap, kv->pos, m->window[i], y, kv->scratch,
-                                             kv->scratch_floats, stream);
-        });
-        if (e != cudaSuccess) break;
-      }
     }
-    if (kv == nullptr || !kv->decode)
-      e = timed(m, NC_K_ATTN, stream, [&] {
-        return nc::launch_attention(q, k, v, B, T, H, Hkv, D, m->window[i], y, m->status, stream);
-      });
+    e = timed(m, NC_K_ATTN, stream, [&] {
+      return nc::launch_attention(q, k, v, B, T, H, Hkv, D, m->window[i], y, m->status, stream);
+    });
     if (e != cudaSuccess) break;
     nc::GemmEpi oe;
     resid(oe);
@@ -1137,13 +1124,179 @@ nc_status nc_prefill(nc_model* m, const int32_t* tokens, int B, int T, void* kv_
   return nc::cuda_status(e);
 }
 
+namespace {
+
+// Buffers of a decode step that the forward's layout does not have: after Lo.end, the pair
+// tokens [B][2] int32, the q|k|v products [B][max Nqkv] fp32, the partial sums of squares
+// [B][C / 8] fp32 that the residual products write, the attention's split counters [L][B][H]
+// (cleared at the start of each step) and its split partials.
+struct DecodeLayout {
+  size_t pair, raw, ssp8, counters, scratch, end;
+  int ldraw;
+};
+
+DecodeLayout decode_layout(const nc_model* m, int B) {
+  DecodeLayout d;
+  int nq = 0;
+  for (int i = 0; i < m->cfg.n_layer; ++i) nq = std::max(nq, m->Nqkv(i));
+  d.ldraw = nq;
+  d.pair = layout_for(m, B, 2).end;
+  d.raw = d.pair + align_up(2 * static_cast<size_t>(B) * 4);
+  d.ssp8 = d.raw + align_up(static_cast<size_t>(B) * nq * 4);
+  d.counters = d.ssp8 + align_up(static_cast<size_t>(B) * (m->cfg.n_embd / 8) * 4);
+  d.scratch = d.counters + align_up(static_cast<size_t>(m->cfg.n_layer) * B * m->cfg.n_head * 4);
+  d.end = d.scratch + align_up(decode_scratch_floats(m, B) * 4);
+  return d;
+}
+
+// One decode step (one new token per batch row at position pos), "nanochat — 架构与原理" section 2
+// (engine: KV cache, one token at a time).  The embedding runs on the pairs (token at pos - 1,
+// token at pos), so that its smear sees the previous token; everything after it runs on the B
+// second rows only (row 2b + 1 of the pair buffers): per layer the q|k|v product, its RoPE /
+// QK-norm / value-embedding epilogue with the cache append and the attention over the cache (one
+// launch), then the out-projection, fc and down-projection products with their
+// residual, squared-ReLU and mixing epilogues; finally the lm_head straight into `logits`.
+cudaError_t run_decode(nc_model* m, const int32_t* pair, const int32_t* tokens, int B, int pos, uint8_t* cache,
+                       int T_max, void* logits, uint8_t* ws, cudaStream_t stream) {
+  const nc_config& c = m->cfg;
+  const int C = c.n_embd, H = c.n_head, Hkv = c.n_kv_head, D = c.head_dim, F = c.mlp_hidden, V = c.vocab_size;
+  const int L = c.n_layer, HD = H * D, ncg = C / nc::SS_GROUP, n8 = C / 8;
+  const Layout Lo = layout_for(m, B, 2);
+  const DecodeLayout dl = decode_layout(m, B);
+  // the second row of each pair: row 2b + 1, pitch two rows
+  float* x0 = reinterpret_cast<float*>(ws + Lo.x0) + C;
+  float* x = reinterpret_cast<float*>(ws + Lo.x) + C;
+  float* xm = reinterpret_cast<float*>(ws + Lo.xm) + C;
+  bf16* xb = reinterpret_cast<bf16*>(ws + Lo.xb) + C;
+  bf16* y = reinterpret_cast<bf16*>(ws + Lo.y);   // the attention writes row 2b + 1 of its pair
+  bf16* h = reinterpret_cast<bf16*>(ws + Lo.h);   // dense [B][F]
+  float* ssp0 = reinterpret_cast<float*>(ws + Lo.ssp) + ncg;
+  float* raw = reinterpret_cast<float*>(ws + dl.raw);
+  float* ssp8 = reinterpret_cast<float*>(ws + dl.ssp8);
+  float* scratch = reinterpret_cast<float*>(ws + dl.scratch);
+  unsigned* counters = reinterpret_cast<unsigned*>(ws + dl.counters);
+  const int c_s = c.smear_gate_channels ? c.smear_gate_channels : C;
+  const int mid = L / 2 - 1;
+  const float inv_c = 1.0f / static_cast<float>(C);
+  uint8_t* kv_next = cache;
+
+  auto scale_from = [&](nc::GemvEpi& g, bool first) {   // the input's RMSNorm partials
+    g.ssp = first ? ssp0 : ssp8;
+    g.ssp_ld = first ? 2 * ncg : n8;
+    g.ssp_n = first ? ncg : n8;
+    g.inv_ncols = inv_c;
+    g.eps = c.rms_eps;
+  };
+  auto resid = [&](nc::GemvEpi& g) {
+    g.kind = nc::GEMV_RESID;
+    g.resid = x;
+    g.x_out = x;
+    g.ldx = 2 * C;
+    g.xb = xb;
+    g.ldb = 2 * C;
+    g.ssp_out = ssp8;
+    g.ssp_out_ld = n8;
+  };
+
+  cudaError_t e = cudaMemsetAsync(counters, 0, static_cast<size_t>(L) * B * H * sizeof(unsigned), stream);
+  if (e == cudaSuccess)
+    e = timed(m, NC_K_EMBED, stream, [&] {
+    return nc::launch_embed_smear(pair, B, 2, m->wte, V, C, m->smear, c_s, c.embed_norm, c.rms_eps,
+                                  m->lr[0] + m->l0[0], reinterpret_cast<float*>(ws + Lo.x0),
+                                  reinterpret_cast<float*>(ws + Lo.x), reinterpret_cast<bf16*>(ws + Lo.xb),
+                                  reinterpret_cast<float*>(ws + Lo.ssp), m->status, stream);
+  });
+  for (int i = 0; i < L && e == cudaSuccess; ++i) {
+    const int cap = kv_cap(m, i, T_max);
+    bf16* kc = reinterpret_cast<bf16*>(kv_next);
+    bf16* vc = reinterpret_cast<bf16*>(kv_next + kv_tensor_bytes(m, B, cap));
+    kv_next += 2 * kv_tensor_bytes(m, B, cap);
+    nc::GemvEpi qe;
+    qe.kind = nc::GEMV_RAW;
+    scale_from(qe, i == 0);
+    qe.out = raw;
+    qe.ldo = dl.ldraw;
+    e = timed(m, NC_K_QKV, stream, [&] {
+      return nc::launch_gemv(xb, 2 * C, B, m->wqkv + m->qkv_off[i], m->Nqkv(i), C, qe, stream);
+    });
+    if (e != cudaSuccess) break;
+    e = timed(m, NC_K_ATTN, stream, [&] {
+      nc::DecodeAttn da;
+      da.raw = raw;
+      da.ldraw = dl.ldraw;
+      da.B = B;
+      da.H = H;
+      da.Hkv = Hkv;
+      da.D = D;
+      da.vgate = m->has_ve[i] ? 1 : 0;
+      da.gate_scale = c.ve_gate_scale;
+      da.ve = m->ve[i];
+      da.tokens = tokens;
+      da.V = V;
+      da.rope = m->rope;
+      da.rope_ld = c.seq_len_ctx;
+      da.pos = pos;
+      da.eps = c.rms_eps;
+      da.kc = kc;
+      da.vc = vc;
+      da.cap = cap;
+      da.window = m->window[i];
+      da.scratch = scratch;
+      da.scratch_floats = decode_scratch_floats(m, B);
+      da.counters = counters + static_cast<size_t>(i) * B * H;
+      da.y = y + HD;
+      da.ldy = 2 * HD;
+      return nc::launch_decode_attention(da, stream);
+    });
+    if (e != cudaSuccess) break;
+    nc::GemvEpi oe;
+    resid(oe);
+    e = timed(m, NC_K_OPROJ, stream, [&] { return nc::launch_gemv(y + HD, 2 * HD, B, m->wo[i], C, HD, oe, stream); });
+    if (e != cudaSuccess) break;
+    nc::GemvEpi fe;
+    fe.kind = nc::GEMV_RELU2;
+    scale_from(fe, false);
+    fe.out = h;
+    fe.ldo = F;
+    e = timed(m, NC_K_FC, stream, [&] { return nc::launch_gemv(xb, 2 * C, B, m->wfc[i], F, C, fe, stream); });
+    if (e != cudaSuccess) break;
+    nc::GemvEpi pe;
+    resid(pe);
+    if (c.use_backout && i == mid) pe.xm_out = xm;
+    if (i + 1 < L) {   // the next block's residual mix
+      pe.a = m->lr[i + 1];
+      pe.b = m->l0[i + 1];
+      pe.Y = x0;
+    } else {           // final: backout; the lm_head needs only xb and the partials
+      pe.x_out = nullptr;
+      if (c.use_backout) {
+        pe.a = 1.f;
+        pe.b = -m->lb;
+        pe.Y = mid < 0 ? x0 : xm;
+      }
+    }
+    e = timed(m, NC_K_PROJ, stream, [&] { return nc::launch_gemv(h, F, B, m->wproj[i], C, F, pe, stream); });
+  }
+  if (e == cudaSuccess) {
+    nc::GemvEpi le;
+    le.kind = logit_bytes(m) == 2 ? nc::GEMV_SOFTCAP_BF16 : nc::GEMV_SOFTCAP_F32;
+    scale_from(le, L == 0);
+    le.out = logits;
+    le.ldo = V;
+    le.cap = c.softcap;
+    e = timed(m, NC_K_LMHEAD, stream, [&] { return nc::launch_gemv(xb, 2 * C, B, m->lm, V, C, le, stream); });
+  }
+  return e;
+}
+
+}  // namespace
+
 nc_status nc_workspace_bytes_decode(const nc_model* m, int B, size_t* bytes) {
   if (m == nullptr || bytes == nullptr || B < 1) return NC_ERR_INVALID_ARG;
   if (m->cfg.fp8) return NC_ERR_UNSUPPORTED;
   if (m->cfg.seq_len_ctx < 2) return NC_ERR_UNSUPPORTED;
-  const size_t rows = 2 * static_cast<size_t>(B);
-  *bytes = layout_for(m, B, 2).end + align_up(rows * 4) + align_up(rows * m->cfg.vocab_size * logit_bytes(m)) +
-           align_up(decode_scratch_floats(m, B) * 4);
+  if (nc::decode_attention_splits(m->cfg.seq_len_ctx) > nc::DA_MAX_SPLITS) return NC_ERR_UNSUPPORTED;
+  *bytes = decode_layout(m, B).end;
   return NC_OK;
 }
 
@@ -1165,33 +1318,15 @@ nc_status nc_decode_step(nc_model* m, const int32_t* prev_tokens, const int32_t*
   nc_status s = nc_workspace_bytes_decode(m, B, &need);
   if (s != NC_OK) return s;
   if (ws_bytes < need) return NC_ERR_WORKSPACE;
-  const Layout Lo = layout_for(m, B, 2);
-  const int V = m->cfg.vocab_size;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  int32_t* pair = reinterpret_cast<int32_t*>(ws + Lo.end);                        // [B][2] (prev, token)
-  const size_t lb = logit_bytes(m);
-  uint8_t* logits2 = ws + Lo.end + align_up(2 * static_cast<size_t>(B) * 4);   // [B][2][V]
-  float* attn_scratch = reinterpret_cast<float*>(logits2 + align_up(2 * static_cast<size_t>(B) * V * lb));
+  int32_t* pair = reinterpret_cast<int32_t*>(ws + decode_layout(m, B).pair);   // [B][2] (prev, token)
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
-  // Each row becomes the pair (previous token, new token): the embedding's smear then sees the
-  // previous token, and with the rotary table offset by pos - 1 the pair sits at positions
-  // pos - 1, pos.  Only the second row of a pair is used; every kernel but attention treats
-  // rows independently, and the decode attention reads the cache for the second rows only.
+  // Each row becomes the pair (previous token, new token) for the embedding, whose smear reads
+  // the previous token's embedding; the rest of the step runs on the second rows.
   cudaError_t e = cudaMemcpy2DAsync(pair, 8, prev_tokens, 4, 4, B, cudaMemcpyDeviceToDevice, stream);
   if (e == cudaSuccess) e = cudaMemcpy2DAsync(pair + 1, 8, tokens, 4, 4, B, cudaMemcpyDeviceToDevice, stream);
-  KvCtx kv;
-  kv.cache = static_cast<uint8_t*>(kv_cache);
-  kv.T_max = T_max;
-  kv.decode = true;
-  kv.pos = pos;
-  kv.scratch = attn_scratch;
-  kv.scratch_floats = decode_scratch_floats(m, B);
-  if (e == cudaSuccess) e = run_blocks(m, pair, B, 2, Lo, ws, stream, &kv);
   if (e == cudaSuccess)
-    e = launch_lm_head(m, ws, Lo, 2 * B, logits2, stream);
-  if (e == cudaSuccess)   // the second row of each pair
-    e = cudaMemcpy2DAsync(logits, static_cast<size_t>(V) * lb, logits2 + V * lb, 2 * static_cast<size_t>(V) * lb,
-                          static_cast<size_t>(V) * lb, B, cudaMemcpyDeviceToDevice, stream);
+    e = run_decode(m, pair, tokens, B, pos, static_cast<uint8_t*>(kv_cache), T_max, logits, ws, stream);
   return nc::cuda_status(e);
 }
 
@@ -1268,8 +1403,8 @@ int nc_forward_launch_count(const nc_model* m) {
 
 int nc_kv_launch_count(const nc_model* m) {
   if (m == nullptr) return 0;
-  return 2 + 7 * m->cfg.n_layer;   // a decode step: per layer q|k|v, cache append, the two attention
-                                   // passes, out-projection, fc, down projection (a prefill: one fewer)
+  return 2 + 5 * m->cfg.n_layer;   // a decode step: per layer q|k|v, attention (with the cache
+                                   // append), out-projection, fc, down projection
 }
 
 int nc_forward_loss_launch_count(const nc_model* m) {

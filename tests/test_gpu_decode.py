@@ -77,7 +77,7 @@ def test_decode_argument_errors():
     assert lib.nc_decode_step(*args(32, cache.numel(), 32)) == 1         # pos < T_max
     assert lib.nc_decode_step(*args(5, cache.numel(), 65)) == 2          # T_max > seq_len_ctx
     assert lib.nc_decode_step(*args(5, cache.numel() - 1, 32)) == 3      # cache too small
-    assert m.launch_count(kv=True) == 2 + 7 * cfg.n_layer
+    assert m.launch_count(kv=True) == 2 + 5 * cfg.n_layer
 
 
 def test_decode_step_replays_from_a_cuda_graph():
@@ -125,5 +125,22 @@ def test_decode_twelve_rows():
     _, dec = _decode_run(m, tok, T0, 64, pos)
     ref = O.forward(cfg, O.OracleWeights.from_synth(cfg, wts), tok.numpy())
     assert_parity(dec.cpu().numpy(), ref[:, T0:], "decode, 24 rows per step")
+    full = m.forward(tok.to(DEV)).cpu().numpy()
+    np.testing.assert_allclose(dec.cpu().numpy(), full[:, T0:], rtol=0, atol=2e-2)
+
+
+def test_decode_twenty_rows():
+    """B = 20: the step's products take the tokens in groups of 16, so the second group (4 rows)
+    exercises a partly filled group; the steps equal the oracle's rows and the forward's."""
+    wl = get_workload("tiny_all")
+    cfg = replace(wl.model, n_layer=2, window_left=(8, -1), has_ve=(1, 0), seq_len_ctx=64)
+    wts = make_weights(cfg, init="dense")
+    tok = torch.randint(0, cfg.vocab_size, (20, 36), generator=torch.Generator().manual_seed(24), dtype=torch.int32)
+    m = binding().Model(cfg, to_device(wts))
+    T0 = 32
+    pos = list(range(T0, 36))
+    _, dec = _decode_run(m, tok, T0, 64, pos)
+    ref = O.forward(cfg, O.OracleWeights.from_synth(cfg, wts), tok.numpy())
+    assert_parity(dec.cpu().numpy(), ref[:, T0:], "decode, 20 batch rows")
     full = m.forward(tok.to(DEV)).cpu().numpy()
     np.testing.assert_allclose(dec.cpu().numpy(), full[:, T0:], rtol=0, atol=2e-2)
