@@ -11,13 +11,14 @@
 //                  the prefill's append.
 //   decode_attn    a decode step's attention, one launch per layer: the q|k|v epilogue of the new
 //                  token (RoPE, QK-norm, gated value embedding) and its cache append, then one
-//                  query position per batch row split over the keys: one CTA per (row, head, 64
-//                  visible keys), 4 warps of 8 key slots (4 lanes per key, each a quarter of the
-//                  head dimension), online softmax in base 2 per slot (hardware exp2), slots
-//                  combined through shared memory; the last CTA of a (row, head) combines its
-//                  splits in a fixed order.  A key's value row is loaded with its key row (not
-//                  after its score) and two keys per slot are in flight, so the loads' latencies
-//                  overlap.  fp32 arithmetic; GQA reads kv head h / (H/Hkv).
+//                  query position per batch row split over the keys: a cluster of 8 CTAs per
+//                  (row, head), each an eighth of the cached keys, 8 warps reading whole key and
+//                  value rows (D/8 lanes per row), online softmax in base 2 per key slot
+//                  (hardware exp2), slots combined through shared memory; the cluster's rank 0
+//                  combines the splits and the new key in a fixed order from its peers' shared
+//                  memory.  A key's value row is loaded with its key row (not after its score)
+//                  and two steps are in flight, so the loads' latencies overlap.  fp32
+//                  arithmetic; GQA reads kv head h / (H/Hkv).
 #include "decode.h"
 #include "ptx.cuh"
 
@@ -28,8 +29,8 @@ namespace nc {
 namespace {
 
 constexpr int APPEND_THREADS = 256;
-constexpr int DA_WARPS = 4;
-constexpr int DA_KPS = 64;    // keys per split (2 steps of 32 keys for a CTA)
+constexpr int DA_WARPS = 8;
+constexpr int DA_SPLITS = 8;  // CTAs per (row, head): one cluster, combined through shared memory
 
 __global__ void __launch_bounds__(APPEND_THREADS)
     kv_append_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v, int B, int Tsrc, int t_first,
@@ -48,38 +49,41 @@ __global__ void __launch_bounds__(APPEND_THREADS)
   vc[dst] = v[src];
 }
 
-// The decode step's attention for one (batch row b, head h, split) CTA: the split takes the visible
-// keys [jlo + split * KPS, ...) (at most KPS).
+// The decode step's attention for one (batch row b, head h, split) CTA.  The keys before pos
+// (all cached by earlier steps or the prefill) are split evenly over the DA_SPLITS CTAs of a
+// cluster: split s takes [jlo + s * kps, ...) (at most kps); the new key at pos is a partial of
+// its own.
 //   Prologue, from the q|k|v products raw = rs * (x . W^T) of row b: the head's q rotated at pos
 //   and RMS-normed (threads 0 .. D/2-1, each the columns j and j + D/2), rounded to bf16 as the
-//   cache keeps k; on the split that holds position pos also the new key (rotated, normed) and
-//   value (+ gate * ve[token] on value-embedding layers) of kv head g = h / (H / Hkv), kept in
-//   shared memory for this CTA's own use; the CTA of the group's first q head writes them into
-//   the cache slot pos % cap.  No CTA reads that slot from memory in this launch.
-//   Keys: each warp scores 8 keys per step, 4 lanes per key (each lane a quarter of the head
-//   dimension), with an online softmax in base 2 per key slot (hardware exp2); a key's value row
-//   is loaded with its key row and two keys per slot are in flight.  The CTA's 32 slots are
-//   combined through shared memory into (sum_j 2^(s_j - M) v_j, M, sum_j 2^(s_j - M)), written to
-//   part[(b*H + h) * nsplit + split][0 .. D+1].
-//   The last CTA of (b, h) to finish (a counter, after a memory fence) combines the splits in
-//   split order: y = sum_s 2^(M_s - M) O_s / sum_s 2^(M_s - M) L_s, rounded to bf16.
+//   cache keeps k.  The cluster's rank 0 also computes the new key (rotated, normed) and value
+//   (+ gate * ve[token] on value-embedding layers) of kv head g = h / (H / Hkv), rounded to bf16;
+//   the rank 0 of the group's first q head writes them into the cache slot pos % cap, which no
+//   CTA of this launch reads.
+//   Keys: each warp takes 8 keys per step; a key's 256-byte row (D = 128; 128 at D = 64) is
+//   read whole by D/8 lanes, 16 B each, so one load instruction of the warp covers 2 (4) rows;
+//   those 2 (4) groups of lanes are the warp's key slots, each with an online softmax in base 2
+//   (hardware exp2) over its keys.  A key's value row is loaded with its key row and two steps
+//   are in flight.  The CTA's slots are combined through shared memory into
+//   (sum_j 2^(s_j - M) v_j, M, sum_j 2^(s_j - M)).
+//   After a cluster barrier, rank 0 reads the partials from its peers' shared memory and
+//   combines them in split order, then the new key's (score s, 1, v_new):
+//   y = sum 2^(M_s - M) O_s / sum 2^(M_s - M) L_s, rounded to bf16.
 // fp32 arithmetic throughout.
 template <int D>
 __global__ void __launch_bounds__(32 * DA_WARPS)
-    decode_attn_kernel(const __grid_constant__ DecodeAttn a, float scale_log2, int nsplit) {
-  constexpr int EL = D / 4;        // head-dimension elements per lane
-  constexpr int SLOTS = DA_WARPS * 8;
+    decode_attn_kernel(const __grid_constant__ DecodeAttn a, float scale_log2, int kps) {
+  constexpr int LPK = D / 8;             // lanes per key row (16 B each)
+  constexpr int KPI = 32 / LPK;           // key rows per load instruction of a warp: its key slots
+  constexpr int KPL = 8 / KPI;            // keys per lane and step (8 keys per warp and step)
+  constexpr int SLOTS = DA_WARPS * KPI;   // online-softmax slots of the CTA
   constexpr int HALF = D / 2;
-  __shared__ float s_m[SLOTS], s_l[SLOTS];
+  __shared__ float s_m[SLOTS], s_l[SLOTS], s_w[SLOTS];
   __shared__ float s_o[SLOTS][D];
   __shared__ float s_q[D];
   __shared__ __align__(16) bf16 s_kn[D];
   __shared__ __align__(16) bf16 s_vn[D];
-  __shared__ float s_red[2][2];
-  __shared__ float s_mv[DA_MAX_SPLITS], s_lv[DA_MAX_SPLITS], s_f[DA_MAX_SPLITS];
-  __shared__ int s_last;
-  griddep_wait();   // the q|k|v products come from the preceding kernel
-  griddep_launch();
+  __shared__ float s_red[DA_WARPS];
+  __shared__ float s_part[D + 2];   // the CTA's (O[D], M, L), read by the cluster's rank 0
   const int H = a.H, Hkv = a.Hkv;
   const int bh = blockIdx.x, split = blockIdx.y;
   const int b = bh / H, h = bh % H;
@@ -88,31 +92,41 @@ __global__ void __launch_bounds__(32 * DA_WARPS)
   const int kvcols = Hkv * D;
   const int pos = a.pos;
   const int jlo = a.window < 0 ? 0 : max(0, pos - a.window);
-  const int j0 = jlo + split * DA_KPS, j1 = min(pos + 1, j0 + DA_KPS);
-  const bool has_new = j1 == pos + 1;   // this split holds the new position
-  const size_t slot = (static_cast<size_t>(b) * a.cap + pos % a.cap) * kvcols + static_cast<size_t>(g) * D;
+  const int j0 = jlo + split * kps, j1 = min(pos, j0 + kps);   // cached keys only
+  const bool rank0 = split == 0;
+  // The split's cached rows (complete before the preceding kernel started) start their way from
+  // HBM into L2 now, while the preceding kernel still runs: one bulk prefetch per key and tensor.
+  {
+    const size_t base = static_cast<size_t>(b) * a.cap * kvcols + static_cast<size_t>(g) * D;
+    for (int j = j0 + (tid >> 1); j < j1; j += 32 * DA_WARPS / 2) {
+      const bf16* row = ((tid & 1) ? a.vc : a.kc) + base + static_cast<size_t>(j % a.cap) * kvcols;
+      bulk_prefetch_l2(row, D * 2);
+    }
+  }
+  griddep_wait();   // the q|k|v products come from the preceding kernel
+  griddep_launch();
   const float* r = a.raw + static_cast<size_t>(b) * a.ldraw;
   {
-    // role 0: q head h; role 1 (on the new key's split): k and v of kv head g
+    // role 0: q head h; role 1 (rank 0 only): k and v of kv head g
     const int role = tid / HALF, j = tid % HALF;
+    const bool act = role == 0 || (role == 1 && rank0);
     float c0 = 0.f, c1 = 0.f, ss = 0.f;
-    if (role == 0 || (role == 1 && has_new)) {
+    float2 cs = make_float2(0.f, 0.f);
+    if (act) {
       const int col = role == 0 ? h * D : (H + g) * D;
       c0 = r[col + j];
       c1 = r[col + j + HALF];
+      cs = a.rope[static_cast<size_t>(j) * a.rope_ld + pos];
       ss = c0 * c0 + c1 * c1;
     }
     if (role < 2) {
       ss = warp_sum(ss);
-      if (HALF > 32) {
-        if (lane == 0) s_red[role][(tid % HALF) >> 5] = ss;
-      }
+      if (HALF > 32 && lane == 0) s_red[warp] = ss;   // warps 2 role, 2 role + 1
     }
     __syncthreads();
-    if (role == 0 || (role == 1 && has_new)) {
-      if (HALF > 32) ss = s_red[role][0] + s_red[role][1];
+    if (act) {
+      if (HALF > 32) ss = s_red[2 * role] + s_red[2 * role + 1];
       const float sc = rsqrtf(ss * (1.0f / D) + a.eps);
-      const float2 cs = a.rope[static_cast<size_t>(j) * a.rope_ld + pos];
       const bf16 y1 = __float2bfloat16((c0 * cs.x + c1 * cs.y) * sc);
       const bf16 y2 = __float2bfloat16((c1 * cs.x - c0 * cs.y) * sc);
       if (role == 0) {
@@ -132,128 +146,135 @@ __global__ void __launch_bounds__(32 * DA_WARPS)
             v1 = fmaf(gg, __bfloat162float(e[j + HALF]), v1);
           }
         }
-        s_vn[j] = __float2bfloat16(v0);
-        s_vn[j + HALF] = __float2bfloat16(v1);
+        const bf16 w0 = __float2bfloat16(v0), w1 = __float2bfloat16(v1);
+        s_vn[j] = w0;
+        s_vn[j + HALF] = w1;
         if (h % (H / Hkv) == 0) {   // one writer per kv head: the group's first q head
+          const size_t slot = (static_cast<size_t>(b) * a.cap + pos % a.cap) * kvcols + static_cast<size_t>(g) * D;
           a.kc[slot + j] = y1;
           a.kc[slot + j + HALF] = y2;
-          a.vc[slot + j] = s_vn[j];
-          a.vc[slot + j + HALF] = s_vn[j + HALF];
+          a.vc[slot + j] = w0;
+          a.vc[slot + j + HALF] = w1;
         }
       }
     }
     __syncthreads();
   }
-  const int kk = lane >> 2, quarter = lane & 3;   // key slot within the warp, quarter of the head dim
-  float qv[EL];
+  // Key rows are read whole: LPK lanes per key, 16 B (8 elements) each, so one load instruction
+  // of the warp covers KPI complete rows; a lane owns head-dimension elements [8 sub, 8 sub + 8)
+  // of its key and accumulates the same elements of its slot's output.
+  const int kq = lane / LPK, sub = lane % LPK;   // key within an instruction (the slot), lane's 16 B
+  float qv[8];
 #pragma unroll
-  for (int e = 0; e < EL; ++e) qv[e] = s_q[quarter * EL + e];
-  float m = -INFINITY, l = 0.f, o[EL];
+  for (int e = 0; e < 8; ++e) qv[e] = s_q[sub * 8 + e];
+  float m = -INFINITY, l = 0.f, o[8];
 #pragma unroll
-  for (int e = 0; e < EL; ++e) o[e] = 0.f;
-  const size_t rowbase = static_cast<size_t>(b) * a.cap * kvcols + g * D + quarter * EL;
-  const uint4* kn = reinterpret_cast<const uint4*>(s_kn + quarter * EL);
-  const uint4* vn = reinterpret_cast<const uint4*>(s_vn + quarter * EL);
+  for (int e = 0; e < 8; ++e) o[e] = 0.f;
+  const size_t rowbase = static_cast<size_t>(b) * a.cap * kvcols + g * D + sub * 8;
 #pragma unroll 2
-  for (int jb = j0 + warp * 8; jb < j1; jb += SLOTS) {   // uniform across the warp
-    const int j = jb + kk;
-    const bool valid = j < j1;
-    const bool isnew = valid && j == pos;   // the new key: from shared memory
-    const bool ld = valid && !isnew;
-    const size_t off = rowbase + static_cast<size_t>(j % a.cap) * kvcols;
-    const uint4* kp = reinterpret_cast<const uint4*>(a.kc + off);
-    const uint4* vp = reinterpret_cast<const uint4*>(a.vc + off);
-    uint4 kw[EL / 8], vw[EL / 8];   // the key's and the value's rows, loaded together
+  for (int jb = j0 + warp * 8; jb < j1; jb += 32 * DA_WARPS / 4) {   // 8 keys per warp and step
+    uint4 kw[KPL], vw[KPL];   // the lane's 16 B of its KPL keys' key and value rows, loaded together
 #pragma unroll
-    for (int u = 0; u < EL / 8; ++u) {
-      kw[u] = ld ? __ldg(kp + u) : (isnew ? kn[u] : make_uint4(0u, 0u, 0u, 0u));
-      vw[u] = ld ? __ldg(vp + u) : (isnew ? vn[u] : make_uint4(0u, 0u, 0u, 0u));
+    for (int i = 0; i < KPL; ++i) {
+      const int j = jb + i * KPI + kq;
+      const size_t off = rowbase + static_cast<size_t>((j < j1 ? j : jb) % a.cap) * kvcols;
+      kw[i] = __ldg(reinterpret_cast<const uint4*>(a.kc + off));
+      vw[i] = __ldg(reinterpret_cast<const uint4*>(a.vc + off));
     }
-    float sc = 0.f;
 #pragma unroll
-    for (int u = 0; u < EL / 8; ++u) {
-      const uint4 w = kw[u];
-      const __nv_bfloat162* w2 = reinterpret_cast<const __nv_bfloat162*>(&w);
+    for (int i = 0; i < KPL; ++i) {
+      const int j = jb + i * KPI + kq;
+      const __nv_bfloat162* k2 = reinterpret_cast<const __nv_bfloat162*>(&kw[i]);
+      float sc = 0.f;
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
-        const float2 f = __bfloat1622float2(w2[t]);
-        sc = fmaf(qv[u * 8 + 2 * t], f.x, sc);
-        sc = fmaf(qv[u * 8 + 2 * t + 1], f.y, sc);
+        const float2 f = __bfloat1622float2(k2[t]);
+        sc = fmaf(qv[2 * t], f.x, sc);
+        sc = fmaf(qv[2 * t + 1], f.y, sc);
       }
-    }
-    sc += __shfl_xor_sync(0xffffffffu, sc, 1);
-    sc += __shfl_xor_sync(0xffffffffu, sc, 2);   // the key's full score, in base-2 units
-    if (valid) {
-      const float mn = fmaxf(m, sc);
-      const float corr = ex2_approx(m - mn);   // 0 on the slot's first key (m = -inf, sc finite)
-      const float p = ex2_approx(sc - mn);
-      l = fmaf(l, corr, p);
 #pragma unroll
-      for (int u = 0; u < EL / 8; ++u) {
-        const uint4 w = vw[u];
-        const __nv_bfloat162* w2 = reinterpret_cast<const __nv_bfloat162*>(&w);
+      for (int off2 = LPK / 2; off2 > 0; off2 >>= 1) sc += __shfl_xor_sync(0xffffffffu, sc, off2);
+      if (j < j1) {   // uniform across the key's LPK lanes
+        const float mn = fmaxf(m, sc);
+        const float corr = ex2_approx(m - mn);   // 0 on the slot's first key (m = -inf, sc finite)
+        const float p = ex2_approx(sc - mn);
+        l = fmaf(l, corr, p);
+        const __nv_bfloat162* v2 = reinterpret_cast<const __nv_bfloat162*>(&vw[i]);
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
-          const float2 f = __bfloat1622float2(w2[t]);
-          o[u * 8 + 2 * t] = fmaf(p, f.x, o[u * 8 + 2 * t] * corr);
-          o[u * 8 + 2 * t + 1] = fmaf(p, f.y, o[u * 8 + 2 * t + 1] * corr);
+          const float2 f = __bfloat1622float2(v2[t]);
+          o[2 * t] = fmaf(p, f.x, o[2 * t] * corr);
+          o[2 * t + 1] = fmaf(p, f.y, o[2 * t + 1] * corr);
         }
+        m = mn;
       }
-      m = mn;
     }
   }
-  const int kslot = warp * 8 + kk;
-  if (quarter == 0) {
+  const int kslot = warp * KPI + kq;
+  if (sub == 0) {
     s_m[kslot] = m;
     s_l[kslot] = l;
   }
 #pragma unroll
-  for (int e = 0; e < EL; ++e) s_o[kslot][quarter * EL + e] = o[e];
+  for (int e = 0; e < 8; ++e) s_o[kslot][sub * 8 + e] = o[e];
   __syncthreads();
-  float* part = a.scratch + static_cast<size_t>(bh) * nsplit * (D + 2);
-  float* dst = part + static_cast<size_t>(split) * (D + 2);
-  float M = -INFINITY;
-#pragma unroll
-  for (int w = 0; w < SLOTS; ++w) M = fmaxf(M, s_m[w]);
+  // the CTA's partial: the slots' weights 2^(m_w - M) once (an empty slot weighs 0), then sums
+  if (warp == 0) {
+    const float mw = lane < SLOTS ? s_m[lane] : -INFINITY;
+    const float M = warp_max(mw);
+    const float wv = mw == -INFINITY ? 0.f : exp2f(mw - M);
+    if (lane < SLOTS) s_w[lane] = wv;
+    const float L = warp_sum(lane < SLOTS ? s_l[lane] * wv : 0.f);
+    if (lane == 0) {
+      s_part[D] = M;
+      s_part[D + 1] = L;
+    }
+  }
+  __syncthreads();
   for (int d = tid; d < D; d += 32 * DA_WARPS) {
     float O = 0.f;
 #pragma unroll
-    for (int w = 0; w < SLOTS; ++w)
-      if (s_m[w] != -INFINITY) O = fmaf(s_o[w][d], exp2f(s_m[w] - M), O);
-    dst[d] = O;
+    for (int w = 0; w < SLOTS; ++w) O = fmaf(s_o[w][d], s_w[w], O);
+    s_part[d] = O;
   }
-  if (tid == 0) {
+  // The cluster combines: rank 0 reads every CTA's partial from its shared memory in split
+  // order, then adds the new key's; the second barrier keeps the peers' shared memory alive
+  // until it has.
+  cluster_sync();
+  if (rank0) {
+    // the new key's score q . k_new (base-2 units), a sum over the head dimension
+    float dq = tid < D ? s_q[tid] * __bfloat162float(s_kn[tid]) : 0.f;
+    dq = warp_sum(dq);
+    if (lane == 0) s_red[warp] = dq;
+    __syncthreads();
+    float snew = 0.f;
+#pragma unroll
+    for (int w = 0; w < DA_WARPS; ++w) snew += s_red[w];
+    const uint32_t base = smem_u32(s_part);
+    float Ms[DA_SPLITS], f[DA_SPLITS];
+    float Mx = snew;
+#pragma unroll
+    for (int s2 = 0; s2 < DA_SPLITS; ++s2) {
+      Ms[s2] = ld_shared_cluster_f32(mapa_shared(base + D * 4, s2));
+      Mx = fmaxf(Mx, Ms[s2]);
+    }
     float L = 0.f;
 #pragma unroll
-    for (int w = 0; w < SLOTS; ++w)
-      if (s_m[w] != -INFINITY) L = fmaf(s_l[w], exp2f(s_m[w] - M), L);
-    dst[D] = M;
-    dst[D + 1] = L;
+    for (int s2 = 0; s2 < DA_SPLITS; ++s2) {   // an empty split (M = -inf) weighs 0
+      f[s2] = Ms[s2] == -INFINITY ? 0.f : exp2f(Ms[s2] - Mx);
+      L = fmaf(ld_shared_cluster_f32(mapa_shared(base + (D + 1) * 4, s2)), f[s2], L);
+    }
+    const float fn = exp2f(snew - Mx);
+    L += fn;
+    for (int d = tid; d < D; d += 32 * DA_WARPS) {
+      float O = 0.f;
+#pragma unroll
+      for (int s2 = 0; s2 < DA_SPLITS; ++s2) O = fmaf(ld_shared_cluster_f32(mapa_shared(base + d * 4, s2)), f[s2], O);
+      O = fmaf(__bfloat162float(s_vn[d]), fn, O);
+      a.y[static_cast<size_t>(b) * a.ldy + h * D + d] = __float2bfloat16(O / L);
+    }
   }
-  // the last CTA of (b, h) combines the splits
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) s_last = atomicAdd(a.counters + bh, 1u) == static_cast<unsigned>(nsplit - 1);
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  for (int s2 = tid; s2 < nsplit; s2 += 32 * DA_WARPS) {
-    s_mv[s2] = __ldcg(part + static_cast<size_t>(s2) * (D + 2) + D);
-    s_lv[s2] = __ldcg(part + static_cast<size_t>(s2) * (D + 2) + D + 1);
-  }
-  __syncthreads();
-  float Mx = -INFINITY;
-  for (int s2 = 0; s2 < nsplit; ++s2) Mx = fmaxf(Mx, s_mv[s2]);
-  for (int s2 = tid; s2 < nsplit; s2 += 32 * DA_WARPS) s_f[s2] = exp2f(s_mv[s2] - Mx);
-  __syncthreads();
-  float L = 0.f;
-  for (int s2 = 0; s2 < nsplit; ++s2) L = fmaf(s_lv[s2], s_f[s2], L);
-  for (int d = tid; d < D; d += 32 * DA_WARPS) {
-    float O = 0.f;
-#pragma unroll 8
-    for (int s2 = 0; s2 < nsplit; ++s2) O = fmaf(__ldcg(part + static_cast<size_t>(s2) * (D + 2) + d), s_f[s2], O);
-    a.y[static_cast<size_t>(b) * a.ldy + h * D + d] = __float2bfloat16(O / L);
-  }
+  cluster_sync();
 }
 
 template <typename K, typename... Args>
@@ -285,31 +306,31 @@ cudaError_t launch_kv_append(const bf16* k, const bf16* v, int B, int Tsrc, int 
                     reinterpret_cast<uint4*>(kcache), reinterpret_cast<uint4*>(vcache), cap);
 }
 
-int decode_attention_splits(int T_max) { return (T_max + DA_KPS - 1) / DA_KPS; }
-
 cudaError_t launch_decode_attention(const DecodeAttn& a, cudaStream_t stream) {
-  if (a.raw == nullptr || a.kc == nullptr || a.vc == nullptr || a.y == nullptr || a.scratch == nullptr ||
-      a.counters == nullptr || a.rope == nullptr || a.B < 1 || a.H < 1 || a.Hkv < 1 || a.H % a.Hkv != 0 ||
-      a.pos < 0 || a.pos >= a.rope_ld || a.cap < 1 || a.ldy < a.H * a.D ||
-      (a.window < 0 ? a.cap <= a.pos : a.cap <= a.window && a.cap <= a.pos) ||
+  if (a.raw == nullptr || a.kc == nullptr || a.vc == nullptr || a.y == nullptr || a.rope == nullptr || a.B < 1 ||
+      a.H < 1 || a.Hkv < 1 || a.H % a.Hkv != 0 || a.pos < 0 || a.pos >= a.rope_ld || a.cap < 1 ||
+      a.ldy < a.H * a.D || (a.window < 0 ? a.cap <= a.pos : a.cap <= a.window && a.cap <= a.pos) ||
       (a.vgate && (a.ve == nullptr || a.tokens == nullptr)) ||
       a.ldraw < (a.H + a.Hkv) * a.D + a.Hkv * (a.vgate ? a.D + VGATE_ROWS : a.D))
     return cudaErrorInvalidValue;
   if (a.D != 64 && a.D != 128) return cudaErrorInvalidValue;
   const int jlo = a.window < 0 ? 0 : std::max(0, a.pos - a.window);
-  const int nsplit = (a.pos - jlo + 1 + DA_KPS - 1) / DA_KPS;
-  if (nsplit > DA_MAX_SPLITS || static_cast<size_t>(a.B) * a.H * nsplit * (a.D + 2) > a.scratch_floats)
-    return cudaErrorInvalidValue;
+  const int kps = (a.pos - jlo + DA_SPLITS - 1) / DA_SPLITS;   // cached keys per split (some may be empty)
   const float scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(a.D)));
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1] = {pdl_attribute()};
-  cfg.gridDim = dim3(a.B * a.H, nsplit);
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;   // the splits of one (row, head)
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = DA_SPLITS;
+  attr[0].val.clusterDim.z = 1;
+  attr[1] = pdl_attribute();
+  cfg.gridDim = dim3(a.B * a.H, DA_SPLITS);
   cfg.blockDim = dim3(32 * DA_WARPS);
   cfg.stream = stream;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  const cudaError_t e = a.D == 128 ? cudaLaunchKernelEx(&cfg, decode_attn_kernel<128>, a, scale_log2, nsplit)
-                                   : cudaLaunchKernelEx(&cfg, decode_attn_kernel<64>, a, scale_log2, nsplit);
+  cfg.numAttrs = 2;
+  const cudaError_t e = a.D == 128 ? cudaLaunchKernelEx(&cfg, decode_attn_kernel<128>, a, scale_log2, kps)
+                                   : cudaLaunchKernelEx(&cfg, decode_attn_kernel<64>, a, scale_log2, kps);
   if (e != cudaSuccess) cudaGetLastError();
   return e;
 }

@@ -18,14 +18,9 @@ cudaError_t launch_kv_append(const bf16* k, const bf16* v, int B, int Tsrc, int 
 // value embedding of tokens[b] on value-embedding layers), rounded to bf16, written into the
 // layer's cache slot pos % cap and used directly; softmax(q k^T / sqrt(D)) v over the cached
 // keys of positions max(0, pos - window) .. pos (all of 0 .. pos when window < 0), GQA head h
-// reading kv head h / (H / Hkv), rounded to bf16 into y + b * ldy + h * D.  One launch: split
-// over the keys, the splits combined by the last CTA of each (row, head) to finish.
+// reading kv head h / (H / Hkv), rounded to bf16 into y + b * ldy + h * D.  One launch: the keys
+// split over a cluster of CTAs per (row, head), the splits combined through shared memory.
 //   kc, vc: the layer's cache, [B][cap][Hkv * D] bf16.
-//   scratch: at least B * H * decode_attention_splits(T) * (D + 2) floats, T > pos.
-//   counters: B * H words, zero on entry (each CTA adds one).
-constexpr int DA_MAX_SPLITS = 256;   // visible keys per row: at most 64 * 256
-int decode_attention_splits(int T_max);
-
 struct DecodeAttn {
   const float* raw = nullptr;
   int ldraw = 0;
@@ -43,9 +38,6 @@ struct DecodeAttn {
   bf16* vc = nullptr;
   int cap = 0;
   int window = -1;
-  float* scratch = nullptr;
-  size_t scratch_floats = 0;
-  unsigned* counters = nullptr;
   bf16* y = nullptr;
   int ldy = 0;
 };

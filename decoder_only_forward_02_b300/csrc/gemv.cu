@@ -76,6 +76,23 @@ __global__ void __launch_bounds__(32 * GV_MAXW)
   float pv[GV_RSP];
 #pragma unroll
   for (int j = 0; j < GV_RSP; ++j) pv[j] = rsl && rp + 8 * j < ep.ssp_n ? rsp[rp + 8 * j] : 0.f;
+  // The residual epilogue's inputs (warp 0 applies the epilogue), loaded before the products.
+  const int n = n0 + 2 * t;
+  float2 xres[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+  float2 yres[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+  if constexpr (KIND == GEMV_RESID) {
+    if (warp == 0) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int b = b0 + g + 8 * h;
+        if (b < B) {
+          const size_t o = static_cast<size_t>(b) * ep.ldx + n;
+          xres[h] = *reinterpret_cast<const float2*>(ep.resid + o);
+          if (ep.Y != nullptr) yres[h] = *reinterpret_cast<const float2*>(ep.Y + o);
+        }
+      }
+    }
+  }
   // The two token rows of the lane: b0 + g (the fragment's rows g) and b0 + g + 8 (rows g + 8).
   const bool va = b0 + g < B, vb = b0 + g + 8 < B;
   const bf16* ar = A + static_cast<size_t>(va ? b0 + g : 0) * lda + 8 * t;
@@ -128,7 +145,6 @@ __global__ void __launch_bounds__(32 * GV_MAXW)
     for (int i = 0; i < 4; ++i) d[i] += red[w2 - 1][lane][i];
   }
   // d[2h], d[2h+1]: token b0 + g + 8h, columns n, n + 1
-  const int n = n0 + 2 * t;
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     const int b = b0 + g + 8 * h;
@@ -160,11 +176,11 @@ __global__ void __launch_bounds__(32 * GV_MAXW)
       float sq = 0.f;
       if (ok) {
         const size_t o = static_cast<size_t>(b) * ep.ldx + n;
-        const float2 xv = *reinterpret_cast<const float2*>(ep.resid + o);
+        const float2 xv = xres[h];
         const float xr0 = v0 + xv.x, xr1 = v1 + xv.y;
         float x0, x1;
         if (ep.Y != nullptr) {
-          const float2 yv = *reinterpret_cast<const float2*>(ep.Y + o);
+          const float2 yv = yres[h];
           x0 = fmaf(ep.a, xr0, ep.b * yv.x);
           x1 = fmaf(ep.a, xr1, ep.b * yv.y);
         } else {

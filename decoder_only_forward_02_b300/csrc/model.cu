@@ -554,14 +554,6 @@ struct KvCtx {
   int T_max = 0;
 };
 
-// Decode workspace: the forward's layout for B row pairs, then the pair tokens [B][2], the
-// q|k|v products [B][max Nqkv] fp32, the per-8-column partial sums of squares [B][C/8] and the
-// decode attention's split partials.
-size_t decode_scratch_floats(const nc_model* m, int B) {
-  return static_cast<size_t>(B) * m->cfg.n_head * nc::decode_attention_splits(m->cfg.seq_len_ctx) *
-         (m->cfg.head_dim + 2);
-}
-
 // The embedding and every block, up to the final backout: leaves the lm_head's input (before
 // its RMSNorm) as xb with its partial sums of squares in ssp.  With kv, each layer's keys and
 // values also go to the cache (prefill: the positions the layer's window can still see; decode:
@@ -1127,11 +1119,10 @@ nc_status nc_prefill(nc_model* m, const int32_t* tokens, int B, int T, void* kv_
 namespace {
 
 // Buffers of a decode step that the forward's layout does not have: after Lo.end, the pair
-// tokens [B][2] int32, the q|k|v products [B][max Nqkv] fp32, the partial sums of squares
-// [B][C / 8] fp32 that the residual products write, the attention's split counters [L][B][H]
-// (cleared at the start of each step) and its split partials.
+// tokens [B][2] int32, the q|k|v products [B][max Nqkv] fp32 and the partial sums of squares
+// [B][C / 8] fp32 that the residual products write.
 struct DecodeLayout {
-  size_t pair, raw, ssp8, counters, scratch, end;
+  size_t pair, raw, ssp8, end;
   int ldraw;
 };
 
@@ -1143,9 +1134,7 @@ DecodeLayout decode_layout(const nc_model* m, int B) {
   d.pair = layout_for(m, B, 2).end;
   d.raw = d.pair + align_up(2 * static_cast<size_t>(B) * 4);
   d.ssp8 = d.raw + align_up(static_cast<size_t>(B) * nq * 4);
-  d.counters = d.ssp8 + align_up(static_cast<size_t>(B) * (m->cfg.n_embd / 8) * 4);
-  d.scratch = d.counters + align_up(static_cast<size_t>(m->cfg.n_layer) * B * m->cfg.n_head * 4);
-  d.end = d.scratch + align_up(decode_scratch_floats(m, B) * 4);
+  d.end = d.ssp8 + align_up(static_cast<size_t>(B) * (m->cfg.n_embd / 8) * 4);
   return d;
 }
 
@@ -1173,8 +1162,6 @@ cudaError_t run_decode(nc_model* m, const int32_t* pair, const int32_t* tokens, 
   float* ssp0 = reinterpret_cast<float*>(ws + Lo.ssp) + ncg;
   float* raw = reinterpret_cast<float*>(ws + dl.raw);
   float* ssp8 = reinterpret_cast<float*>(ws + dl.ssp8);
-  float* scratch = reinterpret_cast<float*>(ws + dl.scratch);
-  unsigned* counters = reinterpret_cast<unsigned*>(ws + dl.counters);
   const int c_s = c.smear_gate_channels ? c.smear_gate_channels : C;
   const int mid = L / 2 - 1;
   const float inv_c = 1.0f / static_cast<float>(C);
@@ -1198,9 +1185,7 @@ cudaError_t run_decode(nc_model* m, const int32_t* pair, const int32_t* tokens, 
     g.ssp_out_ld = n8;
   };
 
-  cudaError_t e = cudaMemsetAsync(counters, 0, static_cast<size_t>(L) * B * H * sizeof(unsigned), stream);
-  if (e == cudaSuccess)
-    e = timed(m, NC_K_EMBED, stream, [&] {
+  cudaError_t e = timed(m, NC_K_EMBED, stream, [&] {
     return nc::launch_embed_smear(pair, B, 2, m->wte, V, C, m->smear, c_s, c.embed_norm, c.rms_eps,
                                   m->lr[0] + m->l0[0], reinterpret_cast<float*>(ws + Lo.x0),
                                   reinterpret_cast<float*>(ws + Lo.x), reinterpret_cast<bf16*>(ws + Lo.xb),
@@ -1241,9 +1226,6 @@ cudaError_t run_decode(nc_model* m, const int32_t* pair, const int32_t* tokens, 
       da.vc = vc;
       da.cap = cap;
       da.window = m->window[i];
-      da.scratch = scratch;
-      da.scratch_floats = decode_scratch_floats(m, B);
-      da.counters = counters + static_cast<size_t>(i) * B * H;
       da.y = y + HD;
       da.ldy = 2 * HD;
       return nc::launch_decode_attention(da, stream);
@@ -1295,7 +1277,6 @@ nc_status nc_workspace_bytes_decode(const nc_model* m, int B, size_t* bytes) {
   if (m == nullptr || bytes == nullptr || B < 1) return NC_ERR_INVALID_ARG;
   if (m->cfg.fp8) return NC_ERR_UNSUPPORTED;
   if (m->cfg.seq_len_ctx < 2) return NC_ERR_UNSUPPORTED;
-  if (nc::decode_attention_splits(m->cfg.seq_len_ctx) > nc::DA_MAX_SPLITS) return NC_ERR_UNSUPPORTED;
   *bytes = decode_layout(m, B).end;
   return NC_OK;
 }

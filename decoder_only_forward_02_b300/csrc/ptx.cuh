@@ -136,6 +136,11 @@ __device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int x
 }
 
 // Bring the 128-byte line holding `p` into L2 (no registers, no completion to wait for).
+// Bulk prefetch of `bytes` (a multiple of 16, 16-byte aligned source) into L2.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
@@ -386,6 +391,13 @@ __device__ __forceinline__ void cluster_sync() {
 }
 
 // Address of the same shared-memory location in CTA `rank` of the cluster.
+// fp32 load from a shared::cluster address (this CTA's or a peer's shared memory, via mapa).
+__device__ __forceinline__ float ld_shared_cluster_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));

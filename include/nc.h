@@ -266,11 +266,9 @@ NC_API nc_status nc_forward_loss_grad_tail(nc_model *m, const int32_t *tokens, c
  * >= nc_workspace_bytes_decode(B), 256-byte aligned.  A step runs the embedding, per layer the
  * q|k|v product, the attention (q|k|v epilogue, cache append, split attention and its combine in
  * one launch), the out-projection, fc and down-projection products, then the lm_head: each
- * product a small-row kernel that reads every weight once.  NC_ERR_UNSUPPORTED when seq_len_ctx
- * exceeds 16384 (the attention's split limit).
+ * product a small-row kernel that reads every weight once.
  * Both are asynchronous on `stream`; errors as nc_forward.  nc_kv_launch_count gives the kernels a
- * decode step launches (2 + 5 * n_layer, after one memset of its split counters; a prefill
- * launches 2 + 6 * n_layer).  After a first call on
+ * decode step launches (2 + 5 * n_layer; a prefill launches 2 + 6 * n_layer).  After a first call on
  * the device (per-device kernel set-up), nc_forward and nc_decode_step make no host synchronisation
  * or allocation, so a caller can capture them in a CUDA graph. */
 NC_API nc_status nc_kv_cache_bytes(const nc_model *m, int B, int T_max, size_t *bytes);
