@@ -199,6 +199,107 @@ __global__ void __launch_bounds__(32 * GV_MAXW)
   }
 }
 
+// The lm_head of a decode step: far more 8-row blocks than the SMs hold at once.  Persistent
+// CTAs take the row blocks rb = blockIdx.x + i * gridDim.x; the token rows are loaded once, and
+// the next block's weight bytes are in flight while the current block's products and epilogue
+// run.  Each warp's k steps fit in one register chunk (steps <= GV_SMAX).  Soft-capped logits.
+template <int KIND>
+__global__ void __launch_bounds__(32 * GV_MAXW)
+    gemv_rows_kernel(const bf16* __restrict__ A, int lda, int B, const bf16* __restrict__ W, int N, int K,
+                     int steps, const __grid_constant__ GemvEpi ep) {
+  __shared__ float red[GV_MAXW - 1][32][4];
+  __shared__ float rs_s[GV_TOK];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  const int g = lane >> 2, t = lane & 3;
+  const int b0 = blockIdx.y * GV_TOK;
+  const int ksteps = K / 32;
+  const int s0 = warp * steps, s1 = min(ksteps, s0 + steps);
+  const int nrb = N / GV_ROWS;
+  int rb = blockIdx.x;
+  uint4 w[GV_SMAX];
+  {
+    const bf16* wr = W + static_cast<size_t>(rb * GV_ROWS + g) * K + 8 * t;
+#pragma unroll
+    for (int s = 0; s < GV_SMAX; ++s)
+      w[s] = rb < nrb && s0 + s < s1 ? ldg16(wr + (s0 + s) * 32) : make_uint4(0u, 0u, 0u, 0u);
+  }
+  griddep_wait();   // the final stream's bf16 copy and its partial sums come from the preceding kernel
+  griddep_launch();
+  const int rt = threadIdx.x >> 3, rp = threadIdx.x & 7;
+  const bool rsl = ep.ssp != nullptr && threadIdx.x < 8 * GV_TOK && b0 + rt < B;
+  const float* rsp = rsl ? ep.ssp + static_cast<size_t>(b0 + rt) * ep.ssp_ld : nullptr;
+  const bool va = b0 + g < B, vb = b0 + g + 8 < B;
+  const bf16* ar = A + static_cast<size_t>(va ? b0 + g : 0) * lda + 8 * t;
+  const bf16* br = A + static_cast<size_t>(vb ? b0 + g + 8 : 0) * lda + 8 * t;
+  uint4 xa[GV_SMAX], xb[GV_SMAX];   // the token rows: loaded once for every row block
+#pragma unroll
+  for (int s = 0; s < GV_SMAX; ++s) {
+    xa[s] = va && s0 + s < s1 ? ldg16(ar + (s0 + s) * 32) : make_uint4(0u, 0u, 0u, 0u);
+    xb[s] = vb && s0 + s < s1 ? ldg16(br + (s0 + s) * 32) : make_uint4(0u, 0u, 0u, 0u);
+  }
+  if (threadIdx.x < 8 * GV_TOK) {   // the row scales, as in gemv_kernel (rows of any length)
+    float ss = 0.f;
+    for (int i0 = 0; i0 < ep.ssp_n; i0 += 8 * GV_RSP) {
+      float pv[GV_RSP];
+#pragma unroll
+      for (int j = 0; j < GV_RSP; ++j) pv[j] = rsl && i0 + rp + 8 * j < ep.ssp_n ? rsp[i0 + rp + 8 * j] : 0.f;
+#pragma unroll
+      for (int j = 0; j < GV_RSP; ++j) ss += pv[j];
+    }
+    ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+    ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+    ss += __shfl_xor_sync(0xffffffffu, ss, 4);
+    if (rp == 0) rs_s[rt] = ep.ssp != nullptr ? rsqrtf(ss * ep.inv_ncols + ep.eps) : 1.f;
+  }
+  for (; rb < nrb; rb += gridDim.x) {   // uniform across the CTA
+    const int nx = rb + gridDim.x;
+    uint4 wn[GV_SMAX];   // the next block's weight bytes, in flight during this block
+    {
+      const bf16* wr = W + static_cast<size_t>((nx < nrb ? nx : rb) * GV_ROWS + g) * K + 8 * t;
+#pragma unroll
+      for (int s = 0; s < GV_SMAX; ++s)
+        wn[s] = nx < nrb && s0 + s < s1 ? ldg16(wr + (s0 + s) * 32) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int s = 0; s < GV_SMAX; ++s) {
+      if (s0 + s < s1) {
+        mma_16816(d, xa[s].x, xb[s].x, xa[s].y, xb[s].y, w[s].x, w[s].y);
+        mma_16816(d, xa[s].z, xb[s].z, xa[s].w, xb[s].w, w[s].z, w[s].w);
+      }
+    }
+    if (warp > 0) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) red[warp - 1][lane][i] = d[i];
+    }
+    __syncthreads();
+    if (warp == 0) {
+      for (int w2 = 1; w2 < nw; ++w2) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) d[i] += red[w2 - 1][lane][i];
+      }
+      const int n = rb * GV_ROWS + 2 * t;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int b = b0 + g + 8 * h;
+        if (b < B) {
+          const float sc = rs_s[g + 8 * h] / ep.cap;
+          const float z0 = ep.cap * tanh_approx(d[2 * h] * sc), z1 = ep.cap * tanh_approx(d[2 * h + 1] * sc);
+          if constexpr (KIND == GEMV_SOFTCAP_F32)
+            __stcs(reinterpret_cast<float2*>(static_cast<float*>(ep.out) + static_cast<size_t>(b) * ep.ldo + n),
+                   make_float2(z0, z1));
+          else
+            *reinterpret_cast<uint32_t*>(static_cast<bf16*>(ep.out) + static_cast<size_t>(b) * ep.ldo + n) =
+                pack_bf16(z0, z1);
+        }
+      }
+    }
+    __syncthreads();   // red is refilled by the next block
+#pragma unroll
+    for (int s = 0; s < GV_SMAX; ++s) w[s] = wn[s];
+  }
+}
+
 template <typename Kern, typename... Args>
 cudaError_t launch_pdl2(Kern kernel, dim3 grid, int threads, cudaStream_t stream, Args... args) {
   cudaLaunchConfig_t cfg = {};
@@ -246,6 +347,19 @@ cudaError_t launch_gemv(const bf16* A, int lda, int B, const bf16* W, int N, int
   const int warps = std::min(GV_MAXW, std::max(4, nw));
   const int steps = (ksteps + warps - 1) / warps;
   const dim3 grid(N / GV_ROWS, (B + GV_TOK - 1) / GV_TOK);
+  if ((ep.kind == GEMV_SOFTCAP_F32 || ep.kind == GEMV_SOFTCAP_BF16) && steps <= GV_SMAX) {
+    // the lm_head: persistent CTAs, four per SM, when there are more row blocks than that
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return cudaErrorInvalidValue;
+    const int ctas = 4 * sms;
+    if (static_cast<int>(grid.x) > ctas) {
+      const dim3 pgrid(ctas, grid.y);
+      if (ep.kind == GEMV_SOFTCAP_F32)
+        return launch_pdl2(gemv_rows_kernel<GEMV_SOFTCAP_F32>, pgrid, 32 * warps, stream, A, lda, B, W, N, K, steps, ep);
+      return launch_pdl2(gemv_rows_kernel<GEMV_SOFTCAP_BF16>, pgrid, 32 * warps, stream, A, lda, B, W, N, K, steps, ep);
+    }
+  }
   switch (ep.kind) {
     case GEMV_RAW: return launch_pdl2(gemv_kernel<GEMV_RAW>, grid, 32 * warps, stream, A, lda, B, W, N, K, steps, ep);
     case GEMV_RESID:

@@ -245,18 +245,22 @@ def test_logits_bf16_is_the_rounded_fp32_forward(name, B, T):
     assert torch.equal(out_h, z16.cpu())
 
 
-def test_logits_bf16_prefill_and_decode():
-    wl = get_workload("tiny_all")
+@pytest.mark.parametrize("name,rows,T0", [("tiny_all", None, 40), ("d12", 2, 2040)])
+def test_logits_bf16_prefill_and_decode(name, rows, T0):
+    """bf16 logits of the prefill and of a decode step are the rounded fp32 ones.  At d12 the
+    decode step's lm_head (4,096 blocks of 8 vocabulary rows) runs on persistent CTAs."""
+    wl = get_workload(name)
     cfg = wl.model
-    w = to_device(make_weights(cfg, init="dense"))
-    tok = make_tokens(wl).to(DEV)
+    w = to_device(make_weights(cfg, seed=wl.seed, init=wl.init))
+    tok = make_tokens(wl)[:rows].to(DEV)
+    T_max = 64 if name == "tiny_all" else wl.T
     Bn = binding()
     outs = {}
     for bf in (False, True):
         m = Bn.Model(cfg, w, logits_bf16=bf)
-        cache = m.kv_cache(tok.shape[0], 64)
-        pre = m.prefill(tok[:, :40].contiguous(), cache, 64)
-        dec = m.decode_step(tok[:, 39].contiguous(), tok[:, 40].contiguous(), 40, cache, 64)
+        cache = m.kv_cache(tok.shape[0], T_max)
+        pre = m.prefill(tok[:, :T0].contiguous(), cache, T_max)
+        dec = m.decode_step(tok[:, T0 - 1].contiguous(), tok[:, T0].contiguous(), T0, cache, T_max)
         assert m.status() == 0
         outs[bf] = (pre, dec)
     assert outs[True][0].dtype == torch.bfloat16 and outs[True][1].dtype == torch.bfloat16
