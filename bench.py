@@ -489,6 +489,15 @@ def run_ours(args, rank, world, local_rank):
         dk = model.timing_read()
         model.timing(False)
         dec_kernels = {k: {"launches_per_step": n // 10, "us_per_step": 1000.0 * ms / 10} for k, (ms, n) in dk.items() if n}
+        # Algorithmic bytes of one step: every weight once (the packed q|k|v with its gate rows, the
+        # out-projection, fc, down projection, the lm_head) plus the cached keys and values each
+        # layer attends to (the new position's come from the step itself).
+        H_, Hkv_, D_, C_, F_, L_ = cfg.n_head, cfg.n_kv_head, cfg.head_dim, cfg.n_embd, cfg.mlp_hidden, cfg.n_layer
+        w_bytes = 2 * (sum(((H_ + 2 * Hkv_) * D_ + (Hkv_ * 16 if cfg.has_ve[i] else 0)) * C_ + C_ * H_ * D_ + 2 * F_ * C_
+                           for i in range(L_)) + V * C_)
+        kv_bytes = sum(B * (T0 - (0 if cfg.window_left[i] < 0 else max(0, T0 - cfg.window_left[i]))) * Hkv_ * D_ * 2 * 2
+                       for i in range(L_))
+        dec_peak = load_peaks().get("hbm_gbs")
         decode_path = {"metric": "decode tokens/s (one new token per batch row)", "value": job_rate(world, B, dec_ms),
                        "unit": UNIT, "ms_per_step": dec_ms, "steps": n_dec, "batch": B, "context": T,
                        "gpu_launches_per_step": model.launch_count(kv=True),
@@ -496,6 +505,15 @@ def run_ours(args, rank, world, local_rank):
                        "graph": {"value": job_rate(world, B, dec_graph_ms), "unit": UNIT,
                                  "ms_per_step": dec_graph_ms,
                                  "note": "the same nc_decode_step captured once in a CUDA graph and replayed"},
+                       "roofline": {"bound": "hbm", "bytes_per_step": w_bytes + kv_bytes, "weight_bytes": w_bytes,
+                                    "kv_bytes": kv_bytes,
+                                    "achieved": (w_bytes + kv_bytes) / (dec_graph_ms * 1e-3) / 1e9, "unit": "GB/s",
+                                    "peak": dec_peak,
+                                    "frac": ((w_bytes + kv_bytes) / (dec_graph_ms * 1e-3) / 1e9 / dec_peak)
+                                    if dec_peak else None,
+                                    "note": "algorithmic bytes of a step over the graph-replay time, against the "
+                                            "measured HBM copy rate: the step is a chain of 62 dependent launches, "
+                                            "so it is latency-bound, not bandwidth-bound"},
                        "note": "nc_decode_step at position T-1 after nc_prefill of T-1 tokens, repeated at that "
                                "position; small-row weight-streaming products and a one-launch attention per "
                                "layer, bound by the chain of dependent launches"}
