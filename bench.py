@@ -497,7 +497,7 @@ def run_ours(args, rank, world, local_rank):
                            for i in range(L_)) + V * C_)
         kv_bytes = sum(B * (T0 - (0 if cfg.window_left[i] < 0 else max(0, T0 - cfg.window_left[i]))) * Hkv_ * D_ * 2 * 2
                        for i in range(L_))
-        dec_peak = load_peaks().get("hbm_gbs")
+        dec_peak = load_peaks()[0].get("hbm_gbs")
         decode_path = {"metric": "decode tokens/s (one new token per batch row)", "value": job_rate(world, B, dec_ms),
                        "unit": UNIT, "ms_per_step": dec_ms, "steps": n_dec, "batch": B, "context": T,
                        "gpu_launches_per_step": model.launch_count(kv=True),
