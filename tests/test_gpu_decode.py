@@ -113,8 +113,8 @@ def test_decode_step_replays_from_a_cuda_graph():
 
 
 def test_decode_twelve_rows():
-    """B = 12 (24 rows per step, a window that wraps on the first layer): the steps equal the
-    forward's rows and the oracle's."""
+    """B = 12 (one group of 16 token rows, 12 of them filled; a window that wraps on the first
+    layer): the steps equal the forward's rows and the oracle's."""
     wl = get_workload("tiny_all")
     cfg = replace(wl.model, n_layer=2, window_left=(8, -1), has_ve=(0, 1), seq_len_ctx=64)
     wts = make_weights(cfg, init="dense")
@@ -124,7 +124,7 @@ def test_decode_twelve_rows():
     pos = list(range(T0, 40))
     _, dec = _decode_run(m, tok, T0, 64, pos)
     ref = O.forward(cfg, O.OracleWeights.from_synth(cfg, wts), tok.numpy())
-    assert_parity(dec.cpu().numpy(), ref[:, T0:], "decode, 24 rows per step")
+    assert_parity(dec.cpu().numpy(), ref[:, T0:], "decode, 12 batch rows")
     full = m.forward(tok.to(DEV)).cpu().numpy()
     np.testing.assert_allclose(dec.cpu().numpy(), full[:, T0:], rtol=0, atol=2e-2)
 
@@ -144,3 +144,18 @@ def test_decode_twenty_rows():
     assert_parity(dec.cpu().numpy(), ref[:, T0:], "decode, 20 batch rows")
     full = m.forward(tok.to(DEV)).cpu().numpy()
     np.testing.assert_allclose(dec.cpu().numpy(), full[:, T0:], rtol=0, atol=2e-2)
+
+
+def test_decode_from_the_first_positions():
+    """A prefill of one token, then decode steps at positions 1..12: with fewer cached keys than
+    the attention's eight splits, most splits are empty and the new key's partial dominates; a
+    window of 4 makes the ring wrap from position 5 on."""
+    wl = get_workload("tiny_all")
+    cfg = replace(wl.model, n_layer=2, window_left=(4, -1), has_ve=(1, 0), seq_len_ctx=64)
+    wts = make_weights(cfg, init="dense")
+    tok = torch.randint(0, cfg.vocab_size, (3, 13), generator=torch.Generator().manual_seed(25), dtype=torch.int32)
+    m = binding().Model(cfg, to_device(wts))
+    pre, dec = _decode_run(m, tok, 1, 64, list(range(1, 13)))
+    ref = O.forward(cfg, O.OracleWeights.from_synth(cfg, wts), tok.numpy())
+    assert_parity(pre.cpu().numpy(), ref[:, :1], "prefill of one token")
+    assert_parity(dec.cpu().numpy(), ref[:, 1:13], "decode, positions 1..12")
