@@ -351,10 +351,11 @@ __device__ __forceinline__ void lsu_store_box(const uint8_t* buf, void* out, siz
 // staging buffer, the logits with streaming stores.
 enum Bf16Mode { BF16_PLAIN = 0, BF16_RELU2 = 1, BF16_SOFTCAP = 2, BF16_CEGRAD = 3, BF16_DRELU2 = 4 };
 
-template <int MODE>
+template <int MODE, bool AMAX = false>
 __device__ __forceinline__ void epi_bf16(uint32_t taddr, uint32_t tempty, int lane, int m0w, int n0, int M, int N,
                                          const GemmEpi& ep, const OutMaps& om, Slab& sl, const EpiPre& pre) {
   const float rs = pre.rs, rs2 = 2.f * pre.rs;
+  float hmax = 0.f;   // AMAX (squared ReLU, 8-bit path): the largest value this warp stores
   const float cap = ep.cap, sc = rs / cap;
   const int m = m0w + lane;
   // EPI_CE_GRAD: exp(z - lse) = 2^(log2(e) * (cap * th - lse)); rows without a counted target
@@ -408,6 +409,7 @@ __device__ __forceinline__ void epi_bf16(uint32_t taddr, uint32_t tempty, int la
         } else if constexpr (MODE == BF16_RELU2) {
           t = fmaxf(t * rs, 0.f);
           t = t * t;
+          if constexpr (AMAX) hmax = fmaxf(hmax, t);   // rows and columns past the ends are 0
         } else if constexpr (MODE == BF16_SOFTCAP) {
           t = cap * tanh_approx(t * sc);
         } else if constexpr (MODE == BF16_CEGRAD) {
@@ -447,6 +449,11 @@ __device__ __forceinline__ void epi_bf16(uint32_t taddr, uint32_t tempty, int la
     }
   }
   release_acc(lane, tempty);
+  if constexpr (AMAX) {   // bf16 rounding keeps the order: the rounded maximum is the maximum stored
+    hmax = warp_max(hmax);
+    if (lane == 0 && ep.amax_out != nullptr)
+      atomicMax(reinterpret_cast<unsigned int*>(ep.amax_out), __float_as_uint(__bfloat162float(__float2bfloat16(hmax))));
+  }
 }
 
 // fp32 outputs: cap * tanh(rs * acc / cap) (logit soft-cap of the lm_head, streaming stores) or
@@ -896,7 +903,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       } else if constexpr (KIND == EPI_SOFTCAP_BF16) {
         epi_bf16<BF16_SOFTCAP>(taddr, tempty, lane, m0w, n0, M, N, ep, om, sl, pre);
       } else {
-        epi_bf16<KIND == EPI_RELU2_BF16 ? BF16_RELU2 : BF16_PLAIN>(taddr, tempty, lane, m0w, n0, M, N, ep, om, sl, pre);
+        epi_bf16<KIND == EPI_RELU2_BF16 ? BF16_RELU2 : BF16_PLAIN, F8 && KIND == EPI_RELU2_BF16>(
+            taddr, tempty, lane, m0w, n0, M, N, ep, om, sl, pre);
       }
     }
     if (lane == 0) bulk_wait<0>();   // stores complete before the CTA exits

@@ -103,29 +103,33 @@ __device__ __forceinline__ void tile_coords(int t, int num_n, int num_tiles, boo
 // v[0..15] summed over the 32 lanes of the warp, one sum per index: on return lane l holds the
 // total of index l >> 1 (lanes l and l ^ 1 hold the same value).  Halving exchange: at each step a
 // lane keeps one half of its values, adds the partner's copy of that half and sends the other.
+template <bool MAX>
+__device__ __forceinline__ float op(float a, float b) { return MAX ? fmaxf(a, b) : a + b; }
+
+template <bool MAX = false>
 __device__ __forceinline__ float lane_reduce16(const float (&v)[16], int lane) {
   const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4, b1 = lane & 2;
   float w8[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const float send = b4 ? v[i] : v[i + 8];
-    w8[i] = (b4 ? v[i + 8] : v[i]) + __shfl_xor_sync(0xffffffffu, send, 16);
+    w8[i] = op<MAX>(b4 ? v[i + 8] : v[i], __shfl_xor_sync(0xffffffffu, send, 16));
   }
   float w4[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const float send = b3 ? w8[i] : w8[i + 4];
-    w4[i] = (b3 ? w8[i + 4] : w8[i]) + __shfl_xor_sync(0xffffffffu, send, 8);
+    w4[i] = op<MAX>(b3 ? w8[i + 4] : w8[i], __shfl_xor_sync(0xffffffffu, send, 8));
   }
   float w2[2];
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
     const float send = b2 ? w4[i] : w4[i + 2];
-    w2[i] = (b2 ? w4[i + 2] : w4[i]) + __shfl_xor_sync(0xffffffffu, send, 4);
+    w2[i] = op<MAX>(b2 ? w4[i + 2] : w4[i], __shfl_xor_sync(0xffffffffu, send, 4));
   }
   const float send = b1 ? w2[0] : w2[1];
-  const float w = (b1 ? w2[1] : w2[0]) + __shfl_xor_sync(0xffffffffu, send, 2);
-  return w + __shfl_xor_sync(0xffffffffu, w, 1);
+  const float w = op<MAX>(b1 ? w2[1] : w2[0], __shfl_xor_sync(0xffffffffu, send, 2));
+  return op<MAX>(w, __shfl_xor_sync(0xffffffffu, w, 1));
 }
 
 template <bool F8>   // F8: e4m3 operands (the bf16 instantiation is unchanged)
@@ -346,13 +350,14 @@ __global__ void __launch_bounds__(THREADS, 1)
           xv[j] = xs[j / CH][(j % CH) * 32];
           yv[j] = has_y ? ys[j / CH][(j % CH) * 32] : 0.f;
         }
-        float sq[16], xrv[16];
+        float sq[16], xrv[16], ax[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           const float xr = fmaf(dq, __uint_as_float(r[j]), xv[j]);
           const float x = has_y ? fmaf(ea, xr, eb * yv[j]) : ea * xr;
           xrv[j] = xr;
           sq[j] = x * x;
+          ax[j] = fabsf(x);
           xs[j / CH][(j % CH) * 32] = x;
           bs[j / CH][(j % CH) * 32] = __float2bfloat16_rn(x);   // over the second input, already read
         }
@@ -375,6 +380,16 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
           for (int j = 0; j < 16; ++j)
             if (row + j < M) ep.xm_out[static_cast<size_t>(row + j) * N + col + lane] = xrv[j];
+        }
+        // 8-bit path: each token's largest |x'| over this warp's 32 columns, for the maximum
+        // the next quantisation of the stream needs
+        if constexpr (F8) {
+          if (ep.rowmax_out != nullptr) {
+            const float amx = lane_reduce16<true>(ax, lane);
+            const int tok = row + (lane >> 1);
+            if ((lane & 1) == 0 && col_ok && tok < M)
+              ep.rowmax_out[static_cast<size_t>(tok) * (N / 32) + col / 32] = amx;
+          }
         }
         // this warp's 32 columns of each token's sum of squares (across lanes)
         const float ssum = lane_reduce16(sq, lane);

@@ -71,6 +71,14 @@ struct GemmEpi {
   int ldo = 0;
   float cap = 15.f;
 
+  // 8-bit producers of the next quantisation's maximum: EPI_RESID on the 8-bit path writes
+  // rowmax_out[m * (N / 32) + n / 32] = max |x'| over columns [n, n + 32) when set; EPI_RELU2_BF16
+  // on the 8-bit path raises *amax_out (fp32 bits compared as unsigned: the values are >= 0) to the
+  // largest h it stores (after its bf16 rounding) when set.  Both are exact maxima, the same
+  // numbers a pass over the stored tensor would find.
+  float* rowmax_out = nullptr;
+  float* amax_out = nullptr;
+
   // EPI_RESID (launch_gemm_resid; N = ncols of the stream, N % 128 == 0):
   //   xr = resid + acc;  xm_out <- xr (if set);  x' = a * xr + b * Y (Y may be null);
   //   x_out <- x' (if set, may alias resid);  xb <- bf16(x');
@@ -230,14 +238,20 @@ cudaError_t launch_ce_finalize(const float* part, const float* zt, const int32_t
 // ---- 8-bit (e4m3) tensorwise quantisation: q = e4m3(v * s), s = 448 / max|v| over the whole tensor
 // (1 when it is all zero), round to nearest even, saturating at +-448.  v = src[m, c], times the
 // row's RMSNorm scale rs[m] = 1 / sqrt(sum_g ssp[m, g] / C + eps) when ssp is given.  Two launches:
-// fp8_amax writes per-block maxima to partial[FP8_AMAX_BLOCKS]; fp8_quantize reduces them in every
-// block, writes q [M, ld_dst] and inv_scale[0] = 1 / s.  Rows of src are `ld` elements apart; dst
-// row r goes to r + (r / group) * gap (group = 0: no remap), for the packed q|k|v weight's v heads.
+// fp8_amax writes per-block maxima to partial[FP8_AMAX_BLOCKS]; fp8_quantize reduces partial[0 ..
+// npart) in every block, writes q [M, ld_dst] and inv_scale[0] = 1 / s.  Rows of src are `ld`
+// elements apart; dst row r goes to r + (r / group) * gap (group = 0: no remap), for the packed
+// q|k|v weight's v heads.  fp8_amax_rows computes the same per-block maxima of a row-scaled stream
+// from its producer's per-row maxima of |v| over 32-column groups (rowmax [M][C/32], written by
+// the residual GEMM's epilogue), without reading the stream: max over rows of rs[m] * max|v[m, :]|
+// is the same number either way (multiplication by rs > 0 keeps the order of rounded products).
 constexpr int FP8_AMAX_BLOCKS = 592;
 cudaError_t launch_fp8_amax(const void* src, int src_f32, int M, int C, int ld, const float* ssp, float eps,
                             float* partial, cudaStream_t stream);
+cudaError_t launch_fp8_amax_rows(const float* rowmax, int M, int C, const float* ssp, float eps, float* partial,
+                                 cudaStream_t stream);
 cudaError_t launch_fp8_quantize(const void* src, int src_f32, int M, int C, int ld, const float* ssp, float eps,
-                                const float* partial, uint8_t* dst, int ld_dst, int group, int gap,
+                                const float* partial, int npart, uint8_t* dst, int ld_dst, int group, int gap,
                                 float* inv_scale, cudaStream_t stream);
 
 // Backward of the weightless RMSNorm xn = rs * x (rs = 1 / sqrt(mean x^2 + eps), from the partial

@@ -97,7 +97,7 @@ struct Layout {
   // 8-bit path only (zero-sized otherwise): quantised activations (the normed stream, the
   // attention output, the MLP hidden layer), the bf16 gate pre-activations [M, 32], the amax
   // scratch and the 1 / scale of each quantised activation
-  size_t a8, y8, h8, gpre, qpart, qscale;
+  size_t a8, y8, h8, gpre, qpart, qscale, rowmax, hmax;
   size_t end;
 };
 
@@ -230,7 +230,8 @@ cudaError_t quantize_weight(const void* src, int rows, int cols, uint8_t* dst, i
                             float* part, cudaStream_t stream) {
   cudaError_t e = nc::launch_fp8_amax(src, 0, rows, cols, cols, nullptr, 0.f, part, stream);
   if (e == cudaSuccess)
-    e = nc::launch_fp8_quantize(src, 0, rows, cols, cols, nullptr, 0.f, part, dst, cols, group, gap, inv, stream);
+    e = nc::launch_fp8_quantize(src, 0, rows, cols, cols, nullptr, 0.f, part, nc::FP8_AMAX_BLOCKS, dst, cols, group,
+                                gap, inv, stream);
   return e;
 }
 
@@ -303,6 +304,8 @@ Layout layout_for(const nc_model* m, int B, int T) {
   L.gpre = take(f8 * M * 32 * 4);
   L.qpart = take(f8 * nc::FP8_AMAX_BLOCKS * 4);
   L.qscale = take(f8 * 8 * 4);
+  L.rowmax = take(f8 * M * (c.n_embd / 32) * 4);
+  L.hmax = take(f8 * c.n_layer * 4);
   L.end = off;
   return L;
 }
@@ -599,23 +602,41 @@ cudaError_t run_blocks(nc_model* m, const int32_t* tokens, int B, int T, const L
   float* gpre = reinterpret_cast<float*>(ws + Lo.gpre);
   float* qpart = reinterpret_cast<float*>(ws + Lo.qpart);
   float* qscale = reinterpret_cast<float*>(ws + Lo.qscale);   // 1 / scale: [0] q|k|v input, [1] y, [2] fc input, [3] h
+  // The maximum comes from a pass over the tensor, from the producer's per-row maxima of the fp32
+  // stream (the residual GEMMs write them on this path), or as one word the producer raised (the
+  // fc's squared ReLU); the same number each way.
+  float* rowmax = reinterpret_cast<float*>(ws + Lo.rowmax);
+  float* hmax = reinterpret_cast<float*>(ws + Lo.hmax);   // [L]: each block's fc output maximum
   auto quant = [&](const void* src, int f32, int cols, const float* row_ssp, uint8_t* dst, float* inv) {
     cudaError_t r = timed(m, NC_K_QUANT, stream, [&] {
       return nc::launch_fp8_amax(src, f32, M, cols, cols, row_ssp, c.rms_eps, qpart, stream);
     });
     if (r == cudaSuccess)
       r = timed(m, NC_K_QUANT, stream, [&] {
-        return nc::launch_fp8_quantize(src, f32, M, cols, cols, row_ssp, c.rms_eps, qpart, dst, cols, 0, 0, inv,
+        return nc::launch_fp8_quantize(src, f32, M, cols, cols, row_ssp, c.rms_eps, qpart, nc::FP8_AMAX_BLOCKS, dst,
+                                       cols, 0, 0, inv, stream);
+      });
+    return r;
+  };
+  auto quant_stream = [&](uint8_t* dst, float* inv) {   // the normed fp32 stream x, from rowmax
+    cudaError_t r = timed(m, NC_K_QUANT, stream, [&] {
+      return nc::launch_fp8_amax_rows(rowmax, M, C, ssp, c.rms_eps, qpart, stream);
+    });
+    if (r == cudaSuccess)
+      r = timed(m, NC_K_QUANT, stream, [&] {
+        return nc::launch_fp8_quantize(x, 1, M, C, C, ssp, c.rms_eps, qpart, nc::FP8_AMAX_BLOCKS, dst, C, 0, 0, inv,
                                        stream);
       });
     return r;
   };
   auto as8 = [](const void* p) { return static_cast<const bf16*>(p); };   // e4m3 operands travel as untyped bytes
 
-  cudaError_t e = timed(m, NC_K_EMBED, stream, [&] {
-    return nc::launch_embed_smear(tokens, B, T, m->wte, V, C, m->smear, c_s, c.embed_norm, c.rms_eps,
-                                  m->lr[0] + m->l0[0], x0, x, xb, ssp, m->status, stream);
-  });
+  cudaError_t e = f8 ? cudaMemsetAsync(hmax, 0, static_cast<size_t>(L) * sizeof(float), stream) : cudaSuccess;
+  if (e == cudaSuccess)
+    e = timed(m, NC_K_EMBED, stream, [&] {
+      return nc::launch_embed_smear(tokens, B, T, m->wte, V, C, m->smear, c_s, c.embed_norm, c.rms_eps,
+                                    m->lr[0] + m->l0[0], x0, x, xb, ssp, m->status, stream);
+    });
   for (int i = 0; i < L && e == cudaSuccess; ++i) {
     const bool ve = m->has_ve[i] != 0;
     nc::GemmEpi qe;
@@ -636,7 +657,7 @@ cudaError_t run_blocks(nc_model* m, const int32_t* tokens, int B, int T, const L
     qe.tokens = tokens;
     qe.V = V;
     if (f8) {
-      e = quant(x, 1, C, ssp, a8, qscale + 0);
+      e = i == 0 ? quant(x, 1, C, ssp, a8, qscale + 0) : quant_stream(a8, qscale + 0);
       if (e == cudaSuccess && ve) {   // the value-embedding gates' dot products, bf16: rs * (xb . W_g^T)
         nc::GemmEpi ge;
         set_consumer(ge, m, ssp);
@@ -682,6 +703,7 @@ cudaError_t run_blocks(nc_model* m, const int32_t* tokens, int B, int T, const L
       e = quant(y, 0, H * D, nullptr, y8, qscale + 1);
       if (e != cudaSuccess) break;
       oe.fp8 = 1;
+      oe.rowmax_out = rowmax;   // the fc input's maximum
       oe.fp8_sa = qscale + 1;
       oe.fp8_sw = m->wscale + 6 * i + 3;
     }
@@ -697,10 +719,11 @@ cudaError_t run_blocks(nc_model* m, const int32_t* tokens, int B, int T, const L
     fe.out = h;
     fe.ldo = F;
     if (f8) {
-      e = quant(x, 1, C, ssp, a8, qscale + 2);
+      e = quant_stream(a8, qscale + 2);
       if (e != cudaSuccess) break;
       fe.ssp_in = nullptr;
       fe.fp8 = 1;
+      fe.amax_out = hmax + i;   // the down projection's input maximum
       fe.fp8_sa = qscale + 2;
       fe.fp8_sw = m->wscale + 6 * i + 4;
     }
@@ -732,9 +755,13 @@ cudaError_t run_blocks(nc_model* m, const int32_t* tokens, int B, int T, const L
       if (f8) pe.x_out = x;   // the lm_head's input is quantised from the fp32 stream
     }
     if (f8) {
-      e = quant(h, 0, F, nullptr, h8, qscale + 3);
+      e = timed(m, NC_K_QUANT, stream, [&] {
+        return nc::launch_fp8_quantize(h, 0, M, F, F, nullptr, c.rms_eps, hmax + i, 1, h8, F, 0, 0, qscale + 3,
+                                       stream);
+      });
       if (e != cudaSuccess) break;
       pe.fp8 = 1;
+      pe.rowmax_out = rowmax;   // the next block's q|k|v input (or the lm_head's) maximum
       pe.fp8_sa = qscale + 3;
       pe.fp8_sw = m->wscale + 6 * i + 5;
     }
@@ -831,12 +858,15 @@ cudaError_t lm_head_operands(nc_model* m, uint8_t* ws, const Layout& Lo, int M, 
   float* qpart = reinterpret_cast<float*>(ws + Lo.qpart);
   float* inv = reinterpret_cast<float*>(ws + Lo.qscale) + 4;
   uint8_t* a8 = ws + Lo.a8;
+  // the maximum from the last down projection's per-row maxima of x
+  const float* rowmax = reinterpret_cast<const float*>(ws + Lo.rowmax);
   cudaError_t e = timed(m, NC_K_QUANT, stream, [&] {
-    return nc::launch_fp8_amax(x, 1, M, C, C, ssp, m->cfg.rms_eps, qpart, stream);
+    return nc::launch_fp8_amax_rows(rowmax, M, C, ssp, m->cfg.rms_eps, qpart, stream);
   });
   if (e == cudaSuccess)
     e = timed(m, NC_K_QUANT, stream, [&] {
-      return nc::launch_fp8_quantize(x, 1, M, C, C, ssp, m->cfg.rms_eps, qpart, a8, C, 0, 0, inv, stream);
+      return nc::launch_fp8_quantize(x, 1, M, C, C, ssp, m->cfg.rms_eps, qpart, nc::FP8_AMAX_BLOCKS, a8, C, 0, 0, inv,
+                                     stream);
     });
   le.ssp_in = nullptr;
   le.fp8 = 1;
@@ -1375,11 +1405,12 @@ nc_status nc_timing_read(nc_model* m, nc_kernel_class k, double* total_ms, int* 
 int nc_forward_launch_count(const nc_model* m) {
   if (m == nullptr) return 0;
   if (!m->cfg.fp8) return 2 + 5 * m->cfg.n_layer;
-  // 8-bit: per block four quantisations (two launches each) and the gate product on
-  // value-embedding layers; the lm_head's input quantisation
+  // 8-bit: per block four quantisations (two launches each, but one for the fc output, whose
+  // maximum the fc epilogue keeps) and the gate product on value-embedding layers; the lm_head's
+  // input quantisation
   int ve = 0;
   for (int i = 0; i < m->cfg.n_layer; ++i) ve += m->has_ve[i] ? 1 : 0;
-  return 2 + 5 * m->cfg.n_layer + 8 * m->cfg.n_layer + ve + 2;
+  return 2 + 5 * m->cfg.n_layer + 7 * m->cfg.n_layer + ve + 2;
 }
 
 int nc_kv_launch_count(const nc_model* m) {

@@ -295,7 +295,8 @@ nc_status nc_op_fp8_quantize(const void* src, int src_f32, int M, int C, const f
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = nc::launch_fp8_amax(src, src_f32, M, C, C, ssp, eps, part, s);
   if (e == cudaSuccess)
-    e = nc::launch_fp8_quantize(src, src_f32, M, C, C, ssp, eps, part, static_cast<uint8_t*>(dst), C, 0, 0, inv_scale,
+    e = nc::launch_fp8_quantize(src, src_f32, M, C, C, ssp, eps, part, nc::FP8_AMAX_BLOCKS, static_cast<uint8_t*>(dst),
+                                C, 0, 0, inv_scale,
                                 s);
   return cuda_status(e);
 }

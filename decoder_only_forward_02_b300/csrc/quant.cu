@@ -9,8 +9,10 @@
 //
 //   fp8_amax      one warp per row (grid-stride), per-block maxima of |v| (times the row's RMSNorm
 //                 scale when the input is a normed residual stream) -> partial[FP8_AMAX_BLOCKS]
+//   fp8_amax_rows the same per-block maxima of a row-scaled stream from its producer's per-row
+//                 maxima over 32-column groups (the residual GEMM writes them), reading 1/32 of it
 //   fp8_quantize  every block first reduces the partial maxima (the same fixed order in every
-//                 block), then one warp per row converts 8 elements per lane-step to e4m3.  The
+//                 block; a single word when the producer kept the maximum itself), then one warp per row converts 8 elements per lane-step to e4m3.  The
 //                 scaled value is (v * 448) / amax, not v * (448 / amax): for bf16 v the product
 //                 is exact, so a value that the exact scaling puts on a rounding tie of the e4m3
 //                 grid (frequent: bf16 values have few significant bits) stays exactly on it and
@@ -21,7 +23,8 @@
 //                 boundary cases; no per-element division.
 // Both kernels keep four 16- or 32-byte loads per lane in flight (a row's chunks are loaded before
 // they are reduced or converted).
-// No atomics: the scale and the codes are the same on every run.
+// No atomics here; the producers' maxima are exact (order-independent): the scale and the codes are
+// the same on every run.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -105,9 +108,36 @@ __global__ void __launch_bounds__(QT) fp8_amax_kernel(const void* __restrict__ s
   }
 }
 
+// The same per-block maxima as fp8_amax_kernel for a row-scaled fp32 stream, from its per-row,
+// per-32-column maxima of |v| (written by the producer's epilogue): one warp per row.
+__global__ void __launch_bounds__(QT) fp8_amax_rows_kernel(const float* __restrict__ rowmax, int M, int C,
+                                                           const float* __restrict__ ssp, float eps,
+                                                           float* __restrict__ partial) {
+  __shared__ float sh[QT / 32];
+  griddep_wait();
+  griddep_launch();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nw = gridDim.x * (QT / 32), ng = C / 32;
+  float mx = 0.f;
+  for (int row = blockIdx.x * (QT / 32) + warp; row < M; row += nw) {
+    const float rs = row_scale(ssp, row, C, eps, lane);
+    float m = 0.f;
+    for (int gi = lane; gi < ng; gi += 32) m = fmaxf(m, rowmax[static_cast<size_t>(row) * ng + gi]);
+    mx = fmaxf(mx, m * rs);
+  }
+  mx = warp_max(mx);
+  if (lane == 0) sh[warp] = mx;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float b = 0.f;
+    for (int w = 0; w < QT / 32; ++w) b = fmaxf(b, sh[w]);
+    partial[blockIdx.x] = b;
+  }
+}
+
 __global__ void __launch_bounds__(QT) fp8_quantize_kernel(const void* __restrict__ src, int f32, int M, int C, int ld,
                                                           const float* __restrict__ ssp, float eps,
-                                                          const float* __restrict__ partial,
+                                                          const float* __restrict__ partial, int npart,
                                                           uint8_t* __restrict__ dst, int ld_dst, int group, int gap,
                                                           float* __restrict__ inv_scale) {
   __shared__ float sh[QT / 32];
@@ -115,7 +145,7 @@ __global__ void __launch_bounds__(QT) fp8_quantize_kernel(const void* __restrict
   griddep_launch();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   float a = 0.f;
-  for (int i = threadIdx.x; i < FP8_AMAX_BLOCKS; i += QT) a = fmaxf(a, partial[i]);
+  for (int i = threadIdx.x; i < npart; i += QT) a = fmaxf(a, partial[i]);
   a = warp_max(a);
   if (lane == 0) sh[warp] = a;
   __syncthreads();
@@ -188,17 +218,26 @@ cudaError_t launch_fp8_amax(const void* src, int src_f32, int M, int C, int ld, 
   return launch_q(fp8_amax_kernel, FP8_AMAX_BLOCKS, stream, src, src_f32, M, C, ld, ssp, eps, partial);
 }
 
+cudaError_t launch_fp8_amax_rows(const float* rowmax, int M, int C, const float* ssp, float eps, float* partial,
+                                 cudaStream_t stream) {
+  if (rowmax == nullptr || partial == nullptr || M < 1 || C < 32 || C % 32 != 0 ||
+      (ssp != nullptr && C % SS_GROUP != 0))
+    return cudaErrorInvalidValue;
+  return launch_q(fp8_amax_rows_kernel, FP8_AMAX_BLOCKS, stream, rowmax, M, C, ssp, eps, partial);
+}
+
 cudaError_t launch_fp8_quantize(const void* src, int src_f32, int M, int C, int ld, const float* ssp, float eps,
-                                const float* partial, uint8_t* dst, int ld_dst, int group, int gap,
+                                const float* partial, int npart, uint8_t* dst, int ld_dst, int group, int gap,
                                 float* inv_scale, cudaStream_t stream) {
-  if (!q_args_ok(src, src_f32, M, C, ld, ssp) || partial == nullptr || dst == nullptr || inv_scale == nullptr ||
+  if (!q_args_ok(src, src_f32, M, C, ld, ssp) || partial == nullptr || npart < 1 || dst == nullptr ||
+      inv_scale == nullptr ||
       ld_dst < C || ld_dst % 8 != 0 || reinterpret_cast<uintptr_t>(dst) % 8 != 0 || group < 0 || gap < 0)
     return cudaErrorInvalidValue;
   const int rows_per_block = QT / 32;
   int grid = (M + rows_per_block - 1) / rows_per_block;
   grid = grid < 4 * FP8_AMAX_BLOCKS ? grid : 4 * FP8_AMAX_BLOCKS;
-  return launch_q(fp8_quantize_kernel, grid, stream, src, src_f32, M, C, ld, ssp, eps, partial, dst, ld_dst, group,
-                  gap, inv_scale);
+  return launch_q(fp8_quantize_kernel, grid, stream, src, src_f32, M, C, ld, ssp, eps, partial, npart, dst, ld_dst,
+                  group, gap, inv_scale);
 }
 
 }  // namespace nc

@@ -212,10 +212,10 @@ def test_fp8_loss_path_and_rejections():
     with pytest.raises(RuntimeError):
         m.loss_grad_tail(tok.to(DEV), tgt.to(DEV))
     ve = sum(1 for v in cfg.has_ve if v)
-    assert m.launch_count() == 2 + 13 * cfg.n_layer + ve + 2
+    assert m.launch_count() == 2 + 12 * cfg.n_layer + ve + 2
     m.timing(True)
     m.forward(tok.to(DEV))
     t = m.timing_read()
     m.timing(False)
-    assert t["fp8_quantize"][1] == 8 * cfg.n_layer + 2
+    assert t["fp8_quantize"][1] == 7 * cfg.n_layer + 2   # the fc output's maximum comes from its epilogue
     assert sum(n for _, n in t.values()) == m.launch_count()
