@@ -25,6 +25,14 @@
 //   GEMV_SOFTCAP_F32  z = cap tanh(rs * acc / cap), fp32 or bf16  (lm_head)
 // rs is the input's RMSNorm row scale, 1 / sqrt(sum of the row's partial sums of squares / ncols
 // + eps), from the partials its producer wrote (the same formula as the full forward).
+//
+// Why mma.sync: the kernel is bound by the weight stream and the launch chain, not by arithmetic
+// (2B flops per weight byte pair).  The warp-level instruction is used as a register-to-register
+// dot-product unit: one instruction does 16 x 8 x 16 multiply-adds straight from the bf16 bytes
+// the coalesced loads delivered, where CUDA cores would first convert every weight and token
+// element to fp32 (a CUDA-core variant that did so was 2x slower per step).  tcgen05 would need
+// the operands in shared memory, a tensor-memory allocation and at least 64 rows per CTA, all
+// latency on a path whose every launch is on the critical chain.
 #include "decode.h"
 #include "ptx.cuh"
 
