@@ -61,6 +61,20 @@ def window_pairs(T: int, W: int) -> int:
     return (W + 1) * (W + 2) // 2 + (T - W - 1) * (W + 1)
 
 
+def decode_step_bytes(cfg, B: int, pos: int):
+    """Algorithmic bytes of one decode step at position pos: every weight once (the packed q|k|v
+    with its gate rows, the out-projection, fc, down projection, the lm_head; bf16) and the cached
+    keys and values each layer attends to (positions max(0, pos - W) .. pos - 1; the new position's
+    come from the step itself).  Returns (weight bytes, cache bytes)."""
+    H, Hkv, D, C, F, L, V = (cfg.n_head, cfg.n_kv_head, cfg.head_dim, cfg.n_embd, cfg.mlp_hidden, cfg.n_layer,
+                             cfg.vocab_size)
+    w = 2 * (sum(((H + 2 * Hkv) * D + (Hkv * 16 if cfg.has_ve[i] else 0)) * C + C * H * D + 2 * F * C
+                 for i in range(L)) + V * C)
+    kv = sum(B * (pos - (0 if cfg.window_left[i] < 0 else max(0, pos - cfg.window_left[i]))) * Hkv * D * 2 * 2
+             for i in range(L))
+    return w, kv
+
+
 def kernel_work(cfg, B: int, T: int):
     """Algorithmic work per launch of each kernel class (FLOPs for contractions, bytes otherwise)."""
     M = B * T
@@ -489,14 +503,7 @@ def run_ours(args, rank, world, local_rank):
         dk = model.timing_read()
         model.timing(False)
         dec_kernels = {k: {"launches_per_step": n // 10, "us_per_step": 1000.0 * ms / 10} for k, (ms, n) in dk.items() if n}
-        # Algorithmic bytes of one step: every weight once (the packed q|k|v with its gate rows, the
-        # out-projection, fc, down projection, the lm_head) plus the cached keys and values each
-        # layer attends to (the new position's come from the step itself).
-        H_, Hkv_, D_, C_, F_, L_ = cfg.n_head, cfg.n_kv_head, cfg.head_dim, cfg.n_embd, cfg.mlp_hidden, cfg.n_layer
-        w_bytes = 2 * (sum(((H_ + 2 * Hkv_) * D_ + (Hkv_ * 16 if cfg.has_ve[i] else 0)) * C_ + C_ * H_ * D_ + 2 * F_ * C_
-                           for i in range(L_)) + V * C_)
-        kv_bytes = sum(B * (T0 - (0 if cfg.window_left[i] < 0 else max(0, T0 - cfg.window_left[i]))) * Hkv_ * D_ * 2 * 2
-                       for i in range(L_))
+        w_bytes, kv_bytes = decode_step_bytes(cfg, B, T0)
         dec_peak = load_peaks()[0].get("hbm_gbs")
         decode_path = {"metric": "decode tokens/s (one new token per batch row)", "value": job_rate(world, B, dec_ms),
                        "unit": UNIT, "ms_per_step": dec_ms, "steps": n_dec, "batch": B, "context": T,

@@ -27,3 +27,18 @@ def test_model_flops_per_token(name, per_token):
 def test_d12_forward_is_3_966_tflop():
     wl = get_workload("d12")
     assert abs(bench.model_flops(wl.model, wl.B, wl.T) / 1e12 - 3.966) < 5e-4
+
+
+def test_decode_step_bytes_d12():
+    """d12, B = 8, position 2047: per layer 2304 x 768 q|k|v weights (+ 96 gate rows x 768 on the
+    six value-embedding layers), 768 x 768 out-projection and two 3072 x 768 MLP matrices, the
+    32768 x 768 lm_head, all bf16; the cache read is 512 keys on the nine window-512 layers and
+    2047 on the three full ones, 8 rows x 6 heads x 128 x 2 bytes x (key, value) per key."""
+    wl = get_workload("d12")
+    cfg = wl.model
+    assert sum(1 for v in cfg.has_ve if v) == 6
+    per_layer = 2304 * 768 + 768 * 768 + 2 * 3072 * 768
+    weights = 2 * (12 * per_layer + 6 * 96 * 768 + 32768 * 768)
+    cache = (9 * 512 + 3 * 2047) * 8 * 6 * 128 * 2 * 2
+    assert bench.decode_step_bytes(cfg, 8, 2047) == (weights, cache)
+    assert weights == 221_085_696 and cache == 264_167_424
