@@ -95,12 +95,19 @@ __global__ void __launch_bounds__(32 * DA_WARPS)
   const int j0 = jlo + split * kps, j1 = min(pos, j0 + kps);   // cached keys only
   const bool rank0 = split == 0;
   // The split's cached rows (complete before the preceding kernel started) start their way from
-  // HBM into L2 now, while the preceding kernel still runs: one bulk prefetch per key and tensor.
-  {
-    const size_t base = static_cast<size_t>(b) * a.cap * kvcols + static_cast<size_t>(g) * D;
-    for (int j = j0 + (tid >> 1); j < j1; j += 32 * DA_WARPS / 2) {
-      const bf16* row = ((tid & 1) ? a.vc : a.kc) + base + static_cast<size_t>(j % a.cap) * kvcols;
-      bulk_prefetch_l2(row, D * 2);
+  // HBM into L2 now, while the preceding kernel still runs.  A position's keys (values) of all kv
+  // heads are one contiguous row of the cache, so the H CTAs of (b, split) share the work: CTA h
+  // prefetches every kv head's rows of its H-th of the split's positions, in at most two bulk
+  // prefetches per tensor (two when the ring of slots wraps).
+  if (tid < 2 && j1 > j0) {
+    const int per = (j1 - j0 + H - 1) / H;
+    const int p0 = j0 + h * per, p1 = min(j1, p0 + per);
+    if (p0 < p1) {
+      const bf16* base = (tid ? a.vc : a.kc) + static_cast<size_t>(b) * a.cap * kvcols;
+      const uint32_t row_bytes = static_cast<uint32_t>(kvcols) * 2;
+      const int s0 = p0 % a.cap, n = p1 - p0, first = min(n, a.cap - s0);
+      bulk_prefetch_l2(base + static_cast<size_t>(s0) * kvcols, static_cast<uint32_t>(first) * row_bytes);
+      if (n > first) bulk_prefetch_l2(base, static_cast<uint32_t>(n - first) * row_bytes);
     }
   }
   griddep_wait();   // the q|k|v products come from the preceding kernel
