@@ -159,3 +159,19 @@ def test_decode_from_the_first_positions():
     ref = O.forward(cfg, O.OracleWeights.from_synth(cfg, wts), tok.numpy())
     assert_parity(pre.cpu().numpy(), ref[:, :1], "prefill of one token")
     assert_parity(dec.cpu().numpy(), ref[:, 1:13], "decode, positions 1..12")
+
+
+def test_decode_d12_twenty_rows_persistent_lm_head():
+    """d12 weights with B = 20 (two groups of 16 token rows): the lm_head's product runs on
+    persistent CTAs over 4,096 vocabulary blocks for each group; steps at positions 14 and 15 equal
+    the forward's rows and the oracle's."""
+    wl = get_workload("d12")
+    cfg = wl.model
+    wts = make_weights(cfg, seed=wl.seed, init=wl.init)
+    tok = torch.randint(0, cfg.vocab_size, (20, 16), generator=torch.Generator().manual_seed(26), dtype=torch.int32)
+    m = binding().Model(cfg, to_device(wts))
+    _, dec = _decode_run(m, tok, 14, 64, [14, 15])
+    full = m.forward(tok.to(DEV)).cpu().numpy()
+    assert_parity(dec.cpu().numpy(), full[:, 14:16], "decode vs forward, d12, 20 rows")
+    ref = O.forward_row(cfg, O.OracleWeights.from_synth(cfg, wts), tok[19].numpy(), positions=[14, 15])
+    assert_parity(dec[19].cpu().numpy(), ref, "decode vs oracle, d12, row 19")
