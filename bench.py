@@ -576,6 +576,7 @@ def run_ours(args, rank, world, local_rank):
     # fly): the same forward timed the same way, with per-kernel rates; contractions against the
     # e4m3 peak (the measured bf16 figure times 2, the nominal dense ratio), quantisation against HBM.
     fp8_path = None
+    ms_step_bf16 = ms / max(args.steps, 1)   # this rank's bf16 forward, for the ratio below
     if not args.no_fp8:
         m8 = NB.Model(cfg, wts, device=dev, fp8=True)
         z8 = torch.empty((B, T, V), dtype=torch.float32, device=dev)
@@ -615,9 +616,12 @@ def run_ours(args, rank, world, local_rank):
                     "unit": UNIT, "ms_per_step": ms8, "steps": n8, "gpu_launches_per_step": m8.launch_count(),
                     "tflops_model": model_flops(cfg, B, T) / (ms8 / 1000.0) / 1e12,
                     "peak_e4m3_tflops": pk8["bf16_tflops"], "kernels": k8,
+                    "vs_bf16_forward": ms_step_bf16 / ms8 if ms_step_bf16 else None,
                     "note": "nc_forward with fp8: q, k, v, output projection, MLP and lm_head on e4m3 copies "
                             "(weights quantised at model creation, each layer input per call over the whole "
-                            "batch), fp32 accumulation; attention, norms and gates in bf16/fp32"}
+                            "batch; the stream's and the MLP hidden layer's maxima come from the epilogues "
+                            "that write them), fp32 accumulation; attention, norms and gates in bf16/fp32; "
+                            "vs_bf16_forward = bf16 ms per forward / 8-bit ms per forward, same run"}
         del m8, z8
         torch.cuda.empty_cache()
 
