@@ -175,3 +175,17 @@ def test_decode_d12_twenty_rows_persistent_lm_head():
     assert_parity(dec.cpu().numpy(), full[:, 14:16], "decode vs forward, d12, 20 rows")
     ref = O.forward_row(cfg, O.OracleWeights.from_synth(cfg, wts), tok[19].numpy(), positions=[14, 15])
     assert_parity(dec[19].cpu().numpy(), ref, "decode vs oracle, d12, row 19")
+
+
+@pytest.mark.parametrize("windows", [(0, -1), (1, 2)])
+def test_decode_windows_of_zero_to_two_keys(windows):
+    """Windows W = 0, 1, 2: a query sees only itself (no cached key: every split is empty and the
+    new key's partial is the whole softmax) or one or two cached keys; the ring has W + 1 slots."""
+    wl = get_workload("tiny_all")
+    cfg = replace(wl.model, n_layer=2, window_left=windows, has_ve=(1, 1), seq_len_ctx=64)
+    wts = make_weights(cfg, init="dense")
+    tok = torch.randint(0, cfg.vocab_size, (2, 12), generator=torch.Generator().manual_seed(27), dtype=torch.int32)
+    m = binding().Model(cfg, to_device(wts))
+    _, dec = _decode_run(m, tok, 3, 64, list(range(3, 12)))
+    ref = O.forward(cfg, O.OracleWeights.from_synth(cfg, wts), tok.numpy())
+    assert_parity(dec.cpu().numpy(), ref[:, 3:12], f"decode, windows {windows}")
